@@ -1,0 +1,196 @@
+/*
+ * mk.h -- C ABI of the persistent single-launch decode megakernel for GB300 (sm_103a).
+ *
+ * One decode step of a Llama-style decoder runs as ONE launch of a persistent kernel:
+ * one CTA per SM (exactly one wave, "8 · Écrire son megakernel", §8.3), each CTA walking
+ * its own instruction queue (§8.2: RMSNORM_QKV_ROPE, ATTENTION, ATTN_REDUCE, O_PROJ,
+ * MLP_UP_GATE, MLP_DOWN, LM_HEAD), ops gated by dependency counters (§8.5) or by NaN
+ * sentinels ("7 · AMD et le monokernel", §7.3), weights streamed into a shared-memory page
+ * pool by TMA bulk copies from a producer warp so the HBM stream never stops (§7.5, §8.4).
+ *
+ * Conventions for every function below
+ *   - Return value: mk_status; MK_OK (0) on success.  No C++ exception crosses the ABI.
+ *     The text of the last failure on the calling thread is returned by mk_last_error().
+ *   - "device" pointers are CUDA device addresses on the device that was current when
+ *     mk_create was called; "host" pointers are ordinary CPU memory.
+ *   - Ownership: weights, KV cache and optional logits buffers belong to the caller, who
+ *     keeps them alive (and unmodified, for weights) until mk_destroy.  The context owns
+ *     its instruction queues, counters, activation buffers and trace buffer.
+ *   - All device work is enqueued on the stream given to mk_create.  A context is not
+ *     thread-safe: one host thread at a time.
+ */
+#ifndef MK_H_
+#define MK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MK_OK = 0,
+  MK_ERR_INVALID = 1,    /* bad argument, descriptor, pointer alignment or schedule      */
+  MK_ERR_OCCUPANCY = 2,  /* fewer than one resident CTA per SM (§8.3: would deadlock)    */
+  MK_ERR_CUDA = 3,       /* a CUDA runtime call failed                                   */
+  MK_ERR_TIMEOUT = 4,    /* a device-side wait ran past its limit; the step was abandoned */
+  MK_ERR_STATE = 5,      /* context unusable until mk_reset (after a timeout)            */
+  MK_ERR_NAN = 6         /* a logit was NaN; the returned token is meaningless           */
+} mk_status;
+
+typedef enum { MK_F16 = 0, MK_BF16 = 1 } mk_dtype;
+typedef enum { MK_SYNC_COUNTER = 0, MK_SYNC_SENTINEL = 1 } mk_sync_mode;
+typedef enum { MK_EXEC_PERSISTENT = 0, MK_EXEC_MULTILAUNCH = 1 } mk_exec_mode;
+
+typedef struct mk_ctx mk_ctx;
+
+/* Shape of the decoder (the pages never define the layer; see the reading in the oracle):
+ * RMSNorm(eps) -> q,k,v projections -> rotate-half RoPE(theta) -> causal GQA attention
+ * (query head i reads kv head i / (n_heads / n_kv_heads)) -> O projection + residual ->
+ * RMSNorm -> SwiGLU MLP + residual; final RMSNorm; untied LM head; greedy argmax. */
+typedef struct {
+  int n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn_dim, vocab;
+  int dtype;              /* mk_dtype of weights AND KV cache                            */
+  float rms_eps, rope_theta;
+  int max_batch;          /* 1..16 sequences per step                                    */
+  int max_ctx;            /* KV-cache capacity in positions                              */
+} mk_model_desc;
+
+/* Weights: device pointers, row-major, nn.Linear convention [out, in], 16-byte aligned.
+ * Model-level: embed [vocab, d], final_norm [d], lm_head [vocab, d].
+ * Per layer (host arrays of n_layers device pointers): attn_norm [d], wq [n_heads*hd, d],
+ * wk, wv [n_kv_heads*hd, d], wo [d, n_heads*hd], mlp_norm [d], w_gate, w_up [ffn, d],
+ * w_down [d, ffn].  The host arrays are read during mk_create only. */
+typedef struct {
+  const void *embed, *final_norm, *lm_head;
+  const void *const *attn_norm, *const *wq, *const *wk, *const *wv, *const *wo;
+  const void *const *mlp_norm, *const *w_gate, *const *w_up, *const *w_down;
+} mk_weights;
+
+/* KV cache: host arrays of n_layers device pointers, each [max_batch, n_kv_heads,
+ * max_ctx, head_dim] in the model dtype.  Position t of sequence b, kv head j, lives at
+ * ((b * n_kv_heads + j) * max_ctx + t) * head_dim.  The kernel writes the new token's
+ * rotated key and its value at the step's position and reads positions below it. */
+typedef struct {
+  void *const *k_cache;
+  void *const *v_cache;
+} mk_kv;
+
+/* Options; a zero-initialised struct selects the defaults. */
+typedef struct {
+  int sync_mode;          /* mk_sync_mode: counters (§8.5) or NaN sentinels (§7.3)        */
+  int exec_mode;          /* mk_exec_mode: one persistent launch, or the multi-launch control */
+  int page_bytes;         /* shared-memory page size (default 16384; power of two, 4K..32K) */
+  int n_pages;            /* pages in the pool (default: as many as fit)                  */
+  int kv_splits;          /* split-KV partitions per (sequence, kv head); 0 = one wave's worth */
+  int trace;              /* 1: record the per-instruction journal (§8.7)                  */
+  double wait_timeout_s;  /* limit of every device-side wait (default 2.0 s)              */
+  int backoff_max_ns;     /* cap of the exponential __nanosleep backoff (§8.5; default 256) */
+  int max_ctas;           /* test hook: use at most this many CTAs (0 = one per SM)        */
+  int fault_drop_signal;  /* test hook: k > 0 removes the k-th counter signal from the
+                             schedule and skips the host-side validator, so that the
+                             device wait must time out (fault injection on the host)     */
+} mk_options;
+
+typedef struct {
+  int n_sm;               /* multiprocessors on the device                                 */
+  int blocks_per_sm;      /* cudaOccupancyMaxActiveBlocksPerMultiprocessor result          */
+  int n_ctas;             /* grid size = one wave                                          */
+  int threads_per_cta;
+  int smem_bytes;         /* dynamic shared memory per CTA                                 */
+  int page_bytes, n_pages;
+  int kv_splits;
+  int n_instructions;     /* total over all queues                                         */
+  int n_counters;
+  int launches_per_step;  /* 1 for the persistent kernel, ~6 per layer + 2 for multi-launch */
+  long long weight_bytes_per_step;  /* streamed weight bytes of one decode step            */
+} mk_info_t;
+
+/* One journal record per executed instruction (§8.7), times from %globaltimer (ns). */
+typedef struct {
+  int32_t cta, pc, op, layer;
+  uint64_t t_fetch;       /* instruction fetched                                           */
+  uint64_t t_ready;       /* dependency satisfied, inputs loaded                           */
+  uint64_t t_end;         /* outputs written (before the signal)                           */
+} mk_trace_rec;
+
+/* Build the context: validates the descriptor and pointers, sizes the persistent grid
+ * (cudaFuncSetAttribute + cudaOccupancyMaxActiveBlocksPerMultiprocessor, §8.3; refuses
+ * with MK_ERR_OCCUPANCY when fewer than one CTA fits), builds the per-CTA instruction
+ * queues and counter wiring, checks them with the static validator (deadlock freedom,
+ * every read ordered after its writer, every output written exactly once), uploads
+ * them, and precomputes the RoPE table.  `stream` is a cudaStream_t (NULL = legacy). */
+mk_status mk_create(const mk_model_desc *desc, const mk_weights *weights, const mk_kv *kv,
+                    const mk_options *opts, void *stream, mk_ctx **out);
+
+/* Prompt pass: tokens host [B, P] row-major at positions 0..P-1 of each sequence.
+ * Fills KV positions 0..P-1 and returns the greedy next token of each sequence in
+ * next_tok (host [B]); logits (device [B, vocab] fp32, or NULL) receives the last
+ * position's logits.  Runs the decode step once per position (teacher forcing). */
+mk_status mk_prefill(mk_ctx *ctx, const int32_t *tokens, int B, int P,
+                     int32_t *next_tok, float *logits);
+
+/* The hot path: one decode step, ONE kernel launch.  in_tok host [B] sits at position
+ * pos host [B] (the cache holds 0..pos[b]-1); out_tok host [B] receives the argmax
+ * token (lowest index among ties); logits device [B, vocab] fp32 or NULL.  Synchronous
+ * for out_tok (one small device-to-host copy). */
+mk_status mk_decode_step(mk_ctx *ctx, const int32_t *in_tok, const int32_t *pos, int B,
+                         int32_t *out_tok, float *logits);
+
+/* n_steps greedy decode steps enqueued back to back without host round trips: step s
+ * embeds the token chosen by step s-1 on the device.  in_tok host [B] at positions
+ * pos0 host [B], or in_tok NULL to continue from the token the previous step chose on
+ * the device; out_tok device [n_steps, B] int32 (or NULL) receives every step's token.
+ * Asynchronous: returns after enqueueing; call mk_synchronize for the status. */
+mk_status mk_decode_steps(mk_ctx *ctx, const int32_t *in_tok, const int32_t *pos0, int B,
+                          int n_steps, int32_t *out_tok_dev);
+
+/* Waits for the context's stream and reports a device-side error of enqueued steps. */
+mk_status mk_synchronize(mk_ctx *ctx);
+
+/* Clears counters, epoch and the error word after MK_ERR_TIMEOUT / MK_ERR_STATE. */
+mk_status mk_reset(mk_ctx *ctx);
+
+/* Releases everything the context owns (never the caller's buffers).  NULL is a no-op. */
+mk_status mk_destroy(mk_ctx *ctx);
+
+mk_status mk_info(const mk_ctx *ctx, mk_info_t *info);
+
+/* Copies up to max_records journal records of the last step (trace option) to host
+ * memory; *n_records receives the number recorded. */
+mk_status mk_get_trace(mk_ctx *ctx, mk_trace_rec *records, int max_records, int *n_records);
+
+/* Debug/parity read of an activation vector of the last step, fp32, to host memory.
+ * which: 0 h_in of layer (h after the embedding for layer 0; layer = n_layers gives the
+ * final h), 1 h_mid (after attention), 2 q (rotated), 3 attention output o, 4 MLP
+ * activation silu(gate)*up.  dst host [max_batch, width]; bytes must equal that size. */
+mk_status mk_read_activation(mk_ctx *ctx, int which, int layer, float *dst, size_t bytes);
+
+/* Host-only planning (no GPU needed): builds and validates the schedule for n_ctas
+ * queues and reports its statistics in info (n_instructions, n_counters, kv_splits,
+ * weight bytes).  Used to test the builder and validator on a CPU-only machine. */
+mk_status mk_plan(const mk_model_desc *desc, const mk_options *opts, int n_ctas,
+                  mk_info_t *info);
+
+/* Build-ladder self tests of the persistent machinery ("8 · Écrire son megakernel",
+ * §8.6, steps 1-4) on the current device:
+ *   kind 1: a persistent kernel with one trivial instruction per CTA terminates;
+ *   kind 2: dispatch of two opcodes keeps queue order;
+ *   kind 3: counters between dependent instructions on different CTAs;
+ *   kind 4: page pool: many TMA pages through a small pool, checksummed, none leaked.
+ * result host [n] (n >= 4): [0] = 1 on pass, [1] CTAs used, [2..] kind-specific. */
+mk_status mk_selftest(int kind, int64_t *result, int n);
+
+/* Grid-barrier latency microbenchmark (§7.3 measurement): a one-wave kernel doing
+ * n_barriers all-CTA barriers, with atomic counters (mode 0) or NaN sentinels (mode 1).
+ * *us_per_barrier receives the mean latency in microseconds. */
+mk_status mk_barrier_bench(int mode, int n_barriers, double *us_per_barrier);
+
+const char *mk_last_error(void);
+const char *mk_status_string(mk_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MK_H_ */

@@ -1,0 +1,821 @@
+// Host runtime behind the C ABI of include/mk.h: context set-up, one-wave launch sizing
+// ("8 · Écrire son megakernel", §8.3), schedule upload, the decode-step launches, and
+// the build-ladder self tests (§8.6).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <memory>
+#include <string>
+#include <vector>
+
+#include "../../include/mk.h"
+#include "mk_internal.h"
+#include "mk_kernels.h"
+#include "mk_plan.h"
+
+using namespace mk;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+mk_status fail(mk_status s, const std::string& msg) {
+  g_last_error = msg;
+  return s;
+}
+
+#define MK_CUDA(call)                                                                           \
+  do {                                                                                          \
+    cudaError_t e_ = (call);                                                                    \
+    if (e_ != cudaSuccess) {                                                                    \
+      return fail(MK_ERR_CUDA, std::string(#call) + ": " + cudaGetErrorString(e_));            \
+    }                                                                                           \
+  } while (0)
+
+struct DevBuf {
+  void* p = nullptr;
+  ~DevBuf() {
+    if (p) cudaFree(p);
+  }
+};
+
+// one schedule per batch size: queues, per-phase queues and its own counters/epoch
+struct Sched {
+  Plan plan;
+  int n_instr = 0;
+  DevBuf instr, qstart, counters;
+  std::vector<DevBuf> ph_instr, ph_qstart;
+  uint32_t epoch = 0;
+};
+
+}  // namespace
+
+struct mk_ctx {
+  ModelShape m{};
+  mk_options opts{};
+  Geometry geo{};
+  cudaStream_t stream = nullptr;
+  int device = 0;
+  int n_sm = 0, bpsm = 0, n_cta = 0;
+  const void* kernel = nullptr;
+  const void* kernel_trace = nullptr;
+  DevState st{};  // template, counters patched per schedule
+  DevBuf ptr_tables, rope, act, argkeys, ctl, trace;
+  int trace_cap = 0;
+  Ctl* host_ctl = nullptr;  // pinned
+  std::map<int, std::unique_ptr<Sched>> scheds;
+  uint32_t step = 0;
+  bool broken = false;
+  int last_B = 1;
+  ~mk_ctx() {
+    if (host_ctl) cudaFreeHost(host_ctl);
+  }
+};
+
+namespace {
+
+std::string check_desc(const mk_model_desc* d) {
+  if (!d) return "desc is NULL";
+  if (d->n_layers < 1 || d->d_model < 8 || d->n_heads < 1 || d->n_kv_heads < 1 || d->head_dim < 8 ||
+      d->ffn_dim < 8 || d->vocab < 2)
+    return "descriptor dimensions must be positive";
+  if (d->n_heads % d->n_kv_heads) return "n_heads must be a multiple of n_kv_heads";
+  if (d->dtype != MK_F16 && d->dtype != MK_BF16) return "dtype must be MK_F16 or MK_BF16";
+  if (d->max_batch < 1 || d->max_batch > kMaxBatch) return "max_batch must be in [1, 16]";
+  if (d->max_ctx < 1) return "max_ctx must be positive";
+  if (!(d->rms_eps > 0.f) || !(d->rope_theta > 0.f)) return "rms_eps and rope_theta must be positive";
+  if (d->d_model % 8 || d->ffn_dim % 8) return "d_model and ffn_dim must be multiples of 8";
+  return "";
+}
+
+ModelShape shape_of(const mk_model_desc* d) {
+  ModelShape m;
+  m.L = d->n_layers;
+  m.d = d->d_model;
+  m.Hq = d->n_heads;
+  m.Hkv = d->n_kv_heads;
+  m.hd = d->head_dim;
+  m.F = d->ffn_dim;
+  m.V = d->vocab;
+  m.dtype = d->dtype;
+  m.max_batch = d->max_batch;
+  m.max_ctx = d->max_ctx;
+  m.eps = d->rms_eps;
+  m.theta = d->rope_theta;
+  return m;
+}
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+mk_status upload(DevBuf& b, const void* src, size_t bytes) {
+  MK_CUDA(cudaMalloc(&b.p, std::max<size_t>(bytes, 16)));
+  if (src && bytes) MK_CUDA(cudaMemcpy(b.p, src, bytes, cudaMemcpyHostToDevice));
+  return MK_OK;
+}
+
+mk_status upload_queues(const std::vector<std::vector<Instr>>& qs, DevBuf& ibuf, DevBuf& qbuf, int* n_out) {
+  std::vector<Instr> flat;
+  std::vector<int32_t> qs_off;
+  for (const auto& q : qs) {
+    qs_off.push_back((int32_t)flat.size());
+    flat.insert(flat.end(), q.begin(), q.end());
+  }
+  qs_off.push_back((int32_t)flat.size());
+  if (n_out) *n_out = (int)flat.size();
+  mk_status s = upload(ibuf, flat.data(), flat.size() * sizeof(Instr));
+  if (s) return s;
+  return upload(qbuf, qs_off.data(), qs_off.size() * sizeof(int32_t));
+}
+
+mk_status get_sched(mk_ctx* ctx, int B, Sched** out) {
+  auto it = ctx->scheds.find(B);
+  if (it != ctx->scheds.end()) {
+    *out = it->second.get();
+    return MK_OK;
+  }
+  auto sc = std::make_unique<Sched>();
+  std::string e = build_plan(ctx->m, ctx->geo, ctx->n_cta, B, ctx->opts.fault_drop_signal, &sc->plan);
+  if (!e.empty()) return fail(MK_ERR_INVALID, "schedule: " + e);
+  if (ctx->opts.fault_drop_signal <= 0) {
+    e = validate_plan(ctx->m, ctx->geo, sc->plan);
+    if (!e.empty()) return fail(MK_ERR_INVALID, "schedule rejected by the validator: " + e);
+  }
+  mk_status s = upload_queues(sc->plan.queues, sc->instr, sc->qstart, &sc->n_instr);
+  if (s) return s;
+  MK_CUDA(cudaMalloc(&sc->counters.p, sizeof(uint32_t) * std::max(1, sc->plan.n_counters)));
+  MK_CUDA(cudaMemset(sc->counters.p, 0, sizeof(uint32_t) * std::max(1, sc->plan.n_counters)));
+  if (ctx->opts.exec_mode == MK_EXEC_MULTILAUNCH) {
+    const size_t np = sc->plan.phase_queues.size();
+    sc->ph_instr.resize(np);
+    sc->ph_qstart.resize(np);
+    for (size_t k = 0; k < np; ++k) {
+      s = upload_queues(sc->plan.phase_queues[k], sc->ph_instr[k], sc->ph_qstart[k], nullptr);
+      if (s) return s;
+    }
+  }
+  if (ctx->opts.trace) {
+    const int need = sc->n_instr + 64;
+    if (need > ctx->trace_cap) {
+      if (ctx->trace.p) cudaFree(ctx->trace.p);
+      ctx->trace.p = nullptr;
+      MK_CUDA(cudaMalloc(&ctx->trace.p, sizeof(TraceRec) * need));
+      ctx->trace_cap = need;
+      ctx->st.trace = reinterpret_cast<TraceRec*>(ctx->trace.p);
+      ctx->st.trace_cap = need;
+    }
+  }
+  *out = sc.get();
+  ctx->scheds[B] = std::move(sc);
+  return MK_OK;
+}
+
+mk_status launch(mk_ctx* ctx, const void* fn, const DevState& S, const StepArgs& A, bool cooperative) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(ctx->n_cta);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = ctx->geo.smem_bytes;
+  cfg.stream = ctx->stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = cooperative ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[2] = {const_cast<DevState*>(&S), const_cast<StepArgs*>(&A)};
+  MK_CUDA(cudaLaunchKernelExC(&cfg, fn, args));
+  return MK_OK;
+}
+
+// enqueue one decode step (one launch, or the multi-launch control's per-op launches)
+mk_status enqueue_step(mk_ctx* ctx, Sched* sc, int B, const int32_t* tok, const int32_t* pos, bool tok_from_dev,
+                       float* logits, int32_t* tok_hist) {
+  DevState S = ctx->st;
+  S.counters = reinterpret_cast<uint32_t*>(sc->counters.p);
+  S.n_counters = sc->plan.n_counters;
+  StepArgs A{};
+  A.epoch = sc->epoch;
+  A.step = ctx->step;
+  A.B = B;
+  A.flags = SF_RESET_ARGMAX | (tok_from_dev ? SF_TOK_FROM_DEVICE : 0) | (ctx->opts.trace ? SF_TRACE : 0);
+  for (int b = 0; b < B; ++b) {
+    A.tok[b] = tok ? tok[b] : 0;
+    A.pos[b] = pos[b];
+  }
+  A.logits = logits;
+  A.tok_hist = tok_hist;
+  const void* fn = ctx->opts.trace ? ctx->kernel_trace : ctx->kernel;
+  if (ctx->opts.trace) MK_CUDA(cudaMemsetAsync(&reinterpret_cast<Ctl*>(ctx->ctl.p)->trace_n, 0, 4, ctx->stream));
+  mk_status s;
+  if (ctx->opts.exec_mode == MK_EXEC_MULTILAUNCH) {
+    const size_t np = sc->ph_instr.size();
+    for (size_t k = 0; k < np; ++k) {
+      StepArgs Ak = A;
+      Ak.flags |= SF_NO_SYNC;
+      if (k) Ak.flags &= ~SF_RESET_ARGMAX;
+      Ak.instr = reinterpret_cast<const Instr*>(sc->ph_instr[k].p);
+      Ak.q_start = reinterpret_cast<const int32_t*>(sc->ph_qstart[k].p);
+      s = launch(ctx, fn, S, Ak, false);
+      if (s) return s;
+    }
+  } else {
+    A.instr = reinterpret_cast<const Instr*>(sc->instr.p);
+    A.q_start = reinterpret_cast<const int32_t*>(sc->qstart.p);
+    s = launch(ctx, fn, S, A, true);
+    if (s) return s;
+  }
+  sc->epoch++;
+  ctx->step++;
+  ctx->last_B = B;
+  return MK_OK;
+}
+
+mk_status read_status(mk_ctx* ctx) {
+  MK_CUDA(cudaMemcpyAsync(ctx->host_ctl, ctx->ctl.p, sizeof(Ctl), cudaMemcpyDeviceToHost, ctx->stream));
+  MK_CUDA(cudaStreamSynchronize(ctx->stream));
+  const ErrWord& e = ctx->host_ctl->err;
+  if (e.code) {
+    ctx->broken = true;
+    char buf[200];
+    snprintf(buf, sizeof buf, "device error %u at cta %d pc %d counter %d", e.code, e.cta, e.pc, e.ctr);
+    return fail((mk_status)e.code, buf);
+  }
+  if (ctx->host_ctl->nan_seen) return fail(MK_ERR_NAN, "a logit was NaN");
+  return MK_OK;
+}
+
+mk_status check_step_args(mk_ctx* ctx, const int32_t* tok, const int32_t* pos, int B) {
+  if (ctx->broken) return fail(MK_ERR_STATE, "context needs mk_reset after a device error");
+  if (B < 1 || B > ctx->m.max_batch) return fail(MK_ERR_INVALID, "B out of range");
+  if (!pos) return fail(MK_ERR_INVALID, "pos is NULL");
+  for (int b = 0; b < B; ++b) {
+    if (tok && (tok[b] < 0 || tok[b] >= ctx->m.V)) return fail(MK_ERR_INVALID, "token id out of range");
+    if (pos[b] < 0 || pos[b] >= ctx->m.max_ctx) return fail(MK_ERR_INVALID, "position out of range");
+  }
+  return MK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mk_last_error(void) { return g_last_error.c_str(); }
+
+const char* mk_status_string(mk_status s) {
+  switch (s) {
+    case MK_OK: return "MK_OK";
+    case MK_ERR_INVALID: return "MK_ERR_INVALID";
+    case MK_ERR_OCCUPANCY: return "MK_ERR_OCCUPANCY";
+    case MK_ERR_CUDA: return "MK_ERR_CUDA";
+    case MK_ERR_TIMEOUT: return "MK_ERR_TIMEOUT";
+    case MK_ERR_STATE: return "MK_ERR_STATE";
+    case MK_ERR_NAN: return "MK_ERR_NAN";
+  }
+  return "MK_ERR_UNKNOWN";
+}
+
+mk_status mk_plan(const mk_model_desc* desc, const mk_options* opts, int n_ctas, mk_info_t* info) {
+  std::string e = check_desc(desc);
+  if (!e.empty()) return fail(MK_ERR_INVALID, e);
+  if (n_ctas < 1 || !info) return fail(MK_ERR_INVALID, "n_ctas must be positive and info non-NULL");
+  mk_options o{};
+  if (opts) o = *opts;
+  const ModelShape m = shape_of(desc);
+  Geometry g;
+  e = make_geometry(m, n_ctas, o.page_bytes, o.n_pages, o.kv_splits, 232448, &g);
+  if (!e.empty()) return fail(MK_ERR_INVALID, e);
+  Plan p;
+  e = build_plan(m, g, n_ctas, m.max_batch, o.fault_drop_signal, &p);
+  if (!e.empty()) return fail(MK_ERR_INVALID, e);
+  e = validate_plan(m, g, p);
+  if (!e.empty()) return fail(MK_ERR_INVALID, "schedule rejected by the validator: " + e);
+  std::memset(info, 0, sizeof *info);
+  info->n_ctas = n_ctas;
+  info->threads_per_cta = kThreads;
+  info->smem_bytes = g.smem_bytes;
+  info->page_bytes = g.page_bytes;
+  info->n_pages = g.n_pages;
+  info->kv_splits = g.S;
+  for (const auto& q : p.queues) info->n_instructions += (int)q.size();
+  info->n_counters = p.n_counters;
+  info->launches_per_step = o.exec_mode == MK_EXEC_MULTILAUNCH ? (int)p.phase_queues.size() : 1;
+  info->weight_bytes_per_step = p.weight_bytes;
+  return MK_OK;
+}
+
+mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv* kv, const mk_options* opts,
+                    void* stream, mk_ctx** out) {
+  if (!out) return fail(MK_ERR_INVALID, "out is NULL");
+  *out = nullptr;
+  std::string e = check_desc(desc);
+  if (!e.empty()) return fail(MK_ERR_INVALID, e);
+  if (!w || !kv) return fail(MK_ERR_INVALID, "weights or kv is NULL");
+  const ModelShape m = shape_of(desc);
+  // pointer checks: present and 16-byte aligned (TMA bulk copies need it)
+  if (!aligned16(w->embed) || !aligned16(w->final_norm) || !aligned16(w->lm_head))
+    return fail(MK_ERR_INVALID, "embed/final_norm/lm_head must be non-NULL and 16-byte aligned");
+  const void* const* tabs[9] = {w->attn_norm, w->wq, w->wk, w->wv, w->wo, w->mlp_norm, w->w_gate, w->w_up, w->w_down};
+  for (auto t : tabs) {
+    if (!t) return fail(MK_ERR_INVALID, "a per-layer weight table is NULL");
+    for (int l = 0; l < m.L; ++l)
+      if (!aligned16(t[l])) return fail(MK_ERR_INVALID, "per-layer weight pointers must be 16-byte aligned");
+  }
+  if (!kv->k_cache || !kv->v_cache) return fail(MK_ERR_INVALID, "kv tables are NULL");
+  for (int l = 0; l < m.L; ++l)
+    if (!aligned16(kv->k_cache[l]) || !aligned16(kv->v_cache[l]))
+      return fail(MK_ERR_INVALID, "KV-cache pointers must be non-NULL and 16-byte aligned");
+
+  auto ctx = std::make_unique<mk_ctx>();
+  ctx->m = m;
+  if (opts) ctx->opts = *opts;
+  mk_options& o = ctx->opts;
+  if (o.wait_timeout_s <= 0) o.wait_timeout_s = 2.0;
+  if (o.backoff_max_ns <= 0) o.backoff_max_ns = 256;
+  if (o.sync_mode != MK_SYNC_COUNTER && o.sync_mode != MK_SYNC_SENTINEL) return fail(MK_ERR_INVALID, "sync_mode");
+  if (o.exec_mode != MK_EXEC_PERSISTENT && o.exec_mode != MK_EXEC_MULTILAUNCH) return fail(MK_ERR_INVALID, "exec_mode");
+  ctx->stream = reinterpret_cast<cudaStream_t>(stream);
+  MK_CUDA(cudaGetDevice(&ctx->device));
+  MK_CUDA(cudaDeviceGetAttribute(&ctx->n_sm, cudaDevAttrMultiProcessorCount, ctx->device));
+  int smem_optin = 0;
+  MK_CUDA(cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, ctx->device));
+  int n_cta_guess = ctx->n_sm;
+  if (o.max_ctas > 0) n_cta_guess = std::min(n_cta_guess, o.max_ctas);
+  e = make_geometry(m, n_cta_guess, o.page_bytes, o.n_pages, o.kv_splits, smem_optin, &ctx->geo);
+  if (!e.empty()) return fail(MK_ERR_INVALID, e);
+  // one wave (§8.3): opt in to the shared memory, ask how many CTAs fit, launch exactly that
+  ctx->kernel = step_kernel_entry(m.dtype, o.sync_mode, false);
+  ctx->kernel_trace = step_kernel_entry(m.dtype, o.sync_mode, true);
+  for (const void* fn : {ctx->kernel, ctx->kernel_trace})
+    MK_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ctx->geo.smem_bytes));
+  MK_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ctx->bpsm, ctx->kernel, kThreads, ctx->geo.smem_bytes));
+  if (ctx->bpsm < 1) return fail(MK_ERR_OCCUPANCY, "the kernel does not fit on an SM (blocks per SM < 1)");
+  ctx->n_cta = ctx->n_sm * ctx->bpsm;
+  if (o.max_ctas > 0) ctx->n_cta = std::min(ctx->n_cta, o.max_ctas);
+  if (ctx->n_cta != n_cta_guess) {
+    e = make_geometry(m, ctx->n_cta, o.page_bytes, o.n_pages, o.kv_splits, smem_optin, &ctx->geo);
+    if (!e.empty()) return fail(MK_ERR_INVALID, e);
+  }
+  const Geometry& g = ctx->geo;
+
+  // device state
+  DevState& S = ctx->st;
+  S.L = m.L; S.d = m.d; S.Hq = m.Hq; S.Hkv = m.Hkv; S.hd = m.hd; S.F = m.F; S.V = m.V;
+  S.dtype = m.dtype; S.max_batch = m.max_batch; S.max_ctx = m.max_ctx; S.S = g.S; S.eps = m.eps;
+  S.ws_qkv = g.ws_qkv; S.ws_o = g.ws_o; S.ws_up = g.ws_up; S.ws_down = g.ws_down; S.ws_lm = g.ws_lm;
+  S.embed = static_cast<const uint16_t*>(w->embed);
+  S.final_norm = static_cast<const uint16_t*>(w->final_norm);
+  S.lm_head = static_cast<const uint16_t*>(w->lm_head);
+  {
+    std::vector<const void*> tab;
+    for (auto t : tabs)
+      for (int l = 0; l < m.L; ++l) tab.push_back(t[l]);
+    for (int l = 0; l < m.L; ++l) tab.push_back(kv->k_cache[l]);
+    for (int l = 0; l < m.L; ++l) tab.push_back(kv->v_cache[l]);
+    mk_status s = upload(ctx->ptr_tables, tab.data(), tab.size() * sizeof(void*));
+    if (s) return s;
+    auto base = reinterpret_cast<const uint16_t* const*>(ctx->ptr_tables.p);
+    S.attn_norm = base + 0 * m.L; S.wq = base + 1 * m.L; S.wk = base + 2 * m.L; S.wv = base + 3 * m.L;
+    S.wo = base + 4 * m.L; S.mlp_norm = base + 5 * m.L; S.w_gate = base + 6 * m.L; S.w_up = base + 7 * m.L;
+    S.w_down = base + 8 * m.L;
+    auto mbase = reinterpret_cast<uint16_t* const*>(ctx->ptr_tables.p);
+    S.kcache = mbase + 9 * m.L;
+    S.vcache = mbase + 10 * m.L;
+  }
+  {  // RoPE table: angle pos * theta^(-2i/hd), evaluated in double, stored as fp32
+    const int half = m.hd / 2;
+    std::vector<float> tab((size_t)m.max_ctx * half * 2);
+    for (int i = 0; i < half; ++i) {
+      const double f = std::pow((double)m.theta, -2.0 * i / m.hd);
+      for (int t = 0; t < m.max_ctx; ++t) {
+        const double a = (double)t * f;
+        tab[((size_t)t * half + i) * 2] = (float)std::cos(a);
+        tab[((size_t)t * half + i) * 2 + 1] = (float)std::sin(a);
+      }
+    }
+    mk_status s = upload(ctx->rope, tab.data(), tab.size() * sizeof(float));
+    if (s) return s;
+    S.rope = reinterpret_cast<const float2*>(ctx->rope.p);
+  }
+  {  // activation arena: two parity sets
+    const int G = m.Hq / m.Hkv;
+    const long long MB = m.max_batch;
+    long long sizes[ACT_NUM], layers[ACT_NUM];
+    sizes[ACT_H] = MB * m.d; layers[ACT_H] = m.L + 1;
+    sizes[ACT_HMID] = MB * m.d; layers[ACT_HMID] = m.L;
+    sizes[ACT_Q] = MB * m.Hq * m.hd; layers[ACT_Q] = m.L;
+    sizes[ACT_KVN] = MB * 2 * m.Hkv * m.hd; layers[ACT_KVN] = m.L;
+    sizes[ACT_PART] = MB * m.Hkv * (long long)g.S * G * (m.hd + 2); layers[ACT_PART] = m.L;
+    sizes[ACT_O] = MB * m.Hq * m.hd; layers[ACT_O] = m.L;
+    sizes[ACT_A] = MB * m.F; layers[ACT_A] = m.L;
+    long long off = 0;
+    for (int k = 0; k < ACT_NUM; ++k) {
+      const long long stride = (sizes[k] + 31) / 32 * 32;
+      S.act_off[k] = off;
+      S.act_stride[k] = stride;
+      off += stride * layers[k];
+    }
+    S.act_floats = (off + 31) / 32 * 32;
+    MK_CUDA(cudaMalloc(&ctx->act.p, sizeof(float) * 2 * S.act_floats));
+    MK_CUDA(cudaMemset(ctx->act.p, 0xFF, sizeof(float) * 2 * S.act_floats));  // all NaN
+    S.act = reinterpret_cast<float*>(ctx->act.p);
+  }
+  MK_CUDA(cudaMalloc(&ctx->argkeys.p, sizeof(unsigned long long) * 2 * kMaxBatch));
+  MK_CUDA(cudaMemset(ctx->argkeys.p, 0, sizeof(unsigned long long) * 2 * kMaxBatch));
+  S.argkeys = reinterpret_cast<unsigned long long*>(ctx->argkeys.p);
+  MK_CUDA(cudaMalloc(&ctx->ctl.p, sizeof(Ctl)));
+  MK_CUDA(cudaMemset(ctx->ctl.p, 0, sizeof(Ctl)));
+  S.ctl = reinterpret_cast<Ctl*>(ctx->ctl.p);
+  MK_CUDA(cudaMallocHost(reinterpret_cast<void**>(&ctx->host_ctl), sizeof(Ctl)));
+  S.n_cta = ctx->n_cta;
+  S.page_bytes = g.page_bytes;
+  S.n_pages = g.n_pages;
+  S.xbuf_bytes = g.xbuf_bytes;
+  S.scratch_bytes = g.scratch_bytes;
+  S.sync_mode = o.sync_mode;
+  S.timeout_ns = (int64_t)(o.wait_timeout_s * 1e9);
+  S.backoff_max_ns = o.backoff_max_ns;
+  // the schedule for the largest batch is built (and validated) now; others on first use
+  Sched* sc = nullptr;
+  mk_status s = get_sched(ctx.get(), m.max_batch, &sc);
+  if (s) return s;
+  MK_CUDA(cudaDeviceSynchronize());
+  *out = ctx.release();
+  return MK_OK;
+}
+
+mk_status mk_destroy(mk_ctx* ctx) {
+  if (!ctx) return MK_OK;
+  cudaStreamSynchronize(ctx->stream);
+  delete ctx;
+  return MK_OK;
+}
+
+mk_status mk_info(const mk_ctx* ctx, mk_info_t* info) {
+  if (!ctx || !info) return fail(MK_ERR_INVALID, "NULL argument");
+  std::memset(info, 0, sizeof *info);
+  info->n_sm = ctx->n_sm;
+  info->blocks_per_sm = ctx->bpsm;
+  info->n_ctas = ctx->n_cta;
+  info->threads_per_cta = kThreads;
+  info->smem_bytes = ctx->geo.smem_bytes;
+  info->page_bytes = ctx->geo.page_bytes;
+  info->n_pages = ctx->geo.n_pages;
+  info->kv_splits = ctx->geo.S;
+  auto it = ctx->scheds.find(ctx->last_B);
+  if (it == ctx->scheds.end()) it = ctx->scheds.begin();
+  if (it != ctx->scheds.end()) {
+    info->n_instructions = it->second->n_instr;
+    info->n_counters = it->second->plan.n_counters;
+    info->launches_per_step =
+        ctx->opts.exec_mode == MK_EXEC_MULTILAUNCH ? (int)it->second->plan.phase_queues.size() : 1;
+    info->weight_bytes_per_step = it->second->plan.weight_bytes;
+  }
+  return MK_OK;
+}
+
+mk_status mk_decode_step(mk_ctx* ctx, const int32_t* in_tok, const int32_t* pos, int B, int32_t* out_tok,
+                         float* logits) {
+  if (!ctx) return fail(MK_ERR_INVALID, "ctx is NULL");
+  if (!in_tok || !out_tok) return fail(MK_ERR_INVALID, "in_tok/out_tok NULL");
+  mk_status s = check_step_args(ctx, in_tok, pos, B);
+  if (s) return s;
+  Sched* sc = nullptr;
+  s = get_sched(ctx, B, &sc);
+  if (s) return s;
+  s = enqueue_step(ctx, sc, B, in_tok, pos, false, logits, nullptr);
+  if (s) return s;
+  s = read_status(ctx);
+  if (s && s != MK_ERR_NAN) return s;
+  for (int b = 0; b < B; ++b) out_tok[b] = ctx->host_ctl->tok[b];
+  return s;
+}
+
+mk_status mk_decode_steps(mk_ctx* ctx, const int32_t* in_tok, const int32_t* pos0, int B, int n_steps,
+                          int32_t* out_tok_dev) {
+  if (!ctx) return fail(MK_ERR_INVALID, "ctx is NULL");
+  if (n_steps < 1) return fail(MK_ERR_INVALID, "n_steps < 1");
+  if (!in_tok && ctx->step == 0) return fail(MK_ERR_INVALID, "in_tok NULL before any step chose a token");
+  mk_status s = check_step_args(ctx, in_tok, pos0, B);
+  if (s) return s;
+  for (int b = 0; b < B; ++b)
+    if ((long long)pos0[b] + n_steps > ctx->m.max_ctx) return fail(MK_ERR_INVALID, "positions exceed max_ctx");
+  Sched* sc = nullptr;
+  s = get_sched(ctx, B, &sc);
+  if (s) return s;
+  int32_t pos[kMaxBatch];
+  for (int k = 0; k < n_steps; ++k) {
+    for (int b = 0; b < B; ++b) pos[b] = pos0[b] + k;
+    s = enqueue_step(ctx, sc, B, k == 0 ? in_tok : nullptr, pos, k > 0 || !in_tok, nullptr,
+                     out_tok_dev ? out_tok_dev + (size_t)k * B : nullptr);
+    if (s) return s;
+  }
+  return MK_OK;
+}
+
+mk_status mk_synchronize(mk_ctx* ctx) {
+  if (!ctx) return fail(MK_ERR_INVALID, "ctx is NULL");
+  return read_status(ctx);
+}
+
+mk_status mk_prefill(mk_ctx* ctx, const int32_t* tokens, int B, int P, int32_t* next_tok, float* logits) {
+  if (!ctx) return fail(MK_ERR_INVALID, "ctx is NULL");
+  if (!tokens || !next_tok || P < 1) return fail(MK_ERR_INVALID, "tokens/next_tok NULL or P < 1");
+  if (P > ctx->m.max_ctx) return fail(MK_ERR_INVALID, "P exceeds max_ctx");
+  if (B < 1 || B > ctx->m.max_batch) return fail(MK_ERR_INVALID, "B out of range");
+  for (long long i = 0; i < (long long)B * P; ++i)
+    if (tokens[i] < 0 || tokens[i] >= ctx->m.V) return fail(MK_ERR_INVALID, "token id out of range");
+  if (ctx->broken) return fail(MK_ERR_STATE, "context needs mk_reset after a device error");
+  Sched* sc = nullptr;
+  mk_status s = get_sched(ctx, B, &sc);
+  if (s) return s;
+  int32_t tok[kMaxBatch], pos[kMaxBatch];
+  for (int t = 0; t < P; ++t) {  // teacher-forced steps, enqueued back to back
+    for (int b = 0; b < B; ++b) {
+      tok[b] = tokens[(size_t)b * P + t];
+      pos[b] = t;
+    }
+    s = enqueue_step(ctx, sc, B, tok, pos, false, t == P - 1 ? logits : nullptr, nullptr);
+    if (s) return s;
+  }
+  s = read_status(ctx);
+  if (s && s != MK_ERR_NAN) return s;
+  for (int b = 0; b < B; ++b) next_tok[b] = ctx->host_ctl->tok[b];
+  return s;
+}
+
+mk_status mk_reset(mk_ctx* ctx) {
+  if (!ctx) return fail(MK_ERR_INVALID, "ctx is NULL");
+  MK_CUDA(cudaStreamSynchronize(ctx->stream));
+  for (auto& kv : ctx->scheds) {
+    MK_CUDA(cudaMemset(kv.second->counters.p, 0, sizeof(uint32_t) * std::max(1, kv.second->plan.n_counters)));
+    kv.second->epoch = 0;
+  }
+  MK_CUDA(cudaMemset(ctx->ctl.p, 0, sizeof(Ctl)));
+  MK_CUDA(cudaMemset(ctx->argkeys.p, 0, sizeof(unsigned long long) * 2 * kMaxBatch));
+  MK_CUDA(cudaMemset(ctx->act.p, 0xFF, sizeof(float) * 2 * ctx->st.act_floats));
+  MK_CUDA(cudaDeviceSynchronize());
+  ctx->step = 0;
+  ctx->broken = false;
+  return MK_OK;
+}
+
+mk_status mk_get_trace(mk_ctx* ctx, mk_trace_rec* recs, int max_records, int* n_records) {
+  if (!ctx || !n_records) return fail(MK_ERR_INVALID, "NULL argument");
+  *n_records = 0;
+  if (!ctx->opts.trace || !ctx->trace.p) return fail(MK_ERR_INVALID, "context created without the trace option");
+  MK_CUDA(cudaStreamSynchronize(ctx->stream));
+  uint32_t n = 0;
+  MK_CUDA(cudaMemcpy(&n, &reinterpret_cast<Ctl*>(ctx->ctl.p)->trace_n, 4, cudaMemcpyDeviceToHost));
+  n = std::min<uint32_t>(n, (uint32_t)ctx->trace_cap);
+  n = std::min<uint32_t>(n, (uint32_t)std::max(0, max_records));
+  if (n && recs) {
+    std::vector<TraceRec> tmp(n);
+    MK_CUDA(cudaMemcpy(tmp.data(), ctx->trace.p, n * sizeof(TraceRec), cudaMemcpyDeviceToHost));
+    for (uint32_t i = 0; i < n; ++i) {
+      recs[i].cta = tmp[i].cta;
+      recs[i].pc = tmp[i].pc;
+      recs[i].op = tmp[i].op;
+      recs[i].layer = tmp[i].layer;
+      recs[i].t_fetch = tmp[i].t_fetch;
+      recs[i].t_ready = tmp[i].t_ready;
+      recs[i].t_end = tmp[i].t_end;
+    }
+  }
+  *n_records = (int)n;
+  return MK_OK;
+}
+
+mk_status mk_read_activation(mk_ctx* ctx, int which, int layer, float* dst, size_t bytes) {
+  if (!ctx || !dst) return fail(MK_ERR_INVALID, "NULL argument");
+  const ModelShape& m = ctx->m;
+  int kind, width, max_layer = m.L - 1;
+  switch (which) {
+    case 0: kind = ACT_H; width = m.d; max_layer = m.L; break;
+    case 1: kind = ACT_HMID; width = m.d; break;
+    case 2: kind = ACT_Q; width = m.Hq * m.hd; break;
+    case 3: kind = ACT_O; width = m.Hq * m.hd; break;
+    case 4: kind = ACT_A; width = m.F; break;
+    default: return fail(MK_ERR_INVALID, "which must be 0..4");
+  }
+  if (layer < 0 || layer > max_layer) return fail(MK_ERR_INVALID, "layer out of range");
+  const size_t need = sizeof(float) * (size_t)m.max_batch * width;
+  if (bytes != need) return fail(MK_ERR_INVALID, "bytes must equal max_batch * width * 4");
+  MK_CUDA(cudaStreamSynchronize(ctx->stream));
+  const bool multi = ctx->opts.exec_mode == MK_EXEC_MULTILAUNCH;
+  const int par = (ctx->opts.sync_mode == MK_SYNC_SENTINEL && !multi) ? (int)((ctx->step + 1u) & 1u) : 0;
+  const float* src = ctx->st.act + (int64_t)par * ctx->st.act_floats + ctx->st.act_off[kind] +
+                     (int64_t)layer * ctx->st.act_stride[kind];
+  MK_CUDA(cudaMemcpy(dst, src, need, cudaMemcpyDeviceToHost));
+  return MK_OK;
+}
+
+// ---------------------------------------------------------------- build-ladder self tests
+mk_status mk_selftest(int kind, int64_t* result, int n) {
+  if (!result || n < 4 || kind < 1 || kind > 4) return fail(MK_ERR_INVALID, "kind must be 1..4 and n >= 4");
+  std::memset(result, 0, sizeof(int64_t) * n);
+  int dev = 0, n_sm = 0;
+  MK_CUDA(cudaGetDevice(&dev));
+  MK_CUDA(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
+  const void* fn = step_kernel_entry(MK_F16, MK_SYNC_COUNTER, false);
+  const int page = 16384, n_pages = 4;
+  const int smem = n_pages * page + 0 + 256 + kCtlSmem;
+  MK_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448));
+  int bpsm = 0;
+  MK_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bpsm, fn, kThreads, smem));
+  if (bpsm < 1) return fail(MK_ERR_OCCUPANCY, "self-test kernel does not fit");
+  const int n_cta = n_sm;  // one CTA per SM: every pair of CTAs co-resident
+  std::vector<std::vector<Instr>> qs(n_cta);
+  auto I = [](int op, int wc, uint32_t wn, int sc) {
+    Instr in{};
+    in.op = (uint8_t)op;
+    in.wait_ctr = wc;
+    in.wait_n = wn;
+    in.signal_ctr = sc;
+    return in;
+  };
+  int n_ctr = 1;
+  const int chunks = 3 * n_pages + 1;
+  const int64_t words_per_page = page / 8;
+  int64_t test_len = 0;
+  std::vector<int64_t> init;
+  switch (kind) {
+    case 1:  // terminates
+      for (int c = 0; c < n_cta; ++c) qs[c].push_back(I(OP_T_NOP, -1, 0, -1));
+      test_len = 64;
+      break;
+    case 2:  // two opcodes interleaved; the per-CTA log must match queue order
+      for (int c = 0; c < n_cta; ++c)
+        for (int k = 0; k < 20; ++k) {
+          Instr in = I(k % 3 == 2 ? OP_T_PRODUCE : OP_T_ORDER, -1, 0, -1);
+          in.a[0] = n_cta * 64 + c * 32 + k;  // PRODUCE target slot
+          in.a[1] = c * 1000 + k;
+          qs[c].push_back(in);
+        }
+      test_len = (int64_t)n_cta * 96;
+      break;
+    case 3: {  // chain through every CTA, then a fan-in to CTA 0
+      n_ctr = n_cta + 1;
+      const int all = n_cta;
+      {
+        Instr p = I(OP_T_PRODUCE, -1, 0, 0);
+        p.a[0] = 0;
+        p.a[1] = 7;
+        qs[0].push_back(p);
+      }
+      for (int c = 1; c < n_cta; ++c) {
+        Instr in = I(OP_T_CONSUME, c - 1, 1, c);
+        in.a[0] = c - 1;
+        in.a[2] = c;
+        qs[c].push_back(in);
+        qs[c].push_back(I(OP_T_NOP, -1, 0, all));
+      }
+      Instr fin = I(OP_T_CONSUME, all, (uint32_t)(n_cta - 1), -1);
+      fin.a[0] = n_cta - 1;
+      fin.a[2] = n_cta;
+      qs[0].push_back(fin);
+      test_len = n_cta + 8;
+      break;
+    }
+    case 4: {  // more pages than the pool holds, checksummed
+      const int64_t res_base = (int64_t)n_cta * chunks * words_per_page;
+      for (int c = 0; c < n_cta; ++c) {
+        Instr in = I(OP_T_PAGES, -1, 0, -1);
+        in.a[0] = c * chunks * (int)words_per_page;
+        in.a[1] = chunks;
+        in.a[2] = (int)(res_base + (int64_t)c * chunks);
+        qs[c].push_back(in);
+      }
+      test_len = res_base + (int64_t)n_cta * chunks;
+      init.resize(test_len, 0);
+      uint64_t x = 0x9E3779B97F4A7C15ull;
+      for (int64_t i = 0; i < res_base; ++i) {
+        x ^= x << 13; x ^= x >> 7; x ^= x << 17;
+        init[i] = (int64_t)x;
+      }
+      break;
+    }
+  }
+  for (auto& q : qs) q.push_back(I(OP_END, -1, 0, -1));
+  DevBuf ib, qb, ctr, tb, ctl;
+  mk_status s = upload_queues(qs, ib, qb, nullptr);
+  if (s) return s;
+  MK_CUDA(cudaMalloc(&ctr.p, 4 * n_ctr));
+  MK_CUDA(cudaMemset(ctr.p, 0, 4 * n_ctr));
+  MK_CUDA(cudaMalloc(&tb.p, 8 * test_len));
+  if (!init.empty())
+    MK_CUDA(cudaMemcpy(tb.p, init.data(), 8 * test_len, cudaMemcpyHostToDevice));
+  else
+    MK_CUDA(cudaMemset(tb.p, 0, 8 * test_len));
+  MK_CUDA(cudaMalloc(&ctl.p, sizeof(Ctl)));
+  MK_CUDA(cudaMemset(ctl.p, 0, sizeof(Ctl)));
+  DevState S{};
+  S.counters = reinterpret_cast<uint32_t*>(ctr.p);
+  S.n_counters = n_ctr;
+  S.ctl = reinterpret_cast<Ctl*>(ctl.p);
+  S.n_cta = n_cta;
+  S.page_bytes = page;
+  S.n_pages = n_pages;
+  S.xbuf_bytes = 0;
+  S.scratch_bytes = 256;
+  S.timeout_ns = 2000000000LL;
+  S.backoff_max_ns = 256;
+  S.test_buf = reinterpret_cast<int64_t*>(tb.p);
+  S.test_len = test_len;
+  S.max_batch = 1;
+  S.Hq = S.Hkv = 1;
+  S.hd = 64;
+  S.d = 8;
+  StepArgs A{};
+  A.instr = reinterpret_cast<const Instr*>(ib.p);
+  A.q_start = reinterpret_cast<const int32_t*>(qb.p);
+  A.B = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(n_cta);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[2] = {&S, &A};
+  MK_CUDA(cudaLaunchKernelExC(&cfg, fn, args));
+  MK_CUDA(cudaDeviceSynchronize());
+  Ctl hc{};
+  MK_CUDA(cudaMemcpy(&hc, ctl.p, sizeof(Ctl), cudaMemcpyDeviceToHost));
+  std::vector<int64_t> out(test_len);
+  MK_CUDA(cudaMemcpy(out.data(), tb.p, 8 * test_len, cudaMemcpyDeviceToHost));
+  result[1] = n_cta;
+  result[2] = hc.err.code;
+  bool pass = hc.err.code == 0;
+  switch (kind) {
+    case 2:
+      for (int c = 0; c < n_cta && pass; ++c) {
+        int k_order = 0;
+        for (int k = 0; k < 20; ++k) {
+          if (k % 3 == 2) {
+            pass &= out[(int64_t)n_cta * 64 + c * 32 + k] == c * 1000 + k;
+          } else {
+            pass &= out[(int64_t)c * 64 + 1 + k_order] == c * 1000 + k;
+            ++k_order;
+          }
+        }
+        pass &= out[(int64_t)c * 64] == k_order;
+      }
+      break;
+    case 3:
+      for (int c = 0; c < n_cta && pass; ++c) pass &= out[c] == 7 + c;
+      pass &= out[n_cta] == 7 + n_cta;
+      result[3] = out[n_cta];
+      break;
+    case 4: {
+      const int64_t res_base = (int64_t)n_cta * chunks * words_per_page;
+      int64_t bad = 0;
+      for (int c = 0; c < n_cta; ++c)
+        for (int k = 0; k < chunks; ++k) {
+          uint64_t sum = 0;
+          const int64_t base = ((int64_t)c * chunks + k) * words_per_page;
+          for (int64_t i = 0; i < words_per_page; ++i) sum += (uint64_t)init[base + i];
+          if ((uint64_t)out[res_base + (int64_t)c * chunks + k] != sum) ++bad;
+        }
+      result[3] = bad;
+      pass &= bad == 0;
+      break;
+    }
+    default:
+      break;
+  }
+  result[0] = pass ? 1 : 0;
+  return MK_OK;
+}
+
+mk_status mk_barrier_bench(int mode, int n_barriers, double* us_per_barrier) {
+  if (!us_per_barrier || n_barriers < 1 || (mode != 0 && mode != 1))
+    return fail(MK_ERR_INVALID, "mode must be 0/1, n_barriers >= 1");
+  int dev = 0, n_sm = 0;
+  MK_CUDA(cudaGetDevice(&dev));
+  MK_CUDA(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
+  DevBuf ctr, slots, out;
+  MK_CUDA(cudaMalloc(&ctr.p, 4));
+  MK_CUDA(cudaMemset(ctr.p, 0, 4));
+  MK_CUDA(cudaMalloc(&slots.p, sizeof(float) * (size_t)n_barriers * n_sm));
+  MK_CUDA(cudaMemset(slots.p, 0xFF, sizeof(float) * (size_t)n_barriers * n_sm));
+  MK_CUDA(cudaMalloc(&out.p, 16));
+  MK_CUDA(cudaMemset(out.p, 0, 16));
+  uint32_t* c = reinterpret_cast<uint32_t*>(ctr.p);
+  float* sl = reinterpret_cast<float*>(slots.p);
+  int64_t timeout = 2000000000LL;
+  uint64_t* o = reinterpret_cast<uint64_t*>(out.p);
+  void* args[6] = {&c, &sl, &n_barriers, &mode, &timeout, &o};
+  MK_CUDA(cudaLaunchCooperativeKernel(barrier_kernel_entry(), dim3(n_sm), dim3(256), args, 0, nullptr));
+  MK_CUDA(cudaDeviceSynchronize());
+  uint64_t h[2];
+  MK_CUDA(cudaMemcpy(h, out.p, 16, cudaMemcpyDeviceToHost));
+  if (h[1]) return fail(MK_ERR_TIMEOUT, "barrier benchmark timed out");
+  *us_per_barrier = (double)h[0] / 1000.0 / n_barriers;
+  return MK_OK;
+}
+
+}  // extern "C"

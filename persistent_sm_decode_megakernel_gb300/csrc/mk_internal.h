@@ -1,0 +1,144 @@
+// Internal layout shared by the host runtime and the device code (plain old data only).
+//
+// Instruction format follows "8 · Écrire son megakernel", §8.2 (opcode, counter to wait,
+// expected value, counter to signal, integer arguments): here the expected value is the
+// number of signals the counter receives per decode step, and the device compares
+// against (epoch + 1) * that number, so counters never need resetting between steps.
+#pragma once
+#include <stdint.h>
+#include <vector_types.h>  // float2
+
+namespace mk {
+
+constexpr int kMaxBatch = 16;
+constexpr int kConsumerWarps = 8;                 // compute warps per CTA
+constexpr int kThreads = 32 * (kConsumerWarps + 1);  // + one producer (TMA) warp
+constexpr int kConsumerThreads = 32 * kConsumerWarps;
+constexpr int kMaxPages = 16;
+
+enum Op : uint8_t {
+  OP_END = 0,
+  OP_EMBED = 1,        // h0 = E[tok] (fp32)
+  OP_QKV = 2,          // RMSNorm + q/k/v rows + RoPE; k,v into the cache   (§8.2 RMSNORM_QKV_ROPE)
+  OP_ATTN = 3,         // split-KV partial attention                       (§8.2 ATTENTION)
+  OP_ATTN_REDUCE = 4,  // log-sum-exp merge of the splits                  (§8.2 ATTN_REDUCE)
+  OP_OPROJ = 5,        // h_mid = h + W_o o                                (§8.2 O_PROJ)
+  OP_UPGATE = 6,       // RMSNorm + a = silu(W_g x) * (W_u x)              (§8.2 MLP_UP_GATE)
+  OP_DOWN = 7,         // h_out = h_mid + W_d a                            (§8.2 MLP_DOWN)
+  OP_LMHEAD = 8,       // final RMSNorm + logits + argmax                  (§8.2 LM_HEAD)
+  // build-ladder self-test opcodes (§8.6 steps 1-4)
+  OP_T_NOP = 16,
+  OP_T_ORDER = 17,
+  OP_T_PRODUCE = 18,
+  OP_T_CONSUME = 19,
+  OP_T_PAGES = 20,
+};
+
+constexpr int kNumPhaseOps = 8;  // EMBED..LMHEAD, for the multi-launch phase tables
+
+enum : uint8_t { F_LAST_LM = 1 };
+
+// 64-byte instruction
+struct Instr {
+  uint8_t op;
+  uint8_t flags;
+  uint16_t layer;
+  int32_t wait_ctr;     // -1: none
+  uint32_t wait_n;      // signals per step on wait_ctr
+  int32_t signal_ctr;   // -1: none
+  int32_t a[12];        // op arguments (see the builder)
+};
+static_assert(sizeof(Instr) == 64, "instruction is 64 bytes");
+
+struct ErrWord {
+  uint32_t code;        // mk_status, 0 = none
+  int32_t cta;
+  int32_t pc;
+  int32_t ctr;
+};
+
+// small block read back by the host after every step (one device-to-host copy)
+struct Ctl {
+  ErrWord err;
+  int32_t tok[kMaxBatch];       // greedy token of the last completed step (device feed)
+  uint32_t trace_n;
+  uint32_t nan_seen;
+  uint32_t pad[2];
+};
+
+struct TraceRec {
+  int32_t cta, pc, op, layer;
+  uint64_t t_fetch, t_ready, t_end;
+};
+
+enum ActKind { ACT_H = 0, ACT_HMID, ACT_Q, ACT_KVN, ACT_PART, ACT_O, ACT_A, ACT_NUM };
+
+struct DevState {
+  // model
+  int L, d, Hq, Hkv, hd, F, V, dtype, max_batch, max_ctx, S;
+  float eps;
+  // slice widths of the row-major GEMVs (elements), one per weight family
+  int ws_qkv, ws_o, ws_up, ws_down, ws_lm;
+  // weights; per-layer device arrays of device pointers
+  const uint16_t* embed;
+  const uint16_t* final_norm;
+  const uint16_t* lm_head;
+  const uint16_t* const* attn_norm;
+  const uint16_t* const* wq;
+  const uint16_t* const* wk;
+  const uint16_t* const* wv;
+  const uint16_t* const* wo;
+  const uint16_t* const* mlp_norm;
+  const uint16_t* const* w_gate;
+  const uint16_t* const* w_up;
+  const uint16_t* const* w_down;
+  uint16_t* const* kcache;
+  uint16_t* const* vcache;
+  const float2* rope;          // [max_ctx][hd/2] (cos, sin), computed in double on the host
+  // activations: two parity sets of act_floats each (sentinel mode alternates them)
+  float* act;
+  int64_t act_floats;
+  int64_t act_off[ACT_NUM];    // offset of layer 0 of each kind
+  int64_t act_stride[ACT_NUM]; // per-layer stride of each kind
+  unsigned long long* argkeys; // [2][kMaxBatch]
+  uint32_t* counters;
+  int n_counters;
+  Ctl* ctl;
+  TraceRec* trace;
+  int trace_cap;
+  // execution
+  int n_cta;
+  int page_bytes, n_pages;
+  int xbuf_bytes, scratch_bytes;
+  int sync_mode;
+  int64_t timeout_ns;
+  int backoff_max_ns;
+  // self-test buffers
+  int64_t* test_buf;
+  int64_t test_len;
+};
+
+enum StepFlags : int {
+  SF_TOK_FROM_DEVICE = 1,  // embed the token chosen by the previous step (device feed)
+  SF_NO_SYNC = 2,          // multi-launch: stream order replaces waits and signals
+  SF_TRACE = 4,
+  SF_RESET_ARGMAX = 8,     // this launch resets the other parity's argmax keys
+};
+
+struct StepArgs {
+  const Instr* instr;
+  const int32_t* q_start;      // [n_cta + 1] queue offsets of this launch
+  uint32_t epoch;              // counter epoch of this schedule (targets = (epoch+1) * n)
+  uint32_t step;               // global step number (parity of argmax keys / sentinel sets)
+  int B;
+  int flags;
+  int32_t tok[kMaxBatch];
+  int32_t pos[kMaxBatch];
+  float* logits;               // [B][V] or null
+  int32_t* tok_hist;           // device [B] copy of this step's tokens, or null
+};
+
+// shared-memory layout sizes (bytes)
+constexpr int kCtlSmem = 2048;   // barriers, flags, small broadcast values
+
+}  // namespace mk

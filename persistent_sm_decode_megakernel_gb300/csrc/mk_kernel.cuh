@@ -1,0 +1,1006 @@
+// The persistent decode megakernel for sm_103a (templates; instantiated per weight
+// dtype and sync mode in mk_k_*.cu).
+//
+// Structure ("8 · Écrire son megakernel", §8.2): one CTA per SM walks its own queue of
+// 64-byte instructions; for each one it waits for its dependency counter, executes the
+// opcode, and signals the counter of its output.  Roles (§7.5, §8.2 classer_role): warp
+// 8 is the loader -- one lane streams every weight/KV tile of the CTA's whole queue into a
+// ring of shared-memory pages with TMA bulk copies, running ahead across instruction
+// boundaries (weights never depend on activations, so the HBM stream does not stop at a
+// dependency wait); warps 0-7 compute.  A page is handed back the moment its last reader
+// is done with it (§8.4), which is what lets the loader start the next instruction's
+// tiles while the current one still computes.
+#pragma once
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include "mk_internal.h"
+#include "mk_device.cuh"
+
+namespace mk {
+namespace {  // internal linkage: every instantiation unit gets its own copy
+
+struct SmemCtl {
+  uint64_t full[kMaxPages];
+  uint64_t empty[kMaxPages];
+  unsigned long long best[kMaxBatch];
+  float inv_rms[kMaxBatch];
+  float red[kConsumerWarps * kMaxBatch];
+  int last_issue_phase[kMaxPages];
+  volatile int abort;
+};
+static_assert(sizeof(SmemCtl) <= kCtlSmem, "control block fits");
+
+enum { SYNC_COUNTER = 0, SYNC_SENTINEL = 1 };
+
+// ---------------------------------------------------------------- errors
+__device__ __forceinline__ void set_err(const DevState& S, uint32_t code, int pc, int ctr) {
+  if (atomicCAS(&S.ctl->err.code, 0u, code) == 0u) {
+    S.ctl->err.cta = blockIdx.x;
+    S.ctl->err.pc = pc;
+    S.ctl->err.ctr = ctr;
+  }
+}
+__device__ __forceinline__ bool global_err(const DevState& S) {
+  return ld_relaxed_u32(&S.ctl->err.code) != 0u;
+}
+
+// Bounded wait on a dependency counter (§8.5): acquire load, exponential __nanosleep
+// backoff, gives up after the timeout and records where.  Wrap-safe comparison.
+__device__ __noinline__ bool wait_counter(const DevState& S, int ctr, uint32_t target, int pc) {
+  const uint32_t* p = S.counters + ctr;
+  if ((int32_t)(ld_acquire_u32(p) - target) >= 0) return true;
+  const uint64_t t0 = globaltimer_ns();
+  int k = 0;
+  while (true) {
+    int ns = 20 << (k < 8 ? k : 8);
+    __nanosleep(ns < S.backoff_max_ns ? ns : S.backoff_max_ns);
+    ++k;
+    if ((int32_t)(ld_acquire_u32(p) - target) >= 0) return true;
+    if (global_err(S)) return false;
+    if (globaltimer_ns() - t0 > (uint64_t)S.timeout_ns) {
+      set_err(S, 4u /*MK_ERR_TIMEOUT*/, pc, ctr);
+      return false;
+    }
+  }
+}
+
+// Sentinel read: the value itself is the signal (§7.3) -- poll with an L1-bypassing
+// gpu-scope load until it is no longer NaN.
+__device__ __noinline__ float poll_slow(const float* p, const DevState& S, SmemCtl* c) {
+  const uint64_t t0 = globaltimer_ns();
+  int k = 0;
+  while (true) {
+    int ns = 20 << (k < 8 ? k : 8);
+    __nanosleep(ns < S.backoff_max_ns ? ns : S.backoff_max_ns);
+    ++k;
+    float v = ld_poll_f32(p);
+    if (!isnan(v)) return v;
+    if (c->abort || global_err(S)) {
+      c->abort = 1;
+      return 0.f;
+    }
+    if (globaltimer_ns() - t0 > (uint64_t)S.timeout_ns) {
+      set_err(S, 4u, -1, -1);
+      c->abort = 1;
+      return 0.f;
+    }
+  }
+}
+template <int SYNC>
+__device__ __forceinline__ float load_act(const float* p, const DevState& S, SmemCtl* c) {
+  if (SYNC == SYNC_COUNTER) return __ldcg(p);
+  float v = ld_poll_f32(p);
+  if (!isnan(v)) return v;
+  return poll_slow(p, S, c);
+}
+
+// ---------------------------------------------------------------- tile geometry
+// A GEMV instruction covers one or two row segments of a row-major [rows, K] matrix.
+// Its tiles are "slices": WS consecutive elements of one row; a page holds
+// kConsumerWarps consecutive slices, one per compute warp.  Loader and compute warps
+// derive the same slice sequence from the instruction.
+struct Gemv {
+  const uint16_t* seg[2];
+  int segr[2];
+  int K, WS;
+  __device__ __forceinline__ int rows() const { return segr[0] + segr[1]; }
+  __device__ __forceinline__ int spr() const { return K / WS; }
+  __device__ __forceinline__ int nslices() const { return rows() * spr(); }
+  __device__ __forceinline__ const uint16_t* src(int i) const {
+    const int s = spr();
+    const int r = i / s, c = i - r * s;
+    const uint16_t* base = r < segr[0] ? seg[0] + (size_t)r * K : seg[1] + (size_t)(r - segr[0]) * K;
+    return base + (size_t)c * WS;
+  }
+};
+
+__device__ __forceinline__ Gemv make_gemv(const DevState& S, const Instr& in) {
+  Gemv g;
+  g.seg[1] = nullptr;
+  g.segr[1] = 0;
+  const int l = in.layer;
+  switch (in.op) {
+    case OP_QKV: {
+      const int mat = in.a[0], head = in.a[1], i0 = in.a[2], n = in.a[3];
+      const uint16_t* W = mat == 0 ? S.wq[l] : (mat == 1 ? S.wk[l] : S.wv[l]);
+      const size_t ra = (size_t)head * S.hd + i0;
+      g.seg[0] = W + ra * S.d;
+      g.seg[1] = W + (ra + S.hd / 2) * S.d;
+      g.segr[0] = g.segr[1] = n;
+      g.K = S.d;
+      g.WS = S.ws_qkv;
+      break;
+    }
+    case OP_OPROJ:
+      g.seg[0] = S.wo[l] + (size_t)in.a[0] * S.Hq * S.hd;
+      g.segr[0] = in.a[1];
+      g.K = S.Hq * S.hd;
+      g.WS = S.ws_o;
+      break;
+    case OP_UPGATE:
+      g.seg[0] = S.w_gate[l] + (size_t)in.a[0] * S.d;
+      g.seg[1] = S.w_up[l] + (size_t)in.a[0] * S.d;
+      g.segr[0] = g.segr[1] = in.a[1];
+      g.K = S.d;
+      g.WS = S.ws_up;
+      break;
+    case OP_DOWN:
+      g.seg[0] = S.w_down[l] + (size_t)in.a[0] * S.F;
+      g.segr[0] = in.a[1];
+      g.K = S.F;
+      g.WS = S.ws_down;
+      break;
+    default:  // OP_LMHEAD
+      g.seg[0] = S.lm_head + (size_t)in.a[0] * S.d;
+      g.segr[0] = in.a[1];
+      g.K = S.d;
+      g.WS = S.ws_lm;
+      break;
+  }
+  return g;
+}
+
+// Split-KV unit (§8.2 ATTENTION): sequence b, kv head j, split s of S over positions
+// 0..pos_b.  Cached positions [t0, min(t1, pos_b)) stream through pages as K, V blocks;
+// the split holding position pos_b takes the new key/value from the QKV op's fp32 copy.
+struct Attn {
+  int b, j, s, nsp, t0, t1, n_cached, pb, nblocks;
+  bool has_new;
+  const uint16_t* kb;
+  const uint16_t* vb;
+};
+__device__ __forceinline__ Attn make_attn(const DevState& S, const StepArgs& A, const Instr& in) {
+  Attn a;
+  a.b = in.a[0];
+  a.j = in.a[1];
+  a.s = in.a[2];
+  a.nsp = in.a[3];
+  const int npos = A.pos[a.b] + 1;
+  a.t0 = (int)((int64_t)a.s * npos / a.nsp);
+  a.t1 = (int)((int64_t)(a.s + 1) * npos / a.nsp);
+  const int tc = min(a.t1, npos - 1);
+  a.n_cached = max(0, tc - a.t0);
+  a.has_new = (a.t1 == npos);
+  a.pb = S.page_bytes / (S.hd * 2);
+  a.nblocks = (a.n_cached + a.pb - 1) / a.pb;
+  if (a.b >= A.B) {  // no such sequence in this step
+    a.n_cached = 0;
+    a.nblocks = 0;
+    a.has_new = false;
+  }
+  const size_t base = (((size_t)a.b * S.Hkv + a.j) * S.max_ctx + a.t0) * S.hd;
+  a.kb = S.kcache[in.layer] + base;
+  a.vb = S.vcache[in.layer] + base;
+  return a;
+}
+
+__device__ __forceinline__ float* act_ptr(const DevState& S, float* act, int kind, int layer) {
+  return act + S.act_off[kind] + (int64_t)layer * S.act_stride[kind];
+}
+
+// ---------------------------------------------------------------- loader warp
+__device__ bool producer_acquire(const DevState& S, SmemCtl* c, int slot, uint32_t ph) {
+  if (mbar_try_wait(&c->empty[slot], ph ^ 1)) return true;
+  uint64_t t0 = 0;
+  int k = 0;
+  while (!mbar_try_wait(&c->empty[slot], ph ^ 1)) {
+    if (c->abort) return false;
+    if ((++k & 63) == 0) {
+      const uint64_t t = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = t;
+      } else if (t - t0 > (uint64_t)S.timeout_ns) {
+        set_err(S, 4u, -3, -1);
+        c->abort = 1;
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+__device__ __noinline__ void producer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8_t* pages) {
+  const uint64_t pol = l2_evict_first_policy();
+  int slot = 0;
+  uint32_t ph = 0;
+  const int cta = blockIdx.x;
+  const int end = A.q_start[cta + 1];
+  bool ok = true;
+  for (int pc = A.q_start[cta]; pc < end && ok; ++pc) {
+    const Instr in = A.instr[pc];
+    if (in.op == OP_END) break;
+    switch (in.op) {
+      case OP_QKV:
+      case OP_OPROJ:
+      case OP_UPGATE:
+      case OP_DOWN:
+      case OP_LMHEAD: {
+        const Gemv g = make_gemv(S, in);
+        const int ns = g.nslices();
+        const uint32_t sb = (uint32_t)g.WS * 2u;
+        for (int i0 = 0; i0 < ns; i0 += kConsumerWarps) {
+          if (!producer_acquire(S, c, slot, ph)) {
+            ok = false;
+            break;
+          }
+          const int i1 = min(ns, i0 + kConsumerWarps);
+          mbar_arrive_expect_tx(&c->full[slot], (uint32_t)(i1 - i0) * sb);
+          uint8_t* dst = pages + (size_t)slot * S.page_bytes;
+          int i = i0;
+          while (i < i1) {  // one bulk copy per contiguous run of slices
+            const uint16_t* src = g.src(i);
+            int j = i + 1;
+            while (j < i1 && g.src(j) == src + (size_t)(j - i) * g.WS) ++j;
+            tma_load_1d(dst + (size_t)(i - i0) * sb, src, (uint32_t)(j - i) * sb, &c->full[slot], pol);
+            i = j;
+          }
+          c->last_issue_phase[slot] = (int)ph;
+          if (++slot == S.n_pages) { slot = 0; ph ^= 1u; }
+        }
+        break;
+      }
+      case OP_ATTN: {
+        const Attn at = make_attn(S, A, in);
+        for (int blk = 0; blk < at.nblocks && ok; ++blk) {
+          const int p0 = blk * at.pb;
+          const int np = min(at.pb, at.n_cached - p0);
+          const uint32_t bytes = (uint32_t)np * S.hd * 2u;
+          for (int kv = 0; kv < 2; ++kv) {
+            if (!producer_acquire(S, c, slot, ph)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&c->full[slot], bytes);
+            tma_load_1d(pages + (size_t)slot * S.page_bytes, (kv ? at.vb : at.kb) + (size_t)p0 * S.hd, bytes,
+                        &c->full[slot], pol);
+            c->last_issue_phase[slot] = (int)ph;
+            if (++slot == S.n_pages) { slot = 0; ph ^= 1u; }
+          }
+        }
+        break;
+      }
+      case OP_T_PAGES: {
+        const int n = in.a[1];
+        const int64_t words = S.page_bytes / 8;
+        for (int k = 0; k < n; ++k) {
+          if (!producer_acquire(S, c, slot, ph)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&c->full[slot], (uint32_t)S.page_bytes);
+          tma_load_1d(pages + (size_t)slot * S.page_bytes, S.test_buf + in.a[0] + (int64_t)k * words,
+                      (uint32_t)S.page_bytes, &c->full[slot], pol);
+          c->last_issue_phase[slot] = (int)ph;
+          if (++slot == S.n_pages) { slot = 0; ph ^= 1u; }
+        }
+        break;
+      }
+      default:
+        break;
+    }
+  }
+  // Drain: every issued copy must land before the CTA exits, and -- unless the step was
+  // abandoned -- every page must have been handed back (no leak, §8.9).
+  const uint64_t t0 = globaltimer_ns();
+  for (int s = 0; s < S.n_pages; ++s) {
+    const int p = c->last_issue_phase[s];
+    if (p < 0) continue;
+    while (!mbar_try_wait(&c->full[s], (uint32_t)p)) {
+      if (globaltimer_ns() - t0 > (uint64_t)S.timeout_ns) {
+        set_err(S, 4u, -4, s);
+        return;
+      }
+    }
+    if (c->abort) continue;
+    while (!mbar_try_wait(&c->empty[s], (uint32_t)p)) {
+      if (c->abort) break;
+      if (globaltimer_ns() - t0 > (uint64_t)S.timeout_ns) {
+        set_err(S, 5u /*MK_ERR_STATE: page never released*/, -5, s);
+        return;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- compute warps: pages
+struct Ring {
+  int slot;
+  uint32_t ph;
+};
+
+__device__ __forceinline__ const uint8_t* page_wait(const DevState& S, SmemCtl* c, uint8_t* pages, const Ring& r) {
+  if (!mbar_try_wait(&c->full[r.slot], r.ph)) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(&c->full[r.slot], r.ph)) {
+      if (c->abort) break;
+      if (globaltimer_ns() - t0 > (uint64_t)S.timeout_ns) {
+        set_err(S, 4u, -6, r.slot);
+        c->abort = 1;
+        break;
+      }
+    }
+  }
+  return pages + (size_t)r.slot * S.page_bytes;
+}
+// "free at last read" (§8.4): each compute warp hands the page back as soon as its own
+// reads are done; the loader refills it when all warps have done so.
+__device__ __forceinline__ void page_release(const DevState& S, SmemCtl* c, Ring& r) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&c->empty[r.slot]);
+  if (++r.slot == S.n_pages) {
+    r.slot = 0;
+    r.ph ^= 1u;
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ---------------------------------------------------------------- x staging
+// RMSNorm recomputed in every CTA from the full residual vector (it is 8 KB per
+// sequence and L2-resident), result written to the x buffer as fp32.
+template <typename WT, int SYNC, int NB>
+__device__ void stage_rmsnorm(const DevState& S, const float* h, const uint16_t* gain, int B, float* xbuf,
+                              SmemCtl* c) {
+  const int d = S.d, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float ss[NB];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    ss[b] = 0.f;
+    for (int k = tid; k < d; k += kConsumerThreads) {
+      const float v = (b < B) ? load_act<SYNC>(h + (size_t)b * d + k, S, c) : 0.f;
+      xbuf[b * d + k] = v;
+      ss[b] = fmaf(v, v, ss[b]);
+    }
+    ss[b] = warp_sum(ss[b]);
+    if (lane == 0) c->red[warp * NB + b] = ss[b];
+  }
+  consumer_sync();
+  if (tid < NB) {
+    float t = 0.f;
+    for (int w = 0; w < kConsumerWarps; ++w) t += c->red[w * NB + tid];
+    c->inv_rms[tid] = 1.0f / sqrtf(t / (float)d + S.eps);
+  }
+  consumer_sync();
+  for (int k = tid; k < d; k += kConsumerThreads) {
+    const float gk = Unpack<WT>::one(__ldg(gain + k));
+#pragma unroll
+    for (int b = 0; b < NB; ++b) xbuf[b * d + k] *= c->inv_rms[b] * gk;
+  }
+}
+
+template <int SYNC, int NB>
+__device__ void stage_copy(const DevState& S, const float* src, int K, int B, float* xbuf, SmemCtl* c) {
+  for (int t = threadIdx.x; t < NB * K; t += kConsumerThreads) {
+    const int b = t / K;
+    xbuf[t] = (b < B) ? load_act<SYNC>(src + t, S, c) : 0.f;
+  }
+}
+
+// ---------------------------------------------------------------- GEMV slice
+// One warp, one slice: lane l takes 16-byte vectors l, l+32, ... of the slice; fp32
+// accumulation per sequence; then a warp-shuffle reduction.
+template <typename WT, int NB>
+__device__ __forceinline__ void slice_dot(const uint8_t* wp, const float* x, int K, int WS, int lane,
+                                          float (&acc)[NB]) {
+  const uint4* w = reinterpret_cast<const uint4*>(wp);
+  const int nv = WS >> 3;
+#pragma unroll 2
+  for (int v = lane; v < nv; v += 32) {
+    const uint4 wv = w[v];
+    float f[8];
+    Unpack<WT>::u8(wv, f);
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const float4* xp = reinterpret_cast<const float4*>(x + (size_t)b * K + v * 8);
+      const float4 x0 = xp[0], x1 = xp[1];
+      float a = acc[b];
+      a = fmaf(f[0], x0.x, a);
+      a = fmaf(f[1], x0.y, a);
+      a = fmaf(f[2], x0.z, a);
+      a = fmaf(f[3], x0.w, a);
+      a = fmaf(f[4], x1.x, a);
+      a = fmaf(f[5], x1.y, a);
+      a = fmaf(f[6], x1.z, a);
+      a = fmaf(f[7], x1.w, a);
+      acc[b] = a;
+    }
+  }
+}
+
+__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
+
+template <typename WT, int SYNC, int NB>
+__device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const Instr& in, SmemCtl* c, uint8_t* pages,
+                        float* xbuf, float* scratch, Ring& ring, float* act) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int B = A.B, l = in.layer;
+  const Gemv g = make_gemv(S, in);
+
+  // 1. inputs
+  switch (in.op) {
+    case OP_QKV:
+      stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_H, l), S.attn_norm[l], B, xbuf, c);
+      break;
+    case OP_UPGATE:
+      stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_HMID, l), S.mlp_norm[l], B, xbuf, c);
+      break;
+    case OP_LMHEAD:
+      stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_H, S.L), S.final_norm, B, xbuf, c);
+      break;
+    case OP_OPROJ:
+      stage_copy<SYNC, NB>(S, act_ptr(S, act, ACT_O, l), g.K, B, xbuf, c);
+      break;
+    default:  // OP_DOWN
+      stage_copy<SYNC, NB>(S, act_ptr(S, act, ACT_A, l), g.K, B, xbuf, c);
+      break;
+  }
+  consumer_sync();
+
+  // 2. stream the slices
+  float* rowpart = scratch;  // [rows][spr][NB]
+  const int spr = g.spr(), ns = g.nslices();
+  for (int i0 = 0; i0 < ns; i0 += kConsumerWarps) {
+    const uint8_t* pg = page_wait(S, c, pages, ring);
+    const int i = i0 + warp;
+    if (i < ns) {
+      const int r = i / spr, s = i - r * spr;
+      float acc[NB];
+#pragma unroll
+      for (int b = 0; b < NB; ++b) acc[b] = 0.f;
+      slice_dot<WT, NB>(pg + (size_t)warp * g.WS * 2, xbuf + (size_t)s * g.WS, g.K, g.WS, lane, acc);
+#pragma unroll
+      for (int b = 0; b < NB; ++b) acc[b] = warp_sum(acc[b]);
+      if (lane == 0) {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) rowpart[((size_t)r * spr + s) * NB + b] = acc[b];
+      }
+    }
+    page_release(S, c, ring);
+  }
+  consumer_sync();
+
+  // 3. finalize rows in a fixed order and apply the op's epilogue
+  auto rowsum = [&](int r, int b) {
+    float t = 0.f;
+    for (int s = 0; s < spr; ++s) t += rowpart[((size_t)r * spr + s) * NB + b];
+    return t;
+  };
+  const int R = g.rows();
+  switch (in.op) {
+    case OP_QKV: {
+      const int mat = in.a[0], head = in.a[1], i0 = in.a[2], n = in.a[3];
+      const int hd = S.hd, half = hd / 2;
+      for (int t = tid; t < n * B; t += kConsumerThreads) {
+        const int r = t % n, b = t / n;
+        float va = rowsum(r, b), vb = rowsum(r + n, b);
+        const int i = i0 + r;
+        const int pos = A.pos[b];
+        if (mat < 2) {  // rotate-half RoPE on the pair (i, i + hd/2)
+          const float2 cs = S.rope[(size_t)pos * half + i];
+          const float xa = va * cs.x - vb * cs.y;
+          const float xb = vb * cs.x + va * cs.y;
+          va = xa;
+          vb = xb;
+        }
+        if (mat == 0) {
+          float* q = act_ptr(S, act, ACT_Q, l) + (size_t)b * S.Hq * hd + (size_t)head * hd;
+          q[i] = va;
+          q[i + half] = vb;
+        } else {
+          const uint16_t ra = Unpack<WT>::round(va), rb = Unpack<WT>::round(vb);
+          uint16_t* cache = (mat == 1 ? S.kcache[l] : S.vcache[l]) +
+                            (((size_t)b * S.Hkv + head) * S.max_ctx + pos) * hd;
+          cache[i] = ra;
+          cache[i + half] = rb;
+          float* kvn = act_ptr(S, act, ACT_KVN, l) + ((size_t)b * 2 + (mat - 1)) * S.Hkv * hd + (size_t)head * hd;
+          kvn[i] = Unpack<WT>::one(ra);
+          kvn[i + half] = Unpack<WT>::one(rb);
+        }
+      }
+      break;
+    }
+    case OP_OPROJ: {
+      const int row0 = in.a[0];
+      const float* hin = act_ptr(S, act, ACT_H, l);
+      float* hout = act_ptr(S, act, ACT_HMID, l);
+      for (int t = tid; t < R * B; t += kConsumerThreads) {
+        const int r = t % R, b = t / R;
+        const size_t idx = (size_t)b * S.d + row0 + r;
+        hout[idx] = load_act<SYNC>(hin + idx, S, c) + rowsum(r, b);
+      }
+      break;
+    }
+    case OP_UPGATE: {
+      const int row0 = in.a[0], n = in.a[1];
+      float* a = act_ptr(S, act, ACT_A, l);
+      for (int t = tid; t < n * B; t += kConsumerThreads) {
+        const int r = t % n, b = t / n;
+        a[(size_t)b * S.F + row0 + r] = silu_f(rowsum(r, b)) * rowsum(r + n, b);
+      }
+      break;
+    }
+    case OP_DOWN: {
+      const int row0 = in.a[0];
+      const float* hin = act_ptr(S, act, ACT_HMID, l);
+      float* hout = act_ptr(S, act, ACT_H, l + 1);
+      for (int t = tid; t < R * B; t += kConsumerThreads) {
+        const int r = t % R, b = t / R;
+        const size_t idx = (size_t)b * S.d + row0 + r;
+        hout[idx] = load_act<SYNC>(hin + idx, S, c) + rowsum(r, b);
+      }
+      break;
+    }
+    default: {  // OP_LMHEAD: logits and the running argmax (packed key, lowest index wins ties)
+      const int row0 = in.a[0];
+      unsigned long long best[NB];
+#pragma unroll
+      for (int b = 0; b < NB; ++b) best[b] = 0ull;
+      for (int t = tid; t < R * NB; t += kConsumerThreads) {
+        const int r = t % R, b = t / R;
+        if (b >= B) continue;
+        const float z = rowsum(r, b);
+        const int row = row0 + r;
+        if (A.logits) A.logits[(size_t)b * S.V + row] = z;
+        if (isnan(z)) atomicOr(&S.ctl->nan_seen, 1u);
+        const unsigned long long key =
+            ((unsigned long long)orderable(z) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)row);
+#pragma unroll
+        for (int bb = 0; bb < NB; ++bb)
+          if (bb == b && key > best[bb]) best[bb] = key;
+      }
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        unsigned long long v = best[b];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+          v = w > v ? w : v;
+        }
+        if (lane == 0 && v) atomicMax(&c->best[b], v);
+      }
+      break;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- attention
+template <typename WT, int SYNC, int HD, int G>
+__device__ __noinline__ void op_attn(const DevState& S, const StepArgs& A, const Instr& in, SmemCtl* c, uint8_t* pages,
+                        float* xbuf, float* scratch, Ring& ring, float* act) {
+  // 8 dims (one 16-byte row chunk) per lane, hd/8 lanes per position: keeps the G
+  // heads' accumulators inside the register budget (9 warps put 3 warps on one SM
+  // sub-partition of 16K registers, i.e. 168 registers per thread)
+  constexpr int DPL = 8;
+  constexpr int LPP = HD / DPL;      // lanes per position
+  constexpr int NGRP = 32 / LPP;     // positions per warp per pass
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int dl = lane & (LPP - 1), pgi = lane / LPP;
+  const Attn at = make_attn(S, A, in);
+  if (at.b >= A.B) return;  // uniform over the CTA
+  const int l = in.layer;
+  const float qscale = (1.0f / sqrtf((float)HD)) * 1.4426950408889634f;  // scores in log2 units
+
+  const float* qsrc = act_ptr(S, act, ACT_Q, l) + ((size_t)at.b * S.Hq + (size_t)at.j * G) * HD;
+  for (int t = tid; t < G * HD; t += kConsumerThreads) xbuf[t] = load_act<SYNC>(qsrc + t, S, c) * qscale;
+  // the new position's key and value (split holding pos_b), staged as storage-dtype rows
+  // like a page (the values are already rounded to that dtype, so this is exact)
+  uint16_t* knew = reinterpret_cast<uint16_t*>(xbuf + G * HD);
+  if (at.has_new) {
+    const float* kn = act_ptr(S, act, ACT_KVN, l) + (size_t)at.b * 2 * S.Hkv * HD + (size_t)at.j * HD;
+    for (int t = tid; t < 2 * HD; t += kConsumerThreads)
+      knew[t] = Unpack<WT>::round(load_act<SYNC>(kn + (t < HD ? t : (size_t)S.Hkv * HD + (t - HD)), S, c));
+  }
+  consumer_sync();
+  // q in registers when it fits beside the accumulators, else read (broadcast) from smem
+  constexpr bool QREG = G * DPL <= 32;
+  constexpr int QG = QREG ? G : 1, QD = QREG ? DPL : 1;
+  float q[QG][QD];
+  if (QREG) {
+#pragma unroll
+    for (int g = 0; g < QG; ++g)
+#pragma unroll
+      for (int i = 0; i < QD; ++i) q[g][i] = xbuf[g * HD + dl * DPL + i];
+  }
+  const float* qs = xbuf + dl * DPL;
+
+  float m[G], lsum[G], o[G][DPL];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    m[g] = -CUDART_INF_F;
+    lsum[g] = 0.f;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) o[g][i] = 0.f;
+  }
+
+  // One position per LPP-lane group: scores from its key row, online-softmax update,
+  // then its value row.  Rows come from a page (storage dtype) or, for the new
+  // position, from the fp32 staging in smem.
+  auto update = [&](bool valid, const uint16_t* krow, const uint16_t* vrow) {
+    float sc[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) sc[g] = 0.f;
+    if (valid) {
+#pragma unroll
+      for (int u = 0; u < DPL / 8; ++u) {
+        float kv[8];
+        Unpack<WT>::u8(reinterpret_cast<const uint4*>(krow)[u], kv);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float a = sc[g];
+          if (QREG) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) a = fmaf(q[QREG ? g : 0][QREG ? u * 8 + e : 0], kv[e], a);
+          } else {
+            const float4 q0 = *reinterpret_cast<const float4*>(qs + g * HD + u * 8);
+            const float4 q1 = *reinterpret_cast<const float4*>(qs + g * HD + u * 8 + 4);
+            a = fmaf(q0.x, kv[0], a); a = fmaf(q0.y, kv[1], a); a = fmaf(q0.z, kv[2], a); a = fmaf(q0.w, kv[3], a);
+            a = fmaf(q1.x, kv[4], a); a = fmaf(q1.y, kv[5], a); a = fmaf(q1.z, kv[6], a); a = fmaf(q1.w, kv[7], a);
+          }
+          sc[g] = a;
+        }
+      }
+    }
+    float p[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float a = sc[g];
+#pragma unroll
+      for (int o2 = 1; o2 < LPP; o2 <<= 1) a += __shfl_xor_sync(0xffffffffu, a, o2);
+      const float sv = valid ? a : -CUDART_INF_F;
+      float mx = sv;
+#pragma unroll
+      for (int o2 = LPP; o2 < 32; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+      const float mn = fmaxf(m[g], mx);  // warp-uniform
+      p[g] = 0.f;
+      if (mn == -CUDART_INF_F) continue;
+      if (mn != m[g]) {
+        const float corr = exp2f(m[g] - mn);
+        lsum[g] *= corr;
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) o[g][i] *= corr;
+        m[g] = mn;
+      }
+      p[g] = valid ? exp2f(sv - mn) : 0.f;
+      lsum[g] += p[g];
+    }
+    if (valid) {
+#pragma unroll
+      for (int u = 0; u < DPL / 8; ++u) {
+        float vv[8];
+        Unpack<WT>::u8(reinterpret_cast<const uint4*>(vrow)[u], vv);
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[g][u * 8 + e] = fmaf(p[g], vv[e], o[g][u * 8 + e]);
+      }
+    }
+  };
+
+  const int ppw = at.pb / kConsumerWarps;  // positions per warp per page
+  for (int blk = 0; blk < at.nblocks; ++blk) {
+    const int np = min(at.pb, at.n_cached - blk * at.pb);
+    const uint8_t* kp = page_wait(S, c, pages, ring);
+    Ring rv = ring;
+    if (++rv.slot == S.n_pages) { rv.slot = 0; rv.ph ^= 1u; }
+    const uint8_t* vp = page_wait(S, c, pages, rv);
+    for (int ps = 0; ps < ppw; ps += NGRP) {
+      const int t = warp * ppw + ps + pgi;
+      const bool valid = t < np;
+      const size_t off = (size_t)(valid ? t : 0) * HD * 2 + dl * DPL * 2;
+      update(valid, reinterpret_cast<const uint16_t*>(kp + off), reinterpret_cast<const uint16_t*>(vp + off));
+    }
+    page_release(S, c, ring);  // K page
+    page_release(S, c, ring);  // V page
+  }
+  if (at.has_new && warp == 0)  // position pos_b: the new key/value of this step
+    update(pgi == 0, knew + dl * DPL, knew + HD + dl * DPL);
+  // combine the position groups of the warp (same running max), then the warps
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+#pragma unroll
+    for (int o2 = LPP; o2 < 32; o2 <<= 1) {
+      lsum[g] += __shfl_xor_sync(0xffffffffu, lsum[g], o2);
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) o[g][i] += __shfl_xor_sync(0xffffffffu, o[g][i], o2);
+    }
+  }
+  constexpr int RW = HD + 2;
+  if (pgi == 0) {
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) scratch[(warp * G + g) * RW + dl * DPL + i] = o[g][i];
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      scratch[(warp * G + g) * RW + HD] = m[g];
+      scratch[(warp * G + g) * RW + HD + 1] = lsum[g];
+    }
+  }
+  consumer_sync();
+  float* part = act_ptr(S, act, ACT_PART, l) + (((size_t)at.b * S.Hkv + at.j) * S.S + at.s) * G * RW;
+  for (int t = tid; t < G * RW; t += kConsumerThreads) {
+    const int g = t / RW, e = t - g * RW;
+    float M = -CUDART_INF_F;
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, scratch[(w * G + g) * RW + HD]);
+    float r;
+    if (e == HD) {
+      r = M;
+    } else if (M == -CUDART_INF_F) {
+      r = 0.f;
+    } else {
+      r = 0.f;
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float mw = scratch[(w * G + g) * RW + HD];
+        if (mw != -CUDART_INF_F) r = fmaf(exp2f(mw - M), scratch[(w * G + g) * RW + e], r);
+      }
+    }
+    part[t] = r;
+  }
+}
+
+// log-sum-exp merge of the S split partials of one (sequence, kv head) (§8.2 ATTN_REDUCE)
+template <int SYNC>
+__device__ __noinline__ void op_attn_reduce(const DevState& S, const Instr& in, int B, SmemCtl* c, float* scratch, float* act) {
+  const int tid = threadIdx.x;
+  const int b = in.a[0], j = in.a[1], l = in.layer;
+  if (b >= B) return;  // uniform over the CTA
+  const int HD = S.hd, G = S.Hq / S.Hkv, RW = HD + 2, NS = S.S;
+  const float* part = act_ptr(S, act, ACT_PART, l) + ((size_t)b * S.Hkv + j) * NS * G * RW;
+  for (int t = tid; t < NS * G; t += kConsumerThreads) {
+    scratch[2 * t] = load_act<SYNC>(part + (size_t)t * RW + HD, S, c);
+    scratch[2 * t + 1] = load_act<SYNC>(part + (size_t)t * RW + HD + 1, S, c);
+  }
+  consumer_sync();
+  float* out = act_ptr(S, act, ACT_O, l) + (size_t)b * S.Hq * HD + (size_t)j * G * HD;
+  for (int t = tid; t < G * HD; t += kConsumerThreads) {
+    const int g = t / HD, e = t - g * HD;
+    float M = -CUDART_INF_F;
+    for (int s = 0; s < NS; ++s) M = fmaxf(M, scratch[2 * (s * G + g)]);
+    float num = 0.f, den = 0.f;
+    for (int s = 0; s < NS; ++s) {
+      const float ms = scratch[2 * (s * G + g)];
+      if (ms == -CUDART_INF_F) continue;
+      const float w = exp2f(ms - M);
+      num = fmaf(w, load_act<SYNC>(part + (size_t)(s * G + g) * RW + e, S, c), num);
+      den = fmaf(w, scratch[2 * (s * G + g) + 1], den);
+    }
+    out[t] = num / den;
+  }
+}
+
+template <typename WT>
+__device__ void op_embed(const DevState& S, const StepArgs& A, const Instr& in, float* act) {
+  float* h0 = act_ptr(S, act, ACT_H, 0);
+  const bool dev = (A.flags & SF_TOK_FROM_DEVICE) != 0;
+  const int e1 = min(in.a[1], A.B * S.d);
+  for (int e = in.a[0] + threadIdx.x; e < e1; e += kConsumerThreads) {
+    const int b = e / S.d, k = e - b * S.d;
+    int tok = dev ? (int)ld_relaxed_u32(reinterpret_cast<const uint32_t*>(&S.ctl->tok[b])) : A.tok[b];
+    if (tok < 0 || tok >= S.V) {  // only a failed previous step can leave this behind
+      set_err(S, 5u /*MK_ERR_STATE*/, -8, tok);
+      tok = 0;
+    }
+    h0[(size_t)b * S.d + k] = Unpack<WT>::one(S.embed[(size_t)tok * S.d + k]);
+  }
+}
+
+// ---------------------------------------------------------------- self-test opcodes
+__device__ void op_test_pages(const DevState& S, const Instr& in, SmemCtl* c, uint8_t* pages, float* scratch,
+                              Ring& ring) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  unsigned long long* ws = reinterpret_cast<unsigned long long*>(scratch);
+  const int words = S.page_bytes / 8, per_warp = words / kConsumerWarps;
+  for (int k = 0; k < in.a[1]; ++k) {
+    const uint64_t* pg = reinterpret_cast<const uint64_t*>(page_wait(S, c, pages, ring));
+    unsigned long long sum = 0;
+    for (int i = lane; i < per_warp; i += 32) sum += pg[warp * per_warp + i];
+    page_release(S, c, ring);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) ws[warp] = sum;
+    consumer_sync();
+    if (tid == 0) {
+      unsigned long long t = 0;
+      for (int w = 0; w < kConsumerWarps; ++w) t += ws[w];
+      S.test_buf[in.a[2] + k] = (int64_t)t;
+    }
+    consumer_sync();
+  }
+}
+
+// ---------------------------------------------------------------- compute warps: loop
+template <typename WT, int SYNC>
+__device__ void consumer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8_t* pages, float* xbuf,
+                         float* scratch) {
+  const int tid = threadIdx.x, cta = blockIdx.x;
+  const bool nosync = (A.flags & SF_NO_SYNC) != 0;
+  const bool TRACE = (A.flags & SF_TRACE) != 0;
+  const int par = (SYNC == SYNC_SENTINEL && !nosync) ? (int)(A.step & 1u) : 0;
+  float* act = S.act + (int64_t)par * S.act_floats;
+  const int nb = A.B <= 1 ? 1 : A.B <= 2 ? 2 : A.B <= 4 ? 4 : A.B <= 8 ? 8 : 16;
+  const int G = S.Hq / S.Hkv;
+  Ring ring{0, 0u};
+  int order_n = 0;
+  const int end = A.q_start[cta + 1];
+  for (int pc = A.q_start[cta]; pc < end; ++pc) {
+    const Instr in = A.instr[pc];
+    if (in.op == OP_END) break;
+    uint64_t t_fetch = 0, t_ready = 0;
+    if (TRACE) t_fetch = globaltimer_ns();
+    // ---- wait for the dependency (counter mode; sentinel mode polls the data itself)
+    const bool use_ctr = (SYNC == SYNC_COUNTER || in.op >= OP_T_NOP) && !nosync;
+    if (use_ctr && in.wait_ctr >= 0) {
+      bool bad = false;
+      if (tid == 0 && !wait_counter(S, in.wait_ctr, (A.epoch + 1u) * in.wait_n, pc)) {
+        c->abort = 1;
+        bad = true;
+      }
+      if (consumer_sync_or(bad || c->abort)) break;
+    }
+    if (TRACE) t_ready = globaltimer_ns();
+    // ---- execute
+    switch (in.op) {
+      case OP_EMBED:
+        op_embed<WT>(S, A, in, act);
+        break;
+      case OP_QKV:
+      case OP_OPROJ:
+      case OP_UPGATE:
+      case OP_DOWN:
+      case OP_LMHEAD:
+        switch (nb) {
+          case 1: op_gemv<WT, SYNC, 1>(S, A, in, c, pages, xbuf, scratch, ring, act); break;
+          case 2: op_gemv<WT, SYNC, 2>(S, A, in, c, pages, xbuf, scratch, ring, act); break;
+          case 4: op_gemv<WT, SYNC, 4>(S, A, in, c, pages, xbuf, scratch, ring, act); break;
+          case 8: op_gemv<WT, SYNC, 8>(S, A, in, c, pages, xbuf, scratch, ring, act); break;
+          default: op_gemv<WT, SYNC, 16>(S, A, in, c, pages, xbuf, scratch, ring, act); break;
+        }
+        break;
+      case OP_ATTN:
+        if (S.hd == 64 && G == 2)
+          op_attn<WT, SYNC, 64, 2>(S, A, in, c, pages, xbuf, scratch, ring, act);
+        else if (S.hd == 128 && G == 2)
+          op_attn<WT, SYNC, 128, 2>(S, A, in, c, pages, xbuf, scratch, ring, act);
+        else if (S.hd == 128 && G == 4)
+          op_attn<WT, SYNC, 128, 4>(S, A, in, c, pages, xbuf, scratch, ring, act);
+        else if (S.hd == 64 && G == 4)
+          op_attn<WT, SYNC, 64, 4>(S, A, in, c, pages, xbuf, scratch, ring, act);
+        else if (S.hd == 128 && G == 1)
+          op_attn<WT, SYNC, 128, 1>(S, A, in, c, pages, xbuf, scratch, ring, act);
+        else
+          op_attn<WT, SYNC, 64, 1>(S, A, in, c, pages, xbuf, scratch, ring, act);
+        break;
+      case OP_ATTN_REDUCE:
+        op_attn_reduce<SYNC>(S, in, A.B, c, scratch, act);
+        break;
+      case OP_T_ORDER:
+      case OP_T_PRODUCE:
+        if (tid == 0) {
+          if (in.op == OP_T_ORDER) {
+            S.test_buf[(int64_t)cta * 64 + 1 + order_n] = in.a[1];
+            ++order_n;
+            S.test_buf[(int64_t)cta * 64] = order_n;
+          } else {
+            S.test_buf[in.a[0]] = in.a[1];
+          }
+        }
+        break;
+      case OP_T_CONSUME:
+        if (tid == 0) S.test_buf[in.a[2]] = __ldcg(reinterpret_cast<const long long*>(S.test_buf + in.a[0])) + 1;
+        break;
+      case OP_T_PAGES:
+        op_test_pages(S, in, c, pages, scratch, ring);
+        break;
+      default:
+        break;
+    }
+    // ---- signal
+    if (consumer_sync_or(c->abort)) break;
+    if (in.op == OP_LMHEAD && (in.flags & F_LAST_LM)) {
+      // this CTA's share of the vocabulary is done: publish its best key, then the last
+      // CTA to finish turns the winning keys into tokens
+      const uint32_t kp = A.step & 1u;
+      if (tid < A.B) atomicMax(&S.argkeys[kp * kMaxBatch + tid], c->best[tid]);
+      consumer_sync();
+      if (tid == 0) {
+        const uint32_t n_lm = (uint32_t)in.a[5];
+        const uint32_t old = atom_acq_rel_add_u32(&S.counters[in.signal_ctr], 1u);
+        if (old + 1u == (A.epoch + 1u) * n_lm) {
+          for (int b = 0; b < A.B; ++b) {
+            const uint64_t key = ld_relaxed_u64(&S.argkeys[kp * kMaxBatch + b]);
+            const int32_t tok = (int32_t)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+            S.ctl->tok[b] = tok;
+            if (A.tok_hist) A.tok_hist[b] = tok;
+          }
+        }
+      }
+    } else if (tid == 0 && use_ctr && in.signal_ctr >= 0) {
+      red_release_add_u32(&S.counters[in.signal_ctr], 1u);
+    }
+    if (TRACE && tid == 0) {
+      const uint32_t k = atomicAdd(&S.ctl->trace_n, 1u);
+      if ((int)k < S.trace_cap) {
+        TraceRec rec;
+        rec.cta = cta;
+        rec.pc = pc;
+        rec.op = in.op;
+        rec.layer = in.layer;
+        rec.t_fetch = t_fetch;
+        rec.t_ready = t_ready;
+        rec.t_end = globaltimer_ns();
+        S.trace[k] = rec;
+      }
+    }
+  }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- the kernel
+template <typename WT, int SYNC>
+__global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_constant__ DevState S,
+                                                              const __grid_constant__ StepArgs A) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* pages = smem;
+  float* xbuf = reinterpret_cast<float*>(smem + (size_t)S.n_pages * S.page_bytes);
+  float* scratch = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(xbuf) + S.xbuf_bytes);
+  SmemCtl* c = reinterpret_cast<SmemCtl*>(reinterpret_cast<uint8_t*>(scratch) + S.scratch_bytes);
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    for (int i = 0; i < S.n_pages; ++i) {
+      mbar_init(&c->full[i], 1);
+      mbar_init(&c->empty[i], kConsumerWarps);
+      c->last_issue_phase[i] = -1;
+    }
+    c->abort = 0;
+    mbar_fence_init();
+  }
+  if (tid < kMaxBatch) c->best[tid] = 0ull;
+  // per-step housekeeping: the other parity's argmax keys (and, with NaN sentinels, the
+  // other parity's activations) are reset for the next step; nothing reads them now
+  if ((A.flags & SF_RESET_ARGMAX) && blockIdx.x == 0 && tid < kMaxBatch)
+    S.argkeys[((A.step + 1u) & 1u) * kMaxBatch + tid] = 0ull;
+  if (SYNC == SYNC_SENTINEL && !(A.flags & SF_NO_SYNC)) {
+    float* other = S.act + (int64_t)((A.step + 1u) & 1u) * S.act_floats;
+    const int64_t n4 = S.act_floats / 4;
+    float4* o4 = reinterpret_cast<float4*>(other);
+    const float4 nan4 = make_float4(CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F);
+    for (int64_t i = (int64_t)blockIdx.x * kThreads + tid; i < n4; i += (int64_t)gridDim.x * kThreads) o4[i] = nan4;
+  }
+  __syncthreads();
+  if (tid >= kConsumerThreads) {
+    if (tid == kConsumerThreads) producer(S, A, c, pages);
+    return;
+  }
+  consumer<WT, SYNC>(S, A, c, pages, xbuf, scratch);
+  if (c->abort && tid == 0 && !global_err(S)) set_err(S, 4u, -7, -1);
+}
+
+}  // namespace mk

@@ -1,0 +1,9 @@
+// Entry points of the device code, for the host runtime.
+#pragma once
+
+namespace mk {
+// persistent step kernel instantiation for (weight dtype, sync mode, trace on/off)
+const void* step_kernel_entry(int dtype, int sync_mode, bool trace);
+// grid-barrier latency microbenchmark kernel
+const void* barrier_kernel_entry();
+}  // namespace mk

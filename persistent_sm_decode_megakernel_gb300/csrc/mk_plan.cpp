@@ -1,0 +1,461 @@
+// Schedule builder and static validator (host only, no CUDA).
+//
+// The builder turns one decode step into per-CTA instruction queues (§8.2 "liste plate,
+// par SM"): every op of every layer is cut into units balanced over all CTAs by streamed
+// bytes, each CTA's queue lists its units in layer order, and each op's units signal one
+// counter that the next op's units wait for in full.
+//
+// The validator certifies a schedule before it is uploaded (§8.7, static verification):
+// it simulates the queues with counter semantics (every queue must run to its end: no
+// deadlock), checks that every counter's per-step signal count equals what each waiter
+// expects, that every buffer an instruction reads was fully written by instructions that
+// happen before it (no race), that every output element is written exactly once, and
+// that no instruction exceeds the shared-memory scratch it is given.
+#include "mk_plan.h"
+
+#include <algorithm>
+#include <cstdio>
+#include <numeric>
+
+namespace mk {
+
+static int pow2_at_least(int b) {
+  int n = 1;
+  while (n < b) n <<= 1;
+  return n;
+}
+
+// largest divisor of K that is a multiple of 8 elements (16 bytes) and at most max_ws
+static int slice_width(int K, int max_ws) {
+  int best = 0;
+  for (int w = 8; w <= std::min(K, max_ws); w += 8)
+    if (K % w == 0) best = w;
+  return best;
+}
+
+static std::string fmt(const char* f, long long a = 0, long long b = 0, long long c = 0) {
+  char buf[256];
+  snprintf(buf, sizeof buf, f, a, b, c);
+  return buf;
+}
+
+std::string make_geometry(const ModelShape& m, int n_cta, int page_bytes, int n_pages_req, int kv_splits,
+                          int smem_limit, Geometry* g) {
+  *g = Geometry();
+  const int G = m.Hq / m.Hkv;
+  if (m.hd != 64 && m.hd != 128) return "head_dim must be 64 or 128";
+  if (G != 1 && G != 2 && G != 4) return "n_heads / n_kv_heads must be 1, 2 or 4";
+  g->page_bytes = page_bytes > 0 ? page_bytes : 16384;
+  if ((g->page_bytes & (g->page_bytes - 1)) || g->page_bytes < 4096 || g->page_bytes > 32768)
+    return "page_bytes must be a power of two in [4096, 32768]";
+  if (g->page_bytes < 64 * m.hd) return fmt("page_bytes must be at least 64 * head_dim = %lld", 64LL * m.hd);
+  g->nb_max = pow2_at_least(m.max_batch);
+  const int max_ws = g->page_bytes / (2 * kConsumerWarps);
+  g->ws_qkv = slice_width(m.d, max_ws);
+  g->ws_up = g->ws_qkv;
+  g->ws_lm = g->ws_qkv;
+  g->ws_o = slice_width(m.Hq * m.hd, max_ws);
+  g->ws_down = slice_width(m.F, max_ws);
+  if (!g->ws_qkv || !g->ws_o || !g->ws_down) return "d_model, n_heads*head_dim and ffn_dim must be multiples of 8";
+  const int kmax = std::max(m.d, std::max(m.Hq * m.hd, m.F));
+  // x buffer: a batch of GEMV inputs, or q of one GQA group plus the new key/value
+  const int xfloats = std::max(g->nb_max * kmax, (G + 1) * m.hd);
+  g->xbuf_bytes = ((xfloats * 4 + 127) / 128) * 128;
+  if (kv_splits > 0) {
+    g->S = kv_splits;
+  } else {
+    g->S = n_cta / std::gcd(n_cta, m.Hkv);
+    if (g->S > 64) g->S = std::max(1, n_cta / m.Hkv);
+  }
+  if (g->S < 1 || g->S > 256) return "kv_splits out of range [1, 256]";
+  int scratch = 16384;
+  scratch = std::max(scratch, kConsumerWarps * G * (m.hd + 2) * 4);
+  scratch = std::max(scratch, g->S * G * 2 * 4);
+  g->scratch_bytes = ((scratch + 127) / 128) * 128;
+  const int avail = smem_limit - g->xbuf_bytes - g->scratch_bytes - kCtlSmem;
+  int np = avail > 0 ? avail / g->page_bytes : 0;
+  np = std::min(np, kMaxPages);
+  if (n_pages_req > 0) np = std::min(np, n_pages_req);
+  if (np < 2)
+    return fmt("shared memory too small: x buffer %lld B + scratch %lld B leave %lld pages (max_batch too large)",
+               g->xbuf_bytes, g->scratch_bytes, np);
+  g->n_pages = np;
+  g->smem_bytes = np * g->page_bytes + g->xbuf_bytes + g->scratch_bytes + kCtlSmem;
+  return "";
+}
+
+static inline int split_lo(long long total, int parts, int i) { return (int)(total * i / parts); }
+
+static Instr mk_instr(int op, int layer, int wait_ctr, uint32_t wait_n, int signal_ctr) {
+  Instr in{};
+  in.op = (uint8_t)op;
+  in.layer = (uint16_t)layer;
+  in.wait_ctr = wait_ctr;
+  in.wait_n = wait_n;
+  in.signal_ctr = signal_ctr;
+  return in;
+}
+
+std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B, int drop_signal, Plan* p) {
+  if (B < 1 || B > m.max_batch) return "batch out of range";
+  *p = Plan();
+  p->n_cta = n_cta;
+  p->B = B;
+  p->queues.assign(n_cta, {});
+  const int nb = pow2_at_least(B);
+  const int scratch_floats = g.scratch_bytes / 4;
+  const int half = m.hd / 2;
+  const int G = m.Hq / m.Hkv;
+  auto rows_cap = [&](int K, int ws, int segs) {  // rows per GEMV instruction (rowpart scratch)
+    const int spr = K / ws;
+    return std::max(1, scratch_floats / (spr * nb * segs));
+  };
+  auto new_ctr = [&]() {
+    p->signals.push_back(0);
+    return (int)p->signals.size() - 1;
+  };
+  // pending instructions: collected first, then the wait counts are filled in
+  struct Pending {
+    int cta;
+    Instr in;
+  };
+  std::vector<Pending> all;
+  auto emit = [&](int cta, const Instr& in) {
+    all.push_back({cta, in});
+    if (in.signal_ctr >= 0) p->signals[in.signal_ctr]++;
+  };
+
+  // EMBED
+  const int c_emb = new_ctr();
+  for (int c = 0; c < n_cta; ++c) {
+    const int e0 = split_lo((long long)B * m.d, n_cta, c), e1 = split_lo((long long)B * m.d, n_cta, c + 1);
+    if (e1 <= e0) continue;
+    Instr in = mk_instr(OP_EMBED, 0, -1, 0, c_emb);
+    in.a[0] = e0;
+    in.a[1] = e1;
+    emit(c, in);
+  }
+  int prev = c_emb;
+  for (int l = 0; l < m.L; ++l) {
+    // RMSNORM_QKV_ROPE: rotate-half pairs (i, i + hd/2) stay in one instruction
+    const int c_qkv = new_ctr();
+    {
+      const long long pairs = (long long)(m.Hq + 2 * m.Hkv) * half;
+      const int cap = std::max(1, rows_cap(m.d, g.ws_qkv, 1) / 2);
+      for (int c = 0; c < n_cta; ++c) {
+        long long p0 = split_lo(pairs, n_cta, c);
+        const long long p1 = split_lo(pairs, n_cta, c + 1);
+        while (p0 < p1) {
+          const int hh = (int)(p0 / half);
+          const long long seg_end = std::min<long long>(p1, (long long)(hh + 1) * half);
+          const int n = (int)std::min<long long>(seg_end - p0, cap);
+          Instr in = mk_instr(OP_QKV, l, prev, 0, c_qkv);
+          in.a[0] = hh < m.Hq ? 0 : (hh < m.Hq + m.Hkv ? 1 : 2);
+          in.a[1] = hh < m.Hq ? hh : (hh < m.Hq + m.Hkv ? hh - m.Hq : hh - m.Hq - m.Hkv);
+          in.a[2] = (int)(p0 % half);
+          in.a[3] = n;
+          emit(c, in);
+          p0 += n;
+        }
+      }
+    }
+    // ATTENTION: B * Hkv * S split units, dealt round-robin
+    const int c_att = new_ctr();
+    {
+      const int nu = B * m.Hkv * g.S;
+      for (int u = 0; u < nu; ++u) {
+        Instr in = mk_instr(OP_ATTN, l, c_qkv, 0, c_att);
+        in.a[0] = u / (m.Hkv * g.S);
+        in.a[1] = (u / g.S) % m.Hkv;
+        in.a[2] = u % g.S;
+        in.a[3] = g.S;
+        emit(u % n_cta, in);
+      }
+    }
+    // ATTN_REDUCE: one unit per (sequence, kv head), spread over the CTAs
+    const int c_red = new_ctr();
+    {
+      const int nu = B * m.Hkv;
+      for (int u = 0; u < nu; ++u) {
+        Instr in = mk_instr(OP_ATTN_REDUCE, l, c_att, 0, c_red);
+        in.a[0] = u / m.Hkv;
+        in.a[1] = u % m.Hkv;
+        emit((int)((long long)u * n_cta / nu), in);
+      }
+    }
+    // O_PROJ, MLP_UP_GATE, MLP_DOWN: row ranges
+    auto rows_op = [&](int op, int rows, int K, int ws, int segs, int wait, int sig) {
+      const int cap = rows_cap(K, ws, segs);
+      for (int c = 0; c < n_cta; ++c) {
+        int r0 = split_lo(rows, n_cta, c);
+        const int r1 = split_lo(rows, n_cta, c + 1);
+        while (r0 < r1) {
+          const int n = std::min(r1 - r0, cap);
+          Instr in = mk_instr(op, l, wait, 0, sig);
+          in.a[0] = r0;
+          in.a[1] = n;
+          emit(c, in);
+          r0 += n;
+        }
+      }
+    };
+    const int c_o = new_ctr();
+    rows_op(OP_OPROJ, m.d, m.Hq * m.hd, g.ws_o, 1, c_red, c_o);
+    const int c_ug = new_ctr();
+    rows_op(OP_UPGATE, m.F, m.d, g.ws_up, 2, c_o, c_ug);
+    const int c_dn = new_ctr();
+    rows_op(OP_DOWN, m.d, m.F, g.ws_down, 1, c_ug, c_dn);
+    prev = c_dn;
+  }
+  // LM_HEAD: vocabulary rows; the last chunk of each CTA publishes its argmax
+  {
+    const int c_lm = new_ctr();
+    const int cap = rows_cap(m.d, g.ws_lm, 1);
+    int n_lm = 0;
+    for (int c = 0; c < n_cta; ++c)
+      if (split_lo(m.V, n_cta, c + 1) > split_lo(m.V, n_cta, c)) ++n_lm;
+    for (int c = 0; c < n_cta; ++c) {
+      int r0 = split_lo(m.V, n_cta, c);
+      const int r1 = split_lo(m.V, n_cta, c + 1);
+      while (r0 < r1) {
+        const int n = std::min(r1 - r0, cap);
+        const bool last = r0 + n == r1;
+        Instr in = mk_instr(OP_LMHEAD, m.L, prev, 0, last ? c_lm : -1);
+        in.a[0] = r0;
+        in.a[1] = n;
+        if (last) {
+          in.flags = F_LAST_LM;
+          in.a[5] = n_lm;
+        }
+        emit(c, in);
+        r0 += n;
+      }
+    }
+  }
+  p->n_counters = (int)p->signals.size();
+  // wait counts = every signal of the awaited counter in one step
+  for (auto& pe : all)
+    if (pe.in.wait_ctr >= 0) pe.in.wait_n = p->signals[pe.in.wait_ctr];
+  int sig_seen = 0;
+  for (auto& pe : all) {
+    // fault injection: the k-th signal is removed, its waiters keep expecting it
+    if (drop_signal > 0 && pe.in.signal_ctr >= 0 && !(pe.in.flags & F_LAST_LM) && ++sig_seen == drop_signal)
+      pe.in.signal_ctr = -1;
+    p->queues[pe.cta].push_back(pe.in);
+  }
+  for (auto& q : p->queues) q.push_back(mk_instr(OP_END, 0, -1, 0, -1));
+
+  // multi-launch control: one launch per (op, layer) in dependency order
+  auto phase_of = [&](const Instr& in) -> int {
+    if (in.op == OP_EMBED) return 0;
+    if (in.op == OP_LMHEAD) return 1 + 6 * m.L;
+    return 1 + 6 * in.layer + (in.op - OP_QKV);
+  };
+  const int n_phase = 2 + 6 * m.L;
+  p->phase_queues.assign(n_phase, std::vector<std::vector<Instr>>(n_cta));
+  for (int c = 0; c < n_cta; ++c)
+    for (const auto& in : p->queues[c])
+      if (in.op != OP_END) p->phase_queues[phase_of(in)][c].push_back(in);
+  for (auto& ph : p->phase_queues)
+    for (auto& q : ph) q.push_back(mk_instr(OP_END, 0, -1, 0, -1));
+
+  // streamed weight bytes of one step
+  long long per_layer = (long long)(m.Hq + 2 * m.Hkv) * m.hd * m.d + (long long)m.d * m.Hq * m.hd +
+                        3LL * m.d * m.F + 2LL * m.d;
+  p->weight_bytes = 2 * ((long long)m.L * per_layer + (long long)m.V * m.d + m.d);
+  (void)G;
+  return "";
+}
+
+// ---------------------------------------------------------------- validator
+namespace {
+struct Bits {
+  std::vector<uint64_t> w;
+  explicit Bits(int n = 0) : w((n + 63) / 64, 0) {}
+  void set(int i) { w[i >> 6] |= 1ull << (i & 63); }
+  bool has(int i) const { return (w[i >> 6] >> (i & 63)) & 1; }
+  void merge(const Bits& o) {
+    for (size_t i = 0; i < w.size(); ++i) w[i] |= o.w[i];
+  }
+};
+}  // namespace
+
+std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p) {
+  const int n_cta = p.n_cta, B = p.B, half = m.hd / 2;
+  const int nb = pow2_at_least(B);
+  const int scratch_floats = g.scratch_bytes / 4;
+  const int n_group = 2 + 6 * m.L;
+  auto group_of = [&](const Instr& in) -> int {
+    if (in.op == OP_EMBED) return 0;
+    if (in.op == OP_LMHEAD) return 1 + 6 * m.L;
+    return 1 + 6 * in.layer + (in.op - OP_QKV);
+  };
+  if ((int)p.queues.size() != n_cta) return "queue count != CTA count";
+
+  // -- structure, argument ranges, scratch limits, signal counts
+  std::vector<uint32_t> sig(p.n_counters, 0);
+  std::vector<int> group_units(n_group, 0);
+  for (int c = 0; c < n_cta; ++c) {
+    const auto& q = p.queues[c];
+    if (q.empty() || q.back().op != OP_END) return fmt("queue %lld does not end with OP_END", c);
+    for (size_t k = 0; k + 1 < q.size(); ++k) {
+      const Instr& in = q[k];
+      if (in.op < OP_EMBED || in.op > OP_LMHEAD) return fmt("cta %lld pc %lld: bad opcode %lld", c, k, in.op);
+      if (in.op != OP_LMHEAD && in.layer >= m.L) return "layer out of range";
+      if (in.signal_ctr >= p.n_counters || in.wait_ctr >= p.n_counters) return "counter index out of range";
+      if (in.signal_ctr >= 0) sig[in.signal_ctr]++;
+      group_units[group_of(in)]++;
+      int rows = 0, K = 0, ws = 1;
+      switch (in.op) {
+        case OP_QKV: {
+          const int H = in.a[0] == 0 ? m.Hq : m.Hkv;
+          if (in.a[0] < 0 || in.a[0] > 2 || in.a[1] < 0 || in.a[1] >= H || in.a[2] < 0 || in.a[3] < 1 ||
+              in.a[2] + in.a[3] > half)
+            return fmt("cta %lld pc %lld: QKV arguments out of range", c, k);
+          rows = 2 * in.a[3];
+          K = m.d;
+          ws = g.ws_qkv;
+          break;
+        }
+        case OP_ATTN:
+          if (in.a[0] < 0 || in.a[0] >= B || in.a[1] < 0 || in.a[1] >= m.Hkv || in.a[3] != g.S || in.a[2] < 0 ||
+              in.a[2] >= g.S)
+            return fmt("cta %lld pc %lld: ATTENTION arguments out of range", c, k);
+          break;
+        case OP_ATTN_REDUCE:
+          if (in.a[0] < 0 || in.a[0] >= B || in.a[1] < 0 || in.a[1] >= m.Hkv) return "REDUCE arguments out of range";
+          break;
+        case OP_OPROJ: rows = in.a[1]; K = m.Hq * m.hd; ws = g.ws_o; break;
+        case OP_UPGATE: rows = 2 * in.a[1]; K = m.d; ws = g.ws_up; break;
+        case OP_DOWN: rows = in.a[1]; K = m.F; ws = g.ws_down; break;
+        case OP_LMHEAD: rows = in.a[1]; K = m.d; ws = g.ws_lm; break;
+        default: break;
+      }
+      if (K) {
+        if (rows < 1) return "empty GEMV instruction";
+        if ((long long)rows * (K / ws) * nb > scratch_floats)
+          return fmt("cta %lld pc %lld: GEMV row partials exceed the scratch (%lld floats)", c, k, scratch_floats);
+      }
+    }
+  }
+  for (int c = 0; c < n_cta; ++c)
+    for (const auto& in : p.queues[c]) {
+      if (in.wait_ctr >= 0 && in.wait_n != sig[in.wait_ctr])
+        return fmt("counter %lld: waiters expect %lld signals, the schedule gives %lld", in.wait_ctr, in.wait_n,
+                   sig[in.wait_ctr]);
+      if ((in.flags & F_LAST_LM) && (uint32_t)in.a[5] != sig[in.signal_ctr]) return "LM arrival count mismatch";
+    }
+
+  // -- simulation with counter semantics: every queue must reach OP_END
+  std::vector<size_t> pc(n_cta, 0);
+  std::vector<uint32_t> cnt(p.n_counters, 0);
+  // happens-before summary per executed instruction: groups fully done before it
+  std::vector<std::vector<Bits>> done(n_cta);
+  for (int c = 0; c < n_cta; ++c) done[c].assign(p.queues[c].size(), Bits(n_group));
+  std::vector<std::vector<std::pair<int, int>>> signalers(p.n_counters);
+  std::vector<int> ctr_group(p.n_counters, -1);
+  {
+    // a counter "covers" a group when exactly that group's units signal it
+    std::vector<int> sig_group(p.n_counters, -2);
+    for (int c = 0; c < n_cta; ++c)
+      for (const auto& in : p.queues[c])
+        if (in.signal_ctr >= 0 && !(in.flags & F_LAST_LM)) {
+          const int gr = group_of(in);
+          int& sg = sig_group[in.signal_ctr];
+          sg = (sg == -2 || sg == gr) ? gr : -1;
+        }
+    for (int k = 0; k < p.n_counters; ++k)
+      if (sig_group[k] >= 0 && (int)sig[k] == group_units[sig_group[k]]) ctr_group[k] = sig_group[k];
+  }
+  // required inputs (group ids) of each instruction
+  auto required = [&](const Instr& in, int* req) -> int {
+    const int l = in.layer;
+    const int h_writer = l == 0 ? 0 : 1 + 6 * (l - 1) + 5;
+    switch (in.op) {
+      case OP_QKV: req[0] = h_writer; return 1;
+      case OP_ATTN: req[0] = 1 + 6 * l + 0; return 1;
+      case OP_ATTN_REDUCE: req[0] = 1 + 6 * l + 1; return 1;
+      case OP_OPROJ: req[0] = 1 + 6 * l + 2; req[1] = h_writer; return 2;
+      case OP_UPGATE: req[0] = 1 + 6 * l + 3; return 1;
+      case OP_DOWN: req[0] = 1 + 6 * l + 4; req[1] = 1 + 6 * l + 3; return 2;
+      case OP_LMHEAD: req[0] = 1 + 6 * (m.L - 1) + 5; return 1;
+      default: return 0;
+    }
+  };
+  bool progress = true;
+  while (progress) {
+    progress = false;
+    for (int c = 0; c < n_cta; ++c) {
+      const auto& q = p.queues[c];
+      while (pc[c] < q.size() && q[pc[c]].op != OP_END) {
+        const Instr& in = q[pc[c]];
+        if (in.wait_ctr >= 0 && cnt[in.wait_ctr] < in.wait_n) break;
+        Bits f(n_group);
+        if (pc[c] > 0) f = done[c][pc[c] - 1];
+        if (in.wait_ctr >= 0) {
+          for (auto [sc, sp] : signalers[in.wait_ctr]) f.merge(done[sc][sp]);
+          if (ctr_group[in.wait_ctr] >= 0) f.set(ctr_group[in.wait_ctr]);
+        }
+        int req[2];
+        const int nr = required(in, req);
+        for (int r = 0; r < nr; ++r)
+          if (!f.has(req[r]))
+            return fmt("race: cta %lld pc %lld reads data of op group %lld not ordered before it", c, pc[c], req[r]);
+        done[c][pc[c]] = f;
+        if (in.signal_ctr >= 0) {
+          cnt[in.signal_ctr]++;
+          signalers[in.signal_ctr].push_back({c, (int)pc[c]});
+        }
+        pc[c]++;
+        progress = true;
+      }
+    }
+  }
+  for (int c = 0; c < n_cta; ++c)
+    if (p.queues[c][pc[c]].op != OP_END)
+      return fmt("deadlock: cta %lld blocks at pc %lld waiting on counter %lld", c, pc[c], p.queues[c][pc[c]].wait_ctr);
+
+  // -- coverage: every output element written exactly once
+  std::vector<int> emb((size_t)B * m.d, 0), lm(m.V, 0);
+  std::vector<std::vector<int>> qkv(m.L, std::vector<int>((size_t)(m.Hq + 2 * m.Hkv) * half, 0));
+  std::vector<std::vector<int>> att(m.L, std::vector<int>((size_t)B * m.Hkv * g.S, 0));
+  std::vector<std::vector<int>> red(m.L, std::vector<int>((size_t)B * m.Hkv, 0));
+  std::vector<std::vector<int>> orow(m.L, std::vector<int>(m.d, 0)), urow(m.L, std::vector<int>(m.F, 0)),
+      drow(m.L, std::vector<int>(m.d, 0));
+  auto mark = [&](std::vector<int>& v, long long a, long long n) -> bool {
+    if (a < 0 || a + n > (long long)v.size()) return false;
+    for (long long i = a; i < a + n; ++i) v[i]++;
+    return true;
+  };
+  for (int c = 0; c < n_cta; ++c)
+    for (const auto& in : p.queues[c]) {
+      bool ok = true;
+      const int l = in.layer;
+      switch (in.op) {
+        case OP_EMBED: ok = mark(emb, in.a[0], in.a[1] - in.a[0]); break;
+        case OP_QKV: {
+          const int hh = in.a[0] == 0 ? in.a[1] : (in.a[0] == 1 ? m.Hq + in.a[1] : m.Hq + m.Hkv + in.a[1]);
+          ok = mark(qkv[l], (long long)hh * half + in.a[2], in.a[3]);
+          break;
+        }
+        case OP_ATTN: ok = mark(att[l], ((long long)in.a[0] * m.Hkv + in.a[1]) * g.S + in.a[2], 1); break;
+        case OP_ATTN_REDUCE: ok = mark(red[l], (long long)in.a[0] * m.Hkv + in.a[1], 1); break;
+        case OP_OPROJ: ok = mark(orow[l], in.a[0], in.a[1]); break;
+        case OP_UPGATE: ok = mark(urow[l], in.a[0], in.a[1]); break;
+        case OP_DOWN: ok = mark(drow[l], in.a[0], in.a[1]); break;
+        case OP_LMHEAD: ok = mark(lm, in.a[0], in.a[1]); break;
+        default: break;
+      }
+      if (!ok) return fmt("cta %lld: output range out of bounds (op %lld)", c, in.op);
+    }
+  auto once = [](const std::vector<int>& v) {
+    return std::all_of(v.begin(), v.end(), [](int x) { return x == 1; });
+  };
+  if (!once(emb) || !once(lm)) return "embedding or LM-head rows not covered exactly once";
+  for (int l = 0; l < m.L; ++l)
+    if (!once(qkv[l]) || !once(att[l]) || !once(red[l]) || !once(orow[l]) || !once(urow[l]) || !once(drow[l]))
+      return fmt("layer %lld: an op's outputs are not covered exactly once", l);
+  return "";
+}
+
+}  // namespace mk

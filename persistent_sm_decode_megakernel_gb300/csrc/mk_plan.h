@@ -1,0 +1,48 @@
+// Host-side schedule: per-CTA instruction queues, counter wiring, tile geometry, and the
+// static validator that certifies a schedule before it is ever launched
+// ("8 · Écrire son megakernel", §8.7, static verification: no deadlock, no race).
+#pragma once
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "mk_internal.h"
+
+namespace mk {
+
+struct ModelShape {
+  int L, d, Hq, Hkv, hd, F, V, dtype, max_batch, max_ctx;
+  float eps, theta;
+};
+
+// tile and shared-memory geometry shared by every schedule of a context
+struct Geometry {
+  int page_bytes = 16384;
+  int n_pages = 0;
+  int nb_max = 1;        // batch padded to a power of two (register tiles)
+  int xbuf_bytes = 0;
+  int scratch_bytes = 0;
+  int smem_bytes = 0;
+  int ws_qkv = 0, ws_o = 0, ws_up = 0, ws_down = 0, ws_lm = 0;
+  int S = 1;             // kv splits per (sequence, kv head)
+};
+
+struct Plan {
+  int n_cta = 0;
+  int B = 1;
+  std::vector<std::vector<Instr>> queues;  // per CTA, END-terminated
+  std::vector<uint32_t> signals;          // per counter: signals per step
+  int n_counters = 0;
+  // multi-launch control: phases in dependency order; per phase the compacted queues
+  std::vector<std::vector<std::vector<Instr>>> phase_queues;
+  int64_t weight_bytes = 0;               // streamed weight bytes per step
+};
+
+// returns "" on success, else a message
+std::string make_geometry(const ModelShape& m, int n_cta, int page_bytes, int n_pages_req, int kv_splits,
+                          int smem_limit, Geometry* g);
+std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B, int drop_signal, Plan* p);
+std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p);
+
+}  // namespace mk
