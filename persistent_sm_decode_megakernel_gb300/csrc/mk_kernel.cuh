@@ -27,6 +27,7 @@ struct SmemCtl {
   float inv_rms[kMaxBatch];
   float red[kConsumerWarps * kMaxBatch];
   int last_issue_phase[kMaxPages];
+  uint64_t xbar;  // completion of the x-buffer bulk copy
   volatile int abort;
 };
 static_assert(sizeof(SmemCtl) <= kCtlSmem, "control block fits");
@@ -327,6 +328,7 @@ __device__ __noinline__ void producer(const DevState& S, const StepArgs& A, Smem
 struct Ring {
   int slot;
   uint32_t ph;
+  uint32_t xph;  // parity of the next x-buffer copy
 };
 
 __device__ __forceinline__ const uint8_t* page_wait(const DevState& S, SmemCtl* c, uint8_t* pages, const Ring& r) {
@@ -361,23 +363,63 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ---------------------------------------------------------------- x staging
-// RMSNorm recomputed in every CTA from the full residual vector (it is 8 KB per
-// sequence and L2-resident), result written to the x buffer as fp32.
+// The B rows of K fp32 activations ([B][K], contiguous, 128-byte aligned) reach the x
+// buffer through one TMA bulk copy issued by the thread that took the dependency
+// (acquire, then a proxy fence), so no compute-warp registers hold them in flight.
+// Padding rows up to NB are zeroed.  With NaN sentinels, elements the copy caught
+// before their producer wrote them are re-polled one by one.
+template <int SYNC, int NB>
+__device__ void stage_copy(const DevState& S, const float* src, int K, int B, float* xbuf, SmemCtl* c,
+                           Ring& ring) {
+  const int tid = threadIdx.x;
+  const uint32_t bytes = (uint32_t)B * (uint32_t)K * 4u;
+  if (tid == 0) {
+    fence_proxy_async();
+    mbar_arrive_expect_tx(&c->xbar, bytes);
+    tma_load_1d_plain(xbuf, src, bytes, &c->xbar);
+  }
+  float4* x4 = reinterpret_cast<float4*>(xbuf);
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = B * K / 4 + tid; i < NB * K / 4; i += kConsumerThreads) x4[i] = z;
+  if (!mbar_try_wait(&c->xbar, ring.xph)) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(&c->xbar, ring.xph)) {
+      if (globaltimer_ns() - t0 > (uint64_t)S.timeout_ns) {
+        set_err(S, 4u, -9, -1);
+        c->abort = 1;
+        break;
+      }
+    }
+  }
+  ring.xph ^= 1u;
+  if (SYNC == SYNC_SENTINEL) {
+    for (int i = tid; i < B * K; i += kConsumerThreads)
+      if (isnan(xbuf[i])) xbuf[i] = poll_slow(src + i, S, c);
+  }
+  consumer_sync();
+}
+
+// RMSNorm recomputed in every CTA from the full residual vector (8 KB per sequence,
+// L2-resident): stage it, sum squares per sequence in a fixed order, scale by the gain.
 template <typename WT, int SYNC, int NB>
 __device__ void stage_rmsnorm(const DevState& S, const float* h, const uint16_t* gain, int B, float* xbuf,
-                              SmemCtl* c) {
+                              SmemCtl* c, Ring& ring) {
   const int d = S.d, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  float ss[NB];
+  stage_copy<SYNC, NB>(S, h, d, B, xbuf, c, ring);
+  const float4* x4 = reinterpret_cast<const float4*>(xbuf);
+  const int d4 = d / 4;
 #pragma unroll
   for (int b = 0; b < NB; ++b) {
-    ss[b] = 0.f;
-    for (int k = tid; k < d; k += kConsumerThreads) {
-      const float v = (b < B) ? load_act<SYNC>(h + (size_t)b * d + k, S, c) : 0.f;
-      xbuf[b * d + k] = v;
-      ss[b] = fmaf(v, v, ss[b]);
+    float ss = 0.f;
+    for (int k = tid; k < d4; k += kConsumerThreads) {
+      const float4 v = x4[b * d4 + k];
+      ss = fmaf(v.x, v.x, ss);
+      ss = fmaf(v.y, v.y, ss);
+      ss = fmaf(v.z, v.z, ss);
+      ss = fmaf(v.w, v.w, ss);
     }
-    ss[b] = warp_sum(ss[b]);
-    if (lane == 0) c->red[warp * NB + b] = ss[b];
+    ss = warp_sum(ss);
+    if (lane == 0) c->red[warp * NB + b] = ss;
   }
   consumer_sync();
   if (tid < NB) {
@@ -386,18 +428,21 @@ __device__ void stage_rmsnorm(const DevState& S, const float* h, const uint16_t*
     c->inv_rms[tid] = 1.0f / sqrtf(t / (float)d + S.eps);
   }
   consumer_sync();
-  for (int k = tid; k < d; k += kConsumerThreads) {
-    const float gk = Unpack<WT>::one(__ldg(gain + k));
+  float4* w4 = reinterpret_cast<float4*>(xbuf);
+  for (int k = tid; k < d4; k += kConsumerThreads) {
+    const uint2 gb = __ldg(reinterpret_cast<const uint2*>(gain) + k);  // 4 gains
+    const float g0 = Unpack<WT>::one((uint16_t)(gb.x & 0xFFFFu)), g1 = Unpack<WT>::one((uint16_t)(gb.x >> 16));
+    const float g2 = Unpack<WT>::one((uint16_t)(gb.y & 0xFFFFu)), g3 = Unpack<WT>::one((uint16_t)(gb.y >> 16));
 #pragma unroll
-    for (int b = 0; b < NB; ++b) xbuf[b * d + k] *= c->inv_rms[b] * gk;
-  }
-}
-
-template <int SYNC, int NB>
-__device__ void stage_copy(const DevState& S, const float* src, int K, int B, float* xbuf, SmemCtl* c) {
-  for (int t = threadIdx.x; t < NB * K; t += kConsumerThreads) {
-    const int b = t / K;
-    xbuf[t] = (b < B) ? load_act<SYNC>(src + t, S, c) : 0.f;
+    for (int b = 0; b < NB; ++b) {
+      const float r = c->inv_rms[b];
+      float4 v = w4[b * d4 + k];
+      v.x *= r * g0;
+      v.y *= r * g1;
+      v.z *= r * g2;
+      v.w *= r * g3;
+      w4[b * d4 + k] = v;
+    }
   }
 }
 
@@ -444,19 +489,19 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
   // 1. inputs
   switch (in.op) {
     case OP_QKV:
-      stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_H, l), S.attn_norm[l], B, xbuf, c);
+      stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_H, l), S.attn_norm[l], B, xbuf, c, ring);
       break;
     case OP_UPGATE:
-      stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_HMID, l), S.mlp_norm[l], B, xbuf, c);
+      stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_HMID, l), S.mlp_norm[l], B, xbuf, c, ring);
       break;
     case OP_LMHEAD:
-      stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_H, S.L), S.final_norm, B, xbuf, c);
+      stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_H, S.L), S.final_norm, B, xbuf, c, ring);
       break;
     case OP_OPROJ:
-      stage_copy<SYNC, NB>(S, act_ptr(S, act, ACT_O, l), g.K, B, xbuf, c);
+      stage_copy<SYNC, NB>(S, act_ptr(S, act, ACT_O, l), g.K, B, xbuf, c, ring);
       break;
     default:  // OP_DOWN
-      stage_copy<SYNC, NB>(S, act_ptr(S, act, ACT_A, l), g.K, B, xbuf, c);
+      stage_copy<SYNC, NB>(S, act_ptr(S, act, ACT_A, l), g.K, B, xbuf, c, ring);
       break;
   }
   consumer_sync();
@@ -779,17 +824,32 @@ __device__ __noinline__ void op_attn_reduce(const DevState& S, const Instr& in, 
   }
   consumer_sync();
   float* out = act_ptr(S, act, ACT_O, l) + (size_t)b * S.Hq * HD + (size_t)j * G * HD;
+  constexpr int U = 8;  // splits whose partial outputs are in flight together
   for (int t = tid; t < G * HD; t += kConsumerThreads) {
     const int g = t / HD, e = t - g * HD;
     float M = -CUDART_INF_F;
     for (int s = 0; s < NS; ++s) M = fmaxf(M, scratch[2 * (s * G + g)]);
     float num = 0.f, den = 0.f;
-    for (int s = 0; s < NS; ++s) {
-      const float ms = scratch[2 * (s * G + g)];
-      if (ms == -CUDART_INF_F) continue;
-      const float w = exp2f(ms - M);
-      num = fmaf(w, load_act<SYNC>(part + (size_t)(s * G + g) * RW + e, S, c), num);
-      den = fmaf(w, scratch[2 * (s * G + g) + 1], den);
+    for (int s0 = 0; s0 < NS; s0 += U) {
+      float v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int s = min(s0 + u, NS - 1);  // clamped: always a valid address
+        const float* p = part + (size_t)(s * G + g) * RW + e;
+        v[u] = (SYNC == SYNC_COUNTER) ? __ldcg(p) : ld_poll_f32(p);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int s = s0 + u;
+        const float ms = s < NS ? scratch[2 * (s * G + g)] : -CUDART_INF_F;
+        if (ms != -CUDART_INF_F) {
+          float ov = v[u];
+          if (SYNC == SYNC_SENTINEL && isnan(ov)) ov = poll_slow(part + (size_t)(s * G + g) * RW + e, S, c);
+          const float w = exp2f(ms - M);
+          num = fmaf(w, ov, num);
+          den = fmaf(w, scratch[2 * (s * G + g) + 1], den);
+        }
+      }
     }
     out[t] = num / den;
   }
@@ -846,7 +906,7 @@ __device__ void consumer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8
   float* act = S.act + (int64_t)par * S.act_floats;
   const int nb = A.B <= 1 ? 1 : A.B <= 2 ? 2 : A.B <= 4 ? 4 : A.B <= 8 ? 8 : 16;
   const int G = S.Hq / S.Hkv;
-  Ring ring{0, 0u};
+  Ring ring{0, 0u, 0u};
   int order_n = 0;
   const int end = A.q_start[cta + 1];
   for (int pc = A.q_start[cta]; pc < end; ++pc) {
@@ -974,6 +1034,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
   SmemCtl* c = reinterpret_cast<SmemCtl*>(reinterpret_cast<uint8_t*>(scratch) + S.scratch_bytes);
   const int tid = threadIdx.x;
   if (tid == 0) {
+    mbar_init(&c->xbar, 1);
     for (int i = 0; i < S.n_pages; ++i) {
       mbar_init(&c->full[i], 1);
       mbar_init(&c->empty[i], kConsumerWarps);

@@ -1,0 +1,110 @@
+"""Run a few decode steps of a workload for timing, tracing or an ncu capture.
+
+    python -m persistent_sm_decode_megakernel_gb300.profile_step --workload 2b \
+        [--layers L] [--prompt P] [--steps N] [--batch B] [--trace] [--sync counter|sentinel]
+        [--exec persistent|multilaunch] [--page-bytes X] [--n-pages N] [--backoff NS]
+
+Prints the per-step time (CUDA events on the context stream) and, with --trace, a
+summary of the last step's instruction journal: per op, the mean time from fetch to
+dependency-satisfied (waiting) and from there to the end (working), the per-CTA
+waiting share of the step, and the first op groups' start/end on the step's timeline.
+The decode steps are preceded by exactly `prompt` launches of the same kernel (one per
+prompt position), which is the count an ncu capture skips with -s.
+"""
+import argparse
+import json
+import os
+import statistics
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+OPS = {1: "embed", 2: "qkv", 3: "attn", 4: "reduce", 5: "oproj", 6: "upgate", 7: "down", 8: "lmhead"}
+
+
+def summarize(trace):
+    t0 = min(r[4] for r in trace)
+    t1 = max(r[6] for r in trace)
+    span = (t1 - t0) / 1e3
+    ctas = {r[0] for r in trace}
+    by = {}
+    per_cta_wait = {}
+    groups = {}
+    for cta, pc, op, layer, tf, tr, te in trace:
+        d = by.setdefault(OPS.get(op, str(op)), {"wait": [], "work": []})
+        d["wait"].append((tr - tf) / 1e3)
+        d["work"].append((te - tr) / 1e3)
+        per_cta_wait[cta] = per_cta_wait.get(cta, 0.0) + (tr - tf) / 1e3
+        g = groups.setdefault((layer, op), [tf, te])
+        g[0] = min(g[0], tf)
+        g[1] = max(g[1], te)
+    out = {"span_us": span, "ops": {}}
+    for k, d in by.items():
+        out["ops"][k] = {"n": len(d["work"]), "wait_us_mean": statistics.mean(d["wait"]),
+                         "work_us_mean": statistics.mean(d["work"]), "work_us_max": max(d["work"]),
+                         "wait_us_per_cta": sum(d["wait"]) / len(ctas)}
+    out["wait_share_mean"] = statistics.mean(v / span for v in per_cta_wait.values())
+    items = sorted(groups.items(), key=lambda kv: kv[1][0])
+    out["timeline_us"] = {f"L{l}:{OPS.get(o, o)}": [round((a - t0) / 1e3, 2), round((b - t0) / 1e3, 2)]
+                          for (l, o), (a, b) in items[:20]}
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="2b")
+    ap.add_argument("--layers", type=int, default=0)
+    ap.add_argument("--prompt", type=int, default=32)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--trace", action="store_true")
+    ap.add_argument("--sync", default="counter", choices=["counter", "sentinel"])
+    ap.add_argument("--exec", default="persistent", choices=["persistent", "multilaunch"])
+    ap.add_argument("--page-bytes", type=int, default=0)
+    ap.add_argument("--n-pages", type=int, default=0)
+    ap.add_argument("--backoff", type=int, default=0)
+    ap.add_argument("--json", default="")
+    args = ap.parse_args()
+
+    import torch
+
+    import synth
+    from persistent_sm_decode_megakernel_gb300.model import Decoder, DeviceModel
+
+    cfg = synth.CONFIGS[args.workload]
+    if args.layers:
+        cfg = synth.with_overrides(cfg, n_layers=args.layers)
+    w = synth.gen_weights(cfg)
+    B = args.batch
+    dm = DeviceModel(cfg, w, max_batch=B, max_ctx=args.prompt + args.steps + 2)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        dec = Decoder(dm, sync_mode=0 if args.sync == "counter" else 1,
+                      exec_mode=0 if args.exec == "persistent" else 1, trace=1 if args.trace else 0,
+                      page_bytes=args.page_bytes, n_pages=args.n_pages, backoff_max_ns=args.backoff, stream=stream)
+        prompt = synth.gen_prompts(cfg, B, args.prompt)
+        tok = dec.prefill(prompt)
+        pos = args.prompt
+        times = []
+        for _ in range(args.steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            tok = dec.decode_step(tok, [pos] * B)
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3)
+            pos += 1
+        res = {"workload": args.workload, "layers": cfg.n_layers, "step_us": times, "info": dec.info()}
+        if args.trace:
+            res["trace"] = summarize(dec.trace())
+        dec.close()
+    print(json.dumps(res, indent=1))
+    if args.json:
+        with open(args.json, "w") as f:
+            json.dump(res, f, indent=1)
+
+
+if __name__ == "__main__":
+    main()
