@@ -108,12 +108,6 @@ struct Gemv {
   __device__ __forceinline__ int rows() const { return segr[0] + segr[1]; }
   __device__ __forceinline__ int spr() const { return K / WS; }
   __device__ __forceinline__ int nslices() const { return rows() * spr(); }
-  __device__ __forceinline__ const uint16_t* src(int i) const {
-    const int s = spr();
-    const int r = i / s, c = i - r * s;
-    const uint16_t* base = r < segr[0] ? seg[0] + (size_t)r * K : seg[1] + (size_t)(r - segr[0]) * K;
-    return base + (size_t)c * WS;
-  }
 };
 
 __device__ __forceinline__ Gemv make_gemv(const DevState& S, const Instr& in) {
@@ -240,6 +234,9 @@ __device__ __noinline__ void producer(const DevState& S, const StepArgs& A, Smem
         const Gemv g = make_gemv(S, in);
         const int ns = g.nslices();
         const uint32_t sb = (uint32_t)g.WS * 2u;
+        // rows of a segment are contiguous and a row is spr slices, so slice j of
+        // segment k starts at seg[k] + j * WS: a page is at most two bulk copies
+        const int n0 = g.segr[0] * g.spr();
         for (int i0 = 0; i0 < ns; i0 += kConsumerWarps) {
           if (!producer_acquire(S, c, slot, ph)) {
             ok = false;
@@ -248,13 +245,14 @@ __device__ __noinline__ void producer(const DevState& S, const StepArgs& A, Smem
           const int i1 = min(ns, i0 + kConsumerWarps);
           mbar_arrive_expect_tx(&c->full[slot], (uint32_t)(i1 - i0) * sb);
           uint8_t* dst = pages + (size_t)slot * S.page_bytes;
-          int i = i0;
-          while (i < i1) {  // one bulk copy per contiguous run of slices
-            const uint16_t* src = g.src(i);
-            int j = i + 1;
-            while (j < i1 && g.src(j) == src + (size_t)(j - i) * g.WS) ++j;
-            tma_load_1d(dst + (size_t)(i - i0) * sb, src, (uint32_t)(j - i) * sb, &c->full[slot], pol);
-            i = j;
+          if (i0 < n0) {
+            const int e = min(i1, n0);
+            tma_load_1d(dst, g.seg[0] + (size_t)i0 * g.WS, (uint32_t)(e - i0) * sb, &c->full[slot], pol);
+          }
+          if (i1 > n0) {
+            const int b0 = max(i0, n0);
+            tma_load_1d(dst + (size_t)(b0 - i0) * sb, g.seg[1] + (size_t)(b0 - n0) * g.WS, (uint32_t)(i1 - b0) * sb,
+                        &c->full[slot], pol);
           }
           c->last_issue_phase[slot] = (int)ph;
           if (++slot == S.n_pages) { slot = 0; ph ^= 1u; }
