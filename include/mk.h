@@ -187,6 +187,23 @@ mk_status mk_selftest(int kind, int64_t *result, int n);
  * *us_per_barrier receives the mean latency in microseconds. */
 mk_status mk_barrier_bench(int mode, int n_barriers, double *us_per_barrier);
 
+/* One decode step that allocates no device memory, for callers that cannot call
+ * cudaMalloc (code running inside an allocator or under a host framework that owns every
+ * device allocation).  The pages have no counterpart to this entry point.  Same inputs
+ * and outputs as mk_decode_step, passed directly (no context): desc, weights and kv as
+ * for mk_create; in_tok, pos, out_tok host [B]; logits device [B, vocab] or NULL; work is
+ * enqueued on `stream` (a cudaStream_t) and the call returns after it completes.
+ * Every other buffer the step needs (queues, counters, activations, RoPE rows up to the
+ * largest position) lives in one 16 MiB device array built into the library, which each
+ * GPU that loads it holds until exit; models that need more are refused with
+ * MK_ERR_INVALID.  The first call on a device (with that device current) looks the array
+ * up with cudaGetSymbolAddress: make it before any stream capture.  All calls share the
+ * array and keep its last contents; each call clears what must start at zero.  Calls
+ * whose GPU work overlaps race on the array and must be serialised by the caller. */
+mk_status mk_decode_step_noalloc(const mk_model_desc *desc, const mk_weights *weights, const mk_kv *kv,
+                                 const int32_t *in_tok, const int32_t *pos, int B, int32_t *out_tok,
+                                 float *logits, void *stream);
+
 const char *mk_last_error(void);
 const char *mk_status_string(mk_status s);
 

@@ -85,6 +85,9 @@ mk_plan = _fn("mk_plan", [ctypes.POINTER(mk_model_desc), ctypes.POINTER(mk_optio
                           ctypes.POINTER(mk_info_t)])
 mk_selftest = _fn("mk_selftest", [c_int, ctypes.POINTER(ctypes.c_int64), c_int])
 mk_barrier_bench = _fn("mk_barrier_bench", [c_int, c_int, ctypes.POINTER(c_double)])
+mk_decode_step_noalloc = _fn("mk_decode_step_noalloc", [ctypes.POINTER(mk_model_desc), ctypes.POINTER(mk_weights),
+                                                        ctypes.POINTER(mk_kv), P_i32, P_i32, c_int, P_i32, c_void_p,
+                                                        c_void_p])
 mk_last_error = _fn("mk_last_error", [], ctypes.c_char_p)
 mk_status_string = _fn("mk_status_string", [c_int], ctypes.c_char_p)
 

@@ -54,6 +54,11 @@ struct Sched {
 
 }  // namespace
 
+namespace mk {
+// lets the other translation units of the library report through mk_last_error
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+}  // namespace mk
+
 struct mk_ctx {
   ModelShape m{};
   mk_options opts{};

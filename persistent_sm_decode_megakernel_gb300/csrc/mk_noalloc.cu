@@ -1,0 +1,284 @@
+// mk_decode_step_noalloc: one decode step for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc: code running inside an allocator that must not
+// re-enter it, plugins whose host process owns every device allocation and forbids
+// their own, or a process whose memory is fully pre-reserved by another framework's
+// caching allocator.  mk_create needs device memory for its queues, counters and
+// activation buffers, so those callers get this entry point instead: every buffer the
+// step needs beyond the caller's own inputs and outputs lives in one file-scope device
+// array of kScratchBytes, which each GPU that loads the library holds until the process
+// exits.  The step kernel is the same persistent kernel mk_decode_step launches (counter
+// synchronisation); only where its scratch lives differs.
+//
+// Rules of use:
+//   * The first call on a device (with that device current) looks up the array's device
+//     address with cudaGetSymbolAddress; make that first call before any stream capture.
+//   * All calls share the one array and leave their contents in it; every call clears
+//     what must start at zero (counters, error word, argmax keys).  Calls whose GPU work
+//     overlaps (two streams, two host threads) race on the array: serialise them.
+//   * Models whose queues + activations + RoPE table exceed kScratchBytes are refused
+//     with MK_ERR_INVALID and a message giving both sizes.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/mk.h"
+#include "mk_internal.h"
+#include "mk_kernels.h"
+#include "mk_plan.h"
+
+namespace mk {
+void set_last_error(const std::string& msg);  // defined beside mk_last_error
+}
+
+namespace {
+
+constexpr size_t kScratchBytes = 16u << 20;  // 16 MiB per device
+constexpr int kMaxDevices = 64;
+
+// The scratch.  In host code this name is only a stand-in for the device symbol: its
+// device address comes from cudaGetSymbolAddress below, never from taking its address.
+static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
+
+std::mutex g_mu;
+void* g_scratch_dev[kMaxDevices] = {};
+
+mk_status fail(mk_status s, const std::string& m) {
+  mk::set_last_error(m);
+  return s;
+}
+
+#define NA_CUDA(call)                                                                    \
+  do {                                                                                   \
+    cudaError_t e_ = (call);                                                             \
+    if (e_ != cudaSuccess) return fail(MK_ERR_CUDA, std::string(#call) + ": " + cudaGetErrorString(e_)); \
+  } while (0)
+
+mk_status scratch_address(int dev, unsigned char** out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (dev < 0 || dev >= kMaxDevices) return fail(MK_ERR_INVALID, "device index out of range");
+  if (!g_scratch_dev[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(MK_ERR_CUDA, std::string("cudaGetSymbolAddress(scratch): ") + cudaGetErrorString(e));
+    g_scratch_dev[dev] = p;
+  }
+  *out = static_cast<unsigned char*>(g_scratch_dev[dev]);
+  return MK_OK;
+}
+
+bool al16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+extern "C" mk_status mk_decode_step_noalloc(const mk_model_desc* desc, const mk_weights* w, const mk_kv* kv,
+                                            const int32_t* in_tok, const int32_t* pos, int B, int32_t* out_tok,
+                                            float* logits, void* stream) {
+  using namespace mk;
+  if (!desc || !w || !kv || !in_tok || !pos || !out_tok) return fail(MK_ERR_INVALID, "NULL argument");
+  const mk_model_desc& d = *desc;
+  if (d.n_layers < 1 || d.d_model < 8 || d.n_heads < 1 || d.n_kv_heads < 1 || d.head_dim < 8 || d.ffn_dim < 8 ||
+      d.vocab < 2 || d.n_heads % d.n_kv_heads || (d.dtype != MK_F16 && d.dtype != MK_BF16) || d.max_batch < 1 ||
+      d.max_batch > kMaxBatch || d.max_ctx < 1 || d.d_model % 8 || d.ffn_dim % 8 || !(d.rms_eps > 0.f) ||
+      !(d.rope_theta > 0.f))
+    return fail(MK_ERR_INVALID, "invalid model descriptor");
+  if (B < 1 || B > d.max_batch) return fail(MK_ERR_INVALID, "B out of range");
+  for (int b = 0; b < B; ++b) {
+    if (in_tok[b] < 0 || in_tok[b] >= d.vocab) return fail(MK_ERR_INVALID, "token id out of range");
+    if (pos[b] < 0 || pos[b] >= d.max_ctx) return fail(MK_ERR_INVALID, "position out of range");
+  }
+  const int L = d.n_layers;
+  if (!al16(w->embed) || !al16(w->final_norm) || !al16(w->lm_head) || !kv->k_cache || !kv->v_cache)
+    return fail(MK_ERR_INVALID, "weight/KV pointers must be non-NULL and 16-byte aligned");
+  const void* const* tabs[9] = {w->attn_norm, w->wq, w->wk, w->wv, w->wo, w->mlp_norm, w->w_gate, w->w_up, w->w_down};
+  for (auto t : tabs) {
+    if (!t) return fail(MK_ERR_INVALID, "a per-layer weight table is NULL");
+    for (int l = 0; l < L; ++l)
+      if (!al16(t[l])) return fail(MK_ERR_INVALID, "weight pointers must be 16-byte aligned");
+  }
+  for (int l = 0; l < L; ++l)
+    if (!al16(kv->k_cache[l]) || !al16(kv->v_cache[l])) return fail(MK_ERR_INVALID, "KV pointers must be aligned");
+
+  ModelShape m;
+  m.L = L; m.d = d.d_model; m.Hq = d.n_heads; m.Hkv = d.n_kv_heads; m.hd = d.head_dim; m.F = d.ffn_dim;
+  m.V = d.vocab; m.dtype = d.dtype; m.max_batch = d.max_batch; m.max_ctx = d.max_ctx; m.eps = d.rms_eps;
+  m.theta = d.rope_theta;
+
+  // grid: one wave, as for mk_create
+  int dev = 0, n_sm = 0, smem_optin = 0, bpsm = 0;
+  NA_CUDA(cudaGetDevice(&dev));
+  unsigned char* base = nullptr;
+  mk_status st = scratch_address(dev, &base);
+  if (st) return st;
+  NA_CUDA(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
+  NA_CUDA(cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+  Geometry g;
+  std::string e = make_geometry(m, n_sm, 0, 0, 0, smem_optin, &g);
+  if (!e.empty()) return fail(MK_ERR_INVALID, e);
+  const void* fn = step_kernel_entry(m.dtype, MK_SYNC_COUNTER, false);
+  NA_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_bytes));
+  NA_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bpsm, fn, kThreads, g.smem_bytes));
+  if (bpsm < 1) return fail(MK_ERR_OCCUPANCY, "the kernel does not fit on an SM");
+  const int n_cta = n_sm * bpsm;
+  if (n_cta != n_sm) {
+    e = make_geometry(m, n_cta, 0, 0, 0, smem_optin, &g);
+    if (!e.empty()) return fail(MK_ERR_INVALID, e);
+  }
+  Plan plan;
+  e = build_plan(m, g, n_cta, B, 0, &plan);
+  if (!e.empty()) return fail(MK_ERR_INVALID, "schedule: " + e);
+  e = validate_plan(m, g, plan);
+  if (!e.empty()) return fail(MK_ERR_INVALID, "schedule rejected by the validator: " + e);
+
+  // host images of the read-only tables
+  std::vector<Instr> flat;
+  std::vector<int32_t> qoff;
+  for (const auto& q : plan.queues) {
+    qoff.push_back((int32_t)flat.size());
+    flat.insert(flat.end(), q.begin(), q.end());
+  }
+  qoff.push_back((int32_t)flat.size());
+  std::vector<const void*> ptrs;
+  for (auto t : tabs)
+    for (int l = 0; l < L; ++l) ptrs.push_back(t[l]);
+  for (int l = 0; l < L; ++l) ptrs.push_back(kv->k_cache[l]);
+  for (int l = 0; l < L; ++l) ptrs.push_back(kv->v_cache[l]);
+  int max_pos = 0;
+  for (int b = 0; b < B; ++b) max_pos = pos[b] > max_pos ? pos[b] : max_pos;
+  const int half = m.hd / 2, rope_rows = max_pos + 1;
+  std::vector<float> rope((size_t)rope_rows * half * 2);
+  for (int i = 0; i < half; ++i) {
+    const double f = std::pow((double)m.theta, -2.0 * i / m.hd);
+    for (int t = 0; t < rope_rows; ++t) {
+      rope[((size_t)t * half + i) * 2] = (float)std::cos((double)t * f);
+      rope[((size_t)t * half + i) * 2 + 1] = (float)std::sin((double)t * f);
+    }
+  }
+
+  // activation arena (one set: counter synchronisation needs no second parity)
+  DevState S{};
+  const int G = m.Hq / m.Hkv;
+  long long sizes[ACT_NUM], layers[ACT_NUM];
+  sizes[ACT_H] = (long long)B * m.d; layers[ACT_H] = L + 1;
+  sizes[ACT_HMID] = (long long)B * m.d; layers[ACT_HMID] = L;
+  sizes[ACT_Q] = (long long)B * m.Hq * m.hd; layers[ACT_Q] = L;
+  sizes[ACT_KVN] = (long long)B * 2 * m.Hkv * m.hd; layers[ACT_KVN] = L;
+  sizes[ACT_PART] = (long long)B * m.Hkv * g.S * G * (m.hd + 2); layers[ACT_PART] = L;
+  sizes[ACT_O] = (long long)B * m.Hq * m.hd; layers[ACT_O] = L;
+  sizes[ACT_A] = (long long)B * m.F; layers[ACT_A] = L;
+  long long off = 0;
+  for (int k = 0; k < ACT_NUM; ++k) {
+    const long long stride = (sizes[k] + 31) / 32 * 32;
+    S.act_off[k] = off;
+    S.act_stride[k] = stride;
+    off += stride * layers[k];
+  }
+  S.act_floats = (off + 31) / 32 * 32;
+
+  // carve the scratch
+  size_t cur = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = cur;
+    cur = up256(cur + bytes);
+    return at;
+  };
+  const size_t o_ctl = take(sizeof(Ctl));
+  const size_t o_keys = take(sizeof(unsigned long long) * 2 * kMaxBatch);
+  const size_t o_ctr = take(sizeof(uint32_t) * (size_t)plan.n_counters);
+  const size_t o_ptr = take(sizeof(void*) * ptrs.size());
+  const size_t o_rope = take(sizeof(float) * rope.size());
+  const size_t o_q = take(sizeof(int32_t) * qoff.size());
+  const size_t o_ins = take(sizeof(Instr) * flat.size());
+  const size_t o_act = take(sizeof(float) * (size_t)S.act_floats);
+  if (cur > kScratchBytes) {
+    char buf[200];
+    snprintf(buf, sizeof buf, "this model and batch need %zu bytes of scratch; the no-alloc entry holds %zu", cur,
+             kScratchBytes);
+    return fail(MK_ERR_INVALID, buf);
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // inputs of this call (the array still holds the previous call's contents)
+  NA_CUDA(cudaMemsetAsync(base + o_ctl, 0, sizeof(Ctl), s));
+  NA_CUDA(cudaMemsetAsync(base + o_keys, 0, sizeof(unsigned long long) * 2 * kMaxBatch, s));
+  NA_CUDA(cudaMemsetAsync(base + o_ctr, 0, sizeof(uint32_t) * (size_t)plan.n_counters, s));
+  NA_CUDA(cudaMemcpyAsync(base + o_ptr, ptrs.data(), sizeof(void*) * ptrs.size(), cudaMemcpyHostToDevice, s));
+  NA_CUDA(cudaMemcpyAsync(base + o_rope, rope.data(), sizeof(float) * rope.size(), cudaMemcpyHostToDevice, s));
+  NA_CUDA(cudaMemcpyAsync(base + o_q, qoff.data(), sizeof(int32_t) * qoff.size(), cudaMemcpyHostToDevice, s));
+  NA_CUDA(cudaMemcpyAsync(base + o_ins, flat.data(), sizeof(Instr) * flat.size(), cudaMemcpyHostToDevice, s));
+
+  S.L = L; S.d = m.d; S.Hq = m.Hq; S.Hkv = m.Hkv; S.hd = m.hd; S.F = m.F; S.V = m.V; S.dtype = m.dtype;
+  S.max_batch = B;  // the arena holds B rows
+  S.max_ctx = m.max_ctx; S.S = g.S; S.eps = m.eps;
+  S.ws_qkv = g.ws_qkv; S.ws_o = g.ws_o; S.ws_up = g.ws_up; S.ws_down = g.ws_down; S.ws_lm = g.ws_lm;
+  S.embed = static_cast<const uint16_t*>(w->embed);
+  S.final_norm = static_cast<const uint16_t*>(w->final_norm);
+  S.lm_head = static_cast<const uint16_t*>(w->lm_head);
+  auto pt = reinterpret_cast<const uint16_t* const*>(base + o_ptr);
+  auto mpt = reinterpret_cast<uint16_t* const*>(base + o_ptr);
+  S.attn_norm = pt; S.wq = pt + L; S.wk = pt + 2 * L; S.wv = pt + 3 * L; S.wo = pt + 4 * L;
+  S.mlp_norm = pt + 5 * L; S.w_gate = pt + 6 * L; S.w_up = pt + 7 * L; S.w_down = pt + 8 * L;
+  S.kcache = mpt + 9 * L;
+  S.vcache = mpt + 10 * L;
+  S.rope = reinterpret_cast<const float2*>(base + o_rope);
+  S.act = reinterpret_cast<float*>(base + o_act);
+  S.argkeys = reinterpret_cast<unsigned long long*>(base + o_keys);
+  S.counters = reinterpret_cast<uint32_t*>(base + o_ctr);
+  S.n_counters = plan.n_counters;
+  S.ctl = reinterpret_cast<Ctl*>(base + o_ctl);
+  S.n_cta = n_cta;
+  S.page_bytes = g.page_bytes;
+  S.n_pages = g.n_pages;
+  S.xbuf_bytes = g.xbuf_bytes;
+  S.scratch_bytes = g.scratch_bytes;
+  S.sync_mode = MK_SYNC_COUNTER;
+  S.timeout_ns = 2000000000LL;
+  S.backoff_max_ns = 256;
+  // the kernel's kv-cache addressing uses the caller's layout [max_batch, Hkv, max_ctx, hd]
+  // only through max_ctx, and its activation rows through max_batch: both as set above
+  StepArgs A{};
+  A.instr = reinterpret_cast<const Instr*>(base + o_ins);
+  A.q_start = reinterpret_cast<const int32_t*>(base + o_q);
+  A.epoch = 0;
+  A.step = 0;
+  A.B = B;
+  A.flags = SF_RESET_ARGMAX;
+  for (int b = 0; b < B; ++b) {
+    A.tok[b] = in_tok[b];
+    A.pos[b] = pos[b];
+  }
+  A.logits = logits;
+  A.tok_hist = nullptr;
+
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(n_cta);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = g.smem_bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[2] = {&S, &A};
+  NA_CUDA(cudaLaunchKernelExC(&cfg, fn, args));
+  Ctl hc;
+  NA_CUDA(cudaMemcpyAsync(&hc, base + o_ctl, sizeof(Ctl), cudaMemcpyDeviceToHost, s));
+  NA_CUDA(cudaStreamSynchronize(s));
+  if (hc.err.code) {
+    char buf[160];
+    snprintf(buf, sizeof buf, "device error %u at cta %d pc %d counter %d", hc.err.code, hc.err.cta, hc.err.pc,
+             hc.err.ctr);
+    return fail((mk_status)hc.err.code, buf);
+  }
+  for (int b = 0; b < B; ++b) out_tok[b] = hc.tok[b];
+  if (hc.nan_seen) return fail(MK_ERR_NAN, "a logit was NaN");
+  return MK_OK;
+}
