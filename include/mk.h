@@ -204,6 +204,14 @@ mk_status mk_decode_step_noalloc(const mk_model_desc *desc, const mk_weights *we
                                  const int32_t *in_tok, const int32_t *pos, int B, int32_t *out_tok,
                                  float *logits, void *stream);
 
+/* HBM page-stream microbenchmark: the megakernel's loader / compute-warp structure with
+ * nothing else (P1 §7.5 continuous weight streaming, P2 §8.4 pages).  One CTA per SM
+ * streams total_bytes / #SM of contiguous device memory through n_pages TMA pages of
+ * page_bytes; mode 0: pages are released unread, mode 1: each compute warp first runs
+ * the fp16 GEMV slice product on its eighth; hint 1: L2 evict-first policy.  *gbps gets
+ * the best of three timed runs.  Allocates total_bytes of device memory for the run. */
+mk_status mk_stream_bench(int page_bytes, int n_pages, int mode, int hint, long long total_bytes, double *gbps);
+
 const char *mk_last_error(void);
 const char *mk_status_string(mk_status s);
 

@@ -136,6 +136,14 @@ struct Unpack<__half> {
       f[2 * i + 1] = t.y;
     }
   }
+  __device__ __forceinline__ static void u4(const uint2& v, float (&f)[4]) {
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+    f[0] = a.x;
+    f[1] = a.y;
+    f[2] = b.x;
+    f[3] = b.y;
+  }
   __device__ __forceinline__ static float one(uint16_t b) { return __half2float(__ushort_as_half(b)); }
   __device__ __forceinline__ static uint16_t round(float x) { return __half_as_ushort(__float2half_rn(x)); }
 };
@@ -148,6 +156,12 @@ struct Unpack<__nv_bfloat16> {
       f[2 * i] = __uint_as_float(w[i] << 16);
       f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
     }
+  }
+  __device__ __forceinline__ static void u4(const uint2& v, float (&f)[4]) {
+    f[0] = __uint_as_float(v.x << 16);
+    f[1] = __uint_as_float(v.x & 0xFFFF0000u);
+    f[2] = __uint_as_float(v.y << 16);
+    f[3] = __uint_as_float(v.y & 0xFFFF0000u);
   }
   __device__ __forceinline__ static float one(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
   __device__ __forceinline__ static uint16_t round(float x) {

@@ -823,4 +823,46 @@ mk_status mk_barrier_bench(int mode, int n_barriers, double* us_per_barrier) {
   return MK_OK;
 }
 
+mk_status mk_stream_bench(int page_bytes, int n_pages, int mode, int hint, long long total_bytes, double* gbps) {
+  if (!gbps || page_bytes < 1024 || page_bytes > 65536 || (page_bytes & 15) || n_pages < 1 || n_pages > kMaxPages ||
+      (mode != 0 && mode != 1) || total_bytes < (1LL << 20))
+    return fail(MK_ERR_INVALID, "stream bench: bad arguments");
+  int dev = 0, n_sm = 0;
+  MK_CUDA(cudaGetDevice(&dev));
+  MK_CUDA(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
+  const long long per_cta = total_bytes / n_sm / page_bytes * page_bytes;
+  const int smem = n_pages * page_bytes + (page_bytes / 16) * 4;
+  const void* fn = stream_kernel_entry();
+  MK_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+  DevBuf src, sink;
+  MK_CUDA(cudaMalloc(&src.p, (size_t)per_cta * n_sm));
+  MK_CUDA(cudaMemset(src.p, 0x3C, (size_t)per_cta * n_sm));
+  MK_CUDA(cudaMalloc(&sink.p, sizeof(float) * n_sm * kConsumerWarps));
+  const uint8_t* sp = reinterpret_cast<const uint8_t*>(src.p);
+  float* sk = reinterpret_cast<float*>(sink.p);
+  long long pc = per_cta;
+  void* args[7] = {&sp, &pc, &page_bytes, &n_pages, &mode, &hint, &sk};
+  cudaEvent_t e0, e1;
+  MK_CUDA(cudaEventCreate(&e0));
+  MK_CUDA(cudaEventCreate(&e1));
+  float best = 1e30f;
+  for (int it = 0; it < 4; ++it) {
+    MK_CUDA(cudaEventRecord(e0, nullptr));
+    MK_CUDA(cudaLaunchKernel(fn, dim3(n_sm), dim3(kThreads), args, smem, nullptr));
+    MK_CUDA(cudaEventRecord(e1, nullptr));
+    MK_CUDA(cudaEventSynchronize(e1));
+    float ms = 0.f;
+    MK_CUDA(cudaEventElapsedTime(&ms, e0, e1));
+    if (it > 0) best = std::min(best, ms);
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  std::vector<float> hs(n_sm * kConsumerWarps);
+  MK_CUDA(cudaMemcpy(hs.data(), sink.p, hs.size() * 4, cudaMemcpyDeviceToHost));
+  for (float v : hs)
+    if (std::isnan(v)) return fail(MK_ERR_TIMEOUT, "stream bench: a wait ran out");
+  *gbps = (double)per_cta * n_sm / (best * 1e-3) / 1e9;
+  return MK_OK;
+}
+
 }  // extern "C"

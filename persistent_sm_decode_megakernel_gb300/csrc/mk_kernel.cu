@@ -52,6 +52,91 @@ __global__ void __launch_bounds__(256, 1) mk_barrier_kernel(uint32_t* ctr, float
   }
 }
 
+// ---------------------------------------------------------------- page-stream microbenchmark
+// The decode kernel's loader / compute-warp structure with nothing else: one lane of the
+// loader warp streams bytes_per_cta of contiguous HBM through a ring of n_pages pages
+// with TMA bulk copies; the 8 compute warps either hand each page straight back
+// (mode 0) or first run the B=1 fp16 GEMV slice product on their eighth of it (mode 1).
+__global__ void __launch_bounds__(kThreads, 1) mk_stream_kernel(const uint8_t* src, long long bytes_per_cta,
+                                                                int page_bytes, int n_pages, int mode, int hint,
+                                                                float* sink) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ uint64_t full[kMaxPages], empty[kMaxPages];
+  __shared__ int bad;
+  uint8_t* pages = smem;
+  float* x = reinterpret_cast<float*>(smem + (size_t)n_pages * page_bytes);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ws = page_bytes / 16;  // slice elements per warp
+  if (tid == 0) {
+    for (int i = 0; i < n_pages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kConsumerWarps);
+    }
+    bad = 0;
+    mbar_fence_init();
+  }
+  for (int i = tid; i < ws; i += kThreads) x[i] = 1.0f / (1 + (i & 7));
+  __syncthreads();
+  const long long n = bytes_per_cta / page_bytes;
+  const uint8_t* base = src + (long long)blockIdx.x * bytes_per_cta;
+  const uint64_t t0 = globaltimer_ns();
+  const uint64_t limit = 2000000000ull;
+  if (warp == kConsumerWarps) {
+    if (lane != 0) return;
+    const uint64_t pol = l2_evict_first_policy();
+    for (long long c = 0; c < n; ++c) {
+      const int slot = (int)(c % n_pages);
+      const uint32_t ph = (uint32_t)((c / n_pages) & 1);
+      while (!mbar_try_wait(&empty[slot], ph ^ 1u)) {
+        if (globaltimer_ns() - t0 > limit) {
+          bad = 1;
+          return;
+        }
+      }
+      mbar_arrive_expect_tx(&full[slot], (uint32_t)page_bytes);
+      if (hint)
+        tma_load_1d(pages + (size_t)slot * page_bytes, base + c * page_bytes, (uint32_t)page_bytes, &full[slot], pol);
+      else
+        tma_load_1d_plain(pages + (size_t)slot * page_bytes, base + c * page_bytes, (uint32_t)page_bytes, &full[slot]);
+    }
+    return;
+  }
+  float acc = 0.f;
+  for (long long c = 0; c < n; ++c) {
+    const int slot = (int)(c % n_pages);
+    const uint32_t ph = (uint32_t)((c / n_pages) & 1);
+    bool timed_out = false;
+    while (!mbar_try_wait(&full[slot], ph)) {
+      if (bad || globaltimer_ns() - t0 > limit) {
+        timed_out = true;
+        break;
+      }
+    }
+    if (timed_out) {
+      bad = 1;
+      break;
+    }
+    if (mode == 1) {
+      const uint4* w = reinterpret_cast<const uint4*>(pages + (size_t)slot * page_bytes + (size_t)warp * ws * 2);
+      float a = 0.f;
+      for (int v = lane; v < ws / 8; v += 32) {
+        float f[8];
+        Unpack<__half>::u8(w[v], f);
+        const float4 x0 = reinterpret_cast<const float4*>(x + v * 8)[0];
+        const float4 x1 = reinterpret_cast<const float4*>(x + v * 8)[1];
+        a = fmaf(f[0], x0.x, a); a = fmaf(f[1], x0.y, a); a = fmaf(f[2], x0.z, a); a = fmaf(f[3], x0.w, a);
+        a = fmaf(f[4], x1.x, a); a = fmaf(f[5], x1.y, a); a = fmaf(f[6], x1.z, a); a = fmaf(f[7], x1.w, a);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+      acc += a;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+  }
+  if (lane == 0) sink[blockIdx.x * kConsumerWarps + warp] = bad ? CUDART_NAN_F : acc;
+}
+
 // ---------------------------------------------------------------- launch table
 const void* step_kernel_entry_f16_counter();
 const void* step_kernel_entry_f16_sentinel();
@@ -64,5 +149,6 @@ const void* step_kernel_entry(int dtype, int sync_mode, bool /*trace: a runtime 
 }
 
 const void* barrier_kernel_entry() { return reinterpret_cast<const void*>(&mk_barrier_kernel); }
+const void* stream_kernel_entry() { return reinterpret_cast<const void*>(&mk_stream_kernel); }
 
 }  // namespace mk

@@ -445,34 +445,86 @@ __device__ void stage_rmsnorm(const DevState& S, const float* h, const uint16_t*
 }
 
 // ---------------------------------------------------------------- GEMV slice
-// One warp, one slice: lane l takes 16-byte vectors l, l+32, ... of the slice; fp32
-// accumulation per sequence; then a warp-shuffle reduction.
+// One warp, one slice (WS consecutive weights of one row) per page.  Shared memory is
+// the limit here: fp32 x costs twice the bytes of the fp16/bf16 weights, so
+//  * slice_dot_xreg (B <= 2, each warp always on the same slice of a row): the warp's
+//    x segment sits in registers for the whole instruction; only weights are read from
+//    the page, 16 bytes per lane, four loads in flight, two accumulator chains;
+//  * slice_dot_smem (otherwise): 8-byte weight loads and 16-byte x loads, both
+//    contiguous across the warp (no bank conflicts), two accumulator chains.
 template <typename WT, int NB>
-__device__ __forceinline__ void slice_dot(const uint8_t* wp, const float* x, int K, int WS, int lane,
-                                          float (&acc)[NB]) {
+__device__ __forceinline__ void slice_dot_xreg(const uint8_t* wp, const float (&xr)[NB][32], int nv, int lane,
+                                               float (&acc)[NB]) {
   const uint4* w = reinterpret_cast<const uint4*>(wp);
-  const int nv = WS >> 3;
-#pragma unroll 2
-  for (int v = lane; v < nv; v += 32) {
-    const uint4 wv = w[v];
+  uint4 wv[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int v = lane + 32 * j;
+    wv[j] = v < nv ? w[v] : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float a0[NB], a1[NB];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) a0[b] = a1[b] = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
     float f[8];
-    Unpack<WT>::u8(wv, f);
+    Unpack<WT>::u8(wv[j], f);
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (j & 1)
+          a1[b] = fmaf(f[e], xr[b][j * 8 + e], a1[b]);
+        else
+          a0[b] = fmaf(f[e], xr[b][j * 8 + e], a0[b]);
+      }
+  }
+#pragma unroll
+  for (int b = 0; b < NB; ++b) acc[b] = a0[b] + a1[b];
+}
+
+template <typename WT, int NB>
+__device__ __forceinline__ void slice_dot_smem(const uint8_t* wp, const float* x, int K, int WS, int lane,
+                                               float (&acc)[NB]) {
+  const uint2* w = reinterpret_cast<const uint2*>(wp);
+  const int nq = WS >> 2;  // groups of four weights
+  float a0[NB], a1[NB];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) a0[b] = a1[b] = 0.f;
+  int q = lane;
+  for (; q + 32 < nq; q += 64) {
+    const uint2 w0 = w[q], w1 = w[q + 32];
+    float f0[4], f1[4];
+    Unpack<WT>::u4(w0, f0);
+    Unpack<WT>::u4(w1, f1);
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
-      const float4* xp = reinterpret_cast<const float4*>(x + (size_t)b * K + v * 8);
-      const float4 x0 = xp[0], x1 = xp[1];
-      float a = acc[b];
-      a = fmaf(f[0], x0.x, a);
-      a = fmaf(f[1], x0.y, a);
-      a = fmaf(f[2], x0.z, a);
-      a = fmaf(f[3], x0.w, a);
-      a = fmaf(f[4], x1.x, a);
-      a = fmaf(f[5], x1.y, a);
-      a = fmaf(f[6], x1.z, a);
-      a = fmaf(f[7], x1.w, a);
-      acc[b] = a;
+      const float4 x0 = *reinterpret_cast<const float4*>(x + (size_t)b * K + q * 4);
+      const float4 x1 = *reinterpret_cast<const float4*>(x + (size_t)b * K + (q + 32) * 4);
+      a0[b] = fmaf(f0[0], x0.x, a0[b]);
+      a0[b] = fmaf(f0[1], x0.y, a0[b]);
+      a0[b] = fmaf(f0[2], x0.z, a0[b]);
+      a0[b] = fmaf(f0[3], x0.w, a0[b]);
+      a1[b] = fmaf(f1[0], x1.x, a1[b]);
+      a1[b] = fmaf(f1[1], x1.y, a1[b]);
+      a1[b] = fmaf(f1[2], x1.z, a1[b]);
+      a1[b] = fmaf(f1[3], x1.w, a1[b]);
     }
   }
+  if (q < nq) {
+    float f0[4];
+    Unpack<WT>::u4(w[q], f0);
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const float4 x0 = *reinterpret_cast<const float4*>(x + (size_t)b * K + q * 4);
+      a0[b] = fmaf(f0[0], x0.x, a0[b]);
+      a0[b] = fmaf(f0[1], x0.y, a0[b]);
+      a0[b] = fmaf(f0[2], x0.z, a0[b]);
+      a0[b] = fmaf(f0[3], x0.w, a0[b]);
+    }
+  }
+#pragma unroll
+  for (int b = 0; b < NB; ++b) acc[b] = a0[b] + a1[b];
 }
 
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
@@ -504,27 +556,55 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
   }
   consumer_sync();
 
-  // 2. stream the slices
+  // 2. stream the slices: warp w takes slice i0 + w of every page of 8 slices
   float* rowpart = scratch;  // [rows][spr][NB]
   const int spr = g.spr(), ns = g.nslices();
-  for (int i0 = 0; i0 < ns; i0 += kConsumerWarps) {
-    const uint8_t* pg = page_wait(S, c, pages, ring);
-    const int i = i0 + warp;
-    if (i < ns) {
-      const int r = i / spr, s = i - r * spr;
-      float acc[NB];
+  auto run_pages = [&](auto&& dot) {
+    for (int i0 = 0; i0 < ns; i0 += kConsumerWarps) {
+      const uint8_t* pg = page_wait(S, c, pages, ring);
+      const int i = i0 + warp;
+      if (i < ns) {
+        const int r = i / spr, s = i - r * spr;
+        float acc[NB];
+        dot(pg + (size_t)warp * g.WS * 2, s, acc);
 #pragma unroll
-      for (int b = 0; b < NB; ++b) acc[b] = 0.f;
-      slice_dot<WT, NB>(pg + (size_t)warp * g.WS * 2, xbuf + (size_t)s * g.WS, g.K, g.WS, lane, acc);
+        for (int b = 0; b < NB; ++b) acc[b] = warp_sum(acc[b]);
+        if (lane == 0) {
 #pragma unroll
-      for (int b = 0; b < NB; ++b) acc[b] = warp_sum(acc[b]);
-      if (lane == 0) {
-#pragma unroll
-        for (int b = 0; b < NB; ++b) rowpart[((size_t)r * spr + s) * NB + b] = acc[b];
+          for (int b = 0; b < NB; ++b) rowpart[((size_t)r * spr + s) * NB + b] = acc[b];
+        }
       }
+      page_release(S, c, ring);
     }
-    page_release(S, c, ring);
+  };
+  bool done = false;
+  if constexpr (NB <= 2) {
+    // slices i = 8c + w: when spr divides 8, warp w always sees slice w % spr of a row
+    if (kConsumerWarps % spr == 0 && g.WS <= 32 * 32) {
+      const int nv = g.WS >> 3, sw = warp % spr;
+      float xr[NB][32];
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int v = lane + 32 * j;
+          const float* xp = xbuf + (size_t)b * g.K + (size_t)sw * g.WS + v * 8;
+          float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+          if (v < nv) {
+            x0 = reinterpret_cast<const float4*>(xp)[0];
+            x1 = reinterpret_cast<const float4*>(xp)[1];
+          }
+          xr[b][j * 8 + 0] = x0.x; xr[b][j * 8 + 1] = x0.y; xr[b][j * 8 + 2] = x0.z; xr[b][j * 8 + 3] = x0.w;
+          xr[b][j * 8 + 4] = x1.x; xr[b][j * 8 + 5] = x1.y; xr[b][j * 8 + 6] = x1.z; xr[b][j * 8 + 7] = x1.w;
+        }
+      run_pages([&](const uint8_t* wp, int, float(&acc)[NB]) { slice_dot_xreg<WT, NB>(wp, xr, nv, lane, acc); });
+      done = true;
+    }
   }
+  if (!done)
+    run_pages([&](const uint8_t* wp, int s, float(&acc)[NB]) {
+      slice_dot_smem<WT, NB>(wp, xbuf + (size_t)s * g.WS, g.K, g.WS, lane, acc);
+    });
   consumer_sync();
 
   // 3. finalize rows in a fixed order and apply the op's epilogue

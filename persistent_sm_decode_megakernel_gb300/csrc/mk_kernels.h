@@ -6,4 +6,6 @@ namespace mk {
 const void* step_kernel_entry(int dtype, int sync_mode, bool trace);
 // grid-barrier latency microbenchmark kernel
 const void* barrier_kernel_entry();
+// page-stream microbenchmark kernel
+const void* stream_kernel_entry();
 }  // namespace mk
