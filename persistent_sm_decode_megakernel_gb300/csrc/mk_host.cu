@@ -69,6 +69,7 @@ struct mk_ctx {
   const void* kernel = nullptr;
   const void* kernel_trace = nullptr;
   DevState st{};  // template, counters patched per schedule
+  ModelPtrs ptrs;  // device addresses written into every instruction
   DevBuf ptr_tables, rope, act, argkeys, ctl, trace;
   int trace_cap = 0;
   Ctl* host_ctl = nullptr;  // pinned
@@ -143,8 +144,12 @@ mk_status get_sched(mk_ctx* ctx, int B, Sched** out) {
     return MK_OK;
   }
   auto sc = std::make_unique<Sched>();
-  std::string e = build_plan(ctx->m, ctx->geo, ctx->n_cta, B, ctx->opts.fault_drop_signal, &sc->plan);
+  // counter mode merges the KV splits in the last-arriving split; sentinel mode keeps the
+  // separate ATTN_REDUCE op (it has no atomics to elect a last arriver)
+  const bool fuse = ctx->opts.sync_mode == MK_SYNC_COUNTER;
+  std::string e = build_plan(ctx->m, ctx->geo, ctx->n_cta, B, ctx->opts.fault_drop_signal, fuse, &sc->plan);
   if (!e.empty()) return fail(MK_ERR_INVALID, "schedule: " + e);
+  bake_pointers(ctx->m, ctx->ptrs, &sc->plan);
   if (ctx->opts.fault_drop_signal <= 0) {
     e = validate_plan(ctx->m, ctx->geo, sc->plan);
     if (!e.empty()) return fail(MK_ERR_INVALID, "schedule rejected by the validator: " + e);
@@ -292,7 +297,7 @@ mk_status mk_plan(const mk_model_desc* desc, const mk_options* opts, int n_ctas,
   e = make_geometry(m, n_ctas, o.page_bytes, o.n_pages, o.kv_splits, 232448, &g);
   if (!e.empty()) return fail(MK_ERR_INVALID, e);
   Plan p;
-  e = build_plan(m, g, n_ctas, m.max_batch, o.fault_drop_signal, &p);
+  e = build_plan(m, g, n_ctas, m.max_batch, o.fault_drop_signal, o.sync_mode == MK_SYNC_COUNTER, &p);
   if (!e.empty()) return fail(MK_ERR_INVALID, e);
   e = validate_plan(m, g, p);
   if (!e.empty()) return fail(MK_ERR_INVALID, "schedule rejected by the validator: " + e);
@@ -441,6 +446,14 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
   S.sync_mode = o.sync_mode;
   S.timeout_ns = (int64_t)(o.wait_timeout_s * 1e9);
   S.backoff_max_ns = o.backoff_max_ns;
+  ModelPtrs& mp = ctx->ptrs;
+  mp.final_norm = w->final_norm;
+  mp.lm_head = w->lm_head;
+  std::vector<const void*>* dst[11] = {&mp.attn_norm, &mp.wq, &mp.wk, &mp.wv, &mp.wo, &mp.mlp_norm,
+                                       &mp.w_gate, &mp.w_up, &mp.w_down, &mp.kcache, &mp.vcache};
+  for (int k = 0; k < 9; ++k) dst[k]->assign(tabs[k], tabs[k] + m.L);
+  mp.kcache.assign(kv->k_cache, kv->k_cache + m.L);
+  mp.vcache.assign(kv->v_cache, kv->v_cache + m.L);
   // the schedule for the largest batch is built (and validated) now; others on first use
   Sched* sc = nullptr;
   mk_status s = get_sched(ctx.get(), m.max_batch, &sc);

@@ -50,6 +50,25 @@ struct Instr {
 };
 static_assert(sizeof(Instr) == 64, "instruction is 64 bytes");
 
+// Argument layout (the host writes absolute device pointers into the instruction so that
+// neither role has to chase per-layer pointer tables on the critical path):
+//   EMBED   a0 e0, a1 e1 (flattened [B, d] range)
+//   QKV     a0 matrix (0 q, 1 k, 2 v), a1 head, a2 first pair i0, a3 pairs n,
+//           p2 gain, p3 cache of this layer (k or v), p4 rows i0.., p5 rows hd/2+i0..
+//   ATTN    a0 b, a1 kv head j, a2 split s, a3 splits S, a4 arrival counter (-1: the
+//           merge is a separate ATTN_REDUCE), p4 keys of (b, j) at t = 0, p5 values
+//   REDUCE  a0 b, a1 j
+//   OPROJ / DOWN   a0 row0, a1 rows, p4 first row
+//   UPGATE  a0 row0, a1 rows, p2 gain, p4 gate rows, p5 up rows
+//   LMHEAD  a0 row0, a1 rows, a2 CTAs with LM rows, p2 final gain, p4 first row
+// pK = the 64-bit value in a[2K], a[2K+1]
+constexpr int kP2 = 4, kP3 = 6, kP4 = 8, kP5 = 10;
+inline void set_ptr(Instr& in, int at, const void* p) {
+  const uint64_t v = reinterpret_cast<uint64_t>(p);
+  in.a[at] = (int32_t)(uint32_t)(v & 0xFFFFFFFFu);
+  in.a[at + 1] = (int32_t)(uint32_t)(v >> 32);
+}
+
 struct ErrWord {
   uint32_t code;        // mk_status, 0 = none
   int32_t cta;

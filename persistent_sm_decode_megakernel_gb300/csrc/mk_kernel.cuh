@@ -96,6 +96,25 @@ __device__ __forceinline__ float load_act(const float* p, const DevState& S, Sme
   return poll_slow(p, S, c);
 }
 
+// a device pointer the host wrote into the instruction (pK at a[2K], a[2K+1])
+__device__ __forceinline__ const uint16_t* iptr(const Instr& in, int at) {
+  return reinterpret_cast<const uint16_t*>(((uint64_t)(uint32_t)in.a[at + 1] << 32) | (uint32_t)in.a[at]);
+}
+// instructions are read-only for the whole launch: 4 x 16-byte non-coherent loads
+__device__ __forceinline__ Instr load_instr(const Instr* p) {
+  Instr in;
+  const uint4* s = reinterpret_cast<const uint4*>(p);
+  uint4* d = reinterpret_cast<uint4*>(&in);
+  d[0] = __ldg(s);
+  d[1] = __ldg(s + 1);
+  d[2] = __ldg(s + 2);
+  d[3] = __ldg(s + 3);
+  return in;
+}
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 // ---------------------------------------------------------------- tile geometry
 // A GEMV instruction covers one or two row segments of a row-major [rows, K] matrix.
 // Its tiles are "slices": WS consecutive elements of one row; a page holds
@@ -112,42 +131,31 @@ struct Gemv {
 
 __device__ __forceinline__ Gemv make_gemv(const DevState& S, const Instr& in) {
   Gemv g;
-  g.seg[1] = nullptr;
+  g.seg[0] = iptr(in, kP4);
+  g.seg[1] = iptr(in, kP5);
   g.segr[1] = 0;
-  const int l = in.layer;
   switch (in.op) {
-    case OP_QKV: {
-      const int mat = in.a[0], head = in.a[1], i0 = in.a[2], n = in.a[3];
-      const uint16_t* W = mat == 0 ? S.wq[l] : (mat == 1 ? S.wk[l] : S.wv[l]);
-      const size_t ra = (size_t)head * S.hd + i0;
-      g.seg[0] = W + ra * S.d;
-      g.seg[1] = W + (ra + S.hd / 2) * S.d;
-      g.segr[0] = g.segr[1] = n;
+    case OP_QKV:
+      g.segr[0] = g.segr[1] = in.a[3];
       g.K = S.d;
       g.WS = S.ws_qkv;
       break;
-    }
     case OP_OPROJ:
-      g.seg[0] = S.wo[l] + (size_t)in.a[0] * S.Hq * S.hd;
       g.segr[0] = in.a[1];
       g.K = S.Hq * S.hd;
       g.WS = S.ws_o;
       break;
     case OP_UPGATE:
-      g.seg[0] = S.w_gate[l] + (size_t)in.a[0] * S.d;
-      g.seg[1] = S.w_up[l] + (size_t)in.a[0] * S.d;
       g.segr[0] = g.segr[1] = in.a[1];
       g.K = S.d;
       g.WS = S.ws_up;
       break;
     case OP_DOWN:
-      g.seg[0] = S.w_down[l] + (size_t)in.a[0] * S.F;
       g.segr[0] = in.a[1];
       g.K = S.F;
       g.WS = S.ws_down;
       break;
     default:  // OP_LMHEAD
-      g.seg[0] = S.lm_head + (size_t)in.a[0] * S.d;
       g.segr[0] = in.a[1];
       g.K = S.d;
       g.WS = S.ws_lm;
@@ -184,15 +192,15 @@ __device__ __forceinline__ Attn make_attn(const DevState& S, const StepArgs& A, 
     a.nblocks = 0;
     a.has_new = false;
   }
-  const size_t base = (((size_t)a.b * S.Hkv + a.j) * S.max_ctx + a.t0) * S.hd;
-  a.kb = S.kcache[in.layer] + base;
-  a.vb = S.vcache[in.layer] + base;
+  a.kb = iptr(in, kP4) + (size_t)a.t0 * S.hd;  // (b, j) rows start at the baked pointer
+  a.vb = iptr(in, kP5) + (size_t)a.t0 * S.hd;
   return a;
 }
 
 __device__ __forceinline__ float* act_ptr(const DevState& S, float* act, int kind, int layer) {
   return act + S.act_off[kind] + (int64_t)layer * S.act_stride[kind];
 }
+
 
 // ---------------------------------------------------------------- loader warp
 __device__ bool producer_acquire(const DevState& S, SmemCtl* c, int slot, uint32_t ph) {
@@ -223,7 +231,8 @@ __device__ __noinline__ void producer(const DevState& S, const StepArgs& A, Smem
   const int end = A.q_start[cta + 1];
   bool ok = true;
   for (int pc = A.q_start[cta]; pc < end && ok; ++pc) {
-    const Instr in = A.instr[pc];
+    const Instr in = load_instr(A.instr + pc);
+    if (pc + 2 < end) prefetch_l1(A.instr + pc + 2);  // the next instructions, for both roles
     if (in.op == OP_END) break;
     switch (in.op) {
       case OP_QKV:
@@ -539,13 +548,13 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
   // 1. inputs
   switch (in.op) {
     case OP_QKV:
-      stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_H, l), S.attn_norm[l], B, xbuf, c, ring);
+      stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_H, l), iptr(in, kP2), B, xbuf, c, ring);
       break;
     case OP_UPGATE:
-      stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_HMID, l), S.mlp_norm[l], B, xbuf, c, ring);
+      stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_HMID, l), iptr(in, kP2), B, xbuf, c, ring);
       break;
     case OP_LMHEAD:
-      stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_H, S.L), S.final_norm, B, xbuf, c, ring);
+      stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_H, S.L), iptr(in, kP2), B, xbuf, c, ring);
       break;
     case OP_OPROJ:
       stage_copy<SYNC, NB>(S, act_ptr(S, act, ACT_O, l), g.K, B, xbuf, c, ring);
@@ -636,8 +645,7 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
           q[i + half] = vb;
         } else {
           const uint16_t ra = Unpack<WT>::round(va), rb = Unpack<WT>::round(vb);
-          uint16_t* cache = (mat == 1 ? S.kcache[l] : S.vcache[l]) +
-                            (((size_t)b * S.Hkv + head) * S.max_ctx + pos) * hd;
+          uint16_t* cache = const_cast<uint16_t*>(iptr(in, kP3)) + (((size_t)b * S.Hkv + head) * S.max_ctx + pos) * hd;
           cache[i] = ra;
           cache[i + half] = rb;
           float* kvn = act_ptr(S, act, ACT_KVN, l) + ((size_t)b * 2 + (mat - 1)) * S.Hkv * hd + (size_t)head * hd;
@@ -988,7 +996,7 @@ __device__ void consumer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8
   int order_n = 0;
   const int end = A.q_start[cta + 1];
   for (int pc = A.q_start[cta]; pc < end; ++pc) {
-    const Instr in = A.instr[pc];
+    const Instr in = load_instr(A.instr + pc);
     if (in.op == OP_END) break;
     uint64_t t_fetch = 0, t_ready = 0;
     if (TRACE) t_fetch = globaltimer_ns();
@@ -1061,6 +1069,23 @@ __device__ void consumer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8
     }
     // ---- signal
     if (consumer_sync_or(c->abort)) break;
+    bool signal = true;
+    if (in.op == OP_ATTN && in.a[4] >= 0) {
+      // fused merge: count this split's arrival (acq_rel: publishes this CTA's partial,
+      // and for the last arriver makes every other split's partial visible); the CTA
+      // that brings the count to S merges the splits, then signals the O-proj counter
+      bool last = false;
+      if (tid == 0) {
+        const uint32_t old = atom_acq_rel_add_u32(&S.counters[in.a[4]], 1u);
+        last = (old + 1u == (A.epoch + 1u) * (uint32_t)in.a[3]);
+      }
+      if (consumer_sync_or(last)) {
+        op_attn_reduce<SYNC>(S, in, A.B, c, scratch, act);
+        if (consumer_sync_or(c->abort)) break;
+      } else {
+        signal = false;
+      }
+    }
     if (in.op == OP_LMHEAD && (in.flags & F_LAST_LM)) {
       // this CTA's share of the vocabulary is done: publish its best key, then the last
       // CTA to finish turns the winning keys into tokens
@@ -1068,7 +1093,7 @@ __device__ void consumer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8
       if (tid < A.B) atomicMax(&S.argkeys[kp * kMaxBatch + tid], c->best[tid]);
       consumer_sync();
       if (tid == 0) {
-        const uint32_t n_lm = (uint32_t)in.a[5];
+        const uint32_t n_lm = (uint32_t)in.a[2];
         const uint32_t old = atom_acq_rel_add_u32(&S.counters[in.signal_ctr], 1u);
         if (old + 1u == (A.epoch + 1u) * n_lm) {
           for (int b = 0; b < A.B; ++b) {
@@ -1079,7 +1104,7 @@ __device__ void consumer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8
           }
         }
       }
-    } else if (tid == 0 && use_ctr && in.signal_ctr >= 0) {
+    } else if (tid == 0 && use_ctr && signal && in.signal_ctr >= 0) {
       red_release_add_u32(&S.counters[in.signal_ctr], 1u);
     }
     if (TRACE && tid == 0) {

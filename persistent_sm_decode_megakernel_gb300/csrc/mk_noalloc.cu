@@ -133,8 +133,17 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_desc* desc, const mk_
     if (!e.empty()) return fail(MK_ERR_INVALID, e);
   }
   Plan plan;
-  e = build_plan(m, g, n_cta, B, 0, &plan);
+  e = build_plan(m, g, n_cta, B, 0, true, &plan);
   if (!e.empty()) return fail(MK_ERR_INVALID, "schedule: " + e);
+  ModelPtrs mp;
+  mp.final_norm = w->final_norm;
+  mp.lm_head = w->lm_head;
+  std::vector<const void*>* dst[9] = {&mp.attn_norm, &mp.wq, &mp.wk, &mp.wv, &mp.wo,
+                                      &mp.mlp_norm, &mp.w_gate, &mp.w_up, &mp.w_down};
+  for (int k = 0; k < 9; ++k) dst[k]->assign(tabs[k], tabs[k] + L);
+  mp.kcache.assign(kv->k_cache, kv->k_cache + L);
+  mp.vcache.assign(kv->v_cache, kv->v_cache + L);
+  bake_pointers(m, mp, &plan);
   e = validate_plan(m, g, plan);
   if (!e.empty()) return fail(MK_ERR_INVALID, "schedule rejected by the validator: " + e);
 

@@ -96,9 +96,11 @@ static Instr mk_instr(int op, int layer, int wait_ctr, uint32_t wait_n, int sign
   return in;
 }
 
-std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B, int drop_signal, Plan* p) {
+std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B, int drop_signal, bool fuse_reduce,
+                       Plan* p) {
   if (B < 1 || B > m.max_batch) return "batch out of range";
   *p = Plan();
+  p->fused_reduce = fuse_reduce;
   p->n_cta = n_cta;
   p->B = B;
   p->queues.assign(n_cta, {});
@@ -159,22 +161,32 @@ std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B,
         }
       }
     }
-    // ATTENTION: B * Hkv * S split units, dealt round-robin
+    // ATTENTION: B * Hkv * S split units, dealt round-robin.  Fused: each unit counts its
+    // arrival on the (b, j) counter; the last of the S merges the splits and signals c_red
+    // (one signal per (b, j) and step).
     const int c_att = new_ctr();
+    const int c_red = new_ctr();
     {
       const int nu = B * m.Hkv * g.S;
+      std::vector<int> arr;
+      if (fuse_reduce)
+        for (int k = 0; k < B * m.Hkv; ++k) arr.push_back(new_ctr());
       for (int u = 0; u < nu; ++u) {
-        Instr in = mk_instr(OP_ATTN, l, c_qkv, 0, c_att);
+        Instr in = mk_instr(OP_ATTN, l, c_qkv, 0, fuse_reduce ? c_red : c_att);
         in.a[0] = u / (m.Hkv * g.S);
         in.a[1] = (u / g.S) % m.Hkv;
         in.a[2] = u % g.S;
         in.a[3] = g.S;
+        in.a[4] = fuse_reduce ? arr[u / g.S] : -1;
         emit(u % n_cta, in);
+      }
+      if (fuse_reduce) {
+        p->signals[c_red] = (uint32_t)(B * m.Hkv);
+        for (int k : arr) p->signals[k] = (uint32_t)g.S;  // arrivals (never waited on)
       }
     }
     // ATTN_REDUCE: one unit per (sequence, kv head), spread over the CTAs
-    const int c_red = new_ctr();
-    {
+    if (!fuse_reduce) {
       const int nu = B * m.Hkv;
       for (int u = 0; u < nu; ++u) {
         Instr in = mk_instr(OP_ATTN_REDUCE, l, c_att, 0, c_red);
@@ -225,7 +237,7 @@ std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B,
         in.a[1] = n;
         if (last) {
           in.flags = F_LAST_LM;
-          in.a[5] = n_lm;
+          in.a[2] = n_lm;
         }
         emit(c, in);
         r0 += n;
@@ -239,7 +251,9 @@ std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B,
   int sig_seen = 0;
   for (auto& pe : all) {
     // fault injection: the k-th signal is removed, its waiters keep expecting it
-    if (drop_signal > 0 && pe.in.signal_ctr >= 0 && !(pe.in.flags & F_LAST_LM) && ++sig_seen == drop_signal)
+    const bool fused = pe.in.op == OP_ATTN && pe.in.a[4] >= 0;  // signals only if last: not a fixed signal
+    if (drop_signal > 0 && pe.in.signal_ctr >= 0 && !(pe.in.flags & F_LAST_LM) && !fused &&
+        ++sig_seen == drop_signal)
       pe.in.signal_ctr = -1;
     p->queues[pe.cta].push_back(pe.in);
   }
@@ -252,12 +266,19 @@ std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B,
     return 1 + 6 * in.layer + (in.op - OP_QKV);
   };
   const int n_phase = 2 + 6 * m.L;
-  p->phase_queues.assign(n_phase, std::vector<std::vector<Instr>>(n_cta));
+  std::vector<std::vector<std::vector<Instr>>> phases(n_phase, std::vector<std::vector<Instr>>(n_cta));
+  std::vector<int> used(n_phase, 0);
   for (int c = 0; c < n_cta; ++c)
     for (const auto& in : p->queues[c])
-      if (in.op != OP_END) p->phase_queues[phase_of(in)][c].push_back(in);
-  for (auto& ph : p->phase_queues)
-    for (auto& q : ph) q.push_back(mk_instr(OP_END, 0, -1, 0, -1));
+      if (in.op != OP_END) {
+        phases[phase_of(in)][c].push_back(in);
+        used[phase_of(in)] = 1;
+      }
+  for (int k = 0; k < n_phase; ++k) {  // phases with no work (the fused merge) launch nothing
+    if (!used[k]) continue;
+    for (auto& q : phases[k]) q.push_back(mk_instr(OP_END, 0, -1, 0, -1));
+    p->phase_queues.push_back(std::move(phases[k]));
+  }
 
   // streamed weight bytes of one step
   long long per_layer = (long long)(m.Hq + 2 * m.Hkv) * m.hd * m.d + (long long)m.d * m.Hq * m.hd +
@@ -265,6 +286,50 @@ std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B,
   p->weight_bytes = 2 * ((long long)m.L * per_layer + (long long)m.V * m.d + m.d);
   (void)G;
   return "";
+}
+
+void bake_pointers(const ModelShape& m, const ModelPtrs& w, Plan* p) {
+  auto at = [](const void* base, size_t elems) {
+    return static_cast<const void*>(static_cast<const uint16_t*>(base) + elems);
+  };
+  auto bake = [&](Instr& in) {
+    const int l = in.layer;
+    switch (in.op) {
+      case OP_QKV: {
+        const int mat = in.a[0], head = in.a[1], i0 = in.a[2];
+        const void* W = mat == 0 ? w.wq[l] : (mat == 1 ? w.wk[l] : w.wv[l]);
+        const size_t ra = (size_t)head * m.hd + i0;
+        set_ptr(in, kP2, w.attn_norm[l]);
+        set_ptr(in, kP3, mat == 0 ? nullptr : (mat == 1 ? w.kcache[l] : w.vcache[l]));
+        set_ptr(in, kP4, at(W, ra * m.d));
+        set_ptr(in, kP5, at(W, (ra + m.hd / 2) * m.d));
+        break;
+      }
+      case OP_ATTN: {
+        const size_t base = ((size_t)in.a[0] * m.Hkv + in.a[1]) * m.max_ctx * m.hd;
+        set_ptr(in, kP4, at(w.kcache[l], base));
+        set_ptr(in, kP5, at(w.vcache[l], base));
+        break;
+      }
+      case OP_OPROJ: set_ptr(in, kP4, at(w.wo[l], (size_t)in.a[0] * m.Hq * m.hd)); break;
+      case OP_UPGATE:
+        set_ptr(in, kP2, w.mlp_norm[l]);
+        set_ptr(in, kP4, at(w.w_gate[l], (size_t)in.a[0] * m.d));
+        set_ptr(in, kP5, at(w.w_up[l], (size_t)in.a[0] * m.d));
+        break;
+      case OP_DOWN: set_ptr(in, kP4, at(w.w_down[l], (size_t)in.a[0] * m.F)); break;
+      case OP_LMHEAD:
+        set_ptr(in, kP2, w.final_norm);
+        set_ptr(in, kP4, at(w.lm_head, (size_t)in.a[0] * m.d));
+        break;
+      default: break;
+    }
+  };
+  for (auto& q : p->queues)
+    for (auto& in : q) bake(in);
+  for (auto& ph : p->phase_queues)
+    for (auto& q : ph)
+      for (auto& in : q) bake(in);
 }
 
 // ---------------------------------------------------------------- validator
@@ -303,7 +368,10 @@ std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p)
       if (in.op < OP_EMBED || in.op > OP_LMHEAD) return fmt("cta %lld pc %lld: bad opcode %lld", c, k, in.op);
       if (in.op != OP_LMHEAD && in.layer >= m.L) return "layer out of range";
       if (in.signal_ctr >= p.n_counters || in.wait_ctr >= p.n_counters) return "counter index out of range";
-      if (in.signal_ctr >= 0) sig[in.signal_ctr]++;
+      const bool fused = in.op == OP_ATTN && in.a[4] >= 0;
+      if (fused && (!p.fused_reduce || in.a[4] >= p.n_counters)) return "bad arrival counter";
+      // a fused split signals only when it is the last of its (b, j): once per (b, j)
+      if (in.signal_ctr >= 0 && (!fused || in.a[2] == 0)) sig[in.signal_ctr]++;
       group_units[group_of(in)]++;
       int rows = 0, K = 0, ws = 1;
       switch (in.op) {
@@ -343,7 +411,7 @@ std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p)
       if (in.wait_ctr >= 0 && in.wait_n != sig[in.wait_ctr])
         return fmt("counter %lld: waiters expect %lld signals, the schedule gives %lld", in.wait_ctr, in.wait_n,
                    sig[in.wait_ctr]);
-      if ((in.flags & F_LAST_LM) && (uint32_t)in.a[5] != sig[in.signal_ctr]) return "LM arrival count mismatch";
+      if ((in.flags & F_LAST_LM) && (uint32_t)in.a[2] != sig[in.signal_ctr]) return "LM arrival count mismatch";
     }
 
   // -- simulation with counter semantics: every queue must reach OP_END
@@ -352,20 +420,26 @@ std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p)
   // happens-before summary per executed instruction: groups fully done before it
   std::vector<std::vector<Bits>> done(n_cta);
   for (int c = 0; c < n_cta; ++c) done[c].assign(p.queues[c].size(), Bits(n_group));
-  std::vector<std::vector<std::pair<int, int>>> signalers(p.n_counters);
+  std::vector<std::vector<Bits>> signalers(p.n_counters);  // what each signal carries
   std::vector<int> ctr_group(p.n_counters, -1);
+  std::vector<uint32_t> arrivals(p.n_counters, 0);
+  std::vector<Bits> arrived(p.n_counters, Bits(n_group));
   {
     // a counter "covers" a group when exactly that group's units signal it
     std::vector<int> sig_group(p.n_counters, -2);
     for (int c = 0; c < n_cta; ++c)
       for (const auto& in : p.queues[c])
-        if (in.signal_ctr >= 0 && !(in.flags & F_LAST_LM)) {
+        if (in.signal_ctr >= 0 && !(in.flags & F_LAST_LM) && !(in.op == OP_ATTN && in.a[4] >= 0)) {
           const int gr = group_of(in);
           int& sg = sig_group[in.signal_ctr];
           sg = (sg == -2 || sg == gr) ? gr : -1;
         }
     for (int k = 0; k < p.n_counters; ++k)
       if (sig_group[k] >= 0 && (int)sig[k] == group_units[sig_group[k]]) ctr_group[k] = sig_group[k];
+    // fused merge: its counter completes when every split of every (b, j) has arrived
+    for (int c = 0; c < n_cta; ++c)
+      for (const auto& in : p.queues[c])
+        if (in.op == OP_ATTN && in.a[4] >= 0 && in.signal_ctr >= 0) ctr_group[in.signal_ctr] = group_of(in);
   }
   // required inputs (group ids) of each instruction
   auto required = [&](const Instr& in, int* req) -> int {
@@ -375,7 +449,7 @@ std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p)
       case OP_QKV: req[0] = h_writer; return 1;
       case OP_ATTN: req[0] = 1 + 6 * l + 0; return 1;
       case OP_ATTN_REDUCE: req[0] = 1 + 6 * l + 1; return 1;
-      case OP_OPROJ: req[0] = 1 + 6 * l + 2; req[1] = h_writer; return 2;
+      case OP_OPROJ: req[0] = 1 + 6 * l + (p.fused_reduce ? 1 : 2); req[1] = h_writer; return 2;
       case OP_UPGATE: req[0] = 1 + 6 * l + 3; return 1;
       case OP_DOWN: req[0] = 1 + 6 * l + 4; req[1] = 1 + 6 * l + 3; return 2;
       case OP_LMHEAD: req[0] = 1 + 6 * (m.L - 1) + 5; return 1;
@@ -393,7 +467,7 @@ std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p)
         Bits f(n_group);
         if (pc[c] > 0) f = done[c][pc[c] - 1];
         if (in.wait_ctr >= 0) {
-          for (auto [sc, sp] : signalers[in.wait_ctr]) f.merge(done[sc][sp]);
+          for (const Bits& sb : signalers[in.wait_ctr]) f.merge(sb);
           if (ctr_group[in.wait_ctr] >= 0) f.set(ctr_group[in.wait_ctr]);
         }
         int req[2];
@@ -402,9 +476,20 @@ std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p)
           if (!f.has(req[r]))
             return fmt("race: cta %lld pc %lld reads data of op group %lld not ordered before it", c, pc[c], req[r]);
         done[c][pc[c]] = f;
-        if (in.signal_ctr >= 0) {
+        if (in.op == OP_ATTN && in.a[4] >= 0) {  // arrival; the S-th one merges and signals
+          const int a = in.a[4];
+          arrived[a].merge(f);
+          if (++arrivals[a] == (uint32_t)in.a[3]) {
+            arrivals[a] = 0;
+            if (in.signal_ctr >= 0) {
+              cnt[in.signal_ctr]++;
+              signalers[in.signal_ctr].push_back(arrived[a]);
+            }
+            arrived[a] = Bits(n_group);
+          }
+        } else if (in.signal_ctr >= 0) {
           cnt[in.signal_ctr]++;
-          signalers[in.signal_ctr].push_back({c, (int)pc[c]});
+          signalers[in.signal_ctr].push_back(f);
         }
         pc[c]++;
         progress = true;
@@ -453,7 +538,8 @@ std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p)
   };
   if (!once(emb) || !once(lm)) return "embedding or LM-head rows not covered exactly once";
   for (int l = 0; l < m.L; ++l)
-    if (!once(qkv[l]) || !once(att[l]) || !once(red[l]) || !once(orow[l]) || !once(urow[l]) || !once(drow[l]))
+    if (!once(qkv[l]) || !once(att[l]) || (!p.fused_reduce && !once(red[l])) || !once(orow[l]) || !once(urow[l]) ||
+        !once(drow[l]))
       return fmt("layer %lld: an op's outputs are not covered exactly once", l);
   return "";
 }

@@ -37,12 +37,22 @@ struct Plan {
   // multi-launch control: phases in dependency order; per phase the compacted queues
   std::vector<std::vector<std::vector<Instr>>> phase_queues;
   int64_t weight_bytes = 0;               // streamed weight bytes per step
+  bool fused_reduce = false;              // the split merge runs in the last-arriving ATTN unit
+};
+
+// device addresses the host writes into the instructions (see the layout in mk_internal.h)
+struct ModelPtrs {
+  const void* final_norm = nullptr;
+  const void* lm_head = nullptr;
+  std::vector<const void*> attn_norm, wq, wk, wv, wo, mlp_norm, w_gate, w_up, w_down, kcache, vcache;
 };
 
 // returns "" on success, else a message
 std::string make_geometry(const ModelShape& m, int n_cta, int page_bytes, int n_pages_req, int kv_splits,
                           int smem_limit, Geometry* g);
-std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B, int drop_signal, Plan* p);
+std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B, int drop_signal, bool fuse_reduce,
+                       Plan* p);
+void bake_pointers(const ModelShape& m, const ModelPtrs& w, Plan* p);
 std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p);
 
 }  // namespace mk

@@ -69,9 +69,21 @@ def test_plan_batches_and_sizes(mk):
 
 def test_plan_multilaunch_counts_launches(mk):
     cfg = synth.CONFIGS["2b"]
+    # counter sync merges the KV splits inside the attention launch; sentinel sync keeps
+    # a separate reduce launch per layer
     st, info = _plan(mk, _desc(mk, cfg), 152, exec_mode=mk.MK_EXEC_MULTILAUNCH)
     assert st == mk.MK_OK
+    assert info.launches_per_step == 5 * cfg.n_layers + 2
+    st, info = _plan(mk, _desc(mk, cfg), 152, exec_mode=mk.MK_EXEC_MULTILAUNCH, sync_mode=mk.MK_SYNC_SENTINEL)
+    assert st == mk.MK_OK
     assert info.launches_per_step == 6 * cfg.n_layers + 2
+
+
+@pytest.mark.parametrize("sync", [0, 1])
+def test_plan_validates_both_sync_schedules(mk, sync):
+    for name in ("tiny", "2b"):
+        st, _ = _plan(mk, _desc(mk, synth.CONFIGS[name], max_batch=2), 152, sync_mode=sync)
+        assert st == mk.MK_OK, mk.mk_last_error()
 
 
 def test_validator_rejects_dropped_signal(mk):
