@@ -81,7 +81,7 @@ typedef struct {
 typedef struct {
   int sync_mode;          /* mk_sync_mode: counters (§8.5) or NaN sentinels (§7.3)        */
   int exec_mode;          /* mk_exec_mode: one persistent launch, or the multi-launch control */
-  int page_bytes;         /* shared-memory page size (default 16384; power of two, 4K..32K) */
+  int page_bytes;         /* shared-memory page size (default 32768; power of two, 4K..32K) */
   int n_pages;            /* pages in the pool (default: as many as fit)                  */
   int kv_splits;          /* split-KV partitions per (sequence, kv head); 0 = one wave's worth */
   int trace;              /* 1: record the per-instruction journal (§8.7)                  */
@@ -111,7 +111,10 @@ typedef struct {
 typedef struct {
   int32_t cta, pc, op, layer;
   uint64_t t_fetch;       /* instruction fetched                                           */
-  uint64_t t_ready;       /* dependency satisfied, inputs loaded                           */
+  uint64_t t_ready;       /* dependency satisfied                                          */
+  uint64_t t_mark[4];     /* op-internal marks, 0 when unused.  GEMV: [0] inputs staged,
+                             [1] last weight page consumed.  ATTENTION: [0] q staged, [1]
+                             KV pages consumed, [2] split partial written, [3] merge done */
   uint64_t t_end;         /* outputs written (before the signal)                           */
 } mk_trace_rec;
 

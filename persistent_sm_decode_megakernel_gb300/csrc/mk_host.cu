@@ -598,6 +598,7 @@ mk_status mk_get_trace(mk_ctx* ctx, mk_trace_rec* recs, int max_records, int* n_
       recs[i].layer = tmp[i].layer;
       recs[i].t_fetch = tmp[i].t_fetch;
       recs[i].t_ready = tmp[i].t_ready;
+      for (int k = 0; k < 4; ++k) recs[i].t_mark[k] = tmp[i].t_mark[k];
       recs[i].t_end = tmp[i].t_end;
     }
   }
@@ -838,7 +839,7 @@ mk_status mk_barrier_bench(int mode, int n_barriers, double* us_per_barrier) {
 
 mk_status mk_stream_bench(int page_bytes, int n_pages, int mode, int hint, long long total_bytes, double* gbps) {
   if (!gbps || page_bytes < 1024 || page_bytes > 65536 || (page_bytes & 15) || n_pages < 1 || n_pages > kMaxPages ||
-      (mode != 0 && mode != 1) || total_bytes < (1LL << 20))
+      mode < 0 || mode > 3 || total_bytes < (1LL << 20) || (mode >= 2 && page_bytes != 16384))
     return fail(MK_ERR_INVALID, "stream bench: bad arguments");
   int dev = 0, n_sm = 0;
   MK_CUDA(cudaGetDevice(&dev));

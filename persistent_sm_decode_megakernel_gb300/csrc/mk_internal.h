@@ -87,7 +87,7 @@ struct Ctl {
 
 struct TraceRec {
   int32_t cta, pc, op, layer;
-  uint64_t t_fetch, t_ready, t_end;
+  uint64_t t_fetch, t_ready, t_mark[4], t_end;
 };
 
 enum ActKind { ACT_H = 0, ACT_HMID, ACT_Q, ACT_KVN, ACT_PART, ACT_O, ACT_A, ACT_NUM };

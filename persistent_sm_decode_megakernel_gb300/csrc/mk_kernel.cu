@@ -5,6 +5,7 @@
 #include "mk_internal.h"
 #include "mk_device.cuh"
 #include "mk_kernels.h"
+#include "mk_kernel.cuh"  // the step kernel's GEMV inner loops, for the stream benchmark
 
 namespace mk {
 
@@ -115,6 +116,21 @@ __global__ void __launch_bounds__(kThreads, 1) mk_stream_kernel(const uint8_t* s
     if (timed_out) {
       bad = 1;
       break;
+    }
+    if (mode == 2 || mode == 3) {  // the step kernel's own slice products (B = 1)
+      const uint8_t* wp = pages + (size_t)slot * page_bytes + (size_t)warp * ws * 2;
+      float a[1];
+      if (mode == 2) {
+        float xr[1][32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) xr[0][j] = x[(lane + 32 * (j / 8)) * 8 + (j & 7)];
+        slice_dot_xreg<__half, 1, 4>(wp, xr, ws / 8, lane, a);
+      } else {
+        slice_dot_smem<__half, 1>(wp, x, ws, ws, lane, a);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) a[0] += __shfl_xor_sync(0xffffffffu, a[0], o);
+      acc += a[0];
     }
     if (mode == 1) {
       const uint4* w = reinterpret_cast<const uint4*>(pages + (size_t)slot * page_bytes + (size_t)warp * ws * 2);

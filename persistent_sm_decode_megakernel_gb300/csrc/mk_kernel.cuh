@@ -12,6 +12,8 @@
 // tiles while the current one still computes.
 #pragma once
 #include <cuda_runtime.h>
+
+#include <type_traits>
 #include <math_constants.h>
 
 #include "mk_internal.h"
@@ -28,6 +30,7 @@ struct SmemCtl {
   float red[kConsumerWarps * kMaxBatch];
   int last_issue_phase[kMaxPages];
   uint64_t xbar;  // completion of the x-buffer bulk copy
+  uint64_t tmark[4];  // journal marks inside an op
   volatile int abort;
 };
 static_assert(sizeof(SmemCtl) <= kCtlSmem, "control block fits");
@@ -243,6 +246,18 @@ __device__ __noinline__ void producer(const DevState& S, const StepArgs& A, Smem
         const Gemv g = make_gemv(S, in);
         const int ns = g.nslices();
         const uint32_t sb = (uint32_t)g.WS * 2u;
+        // the compute warps will read the RMSNorm gain and the RoPE rows of this
+        // instruction right after its dependency: pull them into L1 now
+        if (in.op == OP_QKV || in.op == OP_UPGATE || in.op == OP_LMHEAD) {
+          const char* gp = reinterpret_cast<const char*>(iptr(in, kP2));
+          for (int off = 0; off < S.d * 2; off += 128) prefetch_l1(gp + off);
+        }
+        if (in.op == OP_QKV && in.a[0] < 2) {
+          for (int b = 0; b < A.B; ++b) {
+            const char* rp = reinterpret_cast<const char*>(S.rope + (size_t)A.pos[b] * (S.hd / 2) + in.a[2]);
+            for (int off = 0; off < in.a[3] * 8 + 128; off += 128) prefetch_l1(rp + off);
+          }
+        }
         // rows of a segment are contiguous and a row is spr slices, so slice j of
         // segment k starts at seg[k] + j * WS: a page is at most two bulk copies
         const int n0 = g.segr[0] * g.spr();
@@ -406,51 +421,52 @@ __device__ void stage_copy(const DevState& S, const float* src, int K, int B, fl
   consumer_sync();
 }
 
-// RMSNorm recomputed in every CTA from the full residual vector (8 KB per sequence,
-// L2-resident): stage it, sum squares per sequence in a fixed order, scale by the gain.
+// RMSNorm, folded: W (g . h / rms) = (W (g . h)) / rms.  The staged residual is scaled by
+// the gain in place while each thread accumulates its share of sum(h^2); the per-warp
+// sums go to c->red and the epilogue turns them into 1/rms (fixed order, same in every
+// thread), so no CTA-wide barrier sits between staging and the weight pages.
 template <typename WT, int SYNC, int NB>
 __device__ void stage_rmsnorm(const DevState& S, const float* h, const uint16_t* gain, int B, float* xbuf,
                               SmemCtl* c, Ring& ring) {
   const int d = S.d, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   stage_copy<SYNC, NB>(S, h, d, B, xbuf, c, ring);
-  const float4* x4 = reinterpret_cast<const float4*>(xbuf);
+  float4* x4 = reinterpret_cast<float4*>(xbuf);
   const int d4 = d / 4;
+  float ss[NB];
 #pragma unroll
-  for (int b = 0; b < NB; ++b) {
-    float ss = 0.f;
-    for (int k = tid; k < d4; k += kConsumerThreads) {
-      const float4 v = x4[b * d4 + k];
-      ss = fmaf(v.x, v.x, ss);
-      ss = fmaf(v.y, v.y, ss);
-      ss = fmaf(v.z, v.z, ss);
-      ss = fmaf(v.w, v.w, ss);
-    }
-    ss = warp_sum(ss);
-    if (lane == 0) c->red[warp * NB + b] = ss;
-  }
-  consumer_sync();
-  if (tid < NB) {
-    float t = 0.f;
-    for (int w = 0; w < kConsumerWarps; ++w) t += c->red[w * NB + tid];
-    c->inv_rms[tid] = 1.0f / sqrtf(t / (float)d + S.eps);
-  }
-  consumer_sync();
-  float4* w4 = reinterpret_cast<float4*>(xbuf);
+  for (int b = 0; b < NB; ++b) ss[b] = 0.f;
   for (int k = tid; k < d4; k += kConsumerThreads) {
     const uint2 gb = __ldg(reinterpret_cast<const uint2*>(gain) + k);  // 4 gains
     const float g0 = Unpack<WT>::one((uint16_t)(gb.x & 0xFFFFu)), g1 = Unpack<WT>::one((uint16_t)(gb.x >> 16));
     const float g2 = Unpack<WT>::one((uint16_t)(gb.y & 0xFFFFu)), g3 = Unpack<WT>::one((uint16_t)(gb.y >> 16));
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
-      const float r = c->inv_rms[b];
-      float4 v = w4[b * d4 + k];
-      v.x *= r * g0;
-      v.y *= r * g1;
-      v.z *= r * g2;
-      v.w *= r * g3;
-      w4[b * d4 + k] = v;
+      float4 v = x4[b * d4 + k];
+      ss[b] = fmaf(v.x, v.x, ss[b]);
+      ss[b] = fmaf(v.y, v.y, ss[b]);
+      ss[b] = fmaf(v.z, v.z, ss[b]);
+      ss[b] = fmaf(v.w, v.w, ss[b]);
+      v.x *= g0;
+      v.y *= g1;
+      v.z *= g2;
+      v.w *= g3;
+      x4[b * d4 + k] = v;
     }
   }
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    const float t = warp_sum(ss[b]);
+    if (lane == 0) c->red[warp * NB + b] = t;
+  }
+}
+
+// 1/rms of sequence b from the per-warp sums stage_rmsnorm left (after a barrier)
+template <int NB>
+__device__ __forceinline__ float inv_rms_of(const DevState& S, const SmemCtl* c, int b) {
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < kConsumerWarps; ++w) t += c->red[w * NB + b];
+  return 1.0f / sqrtf(t / (float)S.d + S.eps);
 }
 
 // ---------------------------------------------------------------- GEMV slice
@@ -461,13 +477,13 @@ __device__ void stage_rmsnorm(const DevState& S, const float* h, const uint16_t*
 //    the page, 16 bytes per lane, four loads in flight, two accumulator chains;
 //  * slice_dot_smem (otherwise): 8-byte weight loads and 16-byte x loads, both
 //    contiguous across the warp (no bank conflicts), two accumulator chains.
-template <typename WT, int NB>
-__device__ __forceinline__ void slice_dot_xreg(const uint8_t* wp, const float (&xr)[NB][32], int nv, int lane,
+template <typename WT, int NB, int J>
+__device__ __forceinline__ void slice_dot_xreg(const uint8_t* wp, const float (&xr)[NB][8 * J], int nv, int lane,
                                                float (&acc)[NB]) {
   const uint4* w = reinterpret_cast<const uint4*>(wp);
-  uint4 wv[4];
+  uint4 wv[J];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < J; ++j) {
     const int v = lane + 32 * j;
     wv[j] = v < nv ? w[v] : make_uint4(0u, 0u, 0u, 0u);
   }
@@ -475,7 +491,7 @@ __device__ __forceinline__ void slice_dot_xreg(const uint8_t* wp, const float (&
 #pragma unroll
   for (int b = 0; b < NB; ++b) a0[b] = a1[b] = 0.f;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < J; ++j) {
     float f[8];
     Unpack<WT>::u8(wv[j], f);
 #pragma unroll
@@ -564,6 +580,15 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
       break;
   }
   consumer_sync();
+  if (tid == 0 && (A.flags & SF_TRACE)) c->tmark[0] = globaltimer_ns();
+  // the residual this thread adds in the epilogue (its first row), loaded now so the
+  // latency hides behind the pages
+  float hres = 0.f;
+  if ((in.op == OP_OPROJ || in.op == OP_DOWN) && tid < g.rows() * B) {
+    const int r = tid % g.rows(), b = tid / g.rows();
+    const float* hin = act_ptr(S, act, in.op == OP_OPROJ ? ACT_H : ACT_HMID, l);
+    hres = load_act<SYNC>(hin + (size_t)b * S.d + in.a[0] + r, S, c);
+  }
 
   // 2. stream the slices: warp w takes slice i0 + w of every page of 8 slices
   float* rowpart = scratch;  // [rows][spr][NB]
@@ -587,26 +612,37 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
     }
   };
   bool done = false;
-  if constexpr (NB <= 2) {
-    // slices i = 8c + w: when spr divides 8, warp w always sees slice w % spr of a row
-    if (kConsumerWarps % spr == 0 && g.WS <= 32 * 32) {
-      const int nv = g.WS >> 3, sw = warp % spr;
-      float xr[NB][32];
+  // slices i = 8c + w: when spr divides 8, warp w always sees slice w % spr of a row and
+  // keeps that segment of x in registers (J 16-byte vectors per lane)
+  auto run_xreg = [&](auto jtag) {
+    constexpr int J = decltype(jtag)::value;
+    const int nv = g.WS >> 3, sw = warp % spr;
+    float xr[NB][8 * J];
 #pragma unroll
-      for (int b = 0; b < NB; ++b)
+    for (int b = 0; b < NB; ++b)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int v = lane + 32 * j;
-          const float* xp = xbuf + (size_t)b * g.K + (size_t)sw * g.WS + v * 8;
-          float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
-          if (v < nv) {
-            x0 = reinterpret_cast<const float4*>(xp)[0];
-            x1 = reinterpret_cast<const float4*>(xp)[1];
-          }
-          xr[b][j * 8 + 0] = x0.x; xr[b][j * 8 + 1] = x0.y; xr[b][j * 8 + 2] = x0.z; xr[b][j * 8 + 3] = x0.w;
-          xr[b][j * 8 + 4] = x1.x; xr[b][j * 8 + 5] = x1.y; xr[b][j * 8 + 6] = x1.z; xr[b][j * 8 + 7] = x1.w;
+      for (int j = 0; j < J; ++j) {
+        const int v = lane + 32 * j;
+        const float* xp = xbuf + (size_t)b * g.K + (size_t)sw * g.WS + v * 8;
+        float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+        if (v < nv) {
+          x0 = reinterpret_cast<const float4*>(xp)[0];
+          x1 = reinterpret_cast<const float4*>(xp)[1];
         }
-      run_pages([&](const uint8_t* wp, int, float(&acc)[NB]) { slice_dot_xreg<WT, NB>(wp, xr, nv, lane, acc); });
+        xr[b][j * 8 + 0] = x0.x; xr[b][j * 8 + 1] = x0.y; xr[b][j * 8 + 2] = x0.z; xr[b][j * 8 + 3] = x0.w;
+        xr[b][j * 8 + 4] = x1.x; xr[b][j * 8 + 5] = x1.y; xr[b][j * 8 + 6] = x1.z; xr[b][j * 8 + 7] = x1.w;
+      }
+    run_pages([&](const uint8_t* wp, int, float(&acc)[NB]) { slice_dot_xreg<WT, NB, J>(wp, xr, nv, lane, acc); });
+  };
+  if constexpr (NB <= 2) {
+    if (kConsumerWarps % spr == 0 && g.WS <= 32 * 8 * 4) {
+      run_xreg(std::integral_constant<int, 4>{});
+      done = true;
+    }
+  }
+  if constexpr (NB == 1) {
+    if (!done && kConsumerWarps % spr == 0 && g.WS <= 32 * 8 * 8) {
+      run_xreg(std::integral_constant<int, 8>{});
       done = true;
     }
   }
@@ -615,6 +651,7 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
       slice_dot_smem<WT, NB>(wp, xbuf + (size_t)s * g.WS, g.K, g.WS, lane, acc);
     });
   consumer_sync();
+  if (tid == 0 && (A.flags & SF_TRACE)) c->tmark[1] = globaltimer_ns();
 
   // 3. finalize rows in a fixed order and apply the op's epilogue
   auto rowsum = [&](int r, int b) {
@@ -629,7 +666,8 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
       const int hd = S.hd, half = hd / 2;
       for (int t = tid; t < n * B; t += kConsumerThreads) {
         const int r = t % n, b = t / n;
-        float va = rowsum(r, b), vb = rowsum(r + n, b);
+        const float ir = inv_rms_of<NB>(S, c, b);
+        float va = rowsum(r, b) * ir, vb = rowsum(r + n, b) * ir;
         const int i = i0 + r;
         const int pos = A.pos[b];
         if (mat < 2) {  // rotate-half RoPE on the pair (i, i + hd/2)
@@ -662,7 +700,7 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
       for (int t = tid; t < R * B; t += kConsumerThreads) {
         const int r = t % R, b = t / R;
         const size_t idx = (size_t)b * S.d + row0 + r;
-        hout[idx] = load_act<SYNC>(hin + idx, S, c) + rowsum(r, b);
+        hout[idx] = (t == tid ? hres : load_act<SYNC>(hin + idx, S, c)) + rowsum(r, b);
       }
       break;
     }
@@ -671,7 +709,8 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
       float* a = act_ptr(S, act, ACT_A, l);
       for (int t = tid; t < n * B; t += kConsumerThreads) {
         const int r = t % n, b = t / n;
-        a[(size_t)b * S.F + row0 + r] = silu_f(rowsum(r, b)) * rowsum(r + n, b);
+        const float ir = inv_rms_of<NB>(S, c, b);
+        a[(size_t)b * S.F + row0 + r] = silu_f(rowsum(r, b) * ir) * (rowsum(r + n, b) * ir);
       }
       break;
     }
@@ -682,7 +721,7 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
       for (int t = tid; t < R * B; t += kConsumerThreads) {
         const int r = t % R, b = t / R;
         const size_t idx = (size_t)b * S.d + row0 + r;
-        hout[idx] = load_act<SYNC>(hin + idx, S, c) + rowsum(r, b);
+        hout[idx] = (t == tid ? hres : load_act<SYNC>(hin + idx, S, c)) + rowsum(r, b);
       }
       break;
     }
@@ -694,7 +733,7 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
       for (int t = tid; t < R * NB; t += kConsumerThreads) {
         const int r = t % R, b = t / R;
         if (b >= B) continue;
-        const float z = rowsum(r, b);
+        const float z = rowsum(r, b) * inv_rms_of<NB>(S, c, b);
         const int row = row0 + r;
         if (A.logits) A.logits[(size_t)b * S.V + row] = z;
         if (isnan(z)) atomicOr(&S.ctl->nan_seen, 1u);
@@ -747,6 +786,8 @@ __device__ __noinline__ void op_attn(const DevState& S, const StepArgs& A, const
       knew[t] = Unpack<WT>::round(load_act<SYNC>(kn + (t < HD ? t : (size_t)S.Hkv * HD + (t - HD)), S, c));
   }
   consumer_sync();
+  const bool mark = (A.flags & SF_TRACE) && tid == 0;
+  if (mark) c->tmark[0] = globaltimer_ns();
   // q in registers when it fits beside the accumulators, else read (broadcast) from smem
   constexpr bool QREG = G * DPL <= 32;
   constexpr int QG = QREG ? G : 1, QD = QREG ? DPL : 1;
@@ -850,6 +891,7 @@ __device__ __noinline__ void op_attn(const DevState& S, const StepArgs& A, const
   }
   if (at.has_new && warp == 0)  // position pos_b: the new key/value of this step
     update(pgi == 0, knew + dl * DPL, knew + HD + dl * DPL);
+  if (mark) c->tmark[1] = globaltimer_ns();
   // combine the position groups of the warp (same running max), then the warps
 #pragma unroll
   for (int g = 0; g < G; ++g) {
@@ -896,20 +938,63 @@ __device__ __noinline__ void op_attn(const DevState& S, const StepArgs& A, const
   }
 }
 
-// log-sum-exp merge of the S split partials of one (sequence, kv head) (§8.2 ATTN_REDUCE)
+// log-sum-exp merge of the S split partials of one (sequence, kv head) (§8.2 ATTN_REDUCE).
+// The (b, j) block of partials is contiguous: one bulk copy into the x buffer when it
+// fits (the caller has acquired the partials), else loads batched eight splits deep.
 template <int SYNC>
-__device__ __noinline__ void op_attn_reduce(const DevState& S, const Instr& in, int B, SmemCtl* c, float* scratch, float* act) {
+__device__ __noinline__ void op_attn_reduce(const DevState& S, const Instr& in, int B, SmemCtl* c, float* xbuf,
+                                            float* scratch, Ring& ring, float* act) {
   const int tid = threadIdx.x;
   const int b = in.a[0], j = in.a[1], l = in.layer;
   if (b >= B) return;  // uniform over the CTA
   const int HD = S.hd, G = S.Hq / S.Hkv, RW = HD + 2, NS = S.S;
   const float* part = act_ptr(S, act, ACT_PART, l) + ((size_t)b * S.Hkv + j) * NS * G * RW;
+  float* out = act_ptr(S, act, ACT_O, l) + (size_t)b * S.Hq * HD + (size_t)j * G * HD;
+  const uint32_t bytes = (uint32_t)NS * G * RW * 4u;
+  // a bulk copy needs a 16-byte aligned start and a 16-byte multiple size
+  if ((int)bytes <= S.xbuf_bytes && (bytes & 15u) == 0 && (reinterpret_cast<uintptr_t>(part) & 15u) == 0) {
+    if (tid == 0) {
+      fence_proxy_async();
+      mbar_arrive_expect_tx(&c->xbar, bytes);
+      tma_load_1d_plain(xbuf, part, bytes, &c->xbar);
+    }
+    if (!mbar_try_wait(&c->xbar, ring.xph)) {
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(&c->xbar, ring.xph)) {
+        if (globaltimer_ns() - t0 > (uint64_t)S.timeout_ns) {
+          set_err(S, 4u, -10, -1);
+          c->abort = 1;
+          break;
+        }
+      }
+    }
+    ring.xph ^= 1u;
+    if (SYNC == SYNC_SENTINEL) {
+      for (int i = tid; i < NS * G * RW; i += kConsumerThreads)
+        if (isnan(xbuf[i])) xbuf[i] = poll_slow(part + i, S, c);
+    }
+    consumer_sync();
+    for (int t = tid; t < G * HD; t += kConsumerThreads) {
+      const int g = t / HD, e = t - g * HD;
+      float M = -CUDART_INF_F;
+      for (int s = 0; s < NS; ++s) M = fmaxf(M, xbuf[(s * G + g) * RW + HD]);
+      float num = 0.f, den = 0.f;
+      for (int s = 0; s < NS; ++s) {
+        const float* ps = xbuf + (s * G + g) * RW;
+        if (ps[HD] == -CUDART_INF_F) continue;
+        const float w = exp2f(ps[HD] - M);
+        num = fmaf(w, ps[e], num);
+        den = fmaf(w, ps[HD + 1], den);
+      }
+      out[t] = num / den;
+    }
+    return;
+  }
   for (int t = tid; t < NS * G; t += kConsumerThreads) {
     scratch[2 * t] = load_act<SYNC>(part + (size_t)t * RW + HD, S, c);
     scratch[2 * t + 1] = load_act<SYNC>(part + (size_t)t * RW + HD + 1, S, c);
   }
   consumer_sync();
-  float* out = act_ptr(S, act, ACT_O, l) + (size_t)b * S.Hq * HD + (size_t)j * G * HD;
   constexpr int U = 8;  // splits whose partial outputs are in flight together
   for (int t = tid; t < G * HD; t += kConsumerThreads) {
     const int g = t / HD, e = t - g * HD;
@@ -999,7 +1084,10 @@ __device__ void consumer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8
     const Instr in = load_instr(A.instr + pc);
     if (in.op == OP_END) break;
     uint64_t t_fetch = 0, t_ready = 0;
-    if (TRACE) t_fetch = globaltimer_ns();
+    if (TRACE) {
+      t_fetch = globaltimer_ns();
+      if (tid == 0) c->tmark[0] = c->tmark[1] = c->tmark[2] = c->tmark[3] = 0ull;
+    }
     // ---- wait for the dependency (counter mode; sentinel mode polls the data itself)
     const bool use_ctr = (SYNC == SYNC_COUNTER || in.op >= OP_T_NOP) && !nosync;
     if (use_ctr && in.wait_ctr >= 0) {
@@ -1044,7 +1132,7 @@ __device__ void consumer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8
           op_attn<WT, SYNC, 64, 1>(S, A, in, c, pages, xbuf, scratch, ring, act);
         break;
       case OP_ATTN_REDUCE:
-        op_attn_reduce<SYNC>(S, in, A.B, c, scratch, act);
+        op_attn_reduce<SYNC>(S, in, A.B, c, xbuf, scratch, ring, act);
         break;
       case OP_T_ORDER:
       case OP_T_PRODUCE:
@@ -1076,12 +1164,14 @@ __device__ void consumer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8
       // that brings the count to S merges the splits, then signals the O-proj counter
       bool last = false;
       if (tid == 0) {
+        if (TRACE) c->tmark[2] = globaltimer_ns();
         const uint32_t old = atom_acq_rel_add_u32(&S.counters[in.a[4]], 1u);
         last = (old + 1u == (A.epoch + 1u) * (uint32_t)in.a[3]);
       }
       if (consumer_sync_or(last)) {
-        op_attn_reduce<SYNC>(S, in, A.B, c, scratch, act);
+        op_attn_reduce<SYNC>(S, in, A.B, c, xbuf, scratch, ring, act);
         if (consumer_sync_or(c->abort)) break;
+        if (TRACE && tid == 0) c->tmark[3] = globaltimer_ns();
       } else {
         signal = false;
       }
@@ -1117,6 +1207,7 @@ __device__ void consumer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8
         rec.layer = in.layer;
         rec.t_fetch = t_fetch;
         rec.t_ready = t_ready;
+        for (int k = 0; k < 4; ++k) rec.t_mark[k] = c->tmark[k];
         rec.t_end = globaltimer_ns();
         S.trace[k] = rec;
       }

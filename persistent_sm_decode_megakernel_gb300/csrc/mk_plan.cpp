@@ -45,7 +45,7 @@ std::string make_geometry(const ModelShape& m, int n_cta, int page_bytes, int n_
   const int G = m.Hq / m.Hkv;
   if (m.hd != 64 && m.hd != 128) return "head_dim must be 64 or 128";
   if (G != 1 && G != 2 && G != 4) return "n_heads / n_kv_heads must be 1, 2 or 4";
-  g->page_bytes = page_bytes > 0 ? page_bytes : 16384;
+  g->page_bytes = page_bytes > 0 ? page_bytes : 32768;
   if ((g->page_bytes & (g->page_bytes - 1)) || g->page_bytes < 4096 || g->page_bytes > 32768)
     return "page_bytes must be a power of two in [4096, 32768]";
   if (g->page_bytes < 64 * m.hd) return fmt("page_bytes must be at least 64 * head_dim = %lld", 64LL * m.hd);
@@ -142,22 +142,43 @@ std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B,
     // RMSNORM_QKV_ROPE: rotate-half pairs (i, i + hd/2) stay in one instruction
     const int c_qkv = new_ctr();
     {
-      const long long pairs = (long long)(m.Hq + 2 * m.Hkv) * half;
+      const int heads = m.Hq + 2 * m.Hkv;
+      const long long pairs = (long long)heads * half;
       const int cap = std::max(1, rows_cap(m.d, g.ws_qkv, 1) / 2);
-      for (int c = 0; c < n_cta; ++c) {
-        long long p0 = split_lo(pairs, n_cta, c);
-        const long long p1 = split_lo(pairs, n_cta, c + 1);
-        while (p0 < p1) {
-          const int hh = (int)(p0 / half);
-          const long long seg_end = std::min<long long>(p1, (long long)(hh + 1) * half);
-          const int n = (int)std::min<long long>(seg_end - p0, cap);
-          Instr in = mk_instr(OP_QKV, l, prev, 0, c_qkv);
-          in.a[0] = hh < m.Hq ? 0 : (hh < m.Hq + m.Hkv ? 1 : 2);
-          in.a[1] = hh < m.Hq ? hh : (hh < m.Hq + m.Hkv ? hh - m.Hq : hh - m.Hq - m.Hkv);
-          in.a[2] = (int)(p0 % half);
-          in.a[3] = n;
-          emit(c, in);
-          p0 += n;
+      auto emit_qkv = [&](int c, int hh, int i0, int n) {
+        Instr in = mk_instr(OP_QKV, l, prev, 0, c_qkv);
+        in.a[0] = hh < m.Hq ? 0 : (hh < m.Hq + m.Hkv ? 1 : 2);
+        in.a[1] = hh < m.Hq ? hh : (hh < m.Hq + m.Hkv ? hh - m.Hq : hh - m.Hq - m.Hkv);
+        in.a[2] = i0;
+        in.a[3] = n;
+        emit(c, in);
+      };
+      if (n_cta >= heads) {
+        // each head to its own group of CTAs: every CTA gets exactly one instruction (a
+        // pair range crossing a head would cost a second one, with its own staging)
+        for (int hh = 0; hh < heads; ++hh) {
+          const int c0 = split_lo(n_cta, heads, hh), c1 = split_lo(n_cta, heads, hh + 1);
+          for (int c = c0; c < c1; ++c) {
+            int i0 = split_lo(half, c1 - c0, c - c0);
+            const int i1 = split_lo(half, c1 - c0, c - c0 + 1);
+            while (i0 < i1) {
+              const int n = std::min(i1 - i0, cap);
+              emit_qkv(c, hh, i0, n);
+              i0 += n;
+            }
+          }
+        }
+      } else {
+        for (int c = 0; c < n_cta; ++c) {
+          long long p0 = split_lo(pairs, n_cta, c);
+          const long long p1 = split_lo(pairs, n_cta, c + 1);
+          while (p0 < p1) {
+            const int hh = (int)(p0 / half);
+            const long long seg_end = std::min<long long>(p1, (long long)(hh + 1) * half);
+            const int n = (int)std::min<long long>(seg_end - p0, cap);
+            emit_qkv(c, hh, (int)(p0 % half), n);
+            p0 += n;
+          }
         }
       }
     }

@@ -32,10 +32,22 @@ def summarize(trace):
     by = {}
     per_cta_wait = {}
     groups = {}
-    for cta, pc, op, layer, tf, tr, te in trace:
-        d = by.setdefault(OPS.get(op, str(op)), {"wait": [], "work": []})
+    for cta, pc, op, layer, tf, tr, te, m0, m1, m2, m3 in trace:
+        d = by.setdefault(OPS.get(op, str(op)), {"wait": [], "work": [], "stage": [], "pages": [], "epi": [],
+                                                 "write": [], "arrive": [], "merge": []})
         d["wait"].append((tr - tf) / 1e3)
         d["work"].append((te - tr) / 1e3)
+        if m0 and m1:
+            d["stage"].append((m0 - tr) / 1e3)
+            d["pages"].append((m1 - m0) / 1e3)
+            if m2:   # attention: partial written, then the arrival (and the merge)
+                d["write"].append((m2 - m1) / 1e3)
+                if m3:
+                    d["merge"].append((m3 - m2) / 1e3)
+                else:
+                    d["arrive"].append((te - m2) / 1e3)
+            else:
+                d["epi"].append((te - m1) / 1e3)
         per_cta_wait[cta] = per_cta_wait.get(cta, 0.0) + (tr - tf) / 1e3
         g = groups.setdefault((layer, op), [tf, te])
         g[0] = min(g[0], tf)
@@ -45,6 +57,9 @@ def summarize(trace):
         out["ops"][k] = {"n": len(d["work"]), "wait_us_mean": statistics.mean(d["wait"]),
                          "work_us_mean": statistics.mean(d["work"]), "work_us_max": max(d["work"]),
                          "wait_us_per_cta": sum(d["wait"]) / len(ctas)}
+        for key in ("stage", "pages", "epi", "write", "arrive", "merge"):
+            if d[key]:
+                out["ops"][k][key + "_us"] = statistics.mean(d[key])
     out["wait_share_mean"] = statistics.mean(v / span for v in per_cta_wait.values())
     items = sorted(groups.items(), key=lambda kv: kv[1][0])
     out["timeline_us"] = {f"L{l}:{OPS.get(o, o)}": [round((a - t0) / 1e3, 2), round((b - t0) / 1e3, 2)]
