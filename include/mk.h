@@ -91,6 +91,10 @@ typedef struct {
   int fault_drop_signal;  /* test hook: k > 0 removes the k-th counter signal from the
                              schedule and skips the host-side validator, so that the
                              device wait must time out (fault injection on the host)     */
+  int l2_prefetch_kb;     /* loader prefetches upcoming weight/KV ranges into L2 this far
+                             ahead of its page loads, per CTA (0: default 256; < 0: off) */
+  int split_min_positions; /* a step uses as many KV splits (up to kv_splits) as give each
+                              at least this many positions (0: default 16)               */
 } mk_options;
 
 typedef struct {

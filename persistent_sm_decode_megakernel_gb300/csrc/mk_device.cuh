@@ -63,6 +63,10 @@ __device__ __forceinline__ void tma_load_1d_plain(void* dst, const void* src, ui
                "l"(src), "r"(bytes), "r"(smem_addr(bar))
                : "memory");
 }
+// one 128-byte line of global memory into L2 (load/store path, not the TMA unit)
+__device__ __forceinline__ void prefetch_l2_line(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 // orders this thread's (acquired) generic-proxy view of memory -- global data published
 // by other SMs, shared memory last written by ordinary stores -- before its following
 // async-proxy (TMA) accesses

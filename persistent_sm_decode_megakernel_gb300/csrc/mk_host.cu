@@ -446,6 +446,8 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
   S.sync_mode = o.sync_mode;
   S.timeout_ns = (int64_t)(o.wait_timeout_s * 1e9);
   S.backoff_max_ns = o.backoff_max_ns;
+  S.l2_prefetch_bytes = o.l2_prefetch_kb < 0 ? 0 : (o.l2_prefetch_kb == 0 ? 256 : o.l2_prefetch_kb) * 1024;
+  S.split_min_positions = o.split_min_positions > 0 ? o.split_min_positions : 16;
   ModelPtrs& mp = ctx->ptrs;
   mp.final_norm = w->final_norm;
   mp.lm_head = w->lm_head;
@@ -839,7 +841,7 @@ mk_status mk_barrier_bench(int mode, int n_barriers, double* us_per_barrier) {
 
 mk_status mk_stream_bench(int page_bytes, int n_pages, int mode, int hint, long long total_bytes, double* gbps) {
   if (!gbps || page_bytes < 1024 || page_bytes > 65536 || (page_bytes & 15) || n_pages < 1 || n_pages > kMaxPages ||
-      mode < 0 || mode > 3 || total_bytes < (1LL << 20) || (mode >= 2 && page_bytes != 16384))
+      mode < 0 || mode > 5 || total_bytes < (1LL << 20) || (mode >= 2 && page_bytes != 32768))
     return fail(MK_ERR_INVALID, "stream bench: bad arguments");
   int dev = 0, n_sm = 0;
   MK_CUDA(cudaGetDevice(&dev));

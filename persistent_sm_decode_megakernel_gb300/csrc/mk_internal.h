@@ -12,7 +12,9 @@ namespace mk {
 
 constexpr int kMaxBatch = 16;
 constexpr int kConsumerWarps = 8;                 // compute warps per CTA
-constexpr int kThreads = 32 * (kConsumerWarps + 1);  // + one producer (TMA) warp
+constexpr int kThreads = 32 * (kConsumerWarps + 2);  // + the loader (TMA) warp + the L2 prefetch warp
+constexpr int kLoaderWarp = kConsumerWarps;
+constexpr int kPrefetchWarp = kConsumerWarps + 1;
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kMaxPages = 16;
 
@@ -132,6 +134,8 @@ struct DevState {
   int sync_mode;
   int64_t timeout_ns;
   int backoff_max_ns;
+  int l2_prefetch_bytes;       // loader's L2 prefetch window ahead of its page loads (0: off)
+  int split_min_positions;     // a KV split of a step covers at least this many positions
   // self-test buffers
   int64_t* test_buf;
   int64_t test_len;

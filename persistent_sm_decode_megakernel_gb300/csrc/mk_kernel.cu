@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_stream_kernel(const uint8_t* s
   const uint8_t* base = src + (long long)blockIdx.x * bytes_per_cta;
   const uint64_t t0 = globaltimer_ns();
   const uint64_t limit = 2000000000ull;
+  if (warp > kConsumerWarps) return;  // this benchmark has no prefetch warp
   if (warp == kConsumerWarps) {
     if (lane != 0) return;
     const uint64_t pol = l2_evict_first_policy();
@@ -103,6 +104,10 @@ __global__ void __launch_bounds__(kThreads, 1) mk_stream_kernel(const uint8_t* s
     return;
   }
   float acc = 0.f;
+  __shared__ float lanep[8 * kThreads];
+  float xr[1][64];
+#pragma unroll
+  for (int j = 0; j < 64; ++j) xr[0][j] = (mode == 2 || mode >= 4) ? x[(lane + 32 * (j / 8)) * 8 + (j & 7)] : 0.f;
   for (long long c = 0; c < n; ++c) {
     const int slot = (int)(c % n_pages);
     const uint32_t ph = (uint32_t)((c / n_pages) & 1);
@@ -121,16 +126,36 @@ __global__ void __launch_bounds__(kThreads, 1) mk_stream_kernel(const uint8_t* s
       const uint8_t* wp = pages + (size_t)slot * page_bytes + (size_t)warp * ws * 2;
       float a[1];
       if (mode == 2) {
-        float xr[1][32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) xr[0][j] = x[(lane + 32 * (j / 8)) * 8 + (j & 7)];
-        slice_dot_xreg<__half, 1, 4>(wp, xr, ws / 8, lane, a);
+        slice_dot_xreg<__half, 1, 8>(wp, xr, ws / 8, lane, a);
       } else {
         slice_dot_smem<__half, 1>(wp, x, ws, ws, lane, a);
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) a[0] += __shfl_xor_sync(0xffffffffu, a[0], o);
       acc += a[0];
+    }
+    if (mode == 4 || mode == 5) {  // four accumulator chains; 4: lane partial to smem, 5: shuffles
+      const uint4* w = reinterpret_cast<const uint4*>(pages + (size_t)slot * page_bytes + (size_t)warp * ws * 2);
+      uint4 wv[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) wv[j] = w[lane + 32 * j];
+      float a4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float f[8];
+        Unpack<__half>::u8(wv[j], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a4[(j * 8 + e) & 3] = fmaf(f[e], xr[0][j * 8 + e], a4[(j * 8 + e) & 3]);
+      }
+      float t = (a4[0] + a4[1]) + (a4[2] + a4[3]);
+      if (mode == 5) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        acc += t;
+      } else {
+        lanep[(c & 7) * kThreads + warp * 32 + lane] = t;
+        acc += t;
+      }
     }
     if (mode == 1) {
       const uint4* w = reinterpret_cast<const uint4*>(pages + (size_t)slot * page_bytes + (size_t)warp * ws * 2);

@@ -31,6 +31,7 @@ struct SmemCtl {
   int last_issue_phase[kMaxPages];
   uint64_t xbar;  // completion of the x-buffer bulk copy
   uint64_t tmark[4];  // journal marks inside an op
+  volatile long long loaded;  // bytes the loader has issued as pages (paces the L2 prefetch)
   volatile int abort;
 };
 static_assert(sizeof(SmemCtl) <= kCtlSmem, "control block fits");
@@ -172,17 +173,26 @@ __device__ __forceinline__ Gemv make_gemv(const DevState& S, const Instr& in) {
 // the split holding position pos_b takes the new key/value from the QKV op's fp32 copy.
 struct Attn {
   int b, j, s, nsp, t0, t1, n_cached, pb, nblocks;
-  bool has_new;
+  bool has_new, active;
   const uint16_t* kb;
   const uint16_t* vb;
 };
+// Splits in use this step: at least split_min_positions positions per split, at most the
+// schedule's S -- short contexts use a few splits (cheap merge), long contexts all.
+__device__ __forceinline__ int active_splits(const DevState& S, const StepArgs& A, int b) {
+  const int npos = A.pos[b] + 1;
+  const int pmin = S.split_min_positions;
+  return max(1, min(S.S, (npos + pmin - 1) / pmin));
+}
 __device__ __forceinline__ Attn make_attn(const DevState& S, const StepArgs& A, const Instr& in) {
   Attn a;
   a.b = in.a[0];
   a.j = in.a[1];
   a.s = in.a[2];
-  a.nsp = in.a[3];
-  const int npos = A.pos[a.b] + 1;
+  a.active = a.b < A.B;
+  const int npos = a.active ? A.pos[a.b] + 1 : 1;
+  a.nsp = a.active ? active_splits(S, A, a.b) : 1;
+  a.active = a.active && a.s < a.nsp;
   a.t0 = (int)((int64_t)a.s * npos / a.nsp);
   a.t1 = (int)((int64_t)(a.s + 1) * npos / a.nsp);
   const int tc = min(a.t1, npos - 1);
@@ -190,7 +200,7 @@ __device__ __forceinline__ Attn make_attn(const DevState& S, const StepArgs& A, 
   a.has_new = (a.t1 == npos);
   a.pb = S.page_bytes / (S.hd * 2);
   a.nblocks = (a.n_cached + a.pb - 1) / a.pb;
-  if (a.b >= A.B) {  // no such sequence in this step
+  if (!a.active) {  // no such sequence, or a split beyond this step's count
     a.n_cached = 0;
     a.nblocks = 0;
     a.has_new = false;
@@ -204,6 +214,46 @@ __device__ __forceinline__ float* act_ptr(const DevState& S, float* act, int kin
   return act + S.act_off[kind] + (int64_t)layer * S.act_stride[kind];
 }
 
+
+// The weight / KV byte ranges an instruction's pages will cover (at most two).
+struct Ranges {
+  const uint16_t* p[2];
+  uint32_t bytes[2];
+  int n;
+};
+__device__ __forceinline__ Ranges instr_ranges(const DevState& S, const StepArgs& A, const Instr& in) {
+  Ranges r;
+  r.n = 0;
+  switch (in.op) {
+    case OP_QKV:
+    case OP_OPROJ:
+    case OP_UPGATE:
+    case OP_DOWN:
+    case OP_LMHEAD: {
+      const Gemv g = make_gemv(S, in);
+      for (int k = 0; k < 2; ++k)
+        if (g.segr[k] > 0) {
+          r.p[r.n] = g.seg[k];
+          r.bytes[r.n] = (uint32_t)g.segr[k] * (uint32_t)g.K * 2u;
+          ++r.n;
+        }
+      break;
+    }
+    case OP_ATTN: {
+      const Attn at = make_attn(S, A, in);
+      if (at.n_cached > 0) {
+        r.p[0] = at.kb;
+        r.p[1] = at.vb;
+        r.bytes[0] = r.bytes[1] = (uint32_t)at.n_cached * S.hd * 2u;
+        r.n = 2;
+      }
+      break;
+    }
+    default:
+      break;
+  }
+  return r;
+}
 
 // ---------------------------------------------------------------- loader warp
 __device__ bool producer_acquire(const DevState& S, SmemCtl* c, int slot, uint32_t ph) {
@@ -233,6 +283,7 @@ __device__ __noinline__ void producer(const DevState& S, const StepArgs& A, Smem
   const int cta = blockIdx.x;
   const int end = A.q_start[cta + 1];
   bool ok = true;
+  long long loaded = 0;
   for (int pc = A.q_start[cta]; pc < end && ok; ++pc) {
     const Instr in = load_instr(A.instr + pc);
     if (pc + 2 < end) prefetch_l1(A.instr + pc + 2);  // the next instructions, for both roles
@@ -267,6 +318,8 @@ __device__ __noinline__ void producer(const DevState& S, const StepArgs& A, Smem
             break;
           }
           const int i1 = min(ns, i0 + kConsumerWarps);
+          loaded += (long long)(i1 - i0) * sb;
+          c->loaded = loaded;
           mbar_arrive_expect_tx(&c->full[slot], (uint32_t)(i1 - i0) * sb);
           uint8_t* dst = pages + (size_t)slot * S.page_bytes;
           if (i0 < n0) {
@@ -294,6 +347,8 @@ __device__ __noinline__ void producer(const DevState& S, const StepArgs& A, Smem
               ok = false;
               break;
             }
+            loaded += bytes;
+            c->loaded = loaded;
             mbar_arrive_expect_tx(&c->full[slot], bytes);
             tma_load_1d(pages + (size_t)slot * S.page_bytes, (kv ? at.vb : at.kb) + (size_t)p0 * S.hd, bytes,
                         &c->full[slot], pol);
@@ -341,6 +396,38 @@ __device__ __noinline__ void producer(const DevState& S, const StepArgs& A, Smem
       if (globaltimer_ns() - t0 > (uint64_t)S.timeout_ns) {
         set_err(S, 5u /*MK_ERR_STATE: page never released*/, -5, s);
         return;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- L2 prefetch warp
+// Walks the CTA's queue ahead of the loader and pulls the weight / KV lines of upcoming
+// instructions into L2 (one line per lane, 4 KB per warp instruction), staying at most
+// l2_prefetch_bytes ahead of what the loader has issued.  The page ring holds only a few
+// microseconds of the stream; L2 (129 MB) lets HBM keep streaming while the compute warps
+// sit in dependency waits, staging and epilogues.  It uses the load/store path, so it
+// never queues in front of the loader's TMA copies.
+__device__ __noinline__ void l2_prefetcher(const DevState& S, const StepArgs& A, SmemCtl* c) {
+  if (S.l2_prefetch_bytes <= 0) return;
+  const int lane = threadIdx.x & 31;
+  const int cta = blockIdx.x, end = A.q_start[cta + 1];
+  long long issued = 0;
+  const uint64_t t0 = globaltimer_ns();
+  for (int pc = A.q_start[cta]; pc < end; ++pc) {
+    const Instr in = load_instr(A.instr + pc);
+    if (in.op == OP_END) break;
+    const Ranges r = instr_ranges(S, A, in);
+    for (int k = 0; k < r.n; ++k) {
+      const char* p = reinterpret_cast<const char*>(r.p[k]);
+      for (uint32_t off = 0; off < r.bytes[k]; off += 32u * 128u) {
+        while (issued - c->loaded >= (long long)S.l2_prefetch_bytes) {
+          if (c->abort || globaltimer_ns() - t0 > (uint64_t)S.timeout_ns) return;
+          __nanosleep(256);
+        }
+        const uint32_t o = off + (uint32_t)lane * 128u;
+        if (o < r.bytes[k]) prefetch_l2_line(p + o);
+        issued += min(32u * 128u, r.bytes[k] - off);
       }
     }
   }
@@ -771,7 +858,7 @@ __device__ __noinline__ void op_attn(const DevState& S, const StepArgs& A, const
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int dl = lane & (LPP - 1), pgi = lane / LPP;
   const Attn at = make_attn(S, A, in);
-  if (at.b >= A.B) return;  // uniform over the CTA
+  if (!at.active) return;  // uniform over the CTA
   const int l = in.layer;
   const float qscale = (1.0f / sqrtf((float)HD)) * 1.4426950408889634f;  // scores in log2 units
 
@@ -873,15 +960,15 @@ __device__ __noinline__ void op_attn(const DevState& S, const StepArgs& A, const
     }
   };
 
-  const int ppw = at.pb / kConsumerWarps;  // positions per warp per page
   for (int blk = 0; blk < at.nblocks; ++blk) {
     const int np = min(at.pb, at.n_cached - blk * at.pb);
     const uint8_t* kp = page_wait(S, c, pages, ring);
     Ring rv = ring;
     if (++rv.slot == S.n_pages) { rv.slot = 0; rv.ph ^= 1u; }
     const uint8_t* vp = page_wait(S, c, pages, rv);
-    for (int ps = 0; ps < ppw; ps += NGRP) {
-      const int t = warp * ppw + ps + pgi;
+    // the block's valid positions dealt over (warp, lane group); the bound is uniform
+    for (int base = 0; base < np; base += kConsumerWarps * NGRP) {
+      const int t = base + warp * NGRP + pgi;
       const bool valid = t < np;
       const size_t off = (size_t)(valid ? t : 0) * HD * 2 + dl * DPL * 2;
       update(valid, reinterpret_cast<const uint16_t*>(kp + off), reinterpret_cast<const uint16_t*>(vp + off));
@@ -942,13 +1029,14 @@ __device__ __noinline__ void op_attn(const DevState& S, const StepArgs& A, const
 // The (b, j) block of partials is contiguous: one bulk copy into the x buffer when it
 // fits (the caller has acquired the partials), else loads batched eight splits deep.
 template <int SYNC>
-__device__ __noinline__ void op_attn_reduce(const DevState& S, const Instr& in, int B, SmemCtl* c, float* xbuf,
-                                            float* scratch, Ring& ring, float* act) {
+__device__ __noinline__ void op_attn_reduce(const DevState& S, const StepArgs& A, const Instr& in, SmemCtl* c,
+                                            float* xbuf, float* scratch, Ring& ring, float* act) {
   const int tid = threadIdx.x;
   const int b = in.a[0], j = in.a[1], l = in.layer;
-  if (b >= B) return;  // uniform over the CTA
-  const int HD = S.hd, G = S.Hq / S.Hkv, RW = HD + 2, NS = S.S;
-  const float* part = act_ptr(S, act, ACT_PART, l) + ((size_t)b * S.Hkv + j) * NS * G * RW;
+  if (b >= A.B) return;  // uniform over the CTA
+  const int HD = S.hd, G = S.Hq / S.Hkv, RW = HD + 2;
+  const int NS = active_splits(S, A, b);  // splits s < NS wrote partials this step
+  const float* part = act_ptr(S, act, ACT_PART, l) + ((size_t)b * S.Hkv + j) * S.S * G * RW;
   float* out = act_ptr(S, act, ACT_O, l) + (size_t)b * S.Hq * HD + (size_t)j * G * HD;
   const uint32_t bytes = (uint32_t)NS * G * RW * 4u;
   // a bulk copy needs a 16-byte aligned start and a 16-byte multiple size
@@ -1132,7 +1220,7 @@ __device__ void consumer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8
           op_attn<WT, SYNC, 64, 1>(S, A, in, c, pages, xbuf, scratch, ring, act);
         break;
       case OP_ATTN_REDUCE:
-        op_attn_reduce<SYNC>(S, in, A.B, c, xbuf, scratch, ring, act);
+        op_attn_reduce<SYNC>(S, A, in, c, xbuf, scratch, ring, act);
         break;
       case OP_T_ORDER:
       case OP_T_PRODUCE:
@@ -1169,7 +1257,7 @@ __device__ void consumer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8
         last = (old + 1u == (A.epoch + 1u) * (uint32_t)in.a[3]);
       }
       if (consumer_sync_or(last)) {
-        op_attn_reduce<SYNC>(S, in, A.B, c, xbuf, scratch, ring, act);
+        op_attn_reduce<SYNC>(S, A, in, c, xbuf, scratch, ring, act);
         if (consumer_sync_or(c->abort)) break;
         if (TRACE && tid == 0) c->tmark[3] = globaltimer_ns();
       } else {
@@ -1198,6 +1286,7 @@ __device__ void consumer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8
       red_release_add_u32(&S.counters[in.signal_ctr], 1u);
     }
     if (TRACE && tid == 0) {
+      const uint64_t t_end = globaltimer_ns();
       const uint32_t k = atomicAdd(&S.ctl->trace_n, 1u);
       if ((int)k < S.trace_cap) {
         TraceRec rec;
@@ -1208,7 +1297,7 @@ __device__ void consumer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8
         rec.t_fetch = t_fetch;
         rec.t_ready = t_ready;
         for (int k = 0; k < 4; ++k) rec.t_mark[k] = c->tmark[k];
-        rec.t_end = globaltimer_ns();
+        rec.t_end = t_end;
         S.trace[k] = rec;
       }
     }
@@ -1235,6 +1324,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
       c->last_issue_phase[i] = -1;
     }
     c->abort = 0;
+    c->loaded = 0;
     mbar_fence_init();
   }
   if (tid < kMaxBatch) c->best[tid] = 0ull;
@@ -1251,7 +1341,9 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
   }
   __syncthreads();
   if (tid >= kConsumerThreads) {
-    if (tid == kConsumerThreads) producer(S, A, c, pages);
+    const int w = tid >> 5;
+    if (w == kLoaderWarp && (tid & 31) == 0) producer(S, A, c, pages);
+    if (w == kPrefetchWarp) l2_prefetcher(S, A, c);
     return;
   }
   consumer<WT, SYNC>(S, A, c, pages, xbuf, scratch);

@@ -71,11 +71,12 @@ class Decoder:
     """A context over a DeviceModel (mk_create ... mk_destroy)."""
 
     def __init__(self, dm: DeviceModel, sync_mode=0, exec_mode=0, trace=0, timeout_s=2.0, page_bytes=0,
-                 n_pages=0, kv_splits=0, max_ctas=0, fault_drop_signal=0, backoff_max_ns=0, stream=None):
+                 n_pages=0, kv_splits=0, max_ctas=0, fault_drop_signal=0, backoff_max_ns=0, l2_prefetch_kb=0,
+                 split_min_positions=0, stream=None):
         self.dm = dm
         self.stream = stream if stream is not None else torch.cuda.current_stream(dm.device)
         self.opts = mk_options(sync_mode, exec_mode, page_bytes, n_pages, kv_splits, trace, timeout_s,
-                               backoff_max_ns, max_ctas, fault_drop_signal)
+                               backoff_max_ns, max_ctas, fault_drop_signal, l2_prefetch_kb, split_min_positions)
         d = dm.desc()
         w, kv, _keep = dm.abi_structs()
         h = ctypes.c_void_p()

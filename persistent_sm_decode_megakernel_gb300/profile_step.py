@@ -80,6 +80,8 @@ def main():
     ap.add_argument("--page-bytes", type=int, default=0)
     ap.add_argument("--n-pages", type=int, default=0)
     ap.add_argument("--backoff", type=int, default=0)
+    ap.add_argument("--l2-prefetch-kb", type=int, default=0)
+    ap.add_argument("--split-min", type=int, default=0)
     ap.add_argument("--json", default="")
     args = ap.parse_args()
 
@@ -98,7 +100,8 @@ def main():
     with torch.cuda.stream(stream):
         dec = Decoder(dm, sync_mode=0 if args.sync == "counter" else 1,
                       exec_mode=0 if args.exec == "persistent" else 1, trace=1 if args.trace else 0,
-                      page_bytes=args.page_bytes, n_pages=args.n_pages, backoff_max_ns=args.backoff, stream=stream)
+                      page_bytes=args.page_bytes, n_pages=args.n_pages, backoff_max_ns=args.backoff,
+                      l2_prefetch_kb=args.l2_prefetch_kb, split_min_positions=args.split_min, stream=stream)
         prompt = synth.gen_prompts(cfg, B, args.prompt)
         tok = dec.prefill(prompt)
         pos = args.prompt

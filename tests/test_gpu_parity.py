@@ -223,3 +223,19 @@ def test_2b_fp16_full_prompt_teacher_forced(lib):
     z, tg = gpu_teacher_forced(dec, prompt, toks, n_new, cfg.vocab)
     dec.close()
     assert_parity(z, tg, zref, toks, P)
+
+
+@pytest.mark.parametrize("page_bytes", [0, 8192])
+def test_tiny_long_context_many_splits(lib, tiny, page_bytes):
+    """A 600-position context: the step uses several KV splits (one page of positions
+    each, up to the schedule's count), merged in the last-arriving split."""
+    cfg, w, m = tiny
+    P, n_new = 600, 4
+    prompt = synth.gen_prompts(cfg, 1, P)
+    toks, zref = oracle_run(cfg, w, prompt, n_new, model=m)
+    for sync in (0, 1):
+        dm = lib.DeviceModel(cfg, w, max_batch=1, max_ctx=P + n_new)
+        dec = lib.Decoder(dm, sync_mode=sync, page_bytes=page_bytes)
+        z, tg = gpu_teacher_forced(dec, prompt, toks, n_new, cfg.vocab)
+        dec.close()
+        assert_parity(z, tg, zref, toks, P)
