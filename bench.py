@@ -144,6 +144,13 @@ def aggregate_max(seconds, world, device=None):
     return float(t.item())
 
 
+def job_rate(units, seconds, world, device=None):
+    """Whole-job throughput of `world` replicas that each processed `units` in their own
+    `seconds`: all units over the slowest rank's time.  Returns (rate, max seconds)."""
+    t = aggregate_max(seconds, world, device)
+    return world * units / t, t
+
+
 def barrier(world, device=None):
     if world > 1:
         import torch.distributed as dist
@@ -283,8 +290,7 @@ def main():
         barrier(world, device)
         per_launch_ms = [ev[k].elapsed_time(ev[k + 1]) for k in range(K)]
         total_s = ev[0].elapsed_time(ev[K]) / 1000.0
-        total_s = aggregate_max(total_s, world, device)
-        value = world * B * K / total_s
+        value, total_s = job_rate(B * K, total_s, world, device)
         mean_launch_s = statistics.mean(per_launch_ms) / 1000.0
 
         # ---- e2e: host buffers through mk_decode_step, host loop timed
@@ -296,8 +302,7 @@ def main():
         for k in range(K2):
             tok = dec.decode_step(tok, [pos] * B)
             pos += 1
-        e2e_s = aggregate_max(time.perf_counter() - t0, world, device)
-        e2e_value = world * B * K2 / e2e_s
+        e2e_value, e2e_s = job_rate(B * K2, time.perf_counter() - t0, world, device)
         dec.close()
 
     if rank != 0:
