@@ -55,6 +55,13 @@ class DeviceModel:
         kv = mk_kv(ctypes.cast(kt, ctypes.POINTER(ctypes.c_void_p)), ctypes.cast(vt, ctypes.POINTER(ctypes.c_void_p)))
         return w, kv, (tabs, kt, vt)   # keep the host tables alive while mk_create reads them
 
+    def set_kv(self, layer, b, k_bits, v_bits):
+        """Fill positions 0..T-1 of sequence b's cache in one layer from storage bits
+        [n_kv_heads, T, head_dim] (uint16)."""
+        T = k_bits.shape[1]
+        self.k_cache[layer][b, :, :T] = _to_device(k_bits, self.device)
+        self.v_cache[layer][b, :, :T] = _to_device(v_bits, self.device)
+
     def weight_bytes(self):
         n = self.lm_head.numel() + self.final_norm.numel()
         for lt in self.layers:

@@ -1,0 +1,110 @@
+"""Parity on the two largest workloads, at their full model dimensions.
+
+* 8b: the bf16 model with 32 layers, d 4096, 32/8 heads, FFN 14336 and vocab 128256.
+  A 32-token prompt goes through mk_prefill, then teacher-forced decode steps follow.
+  The workload's 8192-token prompt would take the fp64 oracle far too long; the decode
+  step is the same code at any context, and the 32k-context test below covers long
+  caches.
+* 2b at 32k context: the 2b fp16 model with 32768 cached positions per sequence, at
+  batch 1, 2 and 4.  The cache holds seeded synthetic keys and values (synth.gen_kv, the
+  same bytes on both sides) instead of a 32k-token prefill, which the oracle cannot run
+  in test time.  The oracle checks sequences 0, 1 and 3 one at a time.  Every sequence
+  of a batch must also match that sequence at the smallest batch that holds it
+  (batch invariance).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from helpers import LOGIT_RTOL, assert_parity, gpu_teacher_forced, oracle_run
+
+pytestmark = pytest.mark.gpu
+
+
+class _UncachedModel(oracle.Model):
+    """The oracle model without its fp64 weight cache (the 8b model's fp64 weights
+    would take 64 GB of host memory); each lookup upcasts again."""
+
+    def w(self, name, layer=-1):
+        src = self._bits[name] if layer < 0 else self._bits["layers"][layer][name]
+        return oracle.upcast(src, self.dtype)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    from persistent_sm_decode_megakernel_gb300 import model
+    return model
+
+
+def test_8b_teacher_forced(lib):
+    cfg = synth.CONFIGS["8b"]
+    w = synth.gen_weights(cfg)
+    P, n_new = 32, 3
+    prompt = synth.gen_prompts(cfg, 1, P)
+    toks, zref = oracle_run(cfg, w, prompt, n_new, model=_UncachedModel(cfg, w))
+    dm = lib.DeviceModel(cfg, w, max_batch=1, max_ctx=P + n_new)
+    dec = lib.Decoder(dm)
+    z, tg = gpu_teacher_forced(dec, prompt, toks, n_new, cfg.vocab)
+    dec.close()
+    assert_parity(z, tg, zref, toks, P)
+
+
+T32K = synth.CONFIGS["2b-32k"].prompt_len     # 32768 cached positions
+N_STEPS = 2
+CHECKED = (0, 1, 3)                            # sequences the oracle decodes
+
+
+@pytest.fixture(scope="module")
+def long_ctx(lib):
+    """Device model at batch 4 with every sequence's 32k cache filled, the teacher-forced
+    tokens, and the oracle's logits [N_STEPS, V] for the checked sequences."""
+    cfg = synth.CONFIGS["2b-32k"]
+    w = synth.gen_weights(cfg)
+    m = oracle.Model(cfg, w)
+    dm = lib.DeviceModel(cfg, w, max_batch=4, max_ctx=T32K + N_STEPS + 1)
+    toks = np.stack([synth.gen_prompt(cfg, b, N_STEPS) for b in range(4)])
+    zref = {}
+    for b in range(4):
+        cache = oracle.KVCache(cfg, 1, T32K + N_STEPS) if b in CHECKED else None
+        for l in range(cfg.n_layers):
+            kb = synth.gen_kv(cfg, l, b, 0, T32K)
+            vb = synth.gen_kv(cfg, l, b, 1, T32K)
+            dm.set_kv(l, b, kb, vb)
+            if cache is not None:
+                cache.k[l][0, :, :T32K] = oracle.upcast(kb, cfg.dtype)
+                cache.v[l][0, :, :T32K] = oracle.upcast(vb, cfg.dtype)
+        if cache is not None:
+            zref[b] = np.stack([oracle.decode_step(m, cache, [toks[b, t]], [T32K + t])[0] for t in range(N_STEPS)])
+            del cache
+    return cfg, dm, toks, zref, {}
+
+
+@pytest.mark.parametrize("B", [1, 2, 4])
+def test_2b_32k_context_batches(long_ctx, lib, B):
+    cfg, dm, toks, zref, seen = long_ctx
+    dec = lib.Decoder(dm)
+    logits = torch.zeros((B, cfg.vocab), dtype=torch.float32, device=dm.device)
+    z = []
+    for t in range(N_STEPS):
+        # every batch rewrites positions T32K + t of its sequences with the same values
+        dec.decode_step(toks[:B, t], [T32K + t] * B, logits=logits)
+        z.append(logits.cpu().numpy().copy())
+    dec.close()
+    z = np.stack(z, axis=1)                                   # [B, N_STEPS, V]
+    for b in range(B):
+        if b in zref:
+            for t in range(N_STEPS):
+                zr = zref[b][t]
+                scale = np.abs(zr).max()
+                err = np.abs(z[b, t] - zr).max()
+                assert err <= LOGIT_RTOL * scale, f"seq {b} step {t}: max |dlogit| {err:.3e}"
+                if oracle.top2_margin(zr) > LOGIT_RTOL * scale:
+                    assert np.argmax(z[b, t]) == np.argmax(zr), f"seq {b} step {t}: token differs"
+        if b in seen:      # the same sequence at a smaller batch
+            assert np.abs(z[b] - seen[b]).max() <= 1e-3 * np.abs(seen[b]).max(), f"seq {b}: batch variance"
+        else:
+            seen[b] = z[b]
