@@ -116,9 +116,12 @@ typedef struct {
   int32_t cta, pc, op, layer;
   uint64_t t_fetch;       /* instruction fetched                                           */
   uint64_t t_ready;       /* dependency satisfied                                          */
-  uint64_t t_mark[4];     /* op-internal marks, 0 when unused.  GEMV: [0] inputs staged,
-                             [1] last weight page consumed.  ATTENTION: [0] q staged, [1]
-                             KV pages consumed, [2] split partial written, [3] merge done */
+  uint64_t t_mark[6];     /* op-internal marks, 0 when unused.  GEMV: [0] inputs staged,
+                             [1] last weight page consumed, [2] and [4] DURATIONS: ns compute
+                             warp 0 spent waiting for pages to land, and from each page's
+                             arrival to its release, [3] outputs written.  ATTENTION: [0] q
+                             staged, [1] KV pages consumed, [2] split partial written,
+                             [3] merge done.  [5] unused                                   */
   uint64_t t_end;         /* outputs written (before the signal)                           */
 } mk_trace_rec;
 

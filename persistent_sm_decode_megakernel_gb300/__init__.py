@@ -61,7 +61,7 @@ class mk_info_t(ctypes.Structure):
 
 class mk_trace_rec(ctypes.Structure):
     _fields_ = [("cta", ctypes.c_int32), ("pc", ctypes.c_int32), ("op", ctypes.c_int32), ("layer", ctypes.c_int32),
-                ("t_fetch", ctypes.c_uint64), ("t_ready", ctypes.c_uint64), ("t_mark", ctypes.c_uint64 * 4),
+                ("t_fetch", ctypes.c_uint64), ("t_ready", ctypes.c_uint64), ("t_mark", ctypes.c_uint64 * 6),
                 ("t_end", ctypes.c_uint64)]
 
 

@@ -97,6 +97,18 @@ __device__ __forceinline__ float ld_poll_f32(const float* p) {
   asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
   return v;
 }
+// four consecutive sentinel-guarded values in one 16-byte gpu-scope load
+__device__ __forceinline__ float4 ld_poll_v4(const float4* p) {
+  float4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ bool any_nan4(const float4& v) {
+  return (v.x != v.x) | (v.y != v.y) | (v.z != v.z) | (v.w != v.w);
+}
 __device__ __forceinline__ uint64_t ld_relaxed_u64(const unsigned long long* p) {
   uint64_t v;
   asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");

@@ -416,7 +416,7 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
     sizes[ACT_HMID] = MB * m.d; layers[ACT_HMID] = m.L;
     sizes[ACT_Q] = MB * m.Hq * m.hd; layers[ACT_Q] = m.L;
     sizes[ACT_KVN] = MB * 2 * m.Hkv * m.hd; layers[ACT_KVN] = m.L;
-    sizes[ACT_PART] = MB * m.Hkv * (long long)g.S * G * (m.hd + 2); layers[ACT_PART] = m.L;
+    sizes[ACT_PART] = MB * m.Hkv * (long long)g.S * G * (m.hd + kPartExtra); layers[ACT_PART] = m.L;
     sizes[ACT_O] = MB * m.Hq * m.hd; layers[ACT_O] = m.L;
     sizes[ACT_A] = MB * m.F; layers[ACT_A] = m.L;
     long long off = 0;
@@ -600,7 +600,7 @@ mk_status mk_get_trace(mk_ctx* ctx, mk_trace_rec* recs, int max_records, int* n_
       recs[i].layer = tmp[i].layer;
       recs[i].t_fetch = tmp[i].t_fetch;
       recs[i].t_ready = tmp[i].t_ready;
-      for (int k = 0; k < 4; ++k) recs[i].t_mark[k] = tmp[i].t_mark[k];
+      for (int k = 0; k < 6; ++k) recs[i].t_mark[k] = tmp[i].t_mark[k];
       recs[i].t_end = tmp[i].t_end;
     }
   }

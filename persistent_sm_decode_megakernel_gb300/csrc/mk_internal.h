@@ -89,7 +89,7 @@ struct Ctl {
 
 struct TraceRec {
   int32_t cta, pc, op, layer;
-  uint64_t t_fetch, t_ready, t_mark[4], t_end;
+  uint64_t t_fetch, t_ready, t_mark[6], t_end;
 };
 
 enum ActKind { ACT_H = 0, ACT_HMID, ACT_Q, ACT_KVN, ACT_PART, ACT_O, ACT_A, ACT_NUM };
@@ -160,6 +160,10 @@ struct StepArgs {
   float* logits;               // [B][V] or null
   int32_t* tok_hist;           // device [B] copy of this step's tokens, or null
 };
+
+// a split's partial attention record per head: hd weighted value sums, the running max,
+// the exp-sum, two pad floats (16-byte rows, so records move as float4)
+constexpr int kPartExtra = 4;
 
 // shared-memory layout sizes (bytes)
 constexpr int kCtlSmem = 2048;   // barriers, flags, small broadcast values

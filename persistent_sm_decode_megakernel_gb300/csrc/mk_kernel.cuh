@@ -29,8 +29,7 @@ struct SmemCtl {
   float inv_rms[kMaxBatch];
   float red[kConsumerWarps * kMaxBatch];
   int last_issue_phase[kMaxPages];
-  uint64_t xbar;  // completion of the x-buffer bulk copy
-  uint64_t tmark[4];  // journal marks inside an op
+  uint64_t tmark[6];  // journal marks inside an op
   volatile long long loaded;  // bytes the loader has issued as pages (paces the L2 prefetch)
   volatile int abort;
 };
@@ -437,7 +436,6 @@ __device__ __noinline__ void l2_prefetcher(const DevState& S, const StepArgs& A,
 struct Ring {
   int slot;
   uint32_t ph;
-  uint32_t xph;  // parity of the next x-buffer copy
 };
 
 __device__ __forceinline__ const uint8_t* page_wait(const DevState& S, SmemCtl* c, uint8_t* pages, const Ring& r) {
@@ -471,75 +469,124 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// ---------------------------------------------------------------- x staging
-// The B rows of K fp32 activations ([B][K], contiguous, 128-byte aligned) reach the x
-// buffer through one TMA bulk copy issued by the thread that took the dependency
-// (acquire, then a proxy fence), so no compute-warp registers hold them in flight.
-// Padding rows up to NB are zeroed.  With NaN sentinels, elements the copy caught
-// before their producer wrote them are re-polled one by one.
-template <int SYNC, int NB>
-__device__ void stage_copy(const DevState& S, const float* src, int K, int B, float* xbuf, SmemCtl* c,
-                           Ring& ring) {
-  const int tid = threadIdx.x;
-  const uint32_t bytes = (uint32_t)B * (uint32_t)K * 4u;
-  if (tid == 0) {
-    fence_proxy_async();
-    mbar_arrive_expect_tx(&c->xbar, bytes);
-    tma_load_1d_plain(xbuf, src, bytes, &c->xbar);
-  }
-  float4* x4 = reinterpret_cast<float4*>(xbuf);
-  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i = B * K / 4 + tid; i < NB * K / 4; i += kConsumerThreads) x4[i] = z;
-  if (!mbar_try_wait(&c->xbar, ring.xph)) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(&c->xbar, ring.xph)) {
-      if (globaltimer_ns() - t0 > (uint64_t)S.timeout_ns) {
-        set_err(S, 4u, -9, -1);
-        c->abort = 1;
-        break;
-      }
+// ---------------------------------------------------------------- input staging
+// A producer's fp32 output reaches shared memory through 16-byte loads by every consumer
+// thread, U vectors in flight per thread: one L2 round trip.  With counters the loads
+// follow the acquire; with NaN sentinels the loads are the polls -- vectors that still
+// hold a sentinel are re-read together (all of a thread's pending vectors in one round
+// trip) until the producer's values land.  put(i, v) stores vector i.
+__device__ __noinline__ float4 poll_slow_v4(const float4* p, const DevState& S, SmemCtl* c) {
+  const uint64_t t0 = globaltimer_ns();
+  int k = 0;
+  while (true) {
+    const int ns = 20 << (k < 8 ? k : 8);
+    __nanosleep(ns < S.backoff_max_ns ? ns : S.backoff_max_ns);
+    ++k;
+    const float4 v = ld_poll_v4(p);
+    if (!any_nan4(v)) return v;
+    if (c->abort || global_err(S)) {
+      c->abort = 1;
+      return make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (globaltimer_ns() - t0 > (uint64_t)S.timeout_ns) {
+      set_err(S, 4u, -1, -1);
+      c->abort = 1;
+      return make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
-  ring.xph ^= 1u;
-  if (SYNC == SYNC_SENTINEL) {
-    for (int i = tid; i < B * K; i += kConsumerThreads)
-      if (isnan(xbuf[i])) xbuf[i] = poll_slow(src + i, S, c);
-  }
-  consumer_sync();
+}
+template <int SYNC>
+__device__ __forceinline__ float4 load_v4(const float4* p, const DevState& S, SmemCtl* c) {
+  if (SYNC == SYNC_COUNTER) return __ldcg(p);
+  const float4 v = ld_poll_v4(p);
+  return any_nan4(v) ? poll_slow_v4(p, S, c) : v;
 }
 
-// RMSNorm, folded: W (g . h / rms) = (W (g . h)) / rms.  The staged residual is scaled by
-// the gain in place while each thread accumulates its share of sum(h^2); the per-warp
-// sums go to c->red and the epilogue turns them into 1/rms (fixed order, same in every
-// thread), so no CTA-wide barrier sits between staging and the weight pages.
+template <int SYNC, typename Put>
+__device__ __forceinline__ void stage_vec(const DevState& S, const float4* src, int n4, SmemCtl* c, Put&& put) {
+  constexpr int U = 4;
+  const int tid = threadIdx.x;
+  for (int base = 0; base < n4; base += U * kConsumerThreads) {
+    float4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * kConsumerThreads + tid;
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < n4) v[u] = SYNC == SYNC_COUNTER ? __ldcg(src + i) : ld_poll_v4(src + i);
+    }
+    if (SYNC == SYNC_SENTINEL) {
+      bool pend = false;
+#pragma unroll
+      for (int u = 0; u < U; ++u) pend |= any_nan4(v[u]);
+      if (pend) {
+        const uint64_t t0 = globaltimer_ns();
+        int k = 0;
+        while (pend) {
+          const int ns = 20 << (k < 8 ? k : 8);
+          __nanosleep(ns < S.backoff_max_ns ? ns : S.backoff_max_ns);
+          ++k;
+          pend = false;
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            if (any_nan4(v[u])) {
+              v[u] = ld_poll_v4(src + base + u * kConsumerThreads + tid);
+              pend |= any_nan4(v[u]);
+            }
+          }
+          if (pend && (c->abort || global_err(S) || globaltimer_ns() - t0 > (uint64_t)S.timeout_ns)) {
+            if (!global_err(S)) set_err(S, 4u, -1, -1);
+            c->abort = 1;
+            break;
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * kConsumerThreads + tid;
+      if (i < n4) put(i, v[u]);
+    }
+  }
+}
+
+// B rows of K fp32 values ([B][K], 16-byte aligned) into the x buffer; padding rows up
+// to NB are zeroed.
+template <int SYNC, int NB>
+__device__ void stage_copy(const DevState& S, const float* src, int K, int B, float* xbuf, SmemCtl* c) {
+  float4* x4 = reinterpret_cast<float4*>(xbuf);
+  const int k4 = K / 4;
+  stage_vec<SYNC>(S, reinterpret_cast<const float4*>(src), B * k4, c, [&](int i, const float4& v) { x4[i] = v; });
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = B * k4 + threadIdx.x; i < NB * k4; i += kConsumerThreads) x4[i] = z;
+}
+
+// RMSNorm, folded: W (g . h / rms) = (W (g . h)) / rms.  The residual is staged scaled by
+// the gain while each thread accumulates its share of sum(h^2); the per-warp sums go to
+// c->red and the epilogue turns them into 1/rms (fixed order, same in every thread), so
+// no CTA-wide pass sits between staging and the weight pages.
 template <typename WT, int SYNC, int NB>
 __device__ void stage_rmsnorm(const DevState& S, const float* h, const uint16_t* gain, int B, float* xbuf,
-                              SmemCtl* c, Ring& ring) {
-  const int d = S.d, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  stage_copy<SYNC, NB>(S, h, d, B, xbuf, c, ring);
+                              SmemCtl* c) {
+  const int d = S.d, d4 = d / 4, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   float4* x4 = reinterpret_cast<float4*>(xbuf);
-  const int d4 = d / 4;
   float ss[NB];
 #pragma unroll
   for (int b = 0; b < NB; ++b) ss[b] = 0.f;
-  for (int k = tid; k < d4; k += kConsumerThreads) {
+  stage_vec<SYNC>(S, reinterpret_cast<const float4*>(h), B * d4, c, [&](int i, float4 w) {
+    const int b = i / d4, k = i - b * d4;
     const uint2 gb = __ldg(reinterpret_cast<const uint2*>(gain) + k);  // 4 gains
-    const float g0 = Unpack<WT>::one((uint16_t)(gb.x & 0xFFFFu)), g1 = Unpack<WT>::one((uint16_t)(gb.x >> 16));
-    const float g2 = Unpack<WT>::one((uint16_t)(gb.y & 0xFFFFu)), g3 = Unpack<WT>::one((uint16_t)(gb.y >> 16));
+    const float sq = w.x * w.x + w.y * w.y + w.z * w.z + w.w * w.w;
 #pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      float4 v = x4[b * d4 + k];
-      ss[b] = fmaf(v.x, v.x, ss[b]);
-      ss[b] = fmaf(v.y, v.y, ss[b]);
-      ss[b] = fmaf(v.z, v.z, ss[b]);
-      ss[b] = fmaf(v.w, v.w, ss[b]);
-      v.x *= g0;
-      v.y *= g1;
-      v.z *= g2;
-      v.w *= g3;
-      x4[b * d4 + k] = v;
-    }
-  }
+    for (int bb = 0; bb < NB; ++bb)
+      if (bb == b) ss[bb] += sq;
+    w.x *= Unpack<WT>::one((uint16_t)(gb.x & 0xFFFFu));
+    w.y *= Unpack<WT>::one((uint16_t)(gb.x >> 16));
+    w.z *= Unpack<WT>::one((uint16_t)(gb.y & 0xFFFFu));
+    w.w *= Unpack<WT>::one((uint16_t)(gb.y >> 16));
+    x4[i] = w;
+  });
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = B * d4 + tid; i < NB * d4; i += kConsumerThreads) x4[i] = z;
 #pragma unroll
   for (int b = 0; b < NB; ++b) {
     const float t = warp_sum(ss[b]);
@@ -651,19 +698,19 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
   // 1. inputs
   switch (in.op) {
     case OP_QKV:
-      stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_H, l), iptr(in, kP2), B, xbuf, c, ring);
+      stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_H, l), iptr(in, kP2), B, xbuf, c);
       break;
     case OP_UPGATE:
-      stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_HMID, l), iptr(in, kP2), B, xbuf, c, ring);
+      stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_HMID, l), iptr(in, kP2), B, xbuf, c);
       break;
     case OP_LMHEAD:
-      stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_H, S.L), iptr(in, kP2), B, xbuf, c, ring);
+      stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_H, S.L), iptr(in, kP2), B, xbuf, c);
       break;
     case OP_OPROJ:
-      stage_copy<SYNC, NB>(S, act_ptr(S, act, ACT_O, l), g.K, B, xbuf, c, ring);
+      stage_copy<SYNC, NB>(S, act_ptr(S, act, ACT_O, l), g.K, B, xbuf, c);
       break;
     default:  // OP_DOWN
-      stage_copy<SYNC, NB>(S, act_ptr(S, act, ACT_A, l), g.K, B, xbuf, c, ring);
+      stage_copy<SYNC, NB>(S, act_ptr(S, act, ACT_A, l), g.K, B, xbuf, c);
       break;
   }
   consumer_sync();
@@ -680,9 +727,14 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
   // 2. stream the slices: warp w takes slice i0 + w of every page of 8 slices
   float* rowpart = scratch;  // [rows][spr][NB]
   const int spr = g.spr(), ns = g.nslices();
+  const bool trace = (A.flags & SF_TRACE) != 0;
+  uint64_t page_wait_ns = 0, page_work_ns = 0;
   auto run_pages = [&](auto&& dot) {
     for (int i0 = 0; i0 < ns; i0 += kConsumerWarps) {
+      const uint64_t tw = trace ? globaltimer_ns() : 0ull;
       const uint8_t* pg = page_wait(S, c, pages, ring);
+      const uint64_t tr = trace ? globaltimer_ns() : 0ull;
+      if (trace) page_wait_ns += tr - tw;
       const int i = i0 + warp;
       if (i < ns) {
         const int r = i / spr, s = i - r * spr;
@@ -696,6 +748,7 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
         }
       }
       page_release(S, c, ring);
+      if (trace) page_work_ns += globaltimer_ns() - tr;
     }
   };
   bool done = false;
@@ -738,7 +791,11 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
       slice_dot_smem<WT, NB>(wp, xbuf + (size_t)s * g.WS, g.K, g.WS, lane, acc);
     });
   consumer_sync();
-  if (tid == 0 && (A.flags & SF_TRACE)) c->tmark[1] = globaltimer_ns();
+  if (tid == 0 && trace) {
+    c->tmark[1] = globaltimer_ns();
+    c->tmark[2] = page_wait_ns;
+    c->tmark[4] = page_work_ns;
+  }
 
   // 3. finalize rows in a fixed order and apply the op's epilogue
   auto rowsum = [&](int r, int b) {
@@ -843,6 +900,7 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
       break;
     }
   }
+  if (tid == 0 && trace) c->tmark[3] = globaltimer_ns();
 }
 
 // ---------------------------------------------------------------- attention
@@ -863,14 +921,26 @@ __device__ __noinline__ void op_attn(const DevState& S, const StepArgs& A, const
   const float qscale = (1.0f / sqrtf((float)HD)) * 1.4426950408889634f;  // scores in log2 units
 
   const float* qsrc = act_ptr(S, act, ACT_Q, l) + ((size_t)at.b * S.Hq + (size_t)at.j * G) * HD;
-  for (int t = tid; t < G * HD; t += kConsumerThreads) xbuf[t] = load_act<SYNC>(qsrc + t, S, c) * qscale;
+  float4* q4 = reinterpret_cast<float4*>(xbuf);
+  stage_vec<SYNC>(S, reinterpret_cast<const float4*>(qsrc), G * HD / 4, c, [&](int i, float4 v) {
+    v.x *= qscale;
+    v.y *= qscale;
+    v.z *= qscale;
+    v.w *= qscale;
+    q4[i] = v;
+  });
   // the new position's key and value (split holding pos_b), staged as storage-dtype rows
   // like a page (the values are already rounded to that dtype, so this is exact)
   uint16_t* knew = reinterpret_cast<uint16_t*>(xbuf + G * HD);
-  if (at.has_new) {
+  if (at.has_new && tid < HD / 2) {
     const float* kn = act_ptr(S, act, ACT_KVN, l) + (size_t)at.b * 2 * S.Hkv * HD + (size_t)at.j * HD;
-    for (int t = tid; t < 2 * HD; t += kConsumerThreads)
-      knew[t] = Unpack<WT>::round(load_act<SYNC>(kn + (t < HD ? t : (size_t)S.Hkv * HD + (t - HD)), S, c));
+    const int kv = tid / (HD / 4), e = (tid % (HD / 4)) * 4;  // HD/4 vectors of k, then of v
+    const float4 v = load_v4<SYNC>(reinterpret_cast<const float4*>(kn + (size_t)kv * S.Hkv * HD + e), S, c);
+    uint16_t* dst = knew + kv * HD + e;
+    dst[0] = Unpack<WT>::round(v.x);
+    dst[1] = Unpack<WT>::round(v.y);
+    dst[2] = Unpack<WT>::round(v.z);
+    dst[3] = Unpack<WT>::round(v.w);
   }
   consumer_sync();
   const bool mark = (A.flags & SF_TRACE) && tid == 0;
@@ -989,7 +1059,7 @@ __device__ __noinline__ void op_attn(const DevState& S, const StepArgs& A, const
       for (int i = 0; i < DPL; ++i) o[g][i] += __shfl_xor_sync(0xffffffffu, o[g][i], o2);
     }
   }
-  constexpr int RW = HD + 2;
+  constexpr int RW = HD + kPartExtra;
   if (pgi == 0) {
 #pragma unroll
     for (int g = 0; g < G; ++g)
@@ -1012,6 +1082,8 @@ __device__ __noinline__ void op_attn(const DevState& S, const StepArgs& A, const
     float r;
     if (e == HD) {
       r = M;
+    } else if (e > HD + 1) {
+      r = 0.f;  // pad: written so that sentinel polls of the whole record end
     } else if (M == -CUDART_INF_F) {
       r = 0.f;
     } else {
@@ -1026,41 +1098,23 @@ __device__ __noinline__ void op_attn(const DevState& S, const StepArgs& A, const
 }
 
 // log-sum-exp merge of the S split partials of one (sequence, kv head) (§8.2 ATTN_REDUCE).
-// The (b, j) block of partials is contiguous: one bulk copy into the x buffer when it
-// fits (the caller has acquired the partials), else loads batched eight splits deep.
+// The (b, j) block of partials is contiguous and made of 16-byte rows: staged into the x
+// buffer with vector loads when it fits (the caller has acquired the partials, or polls
+// them), else read from global memory eight splits deep.
 template <int SYNC>
 __device__ __noinline__ void op_attn_reduce(const DevState& S, const StepArgs& A, const Instr& in, SmemCtl* c,
-                                            float* xbuf, float* scratch, Ring& ring, float* act) {
+                                            float* xbuf, float* scratch, float* act) {
   const int tid = threadIdx.x;
   const int b = in.a[0], j = in.a[1], l = in.layer;
   if (b >= A.B) return;  // uniform over the CTA
-  const int HD = S.hd, G = S.Hq / S.Hkv, RW = HD + 2;
+  const int HD = S.hd, G = S.Hq / S.Hkv, RW = HD + kPartExtra;
   const int NS = active_splits(S, A, b);  // splits s < NS wrote partials this step
   const float* part = act_ptr(S, act, ACT_PART, l) + ((size_t)b * S.Hkv + j) * S.S * G * RW;
   float* out = act_ptr(S, act, ACT_O, l) + (size_t)b * S.Hq * HD + (size_t)j * G * HD;
-  const uint32_t bytes = (uint32_t)NS * G * RW * 4u;
-  // a bulk copy needs a 16-byte aligned start and a 16-byte multiple size
-  if ((int)bytes <= S.xbuf_bytes && (bytes & 15u) == 0 && (reinterpret_cast<uintptr_t>(part) & 15u) == 0) {
-    if (tid == 0) {
-      fence_proxy_async();
-      mbar_arrive_expect_tx(&c->xbar, bytes);
-      tma_load_1d_plain(xbuf, part, bytes, &c->xbar);
-    }
-    if (!mbar_try_wait(&c->xbar, ring.xph)) {
-      const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(&c->xbar, ring.xph)) {
-        if (globaltimer_ns() - t0 > (uint64_t)S.timeout_ns) {
-          set_err(S, 4u, -10, -1);
-          c->abort = 1;
-          break;
-        }
-      }
-    }
-    ring.xph ^= 1u;
-    if (SYNC == SYNC_SENTINEL) {
-      for (int i = tid; i < NS * G * RW; i += kConsumerThreads)
-        if (isnan(xbuf[i])) xbuf[i] = poll_slow(part + i, S, c);
-    }
+  const int n4 = NS * G * RW / 4;
+  if (n4 * 16 <= S.xbuf_bytes) {
+    float4* x4 = reinterpret_cast<float4*>(xbuf);
+    stage_vec<SYNC>(S, reinterpret_cast<const float4*>(part), n4, c, [&](int i, const float4& v) { x4[i] = v; });
     consumer_sync();
     for (int t = tid; t < G * HD; t += kConsumerThreads) {
       const int g = t / HD, e = t - g * HD;
@@ -1165,7 +1219,7 @@ __device__ void consumer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8
   float* act = S.act + (int64_t)par * S.act_floats;
   const int nb = A.B <= 1 ? 1 : A.B <= 2 ? 2 : A.B <= 4 ? 4 : A.B <= 8 ? 8 : 16;
   const int G = S.Hq / S.Hkv;
-  Ring ring{0, 0u, 0u};
+  Ring ring{0, 0u};
   int order_n = 0;
   const int end = A.q_start[cta + 1];
   for (int pc = A.q_start[cta]; pc < end; ++pc) {
@@ -1174,7 +1228,7 @@ __device__ void consumer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8
     uint64_t t_fetch = 0, t_ready = 0;
     if (TRACE) {
       t_fetch = globaltimer_ns();
-      if (tid == 0) c->tmark[0] = c->tmark[1] = c->tmark[2] = c->tmark[3] = 0ull;
+      if (tid == 0) c->tmark[0] = c->tmark[1] = c->tmark[2] = c->tmark[3] = c->tmark[4] = c->tmark[5] = 0ull;
     }
     // ---- wait for the dependency (counter mode; sentinel mode polls the data itself)
     const bool use_ctr = (SYNC == SYNC_COUNTER || in.op >= OP_T_NOP) && !nosync;
@@ -1220,7 +1274,7 @@ __device__ void consumer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8
           op_attn<WT, SYNC, 64, 1>(S, A, in, c, pages, xbuf, scratch, ring, act);
         break;
       case OP_ATTN_REDUCE:
-        op_attn_reduce<SYNC>(S, A, in, c, xbuf, scratch, ring, act);
+        op_attn_reduce<SYNC>(S, A, in, c, xbuf, scratch, act);
         break;
       case OP_T_ORDER:
       case OP_T_PRODUCE:
@@ -1257,7 +1311,7 @@ __device__ void consumer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8
         last = (old + 1u == (A.epoch + 1u) * (uint32_t)in.a[3]);
       }
       if (consumer_sync_or(last)) {
-        op_attn_reduce<SYNC>(S, A, in, c, xbuf, scratch, ring, act);
+        op_attn_reduce<SYNC>(S, A, in, c, xbuf, scratch, act);
         if (consumer_sync_or(c->abort)) break;
         if (TRACE && tid == 0) c->tmark[3] = globaltimer_ns();
       } else {
@@ -1296,7 +1350,7 @@ __device__ void consumer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8
         rec.layer = in.layer;
         rec.t_fetch = t_fetch;
         rec.t_ready = t_ready;
-        for (int k = 0; k < 4; ++k) rec.t_mark[k] = c->tmark[k];
+        for (int k = 0; k < 6; ++k) rec.t_mark[k] = c->tmark[k];
         rec.t_end = t_end;
         S.trace[k] = rec;
       }
@@ -1317,7 +1371,6 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
   SmemCtl* c = reinterpret_cast<SmemCtl*>(reinterpret_cast<uint8_t*>(scratch) + S.scratch_bytes);
   const int tid = threadIdx.x;
   if (tid == 0) {
-    mbar_init(&c->xbar, 1);
     for (int i = 0; i < S.n_pages; ++i) {
       mbar_init(&c->full[i], 1);
       mbar_init(&c->empty[i], kConsumerWarps);

@@ -180,7 +180,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_desc* desc, const mk_
   sizes[ACT_HMID] = (long long)B * m.d; layers[ACT_HMID] = L;
   sizes[ACT_Q] = (long long)B * m.Hq * m.hd; layers[ACT_Q] = L;
   sizes[ACT_KVN] = (long long)B * 2 * m.Hkv * m.hd; layers[ACT_KVN] = L;
-  sizes[ACT_PART] = (long long)B * m.Hkv * g.S * G * (m.hd + 2); layers[ACT_PART] = L;
+  sizes[ACT_PART] = (long long)B * m.Hkv * g.S * G * (m.hd + kPartExtra); layers[ACT_PART] = L;
   sizes[ACT_O] = (long long)B * m.Hq * m.hd; layers[ACT_O] = L;
   sizes[ACT_A] = (long long)B * m.F; layers[ACT_A] = L;
   long long off = 0;

@@ -69,7 +69,7 @@ std::string make_geometry(const ModelShape& m, int n_cta, int page_bytes, int n_
   }
   if (g->S < 1 || g->S > 256) return "kv_splits out of range [1, 256]";
   int scratch = 16384;
-  scratch = std::max(scratch, kConsumerWarps * G * (m.hd + 2) * 4);
+  scratch = std::max(scratch, kConsumerWarps * G * (m.hd + kPartExtra) * 4);
   scratch = std::max(scratch, g->S * G * 2 * 4);
   g->scratch_bytes = ((scratch + 127) / 128) * 128;
   const int avail = smem_limit - g->xbuf_bytes - g->scratch_bytes - kCtlSmem;

@@ -163,4 +163,5 @@ class Decoder:
         buf = (mk_trace_rec * max_records)()
         n = ctypes.c_int()
         check(mk_get_trace(self.h, buf, max_records, ctypes.byref(n)), "mk_get_trace")
-        return [(r.cta, r.pc, r.op, r.layer, r.t_fetch, r.t_ready, r.t_end, *list(r.t_mark)) for r in buf[: n.value]]
+        return [(r.cta, r.pc, r.op, r.layer, r.t_fetch, r.t_ready, r.t_end, *list(r.t_mark)[:4], r.t_mark[4])
+                for r in buf[: n.value]]

@@ -24,7 +24,14 @@ if ROOT not in sys.path:
 OPS = {1: "embed", 2: "qkv", 3: "attn", 4: "reduce", 5: "oproj", 6: "upgate", 7: "down", 8: "lmhead"}
 
 
+GEMV_OPS = (2, 5, 6, 7, 8)
+
+
 def summarize(trace):
+    """Per-op means of the journal's phases.  GEMV: stage (dependency satisfied -> inputs
+    staged), pages (-> last page consumed; page_wait = the part spent waiting for pages to
+    land), epi (-> outputs written), tail (-> end, the closing barrier).  Attention: stage,
+    pages, write (partial written), then arrive (the arrival) or merge (last arriver)."""
     t0 = min(r[4] for r in trace)
     t1 = max(r[6] for r in trace)
     span = (t1 - t0) / 1e3
@@ -32,15 +39,23 @@ def summarize(trace):
     by = {}
     per_cta_wait = {}
     groups = {}
-    for cta, pc, op, layer, tf, tr, te, m0, m1, m2, m3 in trace:
-        d = by.setdefault(OPS.get(op, str(op)), {"wait": [], "work": [], "stage": [], "pages": [], "epi": [],
-                                                 "write": [], "arrive": [], "merge": []})
+    keys = ("stage", "pages", "page_wait", "page_work", "epi", "tail", "write", "arrive", "merge")
+    for cta, pc, op, layer, tf, tr, te, m0, m1, m2, m3, m4 in trace:
+        d = by.setdefault(OPS.get(op, str(op)), {k: [] for k in ("wait", "work") + keys})
         d["wait"].append((tr - tf) / 1e3)
         d["work"].append((te - tr) / 1e3)
-        if m0 and m1:
+        if op in GEMV_OPS and m0 and m1:
             d["stage"].append((m0 - tr) / 1e3)
             d["pages"].append((m1 - m0) / 1e3)
-            if m2:   # attention: partial written, then the arrival (and the merge)
+            d["page_wait"].append(m2 / 1e3)
+            d["page_work"].append(m4 / 1e3)
+            if m3:
+                d["epi"].append((m3 - m1) / 1e3)
+                d["tail"].append((te - m3) / 1e3)
+        elif op == 3 and m0 and m1:
+            d["stage"].append((m0 - tr) / 1e3)
+            d["pages"].append((m1 - m0) / 1e3)
+            if m2:
                 d["write"].append((m2 - m1) / 1e3)
                 if m3:
                     d["merge"].append((m3 - m2) / 1e3)
@@ -57,7 +72,7 @@ def summarize(trace):
         out["ops"][k] = {"n": len(d["work"]), "wait_us_mean": statistics.mean(d["wait"]),
                          "work_us_mean": statistics.mean(d["work"]), "work_us_max": max(d["work"]),
                          "wait_us_per_cta": sum(d["wait"]) / len(ctas)}
-        for key in ("stage", "pages", "epi", "write", "arrive", "merge"):
+        for key in keys:
             if d[key]:
                 out["ops"][k][key + "_us"] = statistics.mean(d[key])
     out["wait_share_mean"] = statistics.mean(v / span for v in per_cta_wait.values())
