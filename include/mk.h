@@ -91,10 +91,16 @@ typedef struct {
   int fault_drop_signal;  /* test hook: k > 0 removes the k-th counter signal from the
                              schedule and skips the host-side validator, so that the
                              device wait must time out (fault injection on the host)     */
-  int l2_prefetch_kb;     /* loader prefetches upcoming weight/KV ranges into L2 this far
-                             ahead of its page loads, per CTA (0: default 256; < 0: off) */
   int split_min_positions; /* a step uses as many KV splits (up to kv_splits) as give each
                               at least this many positions (0: default 16)               */
+  int attn_merge;         /* where the KV-split partials are merged (§8.2 ATTN_REDUCE):
+                             0 auto, 1 a separate step (the ATTN_REDUCE op with sentinels,
+                             the last-arriving split with counters), 2 inside the O-proj
+                             input staging of every O-proj unit (no extra dependency hop;
+                             auto picks it when the partials of a step are small)       */
+  int inflight_pages;     /* at most this many page copies of a CTA in flight at once
+                             (0: no limit below the pool size; landed pages still fill
+                             the whole pool)                                             */
 } mk_options;
 
 typedef struct {
@@ -121,7 +127,8 @@ typedef struct {
                              warp 0 spent waiting for pages to land, and from each page's
                              arrival to its release, [3] outputs written.  ATTENTION: [0] q
                              staged, [1] KV pages consumed, [2] split partial written,
-                             [3] merge done.  [5] unused                                   */
+                             [3] merge done.  GEMV [5]: SM clock cycles compute thread 0
+                             spent in the epilogue                                       */
   uint64_t t_end;         /* outputs written (before the signal)                           */
 } mk_trace_rec;
 

@@ -49,7 +49,8 @@ class mk_options(ctypes.Structure):
     _fields_ = [("sync_mode", c_int), ("exec_mode", c_int), ("page_bytes", c_int), ("n_pages", c_int),
                 ("kv_splits", c_int), ("trace", c_int), ("wait_timeout_s", c_double),
                 ("backoff_max_ns", c_int), ("max_ctas", c_int), ("fault_drop_signal", c_int),
-                ("l2_prefetch_kb", c_int), ("split_min_positions", c_int)]
+                ("split_min_positions", c_int),
+                ("attn_merge", c_int), ("inflight_pages", c_int)]
 
 
 class mk_info_t(ctypes.Structure):

@@ -144,10 +144,11 @@ mk_status get_sched(mk_ctx* ctx, int B, Sched** out) {
     return MK_OK;
   }
   auto sc = std::make_unique<Sched>();
-  // counter mode merges the KV splits in the last-arriving split; sentinel mode keeps the
-  // separate ATTN_REDUCE op (it has no atomics to elect a last arriver)
-  const bool fuse = ctx->opts.sync_mode == MK_SYNC_COUNTER;
-  std::string e = build_plan(ctx->m, ctx->geo, ctx->n_cta, B, ctx->opts.fault_drop_signal, fuse, &sc->plan);
+  // small batches merge the KV splits inside the O-proj staging; otherwise counter mode
+  // merges them in the last-arriving split and sentinel mode keeps the separate
+  // ATTN_REDUCE op (it has no atomics to elect a last arriver)
+  const int merge = choose_merge(ctx->m, ctx->geo, B, ctx->opts.sync_mode == MK_SYNC_COUNTER, ctx->opts.attn_merge);
+  std::string e = build_plan(ctx->m, ctx->geo, ctx->n_cta, B, ctx->opts.fault_drop_signal, merge, &sc->plan);
   if (!e.empty()) return fail(MK_ERR_INVALID, "schedule: " + e);
   bake_pointers(ctx->m, ctx->ptrs, &sc->plan);
   if (ctx->opts.fault_drop_signal <= 0) {
@@ -292,12 +293,14 @@ mk_status mk_plan(const mk_model_desc* desc, const mk_options* opts, int n_ctas,
   if (n_ctas < 1 || !info) return fail(MK_ERR_INVALID, "n_ctas must be positive and info non-NULL");
   mk_options o{};
   if (opts) o = *opts;
+  if (o.attn_merge < 0 || o.attn_merge > 2) return fail(MK_ERR_INVALID, "attn_merge must be 0, 1 or 2");
   const ModelShape m = shape_of(desc);
   Geometry g;
   e = make_geometry(m, n_ctas, o.page_bytes, o.n_pages, o.kv_splits, 232448, &g);
   if (!e.empty()) return fail(MK_ERR_INVALID, e);
   Plan p;
-  e = build_plan(m, g, n_ctas, m.max_batch, o.fault_drop_signal, o.sync_mode == MK_SYNC_COUNTER, &p);
+  e = build_plan(m, g, n_ctas, m.max_batch, o.fault_drop_signal,
+                 choose_merge(m, g, m.max_batch, o.sync_mode == MK_SYNC_COUNTER, o.attn_merge), &p);
   if (!e.empty()) return fail(MK_ERR_INVALID, e);
   e = validate_plan(m, g, p);
   if (!e.empty()) return fail(MK_ERR_INVALID, "schedule rejected by the validator: " + e);
@@ -345,6 +348,7 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
   if (o.backoff_max_ns <= 0) o.backoff_max_ns = 256;
   if (o.sync_mode != MK_SYNC_COUNTER && o.sync_mode != MK_SYNC_SENTINEL) return fail(MK_ERR_INVALID, "sync_mode");
   if (o.exec_mode != MK_EXEC_PERSISTENT && o.exec_mode != MK_EXEC_MULTILAUNCH) return fail(MK_ERR_INVALID, "exec_mode");
+  if (o.attn_merge < 0 || o.attn_merge > 2) return fail(MK_ERR_INVALID, "attn_merge must be 0, 1 or 2");
   ctx->stream = reinterpret_cast<cudaStream_t>(stream);
   MK_CUDA(cudaGetDevice(&ctx->device));
   MK_CUDA(cudaDeviceGetAttribute(&ctx->n_sm, cudaDevAttrMultiProcessorCount, ctx->device));
@@ -446,8 +450,8 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
   S.sync_mode = o.sync_mode;
   S.timeout_ns = (int64_t)(o.wait_timeout_s * 1e9);
   S.backoff_max_ns = o.backoff_max_ns;
-  S.l2_prefetch_bytes = o.l2_prefetch_kb < 0 ? 0 : (o.l2_prefetch_kb == 0 ? 256 : o.l2_prefetch_kb) * 1024;
   S.split_min_positions = o.split_min_positions > 0 ? o.split_min_positions : 16;
+  S.inflight_pages = o.inflight_pages > 0 ? o.inflight_pages : 0;
   ModelPtrs& mp = ctx->ptrs;
   mp.final_norm = w->final_norm;
   mp.lm_head = w->lm_head;

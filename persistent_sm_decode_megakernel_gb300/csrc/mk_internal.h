@@ -12,9 +12,8 @@ namespace mk {
 
 constexpr int kMaxBatch = 16;
 constexpr int kConsumerWarps = 8;                 // compute warps per CTA
-constexpr int kThreads = 32 * (kConsumerWarps + 2);  // + the loader (TMA) warp + the L2 prefetch warp
+constexpr int kThreads = 32 * (kConsumerWarps + 1);  // + the loader (TMA) warp
 constexpr int kLoaderWarp = kConsumerWarps;
-constexpr int kPrefetchWarp = kConsumerWarps + 1;
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kMaxPages = 16;
 
@@ -38,7 +37,13 @@ enum Op : uint8_t {
 
 constexpr int kNumPhaseOps = 8;  // EMBED..LMHEAD, for the multi-launch phase tables
 
-enum : uint8_t { F_LAST_LM = 1 };
+enum : uint8_t {
+  F_LAST_LM = 1,
+  F_MERGE_IN = 2,  // OPROJ: merge the KV-split partials while staging the input
+};
+
+// where a schedule merges the KV-split partials
+enum MergeMode { MERGE_OP = 0, MERGE_LAST_ARRIVER = 1, MERGE_IN_OPROJ = 2 };
 
 // 64-byte instruction
 struct Instr {
@@ -60,7 +65,8 @@ static_assert(sizeof(Instr) == 64, "instruction is 64 bytes");
 //   ATTN    a0 b, a1 kv head j, a2 split s, a3 splits S, a4 arrival counter (-1: the
 //           merge is a separate ATTN_REDUCE), p4 keys of (b, j) at t = 0, p5 values
 //   REDUCE  a0 b, a1 j
-//   OPROJ / DOWN   a0 row0, a1 rows, p4 first row
+//   OPROJ / DOWN   a0 row0, a1 rows, p4 first row (OPROJ with F_MERGE_IN: its input is
+//           merged from the split partials while it is staged)
 //   UPGATE  a0 row0, a1 rows, p2 gain, p4 gate rows, p5 up rows
 //   LMHEAD  a0 row0, a1 rows, a2 CTAs with LM rows, p2 final gain, p4 first row
 // pK = the 64-bit value in a[2K], a[2K+1]
@@ -134,8 +140,8 @@ struct DevState {
   int sync_mode;
   int64_t timeout_ns;
   int backoff_max_ns;
-  int l2_prefetch_bytes;       // loader's L2 prefetch window ahead of its page loads (0: off)
   int split_min_positions;     // a KV split of a step covers at least this many positions
+  int inflight_pages;          // loader: page copies in flight at most (0: the pool size)
   // self-test buffers
   int64_t* test_buf;
   int64_t test_len;

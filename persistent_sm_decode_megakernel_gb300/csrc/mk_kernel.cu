@@ -82,7 +82,6 @@ __global__ void __launch_bounds__(kThreads, 1) mk_stream_kernel(const uint8_t* s
   const uint8_t* base = src + (long long)blockIdx.x * bytes_per_cta;
   const uint64_t t0 = globaltimer_ns();
   const uint64_t limit = 2000000000ull;
-  if (warp > kConsumerWarps) return;  // this benchmark has no prefetch warp
   if (warp == kConsumerWarps) {
     if (lane != 0) return;
     const uint64_t pol = l2_evict_first_policy();

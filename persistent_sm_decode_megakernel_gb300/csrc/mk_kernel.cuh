@@ -30,7 +30,6 @@ struct SmemCtl {
   float red[kConsumerWarps * kMaxBatch];
   int last_issue_phase[kMaxPages];
   uint64_t tmark[6];  // journal marks inside an op
-  volatile long long loaded;  // bytes the loader has issued as pages (paces the L2 prefetch)
   volatile int abort;
 };
 static_assert(sizeof(SmemCtl) <= kCtlSmem, "control block fits");
@@ -214,52 +213,17 @@ __device__ __forceinline__ float* act_ptr(const DevState& S, float* act, int kin
 }
 
 
-// The weight / KV byte ranges an instruction's pages will cover (at most two).
-struct Ranges {
-  const uint16_t* p[2];
-  uint32_t bytes[2];
-  int n;
-};
-__device__ __forceinline__ Ranges instr_ranges(const DevState& S, const StepArgs& A, const Instr& in) {
-  Ranges r;
-  r.n = 0;
-  switch (in.op) {
-    case OP_QKV:
-    case OP_OPROJ:
-    case OP_UPGATE:
-    case OP_DOWN:
-    case OP_LMHEAD: {
-      const Gemv g = make_gemv(S, in);
-      for (int k = 0; k < 2; ++k)
-        if (g.segr[k] > 0) {
-          r.p[r.n] = g.seg[k];
-          r.bytes[r.n] = (uint32_t)g.segr[k] * (uint32_t)g.K * 2u;
-          ++r.n;
-        }
-      break;
-    }
-    case OP_ATTN: {
-      const Attn at = make_attn(S, A, in);
-      if (at.n_cached > 0) {
-        r.p[0] = at.kb;
-        r.p[1] = at.vb;
-        r.bytes[0] = r.bytes[1] = (uint32_t)at.n_cached * S.hd * 2u;
-        r.n = 2;
-      }
-      break;
-    }
-    default:
-      break;
-  }
-  return r;
-}
-
 // ---------------------------------------------------------------- loader warp
-__device__ bool producer_acquire(const DevState& S, SmemCtl* c, int slot, uint32_t ph) {
-  if (mbar_try_wait(&c->empty[slot], ph ^ 1)) return true;
+// A free slot for the next page: its previous page handed back by every compute warp,
+// and -- when the in-flight limit is set -- the page issued `inflight` copies earlier
+// landed, so that at most that many copies of this CTA queue in the memory system (the
+// ring still holds n_pages of landed pages as slack; fewer copies in flight shorten the
+// queues that the dependency-carrying loads and stores wait in).
+__device__ bool producer_wait(const DevState& S, SmemCtl* c, uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = 0;
   int k = 0;
-  while (!mbar_try_wait(&c->empty[slot], ph ^ 1)) {
+  while (!mbar_try_wait(bar, parity)) {
     if (c->abort) return false;
     if ((++k & 63) == 0) {
       const uint64_t t = globaltimer_ns();
@@ -274,15 +238,25 @@ __device__ bool producer_acquire(const DevState& S, SmemCtl* c, int slot, uint32
   }
   return true;
 }
+__device__ bool producer_acquire(const DevState& S, SmemCtl* c, int slot, uint32_t ph, long long issued) {
+  if (!producer_wait(S, c, &c->empty[slot], ph ^ 1)) return false;
+  const int F = S.inflight_pages;
+  if (F > 0 && F < S.n_pages && issued >= F) {
+    const int ps = slot - F < 0 ? slot - F + S.n_pages : slot - F;
+    const uint32_t pp = slot - F < 0 ? ph ^ 1u : ph;
+    if (!producer_wait(S, c, &c->full[ps], pp)) return false;
+  }
+  return true;
+}
 
 __device__ __noinline__ void producer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8_t* pages) {
   const uint64_t pol = l2_evict_first_policy();
   int slot = 0;
   uint32_t ph = 0;
+  long long issued = 0;
   const int cta = blockIdx.x;
   const int end = A.q_start[cta + 1];
   bool ok = true;
-  long long loaded = 0;
   for (int pc = A.q_start[cta]; pc < end && ok; ++pc) {
     const Instr in = load_instr(A.instr + pc);
     if (pc + 2 < end) prefetch_l1(A.instr + pc + 2);  // the next instructions, for both roles
@@ -312,13 +286,11 @@ __device__ __noinline__ void producer(const DevState& S, const StepArgs& A, Smem
         // segment k starts at seg[k] + j * WS: a page is at most two bulk copies
         const int n0 = g.segr[0] * g.spr();
         for (int i0 = 0; i0 < ns; i0 += kConsumerWarps) {
-          if (!producer_acquire(S, c, slot, ph)) {
+          if (!producer_acquire(S, c, slot, ph, issued++)) {
             ok = false;
             break;
           }
           const int i1 = min(ns, i0 + kConsumerWarps);
-          loaded += (long long)(i1 - i0) * sb;
-          c->loaded = loaded;
           mbar_arrive_expect_tx(&c->full[slot], (uint32_t)(i1 - i0) * sb);
           uint8_t* dst = pages + (size_t)slot * S.page_bytes;
           if (i0 < n0) {
@@ -342,12 +314,10 @@ __device__ __noinline__ void producer(const DevState& S, const StepArgs& A, Smem
           const int np = min(at.pb, at.n_cached - p0);
           const uint32_t bytes = (uint32_t)np * S.hd * 2u;
           for (int kv = 0; kv < 2; ++kv) {
-            if (!producer_acquire(S, c, slot, ph)) {
+            if (!producer_acquire(S, c, slot, ph, issued++)) {
               ok = false;
               break;
             }
-            loaded += bytes;
-            c->loaded = loaded;
             mbar_arrive_expect_tx(&c->full[slot], bytes);
             tma_load_1d(pages + (size_t)slot * S.page_bytes, (kv ? at.vb : at.kb) + (size_t)p0 * S.hd, bytes,
                         &c->full[slot], pol);
@@ -361,7 +331,7 @@ __device__ __noinline__ void producer(const DevState& S, const StepArgs& A, Smem
         const int n = in.a[1];
         const int64_t words = S.page_bytes / 8;
         for (int k = 0; k < n; ++k) {
-          if (!producer_acquire(S, c, slot, ph)) {
+          if (!producer_acquire(S, c, slot, ph, issued++)) {
             ok = false;
             break;
           }
@@ -395,38 +365,6 @@ __device__ __noinline__ void producer(const DevState& S, const StepArgs& A, Smem
       if (globaltimer_ns() - t0 > (uint64_t)S.timeout_ns) {
         set_err(S, 5u /*MK_ERR_STATE: page never released*/, -5, s);
         return;
-      }
-    }
-  }
-}
-
-// ---------------------------------------------------------------- L2 prefetch warp
-// Walks the CTA's queue ahead of the loader and pulls the weight / KV lines of upcoming
-// instructions into L2 (one line per lane, 4 KB per warp instruction), staying at most
-// l2_prefetch_bytes ahead of what the loader has issued.  The page ring holds only a few
-// microseconds of the stream; L2 (129 MB) lets HBM keep streaming while the compute warps
-// sit in dependency waits, staging and epilogues.  It uses the load/store path, so it
-// never queues in front of the loader's TMA copies.
-__device__ __noinline__ void l2_prefetcher(const DevState& S, const StepArgs& A, SmemCtl* c) {
-  if (S.l2_prefetch_bytes <= 0) return;
-  const int lane = threadIdx.x & 31;
-  const int cta = blockIdx.x, end = A.q_start[cta + 1];
-  long long issued = 0;
-  const uint64_t t0 = globaltimer_ns();
-  for (int pc = A.q_start[cta]; pc < end; ++pc) {
-    const Instr in = load_instr(A.instr + pc);
-    if (in.op == OP_END) break;
-    const Ranges r = instr_ranges(S, A, in);
-    for (int k = 0; k < r.n; ++k) {
-      const char* p = reinterpret_cast<const char*>(r.p[k]);
-      for (uint32_t off = 0; off < r.bytes[k]; off += 32u * 128u) {
-        while (issued - c->loaded >= (long long)S.l2_prefetch_bytes) {
-          if (c->abort || globaltimer_ns() - t0 > (uint64_t)S.timeout_ns) return;
-          __nanosleep(256);
-        }
-        const uint32_t o = off + (uint32_t)lane * 128u;
-        if (o < r.bytes[k]) prefetch_l2_line(p + o);
-        issued += min(32u * 128u, r.bytes[k] - off);
       }
     }
   }
@@ -502,51 +440,154 @@ __device__ __forceinline__ float4 load_v4(const float4* p, const DevState& S, Sm
   return any_nan4(v) ? poll_slow_v4(p, S, c) : v;
 }
 
+// Up to U 16-byte loads in flight (entries with p[u] == nullptr are skipped and read as
+// zeros); with sentinels, the vectors still holding one are re-read together until the
+// producers' values land (bounded, sets the abort flag on timeout).
+template <int SYNC, int U>
+__device__ __forceinline__ void load_vecs(const DevState& S, SmemCtl* c, const float4* const (&p)[U], float4 (&v)[U]) {
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (p[u] != nullptr) v[u] = SYNC == SYNC_COUNTER ? __ldcg(p[u]) : ld_poll_v4(p[u]);
+  }
+  if (SYNC == SYNC_SENTINEL) {
+    bool pend = false;
+#pragma unroll
+    for (int u = 0; u < U; ++u) pend |= any_nan4(v[u]);
+    if (pend) {
+      const uint64_t t0 = globaltimer_ns();
+      int k = 0;
+      while (pend) {
+        const int ns = 20 << (k < 8 ? k : 8);
+        __nanosleep(ns < S.backoff_max_ns ? ns : S.backoff_max_ns);
+        ++k;
+        pend = false;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          if (any_nan4(v[u])) {
+            v[u] = ld_poll_v4(p[u]);
+            pend |= any_nan4(v[u]);
+          }
+        }
+        if (pend && (c->abort || global_err(S) || globaltimer_ns() - t0 > (uint64_t)S.timeout_ns)) {
+          if (!global_err(S)) set_err(S, 4u, -1, -1);
+          c->abort = 1;
+          break;
+        }
+      }
+    }
+  }
+}
+
 template <int SYNC, typename Put>
 __device__ __forceinline__ void stage_vec(const DevState& S, const float4* src, int n4, SmemCtl* c, Put&& put) {
   constexpr int U = 4;
   const int tid = threadIdx.x;
   for (int base = 0; base < n4; base += U * kConsumerThreads) {
-    float4 v[U];
+    const float4* p[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int i = base + u * kConsumerThreads + tid;
-      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (i < n4) v[u] = SYNC == SYNC_COUNTER ? __ldcg(src + i) : ld_poll_v4(src + i);
+      p[u] = i < n4 ? src + i : nullptr;
     }
-    if (SYNC == SYNC_SENTINEL) {
-      bool pend = false;
-#pragma unroll
-      for (int u = 0; u < U; ++u) pend |= any_nan4(v[u]);
-      if (pend) {
-        const uint64_t t0 = globaltimer_ns();
-        int k = 0;
-        while (pend) {
-          const int ns = 20 << (k < 8 ? k : 8);
-          __nanosleep(ns < S.backoff_max_ns ? ns : S.backoff_max_ns);
-          ++k;
-          pend = false;
-#pragma unroll
-          for (int u = 0; u < U; ++u) {
-            if (any_nan4(v[u])) {
-              v[u] = ld_poll_v4(src + base + u * kConsumerThreads + tid);
-              pend |= any_nan4(v[u]);
-            }
-          }
-          if (pend && (c->abort || global_err(S) || globaltimer_ns() - t0 > (uint64_t)S.timeout_ns)) {
-            if (!global_err(S)) set_err(S, 4u, -1, -1);
-            c->abort = 1;
-            break;
-          }
-        }
-      }
-    }
+    float4 v[U];
+    load_vecs<SYNC, U>(S, c, p, v);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int i = base + u * kConsumerThreads + tid;
       if (i < n4) put(i, v[u]);
     }
   }
+}
+
+// The O-proj input merged from the KV-split partials while it is staged (the §8.2
+// ATTN_REDUCE folded into O_PROJ): for every (b, kv head j, group head g),
+//   o = sum_s w_s o_s,  w_s = 2^(m_s - M) / sum_s' 2^(m_s' - M) l_s',  M = max_s m_s,
+// over the splits s < NS_b that ran this step (o_s, m_s, l_s: split s's weighted value
+// sum, running max and exp-sum, in log2 units).  Every O-proj unit merges all heads, so
+// none waits on a merge step.  Fixed summation order (s ascending).  The unit holding O-proj
+// row 0 also publishes o (for mk_read_activation).
+template <int SYNC, int NB>
+__device__ void stage_merge(const DevState& S, const StepArgs& A, int l, float* xbuf, float* scratch, SmemCtl* c,
+                            float* act, bool publish) {
+  const int tid = threadIdx.x, B = A.B;
+  const int HD = S.hd, G = S.Hq / S.Hkv, RW = HD + kPartExtra, Hkv = S.Hkv, SS = S.S, K = S.Hq * HD;
+  const float* part = act_ptr(S, act, ACT_PART, l);  // [b][j][s][g][RW]
+  const int nrec = B * Hkv * SS * G;
+  float2* ml = reinterpret_cast<float2*>(scratch);         // [b][j][s][g] (max, sum)
+  float* wts = scratch + 2 * nrec;                          // [b][j][g][s] merge weights
+  // 1. (max, sum) of every record that was written this step
+  {
+    constexpr int U = 4;
+    for (int base = 0; base < nrec; base += U * kConsumerThreads) {
+      const float4* p[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int r = base + u * kConsumerThreads + tid;
+        p[u] = nullptr;
+        if (r < nrec) {
+          const int s = (r / G) % SS, b = r / (G * SS * Hkv);
+          if (s < active_splits(S, A, b)) p[u] = reinterpret_cast<const float4*>(part + (size_t)r * RW + HD);
+        }
+      }
+      float4 v[U];
+      load_vecs<SYNC, U>(S, c, p, v);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int r = base + u * kConsumerThreads + tid;
+        if (r < nrec) ml[r] = make_float2(v[u].x, v[u].y);
+      }
+    }
+  }
+  consumer_sync();
+  // 2. weights per (b, j, g)
+  for (int t = tid; t < B * Hkv * G; t += kConsumerThreads) {
+    const int g = t % G, bj = t / G, b = bj / Hkv;
+    const int NS = active_splits(S, A, b);
+    float M = -CUDART_INF_F;
+    for (int s = 0; s < NS; ++s) M = fmaxf(M, ml[(bj * SS + s) * G + g].x);
+    float den = 0.f;
+    for (int s = 0; s < NS; ++s) {
+      const float2 r = ml[(bj * SS + s) * G + g];
+      den = fmaf(exp2f(r.x - M), r.y, den);
+    }
+    const float inv = 1.0f / den;
+    for (int s = 0; s < NS; ++s) wts[t * SS + s] = exp2f(ml[(bj * SS + s) * G + g].x - M) * inv;
+  }
+  consumer_sync();
+  // 3. the merged vectors, four splits in flight per output vector
+  const int n_out = B * K / 4, per_b = K / 4, per_h = HD / 4;
+  float4* x4 = reinterpret_cast<float4*>(xbuf);
+  float4* o4 = reinterpret_cast<float4*>(act_ptr(S, act, ACT_O, l));
+  for (int i = tid; i < n_out; i += kConsumerThreads) {
+    const int b = i / per_b, h = (i % per_b) / per_h, e4 = i % per_h;
+    const int j = h / G, g = h % G, NS = active_splits(S, A, b);
+    const float* w = wts + ((b * Hkv + j) * G + g) * SS;
+    const float* base = part + (((size_t)(b * Hkv + j) * SS) * G + g) * RW + 4 * e4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < NS; s0 += 4) {
+      const float4* p[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        p[u] = s0 + u < NS ? reinterpret_cast<const float4*>(base + (size_t)(s0 + u) * G * RW) : nullptr;
+      float4 v[4];
+      load_vecs<SYNC, 4>(S, c, p, v);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (s0 + u < NS) {
+          const float ws = w[s0 + u];
+          acc.x = fmaf(ws, v[u].x, acc.x);
+          acc.y = fmaf(ws, v[u].y, acc.y);
+          acc.z = fmaf(ws, v[u].z, acc.z);
+          acc.w = fmaf(ws, v[u].w, acc.w);
+        }
+      }
+    }
+    x4[i] = acc;
+    if (publish) o4[i] = acc;
+  }
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = n_out + tid; i < NB * per_b; i += kConsumerThreads) x4[i] = z;
 }
 
 // B rows of K fp32 values ([B][K], 16-byte aligned) into the x buffer; padding rows up
@@ -686,7 +727,8 @@ __device__ __forceinline__ void slice_dot_smem(const uint8_t* wp, const float* x
   for (int b = 0; b < NB; ++b) acc[b] = a0[b] + a1[b];
 }
 
-__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
+// silu(u) = u / (1 + e^-u); the fast exponential (a few ulp) is far inside the tolerance
+__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
 
 template <typename WT, int SYNC, int NB>
 __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const Instr& in, SmemCtl* c, uint8_t* pages,
@@ -707,7 +749,10 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
       stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_H, S.L), iptr(in, kP2), B, xbuf, c);
       break;
     case OP_OPROJ:
-      stage_copy<SYNC, NB>(S, act_ptr(S, act, ACT_O, l), g.K, B, xbuf, c);
+      if (in.flags & F_MERGE_IN)
+        stage_merge<SYNC, NB>(S, A, l, xbuf, scratch, c, act, in.a[0] == 0);
+      else
+        stage_copy<SYNC, NB>(S, act_ptr(S, act, ACT_O, l), g.K, B, xbuf, c);
       break;
     default:  // OP_DOWN
       stage_copy<SYNC, NB>(S, act_ptr(S, act, ACT_A, l), g.K, B, xbuf, c);
@@ -723,6 +768,12 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
     const float* hin = act_ptr(S, act, in.op == OP_OPROJ ? ACT_H : ACT_HMID, l);
     hres = load_act<SYNC>(hin + (size_t)b * S.d + in.a[0] + r, S, c);
   }
+  // likewise the (cos, sin) of the thread's first RoPE pair, and 1/rms per sequence (read
+  // by the epilogue after the barrier that ends the pages)
+  float2 cs0 = make_float2(1.f, 0.f);
+  if (in.op == OP_QKV && in.a[0] < 2 && tid < in.a[3] * B)
+    cs0 = S.rope[(size_t)A.pos[tid / in.a[3]] * (S.hd / 2) + in.a[2] + tid % in.a[3]];
+  if ((in.op == OP_QKV || in.op == OP_UPGATE || in.op == OP_LMHEAD) && tid < B) c->inv_rms[tid] = inv_rms_of<NB>(S, c, tid);
 
   // 2. stream the slices: warp w takes slice i0 + w of every page of 8 slices
   float* rowpart = scratch;  // [rows][spr][NB]
@@ -804,18 +855,19 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
     return t;
   };
   const int R = g.rows();
+  const long long ck0 = trace ? clock64() : 0;
   switch (in.op) {
     case OP_QKV: {
       const int mat = in.a[0], head = in.a[1], i0 = in.a[2], n = in.a[3];
       const int hd = S.hd, half = hd / 2;
       for (int t = tid; t < n * B; t += kConsumerThreads) {
         const int r = t % n, b = t / n;
-        const float ir = inv_rms_of<NB>(S, c, b);
+        const float ir = c->inv_rms[b];
         float va = rowsum(r, b) * ir, vb = rowsum(r + n, b) * ir;
         const int i = i0 + r;
         const int pos = A.pos[b];
         if (mat < 2) {  // rotate-half RoPE on the pair (i, i + hd/2)
-          const float2 cs = S.rope[(size_t)pos * half + i];
+          const float2 cs = t == tid ? cs0 : S.rope[(size_t)pos * half + i];
           const float xa = va * cs.x - vb * cs.y;
           const float xb = vb * cs.x + va * cs.y;
           va = xa;
@@ -853,7 +905,7 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
       float* a = act_ptr(S, act, ACT_A, l);
       for (int t = tid; t < n * B; t += kConsumerThreads) {
         const int r = t % n, b = t / n;
-        const float ir = inv_rms_of<NB>(S, c, b);
+        const float ir = c->inv_rms[b];
         a[(size_t)b * S.F + row0 + r] = silu_f(rowsum(r, b) * ir) * (rowsum(r + n, b) * ir);
       }
       break;
@@ -877,7 +929,7 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
       for (int t = tid; t < R * NB; t += kConsumerThreads) {
         const int r = t % R, b = t / R;
         if (b >= B) continue;
-        const float z = rowsum(r, b) * inv_rms_of<NB>(S, c, b);
+        const float z = rowsum(r, b) * c->inv_rms[b];
         const int row = row0 + r;
         if (A.logits) A.logits[(size_t)b * S.V + row] = z;
         if (isnan(z)) atomicOr(&S.ctl->nan_seen, 1u);
@@ -900,7 +952,10 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
       break;
     }
   }
-  if (tid == 0 && trace) c->tmark[3] = globaltimer_ns();
+  if (tid == 0 && trace) {
+    c->tmark[3] = globaltimer_ns();
+    c->tmark[5] = (uint64_t)(clock64() - ck0);
+  }
 }
 
 // ---------------------------------------------------------------- attention
@@ -1377,7 +1432,6 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
       c->last_issue_phase[i] = -1;
     }
     c->abort = 0;
-    c->loaded = 0;
     mbar_fence_init();
   }
   if (tid < kMaxBatch) c->best[tid] = 0ull;
@@ -1396,7 +1450,6 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
   if (tid >= kConsumerThreads) {
     const int w = tid >> 5;
     if (w == kLoaderWarp && (tid & 31) == 0) producer(S, A, c, pages);
-    if (w == kPrefetchWarp) l2_prefetcher(S, A, c);
     return;
   }
   consumer<WT, SYNC>(S, A, c, pages, xbuf, scratch);

@@ -133,7 +133,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_desc* desc, const mk_
     if (!e.empty()) return fail(MK_ERR_INVALID, e);
   }
   Plan plan;
-  e = build_plan(m, g, n_cta, B, 0, true, &plan);
+  e = build_plan(m, g, n_cta, B, 0, choose_merge(m, g, B, true, 0), &plan);
   if (!e.empty()) return fail(MK_ERR_INVALID, "schedule: " + e);
   ModelPtrs mp;
   mp.final_norm = w->final_norm;
@@ -250,7 +250,6 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_desc* desc, const mk_
   S.sync_mode = MK_SYNC_COUNTER;
   S.timeout_ns = 2000000000LL;
   S.backoff_max_ns = 256;
-  S.l2_prefetch_bytes = 256 * 1024;
   S.split_min_positions = 16;
   // the kernel's kv-cache addressing uses the caller's layout [max_batch, Hkv, max_ctx, hd]
   // only through max_ctx, and its activation rows through max_batch: both as set above

@@ -96,11 +96,21 @@ static Instr mk_instr(int op, int layer, int wait_ctr, uint32_t wait_n, int sign
   return in;
 }
 
-std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B, int drop_signal, bool fuse_reduce,
+int choose_merge(const ModelShape& m, const Geometry& g, int B, bool counters, int requested) {
+  const int G = m.Hq / m.Hkv;
+  const long long part_bytes = 4LL * B * m.Hkv * g.S * G * (m.hd + kPartExtra);
+  const long long weight_floats = 3LL * B * m.Hkv * g.S * G;  // (max, sum) pairs + merge weights
+  const bool fits = part_bytes <= kMergeInBytes && weight_floats * 4 <= g.scratch_bytes;
+  if (requested == 2 || (requested == 0 && fits)) return MERGE_IN_OPROJ;
+  return counters ? MERGE_LAST_ARRIVER : MERGE_OP;
+}
+
+std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B, int drop_signal, int merge,
                        Plan* p) {
   if (B < 1 || B > m.max_batch) return "batch out of range";
   *p = Plan();
-  p->fused_reduce = fuse_reduce;
+  p->merge = merge;
+  const bool fuse_reduce = merge == MERGE_LAST_ARRIVER;
   p->n_cta = n_cta;
   p->B = B;
   p->queues.assign(n_cta, {});
@@ -184,7 +194,8 @@ std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B,
     }
     // ATTENTION: B * Hkv * S split units, dealt round-robin.  Fused: each unit counts its
     // arrival on the (b, j) counter; the last of the S merges the splits and signals c_red
-    // (one signal per (b, j) and step).
+    // (one signal per (b, j) and step).  Merged in the O-proj staging: every unit signals
+    // c_att, which the O-proj units wait for.
     const int c_att = new_ctr();
     const int c_red = new_ctr();
     {
@@ -207,7 +218,7 @@ std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B,
       }
     }
     // ATTN_REDUCE: one unit per (sequence, kv head), spread over the CTAs
-    if (!fuse_reduce) {
+    if (merge == MERGE_OP) {
       const int nu = B * m.Hkv;
       for (int u = 0; u < nu; ++u) {
         Instr in = mk_instr(OP_ATTN_REDUCE, l, c_att, 0, c_red);
@@ -217,7 +228,7 @@ std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B,
       }
     }
     // O_PROJ, MLP_UP_GATE, MLP_DOWN: row ranges
-    auto rows_op = [&](int op, int rows, int K, int ws, int segs, int wait, int sig) {
+    auto rows_op = [&](int op, int rows, int K, int ws, int segs, int wait, int sig, uint8_t flags) {
       const int cap = rows_cap(K, ws, segs);
       for (int c = 0; c < n_cta; ++c) {
         int r0 = split_lo(rows, n_cta, c);
@@ -225,6 +236,7 @@ std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B,
         while (r0 < r1) {
           const int n = std::min(r1 - r0, cap);
           Instr in = mk_instr(op, l, wait, 0, sig);
+          in.flags = flags;
           in.a[0] = r0;
           in.a[1] = n;
           emit(c, in);
@@ -233,11 +245,14 @@ std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B,
       }
     };
     const int c_o = new_ctr();
-    rows_op(OP_OPROJ, m.d, m.Hq * m.hd, g.ws_o, 1, c_red, c_o);
+    if (merge == MERGE_IN_OPROJ)
+      rows_op(OP_OPROJ, m.d, m.Hq * m.hd, g.ws_o, 1, c_att, c_o, F_MERGE_IN);
+    else
+      rows_op(OP_OPROJ, m.d, m.Hq * m.hd, g.ws_o, 1, c_red, c_o, 0);
     const int c_ug = new_ctr();
-    rows_op(OP_UPGATE, m.F, m.d, g.ws_up, 2, c_o, c_ug);
+    rows_op(OP_UPGATE, m.F, m.d, g.ws_up, 2, c_o, c_ug, 0);
     const int c_dn = new_ctr();
-    rows_op(OP_DOWN, m.d, m.F, g.ws_down, 1, c_ug, c_dn);
+    rows_op(OP_DOWN, m.d, m.F, g.ws_down, 1, c_ug, c_dn, 0);
     prev = c_dn;
   }
   // LM_HEAD: vocabulary rows; the last chunk of each CTA publishes its argmax
@@ -390,7 +405,7 @@ std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p)
       if (in.op != OP_LMHEAD && in.layer >= m.L) return "layer out of range";
       if (in.signal_ctr >= p.n_counters || in.wait_ctr >= p.n_counters) return "counter index out of range";
       const bool fused = in.op == OP_ATTN && in.a[4] >= 0;
-      if (fused && (!p.fused_reduce || in.a[4] >= p.n_counters)) return "bad arrival counter";
+      if (fused && (p.merge != MERGE_LAST_ARRIVER || in.a[4] >= p.n_counters)) return "bad arrival counter";
       // a fused split signals only when it is the last of its (b, j): once per (b, j)
       if (in.signal_ctr >= 0 && (!fused || in.a[2] == 0)) sig[in.signal_ctr]++;
       group_units[group_of(in)]++;
@@ -414,7 +429,14 @@ std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p)
         case OP_ATTN_REDUCE:
           if (in.a[0] < 0 || in.a[0] >= B || in.a[1] < 0 || in.a[1] >= m.Hkv) return "REDUCE arguments out of range";
           break;
-        case OP_OPROJ: rows = in.a[1]; K = m.Hq * m.hd; ws = g.ws_o; break;
+        case OP_OPROJ:
+          rows = in.a[1];
+          K = m.Hq * m.hd;
+          ws = g.ws_o;
+          if (((in.flags & F_MERGE_IN) != 0) != (p.merge == MERGE_IN_OPROJ)) return "O-proj merge flag mismatch";
+          if ((in.flags & F_MERGE_IN) && 3LL * B * m.Hkv * g.S * (m.Hq / m.Hkv) > scratch_floats)
+            return "split-merge weights exceed the scratch";
+          break;
         case OP_UPGATE: rows = 2 * in.a[1]; K = m.d; ws = g.ws_up; break;
         case OP_DOWN: rows = in.a[1]; K = m.F; ws = g.ws_down; break;
         case OP_LMHEAD: rows = in.a[1]; K = m.d; ws = g.ws_lm; break;
@@ -470,7 +492,7 @@ std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p)
       case OP_QKV: req[0] = h_writer; return 1;
       case OP_ATTN: req[0] = 1 + 6 * l + 0; return 1;
       case OP_ATTN_REDUCE: req[0] = 1 + 6 * l + 1; return 1;
-      case OP_OPROJ: req[0] = 1 + 6 * l + (p.fused_reduce ? 1 : 2); req[1] = h_writer; return 2;
+      case OP_OPROJ: req[0] = 1 + 6 * l + (p.merge == MERGE_OP ? 2 : 1); req[1] = h_writer; return 2;
       case OP_UPGATE: req[0] = 1 + 6 * l + 3; return 1;
       case OP_DOWN: req[0] = 1 + 6 * l + 4; req[1] = 1 + 6 * l + 3; return 2;
       case OP_LMHEAD: req[0] = 1 + 6 * (m.L - 1) + 5; return 1;
@@ -559,7 +581,7 @@ std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p)
   };
   if (!once(emb) || !once(lm)) return "embedding or LM-head rows not covered exactly once";
   for (int l = 0; l < m.L; ++l)
-    if (!once(qkv[l]) || !once(att[l]) || (!p.fused_reduce && !once(red[l])) || !once(orow[l]) || !once(urow[l]) ||
+    if (!once(qkv[l]) || !once(att[l]) || (p.merge == MERGE_OP && !once(red[l])) || !once(orow[l]) || !once(urow[l]) ||
         !once(drow[l]))
       return fmt("layer %lld: an op's outputs are not covered exactly once", l);
   return "";

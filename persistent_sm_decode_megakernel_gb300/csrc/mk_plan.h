@@ -37,7 +37,7 @@ struct Plan {
   // multi-launch control: phases in dependency order; per phase the compacted queues
   std::vector<std::vector<std::vector<Instr>>> phase_queues;
   int64_t weight_bytes = 0;               // streamed weight bytes per step
-  bool fused_reduce = false;              // the split merge runs in the last-arriving ATTN unit
+  int merge = MERGE_OP;                   // MergeMode of the KV-split partials
 };
 
 // device addresses the host writes into the instructions (see the layout in mk_internal.h)
@@ -50,8 +50,13 @@ struct ModelPtrs {
 // returns "" on success, else a message
 std::string make_geometry(const ModelShape& m, int n_cta, int page_bytes, int n_pages_req, int kv_splits,
                           int smem_limit, Geometry* g);
-std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B, int drop_signal, bool fuse_reduce,
+std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B, int drop_signal, int merge,
                        Plan* p);
+// the merge a schedule of batch B uses: `requested` 1 or 2 (mk_options.attn_merge), or 0 =
+// in the O-proj staging while one step's partials stay under kMergeInBytes, else the
+// separate step of the sync mode
+constexpr long long kMergeInBytes = 24 * 1024;
+int choose_merge(const ModelShape& m, const Geometry& g, int B, bool counters, int requested);
 void bake_pointers(const ModelShape& m, const ModelPtrs& w, Plan* p);
 std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p);
 

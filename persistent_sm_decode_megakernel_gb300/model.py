@@ -78,12 +78,13 @@ class Decoder:
     """A context over a DeviceModel (mk_create ... mk_destroy)."""
 
     def __init__(self, dm: DeviceModel, sync_mode=0, exec_mode=0, trace=0, timeout_s=2.0, page_bytes=0,
-                 n_pages=0, kv_splits=0, max_ctas=0, fault_drop_signal=0, backoff_max_ns=0, l2_prefetch_kb=0,
-                 split_min_positions=0, stream=None):
+                 n_pages=0, kv_splits=0, max_ctas=0, fault_drop_signal=0, backoff_max_ns=0,
+                 split_min_positions=0, attn_merge=0, inflight_pages=0, stream=None):
         self.dm = dm
         self.stream = stream if stream is not None else torch.cuda.current_stream(dm.device)
         self.opts = mk_options(sync_mode, exec_mode, page_bytes, n_pages, kv_splits, trace, timeout_s,
-                               backoff_max_ns, max_ctas, fault_drop_signal, l2_prefetch_kb, split_min_positions)
+                               backoff_max_ns, max_ctas, fault_drop_signal, split_min_positions,
+                               attn_merge, inflight_pages)
         d = dm.desc()
         w, kv, _keep = dm.abi_structs()
         h = ctypes.c_void_p()
@@ -163,5 +164,5 @@ class Decoder:
         buf = (mk_trace_rec * max_records)()
         n = ctypes.c_int()
         check(mk_get_trace(self.h, buf, max_records, ctypes.byref(n)), "mk_get_trace")
-        return [(r.cta, r.pc, r.op, r.layer, r.t_fetch, r.t_ready, r.t_end, *list(r.t_mark)[:4], r.t_mark[4])
+        return [(r.cta, r.pc, r.op, r.layer, r.t_fetch, r.t_ready, r.t_end, *list(r.t_mark))
                 for r in buf[: n.value]]

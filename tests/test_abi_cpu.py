@@ -69,14 +69,24 @@ def test_plan_batches_and_sizes(mk):
 
 def test_plan_multilaunch_counts_launches(mk):
     cfg = synth.CONFIGS["2b"]
-    # counter sync merges the KV splits inside the attention launch; sentinel sync keeps
-    # a separate reduce launch per layer
-    st, info = _plan(mk, _desc(mk, cfg), 152, exec_mode=mk.MK_EXEC_MULTILAUNCH)
-    assert st == mk.MK_OK
-    assert info.launches_per_step == 5 * cfg.n_layers + 2
-    st, info = _plan(mk, _desc(mk, cfg), 152, exec_mode=mk.MK_EXEC_MULTILAUNCH, sync_mode=mk.MK_SYNC_SENTINEL)
-    assert st == mk.MK_OK
-    assert info.launches_per_step == 6 * cfg.n_layers + 2
+    L = cfg.n_layers
+    # the KV-split merge: inside the O-proj staging (attn_merge 2) or in the last-arriving
+    # split (counter sync) -- five launches per layer either way -- or a separate reduce
+    # launch per layer (sentinel sync); auto (0) keeps the separate step at the 2b size
+    for sync, merge, per_layer in ((0, 0, 5), (1, 0, 6), (0, 2, 5), (1, 2, 5), (0, 1, 5), (1, 1, 6)):
+        st, info = _plan(mk, _desc(mk, cfg), 152, exec_mode=mk.MK_EXEC_MULTILAUNCH, sync_mode=sync, attn_merge=merge)
+        assert st == mk.MK_OK, mk.mk_last_error()
+        assert info.launches_per_step == per_layer * L + 2, (sync, merge)
+
+
+def test_plan_merge_choice_and_bad_option(mk):
+    cfg = synth.CONFIGS["2b"]
+    for merge in (0, 1, 2):
+        for b in (1, 2, 4):
+            st, _ = _plan(mk, _desc(mk, cfg, max_batch=b), 152, attn_merge=merge)
+            assert st == mk.MK_OK, (merge, b, mk.mk_last_error())
+    st, _ = _plan(mk, _desc(mk, cfg), 152, attn_merge=3)
+    assert st == mk.MK_ERR_INVALID
 
 
 @pytest.mark.parametrize("sync", [0, 1])

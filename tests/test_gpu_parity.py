@@ -226,16 +226,33 @@ def test_2b_fp16_full_prompt_teacher_forced(lib):
 
 
 @pytest.mark.parametrize("page_bytes", [0, 8192])
-def test_tiny_long_context_many_splits(lib, tiny, page_bytes):
+@pytest.mark.parametrize("merge", [1, 2], ids=["merge-step", "merge-in-oproj"])
+def test_tiny_long_context_many_splits(lib, tiny, page_bytes, merge):
     """A 600-position context: the step uses several KV splits (one page of positions
-    each, up to the schedule's count), merged in the last-arriving split."""
+    each, up to the schedule's count), merged in a separate step (the ATTN_REDUCE op with
+    sentinels, the last-arriving split with counters) or inside the O-proj staging."""
     cfg, w, m = tiny
     P, n_new = 600, 4
     prompt = synth.gen_prompts(cfg, 1, P)
     toks, zref = oracle_run(cfg, w, prompt, n_new, model=m)
     for sync in (0, 1):
         dm = lib.DeviceModel(cfg, w, max_batch=1, max_ctx=P + n_new)
-        dec = lib.Decoder(dm, sync_mode=sync, page_bytes=page_bytes)
+        dec = lib.Decoder(dm, sync_mode=sync, page_bytes=page_bytes, attn_merge=merge)
         z, tg = gpu_teacher_forced(dec, prompt, toks, n_new, cfg.vocab)
         dec.close()
         assert_parity(z, tg, zref, toks, P)
+
+
+@pytest.mark.parametrize("merge", [1, 2], ids=["merge-step", "merge-in-oproj"])
+@pytest.mark.parametrize("sync", [0, 1], ids=["counter", "sentinel"])
+def test_tiny_batched_merge_modes(lib, tiny, merge, sync):
+    """Batch 2 with ragged positions under both split-merge placements."""
+    cfg, w, m = tiny
+    P, n_new = cfg.prompt_len, 6
+    prompt = synth.gen_prompts(cfg, 2, P)
+    toks, zref = oracle_run(cfg, w, prompt, n_new, model=m)
+    dm = lib.DeviceModel(cfg, w, max_batch=2, max_ctx=P + n_new)
+    dec = lib.Decoder(dm, sync_mode=sync, attn_merge=merge)
+    z, tg = gpu_teacher_forced(dec, prompt, toks, n_new, cfg.vocab)
+    dec.close()
+    assert_parity(z, tg, zref, toks, P)
