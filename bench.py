@@ -37,24 +37,25 @@ UNIT = "tok/s"
 PROMPT = 512
 NOMINAL_HBM_GBS = 7900.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "mk_step_kernel_2b_b1.txt")
-KERNEL_SOURCES = ["mk_kernel.cuh", "mk_device.cuh", "mk_internal.h", "mk_k_f16_counter.cu"]
+KERNEL_SOURCES = ["mk_kernel.cuh", "mk_device.cuh", "mk_internal.h"]
 
 
-def kernel_source_hash():
+def kernel_source_hash(sync="sentinel"):
+    """Hash of the sources the timed kernel instance is compiled from."""
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES + [f"mk_k_f16_{sync}.cu"]:
         with open(os.path.join(ROOT, "persistent_sm_decode_megakernel_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
+def profiled_traffic(sync="sentinel"):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the
     current kernel sources (else None)."""
     try:
         with open(PROFILE_SUMMARY) as f:
             kv = dict(l.split(":", 1) for l in f.read().splitlines() if ":" in l)
-        if kv.get("kernel_source_sha", "").strip() != kernel_source_hash():
+        if kv.get("kernel_source_sha", "").strip() != kernel_source_hash(sync):
             return None
         return float(kv["dram_bytes_per_launch"].strip())
     except (OSError, KeyError, ValueError):
@@ -236,7 +237,7 @@ def main():
     ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--sync", default="counter", choices=["counter", "sentinel"])
+    ap.add_argument("--sync", default="sentinel", choices=["counter", "sentinel"])
     ap.add_argument("--exec", default="persistent", choices=["persistent", "multilaunch"])
     ap.add_argument("--batch", type=int, default=1)
     args = ap.parse_args()
@@ -318,7 +319,7 @@ def main():
                "sample": f"{n} fp64 oracle decode steps of the same 2B model, batch 1, from an empty cache "
                          f"(context 1..{n}; attention is a few % of the work at the GPU's contexts), "
                          f"{dt:.1f} s after 1 untimed step"}
-    traffic = profiled_traffic()
+    traffic = profiled_traffic(args.sync)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": 1000.0 * total_s / K, "higher_is_better": True, "scaling": "weak",

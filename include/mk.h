@@ -54,7 +54,7 @@ typedef struct {
   int dtype;              /* mk_dtype of weights AND KV cache                            */
   float rms_eps, rope_theta;
   int max_batch;          /* 1..16 sequences per step                                    */
-  int max_ctx;            /* KV-cache capacity in positions                              */
+  int max_ctx;            /* KV-cache capacity in positions, at most 4194304 (2^22)      */
 } mk_model_desc;
 
 /* Weights: device pointers, row-major, nn.Linear convention [out, in], 16-byte aligned.
@@ -99,8 +99,10 @@ typedef struct {
                              input staging of every O-proj unit (no extra dependency hop;
                              auto picks it when the partials of a step are small)       */
   int inflight_pages;     /* at most this many page copies of a CTA in flight at once
-                             (0: no limit below the pool size; landed pages still fill
-                             the whole pool)                                             */
+                             (0: default 2; < 0: the pool size).  Landed pages still
+                             fill the whole pool; fewer copies queued in the memory
+                             system shorten the waits of the loads and stores that
+                             carry the dependencies between ops                          */
 } mk_options;
 
 typedef struct {

@@ -38,6 +38,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// the same test, but a thread whose phase has not completed is suspended until it does or
+// until about hint_ns pass (no issue slots or shared-memory bandwidth spent spinning)
+__device__ __forceinline__ bool mbar_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // ---------------------------------------------------------------- TMA bulk copy
 // L2 policy: weights and KV are read once per step -- evict them first so activations
 // and counters stay resident (the NVIDIA form of the non-temporal hints of §7.5).

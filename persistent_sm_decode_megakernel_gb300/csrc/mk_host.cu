@@ -92,7 +92,7 @@ std::string check_desc(const mk_model_desc* d) {
   if (d->n_heads % d->n_kv_heads) return "n_heads must be a multiple of n_kv_heads";
   if (d->dtype != MK_F16 && d->dtype != MK_BF16) return "dtype must be MK_F16 or MK_BF16";
   if (d->max_batch < 1 || d->max_batch > kMaxBatch) return "max_batch must be in [1, 16]";
-  if (d->max_ctx < 1) return "max_ctx must be positive";
+  if (d->max_ctx < 1 || d->max_ctx > (1 << 22)) return "max_ctx must be in [1, 4194304]";
   if (!(d->rms_eps > 0.f) || !(d->rope_theta > 0.f)) return "rms_eps and rope_theta must be positive";
   if (d->d_model % 8 || d->ffn_dim % 8) return "d_model and ffn_dim must be multiples of 8";
   return "";
@@ -451,7 +451,7 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
   S.timeout_ns = (int64_t)(o.wait_timeout_s * 1e9);
   S.backoff_max_ns = o.backoff_max_ns;
   S.split_min_positions = o.split_min_positions > 0 ? o.split_min_positions : 16;
-  S.inflight_pages = o.inflight_pages > 0 ? o.inflight_pages : 0;
+  S.inflight_pages = o.inflight_pages < 0 ? 0 : (o.inflight_pages == 0 ? 2 : o.inflight_pages);
   ModelPtrs& mp = ctx->ptrs;
   mp.final_norm = w->final_norm;
   mp.lm_head = w->lm_head;

@@ -141,7 +141,7 @@ struct DevState {
   int64_t timeout_ns;
   int backoff_max_ns;
   int split_min_positions;     // a KV split of a step covers at least this many positions
-  int inflight_pages;          // loader: page copies in flight at most (0: the pool size)
+  int inflight_pages;          // loader: page copies in flight at most (0: up to the pool size)
   // self-test buffers
   int64_t* test_buf;
   int64_t test_len;

@@ -37,7 +37,7 @@ static_assert(sizeof(SmemCtl) <= kCtlSmem, "control block fits");
 enum { SYNC_COUNTER = 0, SYNC_SENTINEL = 1 };
 
 // ---------------------------------------------------------------- errors
-__device__ __forceinline__ void set_err(const DevState& S, uint32_t code, int pc, int ctr) {
+__device__ __noinline__ void set_err(const DevState& S, uint32_t code, int pc, int ctr) {
   if (atomicCAS(&S.ctl->err.code, 0u, code) == 0u) {
     S.ctl->err.cta = blockIdx.x;
     S.ctl->err.pc = pc;
@@ -191,8 +191,8 @@ __device__ __forceinline__ Attn make_attn(const DevState& S, const StepArgs& A, 
   const int npos = a.active ? A.pos[a.b] + 1 : 1;
   a.nsp = a.active ? active_splits(S, A, a.b) : 1;
   a.active = a.active && a.s < a.nsp;
-  a.t0 = (int)((int64_t)a.s * npos / a.nsp);
-  a.t1 = (int)((int64_t)(a.s + 1) * npos / a.nsp);
+  a.t0 = (int)((uint32_t)(a.s * npos) / (uint32_t)a.nsp);  // s * npos < 2^31 (S <= 256, npos < 2^23)
+  a.t1 = (int)((uint32_t)((a.s + 1) * npos) / (uint32_t)a.nsp);
   const int tc = min(a.t1, npos - 1);
   a.n_cached = max(0, tc - a.t0);
   a.has_new = (a.t1 == npos);
@@ -219,26 +219,20 @@ __device__ __forceinline__ float* act_ptr(const DevState& S, float* act, int kin
 // landed, so that at most that many copies of this CTA queue in the memory system (the
 // ring still holds n_pages of landed pages as slack; fewer copies in flight shorten the
 // queues that the dependency-carrying loads and stores wait in).
-__device__ bool producer_wait(const DevState& S, SmemCtl* c, uint64_t* bar, uint32_t parity) {
+__device__ __noinline__ bool producer_wait(const DevState& S, SmemCtl* c, uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = 0;
-  int k = 0;
-  while (!mbar_try_wait(bar, parity)) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_wait_hint(bar, parity, 2000u)) {
     if (c->abort) return false;
-    if ((++k & 63) == 0) {
-      const uint64_t t = globaltimer_ns();
-      if (t0 == 0) {
-        t0 = t;
-      } else if (t - t0 > (uint64_t)S.timeout_ns) {
-        set_err(S, 4u, -3, -1);
-        c->abort = 1;
-        return false;
-      }
+    if (globaltimer_ns() - t0 > (uint64_t)S.timeout_ns) {
+      set_err(S, 4u, -3, -1);
+      c->abort = 1;
+      return false;
     }
   }
   return true;
 }
-__device__ bool producer_acquire(const DevState& S, SmemCtl* c, int slot, uint32_t ph, long long issued) {
+__device__ __noinline__ bool producer_acquire(const DevState& S, SmemCtl* c, int slot, uint32_t ph, long long issued) {
   if (!producer_wait(S, c, &c->empty[slot], ph ^ 1)) return false;
   const int F = S.inflight_pages;
   if (F > 0 && F < S.n_pages && issued >= F) {
@@ -376,10 +370,10 @@ struct Ring {
   uint32_t ph;
 };
 
-__device__ __forceinline__ const uint8_t* page_wait(const DevState& S, SmemCtl* c, uint8_t* pages, const Ring& r) {
-  if (!mbar_try_wait(&c->full[r.slot], r.ph)) {
+__device__ __noinline__ void page_wait_slow(const DevState& S, SmemCtl* c, const Ring& r) {
+  {
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(&c->full[r.slot], r.ph)) {
+    while (!mbar_wait_hint(&c->full[r.slot], r.ph, 2000u)) {
       if (c->abort) break;
       if (globaltimer_ns() - t0 > (uint64_t)S.timeout_ns) {
         set_err(S, 4u, -6, r.slot);
@@ -388,6 +382,9 @@ __device__ __forceinline__ const uint8_t* page_wait(const DevState& S, SmemCtl* 
       }
     }
   }
+}
+__device__ __forceinline__ const uint8_t* page_wait(const DevState& S, SmemCtl* c, uint8_t* pages, const Ring& r) {
+  if (!mbar_try_wait(&c->full[r.slot], r.ph)) page_wait_slow(S, c, r);
   return pages + (size_t)r.slot * S.page_bytes;
 }
 // "free at last read" (§8.4): each compute warp hands the page back as soon as its own
@@ -649,7 +646,7 @@ __device__ __forceinline__ float inv_rms_of(const DevState& S, const SmemCtl* c,
 // the limit here: fp32 x costs twice the bytes of the fp16/bf16 weights, so
 //  * slice_dot_xreg (B <= 2, each warp always on the same slice of a row): the warp's
 //    x segment sits in registers for the whole instruction; only weights are read from
-//    the page, 16 bytes per lane, four loads in flight, two accumulator chains;
+//    the page, 16 bytes per lane, all loads in flight, four accumulator chains;
 //  * slice_dot_smem (otherwise): 8-byte weight loads and 16-byte x loads, both
 //    contiguous across the warp (no bank conflicts), two accumulator chains.
 template <typename WT, int NB, int J>
@@ -662,9 +659,9 @@ __device__ __forceinline__ void slice_dot_xreg(const uint8_t* wp, const float (&
     const int v = lane + 32 * j;
     wv[j] = v < nv ? w[v] : make_uint4(0u, 0u, 0u, 0u);
   }
-  float a0[NB], a1[NB];
+  float a[NB][4];
 #pragma unroll
-  for (int b = 0; b < NB; ++b) a0[b] = a1[b] = 0.f;
+  for (int b = 0; b < NB; ++b) a[b][0] = a[b][1] = a[b][2] = a[b][3] = 0.f;
 #pragma unroll
   for (int j = 0; j < J; ++j) {
     float f[8];
@@ -672,15 +669,10 @@ __device__ __forceinline__ void slice_dot_xreg(const uint8_t* wp, const float (&
 #pragma unroll
     for (int b = 0; b < NB; ++b)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        if (j & 1)
-          a1[b] = fmaf(f[e], xr[b][j * 8 + e], a1[b]);
-        else
-          a0[b] = fmaf(f[e], xr[b][j * 8 + e], a0[b]);
-      }
+      for (int e = 0; e < 8; ++e) a[b][j & 3] = fmaf(f[e], xr[b][j * 8 + e], a[b][j & 3]);
   }
 #pragma unroll
-  for (int b = 0; b < NB; ++b) acc[b] = a0[b] + a1[b];
+  for (int b = 0; b < NB; ++b) acc[b] = (a[b][0] + a[b][1]) + (a[b][2] + a[b][3]);
 }
 
 template <typename WT, int NB>
@@ -856,6 +848,7 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
   };
   const int R = g.rows();
   const long long ck0 = trace ? clock64() : 0;
+  long long ck_mid = ck0;
   switch (in.op) {
     case OP_QKV: {
       const int mat = in.a[0], head = in.a[1], i0 = in.a[2], n = in.a[3];
@@ -906,7 +899,9 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
       for (int t = tid; t < n * B; t += kConsumerThreads) {
         const int r = t % n, b = t / n;
         const float ir = c->inv_rms[b];
-        a[(size_t)b * S.F + row0 + r] = silu_f(rowsum(r, b) * ir) * (rowsum(r + n, b) * ir);
+        const float v = silu_f(rowsum(r, b) * ir) * (rowsum(r + n, b) * ir);
+        if (t == 0 && trace) ck_mid = clock64();
+        a[(size_t)b * S.F + row0 + r] = v;
       }
       break;
     }
@@ -954,7 +949,7 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
   }
   if (tid == 0 && trace) {
     c->tmark[3] = globaltimer_ns();
-    c->tmark[5] = (uint64_t)(clock64() - ck0);
+    c->tmark[5] = (uint64_t)(clock64() - ck0) | ((uint64_t)(ck_mid - ck0) << 32);
   }
 }
 
@@ -962,10 +957,13 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
 template <typename WT, int SYNC, int HD, int G>
 __device__ __noinline__ void op_attn(const DevState& S, const StepArgs& A, const Instr& in, SmemCtl* c, uint8_t* pages,
                         float* xbuf, float* scratch, Ring& ring, float* act) {
-  // 8 dims (one 16-byte row chunk) per lane, hd/8 lanes per position: keeps the G
-  // heads' accumulators inside the register budget (9 warps put 3 warps on one SM
-  // sub-partition of 16K registers, i.e. 168 registers per thread)
-  constexpr int DPL = 8;
+  // DPL dims per lane = DPL/8 16-byte row chunks, lane dl of a position group taking
+  // chunks dl, dl + LPP, ... (each load instruction reads contiguous bytes across the
+  // group: no bank conflicts).  16 dims per lane for G <= 2 (fewer shuffle stages per
+  // score, more positions per pass); 8 for G = 4 keeps the heads' accumulators inside the
+  // register budget (9 warps put 3 warps on one SM sub-partition of 16K registers, i.e.
+  // 168 registers per thread)
+  constexpr int DPL = G <= 2 ? 16 : 8;
   constexpr int LPP = HD / DPL;      // lanes per position
   constexpr int NGRP = 32 / LPP;     // positions per warp per pass
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1008,9 +1006,9 @@ __device__ __noinline__ void op_attn(const DevState& S, const StepArgs& A, const
 #pragma unroll
     for (int g = 0; g < QG; ++g)
 #pragma unroll
-      for (int i = 0; i < QD; ++i) q[g][i] = xbuf[g * HD + dl * DPL + i];
+      for (int i = 0; i < QD; ++i) q[g][i] = xbuf[g * HD + ((i / 8) * LPP + dl) * 8 + (i % 8)];
   }
-  const float* qs = xbuf + dl * DPL;
+  const float* qs = xbuf + dl * 8;  // + u * LPP * 8 for chunk u
 
   float m[G], lsum[G], o[G][DPL];
 #pragma unroll
@@ -1024,7 +1022,7 @@ __device__ __noinline__ void op_attn(const DevState& S, const StepArgs& A, const
   // One position per LPP-lane group: scores from its key row, online-softmax update,
   // then its value row.  Rows come from a page (storage dtype) or, for the new
   // position, from the fp32 staging in smem.
-  auto update = [&](bool valid, const uint16_t* krow, const uint16_t* vrow) {
+  auto update = [&](bool valid, const uint16_t* krow, const uint16_t* vrow) {  // row starts
     float sc[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) sc[g] = 0.f;
@@ -1032,7 +1030,7 @@ __device__ __noinline__ void op_attn(const DevState& S, const StepArgs& A, const
 #pragma unroll
       for (int u = 0; u < DPL / 8; ++u) {
         float kv[8];
-        Unpack<WT>::u8(reinterpret_cast<const uint4*>(krow)[u], kv);
+        Unpack<WT>::u8(reinterpret_cast<const uint4*>(krow)[u * LPP + dl], kv);
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           float a = sc[g];
@@ -1040,8 +1038,8 @@ __device__ __noinline__ void op_attn(const DevState& S, const StepArgs& A, const
 #pragma unroll
             for (int e = 0; e < 8; ++e) a = fmaf(q[QREG ? g : 0][QREG ? u * 8 + e : 0], kv[e], a);
           } else {
-            const float4 q0 = *reinterpret_cast<const float4*>(qs + g * HD + u * 8);
-            const float4 q1 = *reinterpret_cast<const float4*>(qs + g * HD + u * 8 + 4);
+            const float4 q0 = *reinterpret_cast<const float4*>(qs + g * HD + u * LPP * 8);
+            const float4 q1 = *reinterpret_cast<const float4*>(qs + g * HD + u * LPP * 8 + 4);
             a = fmaf(q0.x, kv[0], a); a = fmaf(q0.y, kv[1], a); a = fmaf(q0.z, kv[2], a); a = fmaf(q0.w, kv[3], a);
             a = fmaf(q1.x, kv[4], a); a = fmaf(q1.y, kv[5], a); a = fmaf(q1.z, kv[6], a); a = fmaf(q1.w, kv[7], a);
           }
@@ -1076,7 +1074,7 @@ __device__ __noinline__ void op_attn(const DevState& S, const StepArgs& A, const
 #pragma unroll
       for (int u = 0; u < DPL / 8; ++u) {
         float vv[8];
-        Unpack<WT>::u8(reinterpret_cast<const uint4*>(vrow)[u], vv);
+        Unpack<WT>::u8(reinterpret_cast<const uint4*>(vrow)[u * LPP + dl], vv);
 #pragma unroll
         for (int g = 0; g < G; ++g)
 #pragma unroll
@@ -1095,14 +1093,14 @@ __device__ __noinline__ void op_attn(const DevState& S, const StepArgs& A, const
     for (int base = 0; base < np; base += kConsumerWarps * NGRP) {
       const int t = base + warp * NGRP + pgi;
       const bool valid = t < np;
-      const size_t off = (size_t)(valid ? t : 0) * HD * 2 + dl * DPL * 2;
+      const size_t off = (size_t)(valid ? t : 0) * HD * 2;
       update(valid, reinterpret_cast<const uint16_t*>(kp + off), reinterpret_cast<const uint16_t*>(vp + off));
     }
     page_release(S, c, ring);  // K page
     page_release(S, c, ring);  // V page
   }
   if (at.has_new && warp == 0)  // position pos_b: the new key/value of this step
-    update(pgi == 0, knew + dl * DPL, knew + HD + dl * DPL);
+    update(pgi == 0, knew, knew + HD);
   if (mark) c->tmark[1] = globaltimer_ns();
   // combine the position groups of the warp (same running max), then the warps
 #pragma unroll
@@ -1119,7 +1117,7 @@ __device__ __noinline__ void op_attn(const DevState& S, const StepArgs& A, const
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
-      for (int i = 0; i < DPL; ++i) scratch[(warp * G + g) * RW + dl * DPL + i] = o[g][i];
+      for (int i = 0; i < DPL; ++i) scratch[(warp * G + g) * RW + ((i / 8) * LPP + dl) * 8 + (i % 8)] = o[g][i];
   }
   if (lane == 0) {
 #pragma unroll

@@ -251,6 +251,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_desc* desc, const mk_
   S.timeout_ns = 2000000000LL;
   S.backoff_max_ns = 256;
   S.split_min_positions = 16;
+  S.inflight_pages = 2;
   // the kernel's kv-cache addressing uses the caller's layout [max_batch, Hkv, max_ctx, hd]
   // only through max_ctx, and its activation rows through max_batch: both as set above
   StepArgs A{};

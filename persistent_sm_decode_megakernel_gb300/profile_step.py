@@ -39,7 +39,7 @@ def summarize(trace):
     by = {}
     per_cta_wait = {}
     groups = {}
-    keys = ("stage", "pages", "page_wait", "page_work", "epi", "epi_clk", "tail", "write", "arrive", "merge")
+    keys = ("stage", "pages", "page_wait", "page_work", "epi", "epi_clk", "epi_pre", "tail", "write", "arrive", "merge")
     for cta, pc, op, layer, tf, tr, te, m0, m1, m2, m3, m4, m5 in trace:
         d = by.setdefault(OPS.get(op, str(op)), {k: [] for k in ("wait", "work") + keys})
         d["wait"].append((tr - tf) / 1e3)
@@ -51,7 +51,8 @@ def summarize(trace):
             d["page_work"].append(m4 / 1e3)
             if m3:
                 d["epi"].append((m3 - m1) / 1e3)
-                d["epi_clk"].append(m5 / 2.07e3)   # cycles -> us at the 2070 MHz clock
+                d["epi_clk"].append((m5 & 0xFFFFFFFF) / 2.07e3)   # cycles -> us at the 2070 MHz clock
+                d["epi_pre"].append((m5 >> 32) / 2.07e3)
                 d["tail"].append((te - m3) / 1e3)
         elif op == 3 and m0 and m1:
             d["stage"].append((m0 - tr) / 1e3)
@@ -97,7 +98,7 @@ def main():
     ap.add_argument("--n-pages", type=int, default=0)
     ap.add_argument("--backoff", type=int, default=0)
     ap.add_argument("--merge", type=int, default=0, help="KV-split merge: 0 auto, 1 separate step, 2 in O-proj")
-    ap.add_argument("--inflight", type=int, default=0, help="page copies in flight per CTA (0: pool size)")
+    ap.add_argument("--inflight", type=int, default=0, help="page copies in flight per CTA (0: default, <0: pool)")
     ap.add_argument("--split-min", type=int, default=0)
     ap.add_argument("--json", default="")
     args = ap.parse_args()
