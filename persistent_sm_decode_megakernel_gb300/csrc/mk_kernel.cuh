@@ -753,12 +753,13 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
   consumer_sync();
   if (tid == 0 && (A.flags & SF_TRACE)) c->tmark[0] = globaltimer_ns();
   // the residual this thread adds in the epilogue (its first row), loaded now so the
-  // latency hides behind the pages
+  // latency hides behind the pages: the load is only issued here -- a sentinel is
+  // checked (and re-polled) in the epilogue, so no warp waits for it before its pages
   float hres = 0.f;
   if ((in.op == OP_OPROJ || in.op == OP_DOWN) && tid < g.rows() * B) {
     const int r = tid % g.rows(), b = tid / g.rows();
-    const float* hin = act_ptr(S, act, in.op == OP_OPROJ ? ACT_H : ACT_HMID, l);
-    hres = load_act<SYNC>(hin + (size_t)b * S.d + in.a[0] + r, S, c);
+    const float* hp = act_ptr(S, act, in.op == OP_OPROJ ? ACT_H : ACT_HMID, l) + (size_t)b * S.d + in.a[0] + r;
+    hres = SYNC == SYNC_COUNTER ? __ldcg(hp) : ld_poll_f32(hp);
   }
   // likewise the (cos, sin) of the thread's first RoPE pair, and 1/rms per sequence (read
   // by the epilogue after the barrier that ends the pages)
@@ -889,7 +890,9 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
       for (int t = tid; t < R * B; t += kConsumerThreads) {
         const int r = t % R, b = t / R;
         const size_t idx = (size_t)b * S.d + row0 + r;
-        hout[idx] = (t == tid ? hres : load_act<SYNC>(hin + idx, S, c)) + rowsum(r, b);
+        float hv = t == tid ? hres : load_act<SYNC>(hin + idx, S, c);
+        if (SYNC == SYNC_SENTINEL && isnan(hv)) hv = poll_slow(hin + idx, S, c);
+        hout[idx] = hv + rowsum(r, b);
       }
       break;
     }
@@ -912,7 +915,9 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
       for (int t = tid; t < R * B; t += kConsumerThreads) {
         const int r = t % R, b = t / R;
         const size_t idx = (size_t)b * S.d + row0 + r;
-        hout[idx] = (t == tid ? hres : load_act<SYNC>(hin + idx, S, c)) + rowsum(r, b);
+        float hv = t == tid ? hres : load_act<SYNC>(hin + idx, S, c);
+        if (SYNC == SYNC_SENTINEL && isnan(hv)) hv = poll_slow(hin + idx, S, c);
+        hout[idx] = hv + rowsum(r, b);
       }
       break;
     }
