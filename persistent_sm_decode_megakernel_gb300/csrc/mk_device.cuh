@@ -199,6 +199,44 @@ struct Unpack<__nv_bfloat16> {
   }
 };
 
+// ---------------------------------------------------------------- tensor cores (batch >= 3)
+// D (16x8 f32) += A (16x16, row-major) x B (16x8, column-major), 16-bit inputs.  Fragment
+// ownership (g = lane / 4, c = lane % 4): a0 (row g, k 2c..2c+1), a1 (row g+8, same k),
+// a2 (row g, k 2c+8..2c+9), a3 (row g+8, k 2c+8..); b0 (k 2c..2c+1, col g), b1 (k 2c+8..,
+// col g); d0 (row g, col 2c), d1 (row g, col 2c+1), d2 (row g+8, col 2c), d3 (row g+8, col 2c+1).
+template <typename WT>
+struct Mma;
+template <>
+struct Mma<__half> {
+  __device__ __forceinline__ static void run(float (&d)[4], const uint4& a, uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
+  }
+  // x = hi + lo, both half: hi = x rounded, lo = the rest rounded (about 22 significant bits)
+  __device__ __forceinline__ static void split(float x, uint16_t& hi, uint16_t& lo) {
+    const __half h = __float2half_rn(x);
+    hi = __half_as_ushort(h);
+    lo = __half_as_ushort(__float2half_rn(x - __half2float(h)));
+  }
+};
+template <>
+struct Mma<__nv_bfloat16> {
+  __device__ __forceinline__ static void run(float (&d)[4], const uint4& a, uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
+  }
+  // bf16 keeps 8 significant bits: hi + lo carries about 16
+  __device__ __forceinline__ static void split(float x, uint16_t& hi, uint16_t& lo) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    hi = __bfloat16_as_ushort(h);
+    lo = __bfloat16_as_ushort(__float2bfloat16_rn(x - __bfloat162float(h)));
+  }
+};
+
 // total order on floats as unsigned integers (for the packed argmax key)
 __device__ __forceinline__ uint32_t orderable(float f) {
   uint32_t u = __float_as_uint(f);

@@ -445,6 +445,8 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
   S.n_cta = ctx->n_cta;
   S.page_bytes = g.page_bytes;
   S.n_pages = g.n_pages;
+  S.page_stride = g.page_stride;
+  S.tc = g.tc;
   S.xbuf_bytes = g.xbuf_bytes;
   S.scratch_bytes = g.scratch_bytes;
   S.sync_mode = o.sync_mode;
@@ -741,6 +743,7 @@ mk_status mk_selftest(int kind, int64_t* result, int n) {
   S.ctl = reinterpret_cast<Ctl*>(ctl.p);
   S.n_cta = n_cta;
   S.page_bytes = page;
+  S.page_stride = page;
   S.n_pages = n_pages;
   S.xbuf_bytes = 0;
   S.scratch_bytes = 256;

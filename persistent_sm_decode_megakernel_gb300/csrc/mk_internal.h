@@ -136,6 +136,8 @@ struct DevState {
   // execution
   int n_cta;
   int page_bytes, n_pages;
+  int page_stride;             // bytes between ring slots (>= page_bytes; kTcPageBytes with tc)
+  int tc;                      // batches of 3..16 use the tensor-core GEMV
   int xbuf_bytes, scratch_bytes;
   int sync_mode;
   int64_t timeout_ns;
@@ -166,6 +168,15 @@ struct StepArgs {
   float* logits;               // [B][V] or null
   int32_t* tok_hist;           // device [B] copy of this step's tokens, or null
 };
+
+// Tensor-core GEMV (batches of 3..16 in contexts built for max_batch >= 8): a page holds
+// kTcRows weight rows of kTcKw columns (one window of the input), each row followed by a
+// 16-byte skew so that the 8 rows an mma fragment reads sit in different banks.
+constexpr int kTcKw = 1024;
+constexpr int kTcRows = 16;
+constexpr int kTcRowBytes = kTcKw * 2 + 16;
+constexpr int kTcPageBytes = kTcRows * kTcRowBytes;                        // 33024
+constexpr int kTcPartialFloats = 2 * kConsumerWarps * kTcRows * kMaxBatch;  // double-buffered warp partials
 
 // a split's partial attention record per head: hd weighted value sums, the running max,
 // the exp-sum, two pad floats (16-byte rows, so records move as float4)

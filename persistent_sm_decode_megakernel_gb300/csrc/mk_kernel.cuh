@@ -276,6 +276,32 @@ __device__ __noinline__ void producer(const DevState& S, const StepArgs& A, Smem
             for (int off = 0; off < in.a[3] * 8 + 128; off += 128) prefetch_l1(rp + off);
           }
         }
+        if (S.tc && A.B >= 3) {
+          // tensor-core pages: for each window of kTcKw columns, 16-row blocks of the
+          // instruction's rows (segment 0, then segment 1), one bulk copy per row into its
+          // skewed row slot
+          const int K = g.K, R = g.rows(), nw = (K + kTcKw - 1) / kTcKw, nrb = (R + kTcRows - 1) / kTcRows;
+          for (int w = 0; w < nw && ok; ++w) {
+            const int kw = min(kTcKw, K - w * kTcKw);
+            for (int rb = 0; rb < nrb; ++rb) {
+              if (!producer_acquire(S, c, slot, ph, issued++)) {
+                ok = false;
+                break;
+              }
+              const int nr = min(kTcRows, R - rb * kTcRows);
+              mbar_arrive_expect_tx(&c->full[slot], (uint32_t)(nr * kw * 2));
+              uint8_t* dst = pages + (size_t)slot * S.page_stride;
+              for (int i = 0; i < nr; ++i) {
+                const int fr = rb * kTcRows + i, sg = fr < g.segr[0] ? 0 : 1, r = sg ? fr - g.segr[0] : fr;
+                tma_load_1d(dst + (size_t)i * kTcRowBytes, g.seg[sg] + (size_t)r * K + (size_t)w * kTcKw,
+                            (uint32_t)(kw * 2), &c->full[slot], pol);
+              }
+              c->last_issue_phase[slot] = (int)ph;
+              if (++slot == S.n_pages) { slot = 0; ph ^= 1u; }
+            }
+          }
+          break;
+        }
         // rows of a segment are contiguous and a row is spr slices, so slice j of
         // segment k starts at seg[k] + j * WS: a page is at most two bulk copies
         const int n0 = g.segr[0] * g.spr();
@@ -286,7 +312,7 @@ __device__ __noinline__ void producer(const DevState& S, const StepArgs& A, Smem
           }
           const int i1 = min(ns, i0 + kConsumerWarps);
           mbar_arrive_expect_tx(&c->full[slot], (uint32_t)(i1 - i0) * sb);
-          uint8_t* dst = pages + (size_t)slot * S.page_bytes;
+          uint8_t* dst = pages + (size_t)slot * S.page_stride;
           if (i0 < n0) {
             const int e = min(i1, n0);
             tma_load_1d(dst, g.seg[0] + (size_t)i0 * g.WS, (uint32_t)(e - i0) * sb, &c->full[slot], pol);
@@ -313,7 +339,7 @@ __device__ __noinline__ void producer(const DevState& S, const StepArgs& A, Smem
               break;
             }
             mbar_arrive_expect_tx(&c->full[slot], bytes);
-            tma_load_1d(pages + (size_t)slot * S.page_bytes, (kv ? at.vb : at.kb) + (size_t)p0 * S.hd, bytes,
+            tma_load_1d(pages + (size_t)slot * S.page_stride, (kv ? at.vb : at.kb) + (size_t)p0 * S.hd, bytes,
                         &c->full[slot], pol);
             c->last_issue_phase[slot] = (int)ph;
             if (++slot == S.n_pages) { slot = 0; ph ^= 1u; }
@@ -330,7 +356,7 @@ __device__ __noinline__ void producer(const DevState& S, const StepArgs& A, Smem
             break;
           }
           mbar_arrive_expect_tx(&c->full[slot], (uint32_t)S.page_bytes);
-          tma_load_1d(pages + (size_t)slot * S.page_bytes, S.test_buf + in.a[0] + (int64_t)k * words,
+          tma_load_1d(pages + (size_t)slot * S.page_stride, S.test_buf + in.a[0] + (int64_t)k * words,
                       (uint32_t)S.page_bytes, &c->full[slot], pol);
           c->last_issue_phase[slot] = (int)ph;
           if (++slot == S.n_pages) { slot = 0; ph ^= 1u; }
@@ -385,7 +411,7 @@ __device__ __noinline__ void page_wait_slow(const DevState& S, SmemCtl* c, const
 }
 __device__ __forceinline__ const uint8_t* page_wait(const DevState& S, SmemCtl* c, uint8_t* pages, const Ring& r) {
   if (!mbar_try_wait(&c->full[r.slot], r.ph)) page_wait_slow(S, c, r);
-  return pages + (size_t)r.slot * S.page_bytes;
+  return pages + (size_t)r.slot * S.page_stride;
 }
 // "free at last read" (§8.4): each compute warp hands the page back as soon as its own
 // reads are done; the loader refills it when all warps have done so.
@@ -722,6 +748,122 @@ __device__ __forceinline__ void slice_dot_smem(const uint8_t* wp, const float* x
 // silu(u) = u / (1 + e^-u); the fast exponential (a few ulp) is far inside the tolerance
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
 
+// The GEMV epilogue (after the barrier that ends the pages): each row is finished from its
+// row parts in a fixed order and the op's output is written.  rowpart [rows][spr][NB];
+// hres / cs0 are the thread's prefetched residual and RoPE row (its first row).
+template <typename WT, int SYNC, int NB>
+__device__ __forceinline__ void gemv_epilogue(const DevState& S, const StepArgs& A, const Instr& in, SmemCtl* c,
+                                              float* act, const float* rowpart, int spr, int R, float hres,
+                                              float2 cs0) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int B = A.B, l = in.layer;
+  auto rowsum = [&](int r, int b) {
+    float t = 0.f;
+    for (int s = 0; s < spr; ++s) t += rowpart[((size_t)r * spr + s) * NB + b];
+    return t;
+  };
+  switch (in.op) {
+    case OP_QKV: {
+      const int mat = in.a[0], head = in.a[1], i0 = in.a[2], n = in.a[3];
+      const int hd = S.hd, half = hd / 2;
+      for (int t = tid; t < n * B; t += kConsumerThreads) {
+        const int r = t % n, b = t / n;
+        const float ir = c->inv_rms[b];
+        float va = rowsum(r, b) * ir, vb = rowsum(r + n, b) * ir;
+        const int i = i0 + r;
+        const int pos = A.pos[b];
+        if (mat < 2) {  // rotate-half RoPE on the pair (i, i + hd/2)
+          const float2 cs = t == tid ? cs0 : S.rope[(size_t)pos * half + i];
+          const float xa = va * cs.x - vb * cs.y;
+          const float xb = vb * cs.x + va * cs.y;
+          va = xa;
+          vb = xb;
+        }
+        if (mat == 0) {
+          float* q = act_ptr(S, act, ACT_Q, l) + (size_t)b * S.Hq * hd + (size_t)head * hd;
+          q[i] = va;
+          q[i + half] = vb;
+        } else {
+          const uint16_t ra = Unpack<WT>::round(va), rb = Unpack<WT>::round(vb);
+          uint16_t* cache = const_cast<uint16_t*>(iptr(in, kP3)) + (((size_t)b * S.Hkv + head) * S.max_ctx + pos) * hd;
+          cache[i] = ra;
+          cache[i + half] = rb;
+          float* kvn = act_ptr(S, act, ACT_KVN, l) + ((size_t)b * 2 + (mat - 1)) * S.Hkv * hd + (size_t)head * hd;
+          kvn[i] = Unpack<WT>::one(ra);
+          kvn[i + half] = Unpack<WT>::one(rb);
+        }
+      }
+      break;
+    }
+    case OP_OPROJ: {
+      const int row0 = in.a[0];
+      const float* hin = act_ptr(S, act, ACT_H, l);
+      float* hout = act_ptr(S, act, ACT_HMID, l);
+      for (int t = tid; t < R * B; t += kConsumerThreads) {
+        const int r = t % R, b = t / R;
+        const size_t idx = (size_t)b * S.d + row0 + r;
+        float hv = t == tid ? hres : load_act<SYNC>(hin + idx, S, c);
+        if (SYNC == SYNC_SENTINEL && isnan(hv)) hv = poll_slow(hin + idx, S, c);
+        hout[idx] = hv + rowsum(r, b);
+      }
+      break;
+    }
+    case OP_UPGATE: {
+      const int row0 = in.a[0], n = in.a[1];
+      float* a = act_ptr(S, act, ACT_A, l);
+      for (int t = tid; t < n * B; t += kConsumerThreads) {
+        const int r = t % n, b = t / n;
+        const float ir = c->inv_rms[b];
+        a[(size_t)b * S.F + row0 + r] = silu_f(rowsum(r, b) * ir) * (rowsum(r + n, b) * ir);
+      }
+      break;
+    }
+    case OP_DOWN: {
+      const int row0 = in.a[0];
+      const float* hin = act_ptr(S, act, ACT_HMID, l);
+      float* hout = act_ptr(S, act, ACT_H, l + 1);
+      for (int t = tid; t < R * B; t += kConsumerThreads) {
+        const int r = t % R, b = t / R;
+        const size_t idx = (size_t)b * S.d + row0 + r;
+        float hv = t == tid ? hres : load_act<SYNC>(hin + idx, S, c);
+        if (SYNC == SYNC_SENTINEL && isnan(hv)) hv = poll_slow(hin + idx, S, c);
+        hout[idx] = hv + rowsum(r, b);
+      }
+      break;
+    }
+    default: {  // OP_LMHEAD: logits and the running argmax (packed key, lowest index wins ties)
+      const int row0 = in.a[0];
+      unsigned long long best[NB];
+#pragma unroll
+      for (int b = 0; b < NB; ++b) best[b] = 0ull;
+      for (int t = tid; t < R * NB; t += kConsumerThreads) {
+        const int r = t % R, b = t / R;
+        if (b >= B) continue;
+        const float z = rowsum(r, b) * c->inv_rms[b];
+        const int row = row0 + r;
+        if (A.logits) A.logits[(size_t)b * S.V + row] = z;
+        if (isnan(z)) atomicOr(&S.ctl->nan_seen, 1u);
+        const unsigned long long key =
+            ((unsigned long long)orderable(z) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)row);
+#pragma unroll
+        for (int bb = 0; bb < NB; ++bb)
+          if (bb == b && key > best[bb]) best[bb] = key;
+      }
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        unsigned long long v = best[b];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+          v = w > v ? w : v;
+        }
+        if (lane == 0 && v) atomicMax(&c->best[b], v);
+      }
+      break;
+    }
+  }
+}
+
 template <typename WT, int SYNC, int NB>
 __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const Instr& in, SmemCtl* c, uint8_t* pages,
                         float* xbuf, float* scratch, Ring& ring, float* act) {
@@ -842,119 +984,189 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
   }
 
   // 3. finalize rows in a fixed order and apply the op's epilogue
-  auto rowsum = [&](int r, int b) {
-    float t = 0.f;
-    for (int s = 0; s < spr; ++s) t += rowpart[((size_t)r * spr + s) * NB + b];
-    return t;
-  };
-  const int R = g.rows();
   const long long ck0 = trace ? clock64() : 0;
-  long long ck_mid = ck0;
-  switch (in.op) {
-    case OP_QKV: {
-      const int mat = in.a[0], head = in.a[1], i0 = in.a[2], n = in.a[3];
-      const int hd = S.hd, half = hd / 2;
-      for (int t = tid; t < n * B; t += kConsumerThreads) {
-        const int r = t % n, b = t / n;
-        const float ir = c->inv_rms[b];
-        float va = rowsum(r, b) * ir, vb = rowsum(r + n, b) * ir;
-        const int i = i0 + r;
-        const int pos = A.pos[b];
-        if (mat < 2) {  // rotate-half RoPE on the pair (i, i + hd/2)
-          const float2 cs = t == tid ? cs0 : S.rope[(size_t)pos * half + i];
-          const float xa = va * cs.x - vb * cs.y;
-          const float xb = vb * cs.x + va * cs.y;
-          va = xa;
-          vb = xb;
-        }
-        if (mat == 0) {
-          float* q = act_ptr(S, act, ACT_Q, l) + (size_t)b * S.Hq * hd + (size_t)head * hd;
-          q[i] = va;
-          q[i + half] = vb;
-        } else {
-          const uint16_t ra = Unpack<WT>::round(va), rb = Unpack<WT>::round(vb);
-          uint16_t* cache = const_cast<uint16_t*>(iptr(in, kP3)) + (((size_t)b * S.Hkv + head) * S.max_ctx + pos) * hd;
-          cache[i] = ra;
-          cache[i + half] = rb;
-          float* kvn = act_ptr(S, act, ACT_KVN, l) + ((size_t)b * 2 + (mat - 1)) * S.Hkv * hd + (size_t)head * hd;
-          kvn[i] = Unpack<WT>::one(ra);
-          kvn[i + half] = Unpack<WT>::one(rb);
-        }
-      }
-      break;
-    }
-    case OP_OPROJ: {
-      const int row0 = in.a[0];
-      const float* hin = act_ptr(S, act, ACT_H, l);
-      float* hout = act_ptr(S, act, ACT_HMID, l);
-      for (int t = tid; t < R * B; t += kConsumerThreads) {
-        const int r = t % R, b = t / R;
-        const size_t idx = (size_t)b * S.d + row0 + r;
-        float hv = t == tid ? hres : load_act<SYNC>(hin + idx, S, c);
-        if (SYNC == SYNC_SENTINEL && isnan(hv)) hv = poll_slow(hin + idx, S, c);
-        hout[idx] = hv + rowsum(r, b);
-      }
-      break;
-    }
-    case OP_UPGATE: {
-      const int row0 = in.a[0], n = in.a[1];
-      float* a = act_ptr(S, act, ACT_A, l);
-      for (int t = tid; t < n * B; t += kConsumerThreads) {
-        const int r = t % n, b = t / n;
-        const float ir = c->inv_rms[b];
-        const float v = silu_f(rowsum(r, b) * ir) * (rowsum(r + n, b) * ir);
-        if (t == 0 && trace) ck_mid = clock64();
-        a[(size_t)b * S.F + row0 + r] = v;
-      }
-      break;
-    }
-    case OP_DOWN: {
-      const int row0 = in.a[0];
-      const float* hin = act_ptr(S, act, ACT_HMID, l);
-      float* hout = act_ptr(S, act, ACT_H, l + 1);
-      for (int t = tid; t < R * B; t += kConsumerThreads) {
-        const int r = t % R, b = t / R;
-        const size_t idx = (size_t)b * S.d + row0 + r;
-        float hv = t == tid ? hres : load_act<SYNC>(hin + idx, S, c);
-        if (SYNC == SYNC_SENTINEL && isnan(hv)) hv = poll_slow(hin + idx, S, c);
-        hout[idx] = hv + rowsum(r, b);
-      }
-      break;
-    }
-    default: {  // OP_LMHEAD: logits and the running argmax (packed key, lowest index wins ties)
-      const int row0 = in.a[0];
-      unsigned long long best[NB];
-#pragma unroll
-      for (int b = 0; b < NB; ++b) best[b] = 0ull;
-      for (int t = tid; t < R * NB; t += kConsumerThreads) {
-        const int r = t % R, b = t / R;
-        if (b >= B) continue;
-        const float z = rowsum(r, b) * c->inv_rms[b];
-        const int row = row0 + r;
-        if (A.logits) A.logits[(size_t)b * S.V + row] = z;
-        if (isnan(z)) atomicOr(&S.ctl->nan_seen, 1u);
-        const unsigned long long key =
-            ((unsigned long long)orderable(z) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)row);
-#pragma unroll
-        for (int bb = 0; bb < NB; ++bb)
-          if (bb == b && key > best[bb]) best[bb] = key;
-      }
-#pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        unsigned long long v = best[b];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
-          v = w > v ? w : v;
-        }
-        if (lane == 0 && v) atomicMax(&c->best[b], v);
-      }
-      break;
-    }
-  }
+  gemv_epilogue<WT, SYNC, NB>(S, A, in, c, act, rowpart, spr, g.rows(), hres, cs0);
   if (tid == 0 && trace) {
     c->tmark[3] = globaltimer_ns();
-    c->tmark[5] = (uint64_t)(clock64() - ck0) | ((uint64_t)(ck_mid - ck0) << 32);
+    c->tmark[5] = (uint64_t)(clock64() - ck0);
+  }
+}
+
+// ---------------------------------------------------------------- tensor-core GEMV
+// Batches of 3..16 (contexts built for max_batch >= 8): y[b] = W x[b] for 16-row blocks of
+// weights at a time with mma.sync m16n8k16.  A = the inputs: each 16-row A tile holds 8
+// sequences' inputs split into hi and lo 16-bit halves (rows 0-7 hi, rows 8-15 lo: the
+// MMA's f32 accumulator sums both, so the inputs keep ~22 significant bits with fp16);
+// B = 8 weight rows (a weight row is a column of B, its elements contiguous as in memory).
+// The input is staged one window of kTcKw columns at a time, already in fragment order;
+// the loader brings, per window, 16-row blocks of the instruction's rows.  Warps split a
+// page's k-steps; their partials are summed in a fixed order into per-row accumulators,
+// and the common epilogue finishes the rows.
+template <typename WT, int SYNC, int NB>
+__device__ __noinline__ void op_gemv_tc(const DevState& S, const StepArgs& A, const Instr& in, SmemCtl* c,
+                                        uint8_t* pages, float* xbuf, float* scratch, Ring& ring, float* act) {
+  constexpr int MT = (NB + 7) / 8;  // A tiles of 8 sequences
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, cq = lane & 3;
+  const int B = A.B, l = in.layer;
+  const Gemv g = make_gemv(S, in);
+  const int K = g.K, R = g.rows(), nw = (K + kTcKw - 1) / kTcKw, nrb = (R + kTcRows - 1) / kTcRows;
+  const bool trace = (A.flags & SF_TRACE) != 0;
+  float* part = scratch;                       // [2][warps][kTcRows][NB]
+  float* rowacc = scratch + kTcPartialFloats;  // [R][NB]
+  uint32_t* xt = reinterpret_cast<uint32_t*>(xbuf);  // [kstep][MT][lane][4]
+  const float* src;
+  const uint16_t* gain = nullptr;
+  switch (in.op) {
+    case OP_QKV: src = act_ptr(S, act, ACT_H, l); gain = iptr(in, kP2); break;
+    case OP_UPGATE: src = act_ptr(S, act, ACT_HMID, l); gain = iptr(in, kP2); break;
+    case OP_LMHEAD: src = act_ptr(S, act, ACT_H, S.L); gain = iptr(in, kP2); break;
+    case OP_OPROJ: src = act_ptr(S, act, ACT_O, l); break;
+    default: src = act_ptr(S, act, ACT_A, l); break;
+  }
+  for (int i = tid; i < R * NB; i += kConsumerThreads) rowacc[i] = 0.f;
+  // epilogue inputs, prefetched as in the CUDA-core GEMV
+  float hres = 0.f;
+  if ((in.op == OP_OPROJ || in.op == OP_DOWN) && tid < R * B) {
+    const int r = tid % R, b = tid / R;
+    const float* hp = act_ptr(S, act, in.op == OP_OPROJ ? ACT_H : ACT_HMID, l) + (size_t)b * S.d + in.a[0] + r;
+    hres = SYNC == SYNC_COUNTER ? __ldcg(hp) : ld_poll_f32(hp);
+  }
+  float2 cs0 = make_float2(1.f, 0.f);
+  if (in.op == OP_QKV && in.a[0] < 2 && tid < in.a[3] * B)
+    cs0 = S.rope[(size_t)A.pos[tid / in.a[3]] * (S.hd / 2) + in.a[2] + tid % in.a[3]];
+  float ss[NB];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) ss[b] = 0.f;
+  uint64_t page_wait_ns = 0, page_work_ns = 0;
+  int pcount = 0;
+  for (int w = 0; w < nw; ++w) {
+    const int k0 = w * kTcKw, kw = min(kTcKw, K - k0), nks = kw >> 4;
+    // 1. this window's inputs, split into hi/lo halves in fragment order (8 sequences per
+    //    tile; sequences >= B are zeros).  The previous window's pages are done: every
+    //    warp passed the barrier after its last page.
+    {
+      constexpr int U = 8;
+      const int k4n = kw >> 2, n_items = MT * 8 * k4n;
+      for (int base = 0; base < n_items; base += U * kConsumerThreads) {
+        const float4* pp[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int it = base + u * kConsumerThreads + tid, b = it / k4n, k4 = it - b * k4n;
+          pp[u] = (it < n_items && b < B) ? reinterpret_cast<const float4*>(src + (size_t)b * K + k0) + k4 : nullptr;
+        }
+        float4 v[U];
+        load_vecs<SYNC, U>(S, c, pp, v);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int it = base + u * kConsumerThreads + tid;
+          if (it >= n_items) continue;
+          const int b = it / k4n, k4 = it - b * k4n, k = 4 * k4;
+          float4 x = v[u];
+          if (gain != nullptr && b < B) {
+            const uint2 gb = __ldg(reinterpret_cast<const uint2*>(gain + k0) + k4);
+            const float sq = x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+#pragma unroll
+            for (int bb = 0; bb < NB; ++bb)
+              if (bb == b) ss[bb] += sq;
+            x.x *= Unpack<WT>::one((uint16_t)(gb.x & 0xFFFFu));
+            x.y *= Unpack<WT>::one((uint16_t)(gb.x >> 16));
+            x.z *= Unpack<WT>::one((uint16_t)(gb.y & 0xFFFFu));
+            x.w *= Unpack<WT>::one((uint16_t)(gb.y >> 16));
+          }
+          uint16_t h0, l0, h1, l1, h2, l2, h3, l3;
+          Mma<WT>::split(x.x, h0, l0);
+          Mma<WT>::split(x.y, h1, l1);
+          Mma<WT>::split(x.z, h2, l2);
+          Mma<WT>::split(x.w, h3, l3);
+          const int kk = k & 15, ks = k >> 4, mt = b >> 3, s8 = b & 7;
+          const int reg = kk >= 8 ? 2 : 0, p0 = (kk & 7) >> 1;
+          uint32_t* wd = xt + ((size_t)(ks * MT + mt) * 32 + s8 * 4 + p0) * 4 + reg;
+          wd[0] = (uint32_t)h0 | ((uint32_t)h1 << 16);  // (k, k+1) hi
+          wd[1] = (uint32_t)l0 | ((uint32_t)l1 << 16);  // lo
+          wd[4] = (uint32_t)h2 | ((uint32_t)h3 << 16);  // (k+2, k+3): the next lane's pair
+          wd[5] = (uint32_t)l2 | ((uint32_t)l3 << 16);
+        }
+      }
+    }
+    consumer_sync();
+    if (tid == 0 && trace && w == 0) c->tmark[0] = globaltimer_ns();
+    // 2. the window's row blocks
+    const int per = (nks + kConsumerWarps - 1) / kConsumerWarps, ks0 = warp * per, ks1 = min(nks, ks0 + per);
+    for (int rb = 0; rb < nrb; ++rb) {
+      const uint64_t tw = trace ? globaltimer_ns() : 0ull;
+      const uint8_t* pg = page_wait(S, c, pages, ring);
+      const uint64_t tr = trace ? globaltimer_ns() : 0ull;
+      if (trace) page_wait_ns += tr - tw;
+      float d[MT][2][4];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb) d[mt][nb][0] = d[mt][nb][1] = d[mt][nb][2] = d[mt][nb][3] = 0.f;
+      for (int ks = ks0; ks < ks1; ++ks) {
+        uint32_t bw[2][2];
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb) {
+          const uint8_t* wr = pg + (size_t)(nb * 8 + gq) * kTcRowBytes + (size_t)(ks * 16 + 2 * cq) * 2;
+          bw[nb][0] = *reinterpret_cast<const uint32_t*>(wr);
+          bw[nb][1] = *reinterpret_cast<const uint32_t*>(wr + 16);
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const uint4 a = *reinterpret_cast<const uint4*>(xt + ((size_t)(ks * MT + mt) * 32 + lane) * 4);
+#pragma unroll
+          for (int nb = 0; nb < 2; ++nb) Mma<WT>::run(d[mt][nb], a, bw[nb][0], bw[nb][1]);
+        }
+      }
+      page_release(S, c, ring);
+      // hi + lo of (sequence mt*8 + g, weight rows nb*8 + 2c and + 1) into this warp's partial
+      float* pb = part + ((size_t)((pcount & 1) * kConsumerWarps + warp) * kTcRows) * NB;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const int sq = mt * 8 + gq;
+        if (sq < NB) {
+#pragma unroll
+          for (int nb = 0; nb < 2; ++nb) {
+            pb[(nb * 8 + 2 * cq) * NB + sq] = d[mt][nb][0] + d[mt][nb][2];
+            pb[(nb * 8 + 2 * cq + 1) * NB + sq] = d[mt][nb][1] + d[mt][nb][3];
+          }
+        }
+      }
+      consumer_sync();
+      if (tid < kTcRows * NB) {  // one (row, sequence) per thread: warps summed in a fixed order
+        const int row = tid / NB, sq = tid - row * NB, fr = rb * kTcRows + row;
+        if (fr < R) {
+          const float* pr = part + ((size_t)(pcount & 1) * kConsumerWarps * kTcRows + row) * NB + sq;
+          float t = 0.f;
+#pragma unroll
+          for (int ww = 0; ww < kConsumerWarps; ++ww) t += pr[(size_t)ww * kTcRows * NB];
+          rowacc[(size_t)fr * NB + sq] += t;
+        }
+      }
+      ++pcount;
+      if (trace) page_work_ns += globaltimer_ns() - tr;
+    }
+  }
+  // 1/rms from the sums of squares taken while staging
+  if (gain != nullptr) {
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const float t = warp_sum(ss[b]);
+      if (lane == 0) c->red[warp * NB + b] = t;
+    }
+  }
+  consumer_sync();
+  if (gain != nullptr && tid < B) c->inv_rms[tid] = inv_rms_of<NB>(S, c, tid);
+  consumer_sync();
+  if (tid == 0 && trace) {
+    c->tmark[1] = globaltimer_ns();
+    c->tmark[2] = page_wait_ns;
+    c->tmark[4] = page_work_ns;
+  }
+  const long long ck0 = trace ? clock64() : 0;
+  gemv_epilogue<WT, SYNC, NB>(S, A, in, c, act, rowacc, 1, R, hres, cs0);
+  if (tid == 0 && trace) {
+    c->tmark[3] = globaltimer_ns();
+    c->tmark[5] = (uint64_t)(clock64() - ck0);
   }
 }
 
@@ -1309,6 +1521,14 @@ __device__ void consumer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8
       case OP_UPGATE:
       case OP_DOWN:
       case OP_LMHEAD:
+        if (S.tc && nb >= 4) {  // batches of 3..16: tensor cores
+          switch (nb) {
+            case 4: op_gemv_tc<WT, SYNC, 4>(S, A, in, c, pages, xbuf, scratch, ring, act); break;
+            case 8: op_gemv_tc<WT, SYNC, 8>(S, A, in, c, pages, xbuf, scratch, ring, act); break;
+            default: op_gemv_tc<WT, SYNC, 16>(S, A, in, c, pages, xbuf, scratch, ring, act); break;
+          }
+          break;
+        }
         switch (nb) {
           case 1: op_gemv<WT, SYNC, 1>(S, A, in, c, pages, xbuf, scratch, ring, act); break;
           case 2: op_gemv<WT, SYNC, 2>(S, A, in, c, pages, xbuf, scratch, ring, act); break;
@@ -1424,7 +1644,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
                                                               const __grid_constant__ StepArgs A) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* pages = smem;
-  float* xbuf = reinterpret_cast<float*>(smem + (size_t)S.n_pages * S.page_bytes);
+  float* xbuf = reinterpret_cast<float*>(smem + (size_t)S.n_pages * S.page_stride);
   float* scratch = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(xbuf) + S.xbuf_bytes);
   SmemCtl* c = reinterpret_cast<SmemCtl*>(reinterpret_cast<uint8_t*>(scratch) + S.scratch_bytes);
   const int tid = threadIdx.x;

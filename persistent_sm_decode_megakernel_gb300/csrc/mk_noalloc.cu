@@ -245,6 +245,8 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_desc* desc, const mk_
   S.n_cta = n_cta;
   S.page_bytes = g.page_bytes;
   S.n_pages = g.n_pages;
+  S.page_stride = g.page_stride;
+  S.tc = g.tc;
   S.xbuf_bytes = g.xbuf_bytes;
   S.scratch_bytes = g.scratch_bytes;
   S.sync_mode = MK_SYNC_COUNTER;

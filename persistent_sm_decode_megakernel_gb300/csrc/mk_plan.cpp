@@ -50,6 +50,13 @@ std::string make_geometry(const ModelShape& m, int n_cta, int page_bytes, int n_
     return "page_bytes must be a power of two in [4096, 32768]";
   if (g->page_bytes < 64 * m.hd) return fmt("page_bytes must be at least 64 * head_dim = %lld", 64LL * m.hd);
   g->nb_max = pow2_at_least(m.max_batch);
+  g->tc = m.max_batch >= 8 ? 1 : 0;
+  g->page_stride = g->page_bytes;
+  if (g->tc) {
+    if (g->page_bytes != 32768) return "batches of 8 and more need 32 KB pages";
+    if (m.d % 16 || m.F % 16 || (m.Hq * m.hd) % 16) return "batches of 8 and more need dims that are multiples of 16";
+    g->page_stride = kTcPageBytes;
+  }
   const int max_ws = g->page_bytes / (2 * kConsumerWarps);
   g->ws_qkv = slice_width(m.d, max_ws);
   g->ws_up = g->ws_qkv;
@@ -58,8 +65,10 @@ std::string make_geometry(const ModelShape& m, int n_cta, int page_bytes, int n_
   g->ws_down = slice_width(m.F, max_ws);
   if (!g->ws_qkv || !g->ws_o || !g->ws_down) return "d_model, n_heads*head_dim and ffn_dim must be multiples of 8";
   const int kmax = std::max(m.d, std::max(m.Hq * m.hd, m.F));
-  // x buffer: a batch of GEMV inputs, or q of one GQA group plus the new key/value
-  const int xfloats = std::max(g->nb_max * kmax, (G + 1) * m.hd);
+  // x buffer: a batch of GEMV inputs, or q of one GQA group plus the new key/value; with
+  // the tensor-core path, batches of 1..2 inputs or one window of 16 sequences' hi/lo halves
+  const int xfloats = g->tc ? std::max(std::max(2 * kmax, kMaxBatch * std::min(kTcKw, kmax)), (G + 1) * m.hd)
+                            : std::max(g->nb_max * kmax, (G + 1) * m.hd);
   g->xbuf_bytes = ((xfloats * 4 + 127) / 128) * 128;
   if (kv_splits > 0) {
     g->S = kv_splits;
@@ -68,19 +77,19 @@ std::string make_geometry(const ModelShape& m, int n_cta, int page_bytes, int n_
     if (g->S > 64) g->S = std::max(1, n_cta / m.Hkv);
   }
   if (g->S < 1 || g->S > 256) return "kv_splits out of range [1, 256]";
-  int scratch = 16384;
+  int scratch = g->tc ? kTcPartialFloats * 4 + 8192 : 16384;
   scratch = std::max(scratch, kConsumerWarps * G * (m.hd + kPartExtra) * 4);
   scratch = std::max(scratch, g->S * G * 2 * 4);
   g->scratch_bytes = ((scratch + 127) / 128) * 128;
   const int avail = smem_limit - g->xbuf_bytes - g->scratch_bytes - kCtlSmem;
-  int np = avail > 0 ? avail / g->page_bytes : 0;
+  int np = avail > 0 ? avail / g->page_stride : 0;
   np = std::min(np, kMaxPages);
   if (n_pages_req > 0) np = std::min(np, n_pages_req);
   if (np < 2)
     return fmt("shared memory too small: x buffer %lld B + scratch %lld B leave %lld pages (max_batch too large)",
                g->xbuf_bytes, g->scratch_bytes, np);
   g->n_pages = np;
-  g->smem_bytes = np * g->page_bytes + g->xbuf_bytes + g->scratch_bytes + kCtlSmem;
+  g->smem_bytes = np * g->page_stride + g->xbuf_bytes + g->scratch_bytes + kCtlSmem;
   return "";
 }
 
@@ -101,7 +110,8 @@ int choose_merge(const ModelShape& m, const Geometry& g, int B, bool counters, i
   const long long part_bytes = 4LL * B * m.Hkv * g.S * G * (m.hd + kPartExtra);
   const long long weight_floats = 3LL * B * m.Hkv * g.S * G;  // (max, sum) pairs + merge weights
   const bool fits = part_bytes <= kMergeInBytes && weight_floats * 4 <= g.scratch_bytes;
-  if (requested == 2 || (requested == 0 && fits)) return MERGE_IN_OPROJ;
+  const bool tc = use_tc(g, pow2_at_least(B));  // the tensor-core GEMV stages its own input layout
+  if (!tc && (requested == 2 || (requested == 0 && fits))) return MERGE_IN_OPROJ;
   return counters ? MERGE_LAST_ARRIVER : MERGE_OP;
 }
 
@@ -119,6 +129,7 @@ std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B,
   const int half = m.hd / 2;
   const int G = m.Hq / m.Hkv;
   auto rows_cap = [&](int K, int ws, int segs) {  // rows per GEMV instruction (rowpart scratch)
+    if (use_tc(g, nb)) return std::max(1, (scratch_floats - kTcPartialFloats) / (nb * segs));
     const int spr = K / ws;
     return std::max(1, scratch_floats / (spr * nb * segs));
   };
@@ -444,7 +455,8 @@ std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p)
       }
       if (K) {
         if (rows < 1) return "empty GEMV instruction";
-        if ((long long)rows * (K / ws) * nb > scratch_floats)
+        const long long need = use_tc(g, nb) ? (long long)rows * nb + kTcPartialFloats : (long long)rows * (K / ws) * nb;
+        if (need > scratch_floats)
           return fmt("cta %lld pc %lld: GEMV row partials exceed the scratch (%lld floats)", c, k, scratch_floats);
       }
     }

@@ -39,7 +39,7 @@ def summarize(trace):
     by = {}
     per_cta_wait = {}
     groups = {}
-    keys = ("stage", "pages", "page_wait", "page_work", "epi", "epi_clk", "epi_pre", "tail", "write", "arrive", "merge")
+    keys = ("stage", "pages", "page_wait", "page_work", "epi", "epi_clk", "tail", "write", "arrive", "merge")
     for cta, pc, op, layer, tf, tr, te, m0, m1, m2, m3, m4, m5 in trace:
         d = by.setdefault(OPS.get(op, str(op)), {k: [] for k in ("wait", "work") + keys})
         d["wait"].append((tr - tf) / 1e3)
@@ -51,8 +51,7 @@ def summarize(trace):
             d["page_work"].append(m4 / 1e3)
             if m3:
                 d["epi"].append((m3 - m1) / 1e3)
-                d["epi_clk"].append((m5 & 0xFFFFFFFF) / 2.07e3)   # cycles -> us at the 2070 MHz clock
-                d["epi_pre"].append((m5 >> 32) / 2.07e3)
+                d["epi_clk"].append(m5 / 2.07e3)   # cycles -> us at the 2070 MHz clock
                 d["tail"].append((te - m3) / 1e3)
         elif op == 3 and m0 and m1:
             d["stage"].append((m0 - tr) / 1e3)
@@ -100,6 +99,8 @@ def main():
     ap.add_argument("--merge", type=int, default=0, help="KV-split merge: 0 auto, 1 separate step, 2 in O-proj")
     ap.add_argument("--inflight", type=int, default=0, help="page copies in flight per CTA (0: default, <0: pool)")
     ap.add_argument("--split-min", type=int, default=0)
+    ap.add_argument("--synthetic-kv", action="store_true",
+                    help="fill the first --prompt cache positions with seeded synthetic keys/values instead of a prefill")
     ap.add_argument("--json", default="")
     args = ap.parse_args()
 
@@ -122,7 +123,13 @@ def main():
                       split_min_positions=args.split_min, attn_merge=args.merge,
                       inflight_pages=args.inflight, stream=stream)
         prompt = synth.gen_prompts(cfg, B, args.prompt)
-        tok = dec.prefill(prompt)
+        if args.synthetic_kv:
+            for l in range(cfg.n_layers):
+                for b in range(B):
+                    dm.set_kv(l, b, synth.gen_kv(cfg, l, b, 0, args.prompt), synth.gen_kv(cfg, l, b, 1, args.prompt))
+            tok = prompt[:, -1]
+        else:
+            tok = dec.prefill(prompt)
         pos = args.prompt
         times = []
         for _ in range(args.steps):

@@ -6,9 +6,9 @@
   step is the same code at any context, and the 32k-context test below covers long
   caches.
 * 2b at 32k context: the 2b fp16 model with 32768 cached positions per sequence, at
-  batch 1, 2 and 4.  The cache holds seeded synthetic keys and values (synth.gen_kv, the
+  batch 1, 2, 4, 8 and 16 (3..16 on the tensor-core GEMV).  The cache holds seeded synthetic keys and values (synth.gen_kv, the
   same bytes on both sides) instead of a 32k-token prefill, which the oracle cannot run
-  in test time.  The oracle checks sequences 0, 1 and 3 one at a time.  Every sequence
+  in test time.  The oracle checks sequences 0, 1, 3, 7 and 15 one at a time.  Every sequence
   of a batch must also match that sequence at the smallest batch that holds it
   (batch invariance).
 """
@@ -55,20 +55,21 @@ def test_8b_teacher_forced(lib):
 
 T32K = synth.CONFIGS["2b-32k"].prompt_len     # 32768 cached positions
 N_STEPS = 2
-CHECKED = (0, 1, 3)                            # sequences the oracle decodes
+CHECKED = (0, 1, 3, 7, 15)                     # sequences the oracle decodes
+MAXB = 16
 
 
 @pytest.fixture(scope="module")
 def long_ctx(lib):
-    """Device model at batch 4 with every sequence's 32k cache filled, the teacher-forced
-    tokens, and the oracle's logits [N_STEPS, V] for the checked sequences."""
+    """Device model for 16 sequences with every sequence's 32k cache filled, the
+    teacher-forced tokens, and the oracle's logits [N_STEPS, V] for the checked sequences."""
     cfg = synth.CONFIGS["2b-32k"]
     w = synth.gen_weights(cfg)
     m = oracle.Model(cfg, w)
-    dm = lib.DeviceModel(cfg, w, max_batch=4, max_ctx=T32K + N_STEPS + 1)
-    toks = np.stack([synth.gen_prompt(cfg, b, N_STEPS) for b in range(4)])
+    dm = lib.DeviceModel(cfg, w, max_batch=MAXB, max_ctx=T32K + N_STEPS + 1)
+    toks = np.stack([synth.gen_prompt(cfg, b, N_STEPS) for b in range(MAXB)])
     zref = {}
-    for b in range(4):
+    for b in range(MAXB):
         cache = oracle.KVCache(cfg, 1, T32K + N_STEPS) if b in CHECKED else None
         for l in range(cfg.n_layers):
             kb = synth.gen_kv(cfg, l, b, 0, T32K)
@@ -83,7 +84,7 @@ def long_ctx(lib):
     return cfg, dm, toks, zref, {}
 
 
-@pytest.mark.parametrize("B", [1, 2, 4])
+@pytest.mark.parametrize("B", [1, 2, 4, 8, 16])
 def test_2b_32k_context_batches(long_ctx, lib, B):
     cfg, dm, toks, zref, seen = long_ctx
     dec = lib.Decoder(dm)
