@@ -238,7 +238,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sync", default="sentinel", choices=["counter", "sentinel"])
-    ap.add_argument("--exec", default="persistent", choices=["persistent", "multilaunch"])
+    ap.add_argument("--exec", default="persistent", choices=["persistent", "multilaunch", "graph"])
     ap.add_argument("--batch", type=int, default=1)
     args = ap.parse_args()
     if args.impl == "reference":
@@ -264,7 +264,7 @@ def main():
     stream = torch.cuda.Stream(device)
     with torch.cuda.stream(stream):
         dec = Decoder(dm, sync_mode=0 if args.sync == "counter" else 1,
-                      exec_mode=0 if args.exec == "persistent" else 1, stream=stream)
+                      exec_mode={"persistent": 0, "multilaunch": 1, "graph": 2}[args.exec], stream=stream)
         info = dec.info()
         prompt = synth.gen_prompts(cfg, B, PROMPT)
         first = dec.prefill(prompt)

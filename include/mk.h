@@ -41,7 +41,11 @@ typedef enum {
 
 typedef enum { MK_F16 = 0, MK_BF16 = 1 } mk_dtype;
 typedef enum { MK_SYNC_COUNTER = 0, MK_SYNC_SENTINEL = 1 } mk_sync_mode;
-typedef enum { MK_EXEC_PERSISTENT = 0, MK_EXEC_MULTILAUNCH = 1 } mk_exec_mode;
+/* MK_EXEC_GRAPH: the multi-launch control captured once per batch size into a CUDA graph
+ * whose launches are programmatic dependent launches (each grid's loader streams its
+ * weights while the previous grid drains; its compute warps wait for that grid), with the
+ * per-step arguments in device memory. */
+typedef enum { MK_EXEC_PERSISTENT = 0, MK_EXEC_MULTILAUNCH = 1, MK_EXEC_GRAPH = 2 } mk_exec_mode;
 
 typedef struct mk_ctx mk_ctx;
 

@@ -22,7 +22,7 @@ lib = ctypes.CDLL(LIB_PATH)
 MK_OK, MK_ERR_INVALID, MK_ERR_OCCUPANCY, MK_ERR_CUDA, MK_ERR_TIMEOUT, MK_ERR_STATE, MK_ERR_NAN = range(7)
 MK_F16, MK_BF16 = 0, 1
 MK_SYNC_COUNTER, MK_SYNC_SENTINEL = 0, 1
-MK_EXEC_PERSISTENT, MK_EXEC_MULTILAUNCH = 0, 1
+MK_EXEC_PERSISTENT, MK_EXEC_MULTILAUNCH, MK_EXEC_GRAPH = 0, 1, 2
 
 c_int, c_float, c_double, c_void_p = ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_void_p
 P_void = ctypes.POINTER(ctypes.c_void_p)

@@ -50,6 +50,14 @@ struct Sched {
   DevBuf instr, qstart, counters;
   std::vector<DevBuf> ph_instr, ph_qstart;
   uint32_t epoch = 0;
+  DevBuf dyn;                       // MK_EXEC_GRAPH: the step's arguments in device memory
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t gexec = nullptr;
+  const TraceRec* graph_trace = nullptr;  // the journal buffer the captured launches write
+  ~Sched() {
+    if (gexec) cudaGraphExecDestroy(gexec);
+    if (graph) cudaGraphDestroy(graph);
+  }
 };
 
 }  // namespace
@@ -159,7 +167,7 @@ mk_status get_sched(mk_ctx* ctx, int B, Sched** out) {
   if (s) return s;
   MK_CUDA(cudaMalloc(&sc->counters.p, sizeof(uint32_t) * std::max(1, sc->plan.n_counters)));
   MK_CUDA(cudaMemset(sc->counters.p, 0, sizeof(uint32_t) * std::max(1, sc->plan.n_counters)));
-  if (ctx->opts.exec_mode == MK_EXEC_MULTILAUNCH) {
+  if (ctx->opts.exec_mode != MK_EXEC_PERSISTENT) {
     const size_t np = sc->plan.phase_queues.size();
     sc->ph_instr.resize(np);
     sc->ph_qstart.resize(np);
@@ -184,19 +192,72 @@ mk_status get_sched(mk_ctx* ctx, int B, Sched** out) {
   return MK_OK;
 }
 
-mk_status launch(mk_ctx* ctx, const void* fn, const DevState& S, const StepArgs& A, bool cooperative) {
+mk_status launch(mk_ctx* ctx, const void* fn, const DevState& S, const StepArgs& A, bool cooperative,
+                 bool programmatic = false, cudaStream_t stream = nullptr, bool own_stream = false) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(ctx->n_cta);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = ctx->geo.smem_bytes;
-  cfg.stream = ctx->stream;
-  cudaLaunchAttribute attr[1];
+  cfg.stream = own_stream ? stream : ctx->stream;
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = cooperative ? 1 : 0;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = programmatic ? 2 : 1;
   void* args[2] = {const_cast<DevState*>(&S), const_cast<StepArgs*>(&A)};
   MK_CUDA(cudaLaunchKernelExC(&cfg, fn, args));
+  return MK_OK;
+}
+
+// MK_EXEC_GRAPH: the per-op launches captured once (on a private stream) into a graph with
+// programmatic dependencies between consecutive launches; each step copies its arguments
+// to device memory and launches the graph.
+mk_status run_graph(mk_ctx* ctx, Sched* sc, const DevState& S, const StepArgs& A, const void* fn) {
+  if (sc->gexec && sc->graph_trace != ctx->st.trace) {  // the journal buffer moved: capture again
+    cudaGraphExecDestroy(sc->gexec);
+    cudaGraphDestroy(sc->graph);
+    sc->gexec = nullptr;
+    sc->graph = nullptr;
+  }
+  if (!sc->dyn.p) MK_CUDA(cudaMalloc(&sc->dyn.p, sizeof(StepArgs)));
+  if (!sc->gexec) {
+    cudaStream_t cs;
+    MK_CUDA(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking));
+    cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+    mk_status st = MK_OK;
+    if (e == cudaSuccess) {
+      for (size_t k = 0; k < sc->ph_instr.size() && st == MK_OK; ++k) {
+        StepArgs Ak{};
+        Ak.instr = reinterpret_cast<const Instr*>(sc->ph_instr[k].p);
+        Ak.q_start = reinterpret_cast<const int32_t*>(sc->ph_qstart[k].p);
+        Ak.flags = SF_NO_SYNC | (k == 0 ? SF_RESET_ARGMAX : SF_PDL);
+        Ak.dyn = reinterpret_cast<const StepArgs*>(sc->dyn.p);
+        st = launch(ctx, fn, S, Ak, false, k > 0, cs, true);
+      }
+      cudaGraph_t g = nullptr;
+      const cudaError_t e2 = cudaStreamEndCapture(cs, &g);
+      if (st == MK_OK && e2 != cudaSuccess) e = e2;
+      if (st == MK_OK && e == cudaSuccess) {
+        sc->graph = g;
+        e = cudaGraphInstantiate(&sc->gexec, g, 0);
+      } else if (g) {
+        cudaGraphDestroy(g);
+      }
+    }
+    cudaStreamDestroy(cs);
+    if (st) return st;
+    if (e != cudaSuccess) return fail(MK_ERR_CUDA, std::string("graph capture: ") + cudaGetErrorString(e));
+    sc->graph_trace = ctx->st.trace;
+  }
+  StepArgs D = A;  // the per-step fields; the launches keep their own queues and flags
+  D.instr = nullptr;
+  D.q_start = nullptr;
+  D.dyn = nullptr;
+  D.flags = A.flags & (SF_TOK_FROM_DEVICE | SF_TRACE);
+  MK_CUDA(cudaMemcpyAsync(sc->dyn.p, &D, sizeof(D), cudaMemcpyHostToDevice, ctx->stream));
+  MK_CUDA(cudaGraphLaunch(sc->gexec, ctx->stream));
   return MK_OK;
 }
 
@@ -220,7 +281,10 @@ mk_status enqueue_step(mk_ctx* ctx, Sched* sc, int B, const int32_t* tok, const 
   const void* fn = ctx->opts.trace ? ctx->kernel_trace : ctx->kernel;
   if (ctx->opts.trace) MK_CUDA(cudaMemsetAsync(&reinterpret_cast<Ctl*>(ctx->ctl.p)->trace_n, 0, 4, ctx->stream));
   mk_status s;
-  if (ctx->opts.exec_mode == MK_EXEC_MULTILAUNCH) {
+  if (ctx->opts.exec_mode == MK_EXEC_GRAPH) {
+    s = run_graph(ctx, sc, S, A, fn);
+    if (s) return s;
+  } else if (ctx->opts.exec_mode == MK_EXEC_MULTILAUNCH) {
     const size_t np = sc->ph_instr.size();
     for (size_t k = 0; k < np; ++k) {
       StepArgs Ak = A;
@@ -313,7 +377,7 @@ mk_status mk_plan(const mk_model_desc* desc, const mk_options* opts, int n_ctas,
   info->kv_splits = g.S;
   for (const auto& q : p.queues) info->n_instructions += (int)q.size();
   info->n_counters = p.n_counters;
-  info->launches_per_step = o.exec_mode == MK_EXEC_MULTILAUNCH ? (int)p.phase_queues.size() : 1;
+  info->launches_per_step = o.exec_mode != MK_EXEC_PERSISTENT ? (int)p.phase_queues.size() : 1;
   info->weight_bytes_per_step = p.weight_bytes;
   return MK_OK;
 }
@@ -347,7 +411,8 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
   if (o.wait_timeout_s <= 0) o.wait_timeout_s = 2.0;
   if (o.backoff_max_ns <= 0) o.backoff_max_ns = 256;
   if (o.sync_mode != MK_SYNC_COUNTER && o.sync_mode != MK_SYNC_SENTINEL) return fail(MK_ERR_INVALID, "sync_mode");
-  if (o.exec_mode != MK_EXEC_PERSISTENT && o.exec_mode != MK_EXEC_MULTILAUNCH) return fail(MK_ERR_INVALID, "exec_mode");
+  if (o.exec_mode != MK_EXEC_PERSISTENT && o.exec_mode != MK_EXEC_MULTILAUNCH && o.exec_mode != MK_EXEC_GRAPH)
+    return fail(MK_ERR_INVALID, "exec_mode");
   if (o.attn_merge < 0 || o.attn_merge > 2) return fail(MK_ERR_INVALID, "attn_merge must be 0, 1 or 2");
   ctx->stream = reinterpret_cast<cudaStream_t>(stream);
   MK_CUDA(cudaGetDevice(&ctx->device));
@@ -495,7 +560,7 @@ mk_status mk_info(const mk_ctx* ctx, mk_info_t* info) {
     info->n_instructions = it->second->n_instr;
     info->n_counters = it->second->plan.n_counters;
     info->launches_per_step =
-        ctx->opts.exec_mode == MK_EXEC_MULTILAUNCH ? (int)it->second->plan.phase_queues.size() : 1;
+        ctx->opts.exec_mode != MK_EXEC_PERSISTENT ? (int)it->second->plan.phase_queues.size() : 1;
     info->weight_bytes_per_step = it->second->plan.weight_bytes;
   }
   return MK_OK;
@@ -630,7 +695,7 @@ mk_status mk_read_activation(mk_ctx* ctx, int which, int layer, float* dst, size
   const size_t need = sizeof(float) * (size_t)m.max_batch * width;
   if (bytes != need) return fail(MK_ERR_INVALID, "bytes must equal max_batch * width * 4");
   MK_CUDA(cudaStreamSynchronize(ctx->stream));
-  const bool multi = ctx->opts.exec_mode == MK_EXEC_MULTILAUNCH;
+  const bool multi = ctx->opts.exec_mode != MK_EXEC_PERSISTENT;
   const int par = (ctx->opts.sync_mode == MK_SYNC_SENTINEL && !multi) ? (int)((ctx->step + 1u) & 1u) : 0;
   const float* src = ctx->st.act + (int64_t)par * ctx->st.act_floats + ctx->st.act_off[kind] +
                      (int64_t)layer * ctx->st.act_stride[kind];

@@ -154,6 +154,8 @@ enum StepFlags : int {
   SF_NO_SYNC = 2,          // multi-launch: stream order replaces waits and signals
   SF_TRACE = 4,
   SF_RESET_ARGMAX = 8,     // this launch resets the other parity's argmax keys
+  SF_PDL = 16,             // a programmatic dependent launch: compute warps wait for the
+                           // previous grid; the loader streams weights before that
 };
 
 struct StepArgs {
@@ -167,6 +169,9 @@ struct StepArgs {
   int32_t pos[kMaxBatch];
   float* logits;               // [B][V] or null
   int32_t* tok_hist;           // device [B] copy of this step's tokens, or null
+  // non-null: the per-step fields (epoch .. tok_hist; flags OR-ed) are read from this device
+  // copy at kernel start -- the launches of a CUDA graph keep fixed parameters
+  const StepArgs* dyn;
 };
 
 // Tensor-core GEMV (batches of 3..16 in contexts built for max_batch >= 8): a page holds

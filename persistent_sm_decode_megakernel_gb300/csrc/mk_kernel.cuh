@@ -31,6 +31,7 @@ struct SmemCtl {
   int last_issue_phase[kMaxPages];
   uint64_t tmark[6];  // journal marks inside an op
   volatile int abort;
+  StepArgs args;  // a device-memory copy of the step's arguments (CUDA-graph launches)
 };
 static_assert(sizeof(SmemCtl) <= kCtlSmem, "control block fits");
 
@@ -1648,6 +1649,21 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
   float* scratch = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(xbuf) + S.xbuf_bytes);
   SmemCtl* c = reinterpret_cast<SmemCtl*>(reinterpret_cast<uint8_t*>(scratch) + S.scratch_bytes);
   const int tid = threadIdx.x;
+  StepArgs& sA = c->args;  // the step's arguments when they come from device memory
+  // programmatic dependent launch: let the next grid be scheduled as soon as SMs free up
+  if (A.flags & SF_PDL) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (A.dyn != nullptr) {
+    constexpr int words = (int)(sizeof(StepArgs) / 4);
+    const uint32_t* from = reinterpret_cast<const uint32_t*>(A.dyn);
+    for (int i = tid; i < words; i += kThreads) reinterpret_cast<uint32_t*>(&sA)[i] = from[i];
+    __syncthreads();
+    if (tid == 0) {
+      sA.instr = A.instr;
+      sA.q_start = A.q_start;
+      sA.flags |= A.flags;
+      sA.dyn = nullptr;
+    }
+  }
   if (tid == 0) {
     for (int i = 0; i < S.n_pages; ++i) {
       mbar_init(&c->full[i], 1);
@@ -1658,24 +1674,27 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
     mbar_fence_init();
   }
   if (tid < kMaxBatch) c->best[tid] = 0ull;
+  __syncthreads();
+  const StepArgs& AA = A.dyn != nullptr ? sA : A;
   // per-step housekeeping: the other parity's argmax keys (and, with NaN sentinels, the
   // other parity's activations) are reset for the next step; nothing reads them now
-  if ((A.flags & SF_RESET_ARGMAX) && blockIdx.x == 0 && tid < kMaxBatch)
-    S.argkeys[((A.step + 1u) & 1u) * kMaxBatch + tid] = 0ull;
-  if (SYNC == SYNC_SENTINEL && !(A.flags & SF_NO_SYNC)) {
-    float* other = S.act + (int64_t)((A.step + 1u) & 1u) * S.act_floats;
+  if ((AA.flags & SF_RESET_ARGMAX) && blockIdx.x == 0 && tid < kMaxBatch)
+    S.argkeys[((AA.step + 1u) & 1u) * kMaxBatch + tid] = 0ull;
+  if (SYNC == SYNC_SENTINEL && !(AA.flags & SF_NO_SYNC)) {
+    float* other = S.act + (int64_t)((AA.step + 1u) & 1u) * S.act_floats;
     const int64_t n4 = S.act_floats / 4;
     float4* o4 = reinterpret_cast<float4*>(other);
     const float4 nan4 = make_float4(CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F);
     for (int64_t i = (int64_t)blockIdx.x * kThreads + tid; i < n4; i += (int64_t)gridDim.x * kThreads) o4[i] = nan4;
   }
   __syncthreads();
-  if (tid >= kConsumerThreads) {
+  if (tid >= kConsumerThreads) {  // the loader streams weights without waiting for the previous grid
     const int w = tid >> 5;
-    if (w == kLoaderWarp && (tid & 31) == 0) producer(S, A, c, pages);
+    if (w == kLoaderWarp && (tid & 31) == 0) producer(S, AA, c, pages);
     return;
   }
-  consumer<WT, SYNC>(S, A, c, pages, xbuf, scratch);
+  if (AA.flags & SF_PDL) asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous grid's outputs
+  consumer<WT, SYNC>(S, AA, c, pages, xbuf, scratch);
   if (c->abort && tid == 0 && !global_err(S)) set_err(S, 4u, -7, -1);
 }
 

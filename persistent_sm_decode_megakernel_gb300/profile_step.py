@@ -92,7 +92,7 @@ def main():
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--trace", action="store_true")
     ap.add_argument("--sync", default="counter", choices=["counter", "sentinel"])
-    ap.add_argument("--exec", default="persistent", choices=["persistent", "multilaunch"])
+    ap.add_argument("--exec", default="persistent", choices=["persistent", "multilaunch", "graph"])
     ap.add_argument("--page-bytes", type=int, default=0)
     ap.add_argument("--n-pages", type=int, default=0)
     ap.add_argument("--backoff", type=int, default=0)
@@ -118,7 +118,7 @@ def main():
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         dec = Decoder(dm, sync_mode=0 if args.sync == "counter" else 1,
-                      exec_mode=0 if args.exec == "persistent" else 1, trace=1 if args.trace else 0,
+                      exec_mode={"persistent": 0, "multilaunch": 1, "graph": 2}[args.exec], trace=1 if args.trace else 0,
                       page_bytes=args.page_bytes, n_pages=args.n_pages, backoff_max_ns=args.backoff,
                       split_min_positions=args.split_min, attn_merge=args.merge,
                       inflight_pages=args.inflight, stream=stream)

@@ -73,10 +73,11 @@ def test_plan_multilaunch_counts_launches(mk):
     # the KV-split merge: inside the O-proj staging (attn_merge 2) or in the last-arriving
     # split (counter sync) -- five launches per layer either way -- or a separate reduce
     # launch per layer (sentinel sync); auto (0) keeps the separate step at the 2b size
-    for sync, merge, per_layer in ((0, 0, 5), (1, 0, 6), (0, 2, 5), (1, 2, 5), (0, 1, 5), (1, 1, 6)):
-        st, info = _plan(mk, _desc(mk, cfg), 152, exec_mode=mk.MK_EXEC_MULTILAUNCH, sync_mode=sync, attn_merge=merge)
-        assert st == mk.MK_OK, mk.mk_last_error()
-        assert info.launches_per_step == per_layer * L + 2, (sync, merge)
+    for execm in (mk.MK_EXEC_MULTILAUNCH, mk.MK_EXEC_GRAPH):
+        for sync, merge, per_layer in ((0, 0, 5), (1, 0, 6), (0, 2, 5), (1, 2, 5), (0, 1, 5), (1, 1, 6)):
+            st, info = _plan(mk, _desc(mk, cfg), 152, exec_mode=execm, sync_mode=sync, attn_merge=merge)
+            assert st == mk.MK_OK, mk.mk_last_error()
+            assert info.launches_per_step == per_layer * L + 2, (sync, merge)
 
 
 def test_plan_merge_choice_and_bad_option(mk):

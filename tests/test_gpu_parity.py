@@ -43,7 +43,8 @@ def _close(got, want, rtol=INTER_RTOL, what=""):
     return err / scale
 
 
-@pytest.mark.parametrize("sync,execm", [(0, 0), (1, 0), (0, 1)], ids=["counter", "sentinel", "multilaunch"])
+@pytest.mark.parametrize("sync,execm", [(0, 0), (1, 0), (0, 1), (0, 2), (1, 2)],
+                         ids=["counter", "sentinel", "multilaunch", "graph", "graph-sentinel"])
 def test_tiny_full_model_teacher_forced(lib, tiny, sync, execm):
     cfg, w, m = tiny
     P, n_new = cfg.prompt_len, cfg.decode_len
