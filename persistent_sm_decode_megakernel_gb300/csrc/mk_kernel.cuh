@@ -35,6 +35,23 @@ struct SmemCtl {
 };
 static_assert(sizeof(SmemCtl) <= kCtlSmem, "control block fits");
 
+// The dynamic shared memory: pages | x buffer | scratch | control block.  Functions that
+// are not inlined into the kernel re-derive their pointers from this symbol, so that the
+// compiler emits shared-space accesses (a pointer passed in as a plain argument is a
+// generic address, and generic accesses measured ~50x slower than ld.shared here while
+// the loader's bulk copies stream into the same SM).
+extern __shared__ __align__(1024) uint8_t mk_smem[];
+__device__ __forceinline__ uint8_t* smem_pages() { return mk_smem; }
+__device__ __forceinline__ float* smem_xbuf(const DevState& S) {
+  return reinterpret_cast<float*>(mk_smem + (size_t)S.n_pages * S.page_stride);
+}
+__device__ __forceinline__ float* smem_scratch(const DevState& S) {
+  return reinterpret_cast<float*>(mk_smem + (size_t)S.n_pages * S.page_stride + S.xbuf_bytes);
+}
+__device__ __forceinline__ SmemCtl* smem_ctl(const DevState& S) {
+  return reinterpret_cast<SmemCtl*>(mk_smem + (size_t)S.n_pages * S.page_stride + S.xbuf_bytes + S.scratch_bytes);
+}
+
 enum { SYNC_COUNTER = 0, SYNC_SENTINEL = 1 };
 
 // ---------------------------------------------------------------- errors
@@ -245,6 +262,8 @@ __device__ __noinline__ bool producer_acquire(const DevState& S, SmemCtl* c, int
 }
 
 __device__ __noinline__ void producer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8_t* pages) {
+  c = smem_ctl(S);
+  pages = smem_pages();
   const uint64_t pol = l2_evict_first_policy();
   int slot = 0;
   uint32_t ph = 0;
@@ -395,6 +414,14 @@ __device__ __noinline__ void producer(const DevState& S, const StepArgs& A, Smem
 struct Ring {
   int slot;
   uint32_t ph;
+};
+// an op works on a register copy of the caller's ring position and writes it back when it
+// returns (the caller's copy lives in local memory: reached through a generic pointer)
+struct RingCopy {
+  Ring& io;
+  Ring r;
+  __device__ __forceinline__ explicit RingCopy(Ring& ring) : io(ring), r(ring) {}
+  __device__ __forceinline__ ~RingCopy() { io = r; }
 };
 
 __device__ __noinline__ void page_wait_slow(const DevState& S, SmemCtl* c, const Ring& r) {
@@ -867,7 +894,13 @@ __device__ __forceinline__ void gemv_epilogue(const DevState& S, const StepArgs&
 
 template <typename WT, int SYNC, int NB>
 __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const Instr& in, SmemCtl* c, uint8_t* pages,
-                        float* xbuf, float* scratch, Ring& ring, float* act) {
+                        float* xbuf, float* scratch, Ring& ring_io, float* act) {
+  c = smem_ctl(S);
+  pages = smem_pages();
+  xbuf = smem_xbuf(S);
+  scratch = smem_scratch(S);
+  RingCopy ring_copy(ring_io);
+  Ring& ring = ring_copy.r;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = A.B, l = in.layer;
   const Gemv g = make_gemv(S, in);
@@ -1005,7 +1038,13 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
 // and the common epilogue finishes the rows.
 template <typename WT, int SYNC, int NB>
 __device__ __noinline__ void op_gemv_tc(const DevState& S, const StepArgs& A, const Instr& in, SmemCtl* c,
-                                        uint8_t* pages, float* xbuf, float* scratch, Ring& ring, float* act) {
+                                        uint8_t* pages, float* xbuf, float* scratch, Ring& ring_io, float* act) {
+  c = smem_ctl(S);
+  pages = smem_pages();
+  xbuf = smem_xbuf(S);
+  scratch = smem_scratch(S);
+  RingCopy ring_copy(ring_io);
+  Ring& ring = ring_copy.r;
   constexpr int MT = (NB + 7) / 8;  // A tiles of 8 sequences
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, cq = lane & 3;
   const int B = A.B, l = in.layer;
@@ -1174,7 +1213,13 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S, const StepArgs& A, co
 // ---------------------------------------------------------------- attention
 template <typename WT, int SYNC, int HD, int G>
 __device__ __noinline__ void op_attn(const DevState& S, const StepArgs& A, const Instr& in, SmemCtl* c, uint8_t* pages,
-                        float* xbuf, float* scratch, Ring& ring, float* act) {
+                        float* xbuf, float* scratch, Ring& ring_io, float* act) {
+  c = smem_ctl(S);
+  pages = smem_pages();
+  xbuf = smem_xbuf(S);
+  scratch = smem_scratch(S);
+  RingCopy ring_copy(ring_io);
+  Ring& ring = ring_copy.r;
   // DPL dims per lane = DPL/8 16-byte row chunks, lane dl of a position group taking
   // chunks dl, dl + LPP, ... (each load instruction reads contiguous bytes across the
   // group: no bank conflicts).  16 dims per lane for G <= 2 (fewer shuffle stages per
@@ -1375,6 +1420,9 @@ __device__ __noinline__ void op_attn(const DevState& S, const StepArgs& A, const
 template <int SYNC>
 __device__ __noinline__ void op_attn_reduce(const DevState& S, const StepArgs& A, const Instr& in, SmemCtl* c,
                                             float* xbuf, float* scratch, float* act) {
+  c = smem_ctl(S);
+  xbuf = smem_xbuf(S);
+  scratch = smem_scratch(S);
   const int tid = threadIdx.x;
   const int b = in.a[0], j = in.a[1], l = in.layer;
   if (b >= A.B) return;  // uniform over the CTA
@@ -1457,7 +1505,12 @@ __device__ void op_embed(const DevState& S, const StepArgs& A, const Instr& in, 
 
 // ---------------------------------------------------------------- self-test opcodes
 __device__ void op_test_pages(const DevState& S, const Instr& in, SmemCtl* c, uint8_t* pages, float* scratch,
-                              Ring& ring) {
+                              Ring& ring_io) {
+  c = smem_ctl(S);
+  pages = smem_pages();
+  scratch = smem_scratch(S);
+  RingCopy ring_copy(ring_io);
+  Ring& ring = ring_copy.r;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   unsigned long long* ws = reinterpret_cast<unsigned long long*>(scratch);
   const int words = S.page_bytes / 8, per_warp = words / kConsumerWarps;
@@ -1483,6 +1536,10 @@ __device__ void op_test_pages(const DevState& S, const Instr& in, SmemCtl* c, ui
 template <typename WT, int SYNC>
 __device__ void consumer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8_t* pages, float* xbuf,
                          float* scratch) {
+  c = smem_ctl(S);
+  pages = smem_pages();
+  xbuf = smem_xbuf(S);
+  scratch = smem_scratch(S);
   const int tid = threadIdx.x, cta = blockIdx.x;
   const bool nosync = (A.flags & SF_NO_SYNC) != 0;
   const bool TRACE = (A.flags & SF_TRACE) != 0;
