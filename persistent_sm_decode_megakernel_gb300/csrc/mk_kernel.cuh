@@ -31,25 +31,25 @@ struct SmemCtl {
   int last_issue_phase[kMaxPages];
   uint64_t tmark[6];  // journal marks inside an op
   volatile int abort;
-  StepArgs args;  // a device-memory copy of the step's arguments (CUDA-graph launches)
+  StepArgs args;  // the step's arguments (from the launch, or from device memory for graphs)
+  DevState S;     // the context's state, copied from the launch parameters
 };
 static_assert(sizeof(SmemCtl) <= kCtlSmem, "control block fits");
 
-// The dynamic shared memory: pages | x buffer | scratch | control block.  Functions that
-// are not inlined into the kernel re-derive their pointers from this symbol, so that the
-// compiler emits shared-space accesses (a pointer passed in as a plain argument is a
-// generic address, and generic accesses measured ~50x slower than ld.shared here while
-// the loader's bulk copies stream into the same SM).
+// The dynamic shared memory: control block | pages | x buffer | scratch.  The control
+// block holds copies of the kernel's state and step arguments.  Functions that are not
+// inlined into the kernel take those copies and their pointers from this symbol, so that
+// the compiler emits shared-space accesses: a pointer or reference passed in as an
+// argument is a generic address, and generic loads measured ~50x slower than ld.shared
+// here while the loader's bulk copies stream into the same SM.
 extern __shared__ __align__(1024) uint8_t mk_smem[];
-__device__ __forceinline__ uint8_t* smem_pages() { return mk_smem; }
+__device__ __forceinline__ SmemCtl* smem_ctl() { return reinterpret_cast<SmemCtl*>(mk_smem); }
+__device__ __forceinline__ uint8_t* smem_pages() { return mk_smem + kCtlSmem; }
 __device__ __forceinline__ float* smem_xbuf(const DevState& S) {
-  return reinterpret_cast<float*>(mk_smem + (size_t)S.n_pages * S.page_stride);
+  return reinterpret_cast<float*>(mk_smem + kCtlSmem + (size_t)S.n_pages * S.page_stride);
 }
 __device__ __forceinline__ float* smem_scratch(const DevState& S) {
-  return reinterpret_cast<float*>(mk_smem + (size_t)S.n_pages * S.page_stride + S.xbuf_bytes);
-}
-__device__ __forceinline__ SmemCtl* smem_ctl(const DevState& S) {
-  return reinterpret_cast<SmemCtl*>(mk_smem + (size_t)S.n_pages * S.page_stride + S.xbuf_bytes + S.scratch_bytes);
+  return reinterpret_cast<float*>(mk_smem + kCtlSmem + (size_t)S.n_pages * S.page_stride + S.xbuf_bytes);
 }
 
 enum { SYNC_COUNTER = 0, SYNC_SENTINEL = 1 };
@@ -68,7 +68,8 @@ __device__ __forceinline__ bool global_err(const DevState& S) {
 
 // Bounded wait on a dependency counter (§8.5): acquire load, exponential __nanosleep
 // backoff, gives up after the timeout and records where.  Wrap-safe comparison.
-__device__ __noinline__ bool wait_counter(const DevState& S, int ctr, uint32_t target, int pc) {
+__device__ __noinline__ bool wait_counter(const DevState& S_arg, int ctr, uint32_t target, int pc) {
+  const DevState& S = smem_ctl()->S;
   const uint32_t* p = S.counters + ctr;
   if ((int32_t)(ld_acquire_u32(p) - target) >= 0) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -237,7 +238,8 @@ __device__ __forceinline__ float* act_ptr(const DevState& S, float* act, int kin
 // landed, so that at most that many copies of this CTA queue in the memory system (the
 // ring still holds n_pages of landed pages as slack; fewer copies in flight shorten the
 // queues that the dependency-carrying loads and stores wait in).
-__device__ __noinline__ bool producer_wait(const DevState& S, SmemCtl* c, uint64_t* bar, uint32_t parity) {
+__device__ __noinline__ bool producer_wait(const DevState& S_arg, SmemCtl* c, uint64_t* bar, uint32_t parity) {
+  const DevState& S = smem_ctl()->S;
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_wait_hint(bar, parity, 2000u)) {
@@ -250,7 +252,8 @@ __device__ __noinline__ bool producer_wait(const DevState& S, SmemCtl* c, uint64
   }
   return true;
 }
-__device__ __noinline__ bool producer_acquire(const DevState& S, SmemCtl* c, int slot, uint32_t ph, long long issued) {
+__device__ __noinline__ bool producer_acquire(const DevState& S_arg, SmemCtl* c, int slot, uint32_t ph, long long issued) {
+  const DevState& S = smem_ctl()->S;
   if (!producer_wait(S, c, &c->empty[slot], ph ^ 1)) return false;
   const int F = S.inflight_pages;
   if (F > 0 && F < S.n_pages && issued >= F) {
@@ -261,8 +264,10 @@ __device__ __noinline__ bool producer_acquire(const DevState& S, SmemCtl* c, int
   return true;
 }
 
-__device__ __noinline__ void producer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8_t* pages) {
-  c = smem_ctl(S);
+__device__ __noinline__ void producer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* c, uint8_t* pages) {
+  const DevState& S = smem_ctl()->S;
+  const StepArgs& A = smem_ctl()->args;
+  c = smem_ctl();
   pages = smem_pages();
   const uint64_t pol = l2_evict_first_policy();
   int slot = 0;
@@ -893,9 +898,11 @@ __device__ __forceinline__ void gemv_epilogue(const DevState& S, const StepArgs&
 }
 
 template <typename WT, int SYNC, int NB>
-__device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const Instr& in, SmemCtl* c, uint8_t* pages,
+__device__ __noinline__ void op_gemv(const DevState& S_arg, const StepArgs& A_arg, const Instr& in, SmemCtl* c, uint8_t* pages,
                         float* xbuf, float* scratch, Ring& ring_io, float* act) {
-  c = smem_ctl(S);
+  const DevState& S = smem_ctl()->S;
+  const StepArgs& A = smem_ctl()->args;
+  c = smem_ctl();
   pages = smem_pages();
   xbuf = smem_xbuf(S);
   scratch = smem_scratch(S);
@@ -1037,9 +1044,11 @@ __device__ __noinline__ void op_gemv(const DevState& S, const StepArgs& A, const
 // page's k-steps; their partials are summed in a fixed order into per-row accumulators,
 // and the common epilogue finishes the rows.
 template <typename WT, int SYNC, int NB>
-__device__ __noinline__ void op_gemv_tc(const DevState& S, const StepArgs& A, const Instr& in, SmemCtl* c,
+__device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A_arg, const Instr& in, SmemCtl* c,
                                         uint8_t* pages, float* xbuf, float* scratch, Ring& ring_io, float* act) {
-  c = smem_ctl(S);
+  const DevState& S = smem_ctl()->S;
+  const StepArgs& A = smem_ctl()->args;
+  c = smem_ctl();
   pages = smem_pages();
   xbuf = smem_xbuf(S);
   scratch = smem_scratch(S);
@@ -1212,9 +1221,11 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S, const StepArgs& A, co
 
 // ---------------------------------------------------------------- attention
 template <typename WT, int SYNC, int HD, int G>
-__device__ __noinline__ void op_attn(const DevState& S, const StepArgs& A, const Instr& in, SmemCtl* c, uint8_t* pages,
+__device__ __noinline__ void op_attn(const DevState& S_arg, const StepArgs& A_arg, const Instr& in, SmemCtl* c, uint8_t* pages,
                         float* xbuf, float* scratch, Ring& ring_io, float* act) {
-  c = smem_ctl(S);
+  const DevState& S = smem_ctl()->S;
+  const StepArgs& A = smem_ctl()->args;
+  c = smem_ctl();
   pages = smem_pages();
   xbuf = smem_xbuf(S);
   scratch = smem_scratch(S);
@@ -1418,9 +1429,11 @@ __device__ __noinline__ void op_attn(const DevState& S, const StepArgs& A, const
 // buffer with vector loads when it fits (the caller has acquired the partials, or polls
 // them), else read from global memory eight splits deep.
 template <int SYNC>
-__device__ __noinline__ void op_attn_reduce(const DevState& S, const StepArgs& A, const Instr& in, SmemCtl* c,
+__device__ __noinline__ void op_attn_reduce(const DevState& S_arg, const StepArgs& A_arg, const Instr& in, SmemCtl* c,
                                             float* xbuf, float* scratch, float* act) {
-  c = smem_ctl(S);
+  const DevState& S = smem_ctl()->S;
+  const StepArgs& A = smem_ctl()->args;
+  c = smem_ctl();
   xbuf = smem_xbuf(S);
   scratch = smem_scratch(S);
   const int tid = threadIdx.x;
@@ -1504,9 +1517,10 @@ __device__ void op_embed(const DevState& S, const StepArgs& A, const Instr& in, 
 }
 
 // ---------------------------------------------------------------- self-test opcodes
-__device__ void op_test_pages(const DevState& S, const Instr& in, SmemCtl* c, uint8_t* pages, float* scratch,
+__device__ void op_test_pages(const DevState& S_arg, const Instr& in, SmemCtl* c, uint8_t* pages, float* scratch,
                               Ring& ring_io) {
-  c = smem_ctl(S);
+  const DevState& S = smem_ctl()->S;
+  c = smem_ctl();
   pages = smem_pages();
   scratch = smem_scratch(S);
   RingCopy ring_copy(ring_io);
@@ -1534,9 +1548,11 @@ __device__ void op_test_pages(const DevState& S, const Instr& in, SmemCtl* c, ui
 
 // ---------------------------------------------------------------- compute warps: loop
 template <typename WT, int SYNC>
-__device__ void consumer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8_t* pages, float* xbuf,
+__device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* c, uint8_t* pages, float* xbuf,
                          float* scratch) {
-  c = smem_ctl(S);
+  const DevState& S = smem_ctl()->S;
+  const StepArgs& A = smem_ctl()->args;
+  c = smem_ctl();
   pages = smem_pages();
   xbuf = smem_xbuf(S);
   scratch = smem_scratch(S);
@@ -1700,27 +1716,28 @@ __device__ void consumer(const DevState& S, const StepArgs& A, SmemCtl* c, uint8
 template <typename WT, int SYNC>
 __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_constant__ DevState S,
                                                               const __grid_constant__ StepArgs A) {
-  extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* pages = smem;
-  float* xbuf = reinterpret_cast<float*>(smem + (size_t)S.n_pages * S.page_stride);
-  float* scratch = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(xbuf) + S.xbuf_bytes);
-  SmemCtl* c = reinterpret_cast<SmemCtl*>(reinterpret_cast<uint8_t*>(scratch) + S.scratch_bytes);
+  SmemCtl* c = smem_ctl();
   const int tid = threadIdx.x;
-  StepArgs& sA = c->args;  // the step's arguments when they come from device memory
   // programmatic dependent launch: let the next grid be scheduled as soon as SMs free up
   if (A.flags & SF_PDL) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (A.dyn != nullptr) {
-    constexpr int words = (int)(sizeof(StepArgs) / 4);
-    const uint32_t* from = reinterpret_cast<const uint32_t*>(A.dyn);
-    for (int i = tid; i < words; i += kThreads) reinterpret_cast<uint32_t*>(&sA)[i] = from[i];
+  // the state and the step's arguments into the control block (shared-space reads from here on)
+  {
+    constexpr int ws = (int)(sizeof(DevState) / 4), wa = (int)(sizeof(StepArgs) / 4);
+    const uint32_t* fs = reinterpret_cast<const uint32_t*>(&S);
+    const uint32_t* fa = reinterpret_cast<const uint32_t*>(A.dyn != nullptr ? A.dyn : &A);
+    for (int i = tid; i < ws; i += kThreads) reinterpret_cast<uint32_t*>(&c->S)[i] = fs[i];
+    for (int i = tid; i < wa; i += kThreads) reinterpret_cast<uint32_t*>(&c->args)[i] = fa[i];
     __syncthreads();
-    if (tid == 0) {
-      sA.instr = A.instr;
-      sA.q_start = A.q_start;
-      sA.flags |= A.flags;
-      sA.dyn = nullptr;
+    if (tid == 0 && A.dyn != nullptr) {  // graph launches: their own queues and flags
+      c->args.instr = A.instr;
+      c->args.q_start = A.q_start;
+      c->args.flags |= A.flags;
+      c->args.dyn = nullptr;
     }
   }
+  uint8_t* pages = smem_pages();
+  float* xbuf = smem_xbuf(S);
+  float* scratch = smem_scratch(S);
   if (tid == 0) {
     for (int i = 0; i < S.n_pages; ++i) {
       mbar_init(&c->full[i], 1);
@@ -1732,7 +1749,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
   }
   if (tid < kMaxBatch) c->best[tid] = 0ull;
   __syncthreads();
-  const StepArgs& AA = A.dyn != nullptr ? sA : A;
+  const StepArgs& AA = c->args;
   // per-step housekeeping: the other parity's argmax keys (and, with NaN sentinels, the
   // other parity's activations) are reset for the next step; nothing reads them now
   if ((AA.flags & SF_RESET_ARGMAX) && blockIdx.x == 0 && tid < kMaxBatch)
