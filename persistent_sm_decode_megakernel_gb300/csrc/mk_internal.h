@@ -188,6 +188,6 @@ constexpr int kTcPartialFloats = 2 * kConsumerWarps * kTcRows * kMaxBatch;  // d
 constexpr int kPartExtra = 4;
 
 // shared-memory layout sizes (bytes)
-constexpr int kCtlSmem = 2048;   // barriers, flags, small broadcast values
+constexpr int kCtlSmem = 4096;   // barriers, flags, small broadcast values
 
 }  // namespace mk

@@ -33,6 +33,7 @@ struct SmemCtl {
   volatile int abort;
   StepArgs args;  // the step's arguments (from the launch, or from device memory for graphs)
   DevState S;     // the context's state, copied from the launch parameters
+  Instr cur[kConsumerWarps];  // each compute warp's copy of its current instruction
 };
 static_assert(sizeof(SmemCtl) <= kCtlSmem, "control block fits");
 
@@ -898,8 +899,9 @@ __device__ __forceinline__ void gemv_epilogue(const DevState& S, const StepArgs&
 }
 
 template <typename WT, int SYNC, int NB>
-__device__ __noinline__ void op_gemv(const DevState& S_arg, const StepArgs& A_arg, const Instr& in, SmemCtl* c, uint8_t* pages,
+__device__ __noinline__ void op_gemv(const DevState& S_arg, const StepArgs& A_arg, const Instr& in_arg, SmemCtl* c, uint8_t* pages,
                         float* xbuf, float* scratch, Ring& ring_io, float* act) {
+  const Instr& in = smem_ctl()->cur[threadIdx.x >> 5];
   const DevState& S = smem_ctl()->S;
   const StepArgs& A = smem_ctl()->args;
   c = smem_ctl();
@@ -1044,8 +1046,9 @@ __device__ __noinline__ void op_gemv(const DevState& S_arg, const StepArgs& A_ar
 // page's k-steps; their partials are summed in a fixed order into per-row accumulators,
 // and the common epilogue finishes the rows.
 template <typename WT, int SYNC, int NB>
-__device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A_arg, const Instr& in, SmemCtl* c,
+__device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A_arg, const Instr& in_arg, SmemCtl* c,
                                         uint8_t* pages, float* xbuf, float* scratch, Ring& ring_io, float* act) {
+  const Instr& in = smem_ctl()->cur[threadIdx.x >> 5];
   const DevState& S = smem_ctl()->S;
   const StepArgs& A = smem_ctl()->args;
   c = smem_ctl();
@@ -1221,8 +1224,9 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
 
 // ---------------------------------------------------------------- attention
 template <typename WT, int SYNC, int HD, int G>
-__device__ __noinline__ void op_attn(const DevState& S_arg, const StepArgs& A_arg, const Instr& in, SmemCtl* c, uint8_t* pages,
+__device__ __noinline__ void op_attn(const DevState& S_arg, const StepArgs& A_arg, const Instr& in_arg, SmemCtl* c, uint8_t* pages,
                         float* xbuf, float* scratch, Ring& ring_io, float* act) {
+  const Instr& in = smem_ctl()->cur[threadIdx.x >> 5];
   const DevState& S = smem_ctl()->S;
   const StepArgs& A = smem_ctl()->args;
   c = smem_ctl();
@@ -1429,8 +1433,9 @@ __device__ __noinline__ void op_attn(const DevState& S_arg, const StepArgs& A_ar
 // buffer with vector loads when it fits (the caller has acquired the partials, or polls
 // them), else read from global memory eight splits deep.
 template <int SYNC>
-__device__ __noinline__ void op_attn_reduce(const DevState& S_arg, const StepArgs& A_arg, const Instr& in, SmemCtl* c,
+__device__ __noinline__ void op_attn_reduce(const DevState& S_arg, const StepArgs& A_arg, const Instr& in_arg, SmemCtl* c,
                                             float* xbuf, float* scratch, float* act) {
+  const Instr& in = smem_ctl()->cur[threadIdx.x >> 5];
   const DevState& S = smem_ctl()->S;
   const StepArgs& A = smem_ctl()->args;
   c = smem_ctl();
@@ -1517,8 +1522,9 @@ __device__ void op_embed(const DevState& S, const StepArgs& A, const Instr& in, 
 }
 
 // ---------------------------------------------------------------- self-test opcodes
-__device__ void op_test_pages(const DevState& S_arg, const Instr& in, SmemCtl* c, uint8_t* pages, float* scratch,
+__device__ void op_test_pages(const DevState& S_arg, const Instr& in_arg, SmemCtl* c, uint8_t* pages, float* scratch,
                               Ring& ring_io) {
+  const Instr& in = smem_ctl()->cur[threadIdx.x >> 5];
   const DevState& S = smem_ctl()->S;
   c = smem_ctl();
   pages = smem_pages();
@@ -1569,6 +1575,8 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
   for (int pc = A.q_start[cta]; pc < end; ++pc) {
     const Instr in = load_instr(A.instr + pc);
     if (in.op == OP_END) break;
+    if ((tid & 31) == 0) c->cur[tid >> 5] = in;  // the ops read their warp's shared copy
+    __syncwarp();
     uint64_t t_fetch = 0, t_ready = 0;
     if (TRACE) {
       t_fetch = globaltimer_ns();
