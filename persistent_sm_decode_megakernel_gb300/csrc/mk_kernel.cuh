@@ -1091,14 +1091,18 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
   for (int b = 0; b < NB; ++b) ss[b] = 0.f;
   uint64_t page_wait_ns = 0, page_work_ns = 0;
   int pcount = 0;
+  // the x buffer holds SW page windows of split inputs at once: staged every SW windows
+  const int SW = max(1, (S.xbuf_bytes / 4) / (MT * 8 * kTcKw));
   for (int w = 0; w < nw; ++w) {
     const int k0 = w * kTcKw, kw = min(kTcKw, K - k0), nks = kw >> 4;
-    // 1. this window's inputs, split into hi/lo halves in fragment order (8 sequences per
-    //    tile; sequences >= B are zeros).  The previous window's pages are done: every
-    //    warp passed the barrier after its last page.
-    {
+    const int kso = (w % SW) * (kTcKw >> 4);  // this window's first k-step in the staged tile
+    // 1. the inputs of the next SW windows, split into hi/lo halves in fragment order (8
+    //    sequences per tile; sequences >= B are zeros).  The previous window's pages are
+    //    done: every warp passed the barrier after its last page.
+    if (w % SW == 0) {
       constexpr int U = 8;
-      const int k4n = kw >> 2, n_items = MT * 8 * k4n;
+      const int kws = min(SW * kTcKw, K - k0);
+      const int k4n = kws >> 2, n_items = MT * 8 * k4n;
       for (int base = 0; base < n_items; base += U * kConsumerThreads) {
         const float4* pp[U];
 #pragma unroll
@@ -1139,8 +1143,8 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
           wd[5] = (uint32_t)l2 | ((uint32_t)l3 << 16);
         }
       }
+      consumer_sync();
     }
-    consumer_sync();
     if (tid == 0 && trace && w == 0) c->tmark[0] = globaltimer_ns();
     // 2. the window's row blocks
     const int per = (nks + kConsumerWarps - 1) / kConsumerWarps, ks0 = warp * per, ks1 = min(nks, ks0 + per);
@@ -1164,7 +1168,7 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
         }
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          const uint4 a = *reinterpret_cast<const uint4*>(xt + ((size_t)(ks * MT + mt) * 32 + lane) * 4);
+          const uint4 a = *reinterpret_cast<const uint4*>(xt + ((size_t)((kso + ks) * MT + mt) * 32 + lane) * 4);
 #pragma unroll
           for (int nb = 0; nb < 2; ++nb) Mma<WT>::run(d[mt][nb], a, bw[nb][0], bw[nb][1]);
         }
