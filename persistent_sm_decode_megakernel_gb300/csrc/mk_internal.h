@@ -174,7 +174,7 @@ struct StepArgs {
   const StepArgs* dyn;
 };
 
-// Tensor-core GEMV (batches of 3..16 in contexts built for max_batch >= 8): a page holds
+// Tensor-core GEMV (batches of 3..16): a page holds
 // kTcRows weight rows of kTcKw columns (one window of the input), each row followed by a
 // 16-byte skew so that the 8 rows an mma fragment reads sit in different banks.
 constexpr int kTcKw = 1024;

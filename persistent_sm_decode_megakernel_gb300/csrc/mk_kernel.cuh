@@ -1036,7 +1036,7 @@ __device__ __noinline__ void op_gemv(const DevState& S_arg, const StepArgs& A_ar
 }
 
 // ---------------------------------------------------------------- tensor-core GEMV
-// Batches of 3..16 (contexts built for max_batch >= 8): y[b] = W x[b] for 16-row blocks of
+// Batches of 3..16: y[b] = W x[b] for 16-row blocks of
 // weights at a time with mma.sync m16n8k16.  A = the inputs: each 16-row A tile holds 8
 // sequences' inputs split into hi and lo 16-bit halves (rows 0-7 hi, rows 8-15 lo: the
 // MMA's f32 accumulator sums both, so the inputs keep ~22 significant bits with fp16);
@@ -1607,7 +1607,7 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
       case OP_UPGATE:
       case OP_DOWN:
       case OP_LMHEAD:
-        if (S.tc && nb >= 4) {  // batches of 3..16: tensor cores
+        if (nb >= 4) {  // batches of 3..16: tensor cores (every context for max_batch >= 3 is set up for them)
           switch (nb) {
             case 4: op_gemv_tc<WT, SYNC, 4>(S, A, in, c, pages, xbuf, scratch, ring, act); break;
             case 8: op_gemv_tc<WT, SYNC, 8>(S, A, in, c, pages, xbuf, scratch, ring, act); break;
@@ -1615,13 +1615,10 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
           }
           break;
         }
-        switch (nb) {
-          case 1: op_gemv<WT, SYNC, 1>(S, A, in, c, pages, xbuf, scratch, ring, act); break;
-          case 2: op_gemv<WT, SYNC, 2>(S, A, in, c, pages, xbuf, scratch, ring, act); break;
-          case 4: op_gemv<WT, SYNC, 4>(S, A, in, c, pages, xbuf, scratch, ring, act); break;
-          case 8: op_gemv<WT, SYNC, 8>(S, A, in, c, pages, xbuf, scratch, ring, act); break;
-          default: op_gemv<WT, SYNC, 16>(S, A, in, c, pages, xbuf, scratch, ring, act); break;
-        }
+        if (nb == 1)
+          op_gemv<WT, SYNC, 1>(S, A, in, c, pages, xbuf, scratch, ring, act);
+        else
+          op_gemv<WT, SYNC, 2>(S, A, in, c, pages, xbuf, scratch, ring, act);
         break;
       case OP_ATTN:
         if (S.hd == 64 && G == 2)

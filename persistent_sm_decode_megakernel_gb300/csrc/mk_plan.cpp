@@ -50,11 +50,11 @@ std::string make_geometry(const ModelShape& m, int n_cta, int page_bytes, int n_
     return "page_bytes must be a power of two in [4096, 32768]";
   if (g->page_bytes < 64 * m.hd) return fmt("page_bytes must be at least 64 * head_dim = %lld", 64LL * m.hd);
   g->nb_max = pow2_at_least(m.max_batch);
-  g->tc = m.max_batch >= 8 ? 1 : 0;
+  g->tc = m.max_batch >= 3 ? 1 : 0;  // batches of 3..16 run the tensor-core GEMV
   g->page_stride = g->page_bytes;
   if (g->tc) {
-    if (g->page_bytes != 32768) return "batches of 8 and more need 32 KB pages";
-    if (m.d % 16 || m.F % 16 || (m.Hq * m.hd) % 16) return "batches of 8 and more need dims that are multiples of 16";
+    if (g->page_bytes != 32768) return "batches of 3 and more need 32 KB pages";
+    if (m.d % 16 || m.F % 16 || (m.Hq * m.hd) % 16) return "batches of 3 and more need dims that are multiples of 16";
     g->page_stride = kTcPageBytes;
   }
   const int max_ws = g->page_bytes / (2 * kConsumerWarps);

@@ -26,7 +26,7 @@ struct Geometry {
   int smem_bytes = 0;
   int ws_qkv = 0, ws_o = 0, ws_up = 0, ws_down = 0, ws_lm = 0;
   int S = 1;             // kv splits per (sequence, kv head)
-  int tc = 0;            // max_batch >= 8: batches of 3..16 run the tensor-core GEMV
+  int tc = 0;            // max_batch >= 3: batches of 3..16 run the tensor-core GEMV
   int page_stride = 0;   // bytes between ring slots
 };
 // a GEMV of batch nb uses the tensor-core path

@@ -1,6 +1,6 @@
 """Batches of 3 to 16 sequences on the tensor-core GEMV path, against the oracle.
 
-A context built for max_batch >= 8 runs every GEMV of a 3..16-sequence step with
+Every GEMV of a 3..16-sequence step runs with
 mma.sync on 16-row weight blocks, its inputs split into hi/lo 16-bit halves (both the
 fp16 and the bf16 instances); batches of 1 and 2 in the same context keep the CUDA-core
 path.  Teacher forcing, per-step logits within 1e-2 of the oracle's largest |logit|.
