@@ -536,9 +536,8 @@ __device__ __forceinline__ void load_vecs(const DevState& S, SmemCtl* c, const f
   }
 }
 
-template <int SYNC, typename Put>
+template <int SYNC, int U = 4, typename Put>
 __device__ __forceinline__ void stage_vec(const DevState& S, const float4* src, int n4, SmemCtl* c, Put&& put) {
-  constexpr int U = 4;
   const int tid = threadIdx.x;
   for (int base = 0; base < n4; base += U * kConsumerThreads) {
     const float4* p[U];
@@ -653,7 +652,7 @@ template <int SYNC, int NB>
 __device__ void stage_copy(const DevState& S, const float* src, int K, int B, float* xbuf, SmemCtl* c) {
   float4* x4 = reinterpret_cast<float4*>(xbuf);
   const int k4 = K / 4;
-  stage_vec<SYNC>(S, reinterpret_cast<const float4*>(src), B * k4, c, [&](int i, const float4& v) { x4[i] = v; });
+  stage_vec<SYNC, 8>(S, reinterpret_cast<const float4*>(src), B * k4, c, [&](int i, const float4& v) { x4[i] = v; });
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int i = B * k4 + threadIdx.x; i < NB * k4; i += kConsumerThreads) x4[i] = z;
 }
@@ -1455,7 +1454,7 @@ __device__ __noinline__ void op_attn_reduce(const DevState& S_arg, const StepArg
   const int n4 = NS * G * RW / 4;
   if (n4 * 16 <= S.xbuf_bytes) {
     float4* x4 = reinterpret_cast<float4*>(xbuf);
-    stage_vec<SYNC>(S, reinterpret_cast<const float4*>(part), n4, c, [&](int i, const float4& v) { x4[i] = v; });
+    stage_vec<SYNC, 8>(S, reinterpret_cast<const float4*>(part), n4, c, [&](int i, const float4& v) { x4[i] = v; });
     consumer_sync();
     for (int t = tid; t < G * HD; t += kConsumerThreads) {
       const int g = t / HD, e = t - g * HD;
