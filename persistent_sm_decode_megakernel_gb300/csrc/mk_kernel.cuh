@@ -1383,22 +1383,42 @@ __device__ __noinline__ void op_attn(const DevState& S_arg, const StepArgs& A_ar
   if (at.has_new && warp == 0)  // position pos_b: the new key/value of this step
     update(pgi == 0, knew, knew + HD);
   if (mark) c->tmark[1] = globaltimer_ns();
-  // combine the position groups of the warp (same running max), then the warps
+  // Combine the NGRP position groups of the warp (they share the running max m[g]) with a
+  // butterfly reduce-scatter: each round halves the values a lane holds, so the warp
+  // shuffles V(1 - 1/NGRP) values instead of V log2(NGRP).  Lane group pgi ends with block
+  // bitrev(pgi) of the G*DPL accumulators, reduced over the whole warp.
+  constexpr int V = G * DPL;
+  constexpr int R = NGRP == 1 ? 0 : (NGRP == 2 ? 1 : (NGRP == 4 ? 2 : (NGRP == 8 ? 3 : 4)));
+  static_assert((1 << R) == NGRP && V % NGRP == 0, "reduce-scatter shape");
+  float a[V];
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
+  for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int o2 = LPP; o2 < 32; o2 <<= 1) {
-      lsum[g] += __shfl_xor_sync(0xffffffffu, lsum[g], o2);
+    for (int i = 0; i < DPL; ++i) a[g * DPL + i] = o[g][i];
 #pragma unroll
-      for (int i = 0; i < DPL; ++i) o[g][i] += __shfl_xor_sync(0xffffffffu, o[g][i], o2);
+  for (int r = 0; r < R; ++r) {
+    const int n = V >> r, o2 = LPP << r;
+    const bool upper = (lane & o2) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? a[i] : a[i + n / 2];
+      const float keep = upper ? a[i + n / 2] : a[i];
+      a[i] = keep + __shfl_xor_sync(0xffffffffu, send, o2);
     }
   }
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int o2 = LPP; o2 < 32; o2 <<= 1) lsum[g] += __shfl_xor_sync(0xffffffffu, lsum[g], o2);
   constexpr int RW = HD + kPartExtra;
-  if (pgi == 0) {
+  {
+    constexpr int NH = V / NGRP;  // accumulators a lane holds after the rounds
+    const int blk = R == 0 ? 0 : (int)(__brev((unsigned)pgi) >> (32 - R));
 #pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-      for (int i = 0; i < DPL; ++i) scratch[(warp * G + g) * RW + ((i / 8) * LPP + dl) * 8 + (i % 8)] = o[g][i];
+    for (int k = 0; k < NH; ++k) {
+      const int v = blk * NH + k, g = v / DPL, i = v % DPL;
+      scratch[(warp * G + g) * RW + ((i / 8) * LPP + dl) * 8 + (i % 8)] = a[k];
+    }
   }
   if (lane == 0) {
 #pragma unroll
@@ -1408,26 +1428,38 @@ __device__ __noinline__ void op_attn(const DevState& S_arg, const StepArgs& A_ar
     }
   }
   consumer_sync();
+  // the warps' partials, weighted by exp2(m_w - M) (a warp that saw no position has
+  // m_w = -inf and weight 0); the thread of element 0 of a head also writes M, the
+  // weighted sum and the two zero pads of the record
   float* part = act_ptr(S, act, ACT_PART, l) + (((size_t)at.b * S.Hkv + at.j) * S.S + at.s) * G * RW;
-  for (int t = tid; t < G * RW; t += kConsumerThreads) {
-    const int g = t / RW, e = t - g * RW;
+  for (int t = tid; t < G * HD; t += kConsumerThreads) {
+    const int g = t / HD, e = t - g * HD;
+    const float* sg = scratch + g * RW;
+    float mw[kConsumerWarps], wt[kConsumerWarps];
     float M = -CUDART_INF_F;
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, scratch[(w * G + g) * RW + HD]);
-    float r;
-    if (e == HD) {
-      r = M;
-    } else if (e > HD + 1) {
-      r = 0.f;  // pad: written so that sentinel polls of the whole record end
-    } else if (M == -CUDART_INF_F) {
-      r = 0.f;
-    } else {
-      r = 0.f;
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float mw = scratch[(w * G + g) * RW + HD];
-        if (mw != -CUDART_INF_F) r = fmaf(exp2f(mw - M), scratch[(w * G + g) * RW + e], r);
-      }
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      mw[w] = sg[w * G * RW + HD];
+      M = fmaxf(M, mw[w]);
     }
-    part[t] = r;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) wt[w] = mw[w] == -CUDART_INF_F ? 0.f : exp2f(mw[w] - M);
+    float r0 = 0.f, r1 = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; w += 2) {
+      r0 = fmaf(wt[w], sg[w * G * RW + e], r0);
+      r1 = fmaf(wt[w + 1], sg[(w + 1) * G * RW + e], r1);
+    }
+    part[g * RW + e] = r0 + r1;
+    if (e == 0) {
+      float L = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) L = fmaf(wt[w], sg[w * G * RW + HD + 1], L);
+      part[g * RW + HD] = M;
+      part[g * RW + HD + 1] = L;
+      part[g * RW + HD + 2] = 0.f;  // pads: written so that sentinel polls of the whole record end
+      part[g * RW + HD + 3] = 0.f;
+    }
   }
 }
 
@@ -1452,37 +1484,61 @@ __device__ __noinline__ void op_attn_reduce(const DevState& S_arg, const StepArg
   const float* part = act_ptr(S, act, ACT_PART, l) + ((size_t)b * S.Hkv + j) * S.S * G * RW;
   float* out = act_ptr(S, act, ACT_O, l) + (size_t)b * S.Hq * HD + (size_t)j * G * HD;
   const int n4 = NS * G * RW / 4;
-  if (n4 * 16 <= S.xbuf_bytes) {
+  const bool staged = n4 * 16 <= S.xbuf_bytes;
+  if (staged) {
     float4* x4 = reinterpret_cast<float4*>(xbuf);
     stage_vec<SYNC, 8>(S, reinterpret_cast<const float4*>(part), n4, c, [&](int i, const float4& v) { x4[i] = v; });
     consumer_sync();
+  }
+  // per (head, split) weight exp2(m_s - M) / sum_s' exp2(m_s' - M) l_s', one warp per head;
+  // a lane keeps its own splits' entries, so only the CTA barrier orders them for the readers
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int g = warp; g < G; g += kConsumerWarps) {
+    float* wg = scratch + g * NS;
+    float M = -CUDART_INF_F;
+    for (int s = lane; s < NS; s += 32) {
+      const int o = (s * G + g) * RW + HD;
+      const float ms = staged ? xbuf[o] : load_act<SYNC>(part + o, S, c);
+      wg[s] = ms;
+      M = fmaxf(M, ms);
+    }
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+    float den = 0.f;
+    for (int s = lane; s < NS; s += 32) {
+      const int o = (s * G + g) * RW + HD + 1;
+      const float w = wg[s] == -CUDART_INF_F ? 0.f : exp2f(wg[s] - M);
+      wg[s] = w;
+      den = fmaf(w, staged ? xbuf[o] : load_act<SYNC>(part + o, S, c), den);
+    }
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o2);
+    const float inv = 1.0f / den;
+    for (int s = lane; s < NS; s += 32) wg[s] *= inv;
+  }
+  consumer_sync();
+  if (staged) {
     for (int t = tid; t < G * HD; t += kConsumerThreads) {
       const int g = t / HD, e = t - g * HD;
-      float M = -CUDART_INF_F;
-      for (int s = 0; s < NS; ++s) M = fmaxf(M, xbuf[(s * G + g) * RW + HD]);
-      float num = 0.f, den = 0.f;
-      for (int s = 0; s < NS; ++s) {
-        const float* ps = xbuf + (s * G + g) * RW;
-        if (ps[HD] == -CUDART_INF_F) continue;
-        const float w = exp2f(ps[HD] - M);
-        num = fmaf(w, ps[e], num);
-        den = fmaf(w, ps[HD + 1], den);
+      const float* wg = scratch + g * NS;
+      const float* pe = xbuf + g * RW + e;
+      float r0 = 0.f, r1 = 0.f;
+      int s = 0;
+#pragma unroll 4
+      for (; s + 1 < NS; s += 2) {
+        r0 = fmaf(wg[s], pe[s * G * RW], r0);
+        r1 = fmaf(wg[s + 1], pe[(s + 1) * G * RW], r1);
       }
-      out[t] = num / den;
+      if (s < NS) r0 = fmaf(wg[s], pe[s * G * RW], r0);
+      out[t] = r0 + r1;
     }
     return;
   }
-  for (int t = tid; t < NS * G; t += kConsumerThreads) {
-    scratch[2 * t] = load_act<SYNC>(part + (size_t)t * RW + HD, S, c);
-    scratch[2 * t + 1] = load_act<SYNC>(part + (size_t)t * RW + HD + 1, S, c);
-  }
-  consumer_sync();
   constexpr int U = 8;  // splits whose partial outputs are in flight together
   for (int t = tid; t < G * HD; t += kConsumerThreads) {
     const int g = t / HD, e = t - g * HD;
-    float M = -CUDART_INF_F;
-    for (int s = 0; s < NS; ++s) M = fmaxf(M, scratch[2 * (s * G + g)]);
-    float num = 0.f, den = 0.f;
+    const float* wg = scratch + g * NS;
+    float acc = 0.f;
     for (int s0 = 0; s0 < NS; s0 += U) {
       float v[U];
 #pragma unroll
@@ -1494,17 +1550,14 @@ __device__ __noinline__ void op_attn_reduce(const DevState& S_arg, const StepArg
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int s = s0 + u;
-        const float ms = s < NS ? scratch[2 * (s * G + g)] : -CUDART_INF_F;
-        if (ms != -CUDART_INF_F) {
+        if (s < NS) {
           float ov = v[u];
           if (SYNC == SYNC_SENTINEL && isnan(ov)) ov = poll_slow(part + (size_t)(s * G + g) * RW + e, S, c);
-          const float w = exp2f(ms - M);
-          num = fmaf(w, ov, num);
-          den = fmaf(w, scratch[2 * (s * G + g) + 1], den);
+          acc = fmaf(wg[s], ov, acc);
         }
       }
     }
-    out[t] = num / den;
+    out[t] = acc;
   }
 }
 
