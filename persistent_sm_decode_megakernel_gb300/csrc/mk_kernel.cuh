@@ -500,39 +500,45 @@ __device__ __forceinline__ float4 load_v4(const float4* p, const DevState& S, Sm
 // Up to U 16-byte loads in flight (entries with p[u] == nullptr are skipped and read as
 // zeros); with sentinels, the vectors still holding one are re-read together until the
 // producers' values land (bounded, sets the abort flag on timeout).
+// One pause of a sentinel re-poll loop: backs off (exponentially, up to the configured
+// cap) and returns false once the wait has run past the timeout or another party
+// aborted (the abort flag is set and, if nothing was recorded yet, MK_ERR_TIMEOUT).
+__device__ __forceinline__ bool poll_pause(const DevState& S, SmemCtl* c, int k, uint64_t t0) {
+  const int ns = 20 << (k < 8 ? k : 8);
+  __nanosleep(ns < S.backoff_max_ns ? ns : S.backoff_max_ns);
+  if (c->abort || global_err(S) || globaltimer_ns() - t0 > (uint64_t)S.timeout_ns) {
+    if (!global_err(S)) set_err(S, 4u, -1, -1);
+    c->abort = 1;
+    return false;
+  }
+  return true;
+}
+
 template <int SYNC, int U>
 __device__ __forceinline__ void load_vecs(const DevState& S, SmemCtl* c, const float4* const (&p)[U], float4 (&v)[U]) {
+  if (SYNC == SYNC_COUNTER) {
 #pragma unroll
-  for (int u = 0; u < U; ++u) {
-    v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (p[u] != nullptr) v[u] = SYNC == SYNC_COUNTER ? __ldcg(p[u]) : ld_poll_v4(p[u]);
+    for (int u = 0; u < U; ++u) v[u] = p[u] != nullptr ? __ldcg(p[u]) : make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
   }
-  if (SYNC == SYNC_SENTINEL) {
+  // sentinels: every vector is read, then those still holding one are re-read together
+  // until none does; a pass issues all of its loads before testing any of them
+#pragma unroll
+  for (int u = 0; u < U; ++u) v[u] = p[u] != nullptr ? ld_poll_v4(p[u]) : make_float4(0.f, 0.f, 0.f, 0.f);
+  uint64_t t0 = 0;
+  for (int k = 0;; ++k) {
     bool pend = false;
 #pragma unroll
     for (int u = 0; u < U; ++u) pend |= any_nan4(v[u]);
-    if (pend) {
-      const uint64_t t0 = globaltimer_ns();
-      int k = 0;
-      while (pend) {
-        const int ns = 20 << (k < 8 ? k : 8);
-        __nanosleep(ns < S.backoff_max_ns ? ns : S.backoff_max_ns);
-        ++k;
-        pend = false;
+    if (!pend) break;
+    if (k == 0) t0 = globaltimer_ns();
+    if (!poll_pause(S, c, k, t0)) break;
+    bool need[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          if (any_nan4(v[u])) {
-            v[u] = ld_poll_v4(p[u]);
-            pend |= any_nan4(v[u]);
-          }
-        }
-        if (pend && (c->abort || global_err(S) || globaltimer_ns() - t0 > (uint64_t)S.timeout_ns)) {
-          if (!global_err(S)) set_err(S, 4u, -1, -1);
-          c->abort = 1;
-          break;
-        }
-      }
-    }
+    for (int u = 0; u < U; ++u) need[u] = any_nan4(v[u]);
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (need[u]) v[u] = ld_poll_v4(p[u]);
   }
 }
 
@@ -660,28 +666,47 @@ __device__ void stage_copy(const DevState& S, const float* src, int K, int B, fl
 // RMSNorm, folded: W (g . h / rms) = (W (g . h)) / rms.  The residual is staged scaled by
 // the gain while each thread accumulates its share of sum(h^2); the per-warp sums go to
 // c->red and the epilogue turns them into 1/rms (fixed order, same in every thread), so
-// no CTA-wide pass sits between staging and the weight pages.
+// no CTA-wide pass sits between staging and the weight pages.  The gains do not depend on
+// the producer: their loads are issued ahead of the polls of h and land while those wait.
 template <typename WT, int SYNC, int NB>
 __device__ void stage_rmsnorm(const DevState& S, const float* h, const uint16_t* gain, int B, float* xbuf,
                               SmemCtl* c) {
-  const int d = S.d, d4 = d / 4, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int U = 4;
+  const int d = S.d, d4 = d / 4, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, n4 = B * d4;
   float4* x4 = reinterpret_cast<float4*>(xbuf);
+  const float4* h4 = reinterpret_cast<const float4*>(h);
+  const uint2* g4 = reinterpret_cast<const uint2*>(gain);  // 4 gains per vector
   float ss[NB];
 #pragma unroll
   for (int b = 0; b < NB; ++b) ss[b] = 0.f;
-  stage_vec<SYNC>(S, reinterpret_cast<const float4*>(h), B * d4, c, [&](int i, float4 w) {
-    const int b = i / d4, k = i - b * d4;
-    const uint2 gb = __ldg(reinterpret_cast<const uint2*>(gain) + k);  // 4 gains
-    const float sq = w.x * w.x + w.y * w.y + w.z * w.z + w.w * w.w;
+  for (int base = 0; base < n4; base += U * kConsumerThreads) {
+    const float4* p[U];
+    uint2 gb[U];
 #pragma unroll
-    for (int bb = 0; bb < NB; ++bb)
-      if (bb == b) ss[bb] += sq;
-    w.x *= Unpack<WT>::one((uint16_t)(gb.x & 0xFFFFu));
-    w.y *= Unpack<WT>::one((uint16_t)(gb.x >> 16));
-    w.z *= Unpack<WT>::one((uint16_t)(gb.y & 0xFFFFu));
-    w.w *= Unpack<WT>::one((uint16_t)(gb.y >> 16));
-    x4[i] = w;
-  });
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * kConsumerThreads + tid;
+      p[u] = i < n4 ? h4 + i : nullptr;
+      gb[u] = i < n4 ? __ldg(g4 + (i % d4)) : make_uint2(0u, 0u);
+    }
+    float4 v[U];
+    load_vecs<SYNC, U>(S, c, p, v);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * kConsumerThreads + tid;
+      if (i >= n4) continue;
+      const int b = i / d4;
+      float4 w = v[u];
+      const float sq = w.x * w.x + w.y * w.y + w.z * w.z + w.w * w.w;
+#pragma unroll
+      for (int bb = 0; bb < NB; ++bb)
+        if (bb == b) ss[bb] += sq;
+      w.x *= Unpack<WT>::one((uint16_t)(gb[u].x & 0xFFFFu));
+      w.y *= Unpack<WT>::one((uint16_t)(gb[u].x >> 16));
+      w.z *= Unpack<WT>::one((uint16_t)(gb[u].y & 0xFFFFu));
+      w.w *= Unpack<WT>::one((uint16_t)(gb[u].y >> 16));
+      x4[i] = w;
+    }
+  }
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int i = B * d4 + tid; i < NB * d4; i += kConsumerThreads) x4[i] = z;
 #pragma unroll
@@ -913,27 +938,21 @@ __device__ __noinline__ void op_gemv(const DevState& S_arg, const StepArgs& A_ar
   const int B = A.B, l = in.layer;
   const Gemv g = make_gemv(S, in);
 
-  // 1. inputs
+  // 1. inputs (one inlined copy of each staging routine: the op only picks the source)
+  const float* src;
   switch (in.op) {
-    case OP_QKV:
-      stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_H, l), iptr(in, kP2), B, xbuf, c);
-      break;
-    case OP_UPGATE:
-      stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_HMID, l), iptr(in, kP2), B, xbuf, c);
-      break;
-    case OP_LMHEAD:
-      stage_rmsnorm<WT, SYNC, NB>(S, act_ptr(S, act, ACT_H, S.L), iptr(in, kP2), B, xbuf, c);
-      break;
-    case OP_OPROJ:
-      if (in.flags & F_MERGE_IN)
-        stage_merge<SYNC, NB>(S, A, l, xbuf, scratch, c, act, in.a[0] == 0);
-      else
-        stage_copy<SYNC, NB>(S, act_ptr(S, act, ACT_O, l), g.K, B, xbuf, c);
-      break;
-    default:  // OP_DOWN
-      stage_copy<SYNC, NB>(S, act_ptr(S, act, ACT_A, l), g.K, B, xbuf, c);
-      break;
+    case OP_QKV: src = act_ptr(S, act, ACT_H, l); break;
+    case OP_UPGATE: src = act_ptr(S, act, ACT_HMID, l); break;
+    case OP_LMHEAD: src = act_ptr(S, act, ACT_H, S.L); break;
+    case OP_OPROJ: src = act_ptr(S, act, ACT_O, l); break;
+    default: src = act_ptr(S, act, ACT_A, l); break;  // OP_DOWN
   }
+  if (in.op == OP_QKV || in.op == OP_UPGATE || in.op == OP_LMHEAD)
+    stage_rmsnorm<WT, SYNC, NB>(S, src, iptr(in, kP2), B, xbuf, c);
+  else if (in.flags & F_MERGE_IN)
+    stage_merge<SYNC, NB>(S, A, l, xbuf, scratch, c, act, in.a[0] == 0);
+  else
+    stage_copy<SYNC, NB>(S, src, g.K, B, xbuf, c);
   consumer_sync();
   if (tid == 0 && (A.flags & SF_TRACE)) c->tmark[0] = globaltimer_ns();
   // the residual this thread adds in the epilogue (its first row), loaded now so the
@@ -1104,10 +1123,13 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
       const int k4n = kws >> 2, n_items = MT * 8 * k4n;
       for (int base = 0; base < n_items; base += U * kConsumerThreads) {
         const float4* pp[U];
+        uint2 gbu[U];  // gains: issued ahead of the polls (they do not depend on the producer)
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int it = base + u * kConsumerThreads + tid, b = it / k4n, k4 = it - b * k4n;
-          pp[u] = (it < n_items && b < B) ? reinterpret_cast<const float4*>(src + (size_t)b * K + k0) + k4 : nullptr;
+          const bool live = it < n_items && b < B;
+          pp[u] = live ? reinterpret_cast<const float4*>(src + (size_t)b * K + k0) + k4 : nullptr;
+          gbu[u] = (live && gain != nullptr) ? __ldg(reinterpret_cast<const uint2*>(gain + k0) + k4) : make_uint2(0u, 0u);
         }
         float4 v[U];
         load_vecs<SYNC, U>(S, c, pp, v);
@@ -1118,7 +1140,7 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
           const int b = it / k4n, k4 = it - b * k4n, k = 4 * k4;
           float4 x = v[u];
           if (gain != nullptr && b < B) {
-            const uint2 gb = __ldg(reinterpret_cast<const uint2*>(gain + k0) + k4);
+            const uint2 gb = gbu[u];
             const float sq = x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
 #pragma unroll
             for (int bb = 0; bb < NB; ++bb)
@@ -1364,24 +1386,34 @@ __device__ __noinline__ void op_attn(const DevState& S_arg, const StepArgs& A_ar
     }
   };
 
-  for (int blk = 0; blk < at.nblocks; ++blk) {
-    const int np = min(at.pb, at.n_cached - blk * at.pb);
-    const uint8_t* kp = page_wait(S, c, pages, ring);
-    Ring rv = ring;
-    if (++rv.slot == S.n_pages) { rv.slot = 0; rv.ph ^= 1u; }
-    const uint8_t* vp = page_wait(S, c, pages, rv);
-    // the block's valid positions dealt over (warp, lane group); the bound is uniform
-    for (int base = 0; base < np; base += kConsumerWarps * NGRP) {
-      const int t = base + warp * NGRP + pgi;
-      const bool valid = t < np;
-      const size_t off = (size_t)(valid ? t : 0) * HD * 2;
-      update(valid, reinterpret_cast<const uint16_t*>(kp + off), reinterpret_cast<const uint16_t*>(vp + off));
+  // the cached positions a page block at a time; position pos_b (this step's key/value,
+  // staged above) is one more row of the last block's pass
+  const int nblk = at.nblocks > 0 ? at.nblocks : (at.has_new ? 1 : 0);
+  for (int blk = 0; blk < nblk; ++blk) {
+    const bool paged = blk < at.nblocks;
+    const int np = paged ? min(at.pb, at.n_cached - blk * at.pb) : 0;
+    const int nx = np + (blk == nblk - 1 && at.has_new ? 1 : 0);
+    const uint8_t* kp = nullptr;
+    const uint8_t* vp = nullptr;
+    if (paged) {
+      kp = page_wait(S, c, pages, ring);
+      Ring rv = ring;
+      if (++rv.slot == S.n_pages) { rv.slot = 0; rv.ph ^= 1u; }
+      vp = page_wait(S, c, pages, rv);
     }
-    page_release(S, c, ring);  // K page
-    page_release(S, c, ring);  // V page
+    // the block's rows dealt over (warp, lane group); the bound is uniform
+    for (int base = 0; base < nx; base += kConsumerWarps * NGRP) {
+      const int t = base + warp * NGRP + pgi;
+      const bool cached = t < np;
+      const size_t off = (size_t)(cached ? t : 0) * HD * 2;
+      update(t < nx, cached ? reinterpret_cast<const uint16_t*>(kp + off) : knew,
+             cached ? reinterpret_cast<const uint16_t*>(vp + off) : knew + HD);
+    }
+    if (paged) {
+      page_release(S, c, ring);  // K page
+      page_release(S, c, ring);  // V page
+    }
   }
-  if (at.has_new && warp == 0)  // position pos_b: the new key/value of this step
-    update(pgi == 0, knew, knew + HD);
   if (mark) c->tmark[1] = globaltimer_ns();
   // Combine the NGRP position groups of the warp (they share the running max m[g]) with a
   // butterfly reduce-scatter: each round halves the values a lane holds, so the warp
