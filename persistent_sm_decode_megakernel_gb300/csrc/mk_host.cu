@@ -261,9 +261,10 @@ mk_status run_graph(mk_ctx* ctx, Sched* sc, const DevState& S, const StepArgs& A
   return MK_OK;
 }
 
-// enqueue one decode step (one launch, or the multi-launch control's per-op launches)
+// enqueue one decode step (one launch, or the multi-launch control's per-op launches); with
+// persistent control, n_steps > 1 greedy steps in the one launch (tok_hist then [n_steps][B])
 mk_status enqueue_step(mk_ctx* ctx, Sched* sc, int B, const int32_t* tok, const int32_t* pos, bool tok_from_dev,
-                       float* logits, int32_t* tok_hist) {
+                       float* logits, int32_t* tok_hist, int n_steps = 1) {
   DevState S = ctx->st;
   S.counters = reinterpret_cast<uint32_t*>(sc->counters.p);
   S.n_counters = sc->plan.n_counters;
@@ -278,6 +279,9 @@ mk_status enqueue_step(mk_ctx* ctx, Sched* sc, int B, const int32_t* tok, const 
   }
   A.logits = logits;
   A.tok_hist = tok_hist;
+  A.n_steps = n_steps;
+  if (n_steps > 1 && ctx->opts.exec_mode != MK_EXEC_PERSISTENT)
+    return fail(MK_ERR_INVALID, "several steps in one launch need persistent control");
   const void* fn = ctx->opts.trace ? ctx->kernel_trace : ctx->kernel;
   if (ctx->opts.trace) MK_CUDA(cudaMemsetAsync(&reinterpret_cast<Ctl*>(ctx->ctl.p)->trace_n, 0, 4, ctx->stream));
   mk_status s;
@@ -301,8 +305,8 @@ mk_status enqueue_step(mk_ctx* ctx, Sched* sc, int B, const int32_t* tok, const 
     s = launch(ctx, fn, S, A, true);
     if (s) return s;
   }
-  sc->epoch++;
-  ctx->step++;
+  sc->epoch += (uint32_t)n_steps;
+  ctx->step += (uint32_t)n_steps;
   ctx->last_B = B;
   return MK_OK;
 }
@@ -595,6 +599,8 @@ mk_status mk_decode_steps(mk_ctx* ctx, const int32_t* in_tok, const int32_t* pos
   Sched* sc = nullptr;
   s = get_sched(ctx, B, &sc);
   if (s) return s;
+  if (ctx->opts.exec_mode == MK_EXEC_PERSISTENT)  // all the steps in one launch
+    return enqueue_step(ctx, sc, B, in_tok, pos0, !in_tok, nullptr, out_tok_dev, n_steps);
   int32_t pos[kMaxBatch];
   for (int k = 0; k < n_steps; ++k) {
     for (int b = 0; b < B; ++b) pos[b] = pos0[b] + k;

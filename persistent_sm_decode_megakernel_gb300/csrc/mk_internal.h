@@ -90,7 +90,8 @@ struct Ctl {
   int32_t tok[kMaxBatch];       // greedy token of the last completed step (device feed)
   uint32_t trace_n;
   uint32_t nan_seen;
-  uint32_t pad[2];
+  uint32_t tok_seq;             // step number + 1 of the last step whose tokens are in tok
+  uint32_t pad;
 };
 
 struct TraceRec {
@@ -169,6 +170,7 @@ struct StepArgs {
   int32_t pos[kMaxBatch];
   float* logits;               // [B][V] or null
   int32_t* tok_hist;           // device [B] copy of this step's tokens, or null
+  int n_steps;                 // greedy steps this launch runs back to back (0 or 1: one)
   // non-null: the per-step fields (epoch .. tok_hist; flags OR-ed) are read from this device
   // copy at kernel start -- the launches of a CUDA graph keep fixed parameters
   const StepArgs* dyn;

@@ -32,6 +32,7 @@ struct SmemCtl {
   uint64_t tmark[6];  // journal marks inside an op
   volatile int abort;
   StepArgs args;  // the step's arguments (from the launch, or from device memory for graphs)
+  StepArgs largs; // the loader's copy: it runs ahead into the next step of a multi-step launch
   DevState S;     // the context's state, copied from the launch parameters
   Instr cur[kConsumerWarps];  // each compute warp's copy of its current instruction
 };
@@ -83,6 +84,35 @@ __device__ __noinline__ bool wait_counter(const DevState& S_arg, int ctr, uint32
     if (global_err(S)) return false;
     if (globaltimer_ns() - t0 > (uint64_t)S.timeout_ns) {
       set_err(S, 4u /*MK_ERR_TIMEOUT*/, pc, ctr);
+      return false;
+    }
+  }
+}
+
+// The other parity's activations back to NaN sentinels, this CTA's share of the grid
+// (threads t < nthr of every CTA take part).
+__device__ __forceinline__ void nan_fill(float* base, int64_t n_floats, int t, int nthr) {
+  const int64_t n4 = n_floats / 4;
+  float4* o4 = reinterpret_cast<float4*>(base);
+  const float4 nan4 = make_float4(CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F);
+  for (int64_t i = (int64_t)blockIdx.x * nthr + t; i < n4; i += (int64_t)gridDim.x * nthr) o4[i] = nan4;
+}
+
+// Multi-step launches: wait (acquire) until the token sequence word reaches `target`, i.e.
+// the step before has published its tokens -- every CTA has finished that step.
+__device__ __noinline__ bool wait_seq(const uint32_t* p, uint32_t target, int pc) {
+  const DevState& S = smem_ctl()->S;
+  if ((int32_t)(ld_acquire_u32(p) - target) >= 0) return true;
+  const uint64_t t0 = globaltimer_ns();
+  int k = 0;
+  while (true) {
+    int ns = 20 << (k < 8 ? k : 8);
+    __nanosleep(ns < S.backoff_max_ns ? ns : S.backoff_max_ns);
+    ++k;
+    if ((int32_t)(ld_acquire_u32(p) - target) >= 0) return true;
+    if (global_err(S) || smem_ctl()->abort) return false;
+    if (globaltimer_ns() - t0 > (uint64_t)S.timeout_ns) {
+      set_err(S, 4u /*MK_ERR_TIMEOUT*/, pc, -1);
       return false;
     }
   }
@@ -267,7 +297,7 @@ __device__ __noinline__ bool producer_acquire(const DevState& S_arg, SmemCtl* c,
 
 __device__ __noinline__ void producer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* c, uint8_t* pages) {
   const DevState& S = smem_ctl()->S;
-  const StepArgs& A = smem_ctl()->args;
+  StepArgs& A = smem_ctl()->largs;
   c = smem_ctl();
   pages = smem_pages();
   const uint64_t pol = l2_evict_first_policy();
@@ -276,7 +306,18 @@ __device__ __noinline__ void producer(const DevState& S_arg, const StepArgs& A_a
   long long issued = 0;
   const int cta = blockIdx.x;
   const int end = A.q_start[cta + 1];
+  const int n_steps = A.n_steps > 1 ? A.n_steps : 1;
   bool ok = true;
+  // A multi-step launch walks the queue once per step.  The weights of a step do not depend
+  // on the one before, so they stream ahead across the boundary; the KV blocks do (the
+  // previous step appended its key/value rows): before the first of them the loader waits
+  // for the previous step's tokens, which every CTA's whole step precedes.
+  for (int st = 0; st < n_steps && ok; ++st) {
+  bool kv_ready = st == 0;
+  if (st > 0) {
+    A.step += 1u;
+    for (int b = 0; b < A.B; ++b) A.pos[b] += 1;
+  }
   for (int pc = A.q_start[cta]; pc < end && ok; ++pc) {
     const Instr in = load_instr(A.instr + pc);
     if (pc + 2 < end) prefetch_l1(A.instr + pc + 2);  // the next instructions, for both roles
@@ -354,6 +395,15 @@ __device__ __noinline__ void producer(const DevState& S_arg, const StepArgs& A_a
         break;
       }
       case OP_ATTN: {
+        if (!kv_ready) {
+          if (!wait_seq(&S.ctl->tok_seq, A.step, -10)) {
+            c->abort = 1;
+            ok = false;
+            break;
+          }
+          asm volatile("fence.proxy.async.global;" ::: "memory");  // generic-proxy writes before bulk reads
+          kv_ready = true;
+        }
         const Attn at = make_attn(S, A, in);
         for (int blk = 0; blk < at.nblocks && ok; ++blk) {
           const int p0 = blk * at.pb;
@@ -393,6 +443,7 @@ __device__ __noinline__ void producer(const DevState& S_arg, const StepArgs& A_a
         break;
     }
   }
+  }  // steps
   // Drain: every issued copy must land before the CTA exits, and -- unless the step was
   // abandoned -- every page must have been handed back (no leak, §8.9).
   const uint64_t t0 = globaltimer_ns();
@@ -1653,13 +1704,36 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
   const int tid = threadIdx.x, cta = blockIdx.x;
   const bool nosync = (A.flags & SF_NO_SYNC) != 0;
   const bool TRACE = (A.flags & SF_TRACE) != 0;
-  const int par = (SYNC == SYNC_SENTINEL && !nosync) ? (int)(A.step & 1u) : 0;
-  float* act = S.act + (int64_t)par * S.act_floats;
-  const int nb = A.B <= 1 ? 1 : A.B <= 2 ? 2 : A.B <= 4 ? 4 : A.B <= 8 ? 8 : 16;
-  const int G = S.Hq / S.Hkv;
   Ring ring{0, 0u};
   int order_n = 0;
   const int end = A.q_start[cta + 1];
+  // A multi-step launch runs the queue once per step.  Step st > 0 starts when the step
+  // before has published its tokens (its last CTA's last instruction is done): then the
+  // arguments advance one position, the token comes from the device, and the buffers that
+  // step used are prepared for the step after this one.
+  for (int st = 0; st < (A.n_steps > 1 ? A.n_steps : 1); ++st) {
+  if (st > 0) {
+    bool bad = false;
+    if (tid == 0 && !wait_seq(&S.ctl->tok_seq, A.step + 1u, -9)) {
+      c->abort = 1;
+      bad = true;
+    }
+    if (consumer_sync_or(bad || c->abort)) break;
+    if (tid == 0) {
+      StepArgs& M = smem_ctl()->args;
+      M.step += 1u;
+      M.epoch += 1u;
+      for (int b = 0; b < M.B; ++b) M.pos[b] += 1;
+      M.flags |= SF_TOK_FROM_DEVICE;
+      if (M.tok_hist) M.tok_hist += M.B;
+    }
+    if (tid < kMaxBatch) c->best[tid] = 0ull;
+    consumer_sync();
+    if ((A.flags & SF_RESET_ARGMAX) && cta == 0 && tid < kMaxBatch)
+      S.argkeys[((A.step + 1u) & 1u) * kMaxBatch + tid] = 0ull;
+    if (SYNC == SYNC_SENTINEL && !nosync)
+      nan_fill(S.act + (int64_t)((A.step + 1u) & 1u) * S.act_floats, S.act_floats, tid, kConsumerThreads);
+  }
   for (int pc = A.q_start[cta]; pc < end; ++pc) {
     const Instr in = load_instr(A.instr + pc);
     if (in.op == OP_END) break;
@@ -1681,7 +1755,10 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
       if (consumer_sync_or(bad || c->abort)) break;
     }
     if (TRACE) t_ready = globaltimer_ns();
-    // ---- execute
+    // ---- execute (this step's parity of the activation arena; the batch padded for the GEMV)
+    float* act = S.act + ((SYNC == SYNC_SENTINEL && !nosync) ? (int64_t)(A.step & 1u) * S.act_floats : 0);
+    const int nb = A.B <= 1 ? 1 : A.B <= 2 ? 2 : A.B <= 4 ? 4 : A.B <= 8 ? 8 : 16;
+    const int G = S.Hq / S.Hkv;
     switch (in.op) {
       case OP_EMBED:
         op_embed<WT>(S, A, in, act);
@@ -1779,6 +1856,7 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
             S.ctl->tok[b] = tok;
             if (A.tok_hist) A.tok_hist[b] = tok;
           }
+          st_release_u32(&S.ctl->tok_seq, A.step + 1u);  // after the tokens: a multi-step launch waits on it
         }
       }
     } else if (tid == 0 && use_ctr && signal && in.signal_ctr >= 0) {
@@ -1801,6 +1879,8 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
       }
     }
   }
+  if (consumer_sync_or(c->abort)) break;
+  }  // steps
 }
 
 }  // namespace
@@ -1827,6 +1907,8 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
       c->args.flags |= A.flags;
       c->args.dyn = nullptr;
     }
+    __syncthreads();
+    if (tid == 0) c->largs = c->args;
   }
   uint8_t* pages = smem_pages();
   float* xbuf = smem_xbuf(S);
@@ -1847,13 +1929,8 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
   // other parity's activations) are reset for the next step; nothing reads them now
   if ((AA.flags & SF_RESET_ARGMAX) && blockIdx.x == 0 && tid < kMaxBatch)
     S.argkeys[((AA.step + 1u) & 1u) * kMaxBatch + tid] = 0ull;
-  if (SYNC == SYNC_SENTINEL && !(AA.flags & SF_NO_SYNC)) {
-    float* other = S.act + (int64_t)((AA.step + 1u) & 1u) * S.act_floats;
-    const int64_t n4 = S.act_floats / 4;
-    float4* o4 = reinterpret_cast<float4*>(other);
-    const float4 nan4 = make_float4(CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F);
-    for (int64_t i = (int64_t)blockIdx.x * kThreads + tid; i < n4; i += (int64_t)gridDim.x * kThreads) o4[i] = nan4;
-  }
+  if (SYNC == SYNC_SENTINEL && !(AA.flags & SF_NO_SYNC))
+    nan_fill(S.act + (int64_t)((AA.step + 1u) & 1u) * S.act_floats, S.act_floats, tid, kThreads);
   __syncthreads();
   if (tid >= kConsumerThreads) {  // the loader streams weights without waiting for the previous grid
     const int w = tid >> 5;

@@ -160,6 +160,38 @@ def test_chained_decode_matches_stepwise(lib, tiny):
     np.testing.assert_array_equal(got, toks[0, P + 1: P + 1 + n])
 
 
+@pytest.mark.parametrize("sync", [0, 1], ids=["counter", "sentinel"])
+@pytest.mark.parametrize("B", [1, 2, 4])
+def test_multi_step_launch_matches_single_step_launches(lib, tiny, sync, B):
+    """n greedy steps in ONE persistent launch (the kernel walks its queue once per step,
+    each step waiting for the tokens the step before published) give the same tokens and
+    the same last-step activations, bit for bit, as n launches of one step each."""
+    cfg, w, m = tiny
+    P, n = 6, 9
+    prompt = synth.gen_prompts(cfg, B, P)
+    runs = []
+    for one_launch in (True, False):
+        dm = lib.DeviceModel(cfg, w, max_batch=B, max_ctx=P + n + 1)
+        dec = lib.Decoder(dm, sync_mode=sync)
+        first = dec.prefill(prompt)
+        out = torch.zeros((n, B), dtype=torch.int32, device=dm.device)
+        if one_launch:
+            dec.decode_steps(first, [P] * B, n, out)
+        else:
+            for k in range(n):
+                dec.decode_steps(first if k == 0 else None, [P + k] * B, 1, out[k:k + 1])
+        dec.synchronize()
+        h = dec.read_activation(0, cfg.n_layers)   # the final residual stream of the last step
+        runs.append((first, out.cpu().numpy().copy(), h))
+        dec.close()
+    assert list(runs[0][0]) == list(runs[1][0])
+    np.testing.assert_array_equal(runs[0][1], runs[1][1])
+    np.testing.assert_array_equal(runs[0][2], runs[1][2])
+    # and the chain is the oracle's greedy chain for sequence 0
+    toks, _ = oracle_run(cfg, w, prompt[:1], n + 1, model=m)
+    np.testing.assert_array_equal(runs[0][1][:, 0], toks[0, P + 1: P + 1 + n])
+
+
 def test_fault_injection_times_out_and_recovers(lib, tiny):
     """A dropped counter signal (injected on the host, validator skipped) makes a device
     wait run out: the step returns MK_ERR_TIMEOUT within the limit, the context refuses
