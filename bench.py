@@ -1,5 +1,6 @@
 """Benchmark: batch-1 greedy decode of the 2B fp16 workload through the persistent
-megakernel, one launch per decode step.
+megakernel (by default all timed steps in one launch of mk_decode_steps; with
+--steps-per-launch 1, one launch per decode step).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -10,12 +11,13 @@ embedding (3.545 GB) plus the KV cache -- far above the 129 MB L2, so no flush i
 between steps.  Prints one JSON line (rank 0).
 
 value: tok/s with everything resident in HBM: K chained steps (each step embeds the
-token the previous step chose on the device), CUDA events on the context's stream.
+token the previous step chose on the device), CUDA events on the context's stream
+around every launch.
 e2e: the same metric through mk_decode_step with host token buffers (token and position
 travel as kernel parameters; the step's token and status come back in one 96-byte
 device-to-host copy), host loop included.
-roofline: algorithmic bytes per launch / mean launch duration against the measured HBM
-copy bandwidth.  cpu_baseline / --impl reference: the fp64 oracle on the host cores.
+roofline: algorithmic bytes per step / (mean launch duration / steps per launch) against
+the measured HBM copy bandwidth; traffic: the profiled DRAM bytes of one step.  cpu_baseline / --impl reference: the fp64 oracle on the host cores.
 Multi-GPU (torchrun, N > 1): independent replicas, one per GPU; max time over ranks.
 """
 import argparse
@@ -50,14 +52,15 @@ def kernel_source_hash(sync="sentinel"):
 
 
 def profiled_traffic(sync="sentinel"):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current kernel sources (else None)."""
+    """DRAM bytes of one decode step from the committed ncu summary (single-step launches),
+    if it was taken on the current kernel sources (else None)."""
     try:
         with open(PROFILE_SUMMARY) as f:
             kv = dict(l.split(":", 1) for l in f.read().splitlines() if ":" in l)
         if kv.get("kernel_source_sha", "").strip() != kernel_source_hash(sync):
             return None
-        return float(kv["dram_bytes_per_launch"].strip())
+        key = "dram_bytes_per_step" if "dram_bytes_per_step" in kv else "dram_bytes_per_launch"
+        return float(kv[key].strip())
     except (OSError, KeyError, ValueError):
         return None
 
@@ -240,6 +243,8 @@ def main():
     ap.add_argument("--sync", default="sentinel", choices=["counter", "sentinel"])
     ap.add_argument("--exec", default="persistent", choices=["persistent", "multilaunch", "graph"])
     ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--steps-per-launch", type=int, default=0,
+                    help="decode steps per launch (0: all K in one; persistent control only)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -274,25 +279,29 @@ def main():
         pos += W
         dec.synchronize()
 
-        # ---- timed region: K chained steps, one launch each, events around every launch
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+        # ---- timed region: K chained steps in launches of C steps, events around every launch
+        C = K if args.steps_per_launch <= 0 else min(args.steps_per_launch, K)
+        if args.exec != "persistent":
+            C = 1
+        chunks = [min(C, K - k0) for k0 in range(0, K, C)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(chunks) + 1)]
         positions = []
         barrier(world, device)
         torch.cuda.synchronize(device)
         with ClockSampler(local) as clocks:
             ev[0].record(stream)
-            for k in range(K):
-                dec.decode_steps(None, [pos] * B, 1)
-                positions.append(pos)
-                pos += 1
-                ev[k + 1].record(stream)
+            for i, n in enumerate(chunks):
+                dec.decode_steps(None, [pos] * B, n)
+                positions += list(range(pos, pos + n))
+                pos += n
+                ev[i + 1].record(stream)
             dec.synchronize()
             torch.cuda.synchronize(device)
         barrier(world, device)
-        per_launch_ms = [ev[k].elapsed_time(ev[k + 1]) for k in range(K)]
-        total_s = ev[0].elapsed_time(ev[K]) / 1000.0
+        per_step_ms = [ev[i].elapsed_time(ev[i + 1]) / n for i, n in enumerate(chunks)]
+        total_s = ev[0].elapsed_time(ev[len(chunks)]) / 1000.0
         value, total_s = job_rate(B * K, total_s, world, device)
-        mean_launch_s = statistics.mean(per_launch_ms) / 1000.0
+        mean_step_s = statistics.mean(per_step_ms) / 1000.0
 
         # ---- e2e: host buffers through mk_decode_step, host loop timed
         K2 = min(args.e2e_steps, K)
@@ -310,7 +319,7 @@ def main():
         return 0
     peak, peak_kind = measured_peaks()
     bytes_per_step = statistics.mean(algorithmic_bytes(cfg, [p] * B) for p in positions)
-    achieved_gbs = bytes_per_step / mean_launch_s / 1e9
+    achieved_gbs = bytes_per_step / mean_step_s / 1e9
     t_min = bytes_per_step / (peak * 1e9)
     cpu = None
     if not args.no_cpu_baseline and world >= 1:
@@ -329,11 +338,12 @@ def main():
                    "batch": B, "prompt_len": PROMPT, "context": [positions[0], positions[-1]],
                    "l2": "inputs larger than L2: 3.6 GB streamed per step vs 129 MB L2, no flush",
                    "sync": args.sync, "exec": args.exec, "parallelism": f"replicas x{world}"},
-        "gpu_launches": K * info["launches_per_step"],
+        "gpu_launches": len(chunks) * info["launches_per_step"],
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
                      "frac": achieved_gbs / peak, "traffic": traffic,
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs, copy)",
-                     "bytes_per_launch": bytes_per_step, "mean_launch_us": mean_launch_s * 1e6,
+                     "per": "decode step (a launch runs steps_per_launch of them)",
+                     "steps_per_launch": C, "bytes_per_step": bytes_per_step, "mean_step_us": mean_step_s * 1e6,
                      "frac_of_nominal_7900": achieved_gbs / NOMINAL_HBM_GBS},
         "overhead_fraction": (total_s / K - t_min) / (total_s / K),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 8 * B, "d2h_bytes_per_step": 96,

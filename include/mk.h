@@ -161,11 +161,17 @@ mk_status mk_prefill(mk_ctx *ctx, const int32_t *tokens, int B, int P,
 mk_status mk_decode_step(mk_ctx *ctx, const int32_t *in_tok, const int32_t *pos, int B,
                          int32_t *out_tok, float *logits);
 
-/* n_steps greedy decode steps enqueued back to back without host round trips: step s
- * embeds the token chosen by step s-1 on the device.  in_tok host [B] at positions
- * pos0 host [B], or in_tok NULL to continue from the token the previous step chose on
- * the device; out_tok device [n_steps, B] int32 (or NULL) receives every step's token.
- * Asynchronous: returns after enqueueing; call mk_synchronize for the status. */
+/* n_steps greedy decode steps without host round trips: step s embeds the token chosen
+ * by step s-1 on the device.  With persistent control (MK_EXEC_PERSISTENT) all n_steps
+ * run in ONE launch: the kernel walks its queues once per step, each step starting when
+ * the step before has published its tokens (every CTA waits on that word; the loader
+ * streams the next step's weights meanwhile and waits only before KV-cache blocks).  The
+ * other controls enqueue one step (or one graph) after another.  in_tok host [B] at
+ * positions pos0 host [B], or in_tok NULL to continue from the token the previous step
+ * chose on the device; out_tok device [n_steps, B] int32 (or NULL) receives every step's
+ * token.  Requires pos0[b] + n_steps <= max_ctx.  Asynchronous: returns after enqueueing;
+ * call mk_synchronize for the status (a device wait that runs out ends the launch with
+ * MK_ERR_TIMEOUT, as for one step). */
 mk_status mk_decode_steps(mk_ctx *ctx, const int32_t *in_tok, const int32_t *pos0, int B,
                           int n_steps, int32_t *out_tok_dev);
 
