@@ -1,6 +1,6 @@
 """Benchmark: batch-1 greedy decode of the 2B fp16 workload through the persistent
-megakernel (by default all timed steps in one launch of mk_decode_steps; with
---steps-per-launch 1, one launch per decode step).
+megakernel, one launch per decode step (--steps-per-launch C: C chained steps per launch
+of mk_decode_steps, 0 = all K in one launch; measured the same within noise).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -45,7 +45,7 @@ KERNEL_SOURCES = ["mk_kernel.cuh", "mk_device.cuh", "mk_internal.h"]
 def kernel_source_hash(sync="sentinel"):
     """Hash of the sources the timed kernel instance is compiled from."""
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES + [f"mk_k_f16_{sync}.cu"]:
+    for f in KERNEL_SOURCES + [f"mk_k_f16_{sync}.cu", f"mk_k_f16_{sync}_ms.cu"]:
         with open(os.path.join(ROOT, "persistent_sm_decode_megakernel_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -243,7 +243,7 @@ def main():
     ap.add_argument("--sync", default="sentinel", choices=["counter", "sentinel"])
     ap.add_argument("--exec", default="persistent", choices=["persistent", "multilaunch", "graph"])
     ap.add_argument("--batch", type=int, default=1)
-    ap.add_argument("--steps-per-launch", type=int, default=0,
+    ap.add_argument("--steps-per-launch", type=int, default=1,
                     help="decode steps per launch (0: all K in one; persistent control only)")
     args = ap.parse_args()
     if args.impl == "reference":

@@ -74,8 +74,8 @@ struct mk_ctx {
   cudaStream_t stream = nullptr;
   int device = 0;
   int n_sm = 0, bpsm = 0, n_cta = 0;
-  const void* kernel = nullptr;
-  const void* kernel_trace = nullptr;
+  const void* kernel = nullptr;     // one step per launch
+  const void* kernel_ms = nullptr;  // several steps per launch (mk_decode_steps)
   DevState st{};  // template, counters patched per schedule
   ModelPtrs ptrs;  // device addresses written into every instruction
   DevBuf ptr_tables, rope, act, argkeys, ctl, trace;
@@ -282,7 +282,7 @@ mk_status enqueue_step(mk_ctx* ctx, Sched* sc, int B, const int32_t* tok, const 
   A.n_steps = n_steps;
   if (n_steps > 1 && ctx->opts.exec_mode != MK_EXEC_PERSISTENT)
     return fail(MK_ERR_INVALID, "several steps in one launch need persistent control");
-  const void* fn = ctx->opts.trace ? ctx->kernel_trace : ctx->kernel;
+  const void* fn = n_steps > 1 ? ctx->kernel_ms : ctx->kernel;
   if (ctx->opts.trace) MK_CUDA(cudaMemsetAsync(&reinterpret_cast<Ctl*>(ctx->ctl.p)->trace_n, 0, 4, ctx->stream));
   mk_status s;
   if (ctx->opts.exec_mode == MK_EXEC_GRAPH) {
@@ -429,8 +429,8 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
   if (!e.empty()) return fail(MK_ERR_INVALID, e);
   // one wave (§8.3): opt in to the shared memory, ask how many CTAs fit, launch exactly that
   ctx->kernel = step_kernel_entry(m.dtype, o.sync_mode, false);
-  ctx->kernel_trace = step_kernel_entry(m.dtype, o.sync_mode, true);
-  for (const void* fn : {ctx->kernel, ctx->kernel_trace})
+  ctx->kernel_ms = step_kernel_entry(m.dtype, o.sync_mode, true);
+  for (const void* fn : {ctx->kernel, ctx->kernel_ms})
     MK_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ctx->geo.smem_bytes));
   MK_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ctx->bpsm, ctx->kernel, kThreads, ctx->geo.smem_bytes));
   if (ctx->bpsm < 1) return fail(MK_ERR_OCCUPANCY, "the kernel does not fit on an SM (blocks per SM < 1)");

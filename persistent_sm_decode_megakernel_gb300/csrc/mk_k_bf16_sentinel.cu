@@ -1,9 +1,9 @@
-// Step-kernel instantiation: bf16 weights/KV, sentinel synchronisation.
+// Step-kernel instantiation: bf16 weights/KV, sentinel synchronisation, one step per launch.
 #include "mk_kernel.cuh"
 
 namespace mk {
-template __global__ void mk_step_kernel<__nv_bfloat16, 1>(const __grid_constant__ DevState, const __grid_constant__ StepArgs);
+template __global__ void mk_step_kernel<__nv_bfloat16, 1, false>(const __grid_constant__ DevState, const __grid_constant__ StepArgs);
 const void* step_kernel_entry_bf16_sentinel() {
-  return reinterpret_cast<const void*>(&mk_step_kernel<__nv_bfloat16, 1>);
+  return reinterpret_cast<const void*>(&mk_step_kernel<__nv_bfloat16, 1, false>);
 }
 }  // namespace mk

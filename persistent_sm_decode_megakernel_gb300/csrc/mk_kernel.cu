@@ -182,8 +182,16 @@ const void* step_kernel_entry_f16_counter();
 const void* step_kernel_entry_f16_sentinel();
 const void* step_kernel_entry_bf16_counter();
 const void* step_kernel_entry_bf16_sentinel();
+const void* step_kernel_entry_f16_counter_ms();
+const void* step_kernel_entry_f16_sentinel_ms();
+const void* step_kernel_entry_bf16_counter_ms();
+const void* step_kernel_entry_bf16_sentinel_ms();
 
-const void* step_kernel_entry(int dtype, int sync_mode, bool /*trace: a runtime flag*/) {
+const void* step_kernel_entry(int dtype, int sync_mode, bool multi_step) {
+  if (multi_step) {
+    if (dtype == 0) return sync_mode == 0 ? step_kernel_entry_f16_counter_ms() : step_kernel_entry_f16_sentinel_ms();
+    return sync_mode == 0 ? step_kernel_entry_bf16_counter_ms() : step_kernel_entry_bf16_sentinel_ms();
+  }
   if (dtype == 0) return sync_mode == 0 ? step_kernel_entry_f16_counter() : step_kernel_entry_f16_sentinel();
   return sync_mode == 0 ? step_kernel_entry_bf16_counter() : step_kernel_entry_bf16_sentinel();
 }

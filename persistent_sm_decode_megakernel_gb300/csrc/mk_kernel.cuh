@@ -33,6 +33,9 @@ struct SmemCtl {
   volatile int abort;
   StepArgs args;  // the step's arguments (from the launch, or from device memory for graphs)
   StepArgs largs; // the loader's copy: it runs ahead into the next step of a multi-step launch
+  float* step_act;  // multi-step launches: the current step's activation arena, batch tile and
+  int step_nb;      // GQA group (kept here rather than in registers across the op calls)
+  int step_G;
   DevState S;     // the context's state, copied from the launch parameters
   Instr cur[kConsumerWarps];  // each compute warp's copy of its current instruction
 };
@@ -295,9 +298,10 @@ __device__ __noinline__ bool producer_acquire(const DevState& S_arg, SmemCtl* c,
   return true;
 }
 
+template <bool MS>
 __device__ __noinline__ void producer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* c, uint8_t* pages) {
   const DevState& S = smem_ctl()->S;
-  StepArgs& A = smem_ctl()->largs;
+  StepArgs& A = MS ? smem_ctl()->largs : smem_ctl()->args;
   c = smem_ctl();
   pages = smem_pages();
   const uint64_t pol = l2_evict_first_policy();
@@ -306,7 +310,7 @@ __device__ __noinline__ void producer(const DevState& S_arg, const StepArgs& A_a
   long long issued = 0;
   const int cta = blockIdx.x;
   const int end = A.q_start[cta + 1];
-  const int n_steps = A.n_steps > 1 ? A.n_steps : 1;
+  const int n_steps = (MS && A.n_steps > 1) ? A.n_steps : 1;
   bool ok = true;
   // A multi-step launch walks the queue once per step.  The weights of a step do not depend
   // on the one before, so they stream ahead across the boundary; the KV blocks do (the
@@ -314,7 +318,7 @@ __device__ __noinline__ void producer(const DevState& S_arg, const StepArgs& A_a
   // for the previous step's tokens, which every CTA's whole step precedes.
   for (int st = 0; st < n_steps && ok; ++st) {
   bool kv_ready = st == 0;
-  if (st > 0) {
+  if (MS && st > 0) {
     A.step += 1u;
     for (int b = 0; b < A.B; ++b) A.pos[b] += 1;
   }
@@ -395,7 +399,7 @@ __device__ __noinline__ void producer(const DevState& S_arg, const StepArgs& A_a
         break;
       }
       case OP_ATTN: {
-        if (!kv_ready) {
+        if (MS && !kv_ready) {
           if (!wait_seq(&S.ctl->tok_seq, A.step, -10)) {
             c->abort = 1;
             ok = false;
@@ -1692,7 +1696,7 @@ __device__ void op_test_pages(const DevState& S_arg, const Instr& in_arg, SmemCt
 }
 
 // ---------------------------------------------------------------- compute warps: loop
-template <typename WT, int SYNC>
+template <typename WT, int SYNC, bool MS>
 __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* c, uint8_t* pages, float* xbuf,
                          float* scratch) {
   const DevState& S = smem_ctl()->S;
@@ -1705,14 +1709,14 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
   const bool nosync = (A.flags & SF_NO_SYNC) != 0;
   const bool TRACE = (A.flags & SF_TRACE) != 0;
   Ring ring{0, 0u};
-  int order_n = 0;
   const int end = A.q_start[cta + 1];
   // A multi-step launch runs the queue once per step.  Step st > 0 starts when the step
   // before has published its tokens (its last CTA's last instruction is done): then the
   // arguments advance one position, the token comes from the device, and the buffers that
   // step used are prepared for the step after this one.
-  for (int st = 0; st < (A.n_steps > 1 ? A.n_steps : 1); ++st) {
-  if (st > 0) {
+  const int n_steps = (MS && A.n_steps > 1) ? A.n_steps : 1;
+  for (int st = 0; st < n_steps; ++st) {
+  if (MS && st > 0) {
     bool bad = false;
     if (tid == 0 && !wait_seq(&S.ctl->tok_seq, A.step + 1u, -9)) {
       c->abort = 1;
@@ -1733,6 +1737,20 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
       S.argkeys[((A.step + 1u) & 1u) * kMaxBatch + tid] = 0ull;
     if (SYNC == SYNC_SENTINEL && !nosync)
       nan_fill(S.act + (int64_t)((A.step + 1u) & 1u) * S.act_floats, S.act_floats, tid, kConsumerThreads);
+  }
+  // the step's parity of the activation arena, the batch padded for the GEMV, the GQA
+  // group: fixed for a one-step launch; re-read per instruction when steps advance
+  const int par0 = (SYNC == SYNC_SENTINEL && !nosync) ? (int)(A.step & 1u) : 0;
+  float* act0 = S.act + (int64_t)par0 * S.act_floats;
+  const int nb0 = A.B <= 1 ? 1 : A.B <= 2 ? 2 : A.B <= 4 ? 4 : A.B <= 8 ? 8 : 16;
+  const int G0 = S.Hq / S.Hkv;
+  if (MS) {
+    if (tid == 0) {
+      c->step_act = act0;
+      c->step_nb = nb0;
+      c->step_G = G0;
+    }
+    consumer_sync();
   }
   for (int pc = A.q_start[cta]; pc < end; ++pc) {
     const Instr in = load_instr(A.instr + pc);
@@ -1755,10 +1773,10 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
       if (consumer_sync_or(bad || c->abort)) break;
     }
     if (TRACE) t_ready = globaltimer_ns();
-    // ---- execute (this step's parity of the activation arena; the batch padded for the GEMV)
-    float* act = S.act + ((SYNC == SYNC_SENTINEL && !nosync) ? (int64_t)(A.step & 1u) * S.act_floats : 0);
-    const int nb = A.B <= 1 ? 1 : A.B <= 2 ? 2 : A.B <= 4 ? 4 : A.B <= 8 ? 8 : 16;
-    const int G = S.Hq / S.Hkv;
+    // ---- execute
+    float* act = MS ? c->step_act : act0;
+    const int nb = MS ? c->step_nb : nb0;
+    const int G = MS ? c->step_G : G0;
     switch (in.op) {
       case OP_EMBED:
         op_embed<WT>(S, A, in, act);
@@ -1802,9 +1820,9 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
       case OP_T_PRODUCE:
         if (tid == 0) {
           if (in.op == OP_T_ORDER) {
-            S.test_buf[(int64_t)cta * 64 + 1 + order_n] = in.a[1];
-            ++order_n;
-            S.test_buf[(int64_t)cta * 64] = order_n;
+            const int64_t n = S.test_buf[(int64_t)cta * 64];  // this CTA's own count (zeroed by the host)
+            S.test_buf[(int64_t)cta * 64 + 1 + n] = in.a[1];
+            S.test_buf[(int64_t)cta * 64] = n + 1;
           } else {
             S.test_buf[in.a[0]] = in.a[1];
           }
@@ -1856,7 +1874,7 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
             S.ctl->tok[b] = tok;
             if (A.tok_hist) A.tok_hist[b] = tok;
           }
-          st_release_u32(&S.ctl->tok_seq, A.step + 1u);  // after the tokens: a multi-step launch waits on it
+          if (MS) st_release_u32(&S.ctl->tok_seq, A.step + 1u);  // after the tokens: the next step waits on it
         }
       }
     } else if (tid == 0 && use_ctr && signal && in.signal_ctr >= 0) {
@@ -1879,14 +1897,14 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
       }
     }
   }
-  if (consumer_sync_or(c->abort)) break;
+  if (MS && consumer_sync_or(c->abort)) break;
   }  // steps
 }
 
 }  // namespace
 
 // ---------------------------------------------------------------- the kernel
-template <typename WT, int SYNC>
+template <typename WT, int SYNC, bool MS>
 __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_constant__ DevState S,
                                                               const __grid_constant__ StepArgs A) {
   SmemCtl* c = smem_ctl();
@@ -1907,8 +1925,10 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
       c->args.flags |= A.flags;
       c->args.dyn = nullptr;
     }
-    __syncthreads();
-    if (tid == 0) c->largs = c->args;
+    if (MS) {
+      __syncthreads();
+      if (tid == 0) c->largs = c->args;
+    }
   }
   uint8_t* pages = smem_pages();
   float* xbuf = smem_xbuf(S);
@@ -1934,11 +1954,11 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
   __syncthreads();
   if (tid >= kConsumerThreads) {  // the loader streams weights without waiting for the previous grid
     const int w = tid >> 5;
-    if (w == kLoaderWarp && (tid & 31) == 0) producer(S, AA, c, pages);
+    if (w == kLoaderWarp && (tid & 31) == 0) producer<MS>(S, AA, c, pages);
     return;
   }
   if (AA.flags & SF_PDL) asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous grid's outputs
-  consumer<WT, SYNC>(S, AA, c, pages, xbuf, scratch);
+  consumer<WT, SYNC, MS>(S, AA, c, pages, xbuf, scratch);
   if (c->abort && tid == 0 && !global_err(S)) set_err(S, 4u, -7, -1);
 }
 

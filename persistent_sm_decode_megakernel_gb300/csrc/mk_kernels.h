@@ -2,8 +2,9 @@
 #pragma once
 
 namespace mk {
-// persistent step kernel instantiation for (weight dtype, sync mode, trace on/off)
-const void* step_kernel_entry(int dtype, int sync_mode, bool trace);
+// persistent step kernel instantiation for (weight dtype, sync mode); multi_step: the
+// instance that runs several greedy steps per launch (one step: the other instance)
+const void* step_kernel_entry(int dtype, int sync_mode, bool multi_step);
 // grid-barrier latency microbenchmark kernel
 const void* barrier_kernel_entry();
 // page-stream microbenchmark kernel
