@@ -185,6 +185,9 @@ constexpr int kTcRowBytes = kTcKw * 2 + 16;
 constexpr int kTcPageBytes = kTcRows * kTcRowBytes;                        // 33024
 constexpr int kTcPartialFloats = 2 * kConsumerWarps * kTcRows * kMaxBatch;  // double-buffered warp partials
 
+// above this many positions per KV split a step uses all of the schedule's splits
+constexpr int kSplitLongPositions = 2048;
+
 // a split's partial attention record per head: hd weighted value sums, the running max,
 // the exp-sum, two pad floats (16-byte rows, so records move as float4)
 constexpr int kPartExtra = 4;

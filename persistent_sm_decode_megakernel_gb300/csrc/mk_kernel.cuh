@@ -228,12 +228,19 @@ struct Attn {
   const uint16_t* kb;
   const uint16_t* vb;
 };
-// Splits in use this step: at least split_min_positions positions per split, at most the
-// schedule's S -- short contexts use a few splits (cheap merge), long contexts all.
+// Splits in use this step for sequence b: at most the schedule's S, and at least
+// split_min_positions positions per split (short contexts: a few splits, a cheap merge).
+// Within that, about one unit per CTA: a split costs a fixed ~2-3 us (q staging, the
+// epilogue, its share of the merge) besides its positions, so a batch of B sequences
+// uses n_cta / (B Hkv) splits -- unless a split would then hold more than
+// kSplitLongPositions positions, where streaming the cache dominates and all S splits
+// keep every CTA busy.
 __device__ __forceinline__ int active_splits(const DevState& S, const StepArgs& A, int b) {
   const int npos = A.pos[b] + 1;
   const int pmin = S.split_min_positions;
-  return max(1, min(S.S, (npos + pmin - 1) / pmin));
+  const int per_cta = max(1, S.n_cta / (A.B * S.Hkv));
+  const int want = max(per_cta, (npos + kSplitLongPositions - 1) / kSplitLongPositions);
+  return max(1, min(S.S, min((npos + pmin - 1) / pmin, want)));
 }
 __device__ __forceinline__ Attn make_attn(const DevState& S, const StepArgs& A, const Instr& in) {
   Attn a;

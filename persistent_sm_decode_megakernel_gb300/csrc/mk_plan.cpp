@@ -203,24 +203,27 @@ std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B,
         }
       }
     }
-    // ATTENTION: B * Hkv * S split units, dealt round-robin.  Fused: each unit counts its
-    // arrival on the (b, j) counter; the last of the S merges the splits and signals c_red
-    // (one signal per (b, j) and step).  Merged in the O-proj staging: every unit signals
-    // c_att, which the O-proj units wait for.
+    // ATTENTION: B * Hkv * S split units, dealt round-robin with the split index varying
+    // slowest, so that the units of the splits a step actually uses (s below its active
+    // count, which shrinks with the batch and the context) land on distinct CTAs.  Fused:
+    // each unit counts its arrival on the (b, j) counter; the last of the S merges the
+    // splits and signals c_red (one signal per (b, j) and step).  Merged in the O-proj
+    // staging: every unit signals c_att, which the O-proj units wait for.
     const int c_att = new_ctr();
     const int c_red = new_ctr();
     {
-      const int nu = B * m.Hkv * g.S;
+      const int nbj = B * m.Hkv, nu = nbj * g.S;
       std::vector<int> arr;
       if (fuse_reduce)
-        for (int k = 0; k < B * m.Hkv; ++k) arr.push_back(new_ctr());
+        for (int k = 0; k < nbj; ++k) arr.push_back(new_ctr());
       for (int u = 0; u < nu; ++u) {
+        const int bj = u % nbj, sp = u / nbj;
         Instr in = mk_instr(OP_ATTN, l, c_qkv, 0, fuse_reduce ? c_red : c_att);
-        in.a[0] = u / (m.Hkv * g.S);
-        in.a[1] = (u / g.S) % m.Hkv;
-        in.a[2] = u % g.S;
+        in.a[0] = bj / m.Hkv;
+        in.a[1] = bj % m.Hkv;
+        in.a[2] = sp;
         in.a[3] = g.S;
-        in.a[4] = fuse_reduce ? arr[u / g.S] : -1;
+        in.a[4] = fuse_reduce ? arr[bj] : -1;
         emit(u % n_cta, in);
       }
       if (fuse_reduce) {
