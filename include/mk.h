@@ -216,6 +216,22 @@ mk_status mk_selftest(int kind, int64_t *result, int n);
  * *us_per_barrier receives the mean latency in microseconds. */
 mk_status mk_barrier_bench(int mode, int n_barriers, double *us_per_barrier);
 
+/* SM -> die map ("7 · AMD et le monokernel", §7.4: die/chiplet locality; CUDA exposes no
+ * such map, so it is measured).  A one-wave probe (one CTA per SM of the current device)
+ * times cross-SM round trips from the SM that CTA 0 lands on to every other SM through
+ * one shared 128-byte line, one pair at a time (reps >= 4 round trips each, the first two
+ * discarded), and splits the SMs in two groups by those times (mk_two_groups).  die_of_sm host [max_sm] receives, indexed
+ * by SM id, 0 for the reference SM's group and 1 for the other; rtt_cycles host [max_sm]
+ * (or NULL) the mean round trip in SM cycles (0 for the reference SM); *n_sm the SM count.
+ * MK_ERR_INVALID if max_sm is below the SM count, MK_ERR_TIMEOUT if a probe wait ran out
+ * (each is bounded at 2 s). */
+mk_status mk_die_map(int reps, int max_sm, int *die_of_sm, float *rtt_cycles, int *n_sm);
+
+/* Two-means split of n >= 2 values (host only): group host [n] receives 0 for values at
+ * or below the threshold, 1 above; *threshold (or NULL) the midpoint between the two
+ * group means after convergence.  All values equal: every value in group 0. */
+mk_status mk_two_groups(const float *x, int n, int *group, float *threshold);
+
 /* One decode step that allocates no device memory, for callers that cannot call
  * cudaMalloc (code running inside an allocator or under a host framework that owns every
  * device allocation).  The pages have no counterpart to this entry point.  Same inputs

@@ -890,6 +890,98 @@ mk_status mk_selftest(int kind, int64_t* result, int n) {
   return MK_OK;
 }
 
+mk_status mk_two_groups(const float* x, int n, int* group, float* threshold) {
+  if (!x || !group || n < 2) return fail(MK_ERR_INVALID, "two groups: NULL argument or n < 2");
+  double lo = x[0], hi = x[0];
+  for (int i = 1; i < n; ++i) {
+    lo = std::min(lo, (double)x[i]);
+    hi = std::max(hi, (double)x[i]);
+  }
+  double thr = hi;  // all equal: one group
+  if (hi > lo) {
+    thr = 0.5 * (lo + hi);
+    for (int it = 0; it < 100; ++it) {  // Lloyd's iterations in one dimension
+      double s0 = 0, s1 = 0;
+      int n0 = 0, n1 = 0;
+      for (int i = 0; i < n; ++i) {
+        if (x[i] <= thr) { s0 += x[i]; ++n0; } else { s1 += x[i]; ++n1; }
+      }
+      if (!n0 || !n1) break;
+      const double t = 0.5 * (s0 / n0 + s1 / n1);
+      if (t == thr) break;
+      thr = t;
+    }
+  }
+  for (int i = 0; i < n; ++i) group[i] = x[i] <= thr ? 0 : 1;
+  if (threshold) *threshold = (float)thr;
+  return MK_OK;
+}
+
+mk_status mk_die_map(int reps, int max_sm, int* die_of_sm, float* rtt_cycles, int* n_sm_out) {
+  if (!die_of_sm || !n_sm_out || reps < 4) return fail(MK_ERR_INVALID, "die map: NULL argument or reps < 4");
+  int dev = 0, n_sm = 0, smem_optin = 0;
+  MK_CUDA(cudaGetDevice(&dev));
+  MK_CUDA(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
+  MK_CUDA(cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+  *n_sm_out = n_sm;
+  if (max_sm < n_sm) return fail(MK_ERR_INVALID, "die map: max_sm below the SM count");
+  // more than half an SM's shared memory per CTA: exactly one CTA per SM
+  const int smem = smem_optin / 2 + 1024;
+  const void* fn = rtt_kernel_entry();
+  MK_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+  int bpsm = 0;
+  MK_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bpsm, fn, 32, smem));
+  if (bpsm != 1) return fail(MK_ERR_OCCUPANCY, "die map: the probe does not run one CTA per SM");
+  DevBuf words, smid, cyc, bad;
+  MK_CUDA(cudaMalloc(&words.p, 256));  // turn word | ping, pong (two 128-byte lines)
+  MK_CUDA(cudaMemset(words.p, 0, 256));
+  MK_CUDA(cudaMalloc(&smid.p, sizeof(uint32_t) * n_sm));
+  MK_CUDA(cudaMalloc(&cyc.p, sizeof(uint64_t) * n_sm));
+  MK_CUDA(cudaMalloc(&bad.p, sizeof(uint32_t)));
+  MK_CUDA(cudaMemset(bad.p, 0, sizeof(uint32_t)));
+  uint32_t* w = reinterpret_cast<uint32_t*>(words.p);
+  uint32_t* sp = reinterpret_cast<uint32_t*>(smid.p);
+  uint64_t* cp = reinterpret_cast<uint64_t*>(cyc.p);
+  uint32_t* bp = reinterpret_cast<uint32_t*>(bad.p);
+  int64_t timeout = 2000000000LL;
+  void* args[6] = {&w, &reps, &timeout, &sp, &cp, &bp};
+  MK_CUDA(cudaLaunchCooperativeKernel(fn, dim3(n_sm), dim3(32), args, smem, nullptr));
+  MK_CUDA(cudaDeviceSynchronize());
+  std::vector<uint32_t> hs(n_sm);
+  std::vector<uint64_t> hc(n_sm);
+  uint32_t hb = 0;
+  MK_CUDA(cudaMemcpy(hs.data(), smid.p, sizeof(uint32_t) * n_sm, cudaMemcpyDeviceToHost));
+  MK_CUDA(cudaMemcpy(hc.data(), cyc.p, sizeof(uint64_t) * n_sm, cudaMemcpyDeviceToHost));
+  MK_CUDA(cudaMemcpy(&hb, bad.p, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+  if (hb) return fail(MK_ERR_TIMEOUT, "die map: a probe wait ran out");
+  std::vector<float> rtt(n_sm);
+  for (int i = 0; i < n_sm; ++i) {
+    if (hs[i] >= (uint32_t)max_sm) return fail(MK_ERR_STATE, "die map: SM id out of range");
+    rtt[i] = (float)hc[i];
+  }
+  // the reference SM itself: the smallest time measured, so it joins its own group
+  float mn = 0.f;
+  bool first = true;
+  for (int i = 1; i < n_sm; ++i) {
+    if (first || rtt[i] < mn) mn = rtt[i];
+    first = false;
+  }
+  std::vector<float> x(rtt);
+  x[0] = mn;
+  std::vector<int> grp(n_sm);
+  mk_status s = mk_two_groups(x.data(), n_sm, grp.data(), nullptr);
+  if (s) return s;
+  for (int i = 0; i < max_sm; ++i) {
+    die_of_sm[i] = -1;
+    if (rtt_cycles) rtt_cycles[i] = 0.f;
+  }
+  for (int i = 0; i < n_sm; ++i) {
+    die_of_sm[hs[i]] = grp[i];
+    if (rtt_cycles) rtt_cycles[hs[i]] = rtt[i];
+  }
+  return MK_OK;
+}
+
 mk_status mk_barrier_bench(int mode, int n_barriers, double* us_per_barrier) {
   if (!us_per_barrier || n_barriers < 1 || (mode != 0 && mode != 1))
     return fail(MK_ERR_INVALID, "mode must be 0/1, n_barriers >= 1");

@@ -53,6 +53,61 @@ __global__ void __launch_bounds__(256, 1) mk_barrier_kernel(uint32_t* ctr, float
   }
 }
 
+// ---------------------------------------------------------------- SM round-trip probe
+// Die locality (P1 §7.4): CUDA does not say which SM sits on which die, so it is measured.
+// A one-wave grid, one CTA per SM.  CTA 0 plays ping-pong with every other CTA in turn
+// through the same two words (one 128-byte line, so every pair meets at the same L2
+// home): it stores (partner, sequence number) into ping, the partner echoes it into pong,
+// and CTA 0 times the round trip in SM cycles.  Partners sleep on a separate turn word
+// until their turn, so that only the pair under test loads the memory system.  Every
+// wait is bounded by timeout_ns and raises *bad instead of hanging.
+__global__ void __launch_bounds__(32, 1) mk_rtt_kernel(uint32_t* words, int reps, int64_t timeout_ns,
+                                                       uint32_t* smid_out, uint64_t* cyc_out, uint32_t* bad) {
+  if (threadIdx.x != 0) return;
+  const int me = blockIdx.x, n = gridDim.x;
+  uint32_t sm;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+  smid_out[me] = sm;
+  uint32_t* turn = words;         // line 0
+  uint32_t* ping = words + 32;    // line 1
+  uint32_t* pong = words + 33;
+  const uint64_t t0 = globaltimer_ns();
+  if (me == 0) {
+    cyc_out[0] = 0;
+    for (int j = 1; j < n; ++j) {
+      st_relaxed_u32(turn, (uint32_t)j);
+      uint64_t sum = 0;
+      for (int r = 1; r <= reps; ++r) {
+        const uint32_t v = ((uint32_t)j << 16) | (uint32_t)r;
+        const long long a = clock64();
+        st_relaxed_u32(ping, v);
+        while (ld_relaxed_u32(pong) != v) {
+          if (globaltimer_ns() - t0 > (uint64_t)timeout_ns) {
+            st_relaxed_u32(bad, 1u);
+            st_relaxed_u32(turn, (uint32_t)n);
+            return;
+          }
+        }
+        if (r > 2) sum += (uint64_t)(clock64() - a);  // the first two cover the partner's wake-up
+      }
+      cyc_out[j] = sum / (uint64_t)(reps - 2);
+    }
+    st_relaxed_u32(turn, (uint32_t)n);
+    return;
+  }
+  while (ld_relaxed_u32(turn) < (uint32_t)me) {
+    __nanosleep(2000);
+    if (globaltimer_ns() - t0 > (uint64_t)timeout_ns || ld_relaxed_u32(bad)) return;
+  }
+  for (int r = 1; r <= reps; ++r) {
+    const uint32_t v = ((uint32_t)me << 16) | (uint32_t)r;
+    while (ld_relaxed_u32(ping) != v) {
+      if (globaltimer_ns() - t0 > (uint64_t)timeout_ns || ld_relaxed_u32(bad)) return;
+    }
+    st_relaxed_u32(pong, v);
+  }
+}
+
 // ---------------------------------------------------------------- page-stream microbenchmark
 // The decode kernel's loader / compute-warp structure with nothing else: one lane of the
 // loader warp streams bytes_per_cta of contiguous HBM through a ring of n_pages pages
@@ -197,6 +252,7 @@ const void* step_kernel_entry(int dtype, int sync_mode, bool multi_step) {
 }
 
 const void* barrier_kernel_entry() { return reinterpret_cast<const void*>(&mk_barrier_kernel); }
+const void* rtt_kernel_entry() { return reinterpret_cast<const void*>(&mk_rtt_kernel); }
 const void* stream_kernel_entry() { return reinterpret_cast<const void*>(&mk_stream_kernel); }
 
 }  // namespace mk

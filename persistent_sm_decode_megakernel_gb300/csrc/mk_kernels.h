@@ -7,6 +7,8 @@ namespace mk {
 const void* step_kernel_entry(int dtype, int sync_mode, bool multi_step);
 // grid-barrier latency microbenchmark kernel
 const void* barrier_kernel_entry();
+// SM round-trip probe kernel (SM -> die map)
+const void* rtt_kernel_entry();
 // page-stream microbenchmark kernel
 const void* stream_kernel_entry();
 }  // namespace mk
