@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -81,12 +82,15 @@ struct mk_ctx {
   DevBuf ptr_tables, rope, act, argkeys, ctl, trace;
   int trace_cap = 0;
   Ctl* host_ctl = nullptr;  // pinned
+  HostMail* mail = nullptr;  // pinned, mapped into the device's address space
+  uint32_t mail_seq = 0;
   std::map<int, std::unique_ptr<Sched>> scheds;
   uint32_t step = 0;
   bool broken = false;
   int last_B = 1;
   ~mk_ctx() {
     if (host_ctl) cudaFreeHost(host_ctl);
+    if (mail) cudaFreeHost(mail);
   }
 };
 
@@ -264,7 +268,7 @@ mk_status run_graph(mk_ctx* ctx, Sched* sc, const DevState& S, const StepArgs& A
 // enqueue one decode step (one launch, or the multi-launch control's per-op launches); with
 // persistent control, n_steps > 1 greedy steps in the one launch (tok_hist then [n_steps][B])
 mk_status enqueue_step(mk_ctx* ctx, Sched* sc, int B, const int32_t* tok, const int32_t* pos, bool tok_from_dev,
-                       float* logits, int32_t* tok_hist, int n_steps = 1) {
+                       float* logits, int32_t* tok_hist, int n_steps = 1, uint32_t mail_seq = 0) {
   DevState S = ctx->st;
   S.counters = reinterpret_cast<uint32_t*>(sc->counters.p);
   S.n_counters = sc->plan.n_counters;
@@ -280,6 +284,7 @@ mk_status enqueue_step(mk_ctx* ctx, Sched* sc, int B, const int32_t* tok, const 
   A.logits = logits;
   A.tok_hist = tok_hist;
   A.n_steps = n_steps;
+  A.mail_seq = mail_seq;
   if (n_steps > 1 && ctx->opts.exec_mode != MK_EXEC_PERSISTENT)
     return fail(MK_ERR_INVALID, "several steps in one launch need persistent control");
   const void* fn = n_steps > 1 ? ctx->kernel_ms : ctx->kernel;
@@ -511,6 +516,13 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
   MK_CUDA(cudaMemset(ctx->ctl.p, 0, sizeof(Ctl)));
   S.ctl = reinterpret_cast<Ctl*>(ctx->ctl.p);
   MK_CUDA(cudaMallocHost(reinterpret_cast<void**>(&ctx->host_ctl), sizeof(Ctl)));
+  MK_CUDA(cudaHostAlloc(reinterpret_cast<void**>(&ctx->mail), sizeof(HostMail), cudaHostAllocMapped));
+  memset(ctx->mail, 0, sizeof(HostMail));
+  {
+    void* dp = nullptr;
+    MK_CUDA(cudaHostGetDevicePointer(&dp, ctx->mail, 0));
+    S.mail = reinterpret_cast<HostMail*>(dp);
+  }
   S.n_cta = ctx->n_cta;
   S.page_bytes = g.page_bytes;
   S.n_pages = g.n_pages;
@@ -579,8 +591,28 @@ mk_status mk_decode_step(mk_ctx* ctx, const int32_t* in_tok, const int32_t* pos,
   Sched* sc = nullptr;
   s = get_sched(ctx, B, &sc);
   if (s) return s;
-  s = enqueue_step(ctx, sc, B, in_tok, pos, false, logits, nullptr);
+  // Without logits to hand back, the step posts its tokens to the mapped mailbox and the
+  // host waits on that word alone: no device-to-host copy, no stream synchronisation (the
+  // kernel's tail still runs; the next launch queues behind it).  Any error, or a kernel
+  // that ends without posting, takes the synchronous path through the control block.
+  const bool mail = logits == nullptr && ctx->opts.exec_mode == MK_EXEC_PERSISTENT;
+  const uint32_t seq = mail ? ++ctx->mail_seq : 0u;
+  if (mail && seq == 0u) return fail(MK_ERR_STATE, "mailbox sequence wrapped");
+  s = enqueue_step(ctx, sc, B, in_tok, pos, false, logits, nullptr, 1, seq);
   if (s) return s;
+  if (mail) {
+    const volatile uint32_t* w = &ctx->mail->seq;
+    for (uint32_t k = 1;; ++k) {
+      if (*w == seq) break;
+      if ((k & 255u) == 0u && cudaStreamQuery(ctx->stream) != cudaErrorNotReady) break;
+    }
+    std::atomic_thread_fence(std::memory_order_acquire);
+    if (*w == seq && ctx->mail->err == 0u) {
+      for (int b = 0; b < B; ++b) out_tok[b] = ctx->mail->tok[b];
+      if (ctx->mail->nan_seen) return fail(MK_ERR_NAN, "a logit was NaN");
+      return MK_OK;
+    }
+  }
   s = read_status(ctx);
   if (s && s != MK_ERR_NAN) return s;
   for (int b = 0; b < B; ++b) out_tok[b] = ctx->host_ctl->tok[b];
@@ -655,6 +687,8 @@ mk_status mk_reset(mk_ctx* ctx) {
   MK_CUDA(cudaDeviceSynchronize());
   ctx->step = 0;
   ctx->broken = false;
+  memset(ctx->mail, 0, sizeof(HostMail));
+  ctx->mail_seq = 0;
   return MK_OK;
 }
 

@@ -94,6 +94,17 @@ struct Ctl {
   uint32_t pad;
 };
 
+// Mapped host memory the last LM-head CTA fills for a host-token step (mk_decode_step
+// without logits): the tokens, the sticky error code and the NaN flag, then seq with a
+// system-scope release, so that the host thread waiting on seq needs no copy or sync.
+struct HostMail {
+  uint32_t seq;
+  uint32_t err;
+  uint32_t nan_seen;
+  uint32_t pad;
+  int32_t tok[kMaxBatch];
+};
+
 struct TraceRec {
   int32_t cta, pc, op, layer;
   uint64_t t_fetch, t_ready, t_mark[6], t_end;
@@ -132,6 +143,7 @@ struct DevState {
   uint32_t* counters;
   int n_counters;
   Ctl* ctl;
+  HostMail* mail;              // device address of the context's mapped host mailbox
   TraceRec* trace;
   int trace_cap;
   // execution
@@ -171,6 +183,7 @@ struct StepArgs {
   float* logits;               // [B][V] or null
   int32_t* tok_hist;           // device [B] copy of this step's tokens, or null
   int n_steps;                 // greedy steps this launch runs back to back (0 or 1: one)
+  uint32_t mail_seq;           // non-zero: post the tokens to the host mailbox with this seq
   // non-null: the per-step fields (epoch .. tok_hist; flags OR-ed) are read from this device
   // copy at kernel start -- the launches of a CUDA graph keep fixed parameters
   const StepArgs* dyn;

@@ -1880,6 +1880,12 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
             const int32_t tok = (int32_t)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
             S.ctl->tok[b] = tok;
             if (A.tok_hist) A.tok_hist[b] = tok;
+            if (A.mail_seq) S.mail->tok[b] = tok;
+          }
+          if (A.mail_seq) {  // the host thread waits on this word instead of copying Ctl back
+            S.mail->err = ld_relaxed_u32(&S.ctl->err.code);
+            S.mail->nan_seen = ld_relaxed_u32(&S.ctl->nan_seen);
+            st_release_sys_u32(&S.mail->seq, A.mail_seq);
           }
           if (MS) st_release_u32(&S.ctl->tok_seq, A.step + 1u);  // after the tokens: the next step waits on it
         }

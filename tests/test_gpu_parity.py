@@ -192,6 +192,34 @@ def test_multi_step_launch_matches_single_step_launches(lib, tiny, sync, B):
     np.testing.assert_array_equal(runs[0][1][:, 0], toks[0, P + 1: P + 1 + n])
 
 
+@pytest.mark.parametrize("sync", [0, 1], ids=["counter", "sentinel"])
+def test_host_token_steps_match_device_chain(lib, tiny, sync):
+    """mk_decode_step without logits (tokens come back through the mapped host mailbox, no
+    copy or stream sync) returns the same greedy chain as device-fed steps, and a step with
+    logits (the synchronous path) in the middle of it changes nothing."""
+    cfg, w, m = tiny
+    P, n = 5, 10
+    prompt = synth.gen_prompts(cfg, 2, P)
+    dm = lib.DeviceModel(cfg, w, max_batch=2, max_ctx=P + n + 1)
+    dec = lib.Decoder(dm, sync_mode=sync)
+    first = dec.prefill(prompt)
+    out = torch.zeros((n, 2), dtype=torch.int32, device=dm.device)
+    dec.decode_steps(first, [P] * 2, n, out)
+    dec.synchronize()
+    want = out.cpu().numpy()
+    dec.close()
+    dm2 = lib.DeviceModel(cfg, w, max_batch=2, max_ctx=P + n + 1)
+    dec2 = lib.Decoder(dm2, sync_mode=sync)
+    tok = dec2.prefill(prompt)
+    got = []
+    logits = torch.zeros((2, cfg.vocab), dtype=torch.float32, device=dm2.device)
+    for k in range(n):
+        tok = dec2.decode_step(tok, [P + k] * 2, logits=logits if k == 4 else None)
+        got.append(list(tok))
+    dec2.close()
+    np.testing.assert_array_equal(np.array(got), want)
+
+
 def test_fault_injection_times_out_and_recovers(lib, tiny):
     """A dropped counter signal (injected on the host, validator skipped) makes a device
     wait run out: the step returns MK_ERR_TIMEOUT within the limit, the context refuses
