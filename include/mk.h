@@ -156,8 +156,12 @@ mk_status mk_prefill(mk_ctx *ctx, const int32_t *tokens, int B, int P,
 
 /* The hot path: one decode step, ONE kernel launch.  in_tok host [B] sits at position
  * pos host [B] (the cache holds 0..pos[b]-1); out_tok host [B] receives the argmax
- * token (lowest index among ties); logits device [B, vocab] fp32 or NULL.  Synchronous
- * for out_tok (one small device-to-host copy). */
+ * token (lowest index among ties); logits device [B, vocab] fp32 or NULL.  Returns once
+ * out_tok holds the tokens: with logits NULL (persistent control) the last LM-head CTA
+ * posts them to a mapped host mailbox and the calling thread waits on that word (no copy,
+ * no stream synchronisation; the kernel's last instructions may still be finishing, and
+ * the next call queues behind them); otherwise, or after a device error, through one
+ * small device-to-host copy and a stream synchronisation. */
 mk_status mk_decode_step(mk_ctx *ctx, const int32_t *in_tok, const int32_t *pos, int B,
                          int32_t *out_tok, float *logits);
 
