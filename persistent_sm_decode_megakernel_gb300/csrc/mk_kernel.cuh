@@ -1186,20 +1186,49 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
       for (int base = 0; base < n_items; base += U * kConsumerThreads) {
         const float4* pp[U];
         uint2 gbu[U];  // gains: issued ahead of the polls (they do not depend on the producer)
+        // item -> (sequence, vector): at 8 and 16 sequences stepped from the first without
+        // a division per item (measured faster there; at 4 the division measured faster)
+        const int b0 = (base + tid) / k4n, k40 = base + tid - b0 * k4n;
+        {
+          int b = b0, k4 = k40;
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int it = base + u * kConsumerThreads + tid, b = it / k4n, k4 = it - b * k4n;
-          const bool live = it < n_items && b < B;
-          pp[u] = live ? reinterpret_cast<const float4*>(src + (size_t)b * K + k0) + k4 : nullptr;
-          gbu[u] = (live && gain != nullptr) ? __ldg(reinterpret_cast<const uint2*>(gain + k0) + k4) : make_uint2(0u, 0u);
+          for (int u = 0; u < U; ++u) {
+            const int it = base + u * kConsumerThreads + tid;
+            if (NB < 8) {
+              b = it / k4n;
+              k4 = it - b * k4n;
+            }
+            const bool live = it < n_items && b < B;
+            pp[u] = live ? reinterpret_cast<const float4*>(src + (size_t)b * K + k0) + k4 : nullptr;
+            gbu[u] = (live && gain != nullptr) ? __ldg(reinterpret_cast<const uint2*>(gain + k0) + k4) : make_uint2(0u, 0u);
+            if (NB >= 8) {
+              k4 += kConsumerThreads;
+              while (k4 >= k4n) {
+                k4 -= k4n;
+                ++b;
+              }
+            }
+          }
         }
         float4 v[U];
         load_vecs<SYNC, U>(S, c, pp, v);
+        int bn = b0, k4n_ = k40;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int it = base + u * kConsumerThreads + tid;
+          if (NB < 8) {
+            bn = it / k4n;
+            k4n_ = it - bn * k4n;
+          }
+          const int b = bn, k4 = k4n_, k = 4 * k4;
+          if (NB >= 8) {
+            k4n_ += kConsumerThreads;
+            while (k4n_ >= k4n) {
+              k4n_ -= k4n;
+              ++bn;
+            }
+          }
           if (it >= n_items) continue;
-          const int b = it / k4n, k4 = it - b * k4n, k = 4 * k4;
           float4 x = v[u];
           if (gain != nullptr && b < B) {
             const uint2 gb = gbu[u];
