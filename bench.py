@@ -14,8 +14,8 @@ value: tok/s with everything resident in HBM: K chained steps (each step embeds 
 token the previous step chose on the device), CUDA events on the context's stream
 around every launch.
 e2e: the same metric through mk_decode_step with host token buffers (token and position
-travel as kernel parameters; the step's token and status come back in one 96-byte
-device-to-host copy), host loop included.
+travel as kernel parameters; the step's tokens and status come back through an 80-byte
+mapped host mailbox the kernel writes), host loop included.
 roofline: algorithmic bytes per step / (mean launch duration / steps per launch) against
 the measured HBM copy bandwidth; traffic: the profiled DRAM bytes of one step.  cpu_baseline / --impl reference: the fp64 oracle on the host cores.
 Multi-GPU (torchrun, N > 1): independent replicas, one per GPU; max time over ranks.
@@ -346,8 +346,9 @@ def main():
                      "steps_per_launch": C, "bytes_per_step": bytes_per_step, "mean_step_us": mean_step_s * 1e6,
                      "frac_of_nominal_7900": achieved_gbs / NOMINAL_HBM_GBS},
         "overhead_fraction": (total_s / K - t_min) / (total_s / K),
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 8 * B, "d2h_bytes_per_step": 96,
-                "steps": K2, "note": "token+position as kernel parameters; status+token in one D2H copy"},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 8 * B, "d2h_bytes_per_step": 80,
+                "steps": K2, "note": "token+position as kernel parameters; tokens and status posted by the "
+                                     "kernel to an 80-byte mapped host mailbox"},
         "cpu_baseline": cpu,
         "clocks": clocks.summary(),
         "launch": {"ctas": info["n_ctas"], "threads": info["threads_per_cta"], "smem": info["smem_bytes"],
