@@ -33,6 +33,7 @@ struct SmemCtl {
   volatile int abort;
   StepArgs args;  // the step's arguments (from the launch, or from device memory for graphs)
   StepArgs largs; // the loader's copy: it runs ahead into the next step of a multi-step launch
+  int ms_step;      // multi-step launches: the step being run
   float* step_act;  // multi-step launches: the current step's activation arena, batch tile and
   int step_nb;      // GQA group (kept here rather than in registers across the op calls)
   int step_G;
@@ -1416,43 +1417,60 @@ __device__ __noinline__ void op_attn(const DevState& S_arg, const StepArgs& A_ar
   // One position per LPP-lane group: scores from its key row, online-softmax update,
   // then its value row.  Rows come from a page (storage dtype) or, for the new
   // position, from the fp32 staging in smem.
-  auto update = [&](bool valid, const uint16_t* krow, const uint16_t* vrow) {  // row starts
-    float sc[G];
+  // RC passes of the warp at once (RC positions per lane group): their scores are
+  // independent, so they are computed together; one running-max update and one rescale of
+  // the accumulators per chunk; then the value rows, each with its own weight.  Blocks of
+  // one pass (short splits) take RC = 1.
+  auto chunk = [&](auto rct, int nvalid, const uint16_t* const* krow, const uint16_t* const* vrow) {
+    constexpr int RC = decltype(rct)::value;
+    float sc[RC][G];
 #pragma unroll
-    for (int g = 0; g < G; ++g) sc[g] = 0.f;
-    if (valid) {
+    for (int r = 0; r < RC; ++r) {
 #pragma unroll
-      for (int u = 0; u < DPL / 8; ++u) {
-        float kv[8];
-        Unpack<WT>::u8(reinterpret_cast<const uint4*>(krow)[u * LPP + dl], kv);
+      for (int g = 0; g < G; ++g) sc[r][g] = 0.f;
+      if (r < nvalid) {
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float a = sc[g];
-          if (QREG) {
+        for (int u = 0; u < DPL / 8; ++u) {
+          float kv[8];
+          Unpack<WT>::u8(reinterpret_cast<const uint4*>(krow[r])[u * LPP + dl], kv);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) a = fmaf(q[QREG ? g : 0][QREG ? u * 8 + e : 0], kv[e], a);
-          } else {
-            const float4 q0 = *reinterpret_cast<const float4*>(qs + g * HD + u * LPP * 8);
-            const float4 q1 = *reinterpret_cast<const float4*>(qs + g * HD + u * LPP * 8 + 4);
-            a = fmaf(q0.x, kv[0], a); a = fmaf(q0.y, kv[1], a); a = fmaf(q0.z, kv[2], a); a = fmaf(q0.w, kv[3], a);
-            a = fmaf(q1.x, kv[4], a); a = fmaf(q1.y, kv[5], a); a = fmaf(q1.z, kv[6], a); a = fmaf(q1.w, kv[7], a);
+          for (int g = 0; g < G; ++g) {
+            float a = sc[r][g];
+            if (QREG) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) a = fmaf(q[QREG ? g : 0][QREG ? u * 8 + e : 0], kv[e], a);
+            } else {
+              const float4 q0 = *reinterpret_cast<const float4*>(qs + g * HD + u * LPP * 8);
+              const float4 q1 = *reinterpret_cast<const float4*>(qs + g * HD + u * LPP * 8 + 4);
+              a = fmaf(q0.x, kv[0], a); a = fmaf(q0.y, kv[1], a); a = fmaf(q0.z, kv[2], a); a = fmaf(q0.w, kv[3], a);
+              a = fmaf(q1.x, kv[4], a); a = fmaf(q1.y, kv[5], a); a = fmaf(q1.z, kv[6], a); a = fmaf(q1.w, kv[7], a);
+            }
+            sc[r][g] = a;
           }
-          sc[g] = a;
         }
       }
     }
-    float p[G];
+    // full scores within each lane group; invalid rows (beyond the block) at -inf
+#pragma unroll
+    for (int r = 0; r < RC; ++r)
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float a = sc[r][g];
+#pragma unroll
+        for (int o2 = 1; o2 < LPP; o2 <<= 1) a += __shfl_xor_sync(0xffffffffu, a, o2);
+        sc[r][g] = r < nvalid ? a : -CUDART_INF_F;
+      }
+    float p[RC][G];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      float a = sc[g];
+      float mx = sc[0][g];
 #pragma unroll
-      for (int o2 = 1; o2 < LPP; o2 <<= 1) a += __shfl_xor_sync(0xffffffffu, a, o2);
-      const float sv = valid ? a : -CUDART_INF_F;
-      float mx = sv;
+      for (int r = 1; r < RC; ++r) mx = fmaxf(mx, sc[r][g]);
 #pragma unroll
       for (int o2 = LPP; o2 < 32; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
       const float mn = fmaxf(m[g], mx);  // warp-uniform
-      p[g] = 0.f;
+#pragma unroll
+      for (int r = 0; r < RC; ++r) p[r][g] = 0.f;
       if (mn == -CUDART_INF_F) continue;
       if (mn != m[g]) {
         const float corr = exp2f(m[g] - mn);
@@ -1461,18 +1479,24 @@ __device__ __noinline__ void op_attn(const DevState& S_arg, const StepArgs& A_ar
         for (int i = 0; i < DPL; ++i) o[g][i] *= corr;
         m[g] = mn;
       }
-      p[g] = valid ? exp2f(sv - mn) : 0.f;
-      lsum[g] += p[g];
+#pragma unroll
+      for (int r = 0; r < RC; ++r) {
+        p[r][g] = r < nvalid ? exp2f(sc[r][g] - mn) : 0.f;
+        lsum[g] += p[r][g];
+      }
     }
-    if (valid) {
 #pragma unroll
-      for (int u = 0; u < DPL / 8; ++u) {
-        float vv[8];
-        Unpack<WT>::u8(reinterpret_cast<const uint4*>(vrow)[u * LPP + dl], vv);
+    for (int r = 0; r < RC; ++r) {
+      if (r < nvalid) {
 #pragma unroll
-        for (int g = 0; g < G; ++g)
+        for (int u = 0; u < DPL / 8; ++u) {
+          float vv[8];
+          Unpack<WT>::u8(reinterpret_cast<const uint4*>(vrow[r])[u * LPP + dl], vv);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) o[g][u * 8 + e] = fmaf(p[g], vv[e], o[g][u * 8 + e]);
+          for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[g][u * 8 + e] = fmaf(p[r][g], vv[e], o[g][u * 8 + e]);
+        }
       }
     }
   };
@@ -1492,14 +1516,31 @@ __device__ __noinline__ void op_attn(const DevState& S_arg, const StepArgs& A_ar
       if (++rv.slot == S.n_pages) { rv.slot = 0; rv.ph ^= 1u; }
       vp = page_wait(S, c, pages, rv);
     }
-    // the block's rows dealt over (warp, lane group); the bound is uniform
-    for (int base = 0; base < nx; base += kConsumerWarps * NGRP) {
-      const int t = base + warp * NGRP + pgi;
-      const bool cached = t < np;
-      const size_t off = (size_t)(cached ? t : 0) * HD * 2;
-      update(t < nx, cached ? reinterpret_cast<const uint16_t*>(kp + off) : knew,
-             cached ? reinterpret_cast<const uint16_t*>(vp + off) : knew + HD);
-    }
+    // the block's rows dealt over (warp, lane group), RC passes per chunk: row
+    // base + r * (warps x groups) + (warp, group) for r < RC; the bounds are uniform
+    constexpr int PASS = kConsumerWarps * NGRP;
+    auto run_chunks = [&](auto rct) {
+      constexpr int RC = decltype(rct)::value;
+      for (int base = 0; base < nx; base += RC * PASS) {
+        const uint16_t* kr[RC];
+        const uint16_t* vr[RC];
+        int nvalid = 0;  // rows r < nvalid exist for this lane group (a prefix)
+#pragma unroll
+        for (int r = 0; r < RC; ++r) {
+          const int t = base + r * PASS + warp * NGRP + pgi;
+          const bool cached = t < np;
+          const size_t off = (size_t)(cached ? t : 0) * HD * 2;
+          kr[r] = cached ? reinterpret_cast<const uint16_t*>(kp + off) : knew;
+          vr[r] = cached ? reinterpret_cast<const uint16_t*>(vp + off) : knew + HD;
+          if (t < nx) nvalid = r + 1;
+        }
+        chunk(rct, nvalid, kr, vr);
+      }
+    };
+    if (nx <= PASS)
+      run_chunks(std::integral_constant<int, 1>{});
+    else
+      run_chunks(std::integral_constant<int, 4>{});
     if (paged) {
       page_release(S, c, ring);  // K page
       page_release(S, c, ring);  // V page
@@ -1750,9 +1791,10 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
   // before has published its tokens (its last CTA's last instruction is done): then the
   // arguments advance one position, the token comes from the device, and the buffers that
   // step used are prepared for the step after this one.
-  const int n_steps = (MS && A.n_steps > 1) ? A.n_steps : 1;
-  for (int st = 0; st < n_steps; ++st) {
-  if (MS && st > 0) {
+  // (the step index lives in shared memory, zeroed in the kernel prologue: nothing extra
+  // stays in registers across the op calls of a step)
+  for (;;) {
+  if (MS && c->ms_step > 0) {
     bool bad = false;
     if (tid == 0 && !wait_seq(&S.ctl->tok_seq, A.step + 1u, -9)) {
       c->abort = 1;
@@ -1939,7 +1981,11 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
       }
     }
   }
-  if (MS && consumer_sync_or(c->abort)) break;
+  if (!MS) break;
+  if (consumer_sync_or(c->abort)) break;
+  if (tid == 0) c->ms_step += 1;
+  consumer_sync();
+  if (c->ms_step >= A.n_steps) break;
   }  // steps
 }
 
@@ -1982,6 +2028,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
       c->last_issue_phase[i] = -1;
     }
     c->abort = 0;
+    c->ms_step = 0;
     mbar_fence_init();
   }
   if (tid < kMaxBatch) c->best[tid] = 0ull;
