@@ -1419,8 +1419,8 @@ __device__ __noinline__ void op_attn(const DevState& S_arg, const StepArgs& A_ar
   // position, from the fp32 staging in smem.
   // RC passes of the warp at once (RC positions per lane group): their scores are
   // independent, so they are computed together; one running-max update and one rescale of
-  // the accumulators per chunk; then the value rows, each with its own weight.  Blocks of
-  // one pass (short splits) take RC = 1.
+  // the accumulators per chunk; then the value rows, each with its own weight.  RC is 4
+  // while a block needs at least three more passes, else 1.
   auto chunk = [&](auto rct, int nvalid, const uint16_t* const* krow, const uint16_t* const* vrow) {
     constexpr int RC = decltype(rct)::value;
     float sc[RC][G];
@@ -1519,9 +1519,9 @@ __device__ __noinline__ void op_attn(const DevState& S_arg, const StepArgs& A_ar
     // the block's rows dealt over (warp, lane group), RC passes per chunk: row
     // base + r * (warps x groups) + (warp, group) for r < RC; the bounds are uniform
     constexpr int PASS = kConsumerWarps * NGRP;
-    auto run_chunks = [&](auto rct) {
+    auto run_chunk = [&](auto rct, int base) {
       constexpr int RC = decltype(rct)::value;
-      for (int base = 0; base < nx; base += RC * PASS) {
+      {
         const uint16_t* kr[RC];
         const uint16_t* vr[RC];
         int nvalid = 0;  // rows r < nvalid exist for this lane group (a prefix)
@@ -1537,10 +1537,15 @@ __device__ __noinline__ void op_attn(const DevState& S_arg, const StepArgs& A_ar
         chunk(rct, nvalid, kr, vr);
       }
     };
-    if (nx <= PASS)
-      run_chunks(std::integral_constant<int, 1>{});
-    else
-      run_chunks(std::integral_constant<int, 4>{});
+    // chunks of 4 passes while at least 3 remain, then single passes: a chunk's rows past
+    // the block still cost their shuffles
+    if (nx <= PASS) {
+      run_chunk(std::integral_constant<int, 1>{}, 0);
+    } else {
+      int base = 0;
+      for (; nx - base > 2 * PASS; base += 4 * PASS) run_chunk(std::integral_constant<int, 4>{}, base);
+      for (; base < nx; base += PASS) run_chunk(std::integral_constant<int, 1>{}, base);
+    }
     if (paged) {
       page_release(S, c, ring);  // K page
       page_release(S, c, ring);  // V page
