@@ -37,6 +37,8 @@ WORKLOAD = "2b"
 METRIC = "batch-1 decode tok/s (2B fp16) + weight-stream HBM GB/s vs GB300 peak"
 UNIT = "tok/s"
 PROMPT = 512
+WORKLOAD_DESC = ("2b-fp16 decode: 24 layers, d 2048, 16/8 heads x 128, FFN 8192, vocab 128256; "
+                 "batch 1, 512-token prompt, greedy decode (synthetic seeded weights)")
 NOMINAL_HBM_GBS = 7900.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "mk_step_kernel_2b_b1.txt")
 KERNEL_SOURCES = ["mk_kernel.cuh", "mk_device.cuh", "mk_internal.h"]
@@ -224,7 +226,8 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
             "steps": n, "warmup": 1, "ms_per_step": 1000.0 * dt / max(n, 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "2b-fp16 decode, batch 1 (synthetic seeded weights)", "batch": 1},
+            "config": {"workload": WORKLOAD_DESC, "batch": 1, "prompt_len": PROMPT,
+                       "note": "the oracle's sample steps start from an empty cache (see cpu_baseline.sample)"},
             "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -333,8 +336,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": 1000.0 * total_s / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "accumulate": "f32", "data": "synthetic",
-        "config": {"workload": "2b-fp16 decode: 24 layers, d 2048, 16/8 heads x 128, FFN 8192, vocab 128256; "
-                               "batch 1, 512-token prompt, greedy decode (synthetic seeded weights)",
+        "config": {"workload": WORKLOAD_DESC,
                    "batch": B, "prompt_len": PROMPT, "context": [positions[0], positions[-1]],
                    "l2": "inputs larger than L2: 3.6 GB streamed per step vs 129 MB L2, no flush",
                    "sync": args.sync, "exec": args.exec, "parallelism": f"replicas x{world}"},
