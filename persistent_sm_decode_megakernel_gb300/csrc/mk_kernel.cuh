@@ -1971,8 +1971,8 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
     }
     if (TRACE && tid == 0) {
       const uint64_t t_end = globaltimer_ns();
-      const uint32_t k = atomicAdd(&S.ctl->trace_n, 1u);
-      if ((int)k < S.trace_cap) {
+      const uint32_t idx = atomicAdd(&S.ctl->trace_n, 1u);
+      if ((int)idx < S.trace_cap) {
         TraceRec rec;
         rec.cta = cta;
         rec.pc = pc;
@@ -1982,7 +1982,7 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
         rec.t_ready = t_ready;
         for (int k = 0; k < 6; ++k) rec.t_mark[k] = c->tmark[k];
         rec.t_end = t_end;
-        S.trace[k] = rec;
+        S.trace[idx] = rec;
       }
     }
   }
