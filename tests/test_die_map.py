@@ -47,6 +47,15 @@ def test_two_groups_degenerate_cases(mk):
     assert st == mk.MK_ERR_INVALID
 
 
+def test_die_map_rejects_bad_arguments_before_any_device_call(mk):
+    die = (ctypes.c_int * 8)()
+    n = ctypes.c_int()
+    assert mk.mk_die_map(3, 8, die, None, ctypes.byref(n)) == mk.MK_ERR_INVALID   # reps < 4
+    assert mk.mk_die_map(16, 8, None, None, ctypes.byref(n)) == mk.MK_ERR_INVALID  # no output array
+    st, _, _ = _groups(mk, [])
+    assert st == mk.MK_ERR_INVALID
+
+
 @pytest.mark.gpu
 def test_die_map_covers_every_sm(mk):
     import torch
