@@ -1,5 +1,5 @@
 // The persistent decode megakernel for sm_103a (templates; instantiated per weight
-// dtype and sync mode in mk_k_*.cu).
+// dtype, sync mode and one-step / multi-step launch in mk_k_*.cu).
 //
 // Structure ("8 · Écrire son megakernel", §8.2): one CTA per SM walks its own queue of
 // 64-byte instructions; for each one it waits for its dependency counter, executes the
@@ -560,9 +560,6 @@ __device__ __forceinline__ float4 load_v4(const float4* p, const DevState& S, Sm
   return any_nan4(v) ? poll_slow_v4(p, S, c) : v;
 }
 
-// Up to U 16-byte loads in flight (entries with p[u] == nullptr are skipped and read as
-// zeros); with sentinels, the vectors still holding one are re-read together until the
-// producers' values land (bounded, sets the abort flag on timeout).
 // One pause of a sentinel re-poll loop: backs off (exponentially, up to the configured
 // cap) and returns false once the wait has run past the timeout or another party
 // aborted (the abort flag is set and, if nothing was recorded yet, MK_ERR_TIMEOUT).
@@ -577,6 +574,9 @@ __device__ __forceinline__ bool poll_pause(const DevState& S, SmemCtl* c, int k,
   return true;
 }
 
+// Up to U 16-byte loads in flight (entries with p[u] == nullptr are skipped and read as
+// zeros); with sentinels, the vectors still holding one are re-read together until the
+// producers' values land (bounded, sets the abort flag on timeout).
 template <int SYNC, int U>
 __device__ __forceinline__ void load_vecs(const DevState& S, SmemCtl* c, const float4* const (&p)[U], float4 (&v)[U]) {
   if (SYNC == SYNC_COUNTER) {
@@ -1415,8 +1415,8 @@ __device__ __noinline__ void op_attn(const DevState& S_arg, const StepArgs& A_ar
   }
 
   // One position per LPP-lane group: scores from its key row, online-softmax update,
-  // then its value row.  Rows come from a page (storage dtype) or, for the new
-  // position, from the fp32 staging in smem.
+  // then its value row.  Rows come from a page or, for the new position, from its copy
+  // staged above (both in the storage dtype).
   // RC passes of the warp at once (RC positions per lane group): their scores are
   // independent, so they are computed together; one running-max update and one rescale of
   // the accumulators per chunk; then the value rows, each with its own weight.  RC is 4
