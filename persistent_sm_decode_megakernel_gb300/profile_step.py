@@ -7,7 +7,9 @@
 Prints the per-step time (CUDA events on the context stream) and, with --trace, a
 summary of the last step's instruction journal: per op, the mean time from fetch to
 dependency-satisfied (waiting) and from there to the end (working), the per-CTA
-waiting share of the step, and the first op groups' start/end on the step's timeline.
+waiting share of the step, the first op groups' start/end on the step's timeline, and
+the per-layer dependency chain (chain_us: when each op's inputs were staged and when it
+ended, after the previous layer's end, and the hop between consecutive ops).
 The decode steps are preceded by exactly `prompt` launches of the same kernel (one per
 prompt position), which is the count an ncu capture skips with -s.
 """
@@ -83,6 +85,42 @@ def summarize(trace):
     return out
 
 
+CHAIN = (2, 3, 4, 5, 6, 7)  # one layer's ops in dependency order
+
+
+def chain(trace):
+    """The per-layer dependency chain from the journal: for each op of a layer, the time
+    (us) after the previous layer's last down-projection CTA ended at which its CTAs had
+    their inputs staged (median over CTAs; mark 0) and ended (median and max), and the hop
+    -- the first CTA's staging done minus the previous op's last end.  Medians over the
+    layers that have a previous layer.  Ops without a staging mark (the split merge) report
+    ends only."""
+    by = {}
+    for r in trace:
+        by.setdefault((r[3], r[2]), []).append(r)
+    layers = sorted({l for (l, op) in by if op == 7})
+    acc = {}
+    for L in layers:
+        if (L - 1, 7) not in by:
+            continue
+        ref = max(r[6] for r in by[(L - 1, 7)])
+        prev_max = ref
+        for op in CHAIN:
+            rs = by.get((L, op))
+            if not rs:
+                continue
+            ends = sorted(r[6] for r in rs)
+            marks = sorted(r[7] for r in rs if r[7])
+            d = acc.setdefault(OPS[op], {"staged": [], "end_med": [], "end_max": [], "hop": []})
+            d["end_med"].append((statistics.median(ends) - ref) / 1e3)
+            d["end_max"].append((ends[-1] - ref) / 1e3)
+            if marks:
+                d["staged"].append((statistics.median(marks) - ref) / 1e3)
+                d["hop"].append((marks[0] - prev_max) / 1e3)
+            prev_max = ends[-1]
+    return {op: {k: round(statistics.median(v), 3) for k, v in d.items() if v} for op, d in acc.items()}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--workload", default="2b")
@@ -142,7 +180,9 @@ def main():
             pos += 1
         res = {"workload": args.workload, "layers": cfg.n_layers, "step_us": times, "info": dec.info()}
         if args.trace:
-            res["trace"] = summarize(dec.trace())
+            tr = dec.trace()
+            res["trace"] = summarize(tr)
+            res["chain_us"] = chain(tr)
         dec.close()
     print(json.dumps(res, indent=1))
     if args.json:
