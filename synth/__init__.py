@@ -87,6 +87,10 @@ CONFIGS = {
                       batch=1, prompt_len=512, decode_len=1024),
     "8b": ModelConfig("8b", 32, 4096, 32, 8, 128, 14336, 128256, BF16, seed=4, cfg_index=4,
                       batch=1, prompt_len=8192, decode_len=512),
+    # a tiny decoder with four query heads per kv head (the 8b model's GQA group) for the
+    # grouped attention instance at long contexts in test time
+    "tiny-g4": ModelConfig("tiny-g4", 2, 256, 8, 2, 64, 768, 1024, BF16, seed=6, cfg_index=6,
+                           batch=1, prompt_len=600, decode_len=4),
     # the 2B fp16 model under a batch / 32k-context sweep: same weights as "2b"
     "2b-32k": ModelConfig("2b-32k", 24, 2048, 16, 8, 128, 8192, 128256, F16, seed=3, cfg_index=5,
                           batch=1, prompt_len=32768, decode_len=128, batches=(1, 2, 4, 8, 16)),

@@ -1,16 +1,21 @@
 """Parity on the two largest workloads, at their full model dimensions.
 
 * 8b: the bf16 model with 32 layers, d 4096, 32/8 heads, FFN 14336 and vocab 128256.
-  A 32-token prompt goes through mk_prefill, then teacher-forced decode steps follow.
-  The workload's 8192-token prompt would take the fp64 oracle far too long; the decode
-  step is the same code at any context, and the 32k-context test below covers long
-  caches.
+  (a) A 32-token prompt goes through mk_prefill, then teacher-forced decode steps follow.
+  (b) The workload's own context: 8192 cached positions per sequence (seeded synthetic
+  keys and values, synth.gen_kv, the same bytes on both sides -- an 8192-token fp64
+  prefill of the 8b model would take the oracle hours), then two teacher-forced decode
+  steps at batch 1 and 2 under counter and sentinel sync.  With four query heads per kv
+  head and ~431 positions per split, every split runs the grouped attention instance's
+  four-pass chunks.
 * 2b at 32k context: the 2b fp16 model with 32768 cached positions per sequence, at
   batch 1, 2, 4, 8 and 16 (3..16 on the tensor-core GEMV).  The cache holds seeded synthetic keys and values (synth.gen_kv, the
   same bytes on both sides) instead of a 32k-token prefill, which the oracle cannot run
   in test time.  The oracle checks sequences 0, 1, 3, 7 and 15 one at a time.  Every sequence
   of a batch must also match that sequence at the smallest batch that holds it
-  (batch invariance).
+  (batch invariance).  The same cache is decoded by the persistent kernel with counter
+  sync (every batch), with NaN-sentinel sync and by the multi-launch control (batches 1
+  and 8); the token mk_decode_step returns is checked against the oracle's argmax.
 """
 import numpy as np
 import pytest
@@ -53,6 +58,52 @@ def test_8b_teacher_forced(lib):
     assert_parity(z, tg, zref, toks, P)
 
 
+T8K = synth.CONFIGS["8b"].prompt_len          # 8192 cached positions
+N8 = 2                                         # decode steps per sequence
+
+
+@pytest.fixture(scope="module")
+def ctx_8k(lib):
+    """Device model for two sequences with 8192 cached positions each, the teacher-forced
+    tokens, and the oracle's logits [2, N8, V] (both sequences in one oracle call per step)."""
+    cfg = synth.CONFIGS["8b"]
+    w = synth.gen_weights(cfg)
+    m = _UncachedModel(cfg, w)
+    dm = lib.DeviceModel(cfg, w, max_batch=2, max_ctx=T8K + N8 + 1)
+    cache = oracle.KVCache(cfg, 2, T8K + N8)
+    for b in range(2):
+        for l in range(cfg.n_layers):
+            kb = synth.gen_kv(cfg, l, b, 0, T8K)
+            vb = synth.gen_kv(cfg, l, b, 1, T8K)
+            dm.set_kv(l, b, kb, vb)
+            cache.k[l][b, :, :T8K] = oracle.upcast(kb, cfg.dtype)
+            cache.v[l][b, :, :T8K] = oracle.upcast(vb, cfg.dtype)
+    toks = np.stack([synth.gen_prompt(cfg, b, N8) for b in range(2)])
+    zref = np.stack([oracle.decode_step(m, cache, toks[:, t], [T8K + t] * 2) for t in range(N8)], axis=1)
+    del cache
+    return cfg, dm, toks, zref
+
+
+@pytest.mark.parametrize("sync", [0, 1], ids=["counter", "sentinel"])
+@pytest.mark.parametrize("B", [1, 2])
+def test_8b_at_8k_context(ctx_8k, lib, B, sync):
+    cfg, dm, toks, zref = ctx_8k
+    dec = lib.Decoder(dm, sync_mode=sync)
+    logits = torch.zeros((B, cfg.vocab), dtype=torch.float32, device=dm.device)
+    for t in range(N8):
+        # every run rewrites positions T8K + t of its sequences with the same values
+        got = dec.decode_step(toks[:B, t], [T8K + t] * B, logits=logits)
+        z = logits.cpu().numpy()
+        for b in range(B):
+            zr = zref[b, t]
+            scale = np.abs(zr).max()
+            err = np.abs(z[b] - zr).max()
+            assert err <= LOGIT_RTOL * scale, f"seq {b} step {t}: max |dlogit| {err:.3e}"
+            if oracle.top2_margin(zr) > LOGIT_RTOL * scale:
+                assert got[b] == int(np.argmax(zr)), f"seq {b} step {t}: token {got[b]} != {int(np.argmax(zr))}"
+    dec.close()
+
+
 T32K = synth.CONFIGS["2b-32k"].prompt_len     # 32768 cached positions
 N_STEPS = 2
 CHECKED = (0, 1, 3, 7, 15)                     # sequences the oracle decodes
@@ -84,18 +135,24 @@ def long_ctx(lib):
     return cfg, dm, toks, zref, {}
 
 
-@pytest.mark.parametrize("B", [1, 2, 4, 8, 16])
-def test_2b_32k_context_batches(long_ctx, lib, B):
+ARMS = [(B, 0, 0) for B in (1, 2, 4, 8, 16)] + [(1, 1, 0), (8, 1, 0), (1, 0, 1), (8, 0, 1)]
+
+
+@pytest.mark.parametrize("B,sync,execm", ARMS,
+                         ids=[f"B{b}-{'sentinel' if s else 'counter'}-{'multilaunch' if e else 'persistent'}"
+                              for b, s, e in ARMS])
+def test_2b_32k_context_batches(long_ctx, lib, B, sync, execm):
     cfg, dm, toks, zref, seen = long_ctx
-    dec = lib.Decoder(dm)
+    dec = lib.Decoder(dm, sync_mode=sync, exec_mode=execm)
     logits = torch.zeros((B, cfg.vocab), dtype=torch.float32, device=dm.device)
-    z = []
+    z, tk = [], []
     for t in range(N_STEPS):
-        # every batch rewrites positions T32K + t of its sequences with the same values
-        dec.decode_step(toks[:B, t], [T32K + t] * B, logits=logits)
+        # every run rewrites positions T32K + t of its sequences with the same values
+        tk.append(dec.decode_step(toks[:B, t], [T32K + t] * B, logits=logits))
         z.append(logits.cpu().numpy().copy())
     dec.close()
     z = np.stack(z, axis=1)                                   # [B, N_STEPS, V]
+    tk = np.stack(tk, axis=1)                                 # [B, N_STEPS] returned tokens
     for b in range(B):
         if b in zref:
             for t in range(N_STEPS):
@@ -104,7 +161,7 @@ def test_2b_32k_context_batches(long_ctx, lib, B):
                 err = np.abs(z[b, t] - zr).max()
                 assert err <= LOGIT_RTOL * scale, f"seq {b} step {t}: max |dlogit| {err:.3e}"
                 if oracle.top2_margin(zr) > LOGIT_RTOL * scale:
-                    assert np.argmax(z[b, t]) == np.argmax(zr), f"seq {b} step {t}: token differs"
+                    assert tk[b, t] == np.argmax(zr), f"seq {b} step {t}: token {tk[b, t]} != {np.argmax(zr)}"
         if b in seen:      # the same sequence at a smaller batch
             assert np.abs(z[b] - seen[b]).max() <= 1e-3 * np.abs(seen[b]).max(), f"seq {b}: batch variance"
         else:

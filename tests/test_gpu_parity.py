@@ -317,3 +317,23 @@ def test_tiny_batched_merge_modes(lib, tiny, merge, sync):
     z, tg = gpu_teacher_forced(dec, prompt, toks, n_new, cfg.vocab)
     dec.close()
     assert_parity(z, tg, zref, toks, P)
+
+
+@pytest.mark.parametrize("kv_splits", [2, 3])
+@pytest.mark.parametrize("sync", [0, 1], ids=["counter", "sentinel"])
+def test_tiny_g4_long_context_chunked(lib, sync, kv_splits):
+    """Four query heads per kv head (the 8b model's group) at a 600-position context with
+    few, long splits: each split's block holds more than two passes of positions, so the
+    grouped attention instance takes its four-pass chunks (and, with two splits, a second
+    block and single-pass tail)."""
+    cfg = synth.CONFIGS["tiny-g4"]
+    w = synth.gen_weights(cfg)
+    m = oracle.Model(cfg, w)
+    P, n_new = cfg.prompt_len, cfg.decode_len
+    prompt = synth.gen_prompts(cfg, 1, P)
+    toks, zref = oracle_run(cfg, w, prompt, n_new, model=m)
+    dm = lib.DeviceModel(cfg, w, max_batch=1, max_ctx=P + n_new)
+    dec = lib.Decoder(dm, sync_mode=sync, kv_splits=kv_splits)
+    z, tg = gpu_teacher_forced(dec, prompt, toks, n_new, cfg.vocab)
+    dec.close()
+    assert_parity(z, tg, zref, toks, P)
