@@ -147,14 +147,19 @@ typedef struct {
 mk_status mk_create(const mk_model_desc *desc, const mk_weights *weights, const mk_kv *kv,
                     const mk_options *opts, void *stream, mk_ctx **out);
 
-/* Prompt pass: tokens host [B, P] row-major at positions 0..P-1 of each sequence.
- * Fills KV positions 0..P-1 and returns the greedy next token of each sequence in
- * next_tok (host [B]); logits (device [B, vocab] fp32, or NULL) receives the last
- * position's logits.  Runs the decode step once per position (teacher forcing). */
+/* Prompt pass ("7 · AMD et le monokernel", §7.1: the monokernel runs prefill, decode and
+ * sampling without leaving the persistent kernel).  tokens host [B, P] row-major at
+ * positions 0..P-1 of each sequence.  Fills KV positions 0..P-1 and returns the greedy
+ * next token of each sequence in next_tok (host [B]); logits (device [B, vocab] fp32, or
+ * NULL) receives the last position's logits.  Runs the decode step once per position
+ * (teacher forcing).  Synchronous; MK_ERR_INVALID for a bad argument (nothing enqueued),
+ * a device error as for mk_decode_step. */
 mk_status mk_prefill(mk_ctx *ctx, const int32_t *tokens, int B, int P,
                      int32_t *next_tok, float *logits);
 
-/* The hot path: one decode step, ONE kernel launch.  in_tok host [B] sits at position
+/* The hot path: one decode step, ONE kernel launch ("8 · Écrire son megakernel", §8.2: every
+ * CTA walks its instruction queue -- fetch, wait for the dependency, execute, signal; §8.3:
+ * the grid is one wave, sized by the occupancy query).  in_tok host [B] sits at position
  * pos host [B] (the cache holds 0..pos[b]-1); out_tok host [B] receives the argmax
  * token (lowest index among ties); logits device [B, vocab] fp32 or NULL.  Returns once
  * out_tok holds the tokens: with logits NULL (persistent control) the last LM-head CTA
@@ -185,7 +190,11 @@ mk_status mk_synchronize(mk_ctx *ctx);
 /* Clears counters, epoch and the error word after MK_ERR_TIMEOUT / MK_ERR_STATE. */
 mk_status mk_reset(mk_ctx *ctx);
 
-/* Releases everything the context owns (never the caller's buffers).  NULL is a no-op. */
+/* Releases everything the context owns: the queues, counters, activation buffers and
+ * journal that mk_create allocated beside the launch it sized ("8 · Écrire son
+ * megakernel", §8.3, the launcher and the global state it hands the kernel).  Never the
+ * caller's weights, KV cache or logits.  Waits for the context's stream first.  NULL is a
+ * no-op; always MK_OK. */
 mk_status mk_destroy(mk_ctx *ctx);
 
 mk_status mk_info(const mk_ctx *ctx, mk_info_t *info);
@@ -241,14 +250,18 @@ mk_status mk_two_groups(const float *x, int n, int *group, float *threshold);
  * device allocation).  The pages have no counterpart to this entry point.  Same inputs
  * and outputs as mk_decode_step, passed directly (no context): desc, weights and kv as
  * for mk_create; in_tok, pos, out_tok host [B]; logits device [B, vocab] or NULL; work is
- * enqueued on `stream` (a cudaStream_t) and the call returns after it completes.
- * Every other buffer the step needs (queues, counters, activations, RoPE rows up to the
- * largest position) lives in one 16 MiB device array built into the library, which each
- * GPU that loads it holds until exit; models that need more are refused with
- * MK_ERR_INVALID.  The first call on a device (with that device current) looks the array
- * up with cudaGetSymbolAddress: make it before any stream capture.  All calls share the
- * array and keep its last contents; each call clears what must start at zero.  Calls
- * whose GPU work overlaps race on the array and must be serialised by the caller. */
+ * enqueued on `stream` (a cudaStream_t).
+ * Every other buffer the step needs (queues, counters, the activations of B sequences,
+ * one RoPE row per sequence) lives in one 16 MiB device array built into the library,
+ * which each GPU that loads it holds until exit; models and batches that need more are
+ * refused with MK_ERR_INVALID (the need depends on the model and B, not on positions).
+ * The first call on a device (with that device current) looks the array up with
+ * cudaGetSymbolAddress.  Every call is synchronous -- it waits for its step and copies
+ * the status back -- so it cannot be used inside a stream capture.  All calls share the
+ * array and keep its last contents; each call clears what must start at zero, and a call
+ * with the same descriptor, pointers and B as the previous one on that device reuses the
+ * schedule already in the array.  Calls whose GPU work overlaps race on the array and
+ * must be serialised by the caller. */
 mk_status mk_decode_step_noalloc(const mk_model_desc *desc, const mk_weights *weights, const mk_kv *kv,
                                  const int32_t *in_tok, const int32_t *pos, int B, int32_t *out_tok,
                                  float *logits, void *stream);

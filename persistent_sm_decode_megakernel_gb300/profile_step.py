@@ -41,7 +41,7 @@ def summarize(trace):
     by = {}
     per_cta_wait = {}
     groups = {}
-    keys = ("stage", "pages", "page_wait", "page_work", "epi", "epi_clk", "tail", "write", "arrive", "merge")
+    keys = ("stage", "pages", "page_wait", "page_work", "epi", "epi_cycles", "tail", "write", "arrive", "merge")
     for cta, pc, op, layer, tf, tr, te, m0, m1, m2, m3, m4, m5 in trace:
         d = by.setdefault(OPS.get(op, str(op)), {k: [] for k in ("wait", "work") + keys})
         d["wait"].append((tr - tf) / 1e3)
@@ -53,7 +53,7 @@ def summarize(trace):
             d["page_work"].append(m4 / 1e3)
             if m3:
                 d["epi"].append((m3 - m1) / 1e3)
-                d["epi_clk"].append(m5 / 2.07e3)   # cycles -> us at the 2070 MHz clock
+                d["epi_cycles"].append(m5)         # SM clock cycles (the clock varies; not converted)
                 d["tail"].append((te - m3) / 1e3)
         elif op == 3 and m0 and m1:
             d["stage"].append((m0 - tr) / 1e3)
@@ -77,7 +77,7 @@ def summarize(trace):
                          "wait_us_per_cta": sum(d["wait"]) / len(ctas)}
         for key in keys:
             if d[key]:
-                out["ops"][k][key + "_us"] = statistics.mean(d[key])
+                out["ops"][k][key if key.endswith("cycles") else key + "_us"] = statistics.mean(d[key])
     out["wait_share_mean"] = statistics.mean(v / span for v in per_cta_wait.values())
     items = sorted(groups.items(), key=lambda kv: kv[1][0])
     out["timeline_us"] = {f"L{l}:{OPS.get(o, o)}": [round((a - t0) / 1e3, 2), round((b - t0) / 1e3, 2)]
