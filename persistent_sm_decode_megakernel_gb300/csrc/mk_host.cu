@@ -96,39 +96,6 @@ struct mk_ctx {
 
 namespace {
 
-std::string check_desc(const mk_model_desc* d) {
-  if (!d) return "desc is NULL";
-  if (d->n_layers < 1 || d->d_model < 8 || d->n_heads < 1 || d->n_kv_heads < 1 || d->head_dim < 8 ||
-      d->ffn_dim < 8 || d->vocab < 2)
-    return "descriptor dimensions must be positive";
-  if (d->n_heads % d->n_kv_heads) return "n_heads must be a multiple of n_kv_heads";
-  if (d->dtype != MK_F16 && d->dtype != MK_BF16) return "dtype must be MK_F16 or MK_BF16";
-  if (d->max_batch < 1 || d->max_batch > kMaxBatch) return "max_batch must be in [1, 16]";
-  if (d->max_ctx < 1 || d->max_ctx > (1 << 22)) return "max_ctx must be in [1, 4194304]";
-  if (!(d->rms_eps > 0.f) || !(d->rope_theta > 0.f)) return "rms_eps and rope_theta must be positive";
-  if (d->d_model % 8 || d->ffn_dim % 8) return "d_model and ffn_dim must be multiples of 8";
-  return "";
-}
-
-ModelShape shape_of(const mk_model_desc* d) {
-  ModelShape m;
-  m.L = d->n_layers;
-  m.d = d->d_model;
-  m.Hq = d->n_heads;
-  m.Hkv = d->n_kv_heads;
-  m.hd = d->head_dim;
-  m.F = d->ffn_dim;
-  m.V = d->vocab;
-  m.dtype = d->dtype;
-  m.max_batch = d->max_batch;
-  m.max_ctx = d->max_ctx;
-  m.eps = d->rms_eps;
-  m.theta = d->rope_theta;
-  return m;
-}
-
-bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
-
 mk_status upload(DevBuf& b, const void* src, size_t bytes) {
   MK_CUDA(cudaMalloc(&b.p, std::max<size_t>(bytes, 16)));
   if (src && bytes) MK_CUDA(cudaMemcpy(b.p, src, bytes, cudaMemcpyHostToDevice));
@@ -397,21 +364,10 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
   *out = nullptr;
   std::string e = check_desc(desc);
   if (!e.empty()) return fail(MK_ERR_INVALID, e);
-  if (!w || !kv) return fail(MK_ERR_INVALID, "weights or kv is NULL");
+  e = check_model_pointers(desc, w, kv);  // present and 16-byte aligned (bulk copies need it)
+  if (!e.empty()) return fail(MK_ERR_INVALID, e);
   const ModelShape m = shape_of(desc);
-  // pointer checks: present and 16-byte aligned (TMA bulk copies need it)
-  if (!aligned16(w->embed) || !aligned16(w->final_norm) || !aligned16(w->lm_head))
-    return fail(MK_ERR_INVALID, "embed/final_norm/lm_head must be non-NULL and 16-byte aligned");
   const void* const* tabs[9] = {w->attn_norm, w->wq, w->wk, w->wv, w->wo, w->mlp_norm, w->w_gate, w->w_up, w->w_down};
-  for (auto t : tabs) {
-    if (!t) return fail(MK_ERR_INVALID, "a per-layer weight table is NULL");
-    for (int l = 0; l < m.L; ++l)
-      if (!aligned16(t[l])) return fail(MK_ERR_INVALID, "per-layer weight pointers must be 16-byte aligned");
-  }
-  if (!kv->k_cache || !kv->v_cache) return fail(MK_ERR_INVALID, "kv tables are NULL");
-  for (int l = 0; l < m.L; ++l)
-    if (!aligned16(kv->k_cache[l]) || !aligned16(kv->v_cache[l]))
-      return fail(MK_ERR_INVALID, "KV-cache pointers must be non-NULL and 16-byte aligned");
 
   auto ctx = std::make_unique<mk_ctx>();
   ctx->m = m;

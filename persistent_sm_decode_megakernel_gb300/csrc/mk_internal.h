@@ -134,6 +134,7 @@ struct DevState {
   uint16_t* const* kcache;
   uint16_t* const* vcache;
   const float2* rope;          // [max_ctx][hd/2] (cos, sin), computed in double on the host
+  int rope_by_seq;             // 1: rope holds one row per sequence (row b = position pos[b])
   // activations: two parity sets of act_floats each (sentinel mode alternates them)
   float* act;
   int64_t act_floats;

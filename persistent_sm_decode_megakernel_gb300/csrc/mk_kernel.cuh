@@ -269,6 +269,12 @@ __device__ __forceinline__ Attn make_attn(const DevState& S, const StepArgs& A, 
   return a;
 }
 
+// first (cos, sin) of sequence b's RoPE row: the table's row of its position, or row b of a
+// table that holds one row per sequence of the step
+__device__ __forceinline__ size_t rope_row(const DevState& S, const StepArgs& A, int b) {
+  return (size_t)(S.rope_by_seq ? b : A.pos[b]) * (size_t)(S.hd / 2);
+}
+
 __device__ __forceinline__ float* act_ptr(const DevState& S, float* act, int kind, int layer) {
   return act + S.act_off[kind] + (int64_t)layer * S.act_stride[kind];
 }
@@ -351,7 +357,7 @@ __device__ __noinline__ void producer(const DevState& S_arg, const StepArgs& A_a
         }
         if (in.op == OP_QKV && in.a[0] < 2) {
           for (int b = 0; b < A.B; ++b) {
-            const char* rp = reinterpret_cast<const char*>(S.rope + (size_t)A.pos[b] * (S.hd / 2) + in.a[2]);
+            const char* rp = reinterpret_cast<const char*>(S.rope + rope_row(S, A, b) + in.a[2]);
             for (int off = 0; off < in.a[3] * 8 + 128; off += 128) prefetch_l1(rp + off);
           }
         }
@@ -894,7 +900,7 @@ __device__ __forceinline__ void gemv_epilogue(const DevState& S, const StepArgs&
         const int i = i0 + r;
         const int pos = A.pos[b];
         if (mat < 2) {  // rotate-half RoPE on the pair (i, i + hd/2)
-          const float2 cs = t == tid ? cs0 : S.rope[(size_t)pos * half + i];
+          const float2 cs = t == tid ? cs0 : S.rope[rope_row(S, A, b) + i];
           const float xa = va * cs.x - vb * cs.y;
           const float xb = vb * cs.x + va * cs.y;
           va = xa;
@@ -1031,7 +1037,7 @@ __device__ __noinline__ void op_gemv(const DevState& S_arg, const StepArgs& A_ar
   // by the epilogue after the barrier that ends the pages)
   float2 cs0 = make_float2(1.f, 0.f);
   if (in.op == OP_QKV && in.a[0] < 2 && tid < in.a[3] * B)
-    cs0 = S.rope[(size_t)A.pos[tid / in.a[3]] * (S.hd / 2) + in.a[2] + tid % in.a[3]];
+    cs0 = S.rope[rope_row(S, A, tid / in.a[3]) + in.a[2] + tid % in.a[3]];
   if ((in.op == OP_QKV || in.op == OP_UPGATE || in.op == OP_LMHEAD) && tid < B) c->inv_rms[tid] = inv_rms_of<NB>(S, c, tid);
 
   // 2. stream the slices: warp w takes slice i0 + w of every page of 8 slices
@@ -1166,7 +1172,7 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
   }
   float2 cs0 = make_float2(1.f, 0.f);
   if (in.op == OP_QKV && in.a[0] < 2 && tid < in.a[3] * B)
-    cs0 = S.rope[(size_t)A.pos[tid / in.a[3]] * (S.hd / 2) + in.a[2] + tid % in.a[3]];
+    cs0 = S.rope[rope_row(S, A, tid / in.a[3]) + in.a[2] + tid % in.a[3]];
   float ss[NB];
 #pragma unroll
   for (int b = 0; b < NB; ++b) ss[b] = 0.f;

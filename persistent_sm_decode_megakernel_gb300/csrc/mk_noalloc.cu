@@ -8,16 +8,22 @@
 // step needs beyond the caller's own inputs and outputs lives in one file-scope device
 // array of kScratchBytes, which each GPU that loads the library holds until the process
 // exits.  The step kernel is the same persistent kernel mk_decode_step launches (counter
-// synchronisation); only where its scratch lives differs.
+// synchronisation, the same schedule builder); only where its scratch lives differs.
 //
 // Rules of use:
 //   * The first call on a device (with that device current) looks up the array's device
-//     address with cudaGetSymbolAddress; make that first call before any stream capture.
+//     address with cudaGetSymbolAddress.  Every call is synchronous: it waits for its
+//     step and reads the status back with a device-to-host copy, so it cannot be
+//     enqueued inside a stream capture.
 //   * All calls share the one array and leave their contents in it; every call clears
 //     what must start at zero (counters, error word, argmax keys).  Calls whose GPU work
 //     overlaps (two streams, two host threads) race on the array: serialise them.
-//   * Models whose queues + activations + RoPE table exceed kScratchBytes are refused
-//     with MK_ERR_INVALID and a message giving both sizes.
+//   * The array holds the schedule, the counters, the activations of B sequences and one
+//     RoPE row per sequence: its size depends on the model and the batch, not on the
+//     positions.  Models whose needs exceed kScratchBytes are refused with MK_ERR_INVALID
+//     and a message giving both sizes.
+//   * The schedule of the last call on a device stays in the array: a call with the same
+//     descriptor, weight and cache pointers and batch reuses it (no rebuild, no upload).
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -45,8 +51,18 @@ constexpr int kMaxDevices = 64;
 // device address comes from cudaGetSymbolAddress below, never from taking its address.
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
+// What the array of a device holds after a successful call: the schedule of `key`.
+struct Prepared {
+  bool valid = false;
+  std::vector<uintptr_t> key;
+  mk::DevState S{};
+  int n_cta = 0, smem = 0, n_counters = 0;
+  size_t o_ctl = 0, o_keys = 0, o_ctr = 0, o_rope = 0, o_q = 0, o_ins = 0;
+};
+
 std::mutex g_mu;
 void* g_scratch_dev[kMaxDevices] = {};
+Prepared g_prep[kMaxDevices];
 
 mk_status fail(mk_status s, const std::string& m) {
   mk::set_last_error(m);
@@ -60,7 +76,6 @@ mk_status fail(mk_status s, const std::string& m) {
   } while (0)
 
 mk_status scratch_address(int dev, unsigned char** out) {
-  std::lock_guard<std::mutex> lk(g_mu);
   if (dev < 0 || dev >= kMaxDevices) return fail(MK_ERR_INVALID, "device index out of range");
   if (!g_scratch_dev[dev]) {
     void* p = nullptr;
@@ -73,61 +88,49 @@ mk_status scratch_address(int dev, unsigned char** out) {
   return MK_OK;
 }
 
-bool al16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
-
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
-}  // namespace
-
-extern "C" mk_status mk_decode_step_noalloc(const mk_model_desc* desc, const mk_weights* w, const mk_kv* kv,
-                                            const int32_t* in_tok, const int32_t* pos, int B, int32_t* out_tok,
-                                            float* logits, void* stream) {
-  using namespace mk;
-  if (!desc || !w || !kv || !in_tok || !pos || !out_tok) return fail(MK_ERR_INVALID, "NULL argument");
-  const mk_model_desc& d = *desc;
-  if (d.n_layers < 1 || d.d_model < 8 || d.n_heads < 1 || d.n_kv_heads < 1 || d.head_dim < 8 || d.ffn_dim < 8 ||
-      d.vocab < 2 || d.n_heads % d.n_kv_heads || (d.dtype != MK_F16 && d.dtype != MK_BF16) || d.max_batch < 1 ||
-      d.max_batch > kMaxBatch || d.max_ctx < 1 || d.d_model % 8 || d.ffn_dim % 8 || !(d.rms_eps > 0.f) ||
-      !(d.rope_theta > 0.f))
-    return fail(MK_ERR_INVALID, "invalid model descriptor");
-  if (B < 1 || B > d.max_batch) return fail(MK_ERR_INVALID, "B out of range");
-  for (int b = 0; b < B; ++b) {
-    if (in_tok[b] < 0 || in_tok[b] >= d.vocab) return fail(MK_ERR_INVALID, "token id out of range");
-    if (pos[b] < 0 || pos[b] >= d.max_ctx) return fail(MK_ERR_INVALID, "position out of range");
-  }
-  const int L = d.n_layers;
-  if (!al16(w->embed) || !al16(w->final_norm) || !al16(w->lm_head) || !kv->k_cache || !kv->v_cache)
-    return fail(MK_ERR_INVALID, "weight/KV pointers must be non-NULL and 16-byte aligned");
+// everything the schedule and the device state of a call depend on
+std::vector<uintptr_t> key_of(const mk_model_desc& d, const mk_weights* w, const mk_kv* kv, int B, int n_sm,
+                              int smem_optin) {
+  std::vector<uintptr_t> k;
+  const int iv[] = {d.n_layers, d.d_model, d.n_heads, d.n_kv_heads, d.head_dim, d.ffn_dim, d.vocab, d.dtype,
+                    d.max_batch, d.max_ctx, B, n_sm, smem_optin};
+  for (int v : iv) k.push_back((uintptr_t)(uint32_t)v);
+  uint32_t fb[2];
+  std::memcpy(&fb[0], &d.rms_eps, 4);
+  std::memcpy(&fb[1], &d.rope_theta, 4);
+  k.push_back(fb[0]);
+  k.push_back(fb[1]);
+  k.push_back((uintptr_t)w->embed);
+  k.push_back((uintptr_t)w->final_norm);
+  k.push_back((uintptr_t)w->lm_head);
   const void* const* tabs[9] = {w->attn_norm, w->wq, w->wk, w->wv, w->wo, w->mlp_norm, w->w_gate, w->w_up, w->w_down};
-  for (auto t : tabs) {
-    if (!t) return fail(MK_ERR_INVALID, "a per-layer weight table is NULL");
-    for (int l = 0; l < L; ++l)
-      if (!al16(t[l])) return fail(MK_ERR_INVALID, "weight pointers must be 16-byte aligned");
+  for (auto t : tabs)
+    for (int l = 0; l < d.n_layers; ++l) k.push_back((uintptr_t)t[l]);
+  for (int l = 0; l < d.n_layers; ++l) {
+    k.push_back((uintptr_t)kv->k_cache[l]);
+    k.push_back((uintptr_t)kv->v_cache[l]);
   }
-  for (int l = 0; l < L; ++l)
-    if (!al16(kv->k_cache[l]) || !al16(kv->v_cache[l])) return fail(MK_ERR_INVALID, "KV pointers must be aligned");
+  return k;
+}
 
-  ModelShape m;
-  m.L = L; m.d = d.d_model; m.Hq = d.n_heads; m.Hkv = d.n_kv_heads; m.hd = d.head_dim; m.F = d.ffn_dim;
-  m.V = d.vocab; m.dtype = d.dtype; m.max_batch = d.max_batch; m.max_ctx = d.max_ctx; m.eps = d.rms_eps;
-  m.theta = d.rope_theta;
-
-  // grid: one wave, as for mk_create
-  int dev = 0, n_sm = 0, smem_optin = 0, bpsm = 0;
-  NA_CUDA(cudaGetDevice(&dev));
-  unsigned char* base = nullptr;
-  mk_status st = scratch_address(dev, &base);
-  if (st) return st;
-  NA_CUDA(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
-  NA_CUDA(cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+// Builds, validates and uploads the schedule of one call into the array (stream-ordered),
+// and fills P with the device state that points into it.
+mk_status prepare(const mk_model_desc& d, const mk_weights* w, const mk_kv* kv, int B, int n_sm, int smem_optin,
+                  unsigned char* base, cudaStream_t s, Prepared* P) {
+  using namespace mk;
+  const ModelShape m = shape_of(&d);
+  const int L = m.L;
   Geometry g;
   std::string e = make_geometry(m, n_sm, 0, 0, 0, smem_optin, &g);
   if (!e.empty()) return fail(MK_ERR_INVALID, e);
   const void* fn = step_kernel_entry(m.dtype, MK_SYNC_COUNTER, false);
   NA_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_bytes));
+  int bpsm = 0;
   NA_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bpsm, fn, kThreads, g.smem_bytes));
   if (bpsm < 1) return fail(MK_ERR_OCCUPANCY, "the kernel does not fit on an SM");
-  const int n_cta = n_sm * bpsm;
+  const int n_cta = n_sm * bpsm;  // one wave, as for mk_create
   if (n_cta != n_sm) {
     e = make_geometry(m, n_cta, 0, 0, 0, smem_optin, &g);
     if (!e.empty()) return fail(MK_ERR_INVALID, e);
@@ -138,6 +141,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_desc* desc, const mk_
   ModelPtrs mp;
   mp.final_norm = w->final_norm;
   mp.lm_head = w->lm_head;
+  const void* const* tabs[9] = {w->attn_norm, w->wq, w->wk, w->wv, w->wo, w->mlp_norm, w->w_gate, w->w_up, w->w_down};
   std::vector<const void*>* dst[9] = {&mp.attn_norm, &mp.wq, &mp.wk, &mp.wv, &mp.wo,
                                       &mp.mlp_norm, &mp.w_gate, &mp.w_up, &mp.w_down};
   for (int k = 0; k < 9; ++k) dst[k]->assign(tabs[k], tabs[k] + L);
@@ -160,17 +164,6 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_desc* desc, const mk_
     for (int l = 0; l < L; ++l) ptrs.push_back(t[l]);
   for (int l = 0; l < L; ++l) ptrs.push_back(kv->k_cache[l]);
   for (int l = 0; l < L; ++l) ptrs.push_back(kv->v_cache[l]);
-  int max_pos = 0;
-  for (int b = 0; b < B; ++b) max_pos = pos[b] > max_pos ? pos[b] : max_pos;
-  const int half = m.hd / 2, rope_rows = max_pos + 1;
-  std::vector<float> rope((size_t)rope_rows * half * 2);
-  for (int i = 0; i < half; ++i) {
-    const double f = std::pow((double)m.theta, -2.0 * i / m.hd);
-    for (int t = 0; t < rope_rows; ++t) {
-      rope[((size_t)t * half + i) * 2] = (float)std::cos((double)t * f);
-      rope[((size_t)t * half + i) * 2 + 1] = (float)std::sin((double)t * f);
-    }
-  }
 
   // activation arena (one set: counter synchronisation needs no second parity)
   DevState S{};
@@ -192,20 +185,20 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_desc* desc, const mk_
   }
   S.act_floats = (off + 31) / 32 * 32;
 
-  // carve the scratch
+  // carve the array
   size_t cur = 0;
   auto take = [&](size_t bytes) {
     const size_t at = cur;
     cur = up256(cur + bytes);
     return at;
   };
-  const size_t o_ctl = take(sizeof(Ctl));
-  const size_t o_keys = take(sizeof(unsigned long long) * 2 * kMaxBatch);
-  const size_t o_ctr = take(sizeof(uint32_t) * (size_t)plan.n_counters);
+  P->o_ctl = take(sizeof(Ctl));
+  P->o_keys = take(sizeof(unsigned long long) * 2 * kMaxBatch);
+  P->o_ctr = take(sizeof(uint32_t) * (size_t)plan.n_counters);
   const size_t o_ptr = take(sizeof(void*) * ptrs.size());
-  const size_t o_rope = take(sizeof(float) * rope.size());
-  const size_t o_q = take(sizeof(int32_t) * qoff.size());
-  const size_t o_ins = take(sizeof(Instr) * flat.size());
+  P->o_rope = take(sizeof(float2) * (size_t)kMaxBatch * (m.hd / 2));
+  P->o_q = take(sizeof(int32_t) * qoff.size());
+  P->o_ins = take(sizeof(Instr) * flat.size());
   const size_t o_act = take(sizeof(float) * (size_t)S.act_floats);
   if (cur > kScratchBytes) {
     char buf[200];
@@ -213,15 +206,10 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_desc* desc, const mk_
              kScratchBytes);
     return fail(MK_ERR_INVALID, buf);
   }
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // inputs of this call (the array still holds the previous call's contents)
-  NA_CUDA(cudaMemsetAsync(base + o_ctl, 0, sizeof(Ctl), s));
-  NA_CUDA(cudaMemsetAsync(base + o_keys, 0, sizeof(unsigned long long) * 2 * kMaxBatch, s));
-  NA_CUDA(cudaMemsetAsync(base + o_ctr, 0, sizeof(uint32_t) * (size_t)plan.n_counters, s));
   NA_CUDA(cudaMemcpyAsync(base + o_ptr, ptrs.data(), sizeof(void*) * ptrs.size(), cudaMemcpyHostToDevice, s));
-  NA_CUDA(cudaMemcpyAsync(base + o_rope, rope.data(), sizeof(float) * rope.size(), cudaMemcpyHostToDevice, s));
-  NA_CUDA(cudaMemcpyAsync(base + o_q, qoff.data(), sizeof(int32_t) * qoff.size(), cudaMemcpyHostToDevice, s));
-  NA_CUDA(cudaMemcpyAsync(base + o_ins, flat.data(), sizeof(Instr) * flat.size(), cudaMemcpyHostToDevice, s));
+  NA_CUDA(cudaMemcpyAsync(base + P->o_q, qoff.data(), sizeof(int32_t) * qoff.size(), cudaMemcpyHostToDevice, s));
+  NA_CUDA(cudaMemcpyAsync(base + P->o_ins, flat.data(), sizeof(Instr) * flat.size(), cudaMemcpyHostToDevice, s));
+  // the pageable copies above return once their source is consumed: the host vectors may go
 
   S.L = L; S.d = m.d; S.Hq = m.Hq; S.Hkv = m.Hkv; S.hd = m.hd; S.F = m.F; S.V = m.V; S.dtype = m.dtype;
   S.max_batch = B;  // the arena holds B rows
@@ -236,12 +224,13 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_desc* desc, const mk_
   S.mlp_norm = pt + 5 * L; S.w_gate = pt + 6 * L; S.w_up = pt + 7 * L; S.w_down = pt + 8 * L;
   S.kcache = mpt + 9 * L;
   S.vcache = mpt + 10 * L;
-  S.rope = reinterpret_cast<const float2*>(base + o_rope);
+  S.rope = reinterpret_cast<const float2*>(base + P->o_rope);
+  S.rope_by_seq = 1;  // row b holds sequence b's position
   S.act = reinterpret_cast<float*>(base + o_act);
-  S.argkeys = reinterpret_cast<unsigned long long*>(base + o_keys);
-  S.counters = reinterpret_cast<uint32_t*>(base + o_ctr);
+  S.argkeys = reinterpret_cast<unsigned long long*>(base + P->o_keys);
+  S.counters = reinterpret_cast<uint32_t*>(base + P->o_ctr);
   S.n_counters = plan.n_counters;
-  S.ctl = reinterpret_cast<Ctl*>(base + o_ctl);
+  S.ctl = reinterpret_cast<Ctl*>(base + P->o_ctl);
   S.n_cta = n_cta;
   S.page_bytes = g.page_bytes;
   S.n_pages = g.n_pages;
@@ -254,11 +243,65 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_desc* desc, const mk_
   S.backoff_max_ns = 256;
   S.split_min_positions = 16;
   S.inflight_pages = 2;
-  // the kernel's kv-cache addressing uses the caller's layout [max_batch, Hkv, max_ctx, hd]
-  // only through max_ctx, and its activation rows through max_batch: both as set above
+  P->S = S;
+  P->n_cta = n_cta;
+  P->smem = g.smem_bytes;
+  P->n_counters = plan.n_counters;
+  return MK_OK;
+}
+
+}  // namespace
+
+extern "C" mk_status mk_decode_step_noalloc(const mk_model_desc* desc, const mk_weights* w, const mk_kv* kv,
+                                            const int32_t* in_tok, const int32_t* pos, int B, int32_t* out_tok,
+                                            float* logits, void* stream) {
+  using namespace mk;
+  if (!in_tok || !pos || !out_tok) return fail(MK_ERR_INVALID, "NULL argument");
+  std::string e = check_desc(desc);  // the same checks as mk_create
+  if (!e.empty()) return fail(MK_ERR_INVALID, e);
+  e = check_model_pointers(desc, w, kv);
+  if (!e.empty()) return fail(MK_ERR_INVALID, e);
+  const mk_model_desc& d = *desc;
+  if (B < 1 || B > d.max_batch) return fail(MK_ERR_INVALID, "B out of range");
+  if (d.head_dim != 64 && d.head_dim != 128) return fail(MK_ERR_INVALID, "head_dim must be 64 or 128");
+  for (int b = 0; b < B; ++b) {
+    if (in_tok[b] < 0 || in_tok[b] >= d.vocab) return fail(MK_ERR_INVALID, "token id out of range");
+    if (pos[b] < 0 || pos[b] >= d.max_ctx) return fail(MK_ERR_INVALID, "position out of range");
+  }
+  int dev = 0, n_sm = 0, smem_optin = 0;
+  NA_CUDA(cudaGetDevice(&dev));
+  NA_CUDA(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
+  NA_CUDA(cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  std::lock_guard<std::mutex> lk(g_mu);
+  unsigned char* base = nullptr;
+  mk_status st = scratch_address(dev, &base);
+  if (st) return st;
+  Prepared& P = g_prep[dev];
+  std::vector<uintptr_t> key = key_of(d, w, kv, B, n_sm, smem_optin);
+  if (!P.valid || P.key != key) {
+    P.valid = false;  // the array's schedule is about to change
+    st = prepare(d, w, kv, B, n_sm, smem_optin, base, s, &P);
+    if (st) return st;
+    P.key = std::move(key);
+  }
+  const int half = d.head_dim / 2;
+  float2 rope[kMaxBatch * 64];  // one RoPE row per sequence: angle pos[b] * theta^(-2i/hd), in double
+  for (int b = 0; b < B; ++b)
+    for (int i = 0; i < half; ++i) {
+      const double a = (double)pos[b] * std::pow((double)d.rope_theta, -2.0 * i / d.head_dim);
+      rope[b * half + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+    }
+  // this call's inputs (the array still holds the previous call's contents)
+  NA_CUDA(cudaMemsetAsync(base + P.o_ctl, 0, sizeof(Ctl), s));
+  NA_CUDA(cudaMemsetAsync(base + P.o_keys, 0, sizeof(unsigned long long) * 2 * kMaxBatch, s));
+  NA_CUDA(cudaMemsetAsync(base + P.o_ctr, 0, sizeof(uint32_t) * (size_t)P.n_counters, s));
+  NA_CUDA(cudaMemcpyAsync(base + P.o_rope, rope, sizeof(float2) * (size_t)B * half, cudaMemcpyHostToDevice, s));
+
   StepArgs A{};
-  A.instr = reinterpret_cast<const Instr*>(base + o_ins);
-  A.q_start = reinterpret_cast<const int32_t*>(base + o_q);
+  A.instr = reinterpret_cast<const Instr*>(base + P.o_ins);
+  A.q_start = reinterpret_cast<const int32_t*>(base + P.o_q);
   A.epoch = 0;
   A.step = 0;
   A.B = B;
@@ -269,11 +312,13 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_desc* desc, const mk_
   }
   A.logits = logits;
   A.tok_hist = nullptr;
-
+  DevState S = P.S;
+  const void* fn = step_kernel_entry(d.dtype, MK_SYNC_COUNTER, false);
+  NA_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, P.smem));
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(n_cta);
+  cfg.gridDim = dim3(P.n_cta);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = g.smem_bytes;
+  cfg.dynamicSmemBytes = P.smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -283,8 +328,9 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_desc* desc, const mk_
   void* args[2] = {&S, &A};
   NA_CUDA(cudaLaunchKernelExC(&cfg, fn, args));
   Ctl hc;
-  NA_CUDA(cudaMemcpyAsync(&hc, base + o_ctl, sizeof(Ctl), cudaMemcpyDeviceToHost, s));
+  NA_CUDA(cudaMemcpyAsync(&hc, base + P.o_ctl, sizeof(Ctl), cudaMemcpyDeviceToHost, s));
   NA_CUDA(cudaStreamSynchronize(s));
+  P.valid = true;
   if (hc.err.code) {
     char buf[160];
     snprintf(buf, sizeof buf, "device error %u at cta %d pc %d counter %d", hc.err.code, hc.err.cta, hc.err.pc,

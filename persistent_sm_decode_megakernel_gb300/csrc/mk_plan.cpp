@@ -39,6 +39,56 @@ static std::string fmt(const char* f, long long a = 0, long long b = 0, long lon
   return buf;
 }
 
+std::string check_desc(const mk_model_desc* d) {
+  if (!d) return "desc is NULL";
+  if (d->n_layers < 1 || d->d_model < 8 || d->n_heads < 1 || d->n_kv_heads < 1 || d->head_dim < 8 ||
+      d->ffn_dim < 8 || d->vocab < 2)
+    return "descriptor dimensions must be positive";
+  if (d->n_heads % d->n_kv_heads) return "n_heads must be a multiple of n_kv_heads";
+  if (d->dtype != MK_F16 && d->dtype != MK_BF16) return "dtype must be MK_F16 or MK_BF16";
+  if (d->max_batch < 1 || d->max_batch > kMaxBatch) return "max_batch must be in [1, 16]";
+  if (d->max_ctx < 1 || d->max_ctx > (1 << 22)) return "max_ctx must be in [1, 4194304]";
+  if (!(d->rms_eps > 0.f) || !(d->rope_theta > 0.f)) return "rms_eps and rope_theta must be positive";
+  if (d->d_model % 8 || d->ffn_dim % 8) return "d_model and ffn_dim must be multiples of 8";
+  return "";
+}
+
+static bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+std::string check_model_pointers(const mk_model_desc* d, const mk_weights* w, const mk_kv* kv) {
+  if (!w || !kv) return "weights or kv is NULL";
+  if (!aligned16(w->embed) || !aligned16(w->final_norm) || !aligned16(w->lm_head))
+    return "embed/final_norm/lm_head must be non-NULL and 16-byte aligned";
+  const void* const* tabs[9] = {w->attn_norm, w->wq, w->wk, w->wv, w->wo, w->mlp_norm, w->w_gate, w->w_up, w->w_down};
+  for (auto t : tabs) {
+    if (!t) return "a per-layer weight table is NULL";
+    for (int l = 0; l < d->n_layers; ++l)
+      if (!aligned16(t[l])) return "per-layer weight pointers must be 16-byte aligned";
+  }
+  if (!kv->k_cache || !kv->v_cache) return "kv tables are NULL";
+  for (int l = 0; l < d->n_layers; ++l)
+    if (!aligned16(kv->k_cache[l]) || !aligned16(kv->v_cache[l]))
+      return "KV-cache pointers must be non-NULL and 16-byte aligned";
+  return "";
+}
+
+ModelShape shape_of(const mk_model_desc* d) {
+  ModelShape m;
+  m.L = d->n_layers;
+  m.d = d->d_model;
+  m.Hq = d->n_heads;
+  m.Hkv = d->n_kv_heads;
+  m.hd = d->head_dim;
+  m.F = d->ffn_dim;
+  m.V = d->vocab;
+  m.dtype = d->dtype;
+  m.max_batch = d->max_batch;
+  m.max_ctx = d->max_ctx;
+  m.eps = d->rms_eps;
+  m.theta = d->rope_theta;
+  return m;
+}
+
 std::string make_geometry(const ModelShape& m, int n_cta, int page_bytes, int n_pages_req, int kv_splits,
                           int smem_limit, Geometry* g) {
   *g = Geometry();

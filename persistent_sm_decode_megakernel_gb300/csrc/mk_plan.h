@@ -7,6 +7,7 @@
 #include <string>
 #include <vector>
 
+#include "../../include/mk.h"
 #include "mk_internal.h"
 
 namespace mk {
@@ -50,6 +51,13 @@ struct ModelPtrs {
   const void* lm_head = nullptr;
   std::vector<const void*> attn_norm, wq, wk, wv, wo, mlp_norm, w_gate, w_up, w_down, kcache, vcache;
 };
+
+// The checks every entry point that takes a model descriptor applies (mk_create, mk_plan and
+// the allocation-free step): "" when the descriptor is usable, else the reason.
+std::string check_desc(const mk_model_desc* d);
+// weights and KV tables: every pointer present and 16-byte aligned (bulk copies need it)
+std::string check_model_pointers(const mk_model_desc* d, const mk_weights* w, const mk_kv* kv);
+ModelShape shape_of(const mk_model_desc* d);
 
 // returns "" on success, else a message
 std::string make_geometry(const ModelShape& m, int n_cta, int page_bytes, int n_pages_req, int kv_splits,
