@@ -68,6 +68,19 @@ namespace mk {
 void set_last_error(const std::string& msg) { g_last_error = msg; }
 }  // namespace mk
 
+// Prompt chunks (mk_prefill): up to kMaxBatch rows per launch -- consecutive positions of
+// each prompt -- run through the same kernel with the tensor-core geometry, schedules of
+// their own and an activation arena of kMaxBatch rows (kept apart from the decode arena, so
+// that a decode step's NaN refill does not grow with the chunk size).
+struct PrefillState {
+  bool ready = false;
+  ModelShape m{};     // the model with max_batch = kMaxBatch (schedules of up to 16 rows)
+  Geometry geo{};
+  DevState st{};      // the context's state with this geometry and the chunk arena
+  DevBuf act, logits; // arena [2 parities]; logits of the last chunk's rows [kMaxBatch][V]
+  std::map<int, std::unique_ptr<Sched>> scheds;
+};
+
 struct mk_ctx {
   ModelShape m{};
   mk_options opts{};
@@ -88,6 +101,8 @@ struct mk_ctx {
   uint32_t step = 0;
   bool broken = false;
   int last_B = 1;
+  PrefillState pf;
+  const void* last_arena = nullptr;  // activation arena of the last launch (NaN sentinels)
   ~mk_ctx() {
     if (host_ctl) cudaFreeHost(host_ctl);
     if (mail) cudaFreeHost(mail);
@@ -116,9 +131,10 @@ mk_status upload_queues(const std::vector<std::vector<Instr>>& qs, DevBuf& ibuf,
   return upload(qbuf, qs_off.data(), qs_off.size() * sizeof(int32_t));
 }
 
-mk_status get_sched(mk_ctx* ctx, int B, Sched** out) {
-  auto it = ctx->scheds.find(B);
-  if (it != ctx->scheds.end()) {
+mk_status get_sched_in(mk_ctx* ctx, const ModelShape& m, const Geometry& geo,
+                       std::map<int, std::unique_ptr<Sched>>& scheds, int B, Sched** out) {
+  auto it = scheds.find(B);
+  if (it != scheds.end()) {
     *out = it->second.get();
     return MK_OK;
   }
@@ -126,12 +142,12 @@ mk_status get_sched(mk_ctx* ctx, int B, Sched** out) {
   // small batches merge the KV splits inside the O-proj staging; otherwise counter mode
   // merges them in the last-arriving split and sentinel mode keeps the separate
   // ATTN_REDUCE op (it has no atomics to elect a last arriver)
-  const int merge = choose_merge(ctx->m, ctx->geo, B, ctx->opts.sync_mode == MK_SYNC_COUNTER, ctx->opts.attn_merge);
-  std::string e = build_plan(ctx->m, ctx->geo, ctx->n_cta, B, ctx->opts.fault_drop_signal, merge, &sc->plan);
+  const int merge = choose_merge(m, geo, B, ctx->opts.sync_mode == MK_SYNC_COUNTER, ctx->opts.attn_merge);
+  std::string e = build_plan(m, geo, ctx->n_cta, B, ctx->opts.fault_drop_signal, merge, &sc->plan);
   if (!e.empty()) return fail(MK_ERR_INVALID, "schedule: " + e);
-  bake_pointers(ctx->m, ctx->ptrs, &sc->plan);
+  bake_pointers(m, ctx->ptrs, &sc->plan);
   if (ctx->opts.fault_drop_signal <= 0) {
-    e = validate_plan(ctx->m, ctx->geo, sc->plan);
+    e = validate_plan(m, geo, sc->plan);
     if (!e.empty()) return fail(MK_ERR_INVALID, "schedule rejected by the validator: " + e);
   }
   mk_status s = upload_queues(sc->plan.queues, sc->instr, sc->qstart, &sc->n_instr);
@@ -159,16 +175,18 @@ mk_status get_sched(mk_ctx* ctx, int B, Sched** out) {
     }
   }
   *out = sc.get();
-  ctx->scheds[B] = std::move(sc);
+  scheds[B] = std::move(sc);
   return MK_OK;
 }
+
+mk_status get_sched(mk_ctx* ctx, int B, Sched** out) { return get_sched_in(ctx, ctx->m, ctx->geo, ctx->scheds, B, out); }
 
 mk_status launch(mk_ctx* ctx, const void* fn, const DevState& S, const StepArgs& A, bool cooperative,
                  bool programmatic = false, cudaStream_t stream = nullptr, bool own_stream = false) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(ctx->n_cta);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = ctx->geo.smem_bytes;
+  cfg.dynamicSmemBytes = S.smem_bytes;
   cfg.stream = own_stream ? stream : ctx->stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -235,8 +253,17 @@ mk_status run_graph(mk_ctx* ctx, Sched* sc, const DevState& S, const StepArgs& A
 // enqueue one decode step (one launch, or the multi-launch control's per-op launches); with
 // persistent control, n_steps > 1 greedy steps in the one launch (tok_hist then [n_steps][B])
 mk_status enqueue_step(mk_ctx* ctx, Sched* sc, int B, const int32_t* tok, const int32_t* pos, bool tok_from_dev,
-                       float* logits, int32_t* tok_hist, int n_steps = 1, uint32_t mail_seq = 0) {
-  DevState S = ctx->st;
+                       float* logits, int32_t* tok_hist, int n_steps = 1, uint32_t mail_seq = 0,
+                       const DevState* base = nullptr, const int32_t* seq = nullptr, const int32_t* p0 = nullptr) {
+  DevState S = base ? *base : ctx->st;
+  S.trace = ctx->st.trace;
+  S.trace_cap = ctx->st.trace_cap;
+  // NaN sentinels: a launch expects its arena's current parity to hold sentinels, which the
+  // launch before it on the same arena left behind; after a switch of arenas, refill both
+  if (ctx->opts.sync_mode == MK_SYNC_SENTINEL && ctx->last_arena != S.act) {
+    if (ctx->last_arena) MK_CUDA(cudaMemsetAsync(S.act, 0xFF, sizeof(float) * 2 * S.act_floats, ctx->stream));
+    ctx->last_arena = S.act;
+  }
   S.counters = reinterpret_cast<uint32_t*>(sc->counters.p);
   S.n_counters = sc->plan.n_counters;
   StepArgs A{};
@@ -247,6 +274,16 @@ mk_status enqueue_step(mk_ctx* ctx, Sched* sc, int B, const int32_t* tok, const 
   for (int b = 0; b < B; ++b) {
     A.tok[b] = tok ? tok[b] : 0;
     A.pos[b] = pos[b];
+    A.seq[b] = seq ? seq[b] : b;
+    A.p0[b] = p0 ? p0[b] : pos[b];
+    // the kernel reads this launch's positions p0..pos of row b from rows b - (pos - p0) .. b:
+    // they must exist and hold that sequence's consecutive positions
+    const int n_new = A.pos[b] - A.p0[b] + 1;
+    if (n_new < 1 || n_new > b + 1 || A.seq[b] < 0 || A.seq[b] >= ctx->m.max_batch)
+      return fail(MK_ERR_INVALID, "step rows: bad sequence or first new position");
+    for (int i = 1; i < n_new; ++i)
+      if (A.seq[b - i] != A.seq[b] || A.pos[b - i] != A.pos[b] - i)
+        return fail(MK_ERR_INVALID, "step rows: a chunk's rows must be consecutive positions of one sequence");
   }
   A.logits = logits;
   A.tok_hist = tok_hist;
@@ -294,6 +331,34 @@ mk_status read_status(mk_ctx* ctx) {
     return fail((mk_status)e.code, buf);
   }
   if (ctx->host_ctl->nan_seen) return fail(MK_ERR_NAN, "a logit was NaN");
+  return MK_OK;
+}
+
+// The prompt-chunk state, allocated at the first chunked mk_prefill: the context's device
+// state with the chunk geometry, an arena of kMaxBatch rows (NaN-filled) and the logits of
+// the last chunk's rows.
+mk_status ensure_prefill(mk_ctx* ctx) {
+  PrefillState& pf = ctx->pf;
+  if (pf.ready) return MK_OK;
+  const Geometry& g = pf.geo;
+  DevState S = ctx->st;
+  S.S = g.S;
+  S.ws_qkv = g.ws_qkv; S.ws_o = g.ws_o; S.ws_up = g.ws_up; S.ws_down = g.ws_down; S.ws_lm = g.ws_lm;
+  S.page_bytes = g.page_bytes;
+  S.n_pages = g.n_pages;
+  S.page_stride = g.page_stride;
+  S.tc = g.tc;
+  S.xbuf_bytes = g.xbuf_bytes;
+  S.scratch_bytes = g.scratch_bytes;
+  S.smem_bytes = g.smem_bytes;
+  S.max_batch = kMaxBatch;
+  arena_layout(pf.m, g, kMaxBatch, &S);
+  MK_CUDA(cudaMalloc(&pf.act.p, sizeof(float) * 2 * S.act_floats));
+  MK_CUDA(cudaMemset(pf.act.p, 0xFF, sizeof(float) * 2 * S.act_floats));  // all NaN
+  S.act = reinterpret_cast<float*>(pf.act.p);
+  MK_CUDA(cudaMalloc(&pf.logits.p, sizeof(float) * (size_t)kMaxBatch * ctx->m.V));
+  pf.st = S;
+  pf.ready = true;
   return MK_OK;
 }
 
@@ -392,7 +457,9 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
   ctx->kernel = step_kernel_entry(m.dtype, o.sync_mode, false);
   ctx->kernel_ms = step_kernel_entry(m.dtype, o.sync_mode, true);
   for (const void* fn : {ctx->kernel, ctx->kernel_ms})
-    MK_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ctx->geo.smem_bytes));
+    // the attribute is per function (shared by every context in the process): the device's
+    // limit, so that no context's launch is refused after another context sets a lower one
+    MK_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin));
   MK_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ctx->bpsm, ctx->kernel, kThreads, ctx->geo.smem_bytes));
   if (ctx->bpsm < 1) return fail(MK_ERR_OCCUPANCY, "the kernel does not fit on an SM (blocks per SM < 1)");
   ctx->n_cta = ctx->n_sm * ctx->bpsm;
@@ -402,6 +469,19 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
     if (!e.empty()) return fail(MK_ERR_INVALID, e);
   }
   const Geometry& g = ctx->geo;
+  {  // prompt chunks: the tensor-core geometry of kMaxBatch rows, if it fits the same wave
+    PrefillState& pf = ctx->pf;
+    pf.m = m;
+    pf.m.max_batch = kMaxBatch;
+    if (o.exec_mode == MK_EXEC_PERSISTENT &&
+        make_geometry(pf.m, ctx->n_cta, o.page_bytes, o.n_pages, o.kv_splits, smem_optin, &pf.geo).empty()) {
+      int bp = 0;
+      MK_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bp, ctx->kernel, kThreads, pf.geo.smem_bytes));
+      if (bp < ctx->bpsm) pf.geo.smem_bytes = 0;  // chunks would not run in one wave: per-position prefill
+    } else {
+      pf.geo.smem_bytes = 0;
+    }
+  }
 
   // device state
   DevState& S = ctx->st;
@@ -443,24 +523,7 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
     S.rope = reinterpret_cast<const float2*>(ctx->rope.p);
   }
   {  // activation arena: two parity sets
-    const int G = m.Hq / m.Hkv;
-    const long long MB = m.max_batch;
-    long long sizes[ACT_NUM], layers[ACT_NUM];
-    sizes[ACT_H] = MB * m.d; layers[ACT_H] = m.L + 1;
-    sizes[ACT_HMID] = MB * m.d; layers[ACT_HMID] = m.L;
-    sizes[ACT_Q] = MB * m.Hq * m.hd; layers[ACT_Q] = m.L;
-    sizes[ACT_KVN] = MB * 2 * m.Hkv * m.hd; layers[ACT_KVN] = m.L;
-    sizes[ACT_PART] = MB * m.Hkv * (long long)g.S * G * (m.hd + kPartExtra); layers[ACT_PART] = m.L;
-    sizes[ACT_O] = MB * m.Hq * m.hd; layers[ACT_O] = m.L;
-    sizes[ACT_A] = MB * m.F; layers[ACT_A] = m.L;
-    long long off = 0;
-    for (int k = 0; k < ACT_NUM; ++k) {
-      const long long stride = (sizes[k] + 31) / 32 * 32;
-      S.act_off[k] = off;
-      S.act_stride[k] = stride;
-      off += stride * layers[k];
-    }
-    S.act_floats = (off + 31) / 32 * 32;
+    arena_layout(m, g, m.max_batch, &S);
     MK_CUDA(cudaMalloc(&ctx->act.p, sizeof(float) * 2 * S.act_floats));
     MK_CUDA(cudaMemset(ctx->act.p, 0xFF, sizeof(float) * 2 * S.act_floats));  // all NaN
     S.act = reinterpret_cast<float*>(ctx->act.p);
@@ -486,6 +549,7 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
   S.tc = g.tc;
   S.xbuf_bytes = g.xbuf_bytes;
   S.scratch_bytes = g.scratch_bytes;
+  S.smem_bytes = g.smem_bytes;
   S.sync_mode = o.sync_mode;
   S.timeout_ns = (int64_t)(o.wait_timeout_s * 1e9);
   S.backoff_max_ns = o.backoff_max_ns;
@@ -612,8 +676,52 @@ mk_status mk_prefill(mk_ctx* ctx, const int32_t* tokens, int B, int P, int32_t* 
   for (long long i = 0; i < (long long)B * P; ++i)
     if (tokens[i] < 0 || tokens[i] >= ctx->m.V) return fail(MK_ERR_INVALID, "token id out of range");
   if (ctx->broken) return fail(MK_ERR_STATE, "context needs mk_reset after a device error");
+  mk_status s;
+  if (ctx->pf.geo.smem_bytes > 0) {
+    // Prompt chunks: each launch takes c = kMaxBatch / B consecutive positions of every
+    // sequence as rows (row b*n + i = position t0 + i of sequence b), so that the weights
+    // stream once per chunk for up to kMaxBatch rows on the tensor-core GEMV; a row
+    // attends to the cached positions below t0 and to its chunk's rows up to its own.
+    s = ensure_prefill(ctx);
+    if (s) return s;
+    const int c = std::max(1, kMaxBatch / B);
+    int32_t tok[kMaxBatch], pos[kMaxBatch], seq[kMaxBatch], p0[kMaxBatch];
+    int n = 0;
+    for (int t0 = 0; t0 < P; t0 += c) {
+      n = std::min(c, P - t0);
+      const int rows = B * n;
+      for (int b = 0; b < B; ++b)
+        for (int i = 0; i < n; ++i) {
+          const int r = b * n + i;
+          tok[r] = tokens[(size_t)b * P + t0 + i];
+          pos[r] = t0 + i;
+          seq[r] = b;
+          p0[r] = t0;
+        }
+      Sched* sc = nullptr;
+      s = get_sched_in(ctx, ctx->pf.m, ctx->pf.geo, ctx->pf.scheds, rows, &sc);
+      if (s) return s;
+      const bool last = t0 + n >= P;
+      float* lg = last && logits ? reinterpret_cast<float*>(ctx->pf.logits.p) : nullptr;
+      s = enqueue_step(ctx, sc, rows, tok, pos, false, lg, nullptr, 1, 0, &ctx->pf.st, seq, p0);
+      if (s) return s;
+    }
+    // each sequence's last position is row b*n + n-1 of the last chunk
+    if (logits)
+      for (int b = 0; b < B; ++b)
+        MK_CUDA(cudaMemcpyAsync(logits + (size_t)b * ctx->m.V,
+                                reinterpret_cast<float*>(ctx->pf.logits.p) + (size_t)(b * n + n - 1) * ctx->m.V,
+                                sizeof(float) * ctx->m.V, cudaMemcpyDeviceToDevice, ctx->stream));
+    s = read_status(ctx);
+    if (s && s != MK_ERR_NAN) return s;
+    for (int b = 0; b < B; ++b) next_tok[b] = ctx->host_ctl->tok[b * n + n - 1];
+    // the device copy of the chosen tokens (read by steps that embed them on the device)
+    MK_CUDA(cudaMemcpy(reinterpret_cast<Ctl*>(ctx->ctl.p)->tok, next_tok, sizeof(int32_t) * B, cudaMemcpyHostToDevice));
+    ctx->last_B = B;
+    return s;
+  }
   Sched* sc = nullptr;
-  mk_status s = get_sched(ctx, B, &sc);
+  s = get_sched(ctx, B, &sc);
   if (s) return s;
   int32_t tok[kMaxBatch], pos[kMaxBatch];
   for (int t = 0; t < P; ++t) {  // teacher-forced steps, enqueued back to back

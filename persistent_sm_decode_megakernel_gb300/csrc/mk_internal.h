@@ -153,6 +153,7 @@ struct DevState {
   int page_stride;             // bytes between ring slots (>= page_bytes; kTcPageBytes with tc)
   int tc;                      // batches of 3..16 use the tensor-core GEMV
   int xbuf_bytes, scratch_bytes;
+  int smem_bytes;              // dynamic shared memory of a launch with this state (host use)
   int sync_mode;
   int64_t timeout_ns;
   int backoff_max_ns;
@@ -181,6 +182,12 @@ struct StepArgs {
   int flags;
   int32_t tok[kMaxBatch];
   int32_t pos[kMaxBatch];
+  // Row b of the step is position pos[b] of cache sequence seq[b]; positions below p0[b]
+  // are in the cache from earlier launches, positions p0[b]..pos[b] are this launch's rows
+  // b - (pos[b] - p0[b]) .. b (a prompt chunk: consecutive rows, consecutive positions).
+  // A decode step has seq[b] = b and p0[b] = pos[b].
+  int32_t seq[kMaxBatch];
+  int32_t p0[kMaxBatch];
   float* logits;               // [B][V] or null
   int32_t* tok_hist;           // device [B] copy of this step's tokens, or null
   int n_steps;                 // greedy steps this launch runs back to back (0 or 1: one)

@@ -220,11 +220,13 @@ __device__ __forceinline__ Gemv make_gemv(const DevState& S, const Instr& in) {
   return g;
 }
 
-// Split-KV unit (§8.2 ATTENTION): sequence b, kv head j, split s of S over positions
-// 0..pos_b.  Cached positions [t0, min(t1, pos_b)) stream through pages as K, V blocks;
-// the split holding position pos_b takes the new key/value from the QKV op's fp32 copy.
+// Split-KV unit (§8.2 ATTENTION): row b (position pos_b of cache sequence seq_b), kv head
+// j, split s of S over positions 0..p0_b.  Cached positions [t0, min(t1, p0_b)) stream
+// through pages as K, V blocks; the split holding position p0_b takes the keys/values of
+// this launch's positions p0_b..pos_b (n_new rows: one for a decode step, the row's
+// earlier rows of a prompt chunk plus its own) from the QKV op's fp32 copies.
 struct Attn {
-  int b, j, s, nsp, t0, t1, n_cached, pb, nblocks;
+  int b, j, s, nsp, t0, t1, n_cached, pb, nblocks, n_new;
   bool has_new, active;
   const uint16_t* kb;
   const uint16_t* vb;
@@ -237,7 +239,7 @@ struct Attn {
 // kSplitLongPositions positions, where streaming the cache dominates and all S splits
 // keep every CTA busy.
 __device__ __forceinline__ int active_splits(const DevState& S, const StepArgs& A, int b) {
-  const int npos = A.pos[b] + 1;
+  const int npos = A.p0[b] + 1;
   const int pmin = S.split_min_positions;
   const int per_cta = max(1, S.n_cta / (A.B * S.Hkv));
   const int want = max(per_cta, (npos + kSplitLongPositions - 1) / kSplitLongPositions);
@@ -249,7 +251,7 @@ __device__ __forceinline__ Attn make_attn(const DevState& S, const StepArgs& A, 
   a.j = in.a[1];
   a.s = in.a[2];
   a.active = a.b < A.B;
-  const int npos = a.active ? A.pos[a.b] + 1 : 1;
+  const int npos = a.active ? A.p0[a.b] + 1 : 1;
   a.nsp = a.active ? active_splits(S, A, a.b) : 1;
   a.active = a.active && a.s < a.nsp;
   a.t0 = (int)((uint32_t)(a.s * npos) / (uint32_t)a.nsp);  // s * npos < 2^31 (S <= 256, npos < 2^23)
@@ -257,6 +259,7 @@ __device__ __forceinline__ Attn make_attn(const DevState& S, const StepArgs& A, 
   const int tc = min(a.t1, npos - 1);
   a.n_cached = max(0, tc - a.t0);
   a.has_new = (a.t1 == npos);
+  a.n_new = a.active ? A.pos[a.b] - A.p0[a.b] + 1 : 0;
   a.pb = S.page_bytes / (S.hd * 2);
   a.nblocks = (a.n_cached + a.pb - 1) / a.pb;
   if (!a.active) {  // no such sequence, or a split beyond this step's count
@@ -264,8 +267,10 @@ __device__ __forceinline__ Attn make_attn(const DevState& S, const StepArgs& A, 
     a.nblocks = 0;
     a.has_new = false;
   }
-  a.kb = iptr(in, kP4) + (size_t)a.t0 * S.hd;  // (b, j) rows start at the baked pointer
-  a.vb = iptr(in, kP5) + (size_t)a.t0 * S.hd;
+  // the baked pointer addresses cache sequence b; row b reads sequence seq_b
+  const int64_t rows = a.active ? (int64_t)(A.seq[a.b] - a.b) * S.Hkv * S.max_ctx : 0;
+  a.kb = iptr(in, kP4) + (rows + a.t0) * S.hd;
+  a.vb = iptr(in, kP5) + (rows + a.t0) * S.hd;
   return a;
 }
 
@@ -334,7 +339,10 @@ __device__ __noinline__ void producer(const DevState& S_arg, const StepArgs& A_a
   bool kv_ready = st == 0;
   if (MS && st > 0) {
     A.step += 1u;
-    for (int b = 0; b < A.B; ++b) A.pos[b] += 1;
+    for (int b = 0; b < A.B; ++b) {
+      A.pos[b] += 1;
+      A.p0[b] += 1;
+    }
   }
   for (int pc = A.q_start[cta]; pc < end && ok; ++pc) {
     const Instr in = load_instr(A.instr + pc);
@@ -912,7 +920,8 @@ __device__ __forceinline__ void gemv_epilogue(const DevState& S, const StepArgs&
           q[i + half] = vb;
         } else {
           const uint16_t ra = Unpack<WT>::round(va), rb = Unpack<WT>::round(vb);
-          uint16_t* cache = const_cast<uint16_t*>(iptr(in, kP3)) + (((size_t)b * S.Hkv + head) * S.max_ctx + pos) * hd;
+          uint16_t* cache =
+              const_cast<uint16_t*>(iptr(in, kP3)) + (((size_t)A.seq[b] * S.Hkv + head) * S.max_ctx + pos) * hd;
           cache[i] = ra;
           cache[i + half] = rb;
           float* kvn = act_ptr(S, act, ACT_KVN, l) + ((size_t)b * 2 + (mat - 1)) * S.Hkv * hd + (size_t)head * hd;
@@ -1383,18 +1392,23 @@ __device__ __noinline__ void op_attn(const DevState& S_arg, const StepArgs& A_ar
     v.w *= qscale;
     q4[i] = v;
   });
-  // the new position's key and value (split holding pos_b), staged as storage-dtype rows
-  // like a page (the values are already rounded to that dtype, so this is exact)
+  // this launch's positions p0_b..pos_b (split holding p0_b): the keys and values of rows
+  // b - n_new + 1 .. b, staged as storage-dtype rows [n][k | v] like a page (the values are
+  // already rounded to that dtype, so this is exact)
   uint16_t* knew = reinterpret_cast<uint16_t*>(xbuf + G * HD);
-  if (at.has_new && tid < HD / 2) {
-    const float* kn = act_ptr(S, act, ACT_KVN, l) + (size_t)at.b * 2 * S.Hkv * HD + (size_t)at.j * HD;
-    const int kv = tid / (HD / 4), e = (tid % (HD / 4)) * 4;  // HD/4 vectors of k, then of v
-    const float4 v = load_v4<SYNC>(reinterpret_cast<const float4*>(kn + (size_t)kv * S.Hkv * HD + e), S, c);
-    uint16_t* dst = knew + kv * HD + e;
-    dst[0] = Unpack<WT>::round(v.x);
-    dst[1] = Unpack<WT>::round(v.y);
-    dst[2] = Unpack<WT>::round(v.z);
-    dst[3] = Unpack<WT>::round(v.w);
+  if (at.has_new) {
+    const float* kn0 = act_ptr(S, act, ACT_KVN, l) + (size_t)(at.b - at.n_new + 1) * 2 * S.Hkv * HD + (size_t)at.j * HD;
+    for (int t = tid; t < at.n_new * (HD / 2); t += kConsumerThreads) {
+      const int r = t / (HD / 2), u = t % (HD / 2);
+      const int kv = u / (HD / 4), e = (u % (HD / 4)) * 4;  // HD/4 vectors of k, then of v
+      const float* kn = kn0 + (size_t)r * 2 * S.Hkv * HD;
+      const float4 v = load_v4<SYNC>(reinterpret_cast<const float4*>(kn + (size_t)kv * S.Hkv * HD + e), S, c);
+      uint16_t* dst = knew + (r * 2 + kv) * HD + e;
+      dst[0] = Unpack<WT>::round(v.x);
+      dst[1] = Unpack<WT>::round(v.y);
+      dst[2] = Unpack<WT>::round(v.z);
+      dst[3] = Unpack<WT>::round(v.w);
+    }
   }
   consumer_sync();
   const bool mark = (A.flags & SF_TRACE) && tid == 0;
@@ -1507,13 +1521,13 @@ __device__ __noinline__ void op_attn(const DevState& S_arg, const StepArgs& A_ar
     }
   };
 
-  // the cached positions a page block at a time; position pos_b (this step's key/value,
-  // staged above) is one more row of the last block's pass
+  // the cached positions a page block at a time; this launch's positions p0_b..pos_b
+  // (staged above) are n_new more rows of the last block
   const int nblk = at.nblocks > 0 ? at.nblocks : (at.has_new ? 1 : 0);
   for (int blk = 0; blk < nblk; ++blk) {
     const bool paged = blk < at.nblocks;
     const int np = paged ? min(at.pb, at.n_cached - blk * at.pb) : 0;
-    const int nx = np + (blk == nblk - 1 && at.has_new ? 1 : 0);
+    const int nx = np + (blk == nblk - 1 && at.has_new ? at.n_new : 0);
     const uint8_t* kp = nullptr;
     const uint8_t* vp = nullptr;
     if (paged) {
@@ -1536,8 +1550,9 @@ __device__ __noinline__ void op_attn(const DevState& S_arg, const StepArgs& A_ar
           const int t = base + r * PASS + warp * NGRP + pgi;
           const bool cached = t < np;
           const size_t off = (size_t)(cached ? t : 0) * HD * 2;
-          kr[r] = cached ? reinterpret_cast<const uint16_t*>(kp + off) : knew;
-          vr[r] = cached ? reinterpret_cast<const uint16_t*>(vp + off) : knew + HD;
+          const int nr = t < np ? 0 : min(t - np, at.n_new - 1);  // staged row (clamped: a valid address)
+          kr[r] = cached ? reinterpret_cast<const uint16_t*>(kp + off) : knew + nr * 2 * HD;
+          vr[r] = cached ? reinterpret_cast<const uint16_t*>(vp + off) : knew + nr * 2 * HD + HD;
           if (t < nx) nvalid = r + 1;
         }
         chunk(rct, nvalid, kr, vr);
@@ -1816,7 +1831,10 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
       StepArgs& M = smem_ctl()->args;
       M.step += 1u;
       M.epoch += 1u;
-      for (int b = 0; b < M.B; ++b) M.pos[b] += 1;
+      for (int b = 0; b < M.B; ++b) {
+        M.pos[b] += 1;
+        M.p0[b] += 1;
+      }
       M.flags |= SF_TOK_FROM_DEVICE;
       if (M.tok_hist) M.tok_hist += M.B;
     }

@@ -126,7 +126,7 @@ mk_status prepare(const mk_model_desc& d, const mk_weights* w, const mk_kv* kv, 
   std::string e = make_geometry(m, n_sm, 0, 0, 0, smem_optin, &g);
   if (!e.empty()) return fail(MK_ERR_INVALID, e);
   const void* fn = step_kernel_entry(m.dtype, MK_SYNC_COUNTER, false);
-  NA_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_bytes));
+  NA_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin));
   int bpsm = 0;
   NA_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bpsm, fn, kThreads, g.smem_bytes));
   if (bpsm < 1) return fail(MK_ERR_OCCUPANCY, "the kernel does not fit on an SM");
@@ -167,23 +167,7 @@ mk_status prepare(const mk_model_desc& d, const mk_weights* w, const mk_kv* kv, 
 
   // activation arena (one set: counter synchronisation needs no second parity)
   DevState S{};
-  const int G = m.Hq / m.Hkv;
-  long long sizes[ACT_NUM], layers[ACT_NUM];
-  sizes[ACT_H] = (long long)B * m.d; layers[ACT_H] = L + 1;
-  sizes[ACT_HMID] = (long long)B * m.d; layers[ACT_HMID] = L;
-  sizes[ACT_Q] = (long long)B * m.Hq * m.hd; layers[ACT_Q] = L;
-  sizes[ACT_KVN] = (long long)B * 2 * m.Hkv * m.hd; layers[ACT_KVN] = L;
-  sizes[ACT_PART] = (long long)B * m.Hkv * g.S * G * (m.hd + kPartExtra); layers[ACT_PART] = L;
-  sizes[ACT_O] = (long long)B * m.Hq * m.hd; layers[ACT_O] = L;
-  sizes[ACT_A] = (long long)B * m.F; layers[ACT_A] = L;
-  long long off = 0;
-  for (int k = 0; k < ACT_NUM; ++k) {
-    const long long stride = (sizes[k] + 31) / 32 * 32;
-    S.act_off[k] = off;
-    S.act_stride[k] = stride;
-    off += stride * layers[k];
-  }
-  S.act_floats = (off + 31) / 32 * 32;
+  arena_layout(m, g, B, &S);
 
   // carve the array
   size_t cur = 0;
@@ -238,6 +222,7 @@ mk_status prepare(const mk_model_desc& d, const mk_weights* w, const mk_kv* kv, 
   S.tc = g.tc;
   S.xbuf_bytes = g.xbuf_bytes;
   S.scratch_bytes = g.scratch_bytes;
+  S.smem_bytes = g.smem_bytes;
   S.sync_mode = MK_SYNC_COUNTER;
   S.timeout_ns = 2000000000LL;
   S.backoff_max_ns = 256;
@@ -309,12 +294,14 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_desc* desc, const mk_
   for (int b = 0; b < B; ++b) {
     A.tok[b] = in_tok[b];
     A.pos[b] = pos[b];
+    A.seq[b] = b;       // row b is sequence b
+    A.p0[b] = pos[b];   // one new position per row
   }
   A.logits = logits;
   A.tok_hist = nullptr;
   DevState S = P.S;
   const void* fn = step_kernel_entry(d.dtype, MK_SYNC_COUNTER, false);
-  NA_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, P.smem));
+  NA_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin));
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(P.n_cta);
   cfg.blockDim = dim3(kThreads);

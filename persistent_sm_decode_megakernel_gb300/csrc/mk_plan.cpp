@@ -117,7 +117,8 @@ std::string make_geometry(const ModelShape& m, int n_cta, int page_bytes, int n_
   const int kmax = std::max(m.d, std::max(m.Hq * m.hd, m.F));
   // x buffer: a batch of GEMV inputs, or q of one GQA group plus the new key/value; with
   // the tensor-core path, batches of 1..2 inputs or one window of 16 sequences' hi/lo halves
-  const int xfloats = g->tc ? std::max(std::max(2 * kmax, kMaxBatch * std::min(kTcKw, kmax)), (G + 1) * m.hd)
+  // (a prompt chunk's attention stages q and up to kMaxBatch new key/value rows: tc only)
+  const int xfloats = g->tc ? std::max(std::max(2 * kmax, kMaxBatch * std::min(kTcKw, kmax)), (G + kMaxBatch) * m.hd)
                             : std::max(g->nb_max * kmax, (G + 1) * m.hd);
   g->xbuf_bytes = ((xfloats * 4 + 127) / 128) * 128;
   if (kv_splits > 0) {
@@ -141,6 +142,27 @@ std::string make_geometry(const ModelShape& m, int n_cta, int page_bytes, int n_
   g->n_pages = np;
   g->smem_bytes = np * g->page_stride + g->xbuf_bytes + g->scratch_bytes + kCtlSmem;
   return "";
+}
+
+void arena_layout(const ModelShape& m, const Geometry& g, int rows, DevState* S) {
+  const int G = m.Hq / m.Hkv;
+  const long long R = rows;
+  long long sizes[ACT_NUM], layers[ACT_NUM];
+  sizes[ACT_H] = R * m.d; layers[ACT_H] = m.L + 1;
+  sizes[ACT_HMID] = R * m.d; layers[ACT_HMID] = m.L;
+  sizes[ACT_Q] = R * m.Hq * m.hd; layers[ACT_Q] = m.L;
+  sizes[ACT_KVN] = R * 2 * m.Hkv * m.hd; layers[ACT_KVN] = m.L;
+  sizes[ACT_PART] = R * m.Hkv * (long long)g.S * G * (m.hd + kPartExtra); layers[ACT_PART] = m.L;
+  sizes[ACT_O] = R * m.Hq * m.hd; layers[ACT_O] = m.L;
+  sizes[ACT_A] = R * m.F; layers[ACT_A] = m.L;
+  long long off = 0;
+  for (int k = 0; k < ACT_NUM; ++k) {
+    const long long stride = (sizes[k] + 31) / 32 * 32;
+    S->act_off[k] = off;
+    S->act_stride[k] = stride;
+    off += stride * layers[k];
+  }
+  S->act_floats = (off + 31) / 32 * 32;
 }
 
 static inline int split_lo(long long total, int parts, int i) { return (int)(total * i / parts); }

@@ -59,6 +59,9 @@ std::string check_desc(const mk_model_desc* d);
 std::string check_model_pointers(const mk_model_desc* d, const mk_weights* w, const mk_kv* kv);
 ModelShape shape_of(const mk_model_desc* d);
 
+// activation arena of `rows` rows: fills S->act_off, act_stride and act_floats (one parity)
+void arena_layout(const ModelShape& m, const Geometry& g, int rows, DevState* S);
+
 // returns "" on success, else a message
 std::string make_geometry(const ModelShape& m, int n_cta, int page_bytes, int n_pages_req, int kv_splits,
                           int smem_limit, Geometry* g);
