@@ -107,6 +107,12 @@ typedef struct {
                              fill the whole pool; fewer copies queued in the memory
                              system shorten the waits of the loads and stores that
                              carry the dependencies between ops                          */
+  int attn_pool;          /* 1: dynamic work queue of the split-KV attention units ("8 ·
+                             Écrire son megakernel", §8.8, dynamic queue): each layer's
+                             units sit in a shared pool and every CTA's loader claims them
+                             one at a time (an atomic claim counter) as its ring frees,
+                             instead of a fixed share dealt to its queue; persistent
+                             control only (0: fixed shares, the default)                 */
 } mk_options;
 
 typedef struct {

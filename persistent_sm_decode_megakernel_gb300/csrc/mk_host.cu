@@ -117,7 +117,10 @@ mk_status upload(DevBuf& b, const void* src, size_t bytes) {
   return MK_OK;
 }
 
-mk_status upload_queues(const std::vector<std::vector<Instr>>& qs, DevBuf& ibuf, DevBuf& qbuf, int* n_out) {
+// the queues back to back, then the attention pools (their claim loops' a0 becomes an
+// index into the uploaded array)
+mk_status upload_queues(const std::vector<std::vector<Instr>>& qs, DevBuf& ibuf, DevBuf& qbuf, int* n_out,
+                        const std::vector<Instr>* pool = nullptr) {
   std::vector<Instr> flat;
   std::vector<int32_t> qs_off;
   for (const auto& q : qs) {
@@ -125,6 +128,12 @@ mk_status upload_queues(const std::vector<std::vector<Instr>>& qs, DevBuf& ibuf,
     flat.insert(flat.end(), q.begin(), q.end());
   }
   qs_off.push_back((int32_t)flat.size());
+  if (pool && !pool->empty()) {
+    const int32_t base = (int32_t)flat.size();
+    for (auto& in : flat)
+      if (in.op == OP_ATTN_POOL) in.a[0] += base;
+    flat.insert(flat.end(), pool->begin(), pool->end());
+  }
   if (n_out) *n_out = (int)flat.size();
   mk_status s = upload(ibuf, flat.data(), flat.size() * sizeof(Instr));
   if (s) return s;
@@ -143,14 +152,15 @@ mk_status get_sched_in(mk_ctx* ctx, const ModelShape& m, const Geometry& geo,
   // merges them in the last-arriving split and sentinel mode keeps the separate
   // ATTN_REDUCE op (it has no atomics to elect a last arriver)
   const int merge = choose_merge(m, geo, B, ctx->opts.sync_mode == MK_SYNC_COUNTER, ctx->opts.attn_merge);
-  std::string e = build_plan(m, geo, ctx->n_cta, B, ctx->opts.fault_drop_signal, merge, &sc->plan);
+  const bool pool = ctx->opts.attn_pool == 1 && ctx->opts.exec_mode == MK_EXEC_PERSISTENT;
+  std::string e = build_plan(m, geo, ctx->n_cta, B, ctx->opts.fault_drop_signal, merge, &sc->plan, pool);
   if (!e.empty()) return fail(MK_ERR_INVALID, "schedule: " + e);
   bake_pointers(m, ctx->ptrs, &sc->plan);
   if (ctx->opts.fault_drop_signal <= 0) {
     e = validate_plan(m, geo, sc->plan);
     if (!e.empty()) return fail(MK_ERR_INVALID, "schedule rejected by the validator: " + e);
   }
-  mk_status s = upload_queues(sc->plan.queues, sc->instr, sc->qstart, &sc->n_instr);
+  mk_status s = upload_queues(sc->plan.queues, sc->instr, sc->qstart, &sc->n_instr, &sc->plan.pool);
   if (s) return s;
   MK_CUDA(cudaMalloc(&sc->counters.p, sizeof(uint32_t) * std::max(1, sc->plan.n_counters)));
   MK_CUDA(cudaMemset(sc->counters.p, 0, sizeof(uint32_t) * std::max(1, sc->plan.n_counters)));
@@ -405,7 +415,8 @@ mk_status mk_plan(const mk_model_desc* desc, const mk_options* opts, int n_ctas,
   if (!e.empty()) return fail(MK_ERR_INVALID, e);
   Plan p;
   e = build_plan(m, g, n_ctas, m.max_batch, o.fault_drop_signal,
-                 choose_merge(m, g, m.max_batch, o.sync_mode == MK_SYNC_COUNTER, o.attn_merge), &p);
+                 choose_merge(m, g, m.max_batch, o.sync_mode == MK_SYNC_COUNTER, o.attn_merge), &p,
+                 o.attn_pool == 1 && o.exec_mode == MK_EXEC_PERSISTENT);
   if (!e.empty()) return fail(MK_ERR_INVALID, e);
   e = validate_plan(m, g, p);
   if (!e.empty()) return fail(MK_ERR_INVALID, "schedule rejected by the validator: " + e);
@@ -417,6 +428,7 @@ mk_status mk_plan(const mk_model_desc* desc, const mk_options* opts, int n_ctas,
   info->n_pages = g.n_pages;
   info->kv_splits = g.S;
   for (const auto& q : p.queues) info->n_instructions += (int)q.size();
+  info->n_instructions += (int)p.pool.size();
   info->n_counters = p.n_counters;
   info->launches_per_step = o.exec_mode != MK_EXEC_PERSISTENT ? (int)p.phase_queues.size() : 1;
   info->weight_bytes_per_step = p.weight_bytes;
@@ -444,6 +456,7 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
   if (o.exec_mode != MK_EXEC_PERSISTENT && o.exec_mode != MK_EXEC_MULTILAUNCH && o.exec_mode != MK_EXEC_GRAPH)
     return fail(MK_ERR_INVALID, "exec_mode");
   if (o.attn_merge < 0 || o.attn_merge > 2) return fail(MK_ERR_INVALID, "attn_merge must be 0, 1 or 2");
+  if (o.attn_pool < 0 || o.attn_pool > 1) return fail(MK_ERR_INVALID, "attn_pool must be 0 or 1");
   ctx->stream = reinterpret_cast<cudaStream_t>(stream);
   MK_CUDA(cudaGetDevice(&ctx->device));
   MK_CUDA(cudaDeviceGetAttribute(&ctx->n_sm, cudaDevAttrMultiProcessorCount, ctx->device));

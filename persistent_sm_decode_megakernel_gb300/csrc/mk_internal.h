@@ -27,6 +27,7 @@ enum Op : uint8_t {
   OP_UPGATE = 6,       // RMSNorm + a = silu(W_g x) * (W_u x)              (§8.2 MLP_UP_GATE)
   OP_DOWN = 7,         // h_out = h_mid + W_d a                            (§8.2 MLP_DOWN)
   OP_LMHEAD = 8,       // final RMSNorm + logits + argmax                  (§8.2 LM_HEAD)
+  OP_ATTN_POOL = 9,    // claim ATTENTION units of a layer from a shared pool until it is empty
   // build-ladder self-test opcodes (§8.6 steps 1-4)
   OP_T_NOP = 16,
   OP_T_ORDER = 17,
@@ -69,6 +70,9 @@ static_assert(sizeof(Instr) == 64, "instruction is 64 bytes");
 //           merged from the split partials while it is staged)
 //   UPGATE  a0 row0, a1 rows, p2 gain, p4 gate rows, p5 up rows
 //   LMHEAD  a0 row0, a1 rows, a2 CTAs with LM rows, p2 final gain, p4 first row
+//   POOL    a0 index of the layer's first ATTENTION unit in the instruction array (the pools
+//           follow the queues), a1 units, a2 claim counter, a3 CTAs (a step claims a1 + a3
+//           times: every CTA's last claim comes back empty)
 // pK = the 64-bit value in a[2K], a[2K+1]
 constexpr int kP2 = 4, kP3 = 6, kP4 = 8, kP5 = 10;
 inline void set_ptr(Instr& in, int at, const void* p) {

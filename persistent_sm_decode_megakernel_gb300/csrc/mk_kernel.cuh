@@ -22,9 +22,17 @@
 namespace mk {
 namespace {  // internal linkage: every instantiation unit gets its own copy
 
+constexpr int kPoolSlots = 2;  // claimed attention units the loader may hold ahead of the compute warps
+
 struct SmemCtl {
   uint64_t full[kMaxPages];
   uint64_t empty[kMaxPages];
+  uint64_t pool_full[kPoolSlots];   // attention pool: the loader's claimed units, in claim order
+  uint64_t pool_empty[kPoolSlots];
+  int pool_fifo[kPoolSlots];        // unit index within the layer's pool, -1: the pool is empty
+  int pool_slot;                    // compute side: next FIFO slot and its phase (thread 0)
+  uint32_t pool_ph;
+  int pool_unit;                    // the unit thread 0 took, for the other compute threads
   unsigned long long best[kMaxBatch];
   float inv_rms[kMaxBatch];
   float red[kConsumerWarps * kMaxBatch];
@@ -335,10 +343,43 @@ __device__ __noinline__ void producer(const DevState& S_arg, const StepArgs& A_a
   // on the one before, so they stream ahead across the boundary; the KV blocks do (the
   // previous step appended its key/value rows): before the first of them the loader waits
   // for the previous step's tokens, which every CTA's whole step precedes.
+  int ps = 0;          // attention pool FIFO slot and phase
+  uint32_t pph = 0;
   for (int st = 0; st < n_steps && ok; ++st) {
   bool kv_ready = st == 0;
+  // the K, V blocks of one split-KV unit (before the first of a multi-step launch's later
+  // steps, wait for the previous step's tokens: that step appended its key/value rows)
+  auto stream_attn = [&](const Instr& un) {
+    if (MS && !kv_ready) {
+      if (!wait_seq(&S.ctl->tok_seq, A.step, -10)) {
+        c->abort = 1;
+        ok = false;
+        return;
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // generic-proxy writes before bulk reads
+      kv_ready = true;
+    }
+    const Attn at = make_attn(S, A, un);
+    for (int blk = 0; blk < at.nblocks && ok; ++blk) {
+      const int p0 = blk * at.pb;
+      const int np = min(at.pb, at.n_cached - p0);
+      const uint32_t bytes = (uint32_t)np * S.hd * 2u;
+      for (int kv = 0; kv < 2; ++kv) {
+        if (!producer_acquire(S, c, slot, ph, issued++)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&c->full[slot], bytes);
+        tma_load_1d(pages + (size_t)slot * S.page_stride, (kv ? at.vb : at.kb) + (size_t)p0 * S.hd, bytes,
+                    &c->full[slot], pol);
+        c->last_issue_phase[slot] = (int)ph;
+        if (++slot == S.n_pages) { slot = 0; ph ^= 1u; }
+      }
+    }
+  };
   if (MS && st > 0) {
     A.step += 1u;
+    A.epoch += 1u;
     for (int b = 0; b < A.B; ++b) {
       A.pos[b] += 1;
       A.p0[b] += 1;
@@ -420,7 +461,18 @@ __device__ __noinline__ void producer(const DevState& S_arg, const StepArgs& A_a
         }
         break;
       }
-      case OP_ATTN: {
+      case OP_ATTN:
+        stream_attn(in);
+        break;
+      case OP_ATTN_POOL: {
+        // dynamic work queue (§8.8): claim the layer's units one at a time while the ring
+        // frees -- a CTA that reaches its attention early takes more of them -- and hand
+        // each unit to the compute warps (in claim order) before streaming its K, V blocks.
+        // A step makes a1 + a3 claims on the counter: every CTA's last one comes back empty.
+        // In a multi-step launch a later step claims only once the step before has published
+        // its tokens (every CTA is through all its claims of that step): a claim taken earlier
+        // could land in the previous step's range of the counter.
+        const uint32_t per_step = (uint32_t)(in.a[1] + in.a[3]);
         if (MS && !kv_ready) {
           if (!wait_seq(&S.ctl->tok_seq, A.step, -10)) {
             c->abort = 1;
@@ -430,22 +482,20 @@ __device__ __noinline__ void producer(const DevState& S_arg, const StepArgs& A_a
           asm volatile("fence.proxy.async.global;" ::: "memory");  // generic-proxy writes before bulk reads
           kv_ready = true;
         }
-        const Attn at = make_attn(S, A, in);
-        for (int blk = 0; blk < at.nblocks && ok; ++blk) {
-          const int p0 = blk * at.pb;
-          const int np = min(at.pb, at.n_cached - p0);
-          const uint32_t bytes = (uint32_t)np * S.hd * 2u;
-          for (int kv = 0; kv < 2; ++kv) {
-            if (!producer_acquire(S, c, slot, ph, issued++)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&c->full[slot], bytes);
-            tma_load_1d(pages + (size_t)slot * S.page_stride, (kv ? at.vb : at.kb) + (size_t)p0 * S.hd, bytes,
-                        &c->full[slot], pol);
-            c->last_issue_phase[slot] = (int)ph;
-            if (++slot == S.n_pages) { slot = 0; ph ^= 1u; }
+        for (;;) {
+          if (!producer_wait(S, c, &c->pool_empty[ps], pph ^ 1u)) {
+            ok = false;
+            break;
           }
+          const uint32_t k = atomicAdd(&S.counters[in.a[2]], 1u);
+          const uint32_t u = k - A.epoch * per_step;
+          const int unit = u < (uint32_t)in.a[1] ? (int)u : -1;
+          c->pool_fifo[ps] = unit;
+          mbar_arrive(&c->pool_full[ps]);
+          if (++ps == kPoolSlots) { ps = 0; pph ^= 1u; }
+          if (unit < 0) break;
+          stream_attn(load_instr(A.instr + in.a[0] + unit));
+          if (!ok) break;
         }
         break;
       }
@@ -1799,6 +1849,32 @@ __device__ void op_test_pages(const DevState& S_arg, const Instr& in_arg, SmemCt
 }
 
 // ---------------------------------------------------------------- compute warps: loop
+// Thread 0 takes the next unit its loader claimed from the attention pool (bounded wait).
+__device__ __noinline__ bool pool_take(const DevState& S_arg, SmemCtl* c) {
+  const DevState& S = smem_ctl()->S;
+  c = smem_ctl();
+  const int s = c->pool_slot;
+  const uint32_t ph = c->pool_ph;
+  if (!mbar_try_wait(&c->pool_full[s], ph)) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_wait_hint(&c->pool_full[s], ph, 2000u)) {
+      if (c->abort) return false;
+      if (globaltimer_ns() - t0 > (uint64_t)S.timeout_ns) {
+        set_err(S, 4u, -11, s);
+        c->abort = 1;
+        return false;
+      }
+    }
+  }
+  c->pool_unit = c->pool_fifo[s];
+  mbar_arrive(&c->pool_empty[s]);
+  if (++c->pool_slot == kPoolSlots) {
+    c->pool_slot = 0;
+    c->pool_ph ^= 1u;
+  }
+  return true;
+}
+
 template <typename WT, int SYNC, bool MS>
 __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* c, uint8_t* pages, float* xbuf,
                          float* scratch) {
@@ -1860,8 +1936,20 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
     consumer_sync();
   }
   for (int pc = A.q_start[cta]; pc < end; ++pc) {
-    const Instr in = load_instr(A.instr + pc);
+    Instr in = load_instr(A.instr + pc);
     if (in.op == OP_END) break;
+    if (in.op == OP_ATTN_POOL) {
+      // dynamic attention: the next unit this CTA's loader claimed from the layer's pool,
+      // run below as an ATTENTION instruction; the loop comes back here until the loader
+      // reports the pool empty
+      bool bad = false;
+      if (tid == 0 && !pool_take(S, c)) bad = true;
+      if (consumer_sync_or(bad || c->abort)) break;
+      const int u = c->pool_unit;
+      if (u < 0) continue;
+      in = load_instr(A.instr + in.a[0] + u);
+      --pc;
+    }
     if ((tid & 31) == 0) c->cur[tid >> 5] = in;  // the ops read their warp's shared copy
     __syncwarp();
     uint64_t t_fetch = 0, t_ready = 0;
@@ -2056,6 +2144,12 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
       mbar_init(&c->empty[i], kConsumerWarps);
       c->last_issue_phase[i] = -1;
     }
+    for (int i = 0; i < kPoolSlots; ++i) {
+      mbar_init(&c->pool_full[i], 1);
+      mbar_init(&c->pool_empty[i], 1);
+    }
+    c->pool_slot = 0;
+    c->pool_ph = 0;
     c->abort = 0;
     c->ms_step = 0;
     mbar_fence_init();

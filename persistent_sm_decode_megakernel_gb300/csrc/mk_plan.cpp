@@ -188,7 +188,7 @@ int choose_merge(const ModelShape& m, const Geometry& g, int B, bool counters, i
 }
 
 std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B, int drop_signal, int merge,
-                       Plan* p) {
+                       Plan* p, bool attn_pool) {
   if (B < 1 || B > m.max_batch) return "batch out of range";
   *p = Plan();
   p->merge = merge;
@@ -288,6 +288,7 @@ std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B,
       std::vector<int> arr;
       if (fuse_reduce)
         for (int k = 0; k < nbj; ++k) arr.push_back(new_ctr());
+      const int pool0 = (int)p->pool.size();
       for (int u = 0; u < nu; ++u) {
         const int bj = u % nbj, sp = u / nbj;
         Instr in = mk_instr(OP_ATTN, l, c_qkv, 0, fuse_reduce ? c_red : c_att);
@@ -296,7 +297,23 @@ std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B,
         in.a[2] = sp;
         in.a[3] = g.S;
         in.a[4] = fuse_reduce ? arr[bj] : -1;
-        emit(u % n_cta, in);
+        if (attn_pool) {
+          p->pool.push_back(in);  // claimed at run time; its signal is counted below
+          p->signals[in.signal_ctr]++;
+        } else {
+          emit(u % n_cta, in);
+        }
+      }
+      if (attn_pool) {  // one claim loop per CTA and layer
+        const int c_claim = new_ctr();
+        for (int c = 0; c < n_cta; ++c) {
+          Instr in = mk_instr(OP_ATTN_POOL, l, c_qkv, 0, -1);
+          in.a[0] = pool0;
+          in.a[1] = nu;
+          in.a[2] = c_claim;
+          in.a[3] = n_cta;
+          emit(c, in);
+        }
       }
       if (fuse_reduce) {
         p->signals[c_red] = (uint32_t)(B * m.Hkv);
@@ -370,6 +387,8 @@ std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B,
   // wait counts = every signal of the awaited counter in one step
   for (auto& pe : all)
     if (pe.in.wait_ctr >= 0) pe.in.wait_n = p->signals[pe.in.wait_ctr];
+  for (auto& in : p->pool)
+    if (in.wait_ctr >= 0) in.wait_n = p->signals[in.wait_ctr];
   int sig_seen = 0;
   for (auto& pe : all) {
     // fault injection: the k-th signal is removed, its waiters keep expecting it
@@ -385,6 +404,7 @@ std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B,
   auto phase_of = [&](const Instr& in) -> int {
     if (in.op == OP_EMBED) return 0;
     if (in.op == OP_LMHEAD) return 1 + 6 * m.L;
+    if (in.op == OP_ATTN_POOL) return 1 + 6 * in.layer + (OP_ATTN - OP_QKV);
     return 1 + 6 * in.layer + (in.op - OP_QKV);
   };
   const int n_phase = 2 + 6 * m.L;
@@ -449,6 +469,7 @@ void bake_pointers(const ModelShape& m, const ModelPtrs& w, Plan* p) {
   };
   for (auto& q : p->queues)
     for (auto& in : q) bake(in);
+  for (auto& in : p->pool) bake(in);
   for (auto& ph : p->phase_queues)
     for (auto& q : ph)
       for (auto& in : q) bake(in);
@@ -475,18 +496,50 @@ std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p)
   auto group_of = [&](const Instr& in) -> int {
     if (in.op == OP_EMBED) return 0;
     if (in.op == OP_LMHEAD) return 1 + 6 * m.L;
+    if (in.op == OP_ATTN_POOL) return 1 + 6 * in.layer + (OP_ATTN - OP_QKV);
     return 1 + 6 * in.layer + (in.op - OP_QKV);
   };
   if ((int)p.queues.size() != n_cta) return "queue count != CTA count";
+  // Attention pools: the units of a layer may run on any CTA, each exactly once, after its
+  // claim loop's dependency.  For the checks below each pool is run whole by the first CTA
+  // that reaches one of its claim loops (one admissible interleaving; a unit waits on
+  // nothing but the QKV counter every claim loop also waits on, so any other assignment
+  // is ordered the same way).
+  std::vector<int> pool_layer(p.pool.size(), -1);
+  for (int c = 0; c < n_cta; ++c)
+    for (const auto& in : p.queues[c])
+      if (in.op == OP_ATTN_POOL) {
+        if (in.a[0] < 0 || in.a[1] < 1 || (size_t)in.a[0] + in.a[1] > p.pool.size() || in.a[3] != n_cta ||
+            in.a[2] < 0 || in.a[2] >= p.n_counters)
+          return fmt("cta %lld: bad attention pool arguments", c);
+        for (int u = in.a[0]; u < in.a[0] + in.a[1]; ++u) {
+          const Instr& un = p.pool[u];
+          if (un.op != OP_ATTN || un.layer != in.layer || un.wait_ctr != in.wait_ctr)
+            return "attention pool unit does not match its claim loop";
+          if (pool_layer[u] >= 0 && pool_layer[u] != in.layer) return "attention pool ranges overlap";
+          pool_layer[u] = in.layer;
+        }
+      }
+  for (size_t u = 0; u < p.pool.size(); ++u)
+    if (pool_layer[u] < 0) return "attention pool unit without a claim loop";
 
   // -- structure, argument ranges, scratch limits, signal counts
   std::vector<uint32_t> sig(p.n_counters, 0);
   std::vector<int> group_units(n_group, 0);
-  for (int c = 0; c < n_cta; ++c) {
-    const auto& q = p.queues[c];
+  for (int c = 0; c <= n_cta; ++c) {  // c == n_cta: the pooled units
+    std::vector<Instr> pooled;
+    if (c == n_cta) {
+      pooled = p.pool;
+      pooled.push_back(mk_instr(OP_END, 0, -1, 0, -1));
+    }
+    const auto& q = c < n_cta ? p.queues[c] : pooled;
     if (q.empty() || q.back().op != OP_END) return fmt("queue %lld does not end with OP_END", c);
     for (size_t k = 0; k + 1 < q.size(); ++k) {
       const Instr& in = q[k];
+      if (in.op == OP_ATTN_POOL) {
+        if (in.wait_ctr >= p.n_counters || in.signal_ctr != -1) return "bad attention pool counters";
+        continue;
+      }
       if (in.op < OP_EMBED || in.op > OP_LMHEAD) return fmt("cta %lld pc %lld: bad opcode %lld", c, k, in.op);
       if (in.op != OP_LMHEAD && in.layer >= m.L) return "layer out of range";
       if (in.signal_ctr >= p.n_counters || in.wait_ctr >= p.n_counters) return "counter index out of range";
@@ -536,8 +589,8 @@ std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p)
       }
     }
   }
-  for (int c = 0; c < n_cta; ++c)
-    for (const auto& in : p.queues[c]) {
+  for (int c = 0; c <= n_cta; ++c)
+    for (const auto& in : c < n_cta ? p.queues[c] : p.pool) {
       if (in.wait_ctr >= 0 && in.wait_n != sig[in.wait_ctr])
         return fmt("counter %lld: waiters expect %lld signals, the schedule gives %lld", in.wait_ctr, in.wait_n,
                    sig[in.wait_ctr]);
@@ -553,12 +606,13 @@ std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p)
   std::vector<std::vector<Bits>> signalers(p.n_counters);  // what each signal carries
   std::vector<int> ctr_group(p.n_counters, -1);
   std::vector<uint32_t> arrivals(p.n_counters, 0);
+  std::vector<char> pool_run(p.pool.size() + 1, 0);
   std::vector<Bits> arrived(p.n_counters, Bits(n_group));
   {
     // a counter "covers" a group when exactly that group's units signal it
     std::vector<int> sig_group(p.n_counters, -2);
-    for (int c = 0; c < n_cta; ++c)
-      for (const auto& in : p.queues[c])
+    for (int c = 0; c <= n_cta; ++c)
+      for (const auto& in : c < n_cta ? p.queues[c] : p.pool)
         if (in.signal_ctr >= 0 && !(in.flags & F_LAST_LM) && !(in.op == OP_ATTN && in.a[4] >= 0)) {
           const int gr = group_of(in);
           int& sg = sig_group[in.signal_ctr];
@@ -567,8 +621,8 @@ std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p)
     for (int k = 0; k < p.n_counters; ++k)
       if (sig_group[k] >= 0 && (int)sig[k] == group_units[sig_group[k]]) ctr_group[k] = sig_group[k];
     // fused merge: its counter completes when every split of every (b, j) has arrived
-    for (int c = 0; c < n_cta; ++c)
-      for (const auto& in : p.queues[c])
+    for (int c = 0; c <= n_cta; ++c)
+      for (const auto& in : c < n_cta ? p.queues[c] : p.pool)
         if (in.op == OP_ATTN && in.a[4] >= 0 && in.signal_ctr >= 0) ctr_group[in.signal_ctr] = group_of(in);
   }
   // required inputs (group ids) of each instruction
@@ -577,7 +631,8 @@ std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p)
     const int h_writer = l == 0 ? 0 : 1 + 6 * (l - 1) + 5;
     switch (in.op) {
       case OP_QKV: req[0] = h_writer; return 1;
-      case OP_ATTN: req[0] = 1 + 6 * l + 0; return 1;
+      case OP_ATTN:
+      case OP_ATTN_POOL: req[0] = 1 + 6 * l + 0; return 1;
       case OP_ATTN_REDUCE: req[0] = 1 + 6 * l + 1; return 1;
       case OP_OPROJ: req[0] = 1 + 6 * l + (p.merge == MERGE_OP ? 2 : 1); req[1] = h_writer; return 2;
       case OP_UPGATE: req[0] = 1 + 6 * l + 3; return 1;
@@ -606,20 +661,30 @@ std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p)
           if (!f.has(req[r]))
             return fmt("race: cta %lld pc %lld reads data of op group %lld not ordered before it", c, pc[c], req[r]);
         done[c][pc[c]] = f;
-        if (in.op == OP_ATTN && in.a[4] >= 0) {  // arrival; the S-th one merges and signals
-          const int a = in.a[4];
-          arrived[a].merge(f);
-          if (++arrivals[a] == (uint32_t)in.a[3]) {
-            arrivals[a] = 0;
-            if (in.signal_ctr >= 0) {
-              cnt[in.signal_ctr]++;
-              signalers[in.signal_ctr].push_back(arrived[a]);
+        auto run_unit = [&](const Instr& un) {
+          if (un.op == OP_ATTN && un.a[4] >= 0) {  // arrival; the S-th one merges and signals
+            const int a = un.a[4];
+            arrived[a].merge(f);
+            if (++arrivals[a] == (uint32_t)un.a[3]) {
+              arrivals[a] = 0;
+              if (un.signal_ctr >= 0) {
+                cnt[un.signal_ctr]++;
+                signalers[un.signal_ctr].push_back(arrived[a]);
+              }
+              arrived[a] = Bits(n_group);
             }
-            arrived[a] = Bits(n_group);
+          } else if (un.signal_ctr >= 0) {
+            cnt[un.signal_ctr]++;
+            signalers[un.signal_ctr].push_back(f);
           }
-        } else if (in.signal_ctr >= 0) {
-          cnt[in.signal_ctr]++;
-          signalers[in.signal_ctr].push_back(f);
+        };
+        if (in.op == OP_ATTN_POOL) {
+          if (!pool_run[in.a[0]]) {  // the first claim loop of the layer runs every unit
+            pool_run[in.a[0]] = 1;
+            for (int u = in.a[0]; u < in.a[0] + in.a[1]; ++u) run_unit(p.pool[u]);
+          }
+        } else {
+          run_unit(in);
         }
         pc[c]++;
         progress = true;
@@ -642,8 +707,8 @@ std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p)
     for (long long i = a; i < a + n; ++i) v[i]++;
     return true;
   };
-  for (int c = 0; c < n_cta; ++c)
-    for (const auto& in : p.queues[c]) {
+  for (int c = 0; c <= n_cta; ++c)
+    for (const auto& in : c < n_cta ? p.queues[c] : p.pool) {
       bool ok = true;
       const int l = in.layer;
       switch (in.op) {

@@ -43,6 +43,9 @@ struct Plan {
   std::vector<std::vector<std::vector<Instr>>> phase_queues;
   int64_t weight_bytes = 0;               // streamed weight bytes per step
   int merge = MERGE_OP;                   // MergeMode of the KV-split partials
+  // dynamic attention (attn_pool): each layer's ATTENTION units, in claim order (split-major),
+  // layer after layer; the queues hold one OP_ATTN_POOL per layer whose a0 indexes this array
+  std::vector<Instr> pool;
 };
 
 // device addresses the host writes into the instructions (see the layout in mk_internal.h)
@@ -65,8 +68,10 @@ void arena_layout(const ModelShape& m, const Geometry& g, int rows, DevState* S)
 // returns "" on success, else a message
 std::string make_geometry(const ModelShape& m, int n_cta, int page_bytes, int n_pages_req, int kv_splits,
                           int smem_limit, Geometry* g);
+// attn_pool: ATTENTION units claimed at run time from a per-layer pool instead of dealt to
+// the CTAs' queues (persistent control only: the multi-launch phases keep static units)
 std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B, int drop_signal, int merge,
-                       Plan* p);
+                       Plan* p, bool attn_pool = false);
 // the merge a schedule of batch B uses: `requested` 1 or 2 (mk_options.attn_merge), or 0 =
 // in the O-proj staging while one step's partials stay under kMergeInBytes, else the
 // separate step of the sync mode

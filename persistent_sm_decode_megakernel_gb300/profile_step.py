@@ -23,7 +23,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-OPS = {1: "embed", 2: "qkv", 3: "attn", 4: "reduce", 5: "oproj", 6: "upgate", 7: "down", 8: "lmhead"}
+OPS = {1: "embed", 2: "qkv", 3: "attn", 4: "reduce", 5: "oproj", 6: "upgate", 7: "down", 8: "lmhead", 9: "attn_pool"}
 
 
 GEMV_OPS = (2, 5, 6, 7, 8)
@@ -137,6 +137,7 @@ def main():
     ap.add_argument("--merge", type=int, default=0, help="KV-split merge: 0 auto, 1 separate step, 2 in O-proj")
     ap.add_argument("--inflight", type=int, default=0, help="page copies in flight per CTA (0: default, <0: pool)")
     ap.add_argument("--split-min", type=int, default=0)
+    ap.add_argument("--pool", type=int, default=0, help="attention units claimed from a per-layer pool")
     ap.add_argument("--synthetic-kv", action="store_true",
                     help="fill the first --prompt cache positions with seeded synthetic keys/values instead of a prefill")
     ap.add_argument("--json", default="")
@@ -159,7 +160,7 @@ def main():
                       exec_mode={"persistent": 0, "multilaunch": 1, "graph": 2}[args.exec], trace=1 if args.trace else 0,
                       page_bytes=args.page_bytes, n_pages=args.n_pages, backoff_max_ns=args.backoff,
                       split_min_positions=args.split_min, attn_merge=args.merge,
-                      inflight_pages=args.inflight, stream=stream)
+                      inflight_pages=args.inflight, attn_pool=args.pool, stream=stream)
         prompt = synth.gen_prompts(cfg, B, args.prompt)
         if args.synthetic_kv:
             for l in range(cfg.n_layers):

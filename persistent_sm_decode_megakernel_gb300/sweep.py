@@ -16,7 +16,7 @@ Each part prints one JSON object (and all of them go to --json):
   ragged    batches of 8 and 16 at 32768 cached positions for all sequences against
             positions spread evenly over 8192..32767: step time, and from the journal the
             attention phase's tail per layer (the last CTA's attention end minus the median
-            CTA's: the room a dynamic queue of attention units would have)
+            CTA's), with the attention units dealt to fixed queues and claimed from a pool
   ctx8k     the 8b model at 8192 cached positions, batch 1, both sync modes
   prefill   mk_prefill wall time of the 2b model: 512- and 32768-token prompts in chunks,
             and the 512-token prompt fed one position per mk_decode_step launch
@@ -145,7 +145,7 @@ def _attn_tail(trace):
     last, downs = {}, {}
     for r in trace:
         cta, op, layer, t_end = r[0], r[2], r[3], r[6]
-        if op == 3:
+        if op in (3, 9):
             k = (layer, cta)
             last[k] = max(last.get(k, 0), t_end)
         elif op == 7:
@@ -171,19 +171,23 @@ def part_ragged():
     dm = DeviceModel(cfg, w, max_batch=16, max_ctx=T + 16)
     _fill_kv(dm, cfg, 16, T)
     out = {}
-    for B in (8, 16):
+    for B in (1, 8, 16):
         for kind in ("uniform", "ragged"):
+            if B == 1 and kind == "ragged":
+                continue
             pos = [T] * B if kind == "uniform" else [8192 + (T - 8192) * b // B for b in range(B)]
-            dec = Decoder(dm, sync_mode=1)
-            us, _, _ = _time_steps(dec, [1] * B, pos, n_warm=2, n=4)
-            dec.close()
-            dec = Decoder(dm, sync_mode=1, trace=1)
-            _time_steps(dec, [1] * B, pos, n_warm=1, n=1)
-            tail, span = _attn_tail(dec.trace())
-            dec.close()
-            out[f"B{B}_{kind}"] = {"us_per_step": us, "attn_tail_us": tail, "layer_us": span,
-                                   "tail_share_of_layer": tail / span, "positions": [min(pos), max(pos)]}
-            print(json.dumps({f"B{B}_{kind}": out[f"B{B}_{kind}"]}), flush=True)
+            for pool in (0, 1):
+                dec = Decoder(dm, sync_mode=1, attn_pool=pool)
+                us, _, _ = _time_steps(dec, [1] * B, pos, n_warm=2, n=4)
+                dec.close()
+                dec = Decoder(dm, sync_mode=1, trace=1, attn_pool=pool)
+                _time_steps(dec, [1] * B, pos, n_warm=1, n=1)
+                tail, span = _attn_tail(dec.trace())
+                dec.close()
+                key = f"B{B}_{kind}{'_pool' if pool else ''}"
+                out[key] = {"us_per_step": us, "attn_tail_us": tail, "layer_us": span,
+                            "tail_share_of_layer": tail / span, "positions": [min(pos), max(pos)]}
+                print(json.dumps({key: out[key]}), flush=True)
     return out
 
 

@@ -138,3 +138,25 @@ def test_create_rejects_null_and_misaligned_pointers(mk):
     kv = mk.mk_kv(P, P)
     st = mk.mk_create(ctypes.byref(d), ctypes.byref(w), ctypes.byref(kv), ctypes.byref(o), None, ctypes.byref(h))
     assert st == mk.MK_ERR_INVALID and b"aligned" in mk.mk_last_error()
+
+
+@pytest.mark.parametrize("name,max_batch", [("tiny", 1), ("tiny", 4), ("2b", 1), ("2b", 16), ("8b", 2)])
+@pytest.mark.parametrize("sync", [0, 1])
+def test_plan_with_attention_pool_validates(mk, name, max_batch, sync):
+    """Dynamic attention (one claim loop per CTA and layer, the units in per-layer pools):
+    the validator runs each pool whole on the first CTA that reaches it and checks
+    coverage, signal counts and ordering as for static units; the instruction count
+    is the static plan's minus the units plus the claim loops."""
+    cfg = synth.CONFIGS[name]
+    d = _desc(mk, cfg, max_batch=max_batch)
+    st0, static = _plan(mk, d, 152, sync_mode=sync)
+    st1, pooled = _plan(mk, d, 152, sync_mode=sync, attn_pool=1)
+    assert st0 == mk.MK_OK and st1 == mk.MK_OK, mk.mk_last_error()
+    assert pooled.n_instructions == static.n_instructions + 152 * cfg.n_layers
+    assert pooled.n_counters == static.n_counters + cfg.n_layers   # one claim counter per layer
+
+
+def test_attention_pool_option_range(mk):
+    cfg = synth.CONFIGS["tiny"]
+    st, _ = _plan(mk, _desc(mk, cfg), 152, attn_pool=1, exec_mode=1)   # multi-launch: static units
+    assert st == mk.MK_OK

@@ -15,7 +15,8 @@
   of a batch must also match that sequence at the smallest batch that holds it
   (batch invariance).  The same cache is decoded by the persistent kernel with counter
   sync (every batch), with NaN-sentinel sync and by the multi-launch control (batches 1
-  and 8); the token mk_decode_step returns is checked against the oracle's argmax.
+  and 8), and with the attention units claimed from a pool (batches 8 and 16); the token
+  mk_decode_step returns is checked against the oracle's argmax.
 """
 import numpy as np
 import pytest
@@ -135,15 +136,17 @@ def long_ctx(lib):
     return cfg, dm, toks, zref, {}
 
 
-ARMS = [(B, 0, 0) for B in (1, 2, 4, 8, 16)] + [(1, 1, 0), (8, 1, 0), (1, 0, 1), (8, 0, 1)]
+# (batch, sync, exec, attention pool)
+ARMS = [(B, 0, 0, 0) for B in (1, 2, 4, 8, 16)] + [(1, 1, 0, 0), (8, 1, 0, 0), (1, 0, 1, 0), (8, 0, 1, 0),
+                                                   (8, 0, 0, 1), (16, 1, 0, 1)]
 
 
-@pytest.mark.parametrize("B,sync,execm", ARMS,
+@pytest.mark.parametrize("B,sync,execm,pool", ARMS,
                          ids=[f"B{b}-{'sentinel' if s else 'counter'}-{'multilaunch' if e else 'persistent'}"
-                              for b, s, e in ARMS])
-def test_2b_32k_context_batches(long_ctx, lib, B, sync, execm):
+                              f"{'-pool' if q else ''}" for b, s, e, q in ARMS])
+def test_2b_32k_context_batches(long_ctx, lib, B, sync, execm, pool):
     cfg, dm, toks, zref, seen = long_ctx
-    dec = lib.Decoder(dm, sync_mode=sync, exec_mode=execm)
+    dec = lib.Decoder(dm, sync_mode=sync, exec_mode=execm, attn_pool=pool)
     logits = torch.zeros((B, cfg.vocab), dtype=torch.float32, device=dm.device)
     z, tk = [], []
     for t in range(N_STEPS):

@@ -337,3 +337,60 @@ def test_tiny_g4_long_context_chunked(lib, sync, kv_splits):
     z, tg = gpu_teacher_forced(dec, prompt, toks, n_new, cfg.vocab)
     dec.close()
     assert_parity(z, tg, zref, toks, P)
+
+
+@pytest.mark.parametrize("sync", [0, 1], ids=["counter", "sentinel"])
+@pytest.mark.parametrize("B", [1, 4])
+def test_attention_pool_matches_static_units(lib, tiny, sync, B):
+    """Dynamic work queue of the attention units (§8.8: each CTA's loader claims units of
+    the layer's pool as its ring frees): a unit computes the same thing on whichever CTA
+    claims it and the split merge keeps its fixed order, so the logits equal the static
+    placement's bit for bit -- at a 600-position context (many splits per sequence and
+    head), at batch 1 and 4 -- and match the oracle."""
+    cfg, w, m = tiny
+    P, n = 600, 3
+    seqs = synth.gen_prompts(cfg, B, P + n)
+    zs = []
+    for pool in (0, 1):
+        dm = lib.DeviceModel(cfg, w, max_batch=B, max_ctx=P + n + 1)
+        dec = lib.Decoder(dm, sync_mode=sync, attn_pool=pool)
+        dec.prefill(seqs[:, :P])
+        logits = torch.zeros((B, cfg.vocab), dtype=torch.float32, device=dm.device)
+        z = []
+        for t in range(n):
+            dec.decode_step(seqs[:, P + t], [P + t] * B, logits=logits)
+            z.append(logits.cpu().numpy().copy())
+        dec.close()
+        zs.append(np.stack(z))
+    np.testing.assert_array_equal(zs[0], zs[1])
+    cache = oracle.KVCache(cfg, B, P + n)
+    oracle.prefill(m, seqs[:, :P], cache)
+    for t in range(n):
+        zr = oracle.decode_step(m, cache, seqs[:, P + t], [P + t] * B)
+        for b in range(B):
+            assert np.abs(zs[1][t, b] - zr[b]).max() <= 1e-2 * np.abs(zr[b]).max()
+
+
+@pytest.mark.parametrize("sync", [0, 1], ids=["counter", "sentinel"])
+def test_attention_pool_multi_step_launch(lib, tiny, sync):
+    """Several greedy steps in one launch with the attention pool: the loader's claims of a
+    later step count against that step's epoch while the compute warps finish the one
+    before; the tokens equal those of one launch per step."""
+    cfg, w, m = tiny
+    P, n, B = 40, 7, 2
+    prompt = synth.gen_prompts(cfg, B, P)
+    runs = []
+    for one_launch in (True, False):
+        dm = lib.DeviceModel(cfg, w, max_batch=B, max_ctx=P + n + 1)
+        dec = lib.Decoder(dm, sync_mode=sync, attn_pool=1)
+        first = dec.prefill(prompt)
+        out = torch.zeros((n, B), dtype=torch.int32, device=dm.device)
+        if one_launch:
+            dec.decode_steps(first, [P] * B, n, out)
+        else:
+            for k in range(n):
+                dec.decode_steps(first if k == 0 else None, [P + k] * B, 1, out[k:k + 1])
+        dec.synchronize()
+        runs.append(out.cpu().numpy().copy())
+        dec.close()
+    np.testing.assert_array_equal(runs[0], runs[1])
