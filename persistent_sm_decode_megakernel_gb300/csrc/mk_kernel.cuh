@@ -250,7 +250,11 @@ __device__ __forceinline__ int active_splits(const DevState& S, const StepArgs& 
   const int npos = A.p0[b] + 1;
   const int pmin = S.split_min_positions;
   const int per_cta = max(1, S.n_cta / (A.B * S.Hkv));
-  const int want = max(per_cta, (npos + kSplitLongPositions - 1) / kSplitLongPositions);
+  int want = max(per_cta, (npos + kSplitLongPositions - 1) / kSplitLongPositions);
+  // a long context that needs more than half the schedule's splits takes all of them: the
+  // schedule deals S units per (sequence, head) evenly over the CTAs, so a step whose
+  // sequences all do that leaves no CTA a unit more than another
+  if (2 * want > S.S) want = S.S;
   return max(1, min(S.S, min((npos + pmin - 1) / pmin, want)));
 }
 __device__ __forceinline__ Attn make_attn(const DevState& S, const StepArgs& A, const Instr& in) {
