@@ -104,3 +104,38 @@ def test_prefill_then_decode_chain(lib):
     dec.close()
     np.testing.assert_array_equal(first, toks[:, P])
     np.testing.assert_array_equal(got.T, toks[:, P + 1: P + 1 + n])
+
+
+def test_tiny_prefill_32k_equals_stepwise_decode(lib):
+    """A 32768-token prompt (2048 chunks, attention over up to 32k cached positions per
+    row): prefill in chunks and the same prompt fed one position per decode step leave the
+    same cache (sampled positions, each entry within one storage ulp plus 1e-3 of the
+    largest magnitude) and give the same last-position logits (1e-2 of the largest) --
+    prefill equals incremental decode, a property that holds at any length, where the
+    fp64 oracle's causal prefill would need 8 GB score matrices per head."""
+    cfg = synth.CONFIGS["tiny"]
+    w = synth.gen_weights(cfg)
+    P = 32768
+    prompt = synth.gen_prompts(cfg, 1, P)
+    out = []
+    for chunked in (True, False):
+        dm = lib.DeviceModel(cfg, w, max_batch=1, max_ctx=P + 1)
+        dec = lib.Decoder(dm, sync_mode=1)
+        logits = torch.zeros((1, cfg.vocab), dtype=torch.float32, device=dm.device)
+        if chunked:
+            dec.prefill(prompt, logits=logits)
+        else:
+            for t in range(P):
+                dec.decode_step(prompt[:, t], [t], logits=logits if t == P - 1 else None)
+        dec.close()
+        idx = torch.as_tensor(np.r_[np.arange(0, P, 997), np.arange(P - 16, P)], device=dm.device)
+        caches = [np.stack([oracle.upcast(c[0][:, idx].cpu().numpy().view(np.uint16), cfg.dtype)
+                            for c in (dm.k_cache[l], dm.v_cache[l])]) for l in range(cfg.n_layers)]
+        out.append((logits.cpu().numpy()[0], caches))
+        del dm
+    (za, ca), (zb, cb) = out
+    assert np.abs(za - zb).max() <= LOGIT_RTOL * np.abs(zb).max()
+    for l in range(cfg.n_layers):
+        err = np.abs(ca[l] - cb[l])
+        bound = ULP_REL[cfg.dtype] * np.abs(cb[l]) + 1e-3 * np.abs(cb[l]).max()
+        assert np.all(err <= bound), f"layer {l}: cache err {err.max():.3e}"
