@@ -246,6 +246,16 @@ mk_status mk_barrier_bench(int mode, int n_barriers, double *us_per_barrier);
  * (each is bounded at 2 s). */
 mk_status mk_die_map(int reps, int max_sm, int *die_of_sm, float *rtt_cycles, int *n_sm);
 
+/* L2 line latency from two SMs (the address -> die interleave, "7 · AMD et le monokernel",
+ * §7.4).  Allocates a zeroed device buffer of buf_bytes (freed before returning) and, for
+ * each byte offset offsets host [n] (4-byte aligned, inside the buffer), times from the SM
+ * with id sm_a and from sm_b a chain of reps >= 2 dependent L2-only loads of that line; lat_a,
+ * lat_b host [n] receive the mean SM clock cycles per load (NaN if no CTA ran on that SM).
+ * The line's home die is the one whose SM sees the shorter time.  MK_ERR_INVALID for bad
+ * arguments (nothing launched). */
+mk_status mk_line_latency(long long buf_bytes, const int64_t *offsets, int n, int sm_a, int sm_b, int reps,
+                          float *lat_a, float *lat_b);
+
 /* Two-means split of n >= 2 values (host only): group host [n] receives 0 for values at
  * or below the threshold, 1 above; *threshold (or NULL) the midpoint between the two
  * group means after convergence.  All values equal: every value in group 0. */

@@ -92,6 +92,8 @@ mk_die_map = _fn("mk_die_map", [c_int, c_int, ctypes.POINTER(c_int), ctypes.POIN
                                 ctypes.POINTER(c_int)])
 mk_two_groups = _fn("mk_two_groups", [ctypes.POINTER(ctypes.c_float), c_int, ctypes.POINTER(c_int),
                                       ctypes.POINTER(ctypes.c_float)])
+mk_line_latency = _fn("mk_line_latency", [ctypes.c_longlong, ctypes.POINTER(ctypes.c_int64), c_int, c_int, c_int, c_int,
+                                          ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)])
 mk_stream_bench = _fn("mk_stream_bench", [c_int, c_int, c_int, c_int, ctypes.c_longlong, ctypes.POINTER(c_double)])
 mk_decode_step_noalloc = _fn("mk_decode_step_noalloc", [ctypes.POINTER(mk_model_desc), ctypes.POINTER(mk_weights),
                                                         ctypes.POINTER(mk_kv), P_i32, P_i32, c_int, P_i32, c_void_p,

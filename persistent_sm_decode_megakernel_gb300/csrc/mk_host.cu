@@ -1093,6 +1093,43 @@ mk_status mk_die_map(int reps, int max_sm, int* die_of_sm, float* rtt_cycles, in
   return MK_OK;
 }
 
+mk_status mk_line_latency(long long buf_bytes, const int64_t* offsets, int n, int sm_a, int sm_b, int reps,
+                          float* lat_a, float* lat_b) {
+  if (!offsets || !lat_a || !lat_b || n < 1 || reps < 2 || buf_bytes < 4 || buf_bytes > (1LL << 34))
+    return fail(MK_ERR_INVALID, "line latency: NULL argument or bad size");
+  for (int i = 0; i < n; ++i)
+    if (offsets[i] < 0 || offsets[i] > buf_bytes - 4 || (offsets[i] & 3))
+      return fail(MK_ERR_INVALID, "line latency: an offset is outside the buffer or not 4-byte aligned");
+  int dev = 0, n_sm = 0, smem_optin = 0;
+  MK_CUDA(cudaGetDevice(&dev));
+  MK_CUDA(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
+  MK_CUDA(cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+  if (sm_a < 0 || sm_b < 0 || sm_a >= n_sm || sm_b >= n_sm || sm_a == sm_b)
+    return fail(MK_ERR_INVALID, "line latency: sm_a and sm_b must be two different SM ids");
+  const int smem = smem_optin / 2 + 1024;  // exactly one CTA per SM, so both SMs run one
+  const void* fn = line_lat_kernel_entry();
+  MK_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+  int bpsm = 0;
+  MK_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bpsm, fn, 32, smem));
+  if (bpsm != 1) return fail(MK_ERR_OCCUPANCY, "line latency: the probe does not run one CTA per SM");
+  DevBuf buf, offs, lat;
+  MK_CUDA(cudaMalloc(&buf.p, (size_t)buf_bytes));
+  MK_CUDA(cudaMemset(buf.p, 0, (size_t)buf_bytes));
+  MK_CUDA(cudaMalloc(&offs.p, sizeof(long long) * n));
+  MK_CUDA(cudaMemcpy(offs.p, offsets, sizeof(long long) * n, cudaMemcpyHostToDevice));
+  MK_CUDA(cudaMalloc(&lat.p, sizeof(float) * 2 * n));
+  MK_CUDA(cudaMemset(lat.p, 0xFF, sizeof(float) * 2 * n));  // NaN: not measured
+  const uint32_t* bp = reinterpret_cast<const uint32_t*>(buf.p);
+  const long long* op = reinterpret_cast<const long long*>(offs.p);
+  float* lp = reinterpret_cast<float*>(lat.p);
+  void* args[7] = {&bp, &op, &n, &sm_a, &sm_b, &reps, &lp};
+  MK_CUDA(cudaLaunchCooperativeKernel(fn, dim3(n_sm), dim3(32), args, smem, nullptr));
+  MK_CUDA(cudaDeviceSynchronize());
+  MK_CUDA(cudaMemcpy(lat_a, lp, sizeof(float) * n, cudaMemcpyDeviceToHost));
+  MK_CUDA(cudaMemcpy(lat_b, lp + n, sizeof(float) * n, cudaMemcpyDeviceToHost));
+  return MK_OK;
+}
+
 mk_status mk_barrier_bench(int mode, int n_barriers, double* us_per_barrier) {
   if (!us_per_barrier || n_barriers < 1 || (mode != 0 && mode != 1))
     return fail(MK_ERR_INVALID, "mode must be 0/1, n_barriers >= 1");

@@ -108,6 +108,40 @@ __global__ void __launch_bounds__(32, 1) mk_rtt_kernel(uint32_t* words, int reps
   }
 }
 
+// ---------------------------------------------------------------- L2 line latency from two SMs
+// Which die's L2 holds a line (the address -> die interleave): one CTA per SM; the CTAs on
+// sm_a and sm_b each time, for every offset, a chain of reps (>= 2) dependent L2-only loads
+// of that line and store the mean cycles per load.  The buffer is all zeros (the host
+// clears it and nothing writes it), so each next address -- the line plus the value just
+// loaded -- is the line itself, yet the hardware cannot issue a load before the previous
+// one returns.  No waits.
+__global__ void __launch_bounds__(32, 1) mk_line_lat_kernel(const uint32_t* buf, const long long* offs, int n,
+                                                            int sm_a, int sm_b, int reps, float* lat) {
+  if (threadIdx.x != 0) return;
+  uint32_t sm;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+  const int which = sm == (uint32_t)sm_a ? 0 : (sm == (uint32_t)sm_b ? 1 : -1);
+  if (which < 0) return;
+  uint32_t acc = 0;
+  for (int i = 0; i < n; ++i) {
+    const uint32_t* p = buf + offs[i] / 4;
+    uint32_t v;
+    asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");  // into L2
+    const uint32_t* q = p + v;
+    long long t0, t1;
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(t0) :: "memory");
+    for (int r = 0; r < reps; ++r) {
+      asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(v) : "l"(q) : "memory");
+      q = p + v;
+    }
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(t1) :: "memory");
+    acc += v;
+    // the last load is issued, not completed, by t1: reps - 1 full latencies
+    lat[which * n + i] = (float)(t1 - t0) / (float)(reps - 1);
+  }
+  if (acc) lat[which * n] = -1.f;  // never: the buffer is zeros (keeps the chain's last load)
+}
+
 // ---------------------------------------------------------------- page-stream microbenchmark
 // The decode kernel's loader / compute-warp structure with nothing else: one lane of the
 // loader warp streams bytes_per_cta of contiguous HBM through a ring of n_pages pages
@@ -254,5 +288,6 @@ const void* step_kernel_entry(int dtype, int sync_mode, bool multi_step) {
 const void* barrier_kernel_entry() { return reinterpret_cast<const void*>(&mk_barrier_kernel); }
 const void* rtt_kernel_entry() { return reinterpret_cast<const void*>(&mk_rtt_kernel); }
 const void* stream_kernel_entry() { return reinterpret_cast<const void*>(&mk_stream_kernel); }
+const void* line_lat_kernel_entry() { return reinterpret_cast<const void*>(&mk_line_lat_kernel); }
 
 }  // namespace mk

@@ -11,4 +11,6 @@ const void* barrier_kernel_entry();
 const void* rtt_kernel_entry();
 // page-stream microbenchmark kernel
 const void* stream_kernel_entry();
+// L2 line latency probe (address -> die interleave)
+const void* line_lat_kernel_entry();
 }  // namespace mk

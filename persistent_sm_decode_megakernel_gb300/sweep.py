@@ -20,6 +20,9 @@ Each part prints one JSON object (and all of them go to --json):
   ctx8k     the 8b model at 8192 cached positions, batch 1, both sync modes
   prefill   mk_prefill wall time of the 2b model: 512- and 32768-token prompts in chunks,
             and the 512-token prompt fed one position per mk_decode_step launch
+  dies      the SM -> die map and the address -> die interleave (§7.4): L2 latency of every
+            256-byte line of an 8 MB buffer from an SM of each group; near / far medians
+            and how often the four lines of a 1 KB block share a home
 The caches of the long-context parts hold synthetic keys and values (normal, std 0.9),
 drawn on the device: the timings do not depend on the values.
 """
@@ -243,8 +246,34 @@ def part_prefill():
     return out
 
 
+def part_dies():
+    import numpy as np
+    import persistent_sm_decode_megakernel_gb300 as mk
+    n_max = 512
+    die = (ctypes.c_int * n_max)()
+    rtt = (ctypes.c_float * n_max)()
+    nsm = ctypes.c_int()
+    mk.check(mk.mk_die_map(6, n_max, die, rtt, ctypes.byref(nsm)), "mk_die_map")
+    groups = [[i for i in range(nsm.value) if die[i] == g] for g in (0, 1)]
+    offs = np.arange(0, 8 << 20, 256, dtype=np.int64)
+    la = (ctypes.c_float * len(offs))()
+    lb = (ctypes.c_float * len(offs))()
+    mk.check(mk.mk_line_latency(8 << 20, offs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), len(offs),
+                                groups[0][1], groups[1][1], 8, la, lb), "mk_line_latency")
+    a, b = np.array(la[:]), np.array(lb[:])
+    d = a - b
+    near_a = d < 0
+    blocks = near_a.reshape(-1, 4).sum(axis=1)
+    return {"sm_groups": [len(g) for g in groups], "probe_sms": [groups[0][1], groups[1][1]],
+            "rtt_cycles_med_per_group": [float(np.median([rtt[i] for i in g if rtt[i] > 0])) for g in groups],
+            "line_cycles_near_med": float(np.median(np.where(near_a, a, b))),
+            "line_cycles_far_med": float(np.median(np.where(near_a, b, a))),
+            "lines_near_first_sm": float(np.mean(near_a)),
+            "kb_blocks_one_home": float(np.mean((blocks == 0) | (blocks == 4)))}
+
+
 PARTS = {"barrier": part_barrier, "launch": part_launch, "ctx32k": part_ctx32k, "ragged": part_ragged,
-         "ctx8k": part_ctx8k, "prefill": part_prefill}
+         "ctx8k": part_ctx8k, "prefill": part_prefill, "dies": part_dies}
 
 
 def main():

@@ -77,3 +77,47 @@ def test_die_map_covers_every_sm(mk):
     x[x == 0] = x[x > 0].min()
     _, g, _ = _groups(mk, x)
     np.testing.assert_array_equal(g, d[used])
+
+
+def test_line_latency_arguments_checked_on_host():
+    import ctypes
+    import numpy as np
+    import persistent_sm_decode_megakernel_gb300 as mk
+    la = (ctypes.c_float * 2)()
+    lb = (ctypes.c_float * 2)()
+    for offs in ([0, 4096], [0, 1 << 20]):   # the second lies outside the 64 KB buffer
+        o = np.array(offs, dtype=np.int64)
+        st = mk.mk_line_latency(1 << 16, o.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), 2, 0, 1, 1, la, lb)
+        assert st == mk.MK_ERR_INVALID   # reps < 2, then an offset out of range: nothing launched
+    o = np.array([0, 2], dtype=np.int64)  # not 4-byte aligned
+    st = mk.mk_line_latency(1 << 16, o.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), 2, 0, 1, 8, la, lb)
+    assert st == mk.MK_ERR_INVALID
+
+
+@pytest.mark.gpu
+def test_line_latency_from_both_dies():
+    """Every sampled line has a finite L2 latency from an SM of each group, and the lines
+    split into ones nearer to the first SM and ones nearer to the second (the address ->
+    die interleave)."""
+    import ctypes
+    import numpy as np
+    import __graft_entry__
+    __graft_entry__.build()
+    import persistent_sm_decode_megakernel_gb300 as mk
+    n_max = 512
+    die = (ctypes.c_int * n_max)()
+    nsm = ctypes.c_int()
+    assert mk.mk_die_map(6, n_max, die, None, ctypes.byref(nsm)) == mk.MK_OK, mk.mk_last_error()
+    groups = [[i for i in range(nsm.value) if die[i] == g] for g in (0, 1)]
+    assert groups[0] and groups[1]
+    offs = np.arange(0, 1 << 20, 256, dtype=np.int64)
+    la = (ctypes.c_float * len(offs))()
+    lb = (ctypes.c_float * len(offs))()
+    st = mk.mk_line_latency(1 << 20, offs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), len(offs), groups[0][1],
+                            groups[1][1], 8, la, lb)
+    assert st == mk.MK_OK, mk.mk_last_error()
+    a, b = np.array(la[:]), np.array(lb[:])
+    assert np.all(np.isfinite(a)) and np.all(np.isfinite(b)), "a probe SM measured nothing"
+    assert a.min() > 50 and b.min() > 50, f"latencies {a.min()}, {b.min()} cycles"
+    d = a - b
+    assert 0.1 < np.mean(d < 0) < 0.9, f"share of lines nearer the first SM {np.mean(d < 0):.3f}"
