@@ -1,6 +1,8 @@
 """Benchmark: batch-1 greedy decode of the 2B fp16 workload through the persistent
-megakernel, one launch per decode step (--steps-per-launch C: C chained steps per launch
-of mk_decode_steps, 0 = all K in one launch; measured the same within noise).
+megakernel, all K timed steps in ONE launch of mk_decode_steps (the monokernel runs the whole
+generation; --steps-per-launch C: C chained steps per launch instead, 1 = one launch per
+step, measured ~1.4 % slower: the launch boundary costs a little more than the in-kernel
+step boundary).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -12,7 +14,7 @@ between steps.  Prints one JSON line (rank 0).
 
 value: tok/s with everything resident in HBM: K chained steps (each step embeds the
 token the previous step chose on the device), CUDA events on the context's stream
-around every launch.
+around every launch (one launch by default).
 e2e: the same metric through mk_decode_step with host token buffers (token and position
 travel as kernel parameters; the step's tokens and status come back through an 80-byte
 mapped host mailbox the kernel writes), host loop included.
@@ -254,7 +256,7 @@ def main():
     ap.add_argument("--sync", default="sentinel", choices=["counter", "sentinel"])
     ap.add_argument("--exec", default="persistent", choices=["persistent", "multilaunch", "graph"])
     ap.add_argument("--batch", type=int, default=1)
-    ap.add_argument("--steps-per-launch", type=int, default=1,
+    ap.add_argument("--steps-per-launch", type=int, default=0,
                     help="decode steps per launch (0: all K in one; persistent control only)")
     args = ap.parse_args()
     if args.impl == "reference":

@@ -138,6 +138,7 @@ def main():
     ap.add_argument("--inflight", type=int, default=0, help="page copies in flight per CTA (0: default, <0: pool)")
     ap.add_argument("--split-min", type=int, default=0)
     ap.add_argument("--pool", type=int, default=0, help="attention units claimed from a per-layer pool")
+    ap.add_argument("--kv-splits", type=int, default=0, help="KV splits per (sequence, kv head) in the schedule")
     ap.add_argument("--synthetic-kv", action="store_true",
                     help="fill the first --prompt cache positions with seeded synthetic keys/values instead of a prefill")
     ap.add_argument("--json", default="")
@@ -159,6 +160,7 @@ def main():
         dec = Decoder(dm, sync_mode=0 if args.sync == "counter" else 1,
                       exec_mode={"persistent": 0, "multilaunch": 1, "graph": 2}[args.exec], trace=1 if args.trace else 0,
                       page_bytes=args.page_bytes, n_pages=args.n_pages, backoff_max_ns=args.backoff,
+                      kv_splits=args.kv_splits,
                       split_min_positions=args.split_min, attn_merge=args.merge,
                       inflight_pages=args.inflight, attn_pool=args.pool, stream=stream)
         prompt = synth.gen_prompts(cfg, B, args.prompt)
