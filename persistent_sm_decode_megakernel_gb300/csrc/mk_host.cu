@@ -49,6 +49,7 @@ struct Sched {
   Plan plan;
   int n_instr = 0;
   DevBuf instr, qstart, counters;
+  DevBuf tmaps;                     // tensor maps of the tensor-core pages
   std::vector<DevBuf> ph_instr, ph_qstart;
   uint32_t epoch = 0;
   DevBuf dyn;                       // MK_EXEC_GRAPH: the step's arguments in device memory
@@ -159,6 +160,19 @@ mk_status get_sched_in(mk_ctx* ctx, const ModelShape& m, const Geometry& geo,
   if (ctx->opts.fault_drop_signal <= 0) {
     e = validate_plan(m, geo, sc->plan);
     if (!e.empty()) return fail(MK_ERR_INVALID, "schedule rejected by the validator: " + e);
+  }
+  int nb = 1;
+  while (nb < B) nb <<= 1;
+  if (use_tc(geo, nb)) {
+    std::vector<TmapImage> maps;
+    e = build_tc_maps(m, geo, &sc->plan, &maps);
+    if (!e.empty()) return fail(MK_ERR_CUDA, "tensor maps: " + e);
+    mk_status s = upload(sc->tmaps, maps.data(), maps.size() * sizeof(TmapImage));
+    if (s) return s;
+    const uintptr_t dev = reinterpret_cast<uintptr_t>(sc->tmaps.p);
+    for (auto& q : sc->plan.queues) place_tc_maps(q, dev);
+    for (auto& ph : sc->plan.phase_queues)
+      for (auto& q : ph) place_tc_maps(q, dev);
   }
   mk_status s = upload_queues(sc->plan.queues, sc->instr, sc->qstart, &sc->n_instr, &sc->plan.pool);
   if (s) return s;

@@ -154,7 +154,7 @@ struct DevState {
   // execution
   int n_cta;
   int page_bytes, n_pages;
-  int page_stride;             // bytes between ring slots (>= page_bytes; kTcPageBytes with tc)
+  int page_stride;             // bytes between ring slots (>= page_bytes)
   int tc;                      // batches of 3..16 use the tensor-core GEMV
   int xbuf_bytes, scratch_bytes;
   int smem_bytes;              // dynamic shared memory of a launch with this state (host use)
@@ -201,13 +201,15 @@ struct StepArgs {
   const StepArgs* dyn;
 };
 
-// Tensor-core GEMV (batches of 3..16): a page holds
-// kTcRows weight rows of kTcKw columns (one window of the input), each row followed by a
-// 16-byte skew so that the 8 rows an mma fragment reads sit in different banks.
+// Tensor-core GEMV (batches of 3..16): a page holds kTcRows weight rows of kTcKw columns
+// (one window of the input), landed by one tensor-map copy as kTcKw / 64 column chunks of
+// [kTcRows rows][128 bytes] with the 128-byte swizzle (16-byte granule g of row r stored at
+// g ^ (r % 8)), so that the 8 rows an mma fragment reads sit in different banks.
 constexpr int kTcKw = 1024;
 constexpr int kTcRows = 16;
-constexpr int kTcRowBytes = kTcKw * 2 + 16;
-constexpr int kTcPageBytes = kTcRows * kTcRowBytes;                        // 33024
+constexpr int kTcChunkCols = 64;                          // columns per 128-byte chunk row
+constexpr int kTcChunkBytes = kTcRows * 128;              // one column chunk of a page
+constexpr int kTcPageBytes = kTcRows * kTcKw * 2;         // 32768
 constexpr int kTcPartialFloats = 2 * kConsumerWarps * kTcRows * kMaxBatch;  // double-buffered warp partials
 
 // above this many positions per KV split a step uses all of the schedule's splits

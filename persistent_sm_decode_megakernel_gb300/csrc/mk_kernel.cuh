@@ -415,27 +415,25 @@ __device__ __noinline__ void producer(const DevState& S_arg, const StepArgs& A_a
           }
         }
         if (S.tc && A.B >= 3) {
-          // tensor-core pages: for each window of kTcKw columns, 16-row blocks of the
-          // instruction's rows (segment 0, then segment 1), one bulk copy per row into its
-          // skewed row slot
-          const int K = g.K, R = g.rows(), nw = (K + kTcKw - 1) / kTcKw, nrb = (R + kTcRows - 1) / kTcRows;
+          // tensor-core pages: for each window of kTcKw columns, the 16-row blocks of
+          // segment 0, then of segment 1, each one tensor-map copy (p4 / p5 hold the
+          // segments' maps; rows and columns past the segment land as zeros)
+          const int nw = (g.K + kTcKw - 1) / kTcKw;
           for (int w = 0; w < nw && ok; ++w) {
-            const int kw = min(kTcKw, K - w * kTcKw);
-            for (int rb = 0; rb < nrb; ++rb) {
-              if (!producer_acquire(S, c, slot, ph, issued++)) {
-                ok = false;
-                break;
+            for (int sg = 0; sg < 2 && ok; ++sg) {
+              const void* tm = iptr(in, sg ? kP5 : kP4);
+              const int nrs = (g.segr[sg] + kTcRows - 1) / kTcRows;
+              for (int j = 0; j < nrs; ++j) {
+                if (!producer_acquire(S, c, slot, ph, issued++)) {
+                  ok = false;
+                  break;
+                }
+                mbar_arrive_expect_tx(&c->full[slot], (uint32_t)kTcPageBytes);
+                tma_load_3d(pages + (size_t)slot * S.page_stride, tm, 0, j * kTcRows, w * (kTcKw / kTcChunkCols),
+                            &c->full[slot], pol);
+                c->last_issue_phase[slot] = (int)ph;
+                if (++slot == S.n_pages) { slot = 0; ph ^= 1u; }
               }
-              const int nr = min(kTcRows, R - rb * kTcRows);
-              mbar_arrive_expect_tx(&c->full[slot], (uint32_t)(nr * kw * 2));
-              uint8_t* dst = pages + (size_t)slot * S.page_stride;
-              for (int i = 0; i < nr; ++i) {
-                const int fr = rb * kTcRows + i, sg = fr < g.segr[0] ? 0 : 1, r = sg ? fr - g.segr[0] : fr;
-                tma_load_1d(dst + (size_t)i * kTcRowBytes, g.seg[sg] + (size_t)r * K + (size_t)w * kTcKw,
-                            (uint32_t)(kw * 2), &c->full[slot], pol);
-              }
-              c->last_issue_phase[slot] = (int)ph;
-              if (++slot == S.n_pages) { slot = 0; ph ^= 1u; }
             }
           }
           break;
@@ -1211,7 +1209,9 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, cq = lane & 3;
   const int B = A.B, l = in.layer;
   const Gemv g = make_gemv(S, in);
-  const int K = g.K, R = g.rows(), nw = (K + kTcKw - 1) / kTcKw, nrb = (R + kTcRows - 1) / kTcRows;
+  const int K = g.K, R = g.rows(), nw = (K + kTcKw - 1) / kTcKw;
+  // row blocks: segment 0's, then segment 1's (a page never spans the two)
+  const int nrb0 = (g.segr[0] + kTcRows - 1) / kTcRows, nrb = nrb0 + (g.segr[1] + kTcRows - 1) / kTcRows;
   const bool trace = (A.flags & SF_TRACE) != 0;
   float* part = scratch;                       // [2][warps][kTcRows][NB]
   float* rowacc = scratch + kTcPartialFloats;  // [R][NB]
@@ -1341,12 +1341,16 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
 #pragma unroll
         for (int nb = 0; nb < 2; ++nb) d[mt][nb][0] = d[mt][nb][1] = d[mt][nb][2] = d[mt][nb][3] = 0.f;
       for (int ks = ks0; ks < ks1; ++ks) {
+        // k-step ks: columns 16 ks .. 16 ks + 15 = 16-byte granules 2 (ks % 4) and + 1 of
+        // column chunk ks / 4; row r's granule g sits at g ^ (r % 8), and r % 8 = gq
         uint32_t bw[2][2];
+        const uint8_t* cb = pg + (size_t)(ks >> 2) * kTcChunkBytes + cq * 4;
+        const int g0 = ((ks & 3) * 2) ^ gq;
 #pragma unroll
         for (int nb = 0; nb < 2; ++nb) {
-          const uint8_t* wr = pg + (size_t)(nb * 8 + gq) * kTcRowBytes + (size_t)(ks * 16 + 2 * cq) * 2;
-          bw[nb][0] = *reinterpret_cast<const uint32_t*>(wr);
-          bw[nb][1] = *reinterpret_cast<const uint32_t*>(wr + 16);
+          const uint8_t* wr = cb + (nb * 8 + gq) * 128;
+          bw[nb][0] = *reinterpret_cast<const uint32_t*>(wr + g0 * 16);
+          bw[nb][1] = *reinterpret_cast<const uint32_t*>(wr + (g0 ^ 1) * 16);
         }
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
@@ -1371,8 +1375,10 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
       }
       consumer_sync();
       if (tid < kTcRows * NB) {  // one (row, sequence) per thread: warps summed in a fixed order
-        const int row = tid / NB, sq = tid - row * NB, fr = rb * kTcRows + row;
-        if (fr < R) {
+        const int row = tid / NB, sq = tid - row * NB;
+        const int sg = rb >= nrb0 ? 1 : 0, j = rb - sg * nrb0;
+        const int fr = sg * g.segr[0] + j * kTcRows + row;
+        if (j * kTcRows + row < g.segr[sg]) {
           const float* pr = part + ((size_t)(pcount & 1) * kConsumerWarps * kTcRows + row) * NB + sq;
           float t = 0.f;
 #pragma unroll
@@ -2142,6 +2148,12 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
   uint8_t* pages = smem_pages();
   float* xbuf = smem_xbuf(S);
   float* scratch = smem_scratch(S);
+  // the tensor-core pages are 128-byte swizzled copies, whose destination must sit on a
+  // 1024-byte boundary: refuse to run (an error, not a faulting copy) if it does not
+  if (S.tc && (smem_addr(pages) & 1023u)) {
+    if (tid == 0 && blockIdx.x == 0) set_err(S, 5u /*MK_ERR_STATE*/, -11, (int)(smem_addr(pages) & 1023u));
+    return;
+  }
   if (tid == 0) {
     for (int i = 0; i < S.n_pages; ++i) {
       mbar_init(&c->full[i], 1);

@@ -150,6 +150,13 @@ mk_status prepare(const mk_model_desc& d, const mk_weights* w, const mk_kv* kv, 
   bake_pointers(m, mp, &plan);
   e = validate_plan(m, g, plan);
   if (!e.empty()) return fail(MK_ERR_INVALID, "schedule rejected by the validator: " + e);
+  int nb = 1;
+  while (nb < B) nb <<= 1;
+  std::vector<TmapImage> maps;
+  if (use_tc(g, nb)) {
+    e = build_tc_maps(m, g, &plan, &maps);
+    if (!e.empty()) return fail(MK_ERR_CUDA, "tensor maps: " + e);
+  }
 
   // host images of the read-only tables
   std::vector<Instr> flat;
@@ -183,6 +190,7 @@ mk_status prepare(const mk_model_desc& d, const mk_weights* w, const mk_kv* kv, 
   P->o_rope = take(sizeof(float2) * (size_t)kMaxBatch * (m.hd / 2));
   P->o_q = take(sizeof(int32_t) * qoff.size());
   P->o_ins = take(sizeof(Instr) * flat.size());
+  const size_t o_maps = take(sizeof(TmapImage) * maps.size());
   const size_t o_act = take(sizeof(float) * (size_t)S.act_floats);
   if (cur > kScratchBytes) {
     char buf[200];
@@ -192,6 +200,10 @@ mk_status prepare(const mk_model_desc& d, const mk_weights* w, const mk_kv* kv, 
   }
   NA_CUDA(cudaMemcpyAsync(base + o_ptr, ptrs.data(), sizeof(void*) * ptrs.size(), cudaMemcpyHostToDevice, s));
   NA_CUDA(cudaMemcpyAsync(base + P->o_q, qoff.data(), sizeof(int32_t) * qoff.size(), cudaMemcpyHostToDevice, s));
+  if (!maps.empty()) {
+    place_tc_maps(flat, reinterpret_cast<uintptr_t>(base + o_maps));
+    NA_CUDA(cudaMemcpyAsync(base + o_maps, maps.data(), sizeof(TmapImage) * maps.size(), cudaMemcpyHostToDevice, s));
+  }
   NA_CUDA(cudaMemcpyAsync(base + P->o_ins, flat.data(), sizeof(Instr) * flat.size(), cudaMemcpyHostToDevice, s));
   // the pageable copies above return once their source is consumed: the host vectors may go
 

@@ -104,7 +104,8 @@ std::string make_geometry(const ModelShape& m, int n_cta, int page_bytes, int n_
   g->page_stride = g->page_bytes;
   if (g->tc) {
     if (g->page_bytes != 32768) return "batches of 3 and more need 32 KB pages";
-    if (m.d % 16 || m.F % 16 || (m.Hq * m.hd) % 16) return "batches of 3 and more need dims that are multiples of 16";
+    if (m.d % kTcChunkCols || m.F % kTcChunkCols || (m.Hq * m.hd) % kTcChunkCols)
+      return "batches of 3 and more need d_model, ffn_dim and n_heads*head_dim to be multiples of 64";
     g->page_stride = kTcPageBytes;
   }
   const int max_ws = g->page_bytes / (2 * kConsumerWarps);

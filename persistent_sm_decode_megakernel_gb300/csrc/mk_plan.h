@@ -78,6 +78,17 @@ std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B,
 constexpr long long kMergeInBytes = 24 * 1024;
 int choose_merge(const ModelShape& m, const Geometry& g, int B, bool counters, int requested);
 void bake_pointers(const ModelShape& m, const ModelPtrs& w, Plan* p);
+
+// Tensor-core schedules land each weight page with one tensor-map copy.  build_tc_maps
+// encodes one map per weight segment of every GEMV instruction (segments with the same
+// rows share one) and leaves the map's index + 1 in the instruction's p4 / p5 (0: none);
+// place_tc_maps then turns the indices into the device addresses of the uploaded maps.
+// Call after bake_pointers (the maps are made from the baked row pointers).
+struct TmapImage {
+  alignas(64) unsigned char bytes[128];
+};
+std::string build_tc_maps(const ModelShape& m, const Geometry& g, Plan* p, std::vector<TmapImage>* maps);
+void place_tc_maps(std::vector<Instr>& q, uintptr_t maps_dev);
 std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p);
 
 }  // namespace mk
