@@ -60,19 +60,23 @@ static_assert(sizeof(Instr) == 64, "instruction is 64 bytes");
 
 // Argument layout (the host writes absolute device pointers into the instruction so that
 // neither role has to chase per-layer pointer tables on the critical path):
-//   EMBED   a0 e0, a1 e1 (flattened [B, d] range)
+//   EMBED   a0 e0, a1 e1 (flattened [B, d] range), p2 layer 0's attention gain
 //   QKV     a0 matrix (0 q, 1 k, 2 v), a1 head, a2 first pair i0, a3 pairs n,
 //           p2 gain, p3 cache of this layer (k or v), p4 rows i0.., p5 rows hd/2+i0..
 //   ATTN    a0 b, a1 kv head j, a2 split s, a3 splits S, a4 arrival counter (-1: the
 //           merge is a separate ATTN_REDUCE), p4 keys of (b, j) at t = 0, p5 values
 //   REDUCE  a0 b, a1 j
 //   OPROJ / DOWN   a0 row0, a1 rows, p4 first row (OPROJ with F_MERGE_IN: its input is
-//           merged from the split partials while it is staged)
+//           merged from the split partials while it is staged), p2 the RMSNorm gain of the
+//           output's next consumer (OPROJ: the MLP gain; DOWN: the next layer's attention
+//           gain, or the final gain after the last layer)
 //   UPGATE  a0 row0, a1 rows, p2 gain, p4 gate rows, p5 up rows
 //   LMHEAD  a0 row0, a1 rows, a2 CTAs with LM rows, p2 final gain, p4 first row
 //   POOL    a0 index of the layer's first ATTENTION unit in the instruction array (the pools
 //           follow the queues), a1 units, a2 claim counter, a3 CTAs (a step claims a1 + a3
 //           times: every CTA's last claim comes back empty)
+// With the tensor-core GEMV (batches of 3..16), p4 / p5 of the GEMV ops hold the tensor maps
+// of the row segments instead of the row pointers.
 // pK = the 64-bit value in a[2K], a[2K+1]
 constexpr int kP2 = 4, kP3 = 6, kP4 = 8, kP5 = 10;
 inline void set_ptr(Instr& in, int at, const void* p) {
@@ -114,7 +118,16 @@ struct TraceRec {
   uint64_t t_fetch, t_ready, t_mark[6], t_end;
 };
 
-enum ActKind { ACT_H = 0, ACT_HMID, ACT_Q, ACT_KVN, ACT_PART, ACT_O, ACT_A, ACT_NUM };
+// fp32 activations [rows][width] per layer; with the tensor-core GEMV also the inputs of
+// its ops in fragment form (ACT_HF: RMSNorm gain x h for the next QKV or the LM head,
+// ACT_HMF: gain x h_mid for UP/GATE, ACT_AF: a for DOWN), written by their producers as
+// 16-bit hi/lo halves in the order the mma fragments take them (see frag_index), and the
+// sums of squares of h and h_mid for the RMSNorms, one slot of kMaxBatch floats per
+// producing CTA (ACT_SSH, ACT_SSM: [kMaxSsqSlots][kMaxBatch])
+enum ActKind {
+  ACT_H = 0, ACT_HMID, ACT_Q, ACT_KVN, ACT_PART, ACT_O, ACT_A, ACT_HF, ACT_HMF, ACT_AF, ACT_SSH, ACT_SSM, ACT_NUM
+};
+constexpr int kMaxSsqSlots = 256;  // the tensor-core GEMV runs on at most this many CTAs
 
 struct DevState {
   // model

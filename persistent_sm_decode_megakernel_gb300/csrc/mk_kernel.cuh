@@ -228,6 +228,33 @@ __device__ __forceinline__ Gemv make_gemv(const DevState& S, const Instr& in) {
   return g;
 }
 
+// Fragment form of a tensor-core GEMV input x[b][k] (batch tile of MT * 8 sequences): the
+// 16-bit halves in the order of the m16n8k16 A fragments -- per k-step of 16 columns and
+// tile of 8 sequences, 32 lanes x 4 words, lane g * 4 + c holding sequence g's columns
+// (2c, 2c + 1) in word 0 (hi halves) and 1 (lo halves) and (2c + 8, 2c + 9) in words 2
+// and 3.  Returns the index of x[b][k]'s hi half; its lo half is 2 further.
+__device__ __forceinline__ size_t frag_index(int b, int k, int MT) {
+  const int ks = k >> 4, kk = k & 15, c = (kk & 7) >> 1;
+  return ((((size_t)(ks * MT + (b >> 3)) * 32 + (b & 7) * 4 + c) * 4 + ((kk >> 3) << 1)) << 1) + (kk & 1);
+}
+template <typename WT>
+__device__ __forceinline__ void put_frag(uint16_t* f, int b, int k, int MT, float v) {
+  uint16_t hi, lo;
+  Mma<WT>::split(v, hi, lo);
+  const size_t i = frag_index(b, k, MT);
+  f[i] = hi;
+  f[i + 2] = lo;
+}
+// the batch tiles of 8 sequences of the tensor-core GEMV at a padded batch of NB
+template <int NB>
+constexpr int kFragMT = NB > 8 ? 2 : 1;
+// a word still holding a half of the NaN sentinel (0x7FFF or 0xFFFF: all 15 low bits set,
+// which no finite 16-bit float has)
+__device__ __forceinline__ bool frag_pending(uint32_t w) {
+  const uint32_t x = (w & 0x7FFF7FFFu) ^ 0x7FFF7FFFu;  // a half is zero iff it was a sentinel
+  return ((x - 0x00010001u) & ~x & 0x80008000u) != 0u;
+}
+
 // Split-KV unit (§8.2 ATTENTION): row b (position pos_b of cache sequence seq_b), kv head
 // j, split s of S over positions 0..p0_b.  Cached positions [t0, min(t1, p0_b)) stream
 // through pages as K, V blocks; the split holding position p0_b takes the keys/values of
@@ -592,6 +619,28 @@ __device__ __forceinline__ float warp_sum(float v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
+// This CTA's share of the sums of squares of an RMSNorm input (the tensor-core GEMV's
+// consumer adds the slots of all CTAs): ssp[b] per compute thread, summed over the threads
+// in a fixed order into slot blockIdx.x of kMaxBatch floats (zeros past NB).  All compute
+// threads call it; it uses the control block's reduction array.
+template <int NB>
+__device__ __forceinline__ void put_ssq_slot(SmemCtl* c, const float (&ssp)[NB], float* slots) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    const float t = warp_sum(ssp[b]);
+    if (lane == 0) c->red[warp * NB + b] = t;
+  }
+  consumer_sync();
+  if (tid < kMaxBatch) {
+    float t = 0.f;
+    if (tid < NB)
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) t += c->red[w * NB + tid];
+    slots[(size_t)blockIdx.x * kMaxBatch + tid] = t;
+  }
+  consumer_sync();
+}
 
 // ---------------------------------------------------------------- input staging
 // A producer's fp32 output reaches shared memory through 16-byte loads by every consumer
@@ -670,6 +719,50 @@ __device__ __forceinline__ void load_vecs(const DevState& S, SmemCtl* c, const f
       if (need[u]) v[u] = ld_poll_v4(p[u]);
   }
 }
+
+// Up to U 16-byte fragment vectors of a tensor-core input: vector i (base + u * threads +
+// tid, below n) belongs to sequence ((i / 32) % MT) * 8 + (i % 32) / 4; vectors of
+// sequences >= B are not read and come back as zeros.  With sentinels, vectors still
+// holding a sentinel half are re-read together until the producers' values land
+// (bounded, sets the abort flag on timeout).
+template <int SYNC, int U>
+__device__ __forceinline__ void load_frags(const DevState& S, SmemCtl* c, const uint4* src, int base, int n, int B,
+                                           int MT, uint4 (&v)[U]) {
+  const int tid = threadIdx.x;
+  bool live[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int i = base + u * kConsumerThreads + tid;
+    live[u] = i < n && ((((i >> 5) & (MT - 1)) << 3) + ((i & 31) >> 2)) < B;
+    if (SYNC == SYNC_COUNTER) {
+      v[u] = live[u] ? __ldcg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+    } else {
+      const float4 f = live[u] ? ld_poll_v4(reinterpret_cast<const float4*>(src + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[u] = make_uint4(__float_as_uint(f.x), __float_as_uint(f.y), __float_as_uint(f.z), __float_as_uint(f.w));
+    }
+  }
+  if (SYNC == SYNC_COUNTER) return;
+  uint64_t t0 = 0;
+  for (int k = 0;; ++k) {
+    bool need[U], pend = false;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      need[u] = live[u] && (frag_pending(v[u].x) || frag_pending(v[u].y) || frag_pending(v[u].z) ||
+                            frag_pending(v[u].w));
+      pend |= need[u];
+    }
+    if (!pend) break;
+    if (k == 0) t0 = globaltimer_ns();
+    if (!poll_pause(S, c, k, t0)) break;
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (need[u]) {
+        const float4 f = ld_poll_v4(reinterpret_cast<const float4*>(src + base + u * kConsumerThreads + tid));
+        v[u] = make_uint4(__float_as_uint(f.x), __float_as_uint(f.y), __float_as_uint(f.z), __float_as_uint(f.w));
+      }
+  }
+}
+
 
 template <int SYNC, int U = 4, typename Put>
 __device__ __forceinline__ void stage_vec(const DevState& S, const float4* src, int n4, SmemCtl* c, Put&& put) {
@@ -987,22 +1080,38 @@ __device__ __forceinline__ void gemv_epilogue(const DevState& S, const StepArgs&
       const int row0 = in.a[0];
       const float* hin = act_ptr(S, act, ACT_H, l);
       float* hout = act_ptr(S, act, ACT_HMID, l);
+      uint16_t* fo = reinterpret_cast<uint16_t*>(act_ptr(S, act, ACT_HMF, l));
+      const uint16_t* gn = iptr(in, kP2);
+      float ssp[NB];
+#pragma unroll
+      for (int b = 0; b < NB; ++b) ssp[b] = 0.f;
       for (int t = tid; t < R * B; t += kConsumerThreads) {
         const int r = t % R, b = t / R;
         const size_t idx = (size_t)b * S.d + row0 + r;
         float hv = t == tid ? hres : load_act<SYNC>(hin + idx, S, c);
         if (SYNC == SYNC_SENTINEL && isnan(hv)) hv = poll_slow(hin + idx, S, c);
-        hout[idx] = hv + rowsum(r, b);
+        const float y = hv + rowsum(r, b);
+        hout[idx] = y;
+        if (NB >= 4) {
+          put_frag<WT>(fo, b, row0 + r, kFragMT<NB>, y * Unpack<WT>::one(gn[row0 + r]));
+#pragma unroll
+          for (int bb = 0; bb < NB; ++bb)
+            if (bb == b) ssp[bb] += y * y;
+        }
       }
+      if (NB >= 4) put_ssq_slot<NB>(c, ssp, act_ptr(S, act, ACT_SSM, l));
       break;
     }
     case OP_UPGATE: {
       const int row0 = in.a[0], n = in.a[1];
       float* a = act_ptr(S, act, ACT_A, l);
+      uint16_t* fo = reinterpret_cast<uint16_t*>(act_ptr(S, act, ACT_AF, l));
       for (int t = tid; t < n * B; t += kConsumerThreads) {
         const int r = t % n, b = t / n;
         const float ir = c->inv_rms[b];
-        a[(size_t)b * S.F + row0 + r] = silu_f(rowsum(r, b) * ir) * (rowsum(r + n, b) * ir);
+        const float y = silu_f(rowsum(r, b) * ir) * (rowsum(r + n, b) * ir);
+        a[(size_t)b * S.F + row0 + r] = y;
+        if (NB >= 4) put_frag<WT>(fo, b, row0 + r, kFragMT<NB>, y);
       }
       break;
     }
@@ -1010,13 +1119,26 @@ __device__ __forceinline__ void gemv_epilogue(const DevState& S, const StepArgs&
       const int row0 = in.a[0];
       const float* hin = act_ptr(S, act, ACT_HMID, l);
       float* hout = act_ptr(S, act, ACT_H, l + 1);
+      uint16_t* fo = reinterpret_cast<uint16_t*>(act_ptr(S, act, ACT_HF, l + 1));
+      const uint16_t* gn = iptr(in, kP2);
+      float ssp[NB];
+#pragma unroll
+      for (int b = 0; b < NB; ++b) ssp[b] = 0.f;
       for (int t = tid; t < R * B; t += kConsumerThreads) {
         const int r = t % R, b = t / R;
         const size_t idx = (size_t)b * S.d + row0 + r;
         float hv = t == tid ? hres : load_act<SYNC>(hin + idx, S, c);
         if (SYNC == SYNC_SENTINEL && isnan(hv)) hv = poll_slow(hin + idx, S, c);
-        hout[idx] = hv + rowsum(r, b);
+        const float y = hv + rowsum(r, b);
+        hout[idx] = y;
+        if (NB >= 4) {
+          put_frag<WT>(fo, b, row0 + r, kFragMT<NB>, y * Unpack<WT>::one(gn[row0 + r]));
+#pragma unroll
+          for (int bb = 0; bb < NB; ++bb)
+            if (bb == b) ssp[bb] += y * y;
+        }
       }
+      if (NB >= 4) put_ssq_slot<NB>(c, ssp, act_ptr(S, act, ACT_SSH, l + 1));
       break;
     }
     default: {  // OP_LMHEAD: logits and the running argmax (packed key, lowest index wins ties)
@@ -1218,13 +1340,36 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
   uint32_t* xt = reinterpret_cast<uint32_t*>(xbuf);  // [kstep][MT][lane][4]
   const float* src;
   const uint16_t* gain = nullptr;
+  // the input in fragment form, written by its producers (all inputs but O-proj's, which
+  // is staged from fp32 and split here)
+  const uint4* frag = nullptr;
+  const float* ssq = nullptr;  // with an RMSNorm: the producers' sums of squares
   switch (in.op) {
-    case OP_QKV: src = act_ptr(S, act, ACT_H, l); gain = iptr(in, kP2); break;
-    case OP_UPGATE: src = act_ptr(S, act, ACT_HMID, l); gain = iptr(in, kP2); break;
-    case OP_LMHEAD: src = act_ptr(S, act, ACT_H, S.L); gain = iptr(in, kP2); break;
+    case OP_QKV:
+      src = act_ptr(S, act, ACT_H, l);
+      gain = iptr(in, kP2);
+      frag = reinterpret_cast<const uint4*>(act_ptr(S, act, ACT_HF, l));
+      ssq = act_ptr(S, act, ACT_SSH, l);
+      break;
+    case OP_UPGATE:
+      src = act_ptr(S, act, ACT_HMID, l);
+      gain = iptr(in, kP2);
+      frag = reinterpret_cast<const uint4*>(act_ptr(S, act, ACT_HMF, l));
+      ssq = act_ptr(S, act, ACT_SSM, l);
+      break;
+    case OP_LMHEAD:
+      src = act_ptr(S, act, ACT_H, S.L);
+      gain = iptr(in, kP2);
+      frag = reinterpret_cast<const uint4*>(act_ptr(S, act, ACT_HF, S.L));
+      ssq = act_ptr(S, act, ACT_SSH, S.L);
+      break;
     case OP_OPROJ: src = act_ptr(S, act, ACT_O, l); break;
-    default: src = act_ptr(S, act, ACT_A, l); break;
+    default:
+      src = act_ptr(S, act, ACT_A, l);
+      frag = reinterpret_cast<const uint4*>(act_ptr(S, act, ACT_AF, l));
+      break;
   }
+
   for (int i = tid; i < R * NB; i += kConsumerThreads) rowacc[i] = 0.f;
   // epilogue inputs, prefetched as in the CUDA-core GEMV
   float hres = 0.f;
@@ -1249,13 +1394,46 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
     // 1. the inputs of the next SW windows, split into hi/lo halves in fragment order (8
     //    sequences per tile; sequences >= B are zeros).  The previous window's pages are
     //    done: every warp passed the barrier after its last page.
-    if (w % SW == 0) {
+    if (w % SW == 0 && frag != nullptr) {
+      // a straight copy of the staging's k-steps (slots of sequences >= B are zeros)
+      constexpr int U = 8;
+      const int n16 = (min(SW * kTcKw, K - k0) >> 4) * MT * 32;
+      const uint4* fs = frag + (size_t)(k0 >> 4) * MT * 32;
+      uint4* xd = reinterpret_cast<uint4*>(xt);
+      for (int base = 0; base < n16; base += U * kConsumerThreads) {
+        uint4 v[U];
+        load_frags<SYNC, U>(S, c, fs, base, n16, B, MT, v);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int i = base + u * kConsumerThreads + tid;
+          if (i < n16) xd[i] = v[u];
+        }
+      }
+      // with an RMSNorm: the producers' per-CTA sums of squares of the input (one slot of
+      // kMaxBatch floats per producing CTA), slot tid into this thread's ss[]
+      if (w == 0 && gain != nullptr && tid < S.n_cta) {
+        const float4* sp = reinterpret_cast<const float4*>(ssq + (size_t)tid * kMaxBatch);
+        const float4* pp[NB / 4];
+#pragma unroll
+        for (int q = 0; q < NB / 4; ++q) pp[q] = sp + q;
+        float4 v[NB / 4];
+        load_vecs<SYNC, NB / 4>(S, c, pp, v);
+#pragma unroll
+        for (int q = 0; q < NB / 4; ++q) {
+          ss[4 * q] = v[q].x;
+          ss[4 * q + 1] = v[q].y;
+          ss[4 * q + 2] = v[q].z;
+          ss[4 * q + 3] = v[q].w;
+        }
+      }
+      consumer_sync();
+    } else if (w % SW == 0) {
       constexpr int U = 8;
       const int kws = min(SW * kTcKw, K - k0);
       const int k4n = kws >> 2, n_items = MT * 8 * k4n;
+      // the O-proj input: fp32 rows split into hi/lo halves here
       for (int base = 0; base < n_items; base += U * kConsumerThreads) {
         const float4* pp[U];
-        uint2 gbu[U];  // gains: issued ahead of the polls (they do not depend on the producer)
         // item -> (sequence, vector): at 8 and 16 sequences stepped from the first without
         // a division per item (measured faster there; at 4 the division measured faster)
         const int b0 = (base + tid) / k4n, k40 = base + tid - b0 * k4n;
@@ -1270,7 +1448,6 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
             }
             const bool live = it < n_items && b < B;
             pp[u] = live ? reinterpret_cast<const float4*>(src + (size_t)b * K + k0) + k4 : nullptr;
-            gbu[u] = (live && gain != nullptr) ? __ldg(reinterpret_cast<const uint2*>(gain + k0) + k4) : make_uint2(0u, 0u);
             if (NB >= 8) {
               k4 += kConsumerThreads;
               while (k4 >= k4n) {
@@ -1299,18 +1476,7 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
             }
           }
           if (it >= n_items) continue;
-          float4 x = v[u];
-          if (gain != nullptr && b < B) {
-            const uint2 gb = gbu[u];
-            const float sq = x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
-#pragma unroll
-            for (int bb = 0; bb < NB; ++bb)
-              if (bb == b) ss[bb] += sq;
-            x.x *= Unpack<WT>::one((uint16_t)(gb.x & 0xFFFFu));
-            x.y *= Unpack<WT>::one((uint16_t)(gb.x >> 16));
-            x.z *= Unpack<WT>::one((uint16_t)(gb.y & 0xFFFFu));
-            x.w *= Unpack<WT>::one((uint16_t)(gb.y >> 16));
-          }
+          const float4 x = v[u];
           uint16_t h0, l0, h1, l1, h2, l2, h3, l3;
           Mma<WT>::split(x.x, h0, l0);
           Mma<WT>::split(x.y, h1, l1);
@@ -1390,7 +1556,7 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
       if (trace) page_work_ns += globaltimer_ns() - tr;
     }
   }
-  // 1/rms from the sums of squares taken while staging
+  // 1/rms from the sums of squares
   if (gain != nullptr) {
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
@@ -1812,8 +1978,15 @@ __device__ __noinline__ void op_attn_reduce(const DevState& S_arg, const StepArg
 }
 
 template <typename WT>
-__device__ void op_embed(const DevState& S, const StepArgs& A, const Instr& in, float* act) {
+__device__ __noinline__ void op_embed(const DevState& S, const StepArgs& A, const Instr& in, float* act) {
   float* h0 = act_ptr(S, act, ACT_H, 0);
+  // the tensor-core GEMV (batches of 3..16) takes layer 0's QKV input in fragment form
+  uint16_t* fo = (S.tc && A.B >= 3) ? reinterpret_cast<uint16_t*>(act_ptr(S, act, ACT_HF, 0)) : nullptr;
+  const int MT = A.B > 8 ? 2 : 1;
+  const uint16_t* gn = iptr(in, kP2);
+  float ssp[kMaxBatch];
+#pragma unroll
+  for (int b = 0; b < kMaxBatch; ++b) ssp[b] = 0.f;
   const bool dev = (A.flags & SF_TOK_FROM_DEVICE) != 0;
   const int e1 = min(in.a[1], A.B * S.d);
   for (int e = in.a[0] + threadIdx.x; e < e1; e += kConsumerThreads) {
@@ -1823,8 +1996,16 @@ __device__ void op_embed(const DevState& S, const StepArgs& A, const Instr& in, 
       set_err(S, 5u /*MK_ERR_STATE*/, -8, tok);
       tok = 0;
     }
-    h0[(size_t)b * S.d + k] = Unpack<WT>::one(S.embed[(size_t)tok * S.d + k]);
+    const float y = Unpack<WT>::one(S.embed[(size_t)tok * S.d + k]);
+    h0[(size_t)b * S.d + k] = y;
+    if (fo) {
+      put_frag<WT>(fo, b, k, MT, y * Unpack<WT>::one(gn[k]));
+#pragma unroll
+      for (int bb = 0; bb < kMaxBatch; ++bb)
+        if (bb == b) ssp[bb] += y * y;
+    }
   }
+  if (fo) put_ssq_slot<kMaxBatch>(smem_ctl(), ssp, act_ptr(S, act, ACT_SSH, 0));
 }
 
 // ---------------------------------------------------------------- self-test opcodes

@@ -156,6 +156,15 @@ void arena_layout(const ModelShape& m, const Geometry& g, int rows, DevState* S)
   sizes[ACT_PART] = R * m.Hkv * (long long)g.S * G * (m.hd + kPartExtra); layers[ACT_PART] = m.L;
   sizes[ACT_O] = R * m.Hq * m.hd; layers[ACT_O] = m.L;
   sizes[ACT_A] = R * m.F; layers[ACT_A] = m.L;
+  // fragment forms: the tensor-core GEMV's batch tile (8 or 16 sequences) x width, as
+  // hi/lo 16-bit halves (one float's worth per element)
+  const long long FR = g.tc ? (rows > 8 ? 16 : 8) : 0;
+  sizes[ACT_HF] = FR * m.d; layers[ACT_HF] = m.L + 1;
+  sizes[ACT_HMF] = FR * m.d; layers[ACT_HMF] = m.L;
+  sizes[ACT_AF] = FR * m.F; layers[ACT_AF] = m.L;
+  const long long SS = g.tc ? (long long)kMaxSsqSlots * kMaxBatch : 0;
+  sizes[ACT_SSH] = SS; layers[ACT_SSH] = m.L + 1;
+  sizes[ACT_SSM] = SS; layers[ACT_SSM] = m.L;
   long long off = 0;
   for (int k = 0; k < ACT_NUM; ++k) {
     const long long stride = (sizes[k] + 31) / 32 * 32;
@@ -400,6 +409,27 @@ std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B,
     p->queues[pe.cta].push_back(pe.in);
   }
   for (auto& q : p->queues) q.push_back(mk_instr(OP_END, 0, -1, 0, -1));
+  // the tensor-core GEMV's RMSNorm inputs carry one sum-of-squares slot per CTA, written by
+  // that CTA's EMBED, O-proj or DOWN instruction: each CTA must hold exactly one of each
+  // (per layer)
+  if (use_tc(g, nb)) {
+    if (n_cta > kMaxSsqSlots) return fmt("the tensor-core GEMV runs on at most %lld CTAs", (long long)kMaxSsqSlots);
+    for (int c = 0; c < n_cta; ++c) {
+      std::vector<int> n_o(m.L, 0), n_dn(m.L, 0);
+      int n_emb = 0;
+      for (const auto& in : p->queues[c]) {
+        if (in.op == OP_EMBED) ++n_emb;
+        if (in.op == OP_OPROJ) ++n_o[in.layer];
+        if (in.op == OP_DOWN) ++n_dn[in.layer];
+      }
+      bool ok = n_emb == 1;
+      for (int l = 0; l < m.L; ++l) ok = ok && n_o[l] == 1 && n_dn[l] == 1;
+      if (!ok)
+        return fmt("cta %lld: the tensor-core GEMV needs one EMBED, O-proj and DOWN instruction per CTA and layer "
+                   "(d_model too small for the CTA count?)",
+                   (long long)c);
+    }
+  }
 
   // multi-launch control: one launch per (op, layer) in dependency order
   auto phase_of = [&](const Instr& in) -> int {
@@ -454,13 +484,20 @@ void bake_pointers(const ModelShape& m, const ModelPtrs& w, Plan* p) {
         set_ptr(in, kP5, at(w.vcache[l], base));
         break;
       }
-      case OP_OPROJ: set_ptr(in, kP4, at(w.wo[l], (size_t)in.a[0] * m.Hq * m.hd)); break;
+      case OP_OPROJ:
+        set_ptr(in, kP2, w.mlp_norm[l]);  // the gain of h_mid's consumer (fragment form)
+        set_ptr(in, kP4, at(w.wo[l], (size_t)in.a[0] * m.Hq * m.hd));
+        break;
+      case OP_EMBED: set_ptr(in, kP2, w.attn_norm[0]); break;
       case OP_UPGATE:
         set_ptr(in, kP2, w.mlp_norm[l]);
         set_ptr(in, kP4, at(w.w_gate[l], (size_t)in.a[0] * m.d));
         set_ptr(in, kP5, at(w.w_up[l], (size_t)in.a[0] * m.d));
         break;
-      case OP_DOWN: set_ptr(in, kP4, at(w.w_down[l], (size_t)in.a[0] * m.F)); break;
+      case OP_DOWN:
+        set_ptr(in, kP2, l + 1 < m.L ? w.attn_norm[l + 1] : w.final_norm);  // the gain of h's next consumer
+        set_ptr(in, kP4, at(w.w_down[l], (size_t)in.a[0] * m.F));
+        break;
       case OP_LMHEAD:
         set_ptr(in, kP2, w.final_norm);
         set_ptr(in, kP4, at(w.lm_head, (size_t)in.a[0] * m.d));
