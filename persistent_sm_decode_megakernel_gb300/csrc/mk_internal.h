@@ -120,12 +120,14 @@ struct TraceRec {
 
 // fp32 activations [rows][width] per layer; with the tensor-core GEMV also the inputs of
 // its ops in fragment form (ACT_HF: RMSNorm gain x h for the next QKV or the LM head,
-// ACT_HMF: gain x h_mid for UP/GATE, ACT_AF: a for DOWN), written by their producers as
+// ACT_HMF: gain x h_mid for UP/GATE, ACT_AF: a for DOWN, ACT_OF: o for O-proj), written by
+// their producers as
 // 16-bit hi/lo halves in the order the mma fragments take them (see frag_index), and the
 // sums of squares of h and h_mid for the RMSNorms, one slot of kMaxBatch floats per
 // producing CTA (ACT_SSH, ACT_SSM: [kMaxSsqSlots][kMaxBatch])
 enum ActKind {
-  ACT_H = 0, ACT_HMID, ACT_Q, ACT_KVN, ACT_PART, ACT_O, ACT_A, ACT_HF, ACT_HMF, ACT_AF, ACT_SSH, ACT_SSM, ACT_NUM
+  ACT_H = 0, ACT_HMID, ACT_Q, ACT_KVN, ACT_PART, ACT_O, ACT_A, ACT_HF, ACT_HMF, ACT_AF, ACT_OF, ACT_SSH, ACT_SSM,
+  ACT_NUM
 };
 constexpr int kMaxSsqSlots = 256;  // the tensor-core GEMV runs on at most this many CTAs
 

@@ -313,6 +313,12 @@ __device__ __forceinline__ Attn make_attn(const DevState& S, const StepArgs& A, 
   return a;
 }
 
+// a split-KV unit with work this step: its sequence is in the batch and its split below the
+// sequence's active count (uniform over the CTA)
+__device__ __forceinline__ bool attn_unit_active(const DevState& S, const StepArgs& A, const Instr& in) {
+  return in.a[0] < A.B && in.a[2] < active_splits(S, A, in.a[0]);
+}
+
 // first (cos, sin) of sequence b's RoPE row: the table's row of its position, or row b of a
 // table that holds one row per sequence of the step
 __device__ __forceinline__ size_t rope_row(const DevState& S, const StepArgs& A, int b) {
@@ -1338,36 +1344,29 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
   float* part = scratch;                       // [2][warps][kTcRows][NB]
   float* rowacc = scratch + kTcPartialFloats;  // [R][NB]
   uint32_t* xt = reinterpret_cast<uint32_t*>(xbuf);  // [kstep][MT][lane][4]
-  const float* src;
+  // the input in fragment form, written by its producers (gain x input for the ops after
+  // an RMSNorm), and for those the producers' per-CTA sums of squares of the input
   const uint16_t* gain = nullptr;
-  // the input in fragment form, written by its producers (all inputs but O-proj's, which
-  // is staged from fp32 and split here)
-  const uint4* frag = nullptr;
-  const float* ssq = nullptr;  // with an RMSNorm: the producers' sums of squares
+  const uint4* frag;
+  const float* ssq = nullptr;
   switch (in.op) {
     case OP_QKV:
-      src = act_ptr(S, act, ACT_H, l);
       gain = iptr(in, kP2);
       frag = reinterpret_cast<const uint4*>(act_ptr(S, act, ACT_HF, l));
       ssq = act_ptr(S, act, ACT_SSH, l);
       break;
     case OP_UPGATE:
-      src = act_ptr(S, act, ACT_HMID, l);
       gain = iptr(in, kP2);
       frag = reinterpret_cast<const uint4*>(act_ptr(S, act, ACT_HMF, l));
       ssq = act_ptr(S, act, ACT_SSM, l);
       break;
     case OP_LMHEAD:
-      src = act_ptr(S, act, ACT_H, S.L);
       gain = iptr(in, kP2);
       frag = reinterpret_cast<const uint4*>(act_ptr(S, act, ACT_HF, S.L));
       ssq = act_ptr(S, act, ACT_SSH, S.L);
       break;
-    case OP_OPROJ: src = act_ptr(S, act, ACT_O, l); break;
-    default:
-      src = act_ptr(S, act, ACT_A, l);
-      frag = reinterpret_cast<const uint4*>(act_ptr(S, act, ACT_AF, l));
-      break;
+    case OP_OPROJ: frag = reinterpret_cast<const uint4*>(act_ptr(S, act, ACT_OF, l)); break;
+    default: frag = reinterpret_cast<const uint4*>(act_ptr(S, act, ACT_AF, l)); break;  // OP_DOWN
   }
 
   for (int i = tid; i < R * NB; i += kConsumerThreads) rowacc[i] = 0.f;
@@ -1391,11 +1390,11 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
   for (int w = 0; w < nw; ++w) {
     const int k0 = w * kTcKw, kw = min(kTcKw, K - k0), nks = kw >> 4;
     const int kso = (w % SW) * (kTcKw >> 4);  // this window's first k-step in the staged tile
-    // 1. the inputs of the next SW windows, split into hi/lo halves in fragment order (8
-    //    sequences per tile; sequences >= B are zeros).  The previous window's pages are
+    // 1. the inputs of the next SW windows: the producers wrote them as hi/lo halves in
+    //    fragment order, so this is a straight copy of the staging's k-steps (8 sequences
+    //    per tile; slots of sequences >= B are zeros).  The previous window's pages are
     //    done: every warp passed the barrier after its last page.
-    if (w % SW == 0 && frag != nullptr) {
-      // a straight copy of the staging's k-steps (slots of sequences >= B are zeros)
+    if (w % SW == 0) {
       constexpr int U = 8;
       const int n16 = (min(SW * kTcKw, K - k0) >> 4) * MT * 32;
       const uint4* fs = frag + (size_t)(k0 >> 4) * MT * 32;
@@ -1424,71 +1423,6 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
           ss[4 * q + 1] = v[q].y;
           ss[4 * q + 2] = v[q].z;
           ss[4 * q + 3] = v[q].w;
-        }
-      }
-      consumer_sync();
-    } else if (w % SW == 0) {
-      constexpr int U = 8;
-      const int kws = min(SW * kTcKw, K - k0);
-      const int k4n = kws >> 2, n_items = MT * 8 * k4n;
-      // the O-proj input: fp32 rows split into hi/lo halves here
-      for (int base = 0; base < n_items; base += U * kConsumerThreads) {
-        const float4* pp[U];
-        // item -> (sequence, vector): at 8 and 16 sequences stepped from the first without
-        // a division per item (measured faster there; at 4 the division measured faster)
-        const int b0 = (base + tid) / k4n, k40 = base + tid - b0 * k4n;
-        {
-          int b = b0, k4 = k40;
-#pragma unroll
-          for (int u = 0; u < U; ++u) {
-            const int it = base + u * kConsumerThreads + tid;
-            if (NB < 8) {
-              b = it / k4n;
-              k4 = it - b * k4n;
-            }
-            const bool live = it < n_items && b < B;
-            pp[u] = live ? reinterpret_cast<const float4*>(src + (size_t)b * K + k0) + k4 : nullptr;
-            if (NB >= 8) {
-              k4 += kConsumerThreads;
-              while (k4 >= k4n) {
-                k4 -= k4n;
-                ++b;
-              }
-            }
-          }
-        }
-        float4 v[U];
-        load_vecs<SYNC, U>(S, c, pp, v);
-        int bn = b0, k4n_ = k40;
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int it = base + u * kConsumerThreads + tid;
-          if (NB < 8) {
-            bn = it / k4n;
-            k4n_ = it - bn * k4n;
-          }
-          const int b = bn, k4 = k4n_, k = 4 * k4;
-          if (NB >= 8) {
-            k4n_ += kConsumerThreads;
-            while (k4n_ >= k4n) {
-              k4n_ -= k4n;
-              ++bn;
-            }
-          }
-          if (it >= n_items) continue;
-          const float4 x = v[u];
-          uint16_t h0, l0, h1, l1, h2, l2, h3, l3;
-          Mma<WT>::split(x.x, h0, l0);
-          Mma<WT>::split(x.y, h1, l1);
-          Mma<WT>::split(x.z, h2, l2);
-          Mma<WT>::split(x.w, h3, l3);
-          const int kk = k & 15, ks = k >> 4, mt = b >> 3, s8 = b & 7;
-          const int reg = kk >= 8 ? 2 : 0, p0 = (kk & 7) >> 1;
-          uint32_t* wd = xt + ((size_t)(ks * MT + mt) * 32 + s8 * 4 + p0) * 4 + reg;
-          wd[0] = (uint32_t)h0 | ((uint32_t)h1 << 16);  // (k, k+1) hi
-          wd[1] = (uint32_t)l0 | ((uint32_t)l1 << 16);  // lo
-          wd[4] = (uint32_t)h2 | ((uint32_t)h3 << 16);  // (k+2, k+3): the next lane's pair
-          wd[5] = (uint32_t)l2 | ((uint32_t)l3 << 16);
         }
       }
       consumer_sync();
@@ -1883,7 +1817,7 @@ __device__ __noinline__ void op_attn(const DevState& S_arg, const StepArgs& A_ar
 // The (b, j) block of partials is contiguous and made of 16-byte rows: staged into the x
 // buffer with vector loads when it fits (the caller has acquired the partials, or polls
 // them), else read from global memory eight splits deep.
-template <int SYNC>
+template <typename WT, int SYNC>
 __device__ __noinline__ void op_attn_reduce(const DevState& S_arg, const StepArgs& A_arg, const Instr& in_arg, SmemCtl* c,
                                             float* xbuf, float* scratch, float* act) {
   const Instr& in = smem_ctl()->cur[threadIdx.x >> 5];
@@ -1899,6 +1833,9 @@ __device__ __noinline__ void op_attn_reduce(const DevState& S_arg, const StepArg
   const int NS = active_splits(S, A, b);  // splits s < NS wrote partials this step
   const float* part = act_ptr(S, act, ACT_PART, l) + ((size_t)b * S.Hkv + j) * S.S * G * RW;
   float* out = act_ptr(S, act, ACT_O, l) + (size_t)b * S.Hq * HD + (size_t)j * G * HD;
+  // the tensor-core GEMV takes O-proj's input in fragment form as well (columns j G HD + t)
+  uint16_t* fo = (S.tc && A.B >= 3) ? reinterpret_cast<uint16_t*>(act_ptr(S, act, ACT_OF, l)) : nullptr;
+  const int MT = A.B > 8 ? 2 : 1, col0 = j * G * HD;
   const int n4 = NS * G * RW / 4;
   const bool staged = n4 * 16 <= S.xbuf_bytes;
   if (staged) {
@@ -1947,6 +1884,7 @@ __device__ __noinline__ void op_attn_reduce(const DevState& S_arg, const StepArg
       }
       if (s < NS) r0 = fmaf(wg[s], pe[s * G * RW], r0);
       out[t] = r0 + r1;
+      if (fo) put_frag<WT>(fo, b, col0 + t, MT, r0 + r1);
     }
     return;
   }
@@ -1974,6 +1912,7 @@ __device__ __noinline__ void op_attn_reduce(const DevState& S_arg, const StepArg
       }
     }
     out[t] = acc;
+    if (fo) put_frag<WT>(fo, b, col0 + t, MT, acc);
   }
 }
 
@@ -2141,6 +2080,14 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
       in = load_instr(A.instr + in.a[0] + u);
       --pc;
     }
+    // a split unit past this step's active count has nothing to compute: skipped without a
+    // barrier (the decision is uniform over the CTA); with counters it still signals (its
+    // waiters count every unit) -- the fused merge's arrival counting takes the full path
+    if (in.op == OP_ATTN && in.a[4] < 0 && !attn_unit_active(S, A, in)) {
+      if (SYNC == SYNC_COUNTER && !nosync && tid == 0 && in.signal_ctr >= 0)
+        red_release_add_u32(&S.counters[in.signal_ctr], 1u);
+      continue;
+    }
     if ((tid & 31) == 0) c->cur[tid >> 5] = in;  // the ops read their warp's shared copy
     __syncwarp();
     uint64_t t_fetch = 0, t_ready = 0;
@@ -2200,7 +2147,7 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
           op_attn<WT, SYNC, 64, 1>(S, A, in, c, pages, xbuf, scratch, ring, act);
         break;
       case OP_ATTN_REDUCE:
-        op_attn_reduce<SYNC>(S, A, in, c, xbuf, scratch, act);
+        op_attn_reduce<WT, SYNC>(S, A, in, c, xbuf, scratch, act);
         break;
       case OP_T_ORDER:
       case OP_T_PRODUCE:
@@ -2237,7 +2184,7 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
         last = (old + 1u == (A.epoch + 1u) * (uint32_t)in.a[3]);
       }
       if (consumer_sync_or(last)) {
-        op_attn_reduce<SYNC>(S, A, in, c, xbuf, scratch, act);
+        op_attn_reduce<WT, SYNC>(S, A, in, c, xbuf, scratch, act);
         if (consumer_sync_or(c->abort)) break;
         if (TRACE && tid == 0) c->tmark[3] = globaltimer_ns();
       } else {

@@ -162,6 +162,7 @@ void arena_layout(const ModelShape& m, const Geometry& g, int rows, DevState* S)
   sizes[ACT_HF] = FR * m.d; layers[ACT_HF] = m.L + 1;
   sizes[ACT_HMF] = FR * m.d; layers[ACT_HMF] = m.L;
   sizes[ACT_AF] = FR * m.F; layers[ACT_AF] = m.L;
+  sizes[ACT_OF] = FR * m.Hq * m.hd; layers[ACT_OF] = m.L;
   const long long SS = g.tc ? (long long)kMaxSsqSlots * kMaxBatch : 0;
   sizes[ACT_SSH] = SS; layers[ACT_SSH] = m.L + 1;
   sizes[ACT_SSM] = SS; layers[ACT_SSM] = m.L;
