@@ -101,7 +101,9 @@ typedef struct {
                              0 auto, 1 a separate step (the ATTN_REDUCE op with sentinels,
                              the last-arriving split with counters), 2 inside the O-proj
                              input staging of every O-proj unit (no extra dependency hop;
-                             auto picks it when the partials of a step are small)       */
+                             auto picks it when the partials of a step are small), 3 the
+                             last-arriving split (an atomic arrival count) in either
+                             synchronisation mode                                        */
   int inflight_pages;     /* at most this many page copies of a CTA in flight at once
                              (0: default 2; < 0: the pool size).  Landed pages still
                              fill the whole pool; fewer copies queued in the memory

@@ -16,9 +16,8 @@ LIB = os.path.join(HERE, "libmk.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["mk_k_f16_counter.cu", "mk_k_f16_sentinel.cu", "mk_k_bf16_counter.cu", "mk_k_bf16_sentinel.cu",
-           "mk_k_f16_counter_ms.cu", "mk_k_f16_sentinel_ms.cu", "mk_k_bf16_counter_ms.cu", "mk_k_bf16_sentinel_ms.cu",
-           "mk_kernel.cu", "mk_host.cu", "mk_plan.cpp", "mk_tmap.cpp", "mk_noalloc.cu"]
+SOURCES = [f"mk_k_{d}_{s}{m}{t}.cu" for d in ("f16", "bf16") for s in ("counter", "sentinel") for m in ("", "_ms")
+           for t in ("", "_tc")] + ["mk_kernel.cu", "mk_host.cu", "mk_plan.cpp", "mk_tmap.cpp", "mk_noalloc.cu"]
 
 
 def _nvcc():

@@ -91,6 +91,10 @@ struct mk_ctx {
   int n_sm = 0, bpsm = 0, n_cta = 0;
   const void* kernel = nullptr;     // one step per launch
   const void* kernel_ms = nullptr;  // several steps per launch (mk_decode_steps)
+  // the same with the tensor-core GEMV (geometries for 3..16 rows: max_batch >= 3 and the
+  // prompt chunks); contexts of max_batch <= 2 decode with the instances without it
+  const void* kernel_tc = nullptr;
+  const void* kernel_tc_ms = nullptr;
   DevState st{};  // template, counters patched per schedule
   ModelPtrs ptrs;  // device addresses written into every instruction
   DevBuf ptr_tables, rope, act, argkeys, ctl, trace;
@@ -315,7 +319,7 @@ mk_status enqueue_step(mk_ctx* ctx, Sched* sc, int B, const int32_t* tok, const 
   A.mail_seq = mail_seq;
   if (n_steps > 1 && ctx->opts.exec_mode != MK_EXEC_PERSISTENT)
     return fail(MK_ERR_INVALID, "several steps in one launch need persistent control");
-  const void* fn = n_steps > 1 ? ctx->kernel_ms : ctx->kernel;
+  const void* fn = S.tc ? (n_steps > 1 ? ctx->kernel_tc_ms : ctx->kernel_tc) : (n_steps > 1 ? ctx->kernel_ms : ctx->kernel);
   if (ctx->opts.trace) MK_CUDA(cudaMemsetAsync(&reinterpret_cast<Ctl*>(ctx->ctl.p)->trace_n, 0, 4, ctx->stream));
   mk_status s;
   if (ctx->opts.exec_mode == MK_EXEC_GRAPH) {
@@ -422,7 +426,7 @@ mk_status mk_plan(const mk_model_desc* desc, const mk_options* opts, int n_ctas,
   if (n_ctas < 1 || !info) return fail(MK_ERR_INVALID, "n_ctas must be positive and info non-NULL");
   mk_options o{};
   if (opts) o = *opts;
-  if (o.attn_merge < 0 || o.attn_merge > 2) return fail(MK_ERR_INVALID, "attn_merge must be 0, 1 or 2");
+  if (o.attn_merge < 0 || o.attn_merge > 3) return fail(MK_ERR_INVALID, "attn_merge must be 0..3");
   const ModelShape m = shape_of(desc);
   Geometry g;
   e = make_geometry(m, n_ctas, o.page_bytes, o.n_pages, o.kv_splits, 232448, &g);
@@ -469,7 +473,7 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
   if (o.sync_mode != MK_SYNC_COUNTER && o.sync_mode != MK_SYNC_SENTINEL) return fail(MK_ERR_INVALID, "sync_mode");
   if (o.exec_mode != MK_EXEC_PERSISTENT && o.exec_mode != MK_EXEC_MULTILAUNCH && o.exec_mode != MK_EXEC_GRAPH)
     return fail(MK_ERR_INVALID, "exec_mode");
-  if (o.attn_merge < 0 || o.attn_merge > 2) return fail(MK_ERR_INVALID, "attn_merge must be 0, 1 or 2");
+  if (o.attn_merge < 0 || o.attn_merge > 3) return fail(MK_ERR_INVALID, "attn_merge must be 0..3");
   if (o.attn_pool < 0 || o.attn_pool > 1) return fail(MK_ERR_INVALID, "attn_pool must be 0 or 1");
   ctx->stream = reinterpret_cast<cudaStream_t>(stream);
   MK_CUDA(cudaGetDevice(&ctx->device));
@@ -481,9 +485,11 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
   e = make_geometry(m, n_cta_guess, o.page_bytes, o.n_pages, o.kv_splits, smem_optin, &ctx->geo);
   if (!e.empty()) return fail(MK_ERR_INVALID, e);
   // one wave (§8.3): opt in to the shared memory, ask how many CTAs fit, launch exactly that
-  ctx->kernel = step_kernel_entry(m.dtype, o.sync_mode, false);
-  ctx->kernel_ms = step_kernel_entry(m.dtype, o.sync_mode, true);
-  for (const void* fn : {ctx->kernel, ctx->kernel_ms})
+  ctx->kernel_tc = step_kernel_entry(m.dtype, o.sync_mode, false, true);
+  ctx->kernel_tc_ms = step_kernel_entry(m.dtype, o.sync_mode, true, true);
+  ctx->kernel = ctx->geo.tc ? ctx->kernel_tc : step_kernel_entry(m.dtype, o.sync_mode, false, false);
+  ctx->kernel_ms = ctx->geo.tc ? ctx->kernel_tc_ms : step_kernel_entry(m.dtype, o.sync_mode, true, false);
+  for (const void* fn : {ctx->kernel, ctx->kernel_ms, ctx->kernel_tc, ctx->kernel_tc_ms})
     // the attribute is per function (shared by every context in the process): the device's
     // limit, so that no context's launch is refused after another context sets a lower one
     MK_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin));
@@ -503,7 +509,7 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
     if (o.exec_mode == MK_EXEC_PERSISTENT &&
         make_geometry(pf.m, ctx->n_cta, o.page_bytes, o.n_pages, o.kv_splits, smem_optin, &pf.geo).empty()) {
       int bp = 0;
-      MK_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bp, ctx->kernel, kThreads, pf.geo.smem_bytes));
+      MK_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bp, ctx->kernel_tc, kThreads, pf.geo.smem_bytes));
       if (bp < ctx->bpsm) pf.geo.smem_bytes = 0;  // chunks would not run in one wave: per-position prefill
     } else {
       pf.geo.smem_bytes = 0;
@@ -841,7 +847,7 @@ mk_status mk_selftest(int kind, int64_t* result, int n) {
   int dev = 0, n_sm = 0;
   MK_CUDA(cudaGetDevice(&dev));
   MK_CUDA(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
-  const void* fn = step_kernel_entry(MK_F16, MK_SYNC_COUNTER, false);
+  const void* fn = step_kernel_entry(MK_F16, MK_SYNC_COUNTER, false, false);
   const int page = 16384, n_pages = 4;
   const int smem = n_pages * page + 0 + 256 + kCtlSmem;
   MK_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448));

@@ -267,22 +267,28 @@ __global__ void __launch_bounds__(kThreads, 1) mk_stream_kernel(const uint8_t* s
 }
 
 // ---------------------------------------------------------------- launch table
-const void* step_kernel_entry_f16_counter();
-const void* step_kernel_entry_f16_sentinel();
-const void* step_kernel_entry_bf16_counter();
-const void* step_kernel_entry_bf16_sentinel();
-const void* step_kernel_entry_f16_counter_ms();
-const void* step_kernel_entry_f16_sentinel_ms();
-const void* step_kernel_entry_bf16_counter_ms();
-const void* step_kernel_entry_bf16_sentinel_ms();
+#define MK_ENTRY(n) const void* step_kernel_entry_##n();
+#define MK_ENTRIES(d, s) MK_ENTRY(d##_##s) MK_ENTRY(d##_##s##_tc) MK_ENTRY(d##_##s##_ms) MK_ENTRY(d##_##s##_ms_tc)
+MK_ENTRIES(f16, counter)
+MK_ENTRIES(f16, sentinel)
+MK_ENTRIES(bf16, counter)
+MK_ENTRIES(bf16, sentinel)
+#undef MK_ENTRIES
+#undef MK_ENTRY
 
-const void* step_kernel_entry(int dtype, int sync_mode, bool multi_step) {
-  if (multi_step) {
-    if (dtype == 0) return sync_mode == 0 ? step_kernel_entry_f16_counter_ms() : step_kernel_entry_f16_sentinel_ms();
-    return sync_mode == 0 ? step_kernel_entry_bf16_counter_ms() : step_kernel_entry_bf16_sentinel_ms();
-  }
-  if (dtype == 0) return sync_mode == 0 ? step_kernel_entry_f16_counter() : step_kernel_entry_f16_sentinel();
-  return sync_mode == 0 ? step_kernel_entry_bf16_counter() : step_kernel_entry_bf16_sentinel();
+const void* step_kernel_entry(int dtype, int sync_mode, bool multi_step, bool tc) {
+  using Fn = const void* (*)();
+  // [dtype][sync][multi_step][tc]
+  static const Fn table[2][2][2][2] = {
+      {{{step_kernel_entry_f16_counter, step_kernel_entry_f16_counter_tc},
+        {step_kernel_entry_f16_counter_ms, step_kernel_entry_f16_counter_ms_tc}},
+       {{step_kernel_entry_f16_sentinel, step_kernel_entry_f16_sentinel_tc},
+        {step_kernel_entry_f16_sentinel_ms, step_kernel_entry_f16_sentinel_ms_tc}}},
+      {{{step_kernel_entry_bf16_counter, step_kernel_entry_bf16_counter_tc},
+        {step_kernel_entry_bf16_counter_ms, step_kernel_entry_bf16_counter_ms_tc}},
+       {{step_kernel_entry_bf16_sentinel, step_kernel_entry_bf16_sentinel_tc},
+        {step_kernel_entry_bf16_sentinel_ms, step_kernel_entry_bf16_sentinel_ms_tc}}}};
+  return table[dtype == 0 ? 0 : 1][sync_mode == 0 ? 0 : 1][multi_step ? 1 : 0][tc ? 1 : 0]();
 }
 
 const void* barrier_kernel_entry() { return reinterpret_cast<const void*>(&mk_barrier_kernel); }

@@ -362,7 +362,7 @@ __device__ __noinline__ bool producer_acquire(const DevState& S_arg, SmemCtl* c,
   return true;
 }
 
-template <bool MS>
+template <bool MS, bool TC>
 __device__ __noinline__ void producer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* c, uint8_t* pages) {
   const DevState& S = smem_ctl()->S;
   StepArgs& A = MS ? smem_ctl()->largs : smem_ctl()->args;
@@ -447,7 +447,7 @@ __device__ __noinline__ void producer(const DevState& S_arg, const StepArgs& A_a
             for (int off = 0; off < in.a[3] * 8 + 128; off += 128) prefetch_l1(rp + off);
           }
         }
-        if (S.tc && A.B >= 3) {
+        if (TC && S.tc && A.B >= 3) {
           // tensor-core pages: for each window of kTcKw columns, the 16-row blocks of
           // segment 0, then of segment 1, each one tensor-map copy (p4 / p5 hold the
           // segments' maps; rows and columns past the segment land as zeros)
@@ -1817,7 +1817,7 @@ __device__ __noinline__ void op_attn(const DevState& S_arg, const StepArgs& A_ar
 // The (b, j) block of partials is contiguous and made of 16-byte rows: staged into the x
 // buffer with vector loads when it fits (the caller has acquired the partials, or polls
 // them), else read from global memory eight splits deep.
-template <typename WT, int SYNC>
+template <typename WT, int SYNC, bool TC>
 __device__ __noinline__ void op_attn_reduce(const DevState& S_arg, const StepArgs& A_arg, const Instr& in_arg, SmemCtl* c,
                                             float* xbuf, float* scratch, float* act) {
   const Instr& in = smem_ctl()->cur[threadIdx.x >> 5];
@@ -1834,7 +1834,7 @@ __device__ __noinline__ void op_attn_reduce(const DevState& S_arg, const StepArg
   const float* part = act_ptr(S, act, ACT_PART, l) + ((size_t)b * S.Hkv + j) * S.S * G * RW;
   float* out = act_ptr(S, act, ACT_O, l) + (size_t)b * S.Hq * HD + (size_t)j * G * HD;
   // the tensor-core GEMV takes O-proj's input in fragment form as well (columns j G HD + t)
-  uint16_t* fo = (S.tc && A.B >= 3) ? reinterpret_cast<uint16_t*>(act_ptr(S, act, ACT_OF, l)) : nullptr;
+  uint16_t* fo = (TC && S.tc && A.B >= 3) ? reinterpret_cast<uint16_t*>(act_ptr(S, act, ACT_OF, l)) : nullptr;
   const int MT = A.B > 8 ? 2 : 1, col0 = j * G * HD;
   const int n4 = NS * G * RW / 4;
   const bool staged = n4 * 16 <= S.xbuf_bytes;
@@ -1916,11 +1916,11 @@ __device__ __noinline__ void op_attn_reduce(const DevState& S_arg, const StepArg
   }
 }
 
-template <typename WT>
+template <typename WT, bool TC>
 __device__ __noinline__ void op_embed(const DevState& S, const StepArgs& A, const Instr& in, float* act) {
   float* h0 = act_ptr(S, act, ACT_H, 0);
   // the tensor-core GEMV (batches of 3..16) takes layer 0's QKV input in fragment form
-  uint16_t* fo = (S.tc && A.B >= 3) ? reinterpret_cast<uint16_t*>(act_ptr(S, act, ACT_HF, 0)) : nullptr;
+  uint16_t* fo = (TC && S.tc && A.B >= 3) ? reinterpret_cast<uint16_t*>(act_ptr(S, act, ACT_HF, 0)) : nullptr;
   const int MT = A.B > 8 ? 2 : 1;
   const uint16_t* gn = iptr(in, kP2);
   float ssp[kMaxBatch];
@@ -2005,7 +2005,7 @@ __device__ __noinline__ bool pool_take(const DevState& S_arg, SmemCtl* c) {
   return true;
 }
 
-template <typename WT, int SYNC, bool MS>
+template <typename WT, int SYNC, bool MS, bool TC>
 __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* c, uint8_t* pages, float* xbuf,
                          float* scratch) {
   const DevState& S = smem_ctl()->S;
@@ -2082,9 +2082,9 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
     }
     // a split unit past this step's active count has nothing to compute: skipped without a
     // barrier (the decision is uniform over the CTA); with counters it still signals (its
-    // waiters count every unit) -- the fused merge's arrival counting takes the full path
-    if (in.op == OP_ATTN && in.a[4] < 0 && !attn_unit_active(S, A, in)) {
-      if (SYNC == SYNC_COUNTER && !nosync && tid == 0 && in.signal_ctr >= 0)
+    // waiters count every unit), except under the fused merge, which counts active splits
+    if (in.op == OP_ATTN && !attn_unit_active(S, A, in)) {
+      if (SYNC == SYNC_COUNTER && in.a[4] < 0 && !nosync && tid == 0 && in.signal_ctr >= 0)
         red_release_add_u32(&S.counters[in.signal_ctr], 1u);
       continue;
     }
@@ -2112,14 +2112,14 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
     const int G = MS ? c->step_G : G0;
     switch (in.op) {
       case OP_EMBED:
-        op_embed<WT>(S, A, in, act);
+        op_embed<WT, TC>(S, A, in, act);
         break;
       case OP_QKV:
       case OP_OPROJ:
       case OP_UPGATE:
       case OP_DOWN:
       case OP_LMHEAD:
-        if (nb >= 4) {  // batches of 3..16: tensor cores (every context for max_batch >= 3 is set up for them)
+        if (TC && nb >= 4) {  // batches of 3..16: tensor cores (every context for max_batch >= 3 is set up for them)
           switch (nb) {
             case 4: op_gemv_tc<WT, SYNC, 4>(S, A, in, c, pages, xbuf, scratch, ring, act); break;
             case 8: op_gemv_tc<WT, SYNC, 8>(S, A, in, c, pages, xbuf, scratch, ring, act); break;
@@ -2147,7 +2147,7 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
           op_attn<WT, SYNC, 64, 1>(S, A, in, c, pages, xbuf, scratch, ring, act);
         break;
       case OP_ATTN_REDUCE:
-        op_attn_reduce<WT, SYNC>(S, A, in, c, xbuf, scratch, act);
+        op_attn_reduce<WT, SYNC, TC>(S, A, in, c, xbuf, scratch, act);
         break;
       case OP_T_ORDER:
       case OP_T_PRODUCE:
@@ -2176,15 +2176,19 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
     if (in.op == OP_ATTN && in.a[4] >= 0) {
       // fused merge: count this split's arrival (acq_rel: publishes this CTA's partial,
       // and for the last arriver makes every other split's partial visible); the CTA
-      // that brings the count to S merges the splits, then signals the O-proj counter
+      // that brings the count to the step's active split count merges the splits, sets
+      // the count back to zero for the next step (ordered before the step's end by this
+      // CTA's later releases), then signals the O-proj counter
       bool last = false;
       if (tid == 0) {
         if (TRACE) c->tmark[2] = globaltimer_ns();
+        const uint32_t ns = (uint32_t)active_splits(S, A, in.a[0]);
         const uint32_t old = atom_acq_rel_add_u32(&S.counters[in.a[4]], 1u);
-        last = (old + 1u == (A.epoch + 1u) * (uint32_t)in.a[3]);
+        last = old + 1u == ns;
+        if (last) st_relaxed_u32(&S.counters[in.a[4]], 0u);
       }
       if (consumer_sync_or(last)) {
-        op_attn_reduce<WT, SYNC>(S, A, in, c, xbuf, scratch, act);
+        op_attn_reduce<WT, SYNC, TC>(S, A, in, c, xbuf, scratch, act);
         if (consumer_sync_or(c->abort)) break;
         if (TRACE && tid == 0) c->tmark[3] = globaltimer_ns();
       } else {
@@ -2247,7 +2251,10 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
 }  // namespace
 
 // ---------------------------------------------------------------- the kernel
-template <typename WT, int SYNC, bool MS>
+// WT weight/KV dtype, SYNC counter or sentinel dependencies, MS several steps per launch,
+// TC with the tensor-core GEMV (geometries for 3..16 rows); contexts of batches 1..2 run
+// the instance without that code, whose smaller footprint measured faster at batch 1.
+template <typename WT, int SYNC, bool MS, bool TC>
 __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_constant__ DevState S,
                                                               const __grid_constant__ StepArgs A) {
   SmemCtl* c = smem_ctl();
@@ -2278,7 +2285,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
   float* scratch = smem_scratch(S);
   // the tensor-core pages are 128-byte swizzled copies, whose destination must sit on a
   // 1024-byte boundary: refuse to run (an error, not a faulting copy) if it does not
-  if (S.tc && (smem_addr(pages) & 1023u)) {
+  if (TC && S.tc && (smem_addr(pages) & 1023u)) {
     if (tid == 0 && blockIdx.x == 0) set_err(S, 5u /*MK_ERR_STATE*/, -11, (int)(smem_addr(pages) & 1023u));
     return;
   }
@@ -2310,11 +2317,11 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
   __syncthreads();
   if (tid >= kConsumerThreads) {  // the loader streams weights without waiting for the previous grid
     const int w = tid >> 5;
-    if (w == kLoaderWarp && (tid & 31) == 0) producer<MS>(S, AA, c, pages);
+    if (w == kLoaderWarp && (tid & 31) == 0) producer<MS, TC>(S, AA, c, pages);
     return;
   }
   if (AA.flags & SF_PDL) asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous grid's outputs
-  consumer<WT, SYNC, MS>(S, AA, c, pages, xbuf, scratch);
+  consumer<WT, SYNC, MS, TC>(S, AA, c, pages, xbuf, scratch);
   if (c->abort && tid == 0 && !global_err(S)) set_err(S, 4u, -7, -1);
 }
 

@@ -194,6 +194,7 @@ int choose_merge(const ModelShape& m, const Geometry& g, int B, bool counters, i
   const long long weight_floats = 3LL * B * m.Hkv * g.S * G;  // (max, sum) pairs + merge weights
   const bool fits = part_bytes <= kMergeInBytes && weight_floats * 4 <= g.scratch_bytes;
   const bool tc = use_tc(g, pow2_at_least(B));  // the tensor-core GEMV stages its own input layout
+  if (requested == 3) return MERGE_LAST_ARRIVER;
   if (!tc && (requested == 2 || (requested == 0 && fits))) return MERGE_IN_OPROJ;
   return counters ? MERGE_LAST_ARRIVER : MERGE_OP;
 }

@@ -134,7 +134,7 @@ def main():
     ap.add_argument("--page-bytes", type=int, default=0)
     ap.add_argument("--n-pages", type=int, default=0)
     ap.add_argument("--backoff", type=int, default=0)
-    ap.add_argument("--merge", type=int, default=0, help="KV-split merge: 0 auto, 1 separate step, 2 in O-proj")
+    ap.add_argument("--merge", type=int, default=0, help="KV-split merge: 0 auto, 1 separate step, 2 in O-proj, 3 last-arriving split")
     ap.add_argument("--inflight", type=int, default=0, help="page copies in flight per CTA (0: default, <0: pool)")
     ap.add_argument("--split-min", type=int, default=0)
     ap.add_argument("--pool", type=int, default=0, help="attention units claimed from a per-layer pool")

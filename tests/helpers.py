@@ -42,7 +42,9 @@ def gpu_teacher_forced(dec, prompt, toks, n_new, vocab):
 
 
 def assert_parity(z_gpu, tok_gpu, z_ref, toks_ref, P):
-    """The spec criterion, step by step and sequence by sequence."""
+    """Logits within LOGIT_RTOL of the oracle's largest |logit| and the greedy token equal
+    to the oracle's wherever its top-2 margin exceeds that tolerance, step by step and
+    sequence by sequence."""
     B, n, V = z_ref.shape
     worst = 0.0
     for b in range(B):

@@ -82,11 +82,12 @@ def test_plan_multilaunch_counts_launches(mk):
 
 def test_plan_merge_choice_and_bad_option(mk):
     cfg = synth.CONFIGS["2b"]
-    for merge in (0, 1, 2):
+    for merge in (0, 1, 2, 3):
         for b in (1, 2, 4):
-            st, _ = _plan(mk, _desc(mk, cfg, max_batch=b), 152, attn_merge=merge)
-            assert st == mk.MK_OK, (merge, b, mk.mk_last_error())
-    st, _ = _plan(mk, _desc(mk, cfg), 152, attn_merge=3)
+            for sync in (0, 1):
+                st, _ = _plan(mk, _desc(mk, cfg, max_batch=b), 152, attn_merge=merge, sync_mode=sync)
+                assert st == mk.MK_OK, (merge, b, sync, mk.mk_last_error())
+    st, _ = _plan(mk, _desc(mk, cfg), 152, attn_merge=4)
     assert st == mk.MK_ERR_INVALID
 
 

@@ -287,11 +287,12 @@ def test_2b_fp16_full_prompt_teacher_forced(lib):
 
 
 @pytest.mark.parametrize("page_bytes", [0, 8192])
-@pytest.mark.parametrize("merge", [1, 2], ids=["merge-step", "merge-in-oproj"])
+@pytest.mark.parametrize("merge", [1, 2, 3], ids=["merge-step", "merge-in-oproj", "merge-last-arriver"])
 def test_tiny_long_context_many_splits(lib, tiny, page_bytes, merge):
     """A 600-position context: the step uses several KV splits (one page of positions
     each, up to the schedule's count), merged in a separate step (the ATTN_REDUCE op with
-    sentinels, the last-arriving split with counters) or inside the O-proj staging."""
+    sentinels, the last-arriving split with counters), inside the O-proj staging, or by the
+    last-arriving split under either synchronisation."""
     cfg, w, m = tiny
     P, n_new = 600, 4
     prompt = synth.gen_prompts(cfg, 1, P)
@@ -304,15 +305,17 @@ def test_tiny_long_context_many_splits(lib, tiny, page_bytes, merge):
         assert_parity(z, tg, zref, toks, P)
 
 
-@pytest.mark.parametrize("merge", [1, 2], ids=["merge-step", "merge-in-oproj"])
+@pytest.mark.parametrize("B", [2, 5])
+@pytest.mark.parametrize("merge", [1, 2, 3], ids=["merge-step", "merge-in-oproj", "merge-last-arriver"])
 @pytest.mark.parametrize("sync", [0, 1], ids=["counter", "sentinel"])
-def test_tiny_batched_merge_modes(lib, tiny, merge, sync):
-    """Batch 2 with ragged positions under both split-merge placements."""
+def test_tiny_batched_merge_modes(lib, tiny, merge, sync, B):
+    """Batches 2 (CUDA-core GEMV) and 5 (tensor-core GEMV, O-proj input in fragment form
+    from the merge) under every split-merge placement."""
     cfg, w, m = tiny
     P, n_new = cfg.prompt_len, 6
-    prompt = synth.gen_prompts(cfg, 2, P)
+    prompt = synth.gen_prompts(cfg, B, P)
     toks, zref = oracle_run(cfg, w, prompt, n_new, model=m)
-    dm = lib.DeviceModel(cfg, w, max_batch=2, max_ctx=P + n_new)
+    dm = lib.DeviceModel(cfg, w, max_batch=B, max_ctx=P + n_new)
     dec = lib.Decoder(dm, sync_mode=sync, attn_merge=merge)
     z, tg = gpu_teacher_forced(dec, prompt, toks, n_new, cfg.vocab)
     dec.close()
