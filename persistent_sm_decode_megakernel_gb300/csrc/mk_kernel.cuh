@@ -33,6 +33,8 @@ struct SmemCtl {
   int pool_slot;                    // compute side: next FIFO slot and its phase (thread 0)
   uint32_t pool_ph;
   int pool_unit;                    // the unit thread 0 took, for the other compute threads
+  uint64_t xfull[2];                // tensor-core GEMV: bulk copies of the x staging, per half
+  uint32_t xph[2];                  // their phases between ops
   unsigned long long best[kMaxBatch];
   float inv_rms[kMaxBatch];
   float red[kConsumerWarps * kMaxBatch];
@@ -1321,6 +1323,55 @@ __device__ __noinline__ void op_gemv(const DevState& S_arg, const StepArgs& A_ar
 // the loader brings, per window, 16-row blocks of the instruction's rows.  Warps split a
 // page's k-steps; their partials are summed in a fixed order into per-row accumulators,
 // and the common epilogue finishes the rows.
+// Tensor-core GEMV input staging through the copy engine: thread 0 issues one bulk copy of
+// the staging's fragment vectors into shared memory, landing on half h's mbarrier.  The
+// proxy fence orders this CTA's earlier generic accesses of the destination and the
+// producers' writes it has acquired before the asynchronous copy.
+__device__ __noinline__ void xstage_issue(SmemCtl* c, int h, void* dst, const void* src, uint32_t bytes) {
+  asm volatile("fence.proxy.async;" ::: "memory");
+  mbar_arrive_expect_tx(&c->xfull[h], bytes);
+  tma_load_1d_plain(dst, src, bytes, &c->xfull[h]);
+}
+// a fragment vector still holding sentinel halves, re-read until its producers' values
+// land (bounded: sets the abort flag and returns zeros on timeout)
+__device__ __noinline__ uint4 poll_frag(const uint4* p, const DevState& S, SmemCtl* c) {
+  const uint64_t t0 = globaltimer_ns();
+  for (int k = 0;; ++k) {
+    if (!poll_pause(S, c, k, t0)) return make_uint4(0u, 0u, 0u, 0u);
+    const float4 f = ld_poll_v4(reinterpret_cast<const float4*>(p));
+    const uint4 v = make_uint4(__float_as_uint(f.x), __float_as_uint(f.y), __float_as_uint(f.z), __float_as_uint(f.w));
+    if (!(frag_pending(v.x) || frag_pending(v.y) || frag_pending(v.z) || frag_pending(v.w))) return v;
+  }
+}
+// All compute threads: wait (bounded) for half h's copy of n vectors, then, with sentinels,
+// re-read from src the vectors of live sequences the copy caught before their producers
+// wrote them; ends with a CTA barrier.
+template <int SYNC>
+__device__ __noinline__ void xstage_land(const DevState& S_arg, SmemCtl* c, int h, uint32_t ph, uint4* x, const uint4* src,
+                                         int n, int B, int MT) {
+  const DevState& S = smem_ctl()->S;
+  c = smem_ctl();
+  if (!mbar_try_wait(&c->xfull[h], ph)) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_wait_hint(&c->xfull[h], ph, 2000u)) {
+      if (globaltimer_ns() - t0 > (uint64_t)S.timeout_ns) {
+        set_err(S, 4u, -12, h);
+        c->abort = 1;
+        break;
+      }
+    }
+  }
+  if (SYNC == SYNC_SENTINEL) {
+    for (int i = threadIdx.x; i < n; i += kConsumerThreads) {
+      if ((((i >> 5) & (MT - 1)) << 3) + ((i & 31) >> 2) >= B) continue;  // no such sequence
+      const uint4 v = x[i];
+      if (frag_pending(v.x) || frag_pending(v.y) || frag_pending(v.z) || frag_pending(v.w))
+        x[i] = poll_frag(src + i, S, c);
+    }
+  }
+  consumer_sync();
+}
+
 template <typename WT, int SYNC, int NB>
 __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A_arg, const Instr& in_arg, SmemCtl* c,
                                         uint8_t* pages, float* xbuf, float* scratch, Ring& ring_io, float* act) {
@@ -1343,7 +1394,6 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
   const bool trace = (A.flags & SF_TRACE) != 0;
   float* part = scratch;                       // [2][warps][kTcRows][NB]
   float* rowacc = scratch + kTcPartialFloats;  // [R][NB]
-  uint32_t* xt = reinterpret_cast<uint32_t*>(xbuf);  // [kstep][MT][lane][4]
   // the input in fragment form, written by its producers (gain x input for the ops after
   // an RMSNorm), and for those the producers' per-CTA sums of squares of the input
   const uint16_t* gain = nullptr;
@@ -1385,48 +1435,69 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
   for (int b = 0; b < NB; ++b) ss[b] = 0.f;
   uint64_t page_wait_ns = 0, page_work_ns = 0;
   int pcount = 0;
-  // the x buffer holds SW page windows of split inputs at once: staged every SW windows
-  const int SW = max(1, (S.xbuf_bytes / 4) / (MT * 8 * kTcKw));
+  // x staging.  With counters (the dependency wait has seen the producers done) by bulk
+  // copies of the fragment form: every window at once when they fit the x buffer, else one
+  // window per copy, double-buffered (the next window's copy in flight while this window's
+  // pages run) when two windows fit, else one after the other.  With sentinels a copy could
+  // catch the producers mid-write, so the compute threads poll the vectors in, SW windows
+  // (as many as the buffer holds) per staging.
+  const int wv = (kTcKw >> 4) * MT * 32;  // 16-byte vectors of a full window
+  auto stage_n = [&](int w0, int nwin) { return ((min(K, (w0 + nwin) * kTcKw) - w0 * kTcKw) >> 4) * MT * 32; };
+  const bool whole = stage_n(0, nw) * 16 <= S.xbuf_bytes;
+  const bool dbl = SYNC == SYNC_COUNTER && !whole && 2 * wv * 16 <= S.xbuf_bytes;
+  const int SW = whole ? nw : (dbl ? 1 : max(1, S.xbuf_bytes / (wv * 16)));
+  uint4* xb = reinterpret_cast<uint4*>(xbuf);
+  uint32_t xph[2] = {c->xph[0], c->xph[1]};
+  if (SYNC == SYNC_COUNTER && tid == 0) xstage_issue(c, 0, xb, frag, (uint32_t)stage_n(0, SW) * 16u);
+  // with an RMSNorm: the producers' per-CTA sums of squares of the input (one slot of
+  // kMaxBatch floats per producing CTA), slot tid into this thread's ss[]
+  if (gain != nullptr && tid < S.n_cta) {
+    const float4* sp = reinterpret_cast<const float4*>(ssq + (size_t)tid * kMaxBatch);
+    const float4* pp[NB / 4];
+#pragma unroll
+    for (int q = 0; q < NB / 4; ++q) pp[q] = sp + q;
+    float4 v[NB / 4];
+    load_vecs<SYNC, NB / 4>(S, c, pp, v);
+#pragma unroll
+    for (int q = 0; q < NB / 4; ++q) {
+      ss[4 * q] = v[q].x;
+      ss[4 * q + 1] = v[q].y;
+      ss[4 * q + 2] = v[q].z;
+      ss[4 * q + 3] = v[q].w;
+    }
+  }
   for (int w = 0; w < nw; ++w) {
     const int k0 = w * kTcKw, kw = min(kTcKw, K - k0), nks = kw >> 4;
-    const int kso = (w % SW) * (kTcKw >> 4);  // this window's first k-step in the staged tile
-    // 1. the inputs of the next SW windows: the producers wrote them as hi/lo halves in
-    //    fragment order, so this is a straight copy of the staging's k-steps (8 sequences
-    //    per tile; slots of sequences >= B are zeros).  The previous window's pages are
-    //    done: every warp passed the barrier after its last page.
+    // 1. this staging's inputs: the producers wrote them as hi/lo halves in fragment order
+    //    (8 sequences per tile; slots of sequences >= B are not read).  A copy into a buffer
+    //    the previous window read is issued after that window's last page barrier.
+    const int h = dbl ? (w & 1) : 0;
+    uint4* xw = xb + (dbl ? h * wv : 0);
     if (w % SW == 0) {
-      constexpr int U = 8;
-      const int n16 = (min(SW * kTcKw, K - k0) >> 4) * MT * 32;
-      const uint4* fs = frag + (size_t)(k0 >> 4) * MT * 32;
-      uint4* xd = reinterpret_cast<uint4*>(xt);
-      for (int base = 0; base < n16; base += U * kConsumerThreads) {
-        uint4 v[U];
-        load_frags<SYNC, U>(S, c, fs, base, n16, B, MT, v);
+      const int n16 = stage_n(w, SW);
+      if (SYNC == SYNC_COUNTER) {
+        if (w > 0 && !dbl && tid == 0) xstage_issue(c, 0, xw, frag + (size_t)w * wv, (uint32_t)n16 * 16u);
+        xstage_land<SYNC>(S, c, h, xph[h], xw, frag + (size_t)w * wv, n16, B, MT);
+        xph[h] ^= 1u;
+        if (dbl && w + 1 < nw && tid == 0)
+          xstage_issue(c, h ^ 1, xb + (h ^ 1) * wv, frag + (size_t)(w + 1) * wv, (uint32_t)stage_n(w + 1, 1) * 16u);
+      } else {
+        constexpr int U = 8;
+        const uint4* fs = frag + (size_t)w * wv;
+        for (int base = 0; base < n16; base += U * kConsumerThreads) {
+          uint4 v[U];
+          load_frags<SYNC, U>(S, c, fs, base, n16, B, MT, v);
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int i = base + u * kConsumerThreads + tid;
-          if (i < n16) xd[i] = v[u];
+          for (int u = 0; u < U; ++u) {
+            const int i = base + u * kConsumerThreads + tid;
+            if (i < n16) xw[i] = v[u];
+          }
         }
+        consumer_sync();
       }
-      // with an RMSNorm: the producers' per-CTA sums of squares of the input (one slot of
-      // kMaxBatch floats per producing CTA), slot tid into this thread's ss[]
-      if (w == 0 && gain != nullptr && tid < S.n_cta) {
-        const float4* sp = reinterpret_cast<const float4*>(ssq + (size_t)tid * kMaxBatch);
-        const float4* pp[NB / 4];
-#pragma unroll
-        for (int q = 0; q < NB / 4; ++q) pp[q] = sp + q;
-        float4 v[NB / 4];
-        load_vecs<SYNC, NB / 4>(S, c, pp, v);
-#pragma unroll
-        for (int q = 0; q < NB / 4; ++q) {
-          ss[4 * q] = v[q].x;
-          ss[4 * q + 1] = v[q].y;
-          ss[4 * q + 2] = v[q].z;
-          ss[4 * q + 3] = v[q].w;
-        }
-      }
-      consumer_sync();
     }
+    const int kso = (w % SW) * (kTcKw >> 4);  // this window's first k-step in the staged tile
+    const uint32_t* xtw = reinterpret_cast<const uint32_t*>(xw);
     if (tid == 0 && trace && w == 0) c->tmark[0] = globaltimer_ns();
     // 2. the window's row blocks
     const int per = (nks + kConsumerWarps - 1) / kConsumerWarps, ks0 = warp * per, ks1 = min(nks, ks0 + per);
@@ -1454,7 +1525,7 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
         }
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          const uint4 a = *reinterpret_cast<const uint4*>(xt + ((size_t)((kso + ks) * MT + mt) * 32 + lane) * 4);
+          const uint4 a = *reinterpret_cast<const uint4*>(xtw + ((size_t)((kso + ks) * MT + mt) * 32 + lane) * 4);
 #pragma unroll
           for (int nb = 0; nb < 2; ++nb) Mma<WT>::run(d[mt][nb], a, bw[nb][0], bw[nb][1]);
         }
@@ -1500,6 +1571,10 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
   }
   consumer_sync();
   if (gain != nullptr && tid < B) c->inv_rms[tid] = inv_rms_of<NB>(S, c, tid);
+  if (tid == 0) {  // the staging copies' phases, for the next op (after the loop's barrier)
+    c->xph[0] = xph[0];
+    c->xph[1] = xph[1];
+  }
   consumer_sync();
   if (tid == 0 && trace) {
     c->tmark[1] = globaltimer_ns();
@@ -2301,6 +2376,10 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
     }
     c->pool_slot = 0;
     c->pool_ph = 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&c->xfull[i], 1);
+      c->xph[i] = 0;
+    }
     c->abort = 0;
     c->ms_step = 0;
     mbar_fence_init();
