@@ -35,6 +35,8 @@ struct SmemCtl {
   int pool_unit;                    // the unit thread 0 took, for the other compute threads
   uint64_t xfull[2];                // tensor-core GEMV: bulk copies of the x staging, per half
   uint32_t xph[2];                  // their phases between ops
+  int lm_staged;                    // the x buffer holds the LM head's whole input (and 1/rms)
+  unsigned long long wbest[kConsumerWarps * kMaxBatch];  // LM head: each warp's best keys
   unsigned long long best[kMaxBatch];
   float inv_rms[kMaxBatch];
   float red[kConsumerWarps * kMaxBatch];
@@ -1167,6 +1169,8 @@ __device__ __forceinline__ void gemv_epilogue(const DevState& S, const StepArgs&
         for (int bb = 0; bb < NB; ++bb)
           if (bb == b && key > best[bb]) best[bb] = key;
       }
+      // each warp's best per sequence, then one thread per sequence over the warps (fixed
+      // order) and one atomic on the CTA's running best
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
         unsigned long long v = best[b];
@@ -1175,7 +1179,17 @@ __device__ __forceinline__ void gemv_epilogue(const DevState& S, const StepArgs&
           const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
           v = w > v ? w : v;
         }
-        if (lane == 0 && v) atomicMax(&c->best[b], v);
+        if (lane == 0) c->wbest[(tid >> 5) * NB + b] = v;
+      }
+      consumer_sync();
+      if (tid < B) {
+        unsigned long long v = 0ull;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const unsigned long long x = c->wbest[w * NB + tid];
+          v = x > v ? x : v;
+        }
+        if (v) atomicMax(&c->best[tid], v);
       }
       break;
     }
@@ -1448,10 +1462,13 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
   const int SW = whole ? nw : (dbl ? 1 : max(1, S.xbuf_bytes / (wv * 16)));
   uint4* xb = reinterpret_cast<uint4*>(xbuf);
   uint32_t xph[2] = {c->xph[0], c->xph[1]};
-  if (SYNC == SYNC_COUNTER && tid == 0) xstage_issue(c, 0, xb, frag, (uint32_t)stage_n(0, SW) * 16u);
+  // a CTA's LM head instructions follow each other with the same input: after the first
+  // staged it whole (and set 1/rms), the others reuse it
+  const bool reuse = in.op == OP_LMHEAD && whole && c->lm_staged;
+  if (SYNC == SYNC_COUNTER && !reuse && tid == 0) xstage_issue(c, 0, xb, frag, (uint32_t)stage_n(0, SW) * 16u);
   // with an RMSNorm: the producers' per-CTA sums of squares of the input (one slot of
   // kMaxBatch floats per producing CTA), slot tid into this thread's ss[]
-  if (gain != nullptr && tid < S.n_cta) {
+  if (gain != nullptr && !reuse && tid < S.n_cta) {
     const float4* sp = reinterpret_cast<const float4*>(ssq + (size_t)tid * kMaxBatch);
     const float4* pp[NB / 4];
 #pragma unroll
@@ -1473,7 +1490,7 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
     //    the previous window read is issued after that window's last page barrier.
     const int h = dbl ? (w & 1) : 0;
     uint4* xw = xb + (dbl ? h * wv : 0);
-    if (w % SW == 0) {
+    if (w % SW == 0 && !reuse) {
       const int n16 = stage_n(w, SW);
       if (SYNC == SYNC_COUNTER) {
         if (w > 0 && !dbl && tid == 0) xstage_issue(c, 0, xw, frag + (size_t)w * wv, (uint32_t)n16 * 16u);
@@ -1570,10 +1587,11 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
     }
   }
   consumer_sync();
-  if (gain != nullptr && tid < B) c->inv_rms[tid] = inv_rms_of<NB>(S, c, tid);
+  if (gain != nullptr && !reuse && tid < B) c->inv_rms[tid] = inv_rms_of<NB>(S, c, tid);
   if (tid == 0) {  // the staging copies' phases, for the next op (after the loop's barrier)
     c->xph[0] = xph[0];
     c->xph[1] = xph[1];
+    c->lm_staged = in.op == OP_LMHEAD && whole;
   }
   consumer_sync();
   if (tid == 0 && trace) {
@@ -2164,6 +2182,7 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
       continue;
     }
     if ((tid & 31) == 0) c->cur[tid >> 5] = in;  // the ops read their warp's shared copy
+    if (tid == 0 && in.op != OP_LMHEAD) c->lm_staged = 0;  // any other op may overwrite the x buffer
     __syncwarp();
     uint64_t t_fetch = 0, t_ready = 0;
     if (TRACE) {
@@ -2376,6 +2395,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
     }
     c->pool_slot = 0;
     c->pool_ph = 0;
+    c->lm_staged = 0;
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c->xfull[i], 1);
       c->xph[i] = 0;
