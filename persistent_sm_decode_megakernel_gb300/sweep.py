@@ -10,6 +10,9 @@ Each part prints one JSON object (and all of them go to --json):
             step-time difference over the launch-count difference (§7.2: ~4.5 us per HIP
             launch); and the waiting share of each CTA's step from the journal (§7.2:
             grid synchronisation ~35 % of a token's time)
+  batch512  the 2b model at 512 cached positions (the benchmark's context), batch 1/2/4/8/16,
+            persistent with counters and with sentinels: us per step, aggregate tok/s and the
+            fraction of the HBM roofline (batches 3..16 run the tensor-core GEMV)
   ctx32k    the 2b model at 32768 cached positions, batch 1/2/4/8/16, persistent with
             counters, persistent with sentinels and the multi-launch control: us per step,
             aggregate tok/s, and the fraction of the HBM roofline (weights + KV per step)
@@ -116,6 +119,28 @@ def part_launch():
         _time_steps(dec, [1], [P], n_warm=2, n=1)
         out[name]["wait_share_of_step"] = summarize(dec.trace())["wait_share_mean"]
         dec.close()
+    return out
+
+
+def part_batch512():
+    import synth
+    from persistent_sm_decode_megakernel_gb300.model import Decoder, DeviceModel
+    cfg = synth.CONFIGS["2b"]
+    T = cfg.prompt_len
+    w = synth.gen_weights(cfg)
+    peak = _peak()
+    out = {}
+    for B in (1, 2, 4, 8, 16):
+        dm = DeviceModel(cfg, w, max_batch=B, max_ctx=T + 16)
+        _fill_kv(dm, cfg, B, T)
+        for name, sync in (("counter", 0), ("sentinel", 1)):
+            dec = Decoder(dm, sync_mode=sync)
+            us, _, _ = _time_steps(dec, [1] * B, [T] * B, n_warm=2, n=6)
+            dec.close()
+            gbs = _algo_bytes(cfg, [T + 4] * B) / (us * 1e-6) / 1e9
+            out[f"B{B}_{name}"] = {"us_per_step": us, "tok_s": B / (us * 1e-6), "roofline_frac": gbs / peak}
+            print(json.dumps({f"B{B}_{name}": out[f"B{B}_{name}"]}), flush=True)
+        del dm
     return out
 
 
@@ -272,7 +297,7 @@ def part_dies():
             "kb_blocks_one_home": float(np.mean((blocks == 0) | (blocks == 4)))}
 
 
-PARTS = {"barrier": part_barrier, "launch": part_launch, "ctx32k": part_ctx32k, "ragged": part_ragged,
+PARTS = {"barrier": part_barrier, "launch": part_launch, "batch512": part_batch512, "ctx32k": part_ctx32k, "ragged": part_ragged,
          "ctx8k": part_ctx8k, "prefill": part_prefill, "dies": part_dies}
 
 
