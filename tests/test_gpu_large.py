@@ -1,7 +1,8 @@
 """Parity on the two largest workloads, at their full model dimensions.
 
 * 8b: the bf16 model with 32 layers, d 4096, 32/8 heads, FFN 14336 and vocab 128256.
-  (a) A 32-token prompt goes through mk_prefill, then teacher-forced decode steps follow.
+  (a) A 32-token prompt goes through mk_prefill, then teacher-forced decode steps follow;
+  the same at batch 4 (the tensor-core GEMV) under both syncs.
   (b) The workload's own context: 8192 cached positions per sequence (seeded synthetic
   keys and values, synth.gen_kv, the same bytes on both sides -- an 8192-token fp64
   prefill of the 8b model would take the oracle hours), then two teacher-forced decode
@@ -56,6 +57,31 @@ def test_8b_teacher_forced(lib):
     dec = lib.Decoder(dm)
     z, tg = gpu_teacher_forced(dec, prompt, toks, n_new, cfg.vocab)
     dec.close()
+    assert_parity(z, tg, zref, toks, P)
+
+
+@pytest.fixture(scope="module")
+def b4_8b(lib):
+    """The 8b model at batch 4: an 8-token prompt per sequence, three teacher-forced steps."""
+    cfg = synth.CONFIGS["8b"]
+    w = synth.gen_weights(cfg)
+    P, n_new = 8, 3
+    prompt = synth.gen_prompts(cfg, 4, P)
+    toks, zref = oracle_run(cfg, w, prompt, n_new, model=_UncachedModel(cfg, w))
+    return cfg, w, prompt, toks, zref, P, n_new
+
+
+@pytest.mark.parametrize("sync", [0, 1], ids=["counter", "sentinel"])
+def test_8b_batch4_teacher_forced(b4_8b, lib, sync):
+    """bf16 on the tensor-core GEMV at the 8b widths: d 4096 does not fit the x buffer whole,
+    so every GEMV stages window by window (double-buffered bulk copies with counters, three
+    windows per polled staging with sentinels) and the down projection walks 14 windows."""
+    cfg, w, prompt, toks, zref, P, n_new = b4_8b
+    dm = lib.DeviceModel(cfg, w, max_batch=4, max_ctx=P + n_new)
+    dec = lib.Decoder(dm, sync_mode=sync)
+    z, tg = gpu_teacher_forced(dec, prompt, toks, n_new, cfg.vocab)
+    dec.close()
+    del dm
     assert_parity(z, tg, zref, toks, P)
 
 
