@@ -305,12 +305,13 @@ def test_tiny_long_context_many_splits(lib, tiny, page_bytes, merge):
         assert_parity(z, tg, zref, toks, P)
 
 
-@pytest.mark.parametrize("B", [2, 5])
+@pytest.mark.parametrize("B", [2, 5, 11])
 @pytest.mark.parametrize("merge", [1, 2, 3], ids=["merge-step", "merge-in-oproj", "merge-last-arriver"])
 @pytest.mark.parametrize("sync", [0, 1], ids=["counter", "sentinel"])
 def test_tiny_batched_merge_modes(lib, tiny, merge, sync, B):
-    """Batches 2 (CUDA-core GEMV) and 5 (tensor-core GEMV, O-proj input in fragment form
-    from the merge) under every split-merge placement."""
+    """Batches 2 (CUDA-core GEMV), 5 and 11 (tensor-core GEMV with one and two tiles of 8
+    sequences, three and five of them empty; O-proj input in fragment form from the merge)
+    under every split-merge placement."""
     cfg, w, m = tiny
     P, n_new = cfg.prompt_len, 6
     prompt = synth.gen_prompts(cfg, B, P)
