@@ -57,7 +57,10 @@ typedef struct {
   int n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn_dim, vocab;
   int dtype;              /* mk_dtype of weights AND KV cache                            */
   float rms_eps, rope_theta;
-  int max_batch;          /* 1..16 sequences per step                                    */
+  int max_batch;          /* 1..16 sequences per step; from 3 on, steps of 3..16 sequences
+                             run the tensor-core GEMV (mma.sync, weights landed by tensor-map
+                             copies), which needs d_model, ffn_dim and n_heads*head_dim to be
+                             multiples of 64                                              */
   int max_ctx;            /* KV-cache capacity in positions, at most 4194304 (2^22)      */
 } mk_model_desc;
 
@@ -83,7 +86,10 @@ typedef struct {
 
 /* Options; a zero-initialised struct selects the defaults. */
 typedef struct {
-  int sync_mode;          /* mk_sync_mode: counters (§8.5) or NaN sentinels (§7.3)        */
+  int sync_mode;          /* mk_sync_mode: counters (§8.5) or NaN sentinels (§7.3).
+                             Measured on the 2b model: sentinels are faster at batches 1..2,
+                             counters from batch 4 on (their dependency wait lets the
+                             tensor-core GEMV's inputs land by one bulk copy per op)       */
   int exec_mode;          /* mk_exec_mode: one persistent launch, or the multi-launch control */
   int page_bytes;         /* shared-memory page size (default 32768; power of two, 4K..32K) */
   int n_pages;            /* pages in the pool (default: as many as fit)                  */
