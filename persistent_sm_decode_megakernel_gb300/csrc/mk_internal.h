@@ -64,7 +64,8 @@ static_assert(sizeof(Instr) == 64, "instruction is 64 bytes");
 //   QKV     a0 matrix (0 q, 1 k, 2 v), a1 head, a2 first pair i0, a3 pairs n,
 //           p2 gain, p3 cache of this layer (k or v), p4 rows i0.., p5 rows hd/2+i0..
 //   ATTN    a0 b, a1 kv head j, a2 split s, a3 splits S, a4 arrival counter (-1: the
-//           merge is a separate ATTN_REDUCE), p4 keys of (b, j) at t = 0, p5 values
+//           merge is a separate ATTN_REDUCE), a5 units of the same layer that follow in
+//           this queue (split order), p4 keys of (b, j) at t = 0, p5 values
 //   REDUCE  a0 b, a1 j
 //   OPROJ / DOWN   a0 row0, a1 rows, p4 first row (OPROJ with F_MERGE_IN: its input is
 //           merged from the split partials while it is staged), p2 the RMSNorm gain of the

@@ -322,6 +322,14 @@ __device__ __forceinline__ Attn make_attn(const DevState& S, const StepArgs& A, 
 __device__ __forceinline__ bool attn_unit_active(const DevState& S, const StepArgs& A, const Instr& in) {
   return in.a[0] < A.B && in.a[2] < active_splits(S, A, in.a[0]);
 }
+// how many queued units to skip after an inactive one: all of its run (a5) when its split is
+// past every sequence's active count -- the run's later units have no smaller split
+__device__ __noinline__ int attn_run_skip(const DevState& S, const StepArgs& A, const Instr& in) {
+  if (in.a[5] <= 0) return 0;
+  int mx = 0;
+  for (int b = 0; b < A.B; ++b) mx = max(mx, active_splits(S, A, b));
+  return in.a[2] >= mx ? in.a[5] : 0;
+}
 
 // first (cos, sin) of sequence b's RoPE row: the table's row of its position, or row b of a
 // table that holds one row per sequence of the step
@@ -502,6 +510,8 @@ __device__ __noinline__ void producer(const DevState& S_arg, const StepArgs& A_a
       }
       case OP_ATTN:
         stream_attn(in);
+        // the compute warps skip the rest of an inactive run; so does the loader
+        if (!attn_unit_active(S, A, in)) pc += attn_run_skip(S, A, in);
         break;
       case OP_ATTN_POOL: {
         // dynamic work queue (§8.8): claim the layer's units one at a time while the ring
@@ -2177,8 +2187,10 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
     // barrier (the decision is uniform over the CTA); with counters it still signals (its
     // waiters count every unit), except under the fused merge, which counts active splits
     if (in.op == OP_ATTN && !attn_unit_active(S, A, in)) {
+      const int skip = attn_run_skip(S, A, in);  // the rest of the run as well (uniform)
       if (SYNC == SYNC_COUNTER && in.a[4] < 0 && !nosync && tid == 0 && in.signal_ctr >= 0)
-        red_release_add_u32(&S.counters[in.signal_ctr], 1u);
+        red_release_add_u32(&S.counters[in.signal_ctr], 1u + (uint32_t)skip);
+      pc += skip;
       continue;
     }
     if ((tid & 31) == 0) c->cur[tid >> 5] = in;  // the ops read their warp's shared copy

@@ -411,6 +411,16 @@ std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B,
     p->queues[pe.cta].push_back(pe.in);
   }
   for (auto& q : p->queues) q.push_back(mk_instr(OP_END, 0, -1, 0, -1));
+  // a CTA's split-KV units of one layer sit together, in split order: each carries how many
+  // units of the same run follow it (a5), so that a CTA meeting a split past every
+  // sequence's active count skips the rest of the run in one step
+  for (auto& q : p->queues)
+    for (size_t i = 0; i < q.size(); ++i)
+      if (q[i].op == OP_ATTN) {
+        int n = 0;
+        while (i + 1 + n < q.size() && q[i + 1 + n].op == OP_ATTN && q[i + 1 + n].layer == q[i].layer) ++n;
+        q[i].a[5] = n;
+      }
   // the tensor-core GEMV's RMSNorm inputs carry one sum-of-squares slot per CTA, written by
   // that CTA's EMBED, O-proj or DOWN instruction: each CTA must hold exactly one of each
   // (per layer)
