@@ -511,7 +511,7 @@ __device__ __noinline__ void producer(const DevState& S_arg, const StepArgs& A_a
       case OP_ATTN:
         stream_attn(in);
         // the compute warps skip the rest of an inactive run; so does the loader
-        if (!attn_unit_active(S, A, in)) pc += attn_run_skip(S, A, in);
+        if (TC && !attn_unit_active(S, A, in)) pc += attn_run_skip(S, A, in);
         break;
       case OP_ATTN_POOL: {
         // dynamic work queue (§8.8): claim the layer's units one at a time while the ring
@@ -2186,11 +2186,13 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
     // a split unit past this step's active count has nothing to compute: skipped without a
     // barrier (the decision is uniform over the CTA); with counters it still signals (its
     // waiters count every unit), except under the fused merge, which counts active splits
+    // (with the tensor-core GEMV's batches: the rest of the run as well, see attn_run_skip;
+    // batches 1..2 have runs of one or two units, and their instance keeps the simpler loop)
     if (in.op == OP_ATTN && !attn_unit_active(S, A, in)) {
-      const int skip = attn_run_skip(S, A, in);  // the rest of the run as well (uniform)
+      const int skip = TC ? attn_run_skip(S, A, in) : 0;
       if (SYNC == SYNC_COUNTER && in.a[4] < 0 && !nosync && tid == 0 && in.signal_ctr >= 0)
         red_release_add_u32(&S.counters[in.signal_ctr], 1u + (uint32_t)skip);
-      pc += skip;
+      if (TC) pc += skip;
       continue;
     }
     if ((tid & 31) == 0) c->cur[tid >> 5] = in;  // the ops read their warp's shared copy
