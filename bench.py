@@ -56,15 +56,16 @@ def kernel_source_hash(sync="sentinel"):
 
 
 def profiled_traffic(sync="sentinel"):
-    """DRAM bytes of one decode step from the committed ncu summary (single-step launches),
-    if it was taken on the current kernel sources (else None)."""
+    """(DRAM bytes, algorithmic bytes) of one decode step from the committed ncu summary, if it
+    was taken on the current kernel sources (else None)."""
     try:
         with open(PROFILE_SUMMARY) as f:
             kv = dict(l.split(":", 1) for l in f.read().splitlines() if ":" in l)
         if kv.get("kernel_source_sha", "").strip() != kernel_source_hash(sync):
             return None
-        key = "dram_bytes_per_step" if "dram_bytes_per_step" in kv else "dram_bytes_per_launch"
-        return float(kv[key].strip())
+        dram = float(kv["dram_bytes_per_step"].strip())
+        return dram, float(kv["algorithmic_bytes_per_step"].split()[0])
+
     except (OSError, KeyError, ValueError):
         return None
 
@@ -341,7 +342,9 @@ def main():
                "sample": f"{n} fp64 oracle decode steps of the same 2B model, batch 1, at positions "
                          f"{PROMPT + 9}..{PROMPT + 8 + n} (cache of {PROMPT + 8} seeded synthetic positions, the "
                          f"GPU's context), {dt:.1f} s after 1 untimed step"}
-    traffic = profiled_traffic(args.sync)
+    prof = profiled_traffic(args.sync)
+    # the capture ran at a shorter context: scale its DRAM bytes by the algorithmic bytes (K/V grows with it)
+    traffic = None if prof is None else prof[0] * bytes_per_step / prof[1]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": 1000.0 * total_s / K, "higher_is_better": True, "scaling": "weak",
@@ -353,6 +356,9 @@ def main():
         "gpu_launches": len(chunks) * info["launches_per_step"],
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
                      "frac": achieved_gbs / peak, "traffic": traffic,
+                     "traffic_source": None if traffic is None else
+                     "ncu DRAM read+write of a 64-step launch of this command at a shorter context, per step, "
+                     "scaled by the algorithmic bytes (profiles/mk_step_kernel_2b_b1.txt)",
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs, copy)",
                      "per": "decode step (a launch runs steps_per_launch of them)",
                      "steps_per_launch": C, "bytes_per_step": bytes_per_step, "mean_step_us": mean_step_s * 1e6,
