@@ -121,6 +121,11 @@ typedef struct {
                              one at a time (an atomic claim counter) as its ring frees,
                              instead of a fixed share dealt to its queue; persistent
                              control only (0: fixed shares, the default)                 */
+  int attn_cuda_cores;    /* 1: every split-KV unit on CUDA cores.  0 (default): a unit of
+                             at least half a page of cached positions (64 at head_dim 128,
+                             128 at 64) runs q K^T and P V on the tensor cores (mma.sync,
+                             q and P as hi/lo 16-bit halves, fp32 accumulators), its K and
+                             V pages landed by tensor-map copies; needs 32 KB pages       */
 } mk_options;
 
 typedef struct {
@@ -294,8 +299,11 @@ mk_status mk_decode_step_noalloc(const mk_model_desc *desc, const mk_weights *we
  * nothing else (P1 §7.5 continuous weight streaming, P2 §8.4 pages).  One CTA per SM
  * streams total_bytes / #SM of contiguous device memory through n_pages TMA pages of
  * page_bytes; mode 0: pages are released unread, mode 1: each compute warp first runs
- * the fp16 GEMV slice product on its eighth; hint 1: L2 evict-first policy.  *gbps gets
- * the best of three timed runs.  Allocates total_bytes of device memory for the run. */
+ * the fp16 GEMV slice product on its eighth; hint bit 0: L2 evict-first policy; hint bit 1:
+ * every CTA streams the same total_bytes / #SM (the access pattern of a GEMV input that
+ * all SMs read; *gbps then counts the bytes delivered to the SMs).  *gbps gets the best of
+ * three timed runs.  Allocates total_bytes of device memory for the run (hint bit 1:
+ * total_bytes / #SM). */
 mk_status mk_stream_bench(int page_bytes, int n_pages, int mode, int hint, long long total_bytes, double *gbps);
 
 const char *mk_last_error(void);

@@ -50,7 +50,8 @@ class mk_options(ctypes.Structure):
                 ("kv_splits", c_int), ("trace", c_int), ("wait_timeout_s", c_double),
                 ("backoff_max_ns", c_int), ("max_ctas", c_int), ("fault_drop_signal", c_int),
                 ("split_min_positions", c_int),
-                ("attn_merge", c_int), ("inflight_pages", c_int), ("attn_pool", c_int)]
+                ("attn_merge", c_int), ("inflight_pages", c_int), ("attn_pool", c_int),
+                ("attn_cuda_cores", c_int)]
 
 
 class mk_info_t(ctypes.Structure):

@@ -167,16 +167,22 @@ mk_status get_sched_in(mk_ctx* ctx, const ModelShape& m, const Geometry& geo,
   }
   int nb = 1;
   while (nb < B) nb <<= 1;
-  if (use_tc(geo, nb)) {
+  if (use_tc(geo, nb) || geo.attn_mma) {
     std::vector<TmapImage> maps;
-    e = build_tc_maps(m, geo, &sc->plan, &maps);
+    if (use_tc(geo, nb)) {
+      e = build_tc_maps(m, geo, &sc->plan, &maps);
+      if (!e.empty()) return fail(MK_ERR_CUDA, "tensor maps: " + e);
+    }
+    e = build_kv_maps(m, geo, ctx->m.max_batch, &sc->plan, &maps);
     if (!e.empty()) return fail(MK_ERR_CUDA, "tensor maps: " + e);
     mk_status s = upload(sc->tmaps, maps.data(), maps.size() * sizeof(TmapImage));
     if (s) return s;
     const uintptr_t dev = reinterpret_cast<uintptr_t>(sc->tmaps.p);
-    for (auto& q : sc->plan.queues) place_tc_maps(q, dev);
+    const bool gm = use_tc(geo, nb);
+    for (auto& q : sc->plan.queues) place_tc_maps(q, dev, gm);
     for (auto& ph : sc->plan.phase_queues)
-      for (auto& q : ph) place_tc_maps(q, dev);
+      for (auto& q : ph) place_tc_maps(q, dev, gm);
+    place_tc_maps(sc->plan.pool, dev, gm);
   }
   mk_status s = upload_queues(sc->plan.queues, sc->instr, sc->qstart, &sc->n_instr, &sc->plan.pool);
   if (s) return s;
@@ -376,6 +382,7 @@ mk_status ensure_prefill(mk_ctx* ctx) {
   S.n_pages = g.n_pages;
   S.page_stride = g.page_stride;
   S.tc = g.tc;
+  S.attn_mma = g.attn_mma;
   S.xbuf_bytes = g.xbuf_bytes;
   S.scratch_bytes = g.scratch_bytes;
   S.smem_bytes = g.smem_bytes;
@@ -475,6 +482,7 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
     return fail(MK_ERR_INVALID, "exec_mode");
   if (o.attn_merge < 0 || o.attn_merge > 3) return fail(MK_ERR_INVALID, "attn_merge must be 0..3");
   if (o.attn_pool < 0 || o.attn_pool > 1) return fail(MK_ERR_INVALID, "attn_pool must be 0 or 1");
+  if (o.attn_cuda_cores < 0 || o.attn_cuda_cores > 1) return fail(MK_ERR_INVALID, "attn_cuda_cores must be 0 or 1");
   ctx->stream = reinterpret_cast<cudaStream_t>(stream);
   MK_CUDA(cudaGetDevice(&ctx->device));
   MK_CUDA(cudaDeviceGetAttribute(&ctx->n_sm, cudaDevAttrMultiProcessorCount, ctx->device));
@@ -487,8 +495,9 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
   // one wave (§8.3): opt in to the shared memory, ask how many CTAs fit, launch exactly that
   ctx->kernel_tc = step_kernel_entry(m.dtype, o.sync_mode, false, true);
   ctx->kernel_tc_ms = step_kernel_entry(m.dtype, o.sync_mode, true, true);
-  ctx->kernel = ctx->geo.tc ? ctx->kernel_tc : step_kernel_entry(m.dtype, o.sync_mode, false, false);
-  ctx->kernel_ms = ctx->geo.tc ? ctx->kernel_tc_ms : step_kernel_entry(m.dtype, o.sync_mode, true, false);
+  if (o.attn_cuda_cores) ctx->geo.attn_mma = 0;
+  ctx->kernel = ctx->geo.tc_instance() ? ctx->kernel_tc : step_kernel_entry(m.dtype, o.sync_mode, false, false);
+  ctx->kernel_ms = ctx->geo.tc_instance() ? ctx->kernel_tc_ms : step_kernel_entry(m.dtype, o.sync_mode, true, false);
   for (const void* fn : {ctx->kernel, ctx->kernel_ms, ctx->kernel_tc, ctx->kernel_tc_ms})
     // the attribute is per function (shared by every context in the process): the device's
     // limit, so that no context's launch is refused after another context sets a lower one
@@ -501,6 +510,7 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
     e = make_geometry(m, ctx->n_cta, o.page_bytes, o.n_pages, o.kv_splits, smem_optin, &ctx->geo);
     if (!e.empty()) return fail(MK_ERR_INVALID, e);
   }
+  if (o.attn_cuda_cores) ctx->geo.attn_mma = 0;
   const Geometry& g = ctx->geo;
   {  // prompt chunks: the tensor-core geometry of kMaxBatch rows, if it fits the same wave
     PrefillState& pf = ctx->pf;
@@ -511,6 +521,7 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
       int bp = 0;
       MK_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bp, ctx->kernel_tc, kThreads, pf.geo.smem_bytes));
       if (bp < ctx->bpsm) pf.geo.smem_bytes = 0;  // chunks would not run in one wave: per-position prefill
+      if (o.attn_cuda_cores) pf.geo.attn_mma = 0;
     } else {
       pf.geo.smem_bytes = 0;
     }
@@ -580,6 +591,7 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
   S.n_pages = g.n_pages;
   S.page_stride = g.page_stride;
   S.tc = g.tc;
+  S.attn_mma = g.attn_mma;
   S.xbuf_bytes = g.xbuf_bytes;
   S.scratch_bytes = g.scratch_bytes;
   S.smem_bytes = g.smem_bytes;
@@ -1179,7 +1191,7 @@ mk_status mk_barrier_bench(int mode, int n_barriers, double* us_per_barrier) {
 
 mk_status mk_stream_bench(int page_bytes, int n_pages, int mode, int hint, long long total_bytes, double* gbps) {
   if (!gbps || page_bytes < 1024 || page_bytes > 65536 || (page_bytes & 15) || n_pages < 1 || n_pages > kMaxPages ||
-      mode < 0 || mode > 5 || total_bytes < (1LL << 20) || (mode >= 2 && page_bytes != 32768))
+      mode < 0 || mode > 5 || hint < 0 || hint > 3 || total_bytes < (1LL << 20) || (mode >= 2 && page_bytes != 32768))
     return fail(MK_ERR_INVALID, "stream bench: bad arguments");
   int dev = 0, n_sm = 0;
   MK_CUDA(cudaGetDevice(&dev));
@@ -1189,8 +1201,9 @@ mk_status mk_stream_bench(int page_bytes, int n_pages, int mode, int hint, long 
   const void* fn = stream_kernel_entry();
   MK_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
   DevBuf src, sink;
-  MK_CUDA(cudaMalloc(&src.p, (size_t)per_cta * n_sm));
-  MK_CUDA(cudaMemset(src.p, 0x3C, (size_t)per_cta * n_sm));
+  const size_t src_bytes = (size_t)per_cta * ((hint & 2) ? 1 : n_sm);  // bit 1: one region read by all
+  MK_CUDA(cudaMalloc(&src.p, src_bytes));
+  MK_CUDA(cudaMemset(src.p, 0x3C, src_bytes));
   MK_CUDA(cudaMalloc(&sink.p, sizeof(float) * n_sm * kConsumerWarps));
   const uint8_t* sp = reinterpret_cast<const uint8_t*>(src.p);
   float* sk = reinterpret_cast<float*>(sink.p);

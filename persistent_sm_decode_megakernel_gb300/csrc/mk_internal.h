@@ -172,6 +172,7 @@ struct DevState {
   int page_bytes, n_pages;
   int page_stride;             // bytes between ring slots (>= page_bytes)
   int tc;                      // batches of 3..16 use the tensor-core GEMV
+  int attn_mma;                // split-KV units of at least half a page use tensor cores
   int xbuf_bytes, scratch_bytes;
   int smem_bytes;              // dynamic shared memory of a launch with this state (host use)
   int sync_mode;
@@ -234,6 +235,8 @@ constexpr int kSplitLongPositions = 2048;
 // a split's partial attention record per head: hd weighted value sums, the running max,
 // the exp-sum, two pad floats (16-byte rows, so records move as float4)
 constexpr int kPartExtra = 4;
+constexpr int kTmapBytes = 128;  // one tensor map (CUtensorMap) in device memory
+constexpr int kAttnMmaMinCtx = 4096;  // KV capacity from which batch-1..2 contexts take the tensor-core instance
 
 // shared-memory layout sizes (bytes)
 constexpr int kCtlSmem = 4096;   // barriers, flags, small broadcast values

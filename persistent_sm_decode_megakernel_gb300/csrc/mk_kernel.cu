@@ -147,6 +147,7 @@ __global__ void __launch_bounds__(32, 1) mk_line_lat_kernel(const uint32_t* buf,
 // loader warp streams bytes_per_cta of contiguous HBM through a ring of n_pages pages
 // with TMA bulk copies; the 8 compute warps either hand each page straight back
 // (mode 0) or first run the B=1 fp16 GEMV slice product on their eighth of it (mode 1).
+// hint bit 0: L2 evict-first policy; bit 1: all CTAs read the same bytes.
 __global__ void __launch_bounds__(kThreads, 1) mk_stream_kernel(const uint8_t* src, long long bytes_per_cta,
                                                                 int page_bytes, int n_pages, int mode, int hint,
                                                                 float* sink) {
@@ -168,7 +169,9 @@ __global__ void __launch_bounds__(kThreads, 1) mk_stream_kernel(const uint8_t* s
   for (int i = tid; i < ws; i += kThreads) x[i] = 1.0f / (1 + (i & 7));
   __syncthreads();
   const long long n = bytes_per_cta / page_bytes;
-  const uint8_t* base = src + (long long)blockIdx.x * bytes_per_cta;
+  // hint bit 1: every CTA streams the same bytes (the GEMV inputs' access pattern: all SMs
+  // read one vector), else each its own slice
+  const uint8_t* base = (hint & 2) ? src : src + (long long)blockIdx.x * bytes_per_cta;
   const uint64_t t0 = globaltimer_ns();
   const uint64_t limit = 2000000000ull;
   if (warp == kConsumerWarps) {
@@ -184,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_stream_kernel(const uint8_t* s
         }
       }
       mbar_arrive_expect_tx(&full[slot], (uint32_t)page_bytes);
-      if (hint)
+      if (hint & 1)
         tma_load_1d(pages + (size_t)slot * page_bytes, base + c * page_bytes, (uint32_t)page_bytes, &full[slot], pol);
       else
         tma_load_1d_plain(pages + (size_t)slot * page_bytes, base + c * page_bytes, (uint32_t)page_bytes, &full[slot]);

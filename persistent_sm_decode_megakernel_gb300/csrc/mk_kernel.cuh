@@ -317,6 +317,24 @@ __device__ __forceinline__ Attn make_attn(const DevState& S, const StepArgs& A, 
   return a;
 }
 
+// The tensor-core attention takes the units of at least half a page of cached positions
+// (both roles decide alike).  Its page blk is the box of pb positions from attn_box_pos: the
+// block's own positions are the box rows [lo, pb) -- all of them but in the last block, whose
+// box ends at the unit's last cached position, so that its first rows hold earlier positions
+// of the sequence (or zeros before position 0): finite values, masked by the consumer.
+__device__ __forceinline__ bool attn_mma_unit(const DevState& S, const Attn& a) {
+  return S.attn_mma && a.n_cached * 2 >= a.pb;
+}
+__device__ __noinline__ bool attn_use_mma(const DevState& S_arg, const StepArgs& A_arg, const Instr& in_arg) {
+  const Instr& in = smem_ctl()->cur[threadIdx.x >> 5];
+  return attn_mma_unit(smem_ctl()->S, make_attn(smem_ctl()->S, smem_ctl()->args, in));
+}
+__device__ __forceinline__ int attn_box_pos(const Attn& a, int blk, int* lo) {
+  const int start = blk * a.pb, np = min(a.pb, a.n_cached - start);
+  *lo = a.pb - np;
+  return a.t0 + start - *lo;
+}
+
 // a split-KV unit with work this step: its sequence is in the batch and its split below the
 // sequence's active count (uniform over the CTA)
 __device__ __forceinline__ bool attn_unit_active(const DevState& S, const StepArgs& A, const Instr& in) {
@@ -409,6 +427,26 @@ __device__ __noinline__ void producer(const DevState& S_arg, const StepArgs& A_a
       kv_ready = true;
     }
     const Attn at = make_attn(S, A, un);
+    if (TC && attn_mma_unit(S, at)) {  // one tensor-map box per K / V page (key map, value map after it)
+      const uint8_t* km = reinterpret_cast<const uint8_t*>(iptr(un, kP3));
+      const int bh = A.seq[at.b] * S.Hkv + at.j;
+      for (int blk = 0; blk < at.nblocks && ok; ++blk) {
+        int lo;
+        const int p0 = attn_box_pos(at, blk, &lo);
+        for (int kv = 0; kv < 2; ++kv) {
+          if (!producer_acquire(S, c, slot, ph, issued++)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&c->full[slot], (uint32_t)S.page_bytes);
+          tma_load_4d(pages + (size_t)slot * S.page_stride, km + kv * kTmapBytes, 0, p0, 0, bh,
+                      &c->full[slot], pol);
+          c->last_issue_phase[slot] = (int)ph;
+          if (++slot == S.n_pages) { slot = 0; ph ^= 1u; }
+        }
+      }
+      return;
+    }
     for (int blk = 0; blk < at.nblocks && ok; ++blk) {
       const int p0 = blk * at.pb;
       const int np = min(at.pb, at.n_cached - p0);
@@ -1618,6 +1656,47 @@ __device__ __noinline__ void op_gemv_tc(const DevState& S_arg, const StepArgs& A
 }
 
 // ---------------------------------------------------------------- attention
+// The split's partial record from the compute warps' partials in scratch ([warp][G][HD +
+// kPartExtra]: G rows of HD weighted sums, then the warp's running max and sum): the warps'
+// sums weighted by exp2(m_w - M) (a warp that saw no position has m_w = -inf and weight 0);
+// the thread of element 0 of a head also writes M, the weighted sum and the two zero pads
+template <int HD, int G>
+__device__ __forceinline__ void attn_combine_warps(const DevState& S, float* act, const Attn& at, int l,
+                                                   const float* scratch) {
+  constexpr int RW = HD + kPartExtra;
+  const int tid = threadIdx.x;
+  float* part = act_ptr(S, act, ACT_PART, l) + (((size_t)at.b * S.Hkv + at.j) * S.S + at.s) * G * RW;
+  for (int t = tid; t < G * HD; t += kConsumerThreads) {
+    const int g = t / HD, e = t - g * HD;
+    const float* sg = scratch + g * RW;
+    float mw[kConsumerWarps], wt[kConsumerWarps];
+    float M = -CUDART_INF_F;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      mw[w] = sg[w * G * RW + HD];
+      M = fmaxf(M, mw[w]);
+    }
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) wt[w] = mw[w] == -CUDART_INF_F ? 0.f : exp2f(mw[w] - M);
+    float r0 = 0.f, r1 = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; w += 2) {
+      r0 = fmaf(wt[w], sg[w * G * RW + e], r0);
+      r1 = fmaf(wt[w + 1], sg[(w + 1) * G * RW + e], r1);
+    }
+    part[g * RW + e] = r0 + r1;
+    if (e == 0) {
+      float L = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) L = fmaf(wt[w], sg[w * G * RW + HD + 1], L);
+      part[g * RW + HD] = M;
+      part[g * RW + HD + 1] = L;
+      part[g * RW + HD + 2] = 0.f;  // pads: written so that sentinel polls of the whole record end
+      part[g * RW + HD + 3] = 0.f;
+    }
+  }
+}
+
 template <typename WT, int SYNC, int HD, int G>
 __device__ __noinline__ void op_attn(const DevState& S_arg, const StepArgs& A_arg, const Instr& in_arg, SmemCtl* c, uint8_t* pages,
                         float* xbuf, float* scratch, Ring& ring_io, float* act) {
@@ -1881,39 +1960,257 @@ __device__ __noinline__ void op_attn(const DevState& S_arg, const StepArgs& A_ar
     }
   }
   consumer_sync();
-  // the warps' partials, weighted by exp2(m_w - M) (a warp that saw no position has
-  // m_w = -inf and weight 0); the thread of element 0 of a head also writes M, the
-  // weighted sum and the two zero pads of the record
-  float* part = act_ptr(S, act, ACT_PART, l) + (((size_t)at.b * S.Hkv + at.j) * S.S + at.s) * G * RW;
-  for (int t = tid; t < G * HD; t += kConsumerThreads) {
-    const int g = t / HD, e = t - g * HD;
-    const float* sg = scratch + g * RW;
-    float mw[kConsumerWarps], wt[kConsumerWarps];
-    float M = -CUDART_INF_F;
+  attn_combine_warps<HD, G>(S, act, at, l, scratch);
+}
+
+// ---------------------------------------------------------------- attention on tensor cores
+// The split-KV unit of op_attn (the same partial record) with its two contractions on
+// mma.sync m16n8k16.  Warp w takes rows 16w .. 16w+15 of each 128-row pass of a page.
+// Scores: the A tile holds head g's scaled query as 16-bit halves, hi in row g and lo in row
+// g + 8 (heads g >= G: zeros); B is the 16 keys as columns; head g's score of a key is the
+// sum of accumulator rows g and g + 8 -- both in the lane that holds it.  The online softmax
+// runs on those accumulators (a lane group of 4 lanes per head, 4 keys per lane).  Values:
+// the probabilities' hi/lo halves form the A tile of P V straight from the score
+// accumulators' layout (rows g / g + 8 again), B the value rows read transposed by
+// ldmatrix, and head g's output is the sum of accumulator rows g and g + 8.  K and V pages
+// land as [64-element half][row][128 bytes] with 16-byte chunk c of row r at c ^ (r % 8)
+// (the tensor map's 128-byte swizzle), so that ldmatrix's eight row reads of one chunk fall
+// in eight bank groups.  The step's new rows sit in a 16-row page of the same layout.
+template <typename WT, int SYNC, int HD, int G>
+__device__ __noinline__ void op_attn_tc(const DevState& S_arg, const StepArgs& A_arg, const Instr& in_arg, SmemCtl* c,
+                                        uint8_t* pages, float* xbuf, float* scratch, Ring& ring_io, float* act) {
+  const Instr& in = smem_ctl()->cur[threadIdx.x >> 5];
+  const DevState& S = smem_ctl()->S;
+  const StepArgs& A = smem_ctl()->args;
+  c = smem_ctl();
+  pages = smem_pages();
+  xbuf = smem_xbuf(S);
+  scratch = smem_scratch(S);
+  RingCopy ring_copy(ring_io);
+  Ring& ring = ring_copy.r;
+  static_assert(G <= 8 && (HD == 64 || HD == 128), "tensor-core attention shape");
+  constexpr int NKS = HD / 16;          // k-steps of q K^T
+  constexpr int NDT = HD / 8;           // 8-column output tiles of P V
+  constexpr int MINI = (HD / 64) * 16 * 128;  // bytes of one 16-row page of new rows
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, cq = lane & 3;
+  const Attn at = make_attn(S, A, in);
+  if (!at.active) return;  // uniform over the CTA
+  const int l = in.layer;
+  const float qscale = (1.0f / sqrtf((float)HD)) * 1.4426950408889634f;  // scores in log2 units
+
+  const float* qsrc = act_ptr(S, act, ACT_Q, l) + ((size_t)at.b * S.Hq + (size_t)at.j * G) * HD;
+  float4* q4 = reinterpret_cast<float4*>(xbuf);
+  stage_vec<SYNC>(S, reinterpret_cast<const float4*>(qsrc), G * HD / 4, c, [&](int i, float4 v) {
+    v.x *= qscale;
+    v.y *= qscale;
+    v.z *= qscale;
+    v.w *= qscale;
+    q4[i] = v;
+  });
+  consumer_sync();
+  // the query's A fragments, one 16-byte vector per (k-step, lane): rows gq (hi) and gq + 8
+  // (lo) of head gq, zeros for gq >= G -- built once, read with one load per k-step
+  uint4* qf = reinterpret_cast<uint4*>(xbuf + G * HD);
+  if (tid < NKS * 32) {
+    const int ks = tid >> 5, fg = (tid & 31) >> 2, fc = tid & 3;
+    uint32_t f[4] = {0u, 0u, 0u, 0u};
+    if (fg < G) {
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
-      mw[w] = sg[w * G * RW + HD];
-      M = fmaxf(M, mw[w]);
+      for (int h2 = 0; h2 < 2; ++h2) {  // k = 16 ks + 2 fc (+1), then + 8
+        const float* qp = xbuf + fg * HD + 16 * ks + 2 * fc + 8 * h2;
+        uint16_t h0, l0, h1, l1;
+        Mma<WT>::split(qp[0], h0, l0);
+        Mma<WT>::split(qp[1], h1, l1);
+        f[2 * h2] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+        f[2 * h2 + 1] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+      }
     }
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) wt[w] = mw[w] == -CUDART_INF_F ? 0.f : exp2f(mw[w] - M);
-    float r0 = 0.f, r1 = 0.f;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; w += 2) {
-      r0 = fmaf(wt[w], sg[w * G * RW + e], r0);
-      r1 = fmaf(wt[w + 1], sg[(w + 1) * G * RW + e], r1);
-    }
-    part[g * RW + e] = r0 + r1;
-    if (e == 0) {
-      float L = 0.f;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) L = fmaf(wt[w], sg[w * G * RW + HD + 1], L);
-      part[g * RW + HD] = M;
-      part[g * RW + HD + 1] = L;
-      part[g * RW + HD + 2] = 0.f;  // pads: written so that sentinel polls of the whole record end
-      part[g * RW + HD + 3] = 0.f;
+    qf[tid] = make_uint4(f[0], f[1], f[2], f[3]);
+  }
+  // this launch's new rows (keys and values of positions p0_b..pos_b, rounded to the storage
+  // dtype as the cache holds them): rows 0..n_new-1 of a key page and a value page, zeros after
+  uint8_t* mini = reinterpret_cast<uint8_t*>(qf + NKS * 32);
+  if (at.has_new) {
+    const float* kn0 = act_ptr(S, act, ACT_KVN, l) + (size_t)(at.b - at.n_new + 1) * 2 * S.Hkv * HD + (size_t)at.j * HD;
+    for (int t = tid; t < 2 * 16 * (HD / 4); t += kConsumerThreads) {
+      const int kv = t / (16 * (HD / 4)), u = t - kv * (16 * (HD / 4)), r = u / (HD / 4), e = (u % (HD / 4)) * 4;
+      uint2 w = make_uint2(0u, 0u);
+      if (r < at.n_new) {
+        const float* kn = kn0 + (size_t)r * 2 * S.Hkv * HD + (size_t)kv * S.Hkv * HD + e;
+        const float4 v = load_v4<SYNC>(reinterpret_cast<const float4*>(kn), S, c);
+        w.x = (uint32_t)Unpack<WT>::round(v.x) | ((uint32_t)Unpack<WT>::round(v.y) << 16);
+        w.y = (uint32_t)Unpack<WT>::round(v.z) | ((uint32_t)Unpack<WT>::round(v.w) << 16);
+      }
+      const int ch = (e & 63) >> 3;
+      *reinterpret_cast<uint2*>(mini + kv * MINI + (e >> 6) * 2048 + r * 128 + ((ch ^ (r & 7)) << 4) + (e & 7) * 2) = w;
     }
   }
+  consumer_sync();
+  const bool mark = (A.flags & SF_TRACE) && tid == 0;
+  if (mark) c->tmark[0] = globaltimer_ns();
+  uint64_t page_wait_ns = 0;  // journal: time spent waiting for K, V pages to land
+  const uint4* qfl = qf + lane;  // this lane's fragment of k-step ks at qfl[32 ks]
+  float o[NDT][4];
+#pragma unroll
+  for (int d = 0; d < NDT; ++d) o[d][0] = o[d][1] = o[d][2] = o[d][3] = 0.f;
+  float mrun = -CUDART_INF_F, lrun = 0.f;  // head gq's running max and (this lane's) sum
+
+  // rows [lo, hi) of a page whose halves hold rph rows each, npass passes of 128 rows
+  auto block = [&](uint32_t kbase, uint32_t vbase, int rph, int npass, int lo, int hi) {
+    const int mi = lane >> 3, ri = lane & 7;  // the matrix and the row this lane addresses
+    for (int ps = 0; ps < npass; ++ps) {
+      const int r0 = ps * 128 + warp * 16;
+      if (r0 + 16 <= lo || r0 >= hi) continue;  // uniform over the warp
+      // q K^T: key rows r0.. r0+7 and r0+8.. r0+15 (two column tiles), 16 dims per k-step
+      float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      {
+        const int row = r0 + ri + ((mi >> 1) << 3);
+#pragma unroll
+        for (int ks = 0; ks < NKS; ++ks) {
+          const int ch = 2 * ks + (mi & 1);
+          uint32_t b[4];
+          ldsm_x4(kbase + (uint32_t)((ch >> 3) * rph * 128 + row * 128 + (((ch & 7) ^ (row & 7)) << 4)), b);
+          const uint4 qa = qfl[32 * ks];
+          Mma<WT>::run(sa[0], qa, b[0], b[1]);
+          Mma<WT>::run(sa[1], qa, b[2], b[3]);
+        }
+      }
+      // online softmax over this lane group's head: 4 keys per lane, then the group's max
+      float sc[2][2];
+      float bm = -CUDART_INF_F;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int row = r0 + 8 * nt + 2 * cq + e;
+          const bool ok = gq < G && row >= lo && row < hi;
+          sc[nt][e] = ok ? sa[nt][e] + sa[nt][e + 2] : -CUDART_INF_F;
+          bm = fmaxf(bm, sc[nt][e]);
+        }
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+      const float mn = fmaxf(mrun, bm);
+      float p[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+      if (mn != -CUDART_INF_F) {
+        if (mn != mrun) {
+          const float corr = exp2f(mrun - mn);
+          lrun *= corr;
+#pragma unroll
+          for (int d = 0; d < NDT; ++d) {
+            o[d][0] *= corr;
+            o[d][1] *= corr;
+            o[d][2] *= corr;
+            o[d][3] *= corr;
+          }
+          mrun = mn;
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            p[nt][e] = exp2f(sc[nt][e] - mn);
+            lrun += p[nt][e];
+          }
+      }
+      __syncwarp();
+      // P's A fragment: a0 / a2 the hi halves of keys 2cq.. / 8+2cq.., a1 / a3 the lo halves
+      uint4 pa;
+      {
+        uint16_t h[2][2], lw[2][2];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) Mma<WT>::split(p[nt][e], h[nt][e], lw[nt][e]);
+        pa.x = (uint32_t)h[0][0] | ((uint32_t)h[0][1] << 16);
+        pa.y = (uint32_t)lw[0][0] | ((uint32_t)lw[0][1] << 16);
+        pa.z = (uint32_t)h[1][0] | ((uint32_t)h[1][1] << 16);
+        pa.w = (uint32_t)lw[1][0] | ((uint32_t)lw[1][1] << 16);
+      }
+      // P V: value rows r0.. r0+7 (k 0..7) and r0+8.. (k 8..15), two 8-column tiles per load
+      {
+        const int row = r0 + ri + ((mi & 1) << 3);
+#pragma unroll
+        for (int d2 = 0; d2 < NDT / 2; ++d2) {
+          const int ch = 2 * d2 + (mi >> 1);
+          uint32_t b[4];
+          ldsm_x4_trans(vbase + (uint32_t)((ch >> 3) * rph * 128 + row * 128 + (((ch & 7) ^ (row & 7)) << 4)), b);
+          Mma<WT>::run(o[2 * d2], pa, b[0], b[1]);
+          Mma<WT>::run(o[2 * d2 + 1], pa, b[2], b[3]);
+        }
+      }
+    }
+  };
+
+  for (int blk = 0; blk < at.nblocks; ++blk) {
+    int lo;
+    (void)attn_box_pos(at, blk, &lo);
+    const uint64_t tw = mark ? globaltimer_ns() : 0ull;
+    const uint8_t* kp = page_wait(S, c, pages, ring);
+    Ring rv = ring;
+    if (++rv.slot == S.n_pages) { rv.slot = 0; rv.ph ^= 1u; }
+    const uint8_t* vp = page_wait(S, c, pages, rv);
+    if (mark) page_wait_ns += globaltimer_ns() - tw;
+    block(smem_addr(kp), smem_addr(vp), at.pb, at.pb / 128, lo, at.pb);
+    page_release(S, c, ring);  // K page
+    page_release(S, c, ring);  // V page
+  }
+  if (at.has_new) block(smem_addr(mini), smem_addr(mini + MINI), 16, 1, 0, at.n_new);
+  if (mark) {
+    c->tmark[1] = globaltimer_ns();
+    c->tmark[4] = page_wait_ns;
+  }
+  // this warp's partial: head gq's sum over its lane group, output columns 8d + 2cq (+1)
+  lrun += __shfl_xor_sync(0xffffffffu, lrun, 1);
+  lrun += __shfl_xor_sync(0xffffffffu, lrun, 2);
+  constexpr int RW = HD + kPartExtra;
+  if (gq < G) {
+    float* dst = scratch + (warp * G + gq) * RW;
+#pragma unroll
+    for (int d = 0; d < NDT; ++d)
+      *reinterpret_cast<float2*>(dst + 8 * d + 2 * cq) = make_float2(o[d][0] + o[d][2], o[d][1] + o[d][3]);
+    if (cq == 0) {
+      dst[HD] = mrun;
+      dst[HD + 1] = lrun;
+    }
+  }
+  consumer_sync();
+  attn_combine_warps<HD, G>(S, act, at, l, scratch);
+}
+
+// the tensor-core instance's attention unit (one call site): the tensor-core op for units of
+// at least half a page (attn_use_mma), else the CUDA-core op, per head size and group
+template <typename WT, int SYNC>
+__device__ __noinline__ void op_attn_any(const DevState& S_arg, const StepArgs& A_arg, const Instr& in_arg, SmemCtl* c,
+                                         uint8_t* pages, float* xbuf, float* scratch, Ring& ring, float* act) {
+  const DevState& S = smem_ctl()->S;
+  const StepArgs& A = smem_ctl()->args;
+  const Instr& in = smem_ctl()->cur[threadIdx.x >> 5];
+  const int G = S.Hq / S.Hkv;
+  if (S.attn_mma && attn_use_mma(S, A, in)) {
+    if (S.hd == 128 && G == 2)
+      op_attn_tc<WT, SYNC, 128, 2>(S, A, in, c, pages, xbuf, scratch, ring, act);
+    else if (S.hd == 128 && G == 4)
+      op_attn_tc<WT, SYNC, 128, 4>(S, A, in, c, pages, xbuf, scratch, ring, act);
+    else if (S.hd == 128 && G == 1)
+      op_attn_tc<WT, SYNC, 128, 1>(S, A, in, c, pages, xbuf, scratch, ring, act);
+    else if (S.hd == 64 && G == 2)
+      op_attn_tc<WT, SYNC, 64, 2>(S, A, in, c, pages, xbuf, scratch, ring, act);
+    else if (S.hd == 64 && G == 4)
+      op_attn_tc<WT, SYNC, 64, 4>(S, A, in, c, pages, xbuf, scratch, ring, act);
+    else
+      op_attn_tc<WT, SYNC, 64, 1>(S, A, in, c, pages, xbuf, scratch, ring, act);
+  } else if (S.hd == 64 && G == 2)
+    op_attn<WT, SYNC, 64, 2>(S, A, in, c, pages, xbuf, scratch, ring, act);
+  else if (S.hd == 128 && G == 2)
+    op_attn<WT, SYNC, 128, 2>(S, A, in, c, pages, xbuf, scratch, ring, act);
+  else if (S.hd == 128 && G == 4)
+    op_attn<WT, SYNC, 128, 4>(S, A, in, c, pages, xbuf, scratch, ring, act);
+  else if (S.hd == 64 && G == 4)
+    op_attn<WT, SYNC, 64, 4>(S, A, in, c, pages, xbuf, scratch, ring, act);
+  else if (S.hd == 128 && G == 1)
+    op_attn<WT, SYNC, 128, 1>(S, A, in, c, pages, xbuf, scratch, ring, act);
+  else
+    op_attn<WT, SYNC, 64, 1>(S, A, in, c, pages, xbuf, scratch, ring, act);
 }
 
 // log-sum-exp merge of the S split partials of one (sequence, kv head) (§8.2 ATTN_REDUCE).
@@ -2241,7 +2538,9 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
           op_gemv<WT, SYNC, 2>(S, A, in, c, pages, xbuf, scratch, ring, act);
         break;
       case OP_ATTN:
-        if (S.hd == 64 && G == 2)
+        if (TC) {
+          op_attn_any<WT, SYNC>(S, A, in, c, pages, xbuf, scratch, ring, act);
+        } else if (S.hd == 64 && G == 2)
           op_attn<WT, SYNC, 64, 2>(S, A, in, c, pages, xbuf, scratch, ring, act);
         else if (S.hd == 128 && G == 2)
           op_attn<WT, SYNC, 128, 2>(S, A, in, c, pages, xbuf, scratch, ring, act);
@@ -2393,7 +2692,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
   float* scratch = smem_scratch(S);
   // the tensor-core pages are 128-byte swizzled copies, whose destination must sit on a
   // 1024-byte boundary: refuse to run (an error, not a faulting copy) if it does not
-  if (TC && S.tc && (smem_addr(pages) & 1023u)) {
+  if (TC && (S.tc || S.attn_mma) && (smem_addr(pages) & 1023u)) {
     if (tid == 0 && blockIdx.x == 0) set_err(S, 5u /*MK_ERR_STATE*/, -11, (int)(smem_addr(pages) & 1023u));
     return;
   }

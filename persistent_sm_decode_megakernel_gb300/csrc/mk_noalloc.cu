@@ -125,7 +125,7 @@ mk_status prepare(const mk_model_desc& d, const mk_weights* w, const mk_kv* kv, 
   Geometry g;
   std::string e = make_geometry(m, n_sm, 0, 0, 0, smem_optin, &g);
   if (!e.empty()) return fail(MK_ERR_INVALID, e);
-  const void* fn = step_kernel_entry(m.dtype, MK_SYNC_COUNTER, false, g.tc != 0);
+  const void* fn = step_kernel_entry(m.dtype, MK_SYNC_COUNTER, false, g.tc_instance());
   NA_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin));
   int bpsm = 0;
   NA_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bpsm, fn, kThreads, g.smem_bytes));
@@ -157,6 +157,8 @@ mk_status prepare(const mk_model_desc& d, const mk_weights* w, const mk_kv* kv, 
     e = build_tc_maps(m, g, &plan, &maps);
     if (!e.empty()) return fail(MK_ERR_CUDA, "tensor maps: " + e);
   }
+  e = build_kv_maps(m, g, m.max_batch, &plan, &maps);
+  if (!e.empty()) return fail(MK_ERR_CUDA, "tensor maps: " + e);
 
   // host images of the read-only tables
   std::vector<Instr> flat;
@@ -201,7 +203,7 @@ mk_status prepare(const mk_model_desc& d, const mk_weights* w, const mk_kv* kv, 
   NA_CUDA(cudaMemcpyAsync(base + o_ptr, ptrs.data(), sizeof(void*) * ptrs.size(), cudaMemcpyHostToDevice, s));
   NA_CUDA(cudaMemcpyAsync(base + P->o_q, qoff.data(), sizeof(int32_t) * qoff.size(), cudaMemcpyHostToDevice, s));
   if (!maps.empty()) {
-    place_tc_maps(flat, reinterpret_cast<uintptr_t>(base + o_maps));
+    place_tc_maps(flat, reinterpret_cast<uintptr_t>(base + o_maps), use_tc(g, nb));
     NA_CUDA(cudaMemcpyAsync(base + o_maps, maps.data(), sizeof(TmapImage) * maps.size(), cudaMemcpyHostToDevice, s));
   }
   NA_CUDA(cudaMemcpyAsync(base + P->o_ins, flat.data(), sizeof(Instr) * flat.size(), cudaMemcpyHostToDevice, s));
@@ -232,6 +234,7 @@ mk_status prepare(const mk_model_desc& d, const mk_weights* w, const mk_kv* kv, 
   S.n_pages = g.n_pages;
   S.page_stride = g.page_stride;
   S.tc = g.tc;
+  S.attn_mma = g.attn_mma;
   S.xbuf_bytes = g.xbuf_bytes;
   S.scratch_bytes = g.scratch_bytes;
   S.smem_bytes = g.smem_bytes;
@@ -312,7 +315,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_desc* desc, const mk_
   A.logits = logits;
   A.tok_hist = nullptr;
   DevState S = P.S;
-  const void* fn = step_kernel_entry(d.dtype, MK_SYNC_COUNTER, false, S.tc != 0);
+  const void* fn = step_kernel_entry(d.dtype, MK_SYNC_COUNTER, false, S.tc != 0 || S.attn_mma != 0);
   NA_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin));
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(P.n_cta);

@@ -101,6 +101,11 @@ std::string make_geometry(const ModelShape& m, int n_cta, int page_bytes, int n_
   if (g->page_bytes < 64 * m.hd) return fmt("page_bytes must be at least 64 * head_dim = %lld", 64LL * m.hd);
   g->nb_max = pow2_at_least(m.max_batch);
   g->tc = m.max_batch >= 3 ? 1 : 0;  // batches of 3..16 run the tensor-core GEMV
+  // tensor-core attention (a K or V page is one box of page_bytes / (2 hd) positions) in the
+  // instance with the tensor-core code: contexts of batches of 3 and more, or of long
+  // capacity (there its units grow long enough to pay; short ones keep the instance without
+  // it, whose smaller code measured faster at batch 1)
+  g->attn_mma = g->page_bytes == 32768 && (g->tc || m.max_ctx >= kAttnMmaMinCtx) ? 1 : 0;
   g->page_stride = g->page_bytes;
   if (g->tc) {
     if (g->page_bytes != 32768) return "batches of 3 and more need 32 KB pages";
@@ -122,6 +127,9 @@ std::string make_geometry(const ModelShape& m, int n_cta, int page_bytes, int n_
   const int xfloats = g->tc ? std::max(std::max(2 * kmax, kMaxBatch * std::min(kTcKw, kmax)), (G + kMaxBatch) * m.hd)
                             : std::max(g->nb_max * kmax, (G + 1) * m.hd);
   g->xbuf_bytes = ((xfloats * 4 + 127) / 128) * 128;
+  // the tensor-core attention's q, its A fragments and two 16-row pages of new keys / values
+  const int attn_x = G * m.hd * 4 + (m.hd / 16) * 32 * 16 + 2 * (m.hd / 64) * 16 * 128;
+  if (g->attn_mma) g->xbuf_bytes = std::max(g->xbuf_bytes, ((attn_x + 127) / 128) * 128);
   if (kv_splits > 0) {
     g->S = kv_splits;
   } else {

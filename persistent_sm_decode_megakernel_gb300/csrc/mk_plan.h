@@ -29,6 +29,9 @@ struct Geometry {
   int S = 1;             // kv splits per (sequence, kv head)
   int tc = 0;            // max_batch >= 3: batches of 3..16 run the tensor-core GEMV
   int page_stride = 0;   // bytes between ring slots
+  int attn_mma = 0;      // split-KV units of at least half a page run on tensor cores
+  // the kernel instance with the tensor-core code (GEMV and attention)
+  bool tc_instance() const { return tc || attn_mma; }
 };
 // a GEMV of batch nb uses the tensor-core path
 inline bool use_tc(const Geometry& g, int nb) { return g.tc && nb >= 4; }
@@ -88,7 +91,15 @@ struct TmapImage {
   alignas(64) unsigned char bytes[128];
 };
 std::string build_tc_maps(const ModelShape& m, const Geometry& g, Plan* p, std::vector<TmapImage>* maps);
-void place_tc_maps(std::vector<Instr>& q, uintptr_t maps_dev);
+// The tensor-core attention's K and V pages: per layer one map of the key cache and, right
+// after it, one of the value cache, over [64-element half rows, positions, halves, cache
+// sequences x kv heads] (128-byte swizzled boxes of a page's positions); each ATTENTION
+// instruction (queued or pooled) gets the key map's index + 1 in p3.  cache_batch: the
+// caches' sequence extent.  Appends to maps.
+std::string build_kv_maps(const ModelShape& m, const Geometry& g, int cache_batch, Plan* p,
+                          std::vector<TmapImage>* maps);
+// gemv_maps: build_tc_maps ran (else the GEMV instructions keep their row pointers)
+void place_tc_maps(std::vector<Instr>& q, uintptr_t maps_dev, bool gemv_maps);
 std::string validate_plan(const ModelShape& m, const Geometry& g, const Plan& p);
 
 }  // namespace mk

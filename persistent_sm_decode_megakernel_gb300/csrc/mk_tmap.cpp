@@ -13,6 +13,7 @@
 #include <cstring>
 #include <map>
 #include <tuple>
+#include <utility>
 
 #include "mk_plan.h"
 
@@ -80,7 +81,7 @@ std::string build_tc_maps(const ModelShape& m, const Geometry& g, Plan* p, std::
       return 0;
     }
     TmapImage img;
-    static_assert(sizeof(CUtensorMap) == sizeof(TmapImage), "tensor map image size");
+    static_assert(sizeof(CUtensorMap) == sizeof(TmapImage) && sizeof(TmapImage) == kTmapBytes, "tensor map image size");
     std::memcpy(img.bytes, &tm, sizeof tm);
     maps->push_back(img);
     seen[key] = maps->size();
@@ -108,12 +109,72 @@ std::string build_tc_maps(const ModelShape& m, const Geometry& g, Plan* p, std::
   return err;
 }
 
-void place_tc_maps(std::vector<Instr>& q, uintptr_t maps_dev) {
+std::string build_kv_maps(const ModelShape& m, const Geometry& g, int cache_batch, Plan* p,
+                          std::vector<TmapImage>* maps) {
+  std::string err;
+  if (!g.attn_mma) return err;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder(&err);
+  if (!enc) return err;
+  const int esz = 2, halves = m.hd / 64, pb = g.page_bytes / (m.hd * esz);
+  const uint64_t per_seq_head = (uint64_t)m.max_ctx * m.hd * esz;  // bytes of one (sequence, kv head)
+  std::map<std::pair<uint64_t, uint64_t>, uint64_t> seen;         // (key base, value base) -> index + 1
+  auto encode = [&](uint64_t base, TmapImage* img) {
+    CUtensorMap tm;
+    // dim 0: 64 elements of a row (128 bytes), dim 1: positions, dim 2: the row's 64-element
+    // halves, dim 3: cache sequence x kv head; a box is one page: [half][position][128 B]
+    const cuuint64_t dims[4] = {64, (cuuint64_t)m.max_ctx, (cuuint64_t)halves, (cuuint64_t)cache_batch * m.Hkv};
+    const cuuint64_t strides[3] = {(cuuint64_t)m.hd * esz, 128, per_seq_head};
+    const cuuint32_t box[4] = {64, (cuuint32_t)pb, (cuuint32_t)halves, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = enc(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, reinterpret_cast<void*>(base), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      err = "cuTensorMapEncodeTiled (KV cache) failed with " + std::to_string((int)r);
+      return false;
+    }
+    std::memcpy(img->bytes, &tm, sizeof tm);
+    return true;
+  };
+  auto fix = [&](std::vector<Instr>& q) {
+    for (auto& in : q) {
+      if (in.op != OP_ATTN || !err.empty()) continue;
+      // the baked pointers address (b, j) at t = 0: back to the layer's cache base
+      const uint64_t off = ((uint64_t)in.a[0] * m.Hkv + in.a[1]) * per_seq_head;
+      const uint64_t kb = get_u64(in, kP4) - off, vb = get_u64(in, kP5) - off;
+      const auto key = std::make_pair(kb, vb);
+      auto it = seen.find(key);
+      uint64_t idx;
+      if (it != seen.end()) {
+        idx = it->second;
+      } else {
+        TmapImage ik, iv;
+        if (!encode(kb, &ik) || !encode(vb, &iv)) return;
+        maps->push_back(ik);
+        maps->push_back(iv);
+        idx = maps->size() - 1;  // the key map's index + 1
+        seen[key] = idx;
+      }
+      put_u64(in, kP3, idx);
+    }
+  };
+  for (auto& q : p->queues) fix(q);
+  for (auto& ph : p->phase_queues)
+    for (auto& q : ph) fix(q);
+  fix(p->pool);
+  return err;
+}
+
+void place_tc_maps(std::vector<Instr>& q, uintptr_t maps_dev, bool gemv_maps) {
+  static const int gemv_slots[2] = {kP4, kP5}, attn_slots[1] = {kP3};
   for (auto& in : q) {
-    if (!is_gemv(in.op)) continue;
-    for (int at : {kP4, kP5}) {
-      const uint64_t v = get_u64(in, at);
-      put_u64(in, at, v ? (uint64_t)maps_dev + (v - 1) * sizeof(TmapImage) : 0);
+    const bool gemv = is_gemv(in.op);
+    if (gemv ? !gemv_maps : in.op != OP_ATTN) continue;  // without GEMV maps p4 / p5 are row pointers
+    const int* slots = gemv ? gemv_slots : attn_slots;
+    const int n = gemv ? 2 : 1;
+    for (int k = 0; k < n; ++k) {
+      const uint64_t v = get_u64(in, slots[k]);
+      put_u64(in, slots[k], v ? (uint64_t)maps_dev + (v - 1) * sizeof(TmapImage) : 0);
     }
   }
 }

@@ -33,7 +33,8 @@ def summarize(trace):
     """Per-op means of the journal's phases.  GEMV: stage (dependency satisfied -> inputs
     staged), pages (-> last page consumed; page_wait = the part spent waiting for pages to
     land), epi (-> outputs written), tail (-> end, the closing barrier).  Attention: stage,
-    pages, write (partial written), then arrive (the arrival) or merge (last arriver)."""
+    pages (page_wait: the part spent waiting for K, V pages), write (partial written), then
+    arrive (the arrival) or merge (last arriver)."""
     t0 = min(r[4] for r in trace)
     t1 = max(r[6] for r in trace)
     span = (t1 - t0) / 1e3
@@ -58,6 +59,7 @@ def summarize(trace):
         elif op == 3 and m0 and m1:
             d["stage"].append((m0 - tr) / 1e3)
             d["pages"].append((m1 - m0) / 1e3)
+            d["page_wait"].append(m4 / 1e3)
             if m2:
                 d["write"].append((m2 - m1) / 1e3)
                 if m3:
@@ -139,6 +141,7 @@ def main():
     ap.add_argument("--split-min", type=int, default=0)
     ap.add_argument("--pool", type=int, default=0, help="attention units claimed from a per-layer pool")
     ap.add_argument("--kv-splits", type=int, default=0, help="KV splits per (sequence, kv head) in the schedule")
+    ap.add_argument("--cuda-cores", type=int, default=0, help="1: every attention unit on CUDA cores")
     ap.add_argument("--synthetic-kv", action="store_true",
                     help="fill the first --prompt cache positions with seeded synthetic keys/values instead of a prefill")
     ap.add_argument("--json", default="")
@@ -162,7 +165,8 @@ def main():
                       page_bytes=args.page_bytes, n_pages=args.n_pages, backoff_max_ns=args.backoff,
                       kv_splits=args.kv_splits,
                       split_min_positions=args.split_min, attn_merge=args.merge,
-                      inflight_pages=args.inflight, attn_pool=args.pool, stream=stream)
+                      inflight_pages=args.inflight, attn_pool=args.pool, attn_cuda_cores=args.cuda_cores,
+                      stream=stream)
         prompt = synth.gen_prompts(cfg, B, args.prompt)
         if args.synthetic_kv:
             for l in range(cfg.n_layers):
