@@ -17,7 +17,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = [f"mk_k_{d}_{s}{m}{t}.cu" for d in ("f16", "bf16") for s in ("counter", "sentinel") for m in ("", "_ms")
-           for t in ("", "_tc")] + ["mk_kernel.cu", "mk_host.cu", "mk_plan.cpp", "mk_tmap.cpp", "mk_noalloc.cu"]
+           for t in ("", "_am", "_tc")] + ["mk_kernel.cu", "mk_host.cu", "mk_plan.cpp", "mk_tmap.cpp", "mk_noalloc.cu"]
 
 
 def _nvcc():

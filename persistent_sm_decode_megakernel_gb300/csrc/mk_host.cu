@@ -493,11 +493,11 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
   e = make_geometry(m, n_cta_guess, o.page_bytes, o.n_pages, o.kv_splits, smem_optin, &ctx->geo);
   if (!e.empty()) return fail(MK_ERR_INVALID, e);
   // one wave (§8.3): opt in to the shared memory, ask how many CTAs fit, launch exactly that
-  ctx->kernel_tc = step_kernel_entry(m.dtype, o.sync_mode, false, true);
-  ctx->kernel_tc_ms = step_kernel_entry(m.dtype, o.sync_mode, true, true);
+  ctx->kernel_tc = step_kernel_entry(m.dtype, o.sync_mode, false, 2);
+  ctx->kernel_tc_ms = step_kernel_entry(m.dtype, o.sync_mode, true, 2);
   if (o.attn_cuda_cores) ctx->geo.attn_mma = 0;
-  ctx->kernel = ctx->geo.tc_instance() ? ctx->kernel_tc : step_kernel_entry(m.dtype, o.sync_mode, false, false);
-  ctx->kernel_ms = ctx->geo.tc_instance() ? ctx->kernel_tc_ms : step_kernel_entry(m.dtype, o.sync_mode, true, false);
+  ctx->kernel = step_kernel_entry(m.dtype, o.sync_mode, false, ctx->geo.instance());
+  ctx->kernel_ms = step_kernel_entry(m.dtype, o.sync_mode, true, ctx->geo.instance());
   for (const void* fn : {ctx->kernel, ctx->kernel_ms, ctx->kernel_tc, ctx->kernel_tc_ms})
     // the attribute is per function (shared by every context in the process): the device's
     // limit, so that no context's launch is refused after another context sets a lower one
@@ -859,7 +859,7 @@ mk_status mk_selftest(int kind, int64_t* result, int n) {
   int dev = 0, n_sm = 0;
   MK_CUDA(cudaGetDevice(&dev));
   MK_CUDA(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
-  const void* fn = step_kernel_entry(MK_F16, MK_SYNC_COUNTER, false, false);
+  const void* fn = step_kernel_entry(MK_F16, MK_SYNC_COUNTER, false, 0);
   const int page = 16384, n_pages = 4;
   const int smem = n_pages * page + 0 + 256 + kCtlSmem;
   MK_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448));

@@ -1,11 +1,11 @@
 // Step-kernel instantiation: bf16 weights/KV, counter synchronisation, one step per launch,
-// with the tensor-core GEMV (contexts of max_batch >= 3).
+// with the tensor-core GEMV and attention (contexts of max_batch >= 3).
 #include "mk_kernel.cuh"
 
 namespace mk {
-template __global__ void mk_step_kernel<__nv_bfloat16, 0, false, true>(const __grid_constant__ DevState,
-                                                                       const __grid_constant__ StepArgs);
+template __global__ void mk_step_kernel<__nv_bfloat16, 0, false, true, true>(const __grid_constant__ DevState,
+                                                                const __grid_constant__ StepArgs);
 const void* step_kernel_entry_bf16_counter_tc() {
-  return reinterpret_cast<const void*>(&mk_step_kernel<__nv_bfloat16, 0, false, true>);
+  return reinterpret_cast<const void*>(&mk_step_kernel<__nv_bfloat16, 0, false, true, true>);
 }
 }  // namespace mk

@@ -1,11 +1,11 @@
 // Step-kernel instantiation: f16 weights/KV, sentinel synchronisation, several steps per launch,
-// without the tensor-core GEMV (contexts of max_batch <= 2).
+// without the tensor-core code (short contexts of max_batch <= 2).
 #include "mk_kernel.cuh"
 
 namespace mk {
-template __global__ void mk_step_kernel<__half, 1, true, false>(const __grid_constant__ DevState,
+template __global__ void mk_step_kernel<__half, 1, true, false, false>(const __grid_constant__ DevState,
                                                                 const __grid_constant__ StepArgs);
 const void* step_kernel_entry_f16_sentinel_ms() {
-  return reinterpret_cast<const void*>(&mk_step_kernel<__half, 1, true, false>);
+  return reinterpret_cast<const void*>(&mk_step_kernel<__half, 1, true, false, false>);
 }
 }  // namespace mk

@@ -271,7 +271,9 @@ __global__ void __launch_bounds__(kThreads, 1) mk_stream_kernel(const uint8_t* s
 
 // ---------------------------------------------------------------- launch table
 #define MK_ENTRY(n) const void* step_kernel_entry_##n();
-#define MK_ENTRIES(d, s) MK_ENTRY(d##_##s) MK_ENTRY(d##_##s##_tc) MK_ENTRY(d##_##s##_ms) MK_ENTRY(d##_##s##_ms_tc)
+#define MK_ENTRIES(d, s)                                                                         \
+  MK_ENTRY(d##_##s) MK_ENTRY(d##_##s##_am) MK_ENTRY(d##_##s##_tc) MK_ENTRY(d##_##s##_ms) MK_ENTRY(d##_##s##_ms_am) \
+      MK_ENTRY(d##_##s##_ms_tc)
 MK_ENTRIES(f16, counter)
 MK_ENTRIES(f16, sentinel)
 MK_ENTRIES(bf16, counter)
@@ -279,19 +281,17 @@ MK_ENTRIES(bf16, sentinel)
 #undef MK_ENTRIES
 #undef MK_ENTRY
 
-const void* step_kernel_entry(int dtype, int sync_mode, bool multi_step, bool tc) {
+const void* step_kernel_entry(int dtype, int sync_mode, bool multi_step, int variant) {
   using Fn = const void* (*)();
-  // [dtype][sync][multi_step][tc]
-  static const Fn table[2][2][2][2] = {
-      {{{step_kernel_entry_f16_counter, step_kernel_entry_f16_counter_tc},
-        {step_kernel_entry_f16_counter_ms, step_kernel_entry_f16_counter_ms_tc}},
-       {{step_kernel_entry_f16_sentinel, step_kernel_entry_f16_sentinel_tc},
-        {step_kernel_entry_f16_sentinel_ms, step_kernel_entry_f16_sentinel_ms_tc}}},
-      {{{step_kernel_entry_bf16_counter, step_kernel_entry_bf16_counter_tc},
-        {step_kernel_entry_bf16_counter_ms, step_kernel_entry_bf16_counter_ms_tc}},
-       {{step_kernel_entry_bf16_sentinel, step_kernel_entry_bf16_sentinel_tc},
-        {step_kernel_entry_bf16_sentinel_ms, step_kernel_entry_bf16_sentinel_ms_tc}}}};
-  return table[dtype == 0 ? 0 : 1][sync_mode == 0 ? 0 : 1][multi_step ? 1 : 0][tc ? 1 : 0]();
+  // [dtype][sync][multi_step][variant]
+#define MK_ROW(d, s) {{step_kernel_entry_##d##_##s, step_kernel_entry_##d##_##s##_am, step_kernel_entry_##d##_##s##_tc}, \
+                      {step_kernel_entry_##d##_##s##_ms, step_kernel_entry_##d##_##s##_ms_am,                         \
+                       step_kernel_entry_##d##_##s##_ms_tc}}
+  static const Fn table[2][2][2][3] = {{MK_ROW(f16, counter), MK_ROW(f16, sentinel)},
+                                       {MK_ROW(bf16, counter), MK_ROW(bf16, sentinel)}};
+#undef MK_ROW
+  const int v = variant < 0 ? 0 : (variant > 2 ? 2 : variant);
+  return table[dtype == 0 ? 0 : 1][sync_mode == 0 ? 0 : 1][multi_step ? 1 : 0][v]();
 }
 
 const void* barrier_kernel_entry() { return reinterpret_cast<const void*>(&mk_barrier_kernel); }

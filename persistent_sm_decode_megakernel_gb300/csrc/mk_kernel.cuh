@@ -392,7 +392,7 @@ __device__ __noinline__ bool producer_acquire(const DevState& S_arg, SmemCtl* c,
   return true;
 }
 
-template <bool MS, bool TC>
+template <bool MS, bool TC, bool AM>
 __device__ __noinline__ void producer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* c, uint8_t* pages) {
   const DevState& S = smem_ctl()->S;
   StepArgs& A = MS ? smem_ctl()->largs : smem_ctl()->args;
@@ -427,7 +427,7 @@ __device__ __noinline__ void producer(const DevState& S_arg, const StepArgs& A_a
       kv_ready = true;
     }
     const Attn at = make_attn(S, A, un);
-    if (TC && attn_mma_unit(S, at)) {  // one tensor-map box per K / V page (key map, value map after it)
+    if (AM && attn_mma_unit(S, at)) {  // one tensor-map box per K / V page (key map, value map after it)
       const uint8_t* km = reinterpret_cast<const uint8_t*>(iptr(un, kP3));
       const int bh = A.seq[at.b] * S.Hkv + at.j;
       for (int blk = 0; blk < at.nblocks && ok; ++blk) {
@@ -2405,7 +2405,7 @@ __device__ __noinline__ bool pool_take(const DevState& S_arg, SmemCtl* c) {
   return true;
 }
 
-template <typename WT, int SYNC, bool MS, bool TC>
+template <typename WT, int SYNC, bool MS, bool TC, bool AM>
 __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* c, uint8_t* pages, float* xbuf,
                          float* scratch) {
   const DevState& S = smem_ctl()->S;
@@ -2538,7 +2538,7 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
           op_gemv<WT, SYNC, 2>(S, A, in, c, pages, xbuf, scratch, ring, act);
         break;
       case OP_ATTN:
-        if (TC) {
+        if (AM) {
           op_attn_any<WT, SYNC>(S, A, in, c, pages, xbuf, scratch, ring, act);
         } else if (S.hd == 64 && G == 2)
           op_attn<WT, SYNC, 64, 2>(S, A, in, c, pages, xbuf, scratch, ring, act);
@@ -2659,9 +2659,12 @@ __device__ void consumer(const DevState& S_arg, const StepArgs& A_arg, SmemCtl* 
 
 // ---------------------------------------------------------------- the kernel
 // WT weight/KV dtype, SYNC counter or sentinel dependencies, MS several steps per launch,
-// TC with the tensor-core GEMV (geometries for 3..16 rows); contexts of batches 1..2 run
-// the instance without that code, whose smaller footprint measured faster at batch 1.
-template <typename WT, int SYNC, bool MS, bool TC>
+// TC with the tensor-core GEMV (geometries for 3..16 rows), AM with the tensor-core
+// attention.  Three variants are built: both (batches of 3 and more), AM alone (batches of
+// 1..2 with a long KV capacity) and neither (short batch-1..2 contexts): each op's code
+// that a context never runs stays out of its instance, whose instruction footprint and
+// register allocation measured faster at batch 1.
+template <typename WT, int SYNC, bool MS, bool TC, bool AM>
 __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_constant__ DevState S,
                                                               const __grid_constant__ StepArgs A) {
   SmemCtl* c = smem_ctl();
@@ -2692,7 +2695,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
   float* scratch = smem_scratch(S);
   // the tensor-core pages are 128-byte swizzled copies, whose destination must sit on a
   // 1024-byte boundary: refuse to run (an error, not a faulting copy) if it does not
-  if (TC && (S.tc || S.attn_mma) && (smem_addr(pages) & 1023u)) {
+  if (((TC && S.tc) || (AM && S.attn_mma)) && (smem_addr(pages) & 1023u)) {
     if (tid == 0 && blockIdx.x == 0) set_err(S, 5u /*MK_ERR_STATE*/, -11, (int)(smem_addr(pages) & 1023u));
     return;
   }
@@ -2729,11 +2732,11 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
   __syncthreads();
   if (tid >= kConsumerThreads) {  // the loader streams weights without waiting for the previous grid
     const int w = tid >> 5;
-    if (w == kLoaderWarp && (tid & 31) == 0) producer<MS, TC>(S, AA, c, pages);
+    if (w == kLoaderWarp && (tid & 31) == 0) producer<MS, TC, AM>(S, AA, c, pages);
     return;
   }
   if (AA.flags & SF_PDL) asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous grid's outputs
-  consumer<WT, SYNC, MS, TC>(S, AA, c, pages, xbuf, scratch);
+  consumer<WT, SYNC, MS, TC, AM>(S, AA, c, pages, xbuf, scratch);
   if (c->abort && tid == 0 && !global_err(S)) set_err(S, 4u, -7, -1);
 }
 

@@ -3,10 +3,10 @@
 
 namespace mk {
 // persistent step kernel instantiation for (weight dtype, sync mode); multi_step: the
-// instance that runs several greedy steps per launch (one step: the other instance); tc:
-// the instance with the tensor-core GEMV, for geometries set up for it (max_batch >= 3) --
-// contexts of batches 1..2 run the instance without that code
-const void* step_kernel_entry(int dtype, int sync_mode, bool multi_step, bool tc);
+// instance that runs several greedy steps per launch (one step: the other instance);
+// variant (Geometry::instance()): 0 without tensor-core code, 1 with the tensor-core
+// attention, 2 with the tensor-core GEMV and attention (geometries for max_batch >= 3)
+const void* step_kernel_entry(int dtype, int sync_mode, bool multi_step, int variant);
 // grid-barrier latency microbenchmark kernel
 const void* barrier_kernel_entry();
 // SM round-trip probe kernel (SM -> die map)

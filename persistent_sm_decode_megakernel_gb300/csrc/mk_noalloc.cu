@@ -125,7 +125,7 @@ mk_status prepare(const mk_model_desc& d, const mk_weights* w, const mk_kv* kv, 
   Geometry g;
   std::string e = make_geometry(m, n_sm, 0, 0, 0, smem_optin, &g);
   if (!e.empty()) return fail(MK_ERR_INVALID, e);
-  const void* fn = step_kernel_entry(m.dtype, MK_SYNC_COUNTER, false, g.tc_instance());
+  const void* fn = step_kernel_entry(m.dtype, MK_SYNC_COUNTER, false, g.instance());
   NA_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin));
   int bpsm = 0;
   NA_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bpsm, fn, kThreads, g.smem_bytes));
@@ -315,7 +315,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_desc* desc, const mk_
   A.logits = logits;
   A.tok_hist = nullptr;
   DevState S = P.S;
-  const void* fn = step_kernel_entry(d.dtype, MK_SYNC_COUNTER, false, S.tc != 0 || S.attn_mma != 0);
+  const void* fn = step_kernel_entry(d.dtype, MK_SYNC_COUNTER, false, S.tc ? 2 : (S.attn_mma ? 1 : 0));
   NA_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin));
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(P.n_cta);

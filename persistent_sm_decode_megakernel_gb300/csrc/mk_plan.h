@@ -30,8 +30,9 @@ struct Geometry {
   int tc = 0;            // max_batch >= 3: batches of 3..16 run the tensor-core GEMV
   int page_stride = 0;   // bytes between ring slots
   int attn_mma = 0;      // split-KV units of at least half a page run on tensor cores
-  // the kernel instance with the tensor-core code (GEMV and attention)
-  bool tc_instance() const { return tc || attn_mma; }
+  // the kernel instance: 2 with the tensor-core GEMV and attention, 1 with the tensor-core
+  // attention alone, 0 with neither
+  int instance() const { return tc ? 2 : (attn_mma ? 1 : 0); }
 };
 // a GEMV of batch nb uses the tensor-core path
 inline bool use_tc(const Geometry& g, int nb) { return g.tc && nb >= 4; }
