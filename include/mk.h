@@ -121,11 +121,15 @@ typedef struct {
                              one at a time (an atomic claim counter) as its ring frees,
                              instead of a fixed share dealt to its queue; persistent
                              control only (0: fixed shares, the default)                 */
-  int attn_cuda_cores;    /* 1: every split-KV unit on CUDA cores.  0 (default): a unit of
-                             at least half a page of cached positions (64 at head_dim 128,
-                             128 at 64) runs q K^T and P V on the tensor cores (mma.sync,
-                             q and P as hi/lo 16-bit halves, fp32 accumulators), its K and
-                             V pages landed by tensor-map copies; needs 32 KB pages       */
+  int attn_tensor_cores;  /* tensor-core attention: a split-KV unit of at least half a page
+                             of cached positions (64 at head_dim 128, 128 at 64) runs q K^T
+                             and P V on mma.sync (q and P as hi/lo 16-bit halves, fp32
+                             accumulators), its K / V pages landed by tensor-map copies;
+                             needs 32 KB pages.  0 (default): in contexts of max_batch >= 3
+                             and in those of max_ctx >= 8192 (a batch-1..2 context then
+                             runs the kernel variant with this code, which measured ~3.7 %
+                             slower at short positions than the one without); 1: in every
+                             context; -1: never (CUDA cores only)                         */
 } mk_options;
 
 typedef struct {
@@ -140,6 +144,9 @@ typedef struct {
   int n_counters;
   int launches_per_step;  /* 1 for the persistent kernel, ~6 per layer + 2 for multi-launch */
   long long weight_bytes_per_step;  /* streamed weight bytes of one decode step            */
+  int kernel_variant;     /* the step kernel's variant: 0 without tensor-core code, 1 with
+                             the tensor-core attention, 2 with the tensor-core GEMV and
+                             attention (max_batch >= 3)                                  */
 } mk_info_t;
 
 /* One journal record per executed instruction (§8.7), times from %globaltimer (ns). */

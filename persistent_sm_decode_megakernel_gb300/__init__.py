@@ -51,14 +51,14 @@ class mk_options(ctypes.Structure):
                 ("backoff_max_ns", c_int), ("max_ctas", c_int), ("fault_drop_signal", c_int),
                 ("split_min_positions", c_int),
                 ("attn_merge", c_int), ("inflight_pages", c_int), ("attn_pool", c_int),
-                ("attn_cuda_cores", c_int)]
+                ("attn_tensor_cores", c_int)]
 
 
 class mk_info_t(ctypes.Structure):
     _fields_ = [("n_sm", c_int), ("blocks_per_sm", c_int), ("n_ctas", c_int), ("threads_per_cta", c_int),
                 ("smem_bytes", c_int), ("page_bytes", c_int), ("n_pages", c_int), ("kv_splits", c_int),
                 ("n_instructions", c_int), ("n_counters", c_int), ("launches_per_step", c_int),
-                ("weight_bytes_per_step", ctypes.c_longlong)]
+                ("weight_bytes_per_step", ctypes.c_longlong), ("kernel_variant", c_int)]
 
 
 class mk_trace_rec(ctypes.Structure):

@@ -434,9 +434,10 @@ mk_status mk_plan(const mk_model_desc* desc, const mk_options* opts, int n_ctas,
   mk_options o{};
   if (opts) o = *opts;
   if (o.attn_merge < 0 || o.attn_merge > 3) return fail(MK_ERR_INVALID, "attn_merge must be 0..3");
+  if (o.attn_tensor_cores < -1 || o.attn_tensor_cores > 1) return fail(MK_ERR_INVALID, "attn_tensor_cores must be -1, 0 or 1");
   const ModelShape m = shape_of(desc);
   Geometry g;
-  e = make_geometry(m, n_ctas, o.page_bytes, o.n_pages, o.kv_splits, 232448, &g);
+  e = make_geometry(m, n_ctas, o.page_bytes, o.n_pages, o.kv_splits, 232448, &g, o.attn_tensor_cores);
   if (!e.empty()) return fail(MK_ERR_INVALID, e);
   Plan p;
   e = build_plan(m, g, n_ctas, m.max_batch, o.fault_drop_signal,
@@ -449,6 +450,7 @@ mk_status mk_plan(const mk_model_desc* desc, const mk_options* opts, int n_ctas,
   info->n_ctas = n_ctas;
   info->threads_per_cta = kThreads;
   info->smem_bytes = g.smem_bytes;
+  info->kernel_variant = g.instance();
   info->page_bytes = g.page_bytes;
   info->n_pages = g.n_pages;
   info->kv_splits = g.S;
@@ -482,7 +484,7 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
     return fail(MK_ERR_INVALID, "exec_mode");
   if (o.attn_merge < 0 || o.attn_merge > 3) return fail(MK_ERR_INVALID, "attn_merge must be 0..3");
   if (o.attn_pool < 0 || o.attn_pool > 1) return fail(MK_ERR_INVALID, "attn_pool must be 0 or 1");
-  if (o.attn_cuda_cores < 0 || o.attn_cuda_cores > 1) return fail(MK_ERR_INVALID, "attn_cuda_cores must be 0 or 1");
+  if (o.attn_tensor_cores < -1 || o.attn_tensor_cores > 1) return fail(MK_ERR_INVALID, "attn_tensor_cores must be -1, 0 or 1");
   ctx->stream = reinterpret_cast<cudaStream_t>(stream);
   MK_CUDA(cudaGetDevice(&ctx->device));
   MK_CUDA(cudaDeviceGetAttribute(&ctx->n_sm, cudaDevAttrMultiProcessorCount, ctx->device));
@@ -490,12 +492,11 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
   MK_CUDA(cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, ctx->device));
   int n_cta_guess = ctx->n_sm;
   if (o.max_ctas > 0) n_cta_guess = std::min(n_cta_guess, o.max_ctas);
-  e = make_geometry(m, n_cta_guess, o.page_bytes, o.n_pages, o.kv_splits, smem_optin, &ctx->geo);
+  e = make_geometry(m, n_cta_guess, o.page_bytes, o.n_pages, o.kv_splits, smem_optin, &ctx->geo, o.attn_tensor_cores);
   if (!e.empty()) return fail(MK_ERR_INVALID, e);
   // one wave (§8.3): opt in to the shared memory, ask how many CTAs fit, launch exactly that
   ctx->kernel_tc = step_kernel_entry(m.dtype, o.sync_mode, false, 2);
   ctx->kernel_tc_ms = step_kernel_entry(m.dtype, o.sync_mode, true, 2);
-  if (o.attn_cuda_cores) ctx->geo.attn_mma = 0;
   ctx->kernel = step_kernel_entry(m.dtype, o.sync_mode, false, ctx->geo.instance());
   ctx->kernel_ms = step_kernel_entry(m.dtype, o.sync_mode, true, ctx->geo.instance());
   for (const void* fn : {ctx->kernel, ctx->kernel_ms, ctx->kernel_tc, ctx->kernel_tc_ms})
@@ -507,21 +508,20 @@ mk_status mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv*
   ctx->n_cta = ctx->n_sm * ctx->bpsm;
   if (o.max_ctas > 0) ctx->n_cta = std::min(ctx->n_cta, o.max_ctas);
   if (ctx->n_cta != n_cta_guess) {
-    e = make_geometry(m, ctx->n_cta, o.page_bytes, o.n_pages, o.kv_splits, smem_optin, &ctx->geo);
+    e = make_geometry(m, ctx->n_cta, o.page_bytes, o.n_pages, o.kv_splits, smem_optin, &ctx->geo, o.attn_tensor_cores);
     if (!e.empty()) return fail(MK_ERR_INVALID, e);
   }
-  if (o.attn_cuda_cores) ctx->geo.attn_mma = 0;
   const Geometry& g = ctx->geo;
   {  // prompt chunks: the tensor-core geometry of kMaxBatch rows, if it fits the same wave
     PrefillState& pf = ctx->pf;
     pf.m = m;
     pf.m.max_batch = kMaxBatch;
     if (o.exec_mode == MK_EXEC_PERSISTENT &&
-        make_geometry(pf.m, ctx->n_cta, o.page_bytes, o.n_pages, o.kv_splits, smem_optin, &pf.geo).empty()) {
+        make_geometry(pf.m, ctx->n_cta, o.page_bytes, o.n_pages, o.kv_splits, smem_optin, &pf.geo,
+                      o.attn_tensor_cores).empty()) {
       int bp = 0;
       MK_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bp, ctx->kernel_tc, kThreads, pf.geo.smem_bytes));
       if (bp < ctx->bpsm) pf.geo.smem_bytes = 0;  // chunks would not run in one wave: per-position prefill
-      if (o.attn_cuda_cores) pf.geo.attn_mma = 0;
     } else {
       pf.geo.smem_bytes = 0;
     }
@@ -632,6 +632,7 @@ mk_status mk_info(const mk_ctx* ctx, mk_info_t* info) {
   info->n_ctas = ctx->n_cta;
   info->threads_per_cta = kThreads;
   info->smem_bytes = ctx->geo.smem_bytes;
+  info->kernel_variant = ctx->geo.instance();
   info->page_bytes = ctx->geo.page_bytes;
   info->n_pages = ctx->geo.n_pages;
   info->kv_splits = ctx->geo.S;

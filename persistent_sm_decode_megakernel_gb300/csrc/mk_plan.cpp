@@ -90,7 +90,7 @@ ModelShape shape_of(const mk_model_desc* d) {
 }
 
 std::string make_geometry(const ModelShape& m, int n_cta, int page_bytes, int n_pages_req, int kv_splits,
-                          int smem_limit, Geometry* g) {
+                          int smem_limit, Geometry* g, int attn_tc) {
   *g = Geometry();
   const int G = m.Hq / m.Hkv;
   if (m.hd != 64 && m.hd != 128) return "head_dim must be 64 or 128";
@@ -105,7 +105,8 @@ std::string make_geometry(const ModelShape& m, int n_cta, int page_bytes, int n_
   // instance with the tensor-core code: contexts of batches of 3 and more, or of long
   // capacity (there its units grow long enough to pay; short ones keep the instance without
   // it, whose smaller code measured faster at batch 1)
-  g->attn_mma = g->page_bytes == 32768 && (g->tc || m.max_ctx >= kAttnMmaMinCtx) ? 1 : 0;
+  const bool want = attn_tc > 0 || (attn_tc == 0 && (g->tc || m.max_ctx >= kAttnMmaMinCtx));
+  g->attn_mma = g->page_bytes == 32768 && want ? 1 : 0;
   g->page_stride = g->page_bytes;
   if (g->tc) {
     if (g->page_bytes != 32768) return "batches of 3 and more need 32 KB pages";

@@ -70,8 +70,10 @@ ModelShape shape_of(const mk_model_desc* d);
 void arena_layout(const ModelShape& m, const Geometry& g, int rows, DevState* S);
 
 // returns "" on success, else a message
+// attn_tc: the tensor-core attention -- 0 where it pays (contexts of max_batch >= 3 or of
+// KV capacity >= kAttnMmaMinCtx), 1 in every context, -1 never (mk_options.attn_tensor_cores)
 std::string make_geometry(const ModelShape& m, int n_cta, int page_bytes, int n_pages_req, int kv_splits,
-                          int smem_limit, Geometry* g);
+                          int smem_limit, Geometry* g, int attn_tc = 0);
 // attn_pool: ATTENTION units claimed at run time from a per-layer pool instead of dealt to
 // the CTAs' queues (persistent control only: the multi-launch phases keep static units)
 std::string build_plan(const ModelShape& m, const Geometry& g, int n_cta, int B, int drop_signal, int merge,

@@ -79,13 +79,13 @@ class Decoder:
 
     def __init__(self, dm: DeviceModel, sync_mode=0, exec_mode=0, trace=0, timeout_s=2.0, page_bytes=0,
                  n_pages=0, kv_splits=0, max_ctas=0, fault_drop_signal=0, backoff_max_ns=0,
-                 split_min_positions=0, attn_merge=0, inflight_pages=0, attn_pool=0, attn_cuda_cores=0,
+                 split_min_positions=0, attn_merge=0, inflight_pages=0, attn_pool=0, attn_tensor_cores=0,
                  stream=None):
         self.dm = dm
         self.stream = stream if stream is not None else torch.cuda.current_stream(dm.device)
         self.opts = mk_options(sync_mode, exec_mode, page_bytes, n_pages, kv_splits, trace, timeout_s,
                                backoff_max_ns, max_ctas, fault_drop_signal, split_min_positions,
-                               attn_merge, inflight_pages, attn_pool, attn_cuda_cores)
+                               attn_merge, inflight_pages, attn_pool, attn_tensor_cores)
         d = dm.desc()
         w, kv, _keep = dm.abi_structs()
         h = ctypes.c_void_p()

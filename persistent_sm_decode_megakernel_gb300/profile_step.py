@@ -141,7 +141,9 @@ def main():
     ap.add_argument("--split-min", type=int, default=0)
     ap.add_argument("--pool", type=int, default=0, help="attention units claimed from a per-layer pool")
     ap.add_argument("--kv-splits", type=int, default=0, help="KV splits per (sequence, kv head) in the schedule")
-    ap.add_argument("--cuda-cores", type=int, default=0, help="1: every attention unit on CUDA cores")
+    ap.add_argument("--attn-tc", type=int, default=0,
+                    help="tensor-core attention: 0 where it pays, 1 in every context, -1 never")
+    ap.add_argument("--max-ctx", type=int, default=0, help="KV capacity (default: prompt + steps + 2)")
     ap.add_argument("--synthetic-kv", action="store_true",
                     help="fill the first --prompt cache positions with seeded synthetic keys/values instead of a prefill")
     ap.add_argument("--json", default="")
@@ -157,7 +159,7 @@ def main():
         cfg = synth.with_overrides(cfg, n_layers=args.layers)
     w = synth.gen_weights(cfg)
     B = args.batch
-    dm = DeviceModel(cfg, w, max_batch=B, max_ctx=args.prompt + args.steps + 2)
+    dm = DeviceModel(cfg, w, max_batch=B, max_ctx=max(args.max_ctx, args.prompt + args.steps + 2))
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         dec = Decoder(dm, sync_mode=0 if args.sync == "counter" else 1,
@@ -165,7 +167,7 @@ def main():
                       page_bytes=args.page_bytes, n_pages=args.n_pages, backoff_max_ns=args.backoff,
                       kv_splits=args.kv_splits,
                       split_min_positions=args.split_min, attn_merge=args.merge,
-                      inflight_pages=args.inflight, attn_pool=args.pool, attn_cuda_cores=args.cuda_cores,
+                      inflight_pages=args.inflight, attn_pool=args.pool, attn_tensor_cores=args.attn_tc,
                       stream=stream)
         prompt = synth.gen_prompts(cfg, B, args.prompt)
         if args.synthetic_kv:

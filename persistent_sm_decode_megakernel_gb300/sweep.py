@@ -147,14 +147,17 @@ def part_batch512():
 def part_ctx32k():
     import synth
     from persistent_sm_decode_megakernel_gb300.model import Decoder, DeviceModel
+    import torch
     cfg = synth.CONFIGS["2b-32k"]
     T = cfg.prompt_len
     w = synth.gen_weights(cfg)
-    dm = DeviceModel(cfg, w, max_batch=16, max_ctx=T + 16)
-    _fill_kv(dm, cfg, 16, T)
     peak = _peak()
     out = {}
     for B in (1, 2, 4, 8, 16):
+        # a context of max_batch B, as a user serving B sequences creates it (batches of 1..2
+        # run the kernel variant without the tensor-core GEMV)
+        dm = DeviceModel(cfg, w, max_batch=B, max_ctx=T + 16)
+        _fill_kv(dm, cfg, B, T)
         for name, sync, ex in (("persistent_counter", 0, 0), ("persistent_sentinel", 1, 0), ("multilaunch", 0, 1)):
             dec = Decoder(dm, sync_mode=sync, exec_mode=ex)
             us, _, _ = _time_steps(dec, [1] * B, [T] * B, n_warm=2, n=4)
@@ -162,6 +165,8 @@ def part_ctx32k():
             gbs = _algo_bytes(cfg, [T + 3] * B) / (us * 1e-6) / 1e9
             out[f"B{B}_{name}"] = {"us_per_step": us, "tok_s": B / (us * 1e-6), "roofline_frac": gbs / peak}
             print(json.dumps({f"B{B}_{name}": out[f"B{B}_{name}"]}), flush=True)
+        del dm
+        torch.cuda.empty_cache()
     return out
 
 

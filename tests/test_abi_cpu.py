@@ -161,3 +161,23 @@ def test_attention_pool_option_range(mk):
     cfg = synth.CONFIGS["tiny"]
     st, _ = _plan(mk, _desc(mk, cfg), 152, attn_pool=1, exec_mode=1)   # multi-launch: static units
     assert st == mk.MK_OK
+
+
+@pytest.mark.parametrize("max_batch,max_ctx,attn,page_bytes,variant", [
+    (1, 4096, 0, 0, 0), (1, 8192, 0, 0, 1), (2, 32800, 0, 0, 1), (3, 64, 0, 0, 2), (16, 64, 0, 0, 2),
+    (1, 64, 1, 0, 1), (1, 32800, -1, 0, 0), (8, 64, -1, 0, 2), (1, 32800, 0, 16384, 0)])
+def test_kernel_variant_choice(mk, max_batch, max_ctx, attn, page_bytes, variant):
+    """The step kernel variant a context runs: with the tensor-core GEMV and attention from
+    max_batch 3 on; with the tensor-core attention alone for batch-1..2 contexts of KV
+    capacity >= 8192 (or when asked for); without tensor-core code otherwise, or when the
+    attention is kept on CUDA cores, or with pages smaller than the 32 KB box."""
+    cfg = synth.CONFIGS["2b"]
+    st, info = _plan(mk, _desc(mk, cfg, max_batch, max_ctx), 152, attn_tensor_cores=attn, page_bytes=page_bytes)
+    assert st == mk.MK_OK, mk.mk_last_error()
+    assert info.kernel_variant == variant
+
+
+def test_attn_tensor_cores_option_range(mk):
+    for bad in (-2, 2):
+        st, _ = _plan(mk, _desc(mk, synth.CONFIGS["tiny"]), 152, attn_tensor_cores=bad)
+        assert st == mk.MK_ERR_INVALID

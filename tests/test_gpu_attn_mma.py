@@ -39,6 +39,8 @@ def _run(lib, cfg, w, prompt, toks, n_new, **opts):
     B = prompt.shape[0]
     dm = lib.DeviceModel(cfg, w, max_batch=B, max_ctx=prompt.shape[1] + n_new)
     dec = lib.Decoder(dm, **opts)
+    want = 2 if B >= 3 else (1 if opts.get("attn_tensor_cores", 0) == 1 else 0)
+    assert dec.info()["kernel_variant"] == want
     z, tg = gpu_teacher_forced(dec, prompt, toks, n_new, cfg.vocab)
     dec.close()
     return z, tg
@@ -57,9 +59,9 @@ def test_hd128_tensor_core_attention(lib, sync, G, P, kv_splits):
     n_new = 3
     prompt = synth.gen_prompts(cfg, 1, P)
     toks, zref = oracle_run(cfg, w, prompt, n_new, model=m)
-    z1, t1 = _run(lib, cfg, w, prompt, toks, n_new, sync_mode=sync, kv_splits=kv_splits)
+    z1, t1 = _run(lib, cfg, w, prompt, toks, n_new, sync_mode=sync, kv_splits=kv_splits, attn_tensor_cores=1)
     assert_parity(z1, t1, zref, toks, P)
-    z0, _ = _run(lib, cfg, w, prompt, toks, n_new, sync_mode=sync, kv_splits=kv_splits, attn_cuda_cores=1)
+    z0, _ = _run(lib, cfg, w, prompt, toks, n_new, sync_mode=sync, kv_splits=kv_splits, attn_tensor_cores=-1)
     # the two attentions differ only in rounding: q and P as hi/lo 16-bit halves on the
     # tensor cores against fp32 products on the CUDA cores
     scale = np.abs(zref).max()
@@ -78,7 +80,7 @@ def test_hd64_batched_tensor_core_attention(lib, sync, B):
     P, n_new = 600, 3
     prompt = synth.gen_prompts(cfg, B, P)
     toks, zref = oracle_run(cfg, w, prompt, n_new, model=m)
-    z, tg = _run(lib, cfg, w, prompt, toks, n_new, sync_mode=sync, kv_splits=1)
+    z, tg = _run(lib, cfg, w, prompt, toks, n_new, sync_mode=sync, kv_splits=1, attn_tensor_cores=1)
     assert_parity(z, tg, zref, toks, P)
 
 
@@ -94,15 +96,32 @@ def test_hd128_long_prompt_chunks(lib):
     toks, zref = oracle_run(cfg, w, prompt, n_new, model=m)
     z1, t1 = _run(lib, cfg, w, prompt, toks, n_new, sync_mode=0)
     assert_parity(z1, t1, zref, toks, P)
-    z0, _ = _run(lib, cfg, w, prompt, toks, n_new, sync_mode=0, attn_cuda_cores=1)
+    z0, _ = _run(lib, cfg, w, prompt, toks, n_new, sync_mode=0, attn_tensor_cores=-1)
     assert np.abs(z1 - z0).max() <= 1e-3 * np.abs(zref).max()
 
 
-def test_attn_cuda_cores_option_range(lib):
-    """attn_cuda_cores is 0 or 1; anything else is refused at creation."""
+def test_long_capacity_batch1_context_takes_the_attention_variant(lib):
+    """A batch-1 context of KV capacity >= 8192 runs the kernel variant with the
+    tensor-core attention by default, and its decode matches the oracle."""
+    cfg = HD128[2]
+    w = synth.gen_weights(cfg)
+    m = oracle.Model(cfg, w)
+    P, n_new = 200, 3
+    prompt = synth.gen_prompts(cfg, 1, P)
+    toks, zref = oracle_run(cfg, w, prompt, n_new, model=m)
+    dm = lib.DeviceModel(cfg, w, max_batch=1, max_ctx=8192)
+    dec = lib.Decoder(dm, sync_mode=1, kv_splits=2)
+    assert dec.info()["kernel_variant"] == 1
+    z, tg = gpu_teacher_forced(dec, prompt, toks, n_new, cfg.vocab)
+    dec.close()
+    assert_parity(z, tg, zref, toks, P)
+
+
+def test_attn_tensor_cores_option_range(lib):
+    """attn_tensor_cores is -1, 0 or 1; anything else is refused at creation."""
     cfg = synth.CONFIGS["tiny"]
     w = synth.gen_weights(cfg)
     dm = lib.DeviceModel(cfg, w, max_batch=1, max_ctx=64)
     from persistent_sm_decode_megakernel_gb300 import MkError
     with pytest.raises(MkError):
-        lib.Decoder(dm, attn_cuda_cores=2)
+        lib.Decoder(dm, attn_tensor_cores=2)
