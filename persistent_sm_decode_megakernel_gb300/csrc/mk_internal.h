@@ -236,7 +236,6 @@ constexpr int kSplitLongPositions = 2048;
 // the exp-sum, two pad floats (16-byte rows, so records move as float4)
 constexpr int kPartExtra = 4;
 constexpr int kTmapBytes = 128;  // one tensor map (CUtensorMap) in device memory
-constexpr int kAttnMmaMinCtx = 8192;  // KV capacity from which batch-1..2 contexts take the tensor-core attention
 
 // shared-memory layout sizes (bytes)
 constexpr int kCtlSmem = 4096;   // barriers, flags, small broadcast values

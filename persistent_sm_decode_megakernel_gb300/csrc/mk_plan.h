@@ -70,6 +70,9 @@ ModelShape shape_of(const mk_model_desc* d);
 void arena_layout(const ModelShape& m, const Geometry& g, int rows, DevState* S);
 
 // returns "" on success, else a message
+// KV capacity from which batch-1..2 contexts take the tensor-core attention (and the kernel
+// variant with it: at short positions that variant measured ~3.7 % slower than the one without)
+constexpr int kAttnMmaMinCtx = 8192;
 // attn_tc: the tensor-core attention -- 0 where it pays (contexts of max_batch >= 3 or of
 // KV capacity >= kAttnMmaMinCtx), 1 in every context, -1 never (mk_options.attn_tensor_cores)
 std::string make_geometry(const ModelShape& m, int n_cta, int page_bytes, int n_pages_req, int kv_splits,
