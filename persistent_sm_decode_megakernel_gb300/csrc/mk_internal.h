@@ -236,6 +236,7 @@ constexpr int kSplitLongPositions = 2048;
 // the exp-sum, two pad floats (16-byte rows, so records move as float4)
 constexpr int kPartExtra = 4;
 constexpr int kTmapBytes = 128;  // one tensor map (CUtensorMap) in device memory
+constexpr int kKvInflight = 4;    // page copies in flight at least, for the tensor-core attention's K / V boxes
 
 // shared-memory layout sizes (bytes)
 constexpr int kCtlSmem = 4096;   // barriers, flags, small broadcast values

@@ -380,10 +380,12 @@ __device__ __noinline__ bool producer_wait(const DevState& S_arg, SmemCtl* c, ui
   }
   return true;
 }
-__device__ __noinline__ bool producer_acquire(const DevState& S_arg, SmemCtl* c, int slot, uint32_t ph, long long issued) {
+// fmin: the in-flight limit raised to at least this for the pages being issued
+__device__ __noinline__ bool producer_acquire(const DevState& S_arg, SmemCtl* c, int slot, uint32_t ph, long long issued,
+                                              int fmin = 0) {
   const DevState& S = smem_ctl()->S;
   if (!producer_wait(S, c, &c->empty[slot], ph ^ 1)) return false;
-  const int F = S.inflight_pages;
+  const int F = S.inflight_pages > 0 ? max(S.inflight_pages, fmin) : 0;
   if (F > 0 && F < S.n_pages && issued >= F) {
     const int ps = slot - F < 0 ? slot - F + S.n_pages : slot - F;
     const uint32_t pp = slot - F < 0 ? ph ^ 1u : ph;
@@ -434,7 +436,8 @@ __device__ __noinline__ void producer(const DevState& S_arg, const StepArgs& A_a
         int lo;
         const int p0 = attn_box_pos(at, blk, &lo);
         for (int kv = 0; kv < 2; ++kv) {
-          if (!producer_acquire(S, c, slot, ph, issued++)) {
+          // a long unit's K / V boxes are the step's bulk stream here: more of them in flight
+          if (!producer_acquire(S, c, slot, ph, issued++, kKvInflight)) {
             ok = false;
             break;
           }
@@ -1998,29 +2001,22 @@ __device__ __noinline__ void op_attn_tc(const DevState& S_arg, const StepArgs& A
   const int l = in.layer;
   const float qscale = (1.0f / sqrtf((float)HD)) * 1.4426950408889634f;  // scores in log2 units
 
+  // the query's A fragments, one 16-byte vector per (k-step, lane), built straight from the
+  // QKV op's output (scaled): rows fg (hi) and fg + 8 (lo) of head fg, zeros for fg >= G;
+  // the page loop reads them back with one load per k-step
   const float* qsrc = act_ptr(S, act, ACT_Q, l) + ((size_t)at.b * S.Hq + (size_t)at.j * G) * HD;
-  float4* q4 = reinterpret_cast<float4*>(xbuf);
-  stage_vec<SYNC>(S, reinterpret_cast<const float4*>(qsrc), G * HD / 4, c, [&](int i, float4 v) {
-    v.x *= qscale;
-    v.y *= qscale;
-    v.z *= qscale;
-    v.w *= qscale;
-    q4[i] = v;
-  });
-  consumer_sync();
-  // the query's A fragments, one 16-byte vector per (k-step, lane): rows gq (hi) and gq + 8
-  // (lo) of head gq, zeros for gq >= G -- built once, read with one load per k-step
-  uint4* qf = reinterpret_cast<uint4*>(xbuf + G * HD);
+  uint4* qf = reinterpret_cast<uint4*>(xbuf);
   if (tid < NKS * 32) {
     const int ks = tid >> 5, fg = (tid & 31) >> 2, fc = tid & 3;
     uint32_t f[4] = {0u, 0u, 0u, 0u};
     if (fg < G) {
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {  // k = 16 ks + 2 fc (+1), then + 8
-        const float* qp = xbuf + fg * HD + 16 * ks + 2 * fc + 8 * h2;
+      for (int h2 = 0; h2 < 2; ++h2) {  // k = 16 ks + 2 fc (+1), then + 8: one float4 holds the pair
+        const int k = 16 * ks + 2 * fc + 8 * h2;
+        const float4 v = load_v4<SYNC>(reinterpret_cast<const float4*>(qsrc + fg * HD + (k & ~3)), S, c);
         uint16_t h0, l0, h1, l1;
-        Mma<WT>::split(qp[0], h0, l0);
-        Mma<WT>::split(qp[1], h1, l1);
+        Mma<WT>::split(((k & 2) ? v.z : v.x) * qscale, h0, l0);
+        Mma<WT>::split(((k & 2) ? v.w : v.y) * qscale, h1, l1);
         f[2 * h2] = (uint32_t)h0 | ((uint32_t)h1 << 16);
         f[2 * h2 + 1] = (uint32_t)l0 | ((uint32_t)l1 << 16);
       }
@@ -2061,9 +2057,11 @@ __device__ __noinline__ void op_attn_tc(const DevState& S_arg, const StepArgs& A
     for (int ps = 0; ps < npass; ++ps) {
       const int r0 = ps * 128 + warp * 16;
       if (r0 + 16 <= lo || r0 >= hi) continue;  // uniform over the warp
-      // q K^T: key rows r0.. r0+7 and r0+8.. r0+15 (two column tiles), 16 dims per k-step
+      // q K^T: key rows r0.. r0+7 and r0+8.. r0+15 (two column tiles), 16 dims per k-step;
+      // even and odd k-steps in separate accumulators (two chains of dependent MMAs per tile)
       float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       {
+        float sb[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         const int row = r0 + ri + ((mi >> 1) << 3);
 #pragma unroll
         for (int ks = 0; ks < NKS; ++ks) {
@@ -2071,8 +2069,15 @@ __device__ __noinline__ void op_attn_tc(const DevState& S_arg, const StepArgs& A
           uint32_t b[4];
           ldsm_x4(kbase + (uint32_t)((ch >> 3) * rph * 128 + row * 128 + (((ch & 7) ^ (row & 7)) << 4)), b);
           const uint4 qa = qfl[32 * ks];
-          Mma<WT>::run(sa[0], qa, b[0], b[1]);
-          Mma<WT>::run(sa[1], qa, b[2], b[3]);
+          float(&d0)[4] = (ks & 1) ? sb[0] : sa[0];
+          float(&d1)[4] = (ks & 1) ? sb[1] : sa[1];
+          Mma<WT>::run(d0, qa, b[0], b[1]);
+          Mma<WT>::run(d1, qa, b[2], b[3]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          sa[0][e] += sb[0][e];
+          sa[1][e] += sb[1][e];
         }
       }
       // online softmax over this lane group's head: 4 keys per lane, then the group's max

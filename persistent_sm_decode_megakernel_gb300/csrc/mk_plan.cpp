@@ -128,8 +128,8 @@ std::string make_geometry(const ModelShape& m, int n_cta, int page_bytes, int n_
   const int xfloats = g->tc ? std::max(std::max(2 * kmax, kMaxBatch * std::min(kTcKw, kmax)), (G + kMaxBatch) * m.hd)
                             : std::max(g->nb_max * kmax, (G + 1) * m.hd);
   g->xbuf_bytes = ((xfloats * 4 + 127) / 128) * 128;
-  // the tensor-core attention's q, its A fragments and two 16-row pages of new keys / values
-  const int attn_x = G * m.hd * 4 + (m.hd / 16) * 32 * 16 + 2 * (m.hd / 64) * 16 * 128;
+  // the tensor-core attention's query fragments and two 16-row pages of new keys / values
+  const int attn_x = (m.hd / 16) * 32 * 16 + 2 * (m.hd / 64) * 16 * 128;
   if (g->attn_mma) g->xbuf_bytes = std::max(g->xbuf_bytes, ((attn_x + 127) / 128) * 128);
   if (kv_splits > 0) {
     g->S = kv_splits;
