@@ -117,6 +117,38 @@ def test_long_capacity_batch1_context_takes_the_attention_variant(lib):
     assert_parity(z, tg, zref, toks, P)
 
 
+@pytest.mark.parametrize("B", [1, 4])
+def test_multi_step_launch_with_tensor_core_attention(lib, B):
+    """Several greedy steps in ONE launch (the multi-step instances of the attention-only
+    and the tensor-core variant: the loader waits for the previous step's tokens before a
+    unit's K / V boxes, which then include the rows that step appended) give the same tokens
+    and last-step activations, bit for bit, as one launch per step."""
+    import torch
+    cfg = HD128[2]
+    w = synth.gen_weights(cfg)
+    P, n = 130, 6
+    prompt = synth.gen_prompts(cfg, B, P)
+    runs = []
+    for one_launch in (True, False):
+        dm = lib.DeviceModel(cfg, w, max_batch=B, max_ctx=P + n + 1)
+        dec = lib.Decoder(dm, sync_mode=1, kv_splits=1, attn_tensor_cores=1)
+        assert dec.info()["kernel_variant"] == (1 if B == 1 else 2)
+        first = dec.prefill(prompt)
+        out = torch.zeros((n, B), dtype=torch.int32, device=dm.device)
+        if one_launch:
+            dec.decode_steps(first, [P] * B, n, out)
+        else:
+            for k in range(n):
+                dec.decode_steps(first if k == 0 else None, [P + k] * B, 1, out[k:k + 1])
+        dec.synchronize()
+        h = dec.read_activation(0, cfg.n_layers)
+        runs.append((first, out.cpu().numpy().copy(), h))
+        dec.close()
+    assert list(runs[0][0]) == list(runs[1][0])
+    np.testing.assert_array_equal(runs[0][1], runs[1][1])
+    np.testing.assert_array_equal(runs[0][2], runs[1][2])
+
+
 def test_attn_tensor_cores_option_range(lib):
     """attn_tensor_cores is -1, 0 or 1; anything else is refused at creation."""
     cfg = synth.CONFIGS["tiny"]

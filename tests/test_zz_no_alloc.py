@@ -98,6 +98,42 @@ def test_noalloc_batches_in_a_row_match_context():
     dec.close()
 
 
+def test_noalloc_long_context_tensor_core_attention_matches_context():
+    """max_batch 4 at ~3000 cached positions (synthetic keys and values, the same in both
+    caches): every split-KV unit holds more than half a page of positions, so both entry
+    points run the tensor-core attention with its K / V tensor maps -- the allocation-free
+    one keeps them in its array -- and the logits, tokens and written rows agree bit for bit,
+    at ragged positions."""
+    import persistent_sm_decode_megakernel_gb300 as mk
+    from persistent_sm_decode_megakernel_gb300.model import Decoder, DeviceModel
+
+    cfg = synth.CONFIGS["tiny"]
+    w = synth.gen_weights(cfg)
+    T, B = 3000, 4
+    dms = [DeviceModel(cfg, w, max_batch=B, max_ctx=T + 8) for _ in range(2)]
+    for dm in dms:
+        g = torch.Generator(device=dm.device)
+        g.manual_seed(5)
+        for l in range(cfg.n_layers):
+            for cache in (dm.k_cache[l], dm.v_cache[l]):
+                x = torch.randn((B, cfg.n_kv_heads, T, cfg.head_dim), generator=g, device=dm.device)
+                cache[:, :, :T] = (x * 0.9).to(torch.bfloat16).view(torch.int16)
+    ref_dm, na_dm = dms
+    dec = Decoder(ref_dm)
+    assert dec.info()["kernel_variant"] == 2
+    stream = torch.cuda.current_stream()
+    toks = synth.gen_prompts(cfg, 1, B)[0]
+    pos = [T, T - 700, T - 1300, T - 1]
+    z_ref = torch.zeros((B, cfg.vocab), dtype=torch.float32, device="cuda:0")
+    z_na = torch.zeros((B, cfg.vocab), dtype=torch.float32, device="cuda:0")
+    out_ref = dec.decode_step([int(t) for t in toks], pos, logits=z_ref)
+    out = _noalloc(mk, na_dm, toks, pos, z_na, stream)
+    np.testing.assert_array_equal(z_na.cpu().numpy(), z_ref.cpu().numpy())
+    np.testing.assert_array_equal(out, np.asarray(out_ref))
+    _same_rows(na_dm, ref_dm, cfg, pos)
+    dec.close()
+
+
 def test_noalloc_refuses_models_beyond_its_scratch():
     """A descriptor whose schedule alone outgrows the array (the tiny model's tensors
     repeated over 400 layers: ~19 MB of instructions) is refused before anything runs."""
