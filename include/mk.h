@@ -61,7 +61,9 @@ typedef struct {
                              run the tensor-core GEMV (mma.sync, weights landed by tensor-map
                              copies), which needs d_model, ffn_dim and n_heads*head_dim to be
                              multiples of 64                                              */
-  int max_ctx;            /* KV-cache capacity in positions, at most 4194304 (2^22)      */
+  int max_ctx;            /* KV-cache capacity in positions, at most 4194304 (2^22); from
+                             8192 on, batch-1..2 contexts run the tensor-core attention
+                             (mk_options.attn_tensor_cores)                               */
 } mk_model_desc;
 
 /* Weights: device pointers, row-major, nn.Linear convention [out, in], 16-byte aligned.
